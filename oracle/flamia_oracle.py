@@ -1,0 +1,522 @@
+"""FP64 CPU oracle for token-block microscaled causal flash attention.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path may import this
+module: only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` use it.  It shares no code with the CUDA path; the two meet only
+in the seeded input generators (``workloads.py``), which hold no arithmetic of
+the method.
+
+What it follows (citations name the page and its section):
+
+* "FLAMIA ... (jaehun.me review)", sec. 3.1 "Reduce quantization duplication
+  with token-block scales": Q, K, V, dO are E4M3 codes with one power-of-two
+  exponent per 32 consecutive tokens x the full head dimension; dS has one
+  scale per 32x32 block; probability operands are E4M3; outputs and gradients
+  are BF16.  Mixed path: Q, K for the score product are NVFP4 (one scale per
+  16 head-dim elements of a token).
+* same page, sec. 3.1: the score is the plain E4M3 dot product times a row
+  factor (query block exponent, folded with the softmax scale) and a column
+  factor (key block exponent).  The printed formula is missing from the page;
+  the reading used here is S_ij = scale * 2^eQ(i) * 2^eK(j) * sum_k q_ik k_jk.
+* same page, sec. 3.2: exponents are rounded up so that the scaled maximum
+  never exceeds 448 (E4M3 max) -- nothing clips.
+* same page, sec. 1.2 and 3.3: forward S, P, O, row statistics; backward
+  recomputes P, dV = P^T dO, dP = dO V^T, dS = P o (dP - D), dQ = dS K,
+  dK = dS^T Q, with D_i = dO_i . O_i from the same quantised dO.
+* same page, sec. 3.4 "Packed documents": scale groups never cross a document
+  boundary; rows outside a document get an infinite log-sum-exp.
+* same page, sec. 3.4 "Work scheduling": a work item is 256 consecutive
+  queries of one document, its cost the number of key blocks it visits,
+  sorted by descending cost.
+* same page, sec. 2 "A small example": the floor exponent rule
+  e = floor(log2 amax) - emax with clipping at 448, used here only as the
+  negative control of the leakage probe.
+
+Readings where the pages are silent (each listed in the design doc):
+* code rounding is round-to-nearest-even; -0 keeps its sign bit;
+* amax == 0 gives exponent -127 (byte 0) and all-zero codes; exponents are
+  clamped to [-127, 127];
+* the running row maximum is an integer ceil of the log2-domain score, and the
+  probability operand is RNE_E4M3(2^8 * exp2(s - m)); l sums the unquantised
+  exp2(s - m); O = 2^-8 * sum_j P^_ij V^_j / l; LSE = (m + log2 l) * ln 2;
+* the backward probability is exp2(s - lse2) (normalised); the dV operand is
+  RNE_E4M3(2^8 P); dS uses the unquantised P;
+* the dS block exponent uses the same round-up rule on the 32x32 block
+  maximum (masked entries are 0); the softmax scale is applied after the
+  dQ / dK products;
+* the NVFP4 scale is the smallest E4M3 value >= amax / 6, no tensor-wide
+  scale;
+* work items: forward q0 = s + 256k, q1 = min(q0 + 256, e), cost =
+  ceil((q1 - s) / 128); backward k0 = s + 128k, k1 = min(k0 + 128, e),
+  cost = ceil((e - k0) / 128); stable sort by descending cost.
+
+Parity pins for every function live in tests/test_oracle_*.py.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+LOG2E = 1.0 / math.log(2.0)
+LN2 = math.log(2.0)
+E4M3_MAX = 448.0
+E2M1_MAX = 6.0
+P_SCALE_LOG2 = 8  # 2^8: largest power of two <= 448, multiplies P before E4M3
+
+
+# ----------------------------------------------------------------------------
+# Number formats
+# ----------------------------------------------------------------------------
+
+def _e4m3_value(code: int) -> float:
+    """OCP FP8 E4M3FN: sign, 4-bit exponent (bias 7), 3-bit mantissa; 0x7F/0xFF NaN."""
+    s = -1.0 if code & 0x80 else 1.0
+    e = (code >> 3) & 0xF
+    m = code & 0x7
+    if e == 0xF and m == 0x7:
+        return float("nan")
+    if e == 0:
+        return s * (m / 8.0) * 2.0 ** -6
+    return s * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+E4M3_TABLE = np.array([_e4m3_value(c) for c in range(256)], dtype=np.float64)
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    return E4M3_TABLE[np.asarray(codes, dtype=np.uint8)]
+
+
+def e4m3_encode(y, saturate: bool = False) -> np.ndarray:
+    """Round-to-nearest-even of float64 values to E4M3 codes (uint8).
+
+    Values above 448 in magnitude are an error unless ``saturate`` (then they
+    clip to +-448, the behaviour of the floor-rule negative control).
+    """
+    y = np.asarray(y, dtype=np.float64)
+    sign = np.signbit(y)
+    a = np.abs(y)
+    if np.any(~np.isfinite(a)):
+        raise ValueError("non-finite value to E4M3")
+    if saturate:
+        a = np.minimum(a, E4M3_MAX)
+    elif np.any(a > E4M3_MAX):
+        raise ValueError("value above 448 would clip")
+    code = np.zeros(a.shape, dtype=np.int64)
+    sub = a < 2.0 ** -6
+    # subnormal range: multiples of 2^-9
+    q = np.rint(a[sub] * 2.0 ** 9)          # 0..8, rint = ties to even
+    code[sub] = q.astype(np.int64)          # q == 8 is the smallest normal (exp 1, man 0)
+    nrm = ~sub
+    an = a[nrm]
+    _, ex = np.frexp(an)                    # an = f * 2^ex, f in [0.5, 1)
+    E = ex - 1                              # an in [2^E, 2^(E+1))
+    t = np.rint((an / np.ldexp(1.0, E) - 1.0) * 8.0)   # mantissa in eighths, ties to even
+    carry = t >= 8
+    E = np.where(carry, E + 1, E)
+    t = np.where(carry, 0, t)
+    code[nrm] = ((E + 7) << 3) | t.astype(np.int64)
+    if saturate:
+        code = np.minimum(code, 0x7E)
+    return (code | (sign.astype(np.int64) << 7)).astype(np.uint8)
+
+
+E2M1_VALUES = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=np.float64)
+E2M1_TABLE = np.concatenate([E2M1_VALUES, -E2M1_VALUES])
+
+
+def e2m1_decode(codes) -> np.ndarray:
+    return E2M1_TABLE[np.asarray(codes, dtype=np.uint8) & 0xF]
+
+
+def e2m1_encode(y) -> np.ndarray:
+    """Round-to-nearest-even to E2M1 (sign, 2-bit exponent bias 1, 1-bit mantissa).
+
+    Saturates at +-6 (the NVFP4 scale keeps |y| <= 6, so it never triggers
+    except when the scale itself saturated at 448)."""
+    y = np.asarray(y, dtype=np.float64)
+    sign = np.signbit(y)
+    a = np.minimum(np.abs(y), E2M1_MAX)
+    code = np.zeros(a.shape, dtype=np.int64)
+    sub = a < 1.0
+    code[sub] = np.rint(a[sub] * 2.0).astype(np.int64)      # 0, 0.5, (1.0 -> code 2)
+    nrm = ~sub
+    an = a[nrm]
+    _, ex = np.frexp(an)
+    E = ex - 1                                              # 0, 1, 2
+    t = np.rint((an / np.ldexp(1.0, E) - 1.0) * 2.0)        # halves, ties to even
+    carry = t >= 2
+    E = np.where(carry, E + 1, E)
+    t = np.where(carry, 0, t)
+    code[nrm] = ((E + 1) << 1) | t.astype(np.int64)
+    return (code | (sign.astype(np.int64) << 3)).astype(np.uint8)
+
+
+def e8m0_decode(byte) -> np.ndarray:
+    b = np.asarray(byte, dtype=np.int64)
+    return np.ldexp(1.0, b - 127)
+
+
+def bf16_round(x) -> np.ndarray:
+    """float64 -> nearest BF16 value (8 significant bits, ties to even), as float64."""
+    x = np.asarray(x, dtype=np.float64)
+    f, e = np.frexp(x)
+    return np.ldexp(np.rint(f * 256.0) / 256.0, e)
+
+
+# ----------------------------------------------------------------------------
+# Exponent rules
+# ----------------------------------------------------------------------------
+
+def roundup_exponent(amax) -> np.ndarray:
+    """Smallest integer e with amax <= 448 * 2^e, clamped to [-127, 127];
+    amax == 0 gives -127."""
+    amax = np.asarray(amax, dtype=np.float64)
+    e = np.full(amax.shape, -127, dtype=np.int64)
+    pos = amax > 0
+    _, ex = np.frexp(amax[pos])         # amax < 2^ex
+    cand = ex - 10                      # 448 * 2^(ex-10) < 2^(ex-1) <= amax: too small
+    for _ in range(4):                  # step up until the bound holds (at most 3 steps)
+        bad = amax[pos] > E4M3_MAX * np.ldexp(1.0, cand)
+        cand = np.where(bad, cand + 1, cand)
+    e[pos] = cand
+    return np.clip(e, -127, 127)
+
+
+def floor_exponent(amax) -> np.ndarray:
+    """OCP microscaling rule e = floor(log2 amax) - 8 (8 = E4M3 emax); negative control."""
+    amax = np.asarray(amax, dtype=np.float64)
+    e = np.full(amax.shape, -127, dtype=np.int64)
+    pos = amax > 0
+    _, ex = np.frexp(amax[pos])
+    e[pos] = (ex - 1) - 8
+    return np.clip(e, -127, 127)
+
+
+# ----------------------------------------------------------------------------
+# Token-block quantiser
+# ----------------------------------------------------------------------------
+
+def doc_blocks(cu_seqlens, size: int = 32):
+    """Document-local blocks [s + size*b, min(s + size*(b+1), e)) in token order."""
+    out = []
+    cu = list(cu_seqlens)
+    for i in range(len(cu) - 1):
+        s, e = int(cu[i]), int(cu[i + 1])
+        for b0 in range(s, e, size):
+            out.append((b0, min(b0 + size, e)))
+    return out
+
+
+def quantize_tokenblock(x, cu_seqlens, rule: str = "up", group: str = "block"):
+    """E4M3 codes [T, H, d] and E8M0 scale bytes [H, T] (one byte per token).
+
+    group="block": one exponent per (document-local 32-token block, head).
+    group="tensor": one exponent per head over all tokens (negative control).
+    rule="up": round-up exponent (never clips); rule="floor": floor rule with
+    clipping at 448 (negative control).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    T, H, d = x.shape
+    codes = np.zeros((T, H, d), dtype=np.uint8)
+    sbytes = np.zeros((H, T), dtype=np.uint8)
+    if group == "block":
+        blocks = doc_blocks(cu_seqlens, 32)
+    elif group == "tensor":
+        blocks = [(0, T)] if T > 0 else []
+    else:
+        raise ValueError(group)
+    expfn = roundup_exponent if rule == "up" else floor_exponent
+    for (b0, b1) in blocks:
+        xb = x[b0:b1]                                   # [n, H, d]
+        amax = np.abs(xb).max(axis=(0, 2))              # per head
+        e = expfn(amax)                                 # [H]
+        scaled = xb * np.ldexp(1.0, -e)[None, :, None]
+        codes[b0:b1] = e4m3_encode(scaled, saturate=(rule != "up"))
+        sbytes[:, b0:b1] = (e + 127).astype(np.uint8)[:, None]
+    return codes, sbytes
+
+
+def dequantize_tokenblock(codes, sbytes) -> np.ndarray:
+    """code value * 2^(byte - 127); the scale depends only on the token."""
+    return e4m3_decode(codes) * e8m0_decode(sbytes).T[:, :, None]
+
+
+def compute_D(do_codes, do_sbytes, o_bf16) -> np.ndarray:
+    """D[h, t] = sum_k dequant(dO)[t, h, k] * O[t, h, k] (O = the forward's BF16 output)."""
+    return np.einsum("thk,thk->ht", dequantize_tokenblock(do_codes, do_sbytes),
+                     np.asarray(o_bf16, dtype=np.float64))
+
+
+# ----------------------------------------------------------------------------
+# NVFP4 quantiser (mixed path: Q, K for the score product)
+# ----------------------------------------------------------------------------
+
+def nvfp4_scale_code(amax) -> np.ndarray:
+    """E4M3 code of the smallest E4M3 value >= amax / 6 (exact quotient);
+    amax == 0 gives 0; quotients above 448 saturate to 448."""
+    amax = np.asarray(amax, dtype=np.float64)
+    pos_vals = E4M3_TABLE[:0x7F]                       # codes 0x00..0x7E, increasing
+    q = amax / 6.0
+    idx = np.searchsorted(pos_vals, q, side="left")   # first value >= q
+    return np.minimum(idx, 0x7E).astype(np.uint8)
+
+
+def quantize_nvfp4(x):
+    """Packed E2M1 codes [T, H, d/2] (element 2i in the low nibble) and E4M3
+    scale codes [T, H, d/16]."""
+    x = np.asarray(x, dtype=np.float64)
+    T, H, d = x.shape
+    g = x.reshape(T, H, d // 16, 16)
+    sc = nvfp4_scale_code(np.abs(g).max(axis=3))
+    s = e4m3_decode(sc)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        y = np.where(s > 0, g / s, 0.0)
+    c = e2m1_encode(y).reshape(T, H, d)
+    packed = (c[..., 0::2] | (c[..., 1::2] << 4)).astype(np.uint8)
+    return packed, sc
+
+
+def dequantize_nvfp4(packed, sc) -> np.ndarray:
+    T, H, d2 = packed.shape
+    c = np.empty((T, H, 2 * d2), dtype=np.uint8)
+    c[..., 0::2] = packed & 0xF
+    c[..., 1::2] = packed >> 4
+    v = e2m1_decode(c).reshape(T, H, 2 * d2 // 16, 16)
+    return (v * e4m3_decode(sc)[..., None]).reshape(T, H, 2 * d2)
+
+
+# ----------------------------------------------------------------------------
+# Work list
+# ----------------------------------------------------------------------------
+
+def build_worklist(cu_seqlens):
+    """Forward and backward items, int64 arrays [n, 4] = (doc, start, end, cost),
+    each sorted by descending cost, stable over generation order."""
+    cu = [int(c) for c in cu_seqlens]
+    fwd, bwd = [], []
+    for b in range(len(cu) - 1):
+        s, e = cu[b], cu[b + 1]
+        for q0 in range(s, e, 256):
+            q1 = min(q0 + 256, e)
+            fwd.append((b, q0, q1, -(-(q1 - s) // 128)))
+        for k0 in range(s, e, 128):
+            k1 = min(k0 + 128, e)
+            bwd.append((b, k0, k1, -(-(e - k0) // 128)))
+    fwd.sort(key=lambda it: -it[3])   # Python's sort is stable
+    bwd.sort(key=lambda it: -it[3])
+    return (np.array(fwd, dtype=np.int64).reshape(-1, 4),
+            np.array(bwd, dtype=np.int64).reshape(-1, 4))
+
+
+# ----------------------------------------------------------------------------
+# Attention, one (document, head) at a time
+# ----------------------------------------------------------------------------
+
+class DocHead:
+    """Operands of one document and one head, as exact values split into a
+    code part and a per-token power-of-two exponent (for the unquantised mode
+    the code part is the raw value and the exponent is 0)."""
+
+    def __init__(self, q, eq, k, ek, v, ev, do=None, edo=None, qs=None, ks=None):
+        self.q, self.eq = q, eq          # [L, d], [L] int
+        self.k, self.ek = k, ek
+        self.v, self.ev = v, ev
+        self.do, self.edo = do, edo
+        # score operands when they differ from q/k (NVFP4 mixed path): exact values
+        self.qs, self.ks = qs, ks
+        self.L = q.shape[0]
+
+
+def _scores(dh: DocHead, rows: np.ndarray, cols: np.ndarray, sm_scale: float) -> np.ndarray:
+    """log2-domain scores s_ij = S_ij * log2(e), -inf where j > i."""
+    if dh.qs is not None:
+        S = sm_scale * (dh.qs[rows] @ dh.ks[cols].T)
+    else:
+        dots = dh.q[rows] @ dh.k[cols].T                       # code dot products
+        S = sm_scale * dots * np.ldexp(1.0, dh.eq[rows])[:, None] \
+            * np.ldexp(1.0, dh.ek[cols])[None, :]              # row factor x column factor
+    s = S * LOG2E
+    s[cols[None, :] > rows[:, None]] = -np.inf
+    return s
+
+
+def fwd_rows(dh: DocHead, rows: np.ndarray, sm_scale: float, quant: bool = True):
+    """Forward output rows: O [R, d], lse2 [R] (log2 units), m [R], l [R]."""
+    rows = np.asarray(rows, dtype=np.int64)
+    cols = np.arange(int(rows.max()) + 1 if rows.size else 0)
+    s = _scores(dh, rows, cols, sm_scale)
+    m = np.ceil(s.max(axis=1))                                 # integer row maximum
+    pt = np.exp2(s - m[:, None])                               # 0 where masked
+    l = pt.sum(axis=1)                                         # unquantised sum
+    p8 = np.ldexp(pt, P_SCALE_LOG2)
+    ph = e4m3_decode(e4m3_encode(p8)) if quant else p8         # E4M3 probability operand
+    vhat = dh.v[cols] * np.ldexp(1.0, dh.ev[cols])[:, None]
+    o = np.ldexp(ph @ vhat, -P_SCALE_LOG2) / l[:, None]
+    return o, m + np.log2(l), m, l
+
+
+def _block_quantize_dS(dS: np.ndarray, r0: int, c0: int) -> np.ndarray:
+    """dS rounded through E4M3 with one round-up exponent per 32x32 block whose
+    origin is aligned to the document start (r0, c0 are doc-local offsets of
+    the rectangle and must be multiples of 32)."""
+    assert r0 % 32 == 0 and c0 % 32 == 0
+    out = np.empty_like(dS)
+    R, C = dS.shape
+    for i0 in range(0, R, 32):
+        for j0 in range(0, C, 32):
+            blk = dS[i0:i0 + 32, j0:j0 + 32]
+            e = int(roundup_exponent(np.abs(blk).max()))
+            out[i0:i0 + 32, j0:j0 + 32] = e4m3_decode(e4m3_encode(blk * 2.0 ** -e)) * 2.0 ** e
+    return out
+
+
+def bwd_rect(dh: DocHead, rows: np.ndarray, cols: np.ndarray, lse2_rows: np.ndarray,
+             D_rows: np.ndarray, sm_scale: float, quant: bool = True):
+    """Backward contributions of the rectangle rows x cols.
+
+    rows and cols are contiguous doc-local ranges starting on a 32 boundary.
+    Returns (dQ partial [R, d] over these cols, dK partial [C, d] and dV
+    partial [C, d] over these rows, dS [R, C])."""
+    s = _scores(dh, rows, cols, sm_scale)
+    P = np.exp2(s - lse2_rows[:, None])                        # normalised, 0 where masked
+    pb = np.ldexp(P, P_SCALE_LOG2)
+    pbh = e4m3_decode(e4m3_encode(pb)) if quant else pb        # dV operand
+    dohat = dh.do[rows] * np.ldexp(1.0, dh.edo[rows])[:, None]
+    vhat = dh.v[cols] * np.ldexp(1.0, dh.ev[cols])[:, None]
+    dP = dohat @ vhat.T
+    dS = P * (dP - D_rows[:, None])
+    dSh = _block_quantize_dS(dS, int(rows[0]), int(cols[0])) if quant else dS
+    qhat = dh.q[rows] * np.ldexp(1.0, dh.eq[rows])[:, None]
+    khat = dh.k[cols] * np.ldexp(1.0, dh.ek[cols])[:, None]
+    dV = np.ldexp(pbh.T @ dohat, -P_SCALE_LOG2)
+    dK = sm_scale * (dSh.T @ qhat)
+    dQ = sm_scale * (dSh @ khat)
+    return dQ, dK, dV, dS
+
+
+# ----------------------------------------------------------------------------
+# Whole-tensor entry points
+# ----------------------------------------------------------------------------
+
+class Quantized:
+    """Token-block quantised operands of one attention call (+ optional NVFP4 Q, K)."""
+
+    def __init__(self, q, k, v, do, cu_seqlens, qk_format: str = "mxfp8",
+                 rule: str = "up", group: str = "block"):
+        self.cu = [int(c) for c in cu_seqlens]
+        self.qc, self.qs = quantize_tokenblock(q, self.cu, rule, group)
+        self.kc, self.ks = quantize_tokenblock(k, self.cu, rule, group)
+        self.vc, self.vs = quantize_tokenblock(v, self.cu, rule, group)
+        self.doc, self.dos = (quantize_tokenblock(do, self.cu, rule, group)
+                              if do is not None else (None, None))
+        self.qk_format = qk_format
+        if qk_format == "nvfp4":
+            self.q4 = dequantize_nvfp4(*quantize_nvfp4(q))
+            self.k4 = dequantize_nvfp4(*quantize_nvfp4(k))
+
+    def dochead(self, b: int, h: int) -> DocHead:
+        s, e = self.cu[b], self.cu[b + 1]
+        ex = lambda sb: sb[h, s:e].astype(np.int64) - 127
+        dh = DocHead(e4m3_decode(self.qc[s:e, h]), ex(self.qs),
+                     e4m3_decode(self.kc[s:e, h]), ex(self.ks),
+                     e4m3_decode(self.vc[s:e, h]), ex(self.vs),
+                     e4m3_decode(self.doc[s:e, h]) if self.doc is not None else None,
+                     ex(self.dos) if self.doc is not None else None)
+        if self.qk_format == "nvfp4":
+            dh.qs, dh.ks = self.q4[s:e, h], self.k4[s:e, h]
+        return dh
+
+
+def exact_dochead(q, k, v, do, cu, b, h) -> DocHead:
+    s, e = cu[b], cu[b + 1]
+    z = np.zeros(e - s, dtype=np.int64)
+    f = lambda x: np.asarray(x[s:e, h], dtype=np.float64)
+    return DocHead(f(q), z, f(k), z, f(v), z, f(do) if do is not None else None, z)
+
+
+def attention(q, k, v, do, cu_seqlens, sm_scale: float, quant: bool = True,
+              qk_format: str = "mxfp8", rule: str = "up", group: str = "block",
+              heads=None, docs=None, backward: bool = True):
+    """Full forward (+ backward) over packed [T, H, d] float64 inputs.
+
+    Returns a dict with O [T, H, d] (float64), O_bf16, lse [H, T] (natural log,
+    +inf where not computed) and, with backward, dQ, dK, dV [T, H, d] and D
+    [H, T].  ``heads`` / ``docs`` restrict the work (other entries stay 0)."""
+    q = np.asarray(q, dtype=np.float64)
+    T, H, d = q.shape
+    cu = [int(c) for c in cu_seqlens]
+    heads = range(H) if heads is None else heads
+    docs = range(len(cu) - 1) if docs is None else docs
+    qz = Quantized(q, k, v, do if backward else None, cu, qk_format, rule, group) if quant else None
+    out = {n: np.zeros((T, H, d)) for n in ("O", "O_bf16", "dQ", "dK", "dV")}
+    out["lse"] = np.full((H, T), np.inf)
+    out["D"] = np.zeros((H, T))
+    for b in docs:
+        s, e = cu[b], cu[b + 1]
+        if e == s:
+            continue
+        for h in heads:
+            dh = qz.dochead(b, h) if quant else exact_dochead(q, k, v, do, cu, b, h)
+            rows = np.arange(e - s)
+            o, lse2, _, _ = fwd_rows(dh, rows, sm_scale, quant)
+            out["O"][s:e, h] = o
+            out["O_bf16"][s:e, h] = bf16_round(o)
+            out["lse"][h, s:e] = lse2 * LN2
+            if not backward:
+                continue
+            dohat = dh.do * np.ldexp(1.0, dh.edo)[:, None]
+            # D uses the forward's BF16 output in the quantised method and the
+            # exact output in the unquantised reference
+            o_for_D = out["O_bf16"][s:e, h] if quant else o
+            D = (dohat * o_for_D).sum(axis=1)
+            out["D"][h, s:e] = D
+            dQ, dK, dV, _ = bwd_rect(dh, rows, rows, lse2, D, sm_scale, quant)
+            out["dQ"][s:e, h] = dQ
+            out["dK"][s:e, h] = dK
+            out["dV"][s:e, h] = dV
+    if quant:
+        out["quantized"] = qz
+    return out
+
+
+def sampled_rows(qz: Quantized, b: int, h: int, sm_scale: float, qblocks, kblocks):
+    """Outputs of selected 32-token query blocks (O, lse, dQ) and 32-token key
+    blocks (dK, dV) of document b, head h, each computed from its own
+    definition (every key a query row sees, every query row a key sees).
+
+    qblocks / kblocks are doc-local block indices.  Returns dicts keyed by the
+    doc-local block index."""
+    dh = qz.dochead(b, h)
+    L = dh.L
+    res = {"O": {}, "lse": {}, "dQ": {}, "dK": {}, "dV": {}}
+
+    def stats(rows):
+        o, lse2, _, _ = fwd_rows(dh, rows, sm_scale, True)
+        dohat = dh.do[rows] * np.ldexp(1.0, dh.edo[rows])[:, None]
+        D = (dohat * bf16_round(o)).sum(axis=1)
+        return o, lse2, D
+
+    for qb in qblocks:
+        rows = np.arange(32 * qb, min(32 * qb + 32, L))
+        o, lse2, D = stats(rows)
+        cols = np.arange(0, int(rows[-1]) + 1)
+        dQ, _, _, _ = bwd_rect(dh, rows, cols, lse2, D, sm_scale, True)
+        res["O"][qb], res["lse"][qb], res["dQ"][qb] = o, lse2 * LN2, dQ
+    for kb in kblocks:
+        cols = np.arange(32 * kb, min(32 * kb + 32, L))
+        rows = np.arange(32 * kb, L)
+        _, lse2, D = stats(rows)
+        _, dK, dV, _ = bwd_rect(dh, rows, cols, lse2, D, sm_scale, True)
+        res["dK"][kb], res["dV"][kb] = dK, dV
+    return res
+
+
+def cosine(a, b) -> float:
+    a = np.asarray(a, dtype=np.float64).ravel()
+    b = np.asarray(b, dtype=np.float64).ravel()
+    na, nb = np.linalg.norm(a), np.linalg.norm(b)
+    if na == 0 and nb == 0:
+        return 1.0
+    return float(a @ b / (na * nb))
