@@ -1,0 +1,191 @@
+/*
+ * flamia.h -- C ABI of the token-block microscaled (MXFP8) causal flash
+ * attention hot path for one GB300 (sm_103a) GPU.
+ *
+ * The method is the one described in "FLAMIA: FLAsh MIcroscaling Attention
+ * for Fast and Causally Safe Training on Blackwell" (review page
+ * jaehun.me/en/posts/paper-2611-03344v1, sections cited per entry point; and
+ * the summary page agihunt.info/en/papers/2611.03344).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Packed layout.  Documents are concatenated along the token axis.  A tensor
+ *   "[T, H, d]" is row-major (token, head, dim) with no padding.
+ *   cu_seqlens is int32[ndocs + 1] in DEVICE memory: document b is tokens
+ *   [cu_seqlens[b], cu_seqlens[b+1]); cu_seqlens[0] == 0, cu_seqlens[ndocs]
+ *   == T, non-decreasing (empty documents are allowed).
+ * - Ownership.  Every pointer argument is a DEVICE pointer owned by the caller
+ *   unless stated otherwise.  The library never allocates, frees or
+ *   synchronises, and never reads device data on the host.  All work is
+ *   enqueued on `stream` (a cudaStream_t, NULL = legacy default stream).
+ * - Errors.  Argument errors found on the host return a flamia_status and
+ *   enqueue nothing.  Errors found on the device (malformed cu_seqlens,
+ *   capacity overflow, a bounded wait that timed out) are OR-ed into the
+ *   int at `dev_status` (device memory, may be NULL to ignore) as
+ *   FLAMIA_DEV_* bits; read it after synchronising the stream.  No kernel
+ *   traps or spins without bound.
+ * - Support.  head_dim d in {64, 128}; H >= 1; MHA (one K/V head per query
+ *   head); causal masking; T < 2^24.
+ * - Formats.  E4M3 = OCP FP8 E4M3FN (bias 7, max 448, subnormals kept).
+ *   E8M0 = 2^(byte - 127).  E2M1 = {0, .5, 1, 1.5, 2, 3, 4, 6} with sign,
+ *   two codes per byte, element 2i in the low nibble.
+ */
+#ifndef FLAMIA_H
+#define FLAMIA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FLAMIA_OK = 0,
+  FLAMIA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned buffer      */
+  FLAMIA_ERR_UNSUPPORTED = 2,   /* d not in {64,128}, unknown format or flag      */
+  FLAMIA_ERR_WORKSPACE = 3,     /* workspace / work-list buffer too small         */
+  FLAMIA_ERR_CUDA = 4           /* a CUDA runtime call failed (launch, memset)    */
+} flamia_status;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define FLAMIA_DEV_BAD_SEQLENS 0x1  /* cu_seqlens not monotone or not ending at T */
+#define FLAMIA_DEV_CAPACITY    0x2  /* more work items than the buffer holds      */
+#define FLAMIA_DEV_TIMEOUT     0x4  /* a bounded wait gave up; outputs invalid    */
+
+/* Quantiser output formats. */
+#define FLAMIA_FORMAT_MXFP8       0 /* E4M3 codes + per-token E8M0 scales          */
+#define FLAMIA_FORMAT_MXFP8_NVFP4 1 /* the above plus NVFP4 codes and scales       */
+
+/* Attention flags. */
+#define FLAMIA_FLAG_NVFP4_QK 0x1    /* score product QK^T (fwd and bwd recompute)
+                                       from the NVFP4 copy of Q and K (d == 64)   */
+
+/*
+ * One quantised operand, all device pointers owned by the caller.
+ *  codes        u8  [T, H, d]     E4M3 codes.
+ *  scales       u8  [H, T]        E8M0 byte of each token's 32-token block
+ *                                 (dense: one entry per token and head).
+ *  nvfp4_codes  u8  [T, H, d/2]   packed E2M1 (NULL unless NVFP4 requested).
+ *  nvfp4_scales u8  [T, H, d/16]  E4M3 scale of each 16-element group (NULL
+ *                                 unless NVFP4 requested).
+ * codes and nvfp4_codes must be 16-byte aligned.
+ */
+typedef struct {
+  uint8_t* codes;
+  uint8_t* scales;
+  uint8_t* nvfp4_codes;
+  uint8_t* nvfp4_scales;
+} flamia_qtensor;
+
+/*
+ * Fused token-block quantiser.
+ * Source: review page sec. 3.1 (one power-of-two exponent per 32 consecutive
+ * tokens x the full head dimension, E4M3 codes; the scale is constant along
+ * the head dimension, so the payload serves K-major and MN-major products),
+ * sec. 3.2 (exponent rounded up: the scaled block maximum never exceeds 448),
+ * sec. 3.4 "Quantization fusion" (statistics, codes and scales in one launch)
+ * and "Packed documents" (blocks never cross a document; dense per-token
+ * scale table).  Blocks of document [s, e) are [s + 32i, min(s + 32i + 32, e)).
+ * Exponent: smallest e with amax <= 448 * 2^e, clamped to [-127, 127]
+ * (amax == 0 -> -127); codes = RNE_E4M3(x * 2^-e); scale byte = e + 127.
+ * With format FLAMIA_FORMAT_MXFP8_NVFP4 the same pass also writes the NVFP4
+ * copy (sec. 3.1 mixed path): per token and 16-element group, scale = the
+ * smallest E4M3 value >= amax / 6, codes = RNE_E2M1(x / scale).
+ *
+ *  x_bf16     [T, H, d] BF16 input (finite values).
+ *  o_bf16, D  optional (both NULL or both set): the forward output O [T, H, d]
+ *             BF16 and D float [H, T] = sum_k dequant(x)[t,h,k] * O[t,h,k]
+ *             (review sec. 3.3: D from the same quantised dO used for dP).
+ *  out        host pointer to a flamia_qtensor naming the caller's buffers.
+ */
+flamia_status flamia_quantize_tokenblock(const void* x_bf16, int T, int H, int d,
+                                         const int32_t* cu_seqlens, int ndocs, int format,
+                                         const void* o_bf16, float* D,
+                                         const flamia_qtensor* out, int* dev_status,
+                                         void* stream);
+
+/*
+ * Work list.  Source: review page sec. 3.4 "Work scheduling": a forward item
+ * is 256 consecutive queries of one document (two 128-query tiles), its cost
+ * the number of 128-key blocks it visits; items are sorted by descending
+ * cost, built on the GPU once per micro-batch without a host sync.  The
+ * backward items are 128-key tiles costed by the 128-query tiles that see
+ * them.  Ties keep generation order (document, then position).
+ *
+ * Buffer layout (device, caller-owned, flamia_worklist_bytes(T, ndocs) bytes,
+ * 256-byte aligned):
+ *   int32 header[16]: [0] n_fwd, [1] n_bwd, [2] cap_fwd, [3] cap_bwd,
+ *                     [4] max cost; the rest reserved.
+ *   int32x4 fwd_items[cap_fwd] at byte 64: {doc, q_start, q_end, cost}
+ *   int32x4 bwd_items[cap_bwd] after it:    {doc, k_start, k_end, cost}
+ *   followed by the builder's scratch.
+ * cap_fwd = T/256 + ndocs + 1, cap_bwd = T/128 + ndocs + 1 (upper bounds).
+ */
+size_t flamia_worklist_bytes(int T, int ndocs);
+flamia_status flamia_build_worklist(const int32_t* cu_seqlens, int ndocs, int T,
+                                    void* wl, size_t wl_bytes, int* dev_status,
+                                    void* stream);
+
+/*
+ * Causal forward.  Source: review page sec. 1.2 (S = QK^T scale, P =
+ * softmax(S), O = PV, row statistics saved), sec. 3.1 (unscaled E4M3 product
+ * for QK^T with the query factor folded into the softmax scale and the key
+ * factor applied separately; E4M3 probability operand; BF16 output), sec. 3.4
+ * "Packed documents" (outputs written in place to the packed buffer).
+ * Numerics: s_ij = scale * log2(e) * 2^eQ(i) * 2^eK(j) * <q_i, k_j> (codes),
+ * running integer row maximum m_i = ceil(max_j s_ij), P~ = exp2(s - m),
+ * l = sum P~, operand P^ = RNE_E4M3(2^8 P~), O = 2^-8 sum_j P^ V^_j / l,
+ * LSE = (m + log2 l) ln 2.
+ *
+ *  q, k, v      host pointers to quantised operands (E4M3 + scales; with
+ *               FLAMIA_FLAG_NVFP4_QK also the NVFP4 copies of q and k).
+ *  wl           a work list built for the same cu_seqlens / T.
+ *  o_bf16       [T, H, d] BF16 output.   lse  float [H, T] (natural log).
+ * Only tokens inside documents are written.
+ */
+flamia_status flamia_attn_fwd(const flamia_qtensor* q, const flamia_qtensor* k,
+                              const flamia_qtensor* v, const int32_t* cu_seqlens, int ndocs,
+                              int T, int H, int d, float softmax_scale, int flags,
+                              const void* wl, void* o_bf16, float* lse, int* dev_status,
+                              void* stream);
+
+/*
+ * Workspace of the backward: a float32 [T, H, d] dQ accumulator plus
+ * alignment.  The caller allocates it; the backward clears it itself.
+ */
+size_t flamia_bwd_workspace_bytes(int T, int H, int d);
+
+/*
+ * Causal backward.  Source: review page sec. 1.2 (recompute P; dV = P^T dO,
+ * dP = dO V^T, dS = P o (dP - D), dQ = dS K, dK = dS^T Q), sec. 3.3 (the
+ * recompute uses the forward's quantised Q, K, tiling, masks and exp; D from
+ * the same quantised dO), sec. 3.1 (dS to E4M3 with one scale per 32x32 block
+ * so one payload feeds dQ and dK), sec. 3.4 "Backward pass".
+ * Numerics: P = exp2(s - LSE log2 e); dV operand RNE_E4M3(2^8 P); dS in float
+ * from the unquantised P; dS exponent = round-up rule on each document-aligned
+ * 32x32 block maximum; dQ and dK scaled by softmax_scale after the products;
+ * dQ partial sums are added in float32 (no prescale), then converted to BF16.
+ *
+ *  dout         host pointer to the quantised dO (from the quantiser run with
+ *               o_bf16 = the forward output, which also produced D).
+ *  D, lse       float [H, T] from the quantiser and the forward.
+ *  dq, dk, dv   [T, H, d] BF16 outputs (only tokens inside documents written).
+ *  ws           flamia_bwd_workspace_bytes(T, H, d) bytes, 256-byte aligned.
+ */
+flamia_status flamia_attn_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
+                              const flamia_qtensor* v, const flamia_qtensor* dout,
+                              const float* D, const float* lse,
+                              const int32_t* cu_seqlens, int ndocs, int T, int H, int d,
+                              float softmax_scale, int flags, const void* wl,
+                              void* dq_bf16, void* dk_bf16, void* dv_bf16,
+                              void* ws, size_t ws_bytes, int* dev_status, void* stream);
+
+/* Static description of a status code (never NULL). */
+const char* flamia_status_str(flamia_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLAMIA_H */

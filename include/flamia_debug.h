@@ -1,0 +1,47 @@
+/*
+ * flamia_debug.h -- test-only entry points of the flamia library.
+ *
+ * They expose one tensor-core tile product so the tests can check, on a
+ * single 128-row tile, every operand layout and scale-factor layout the
+ * attention kernels rely on (the review page's sec. 3.1: one E4M3 payload read
+ * both K-major and MN-major; block-scaled products with E8M0 scales per 32
+ * elements; the mixed path's NVFP4 product with E4M3 scales per 16).
+ * Not part of the attention API; same ownership and error rules as flamia.h.
+ */
+#ifndef FLAMIA_DEBUG_H
+#define FLAMIA_DEBUG_H
+
+#include <stdint.h>
+
+#include "flamia.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * D[128][N] (float32, device) = A[128 x K] * B[K x N] for one tile.
+ *  mode 0: E4M3 x E4M3, unscaled (K = 128).
+ *  mode 1: E4M3 x E4M3 block-scaled, E8M0 scale per 32 along K (K = 128);
+ *          sfa u8 [128][4], sfb u8 [N][4].
+ *  mode 2: E2M1 x E2M1 block-scaled, E4M3 scale per 16 along K (K = 64,
+ *          two codes per byte, element 2i in the low nibble); sfa u8 [128][4],
+ *          sfb u8 [N][4]; both operands K-major.
+ *  a: a_mn_major == 0 -> u8 [128][K bytes] (rows = M); 1 -> u8 [K][128].
+ *  b: b_mn_major == 0 -> u8 [N][K bytes]   (rows = N); 1 -> u8 [K][N].
+ *  N in {64, 128}.  variant: bit 0 swaps the leading / stride byte offsets of
+ *  MN-major descriptors; bits 1..2 select the scale-factor placement in
+ *  tensor memory (0: column = row / 32, lane = row % 32, replicated in all
+ *  lane quadrants; 1: lane = row).
+ * All pointers are device pointers, 16-byte aligned.
+ */
+flamia_status flamia_debug_mma_tile(int mode, int N, int a_mn_major, int b_mn_major, int variant,
+                                    const uint8_t* a, const uint8_t* b, const uint8_t* sfa,
+                                    const uint8_t* sfb, float* d_out, int* dev_status,
+                                    void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLAMIA_DEBUG_H */

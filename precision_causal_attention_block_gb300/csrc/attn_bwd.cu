@@ -1,0 +1,515 @@
+// Causal backward over token-block MXFP8 operands (FLAMIA review page, sec.
+// 1.2, 3.1, 3.3, 3.4 "Backward pass").
+//
+// One CTA = one 128-key tile of a document x one head; it walks the 128-query
+// tiles of the same document from the diagonal to the document end.  Warp
+// roles:
+//   warp 0      TMA producer: K, V once; Q, dO tiles through a ring.
+//   warp 1      tensor-memory owner and single-thread tcgen05 MMA issuer.
+//   warps 4-7   compute group: thread = key row of S^T / dP^T, and query row
+//               of the dQ partial.
+// Per query tile u:
+//   S^T = K Q^T and dP^T = V dO^T (unscaled E4M3, f32 in TMEM);
+//   the compute group recomputes P = exp2(s - lse2) with the forward's
+//   factors and masks, writes the dV operand RNE_E4M3(2^8 P) and the dS
+//   codes (one round-up exponent per document-aligned 32x32 block) to shared
+//   memory, and the block scales of the three products to TMEM;
+//   dV += P^b^T dO, dK += dS^T Q (both stay in TMEM over all u) and
+//   dQ_u = dS K (into the columns of S^T) are block-scaled MMAs;
+//   dQ_u is read back and added in float32 to a global accumulator.
+// Tensor memory (512 columns): S^T / dQ_u [0,128), dP^T and the scale
+// factors [128,256), dV [256,256+d), dK [256+d,256+2d).
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace flamia {
+namespace {
+
+constexpr int kBStages = 2;
+constexpr int kBwdThreads = 256;
+constexpr uint32_t kColSP = 0, kColDP = 128, kColDV = 256;
+// scale-factor columns inside the dP^T region (written after dP^T is read)
+constexpr uint32_t kSfDvA = 128, kSfDvB = 132, kSfDkA = 136, kSfDkB = 140, kSfDqA = 144,
+                   kSfDqB = 148;
+
+template <int DIM>
+struct BwdSmem {
+  static constexpr int kTileBytes = kTile * DIM;
+  alignas(1024) uint8_t k[kTileBytes];
+  alignas(1024) uint8_t v[kTileBytes];
+  alignas(1024) uint8_t q[kBStages][kTileBytes];
+  alignas(1024) uint8_t dout[kBStages][kTileBytes];
+  alignas(1024) uint8_t pb[kTile * kTile];  // [key][query] E4M3, 128B-swizzled rows
+  alignas(1024) uint8_t ds[kTile * kTile];  // [key][query] E4M3, 128B-swizzled rows
+  float nl[kTile];        // 8 - lse2 of each query column (-inf outside the document)
+  float dd[kTile];        // D of each query column (0 outside)
+  uint32_t qbyte[4], dobyte[4];  // E8M0 bytes of the 4 query blocks of Q and dO
+  uint32_t eds[4][4];     // dS block bytes [query block][key block]
+  uint64_t bar_kv;
+  uint64_t bar_qd_full[kBStages];
+  uint64_t bar_qd_empty[kBStages];
+  uint64_t bar_s_full, bar_ds_full, bar_dq_full, bar_s_free, bar_done;
+  uint32_t tmem_base;
+  volatile int abort;
+};
+
+struct BwdParams {
+  const uint8_t* q_scales;
+  const uint8_t* k_scales;
+  const uint8_t* v_scales;
+  const uint8_t* do_scales;
+  const float* D;
+  const float* lse;
+  const int32_t* cu;
+  const int* wl_header;
+  const int4* items;
+  float* dq_acc;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int T, H, ndocs;
+  float scale_log2;  // softmax_scale * log2(e)
+  float sm_scale;
+  int* status;
+};
+
+template <int DIM>
+__host__ __device__ constexpr uint32_t operand_layout() {
+  return DIM == 128 ? kLayoutSW128 : kLayoutSW64;
+}
+
+__device__ __forceinline__ float pow2_or_zero(int k) { return k < -126 ? 0.f : exp2i(k); }
+
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a),
+               "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+template <int DIM>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_kernel(const __grid_constant__ CUtensorMap map_q,
+                    const __grid_constant__ CUtensorMap map_k,
+                    const __grid_constant__ CUtensorMap map_v,
+                    const __grid_constant__ CUtensorMap map_do, const BwdParams prm) {
+  extern __shared__ uint8_t smem_raw[];
+  BwdSmem<DIM>& sm = *reinterpret_cast<BwdSmem<DIM>*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
+  const int H = prm.H, T = prm.T;
+  const int item_idx = blockIdx.x / H;
+  const int h = blockIdx.x % H;
+  if (item_idx >= prm.wl_header[kHdrNBwd]) return;
+  const int4 item = prm.items[item_idx];
+  // clamped: a malformed work list or offsets cannot index outside [0, T)
+  const int doc = min(max(item.x, 0), prm.ndocs - 1);
+  const int s = min(max(prm.cu[doc], 0), T);
+  const int e = min(max(prm.cu[doc + 1], s), T);
+  const int k0 = s + ((min(max(item.y, s), e) - s) & ~(kTile - 1));
+  const int k1 = min(max(item.z, k0), min(k0 + kTile, e));
+  const int nq = (e - k0 + kTile - 1) / kTile;  // query tiles from the diagonal to the end
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&sm.bar_kv), 1);
+    for (int i = 0; i < kBStages; ++i) {
+      mbar_init(smem_u32(&sm.bar_qd_full[i]), 1);
+      mbar_init(smem_u32(&sm.bar_qd_empty[i]), 1);
+    }
+    mbar_init(smem_u32(&sm.bar_s_full), 1);
+    mbar_init(smem_u32(&sm.bar_ds_full), kTile);
+    mbar_init(smem_u32(&sm.bar_dq_full), 1);
+    mbar_init(smem_u32(&sm.bar_s_free), kTile);
+    mbar_init(smem_u32(&sm.bar_done), 1);
+    sm.abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sm.tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  constexpr uint32_t kTileBytes = BwdSmem<DIM>::kTileBytes;
+  constexpr uint32_t lay = operand_layout<DIM>();
+  constexpr uint32_t sbo = 8 * DIM;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tensormap(&map_q);
+      prefetch_tensormap(&map_k);
+      prefetch_tensormap(&map_v);
+      prefetch_tensormap(&map_do);
+      const uint32_t bkv = smem_u32(&sm.bar_kv);
+      mbar_arrive_expect_tx(bkv, 2 * kTileBytes);
+      tma_load_3d(smem_u32(sm.k), &map_k, bkv, 0, h, k0);
+      tma_load_3d(smem_u32(sm.v), &map_v, bkv, 0, h, k0);
+      int issued = 0;
+      for (int u = 0; u < nq; ++u) {
+        const int st = u % kBStages;
+        if (u >= kBStages) {
+          if (!mbar_wait(smem_u32(&sm.bar_qd_empty[st]), ((u / kBStages) - 1) & 1) ||
+              sm.abort) {
+            sm.abort = 1;
+            break;
+          }
+        }
+        const uint32_t bf = smem_u32(&sm.bar_qd_full[st]);
+        mbar_arrive_expect_tx(bf, 2 * kTileBytes);
+        tma_load_3d(smem_u32(sm.q[st]), &map_q, bf, 0, h, k0 + u * kTile);
+        tma_load_3d(smem_u32(sm.dout[st]), &map_do, bf, 0, h, k0 + u * kTile);
+        issued = u + 1;
+      }
+      bool ok = mbar_wait(bkv, 0);
+      for (int u = max(0, issued - kBStages); u < issued; ++u)
+        ok &= mbar_wait(smem_u32(&sm.bar_qd_full[u % kBStages]), (u / kBStages) & 1);
+      if (!ok) sm.abort = 1;
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t id_s = idesc_f8(kTile, kTile, 0, 0);
+      bool ok = mbar_wait(smem_u32(&sm.bar_kv), 0);
+      const uint32_t ka = smem_u32(sm.k), va = smem_u32(sm.v);
+      const uint32_t pba = smem_u32(sm.pb), dsa = smem_u32(sm.ds);
+      for (int u = 0; ok && u < nq; ++u) {
+        const int st = u % kBStages;
+        if (!mbar_wait(smem_u32(&sm.bar_qd_full[st]), (u / kBStages) & 1) ||
+            (u > 0 && !mbar_wait(smem_u32(&sm.bar_s_free), (u - 1) & 1)) || sm.abort) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t qa = smem_u32(sm.q[st]), da = smem_u32(sm.dout[st]);
+#pragma unroll
+        for (int ks = 0; ks < DIM / 32; ++ks)
+          mma_f8(tmem + kColSP, smem_desc(ka + 32 * ks, 0, sbo, lay),
+                 smem_desc(qa + 32 * ks, 0, sbo, lay), id_s, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < DIM / 32; ++ks)
+          mma_f8(tmem + kColDP, smem_desc(va + 32 * ks, 0, sbo, lay),
+                 smem_desc(da + 32 * ks, 0, sbo, lay), id_s, ks > 0);
+        tc_commit(smem_u32(&sm.bar_s_full));
+        if (!mbar_wait(smem_u32(&sm.bar_ds_full), u & 1) || sm.abort) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // dV += P^b^T dO : A [key][query] K-major, B = dO tile read MN-major
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb)
+          mma_mxf8(tmem + kColDV, smem_desc(pba + 32 * kb, 0, 1024, kLayoutSW128),
+                   smem_desc(da + kb * 32 * DIM, 0, sbo, lay), idesc_mxf8(kTile, DIM, 0, 1, kb, kb),
+                   tmem + kSfDvA, tmem + kSfDvB, (u > 0 || kb > 0));
+        // dK += dS^T Q : A [key][query] K-major, B = Q tile read MN-major
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb)
+          mma_mxf8(tmem + kColDV + DIM, smem_desc(dsa + 32 * kb, 0, 1024, kLayoutSW128),
+                   smem_desc(qa + kb * 32 * DIM, 0, sbo, lay), idesc_mxf8(kTile, DIM, 0, 1, kb, kb),
+                   tmem + kSfDkA, tmem + kSfDkB, (u > 0 || kb > 0));
+        // dQ_u = dS K : A = the same dS bytes read MN-major (M = queries), B = K MN-major
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb)
+          mma_mxf8(tmem + kColSP, smem_desc(dsa + kb * 32 * kTile, 0, 1024, kLayoutSW128),
+                   smem_desc(ka + kb * 32 * DIM, 0, sbo, lay), idesc_mxf8(kTile, DIM, 1, 1, kb, kb),
+                   tmem + kSfDqA, tmem + kSfDqB, kb > 0);
+        tc_commit(smem_u32(&sm.bar_dq_full));
+        tc_commit(smem_u32(&sm.bar_qd_empty[st]));
+      }
+      if (!ok) sm.abort = 1;
+      tc_commit(smem_u32(&sm.bar_done));
+      if (!mbar_wait(smem_u32(&sm.bar_done), 0)) sm.abort = 1;
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ compute group
+    const int quad = warp & 3;
+    const int j = quad * 32 + lane;  // key row (S^T, dP^T, dV, dK) / query row (dQ_u)
+    const int kj = k0 + j;
+    const bool key_valid = kj < k1;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const size_t hT = static_cast<size_t>(h) * T;
+    const int ekj = key_valid ? static_cast<int>(prm.k_scales[hT + kj]) - 127 : 0;
+    const int evj = key_valid ? static_cast<int>(prm.v_scales[hT + kj]) - 127 : 0;
+    const float rowf = pow2_or_zero(ekj);
+    const float rowg = pow2_or_zero(evj);
+    // E8M0 bytes of this key tile's 4 key blocks (B scale of dQ_u = dS K)
+    uint32_t kword = 0;
+#pragma unroll
+    for (int kb = 0; kb < 4; ++kb) {
+      const int kk = k0 + 32 * kb;
+      kword |= (kk < e ? static_cast<uint32_t>(prm.k_scales[hT + kk]) : 127u) << (8 * kb);
+    }
+    const float LOG2E = 1.4426950408889634f;
+    bool ok = true;
+    for (int u = 0; u < nq; ++u) {
+      const int q0 = k0 + u * kTile;
+      {
+        const int qi = q0 + j;
+        const bool qv = qi < e;
+        sm.nl[j] = qv ? 8.f - prm.lse[hT + qi] * LOG2E : -INFINITY;
+        sm.dd[j] = qv ? prm.D[hT + qi] : 0.f;
+        if (lane == 0) {
+          sm.qbyte[quad] = qv ? prm.q_scales[hT + qi] : 127u;
+          sm.dobyte[quad] = qv ? prm.do_scales[hT + qi] : 127u;
+        }
+      }
+      named_barrier_sync(1, kTile);
+      float fS[4], fP[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        fS[c] = rowf * prm.scale_log2 * pow2_or_zero(static_cast<int>(sm.qbyte[c]) - 127);
+        fP[c] = rowg * pow2_or_zero(static_cast<int>(sm.dobyte[c]) - 127);
+      }
+      if (!mbar_wait(smem_u32(&sm.bar_s_full), u & 1) || sm.abort) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint8_t* pbrow = sm.pb + j * kTile;
+      uint8_t* dsrow = sm.ds + j * kTile;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t sv[32], dv[32];
+        tmem_ld32(tmem + lane_off + kColSP + 32 * c, sv);
+        tmem_ld32(tmem + lane_off + kColDP + 32 * c, dv);
+        tmem_ld_wait();
+        float amax = 0.f;
+        uint32_t pw[8];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          float p8[2], d8[2];
+#pragma unroll
+          for (int w = 0; w < 2; ++w) {
+            const int col = 32 * c + i + w;
+            const bool vis = key_valid && (u > 0 || col >= j);
+            const float x = vis ? fmaf(__uint_as_float(sv[i + w]), fS[c], sm.nl[col]) : -INFINITY;
+            p8[w] = ex2_approx(x);
+            d8[w] = p8[w] * fmaf(__uint_as_float(dv[i + w]), fP[c], -sm.dd[col]);
+            amax = fmaxf(amax, fabsf(d8[w]));
+            dv[i + w] = __float_as_uint(d8[w]);
+          }
+          const uint32_t pc = cvt_e4m3x2(p8[0], p8[1]);
+          if ((i & 2) == 0) pw[i / 4] = pc;
+          else pw[i / 4] |= pc << 16;
+        }
+        // one exponent per 32x32 block: this warp's 32 key rows x these 32 queries
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        const int eb = max(roundup_exponent(amax) - 8, -127);  // exponent of dS = 2^-8 dS8
+        const float inv = exp2i(-(eb + 8));
+        uint32_t dw[8];
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          dw[i / 4] = cvt_e4m3x2(__uint_as_float(dv[i]) * inv, __uint_as_float(dv[i + 1]) * inv) |
+                      (cvt_e4m3x2(__uint_as_float(dv[i + 2]) * inv,
+                                  __uint_as_float(dv[i + 3]) * inv)
+                       << 16);
+        }
+        const int ch0 = (2 * c) ^ (j & 7), ch1 = (2 * c + 1) ^ (j & 7);
+        *reinterpret_cast<uint4*>(pbrow + 16 * ch0) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+        *reinterpret_cast<uint4*>(pbrow + 16 * ch1) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
+        *reinterpret_cast<uint4*>(dsrow + 16 * ch0) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
+        *reinterpret_cast<uint4*>(dsrow + 16 * ch1) = make_uint4(dw[4], dw[5], dw[6], dw[7]);
+        if (lane == 0) sm.eds[c][quad] = static_cast<uint32_t>(eb + 127);
+      }
+      named_barrier_sync(1, kTile);
+      {
+        // block scales of the three products; every lane quadrant holds the
+        // same words: column (base + m/32) of an A scale holds the 4 K-block
+        // bytes of rows m/32*32 .. +31
+        uint32_t w0[8], w1[8], w2[8];
+        const uint32_t dow = sm.dobyte[0] | (sm.dobyte[1] << 8) | (sm.dobyte[2] << 16) |
+                             (sm.dobyte[3] << 24);
+        const uint32_t qw = sm.qbyte[0] | (sm.qbyte[1] << 8) | (sm.qbyte[2] << 16) |
+                            (sm.qbyte[3] << 24);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          w0[i] = 0x7F7F7F7Fu;  // dV: A = P^b, scale 2^0
+          w0[4 + i] = dow;      // dV: B = dO, per query block
+          // dK: A = dS^T, row block = key block i, K blocks = query blocks
+          w1[i] = sm.eds[0][i] | (sm.eds[1][i] << 8) | (sm.eds[2][i] << 16) | (sm.eds[3][i] << 24);
+          w1[4 + i] = qw;       // dK: B = Q, per query block
+          // dQ: A = dS, row block = query block i, K blocks = key blocks
+          w2[i] = sm.eds[i][0] | (sm.eds[i][1] << 8) | (sm.eds[i][2] << 16) | (sm.eds[i][3] << 24);
+          w2[4 + i] = kword;    // dQ: B = K, per key block
+        }
+        tmem_st8(tmem + lane_off + kSfDvA, w0);
+        tmem_st8(tmem + lane_off + kSfDkA, w1);
+        tmem_st8(tmem + lane_off + kSfDqA, w2);
+        tmem_st_wait();
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.bar_ds_full));
+      if (!mbar_wait(smem_u32(&sm.bar_dq_full), u & 1) || sm.abort) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      {
+        const int qi = q0 + j;  // TMEM lane j of dQ_u is query row j
+        float* dst = prm.dq_acc + (static_cast<size_t>(qi) * H + h) * DIM;
+#pragma unroll 1
+        for (int c = 0; c < DIM / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_off + kColSP + 32 * c, v);
+          tmem_ld_wait();
+          if (qi < e) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4)
+              red_add_v4(dst + 32 * c + i, __uint_as_float(v[i]) * prm.sm_scale,
+                         __uint_as_float(v[i + 1]) * prm.sm_scale,
+                         __uint_as_float(v[i + 2]) * prm.sm_scale,
+                         __uint_as_float(v[i + 3]) * prm.sm_scale);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.bar_s_free));
+    }
+    if (ok) {
+      // dV = 2^-8 acc, dK = scale * acc, written to the packed buffers
+      __nv_bfloat16* dvrow = prm.dv + (static_cast<size_t>(kj) * H + h) * DIM;
+      __nv_bfloat16* dkrow = prm.dk + (static_cast<size_t>(kj) * H + h) * DIM;
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
+        const float mul = which == 0 ? (1.f / 256.f) : prm.sm_scale;
+        __nv_bfloat16* row = which == 0 ? dvrow : dkrow;
+#pragma unroll 1
+        for (int c = 0; c < DIM / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_off + kColDV + which * DIM + 32 * c, v);
+          tmem_ld_wait();
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * i]) * mul,
+                                                      __uint_as_float(v[2 * i + 1]) * mul);
+            w[i] = *reinterpret_cast<uint32_t*>(&b2);
+          }
+          if (key_valid) {
+            uint4* dst = reinterpret_cast<uint4*>(row + 32 * c);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
+            dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+          }
+        }
+      }
+    }
+    if (!ok) sm.abort = 1;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (sm.abort && threadIdx.x == 0) report(prm.status, FLAMIA_DEV_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// float32 dQ accumulator -> BF16 output.
+__global__ void dq_convert_kernel(const float4* __restrict__ acc, uint2* __restrict__ out,
+                                  size_t n4) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const float4 a = acc[i];
+    __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y), hi = __floats2bfloat162_rn(a.z, a.w);
+    out[i] = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+  }
+}
+
+template <int DIM>
+flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
+                         const flamia_qtensor* v, const flamia_qtensor* dout, const float* D,
+                         const float* lse, const int32_t* cu, int ndocs, int T, int H,
+                         float softmax_scale, const void* wl, void* dq, void* dk, void* dv,
+                         float* acc, int* status, cudaStream_t stream) {
+  CUtensorMap mq, mk, mv, mdo;
+  const CUtensorMapSwizzle swz = swizzle_for_row_bytes(DIM);
+  if (!make_token_map(&mq, q->codes, T, H, DIM, kTile, swz) ||
+      !make_token_map(&mk, k->codes, T, H, DIM, kTile, swz) ||
+      !make_token_map(&mv, v->codes, T, H, DIM, kTile, swz) ||
+      !make_token_map(&mdo, dout->codes, T, H, DIM, kTile, swz))
+    return FLAMIA_ERR_CUDA;
+  const WorklistLayout L = worklist_layout(T, ndocs);
+  BwdParams prm;
+  prm.q_scales = q->scales;
+  prm.k_scales = k->scales;
+  prm.v_scales = v->scales;
+  prm.do_scales = dout->scales;
+  prm.D = D;
+  prm.lse = lse;
+  prm.cu = cu;
+  prm.wl_header = static_cast<const int*>(wl);
+  prm.items = reinterpret_cast<const int4*>(static_cast<const char*>(wl) + L.off_bwd);
+  prm.dq_acc = acc;
+  prm.dk = static_cast<__nv_bfloat16*>(dk);
+  prm.dv = static_cast<__nv_bfloat16*>(dv);
+  prm.T = T;
+  prm.H = H;
+  prm.ndocs = ndocs;
+  prm.scale_log2 = softmax_scale * 1.4426950408889634f;
+  prm.sm_scale = softmax_scale;
+  prm.status = status;
+  const size_t n = static_cast<size_t>(T) * H * DIM;
+  if (cudaMemsetAsync(acc, 0, n * sizeof(float), stream) != cudaSuccess) return FLAMIA_ERR_CUDA;
+  const size_t smem = sizeof(BwdSmem<DIM>) + 1024;
+  if (cudaFuncSetAttribute(attn_bwd_kernel<DIM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return FLAMIA_ERR_CUDA;
+  const long long grid = static_cast<long long>(L.cap_bwd) * H;
+  attn_bwd_kernel<DIM>
+      <<<static_cast<unsigned>(grid), kBwdThreads, smem, stream>>>(mq, mk, mv, mdo, prm);
+  if (cudaGetLastError() != cudaSuccess) return FLAMIA_ERR_CUDA;
+  const size_t n4 = n / 4;
+  const int blocks = static_cast<int>(std::min<size_t>((n4 + 255) / 256, 152 * 16));
+  dq_convert_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(acc),
+                                                static_cast<uint2*>(dq), n4);
+  return cudaGetLastError() == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace flamia
+
+using namespace flamia;
+
+extern "C" size_t flamia_bwd_workspace_bytes(int T, int H, int d) {
+  if (T <= 0 || H <= 0 || !supported_dim(d)) return 0;
+  return align_up(static_cast<size_t>(T) * H * d * sizeof(float), 256);
+}
+
+extern "C" flamia_status flamia_attn_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
+                                         const flamia_qtensor* v, const flamia_qtensor* dout,
+                                         const float* D, const float* lse,
+                                         const int32_t* cu_seqlens, int ndocs, int T, int H,
+                                         int d, float softmax_scale, int flags, const void* wl,
+                                         void* dq_bf16, void* dk_bf16, void* dv_bf16, void* ws,
+                                         size_t ws_bytes, int* dev_status, void* stream) {
+  if (!supported_dim(d)) return FLAMIA_ERR_UNSUPPORTED;
+  if (flags != 0) return FLAMIA_ERR_UNSUPPORTED;
+  if (!valid_sizes(T, H, d, ndocs) || !q || !k || !v || !dout || !D || !lse || !cu_seqlens ||
+      !wl || !dq_bf16 || !dk_bf16 || !dv_bf16 || !ws || !(softmax_scale > 0.f))
+    return FLAMIA_ERR_INVALID_ARG;
+  if (!q->codes || !q->scales || !k->codes || !k->scales || !v->codes || !v->scales ||
+      !dout->codes || !dout->scales)
+    return FLAMIA_ERR_INVALID_ARG;
+  if (!aligned(q->codes, 16) || !aligned(k->codes, 16) || !aligned(v->codes, 16) ||
+      !aligned(dout->codes, 16) || !aligned(dq_bf16, 16) || !aligned(dk_bf16, 16) ||
+      !aligned(dv_bf16, 16) || !aligned(ws, 256) || !aligned(wl, 256))
+    return FLAMIA_ERR_INVALID_ARG;
+  if (ws_bytes < flamia_bwd_workspace_bytes(T, H, d)) return FLAMIA_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* acc = static_cast<float*>(ws);
+  return d == 128 ? launch_bwd<128>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H,
+                                    softmax_scale, wl, dq_bf16, dk_bf16, dv_bf16, acc, dev_status,
+                                    s)
+                  : launch_bwd<64>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, softmax_scale,
+                                   wl, dq_bf16, dk_bf16, dv_bf16, acc, dev_status, s);
+}

@@ -1,0 +1,423 @@
+// Causal forward over token-block MXFP8 operands (FLAMIA review page, sec.
+// 1.2, 3.1, 3.4).
+//
+// One CTA = one work item (256 queries of one document = two 128-query
+// tiles) x one head.  Warp roles:
+//   warp 0      TMA producer: Q tiles once, then K/V tiles through a ring.
+//   warp 1      tensor-memory owner and single-thread tcgen05 MMA issuer.
+//   warps 4-7   softmax of query tile 0   (thread = query row = TMEM lane)
+//   warps 8-11  softmax of query tile 1
+// Per key tile j the MMA warp issues S_t = Q_t K_j^T (unscaled E4M3, f32 in
+// TMEM) and, once the softmax group has written the E4M3 probability tile
+// P^_t to shared memory, O_t += P^_t V_j as a block-scaled MMA whose B scale
+// is the per-32-key E8M0 scale of V.  The two query tiles ping-pong so the
+// tensor core works on one while the other tile's softmax runs.
+//
+// Tensor memory (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+d),
+// O_1 [256+d, 256+2d).  The scale factors of P^_t V_j are written into the
+// first 8 columns of S_t after the softmax has read S_t; the next S_t MMA is
+// issued after P^_t V_j, and tcgen05 MMAs of one thread execute in order.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace flamia {
+namespace {
+
+constexpr int kStages = 3;
+constexpr int kFwdThreads = 384;
+constexpr float kLn2 = 0.69314718055994530942f;
+
+template <int DIM>
+struct FwdSmem {
+  static constexpr int kTileBytes = kTile * DIM;
+  alignas(1024) uint8_t q[2][kTileBytes];
+  alignas(1024) uint8_t k[kStages][kTileBytes];
+  alignas(1024) uint8_t v[kStages][kTileBytes];
+  alignas(1024) uint8_t p[2][kTile * kTile];
+  uint64_t bar_q;
+  uint64_t bar_kv_full[kStages];
+  uint64_t bar_kv_empty[kStages];
+  uint64_t bar_s_full[2];
+  uint64_t bar_p_full[2];
+  uint64_t bar_o_full[2];
+  uint64_t bar_done;
+  uint32_t tmem_base;
+  volatile int abort;
+};
+
+struct FwdParams {
+  const uint8_t* q_scales;
+  const uint8_t* k_scales;
+  const uint8_t* v_scales;
+  const int32_t* cu;
+  const int* wl_header;
+  const int4* items;
+  __nv_bfloat16* o;
+  float* lse;
+  int T, H, ndocs;
+  float scale_log2;  // softmax_scale * log2(e)
+  int* status;
+};
+
+template <int DIM>
+__host__ __device__ constexpr uint32_t operand_layout() {
+  return DIM == 128 ? kLayoutSW128 : kLayoutSW64;
+}
+
+__device__ __forceinline__ float pow2_or_zero(int k) {
+  return k < -126 ? 0.f : exp2i(k);
+}
+
+template <int DIM>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
+                    const __grid_constant__ CUtensorMap map_k,
+                    const __grid_constant__ CUtensorMap map_v, const FwdParams prm) {
+  extern __shared__ uint8_t smem_raw[];
+  FwdSmem<DIM>& sm = *reinterpret_cast<FwdSmem<DIM>*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
+  const int H = prm.H, T = prm.T;
+  const int item_idx = blockIdx.x / H;
+  const int h = blockIdx.x % H;
+  if (item_idx >= prm.wl_header[kHdrNFwd]) return;  // uniform over the CTA
+  const int4 item = prm.items[item_idx];
+  // clamped: a malformed work list or offsets cannot index outside [0, T)
+  const int doc = min(max(item.x, 0), prm.ndocs - 1);
+  const int s = min(max(prm.cu[doc], 0), T);
+  const int e = min(max(prm.cu[doc + 1], s), T);
+  const int q0 = s + ((min(max(item.y, s), e) - s) & ~(kTile - 1));
+  const int q1 = min(max(item.z, q0), e);
+  const bool valid1 = q1 > q0 + kTile;
+  const int n0 = (q0 - s) / kTile + 1;           // key tiles of query tile 0
+  const int n1 = valid1 ? n0 + 1 : 0;            // key tiles of query tile 1
+  const int nkv = valid1 ? n1 : n0;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&sm.bar_q), 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(smem_u32(&sm.bar_kv_full[i]), 1);
+      mbar_init(smem_u32(&sm.bar_kv_empty[i]), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(smem_u32(&sm.bar_s_full[t]), 1);
+      mbar_init(smem_u32(&sm.bar_p_full[t]), kTile);
+      mbar_init(smem_u32(&sm.bar_o_full[t]), 1);
+    }
+    mbar_init(smem_u32(&sm.bar_done), 1);
+    sm.abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sm.tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  constexpr uint32_t kTileBytes = FwdSmem<DIM>::kTileBytes;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tensormap(&map_q);
+      prefetch_tensormap(&map_k);
+      prefetch_tensormap(&map_v);
+      const uint32_t bq = smem_u32(&sm.bar_q);
+      mbar_arrive_expect_tx(bq, (valid1 ? 2 : 1) * kTileBytes);
+      tma_load_3d(smem_u32(sm.q[0]), &map_q, bq, 0, h, q0);
+      if (valid1) tma_load_3d(smem_u32(sm.q[1]), &map_q, bq, 0, h, q0 + kTile);
+      int issued = 0;
+      for (int j = 0; j < nkv; ++j) {
+        const int st = j % kStages;
+        if (j >= kStages) {
+          if (!mbar_wait(smem_u32(&sm.bar_kv_empty[st]), ((j / kStages) - 1) & 1) ||
+              sm.abort) {
+            sm.abort = 1;
+            break;
+          }
+        }
+        const uint32_t bf = smem_u32(&sm.bar_kv_full[st]);
+        mbar_arrive_expect_tx(bf, 2 * kTileBytes);
+        tma_load_3d(smem_u32(sm.k[st]), &map_k, bf, 0, h, s + j * kTile);
+        tma_load_3d(smem_u32(sm.v[st]), &map_v, bf, 0, h, s + j * kTile);
+        issued = j + 1;
+      }
+      // Drain: every issued copy has landed before the CTA can exit.
+      bool ok = mbar_wait(bq, 0);
+      for (int j = max(0, issued - kStages); j < issued; ++j)
+        ok &= mbar_wait(smem_u32(&sm.bar_kv_full[j % kStages]), (j / kStages) & 1);
+      if (!ok) sm.abort = 1;
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t lay = operand_layout<DIM>();
+      constexpr uint32_t sbo = 8 * DIM;  // 8 rows of one swizzle atom
+      const uint32_t id_qk = idesc_f8(kTile, kTile, 0, 0);
+      bool ok = mbar_wait(smem_u32(&sm.bar_q), 0) && mbar_wait(smem_u32(&sm.bar_kv_full[0]), 0);
+      tc_fence_after();
+      auto issue_qk = [&](int t, int st) {
+        const uint32_t qa = smem_u32(sm.q[t]), ka = smem_u32(sm.k[st]);
+#pragma unroll
+        for (int ks = 0; ks < DIM / 32; ++ks)
+          mma_f8(tmem + t * kTile, smem_desc(qa + 32 * ks, 0, sbo, lay),
+                 smem_desc(ka + 32 * ks, 0, sbo, lay), id_qk, ks > 0);
+        tc_commit(smem_u32(&sm.bar_s_full[t]));
+      };
+      if (ok) {
+        issue_qk(0, 0);
+        if (valid1) issue_qk(1, 0);
+      }
+      int kv_ready = 1;  // stages known full: tiles [0, kv_ready)
+      for (int j = 0; ok && j < nkv; ++j) {
+        const int st = j % kStages;
+        for (int t = 0; t < 2 && ok; ++t) {
+          const int nt = t == 0 ? n0 : n1;
+          if (j >= nt) continue;
+          if (!mbar_wait(smem_u32(&sm.bar_p_full[t]), j & 1) || sm.abort) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t pa = smem_u32(sm.p[t]), va = smem_u32(sm.v[st]);
+          const uint32_t sf = tmem + t * kTile;  // scale factors live in S_t columns 0..7
+#pragma unroll
+          for (int kb = 0; kb < 4; ++kb)
+            mma_mxf8(tmem + 256 + t * DIM, smem_desc(pa + 32 * kb, 0, 1024, kLayoutSW128),
+                     smem_desc(va + kb * 32 * DIM, 0, sbo, lay),
+                     idesc_mxf8(kTile, DIM, 0, 1, kb, kb), sf, sf + 4, (j > 0 || kb > 0));
+          if (j + 1 < nt) {
+            if (kv_ready <= j + 1) {
+              if (!mbar_wait(smem_u32(&sm.bar_kv_full[(j + 1) % kStages]),
+                             ((j + 1) / kStages) & 1)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              kv_ready = j + 2;
+            }
+            issue_qk(t, (j + 1) % kStages);
+          } else {
+            tc_commit(smem_u32(&sm.bar_o_full[t]));
+          }
+        }
+        if (ok) tc_commit(smem_u32(&sm.bar_kv_empty[st]));
+      }
+      if (!ok) sm.abort = 1;
+      // Drain: all MMAs of this thread complete before tensor memory is freed.
+      tc_commit(smem_u32(&sm.bar_done));
+      if (!mbar_wait(smem_u32(&sm.bar_done), 0)) sm.abort = 1;
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int t = (warp - 4) >> 2;
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const int nt = t == 0 ? n0 : n1;
+    const int qa = q0 + t * kTile;
+    const int qi = qa + r;
+    const bool row_valid = qi < q1;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t tS = tmem + lane_off + t * kTile;
+    const uint32_t tO = tmem + lane_off + 256 + t * DIM;
+    const size_t hT = static_cast<size_t>(h) * T;
+    const int eq = static_cast<int>(prm.q_scales[hT + min(qi, T - 1)]) - 127;
+    const float c_row = prm.scale_log2 * pow2_or_zero(eq);
+    float m = -INFINITY, l8 = 0.f;
+    uint8_t* prow = sm.p[t] + r * kTile;
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      if (!mbar_wait(smem_u32(&sm.bar_s_full[t]), j & 1) || sm.abort) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int k0 = s + j * kTile;
+      float cf[4];
+      uint32_t sfb = 0;
+#pragma unroll
+      for (int kb = 0; kb < 4; ++kb) {
+        const int kk = k0 + 32 * kb;
+        const int ekb = kk < e ? static_cast<int>(prm.k_scales[hT + kk]) - 127 : 0;
+        cf[kb] = c_row * pow2_or_zero(ekb);
+        const uint32_t vb = kk < e ? prm.v_scales[hT + kk] : 127u;
+        sfb |= vb << (8 * kb);
+      }
+      const bool diag = (j == nt - 1);
+      const int lim = diag ? min(r, e - 1 - k0) : kTile - 1;  // last visible column
+      // pass 1: row maximum in the log2 domain
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tS + 32 * c, v);
+        tmem_ld_wait();
+        float cm = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float x = __uint_as_float(v[i]);
+          cm = (32 * c + i <= lim) ? fmaxf(cm, x) : cm;
+        }
+        mx = fmaxf(mx, cm * cf[c]);
+      }
+      float m_new = (mx == -INFINITY) ? m : fmaxf(m, ceilf(mx));
+      if (m_new == -INFINITY) m_new = 0.f;
+      const bool need = (j > 0) && (m_new > m);
+      const float corr = need ? pow2_or_zero(static_cast<int>(m - m_new)) : 1.f;
+      l8 *= corr;
+      if (__any_sync(0xffffffffu, need)) {
+        // rescale this warp's O rows by the (exact power-of-two) correction
+#pragma unroll
+        for (int c = 0; c < DIM / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tO + 32 * c, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * corr);
+          tmem_st32(tO + 32 * c, v);
+        }
+        tmem_st_wait();
+      }
+      m = m_new;
+      const float moff = m - 8.f;  // P8 = 2^8 exp2(s - m)
+      // pass 2: probabilities, row sum, E4M3 operand
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tS + 32 * c, v);
+        tmem_ld_wait();
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          float p4[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float x = (32 * c + i + u <= lim) ? __uint_as_float(v[i + u]) : -INFINITY;
+            p4[u] = ex2_approx(fmaf(x, cf[c], -moff));
+            l8 += p4[u];
+          }
+          w[i / 4] = cvt_e4m3x2(p4[0], p4[1]) | (cvt_e4m3x2(p4[2], p4[3]) << 16);
+        }
+        // 32 bytes = 16-byte chunks 2c and 2c+1 of row r, 128B-swizzled
+        const int ch0 = (2 * c) ^ (r & 7), ch1 = (2 * c + 1) ^ (r & 7);
+        *reinterpret_cast<uint4*>(prow + 16 * ch0) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(prow + 16 * ch1) = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+      // scale factors of P^_t V_j: A (P^) 2^0 for every K block, B = V's block bytes
+      const uint32_t sfw[8] = {0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu,
+                               sfb, sfb, sfb, sfb};
+      tmem_st8(tS, sfw);
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.bar_p_full[t]));
+    }
+    if (nt > 0 && ok) {
+      if (!mbar_wait(smem_u32(&sm.bar_o_full[t]), 0) || sm.abort) ok = false;
+    }
+    if (nt > 0 && ok) {
+      tc_fence_after();
+      const float inv = 1.f / l8;
+      __nv_bfloat16* orow = prm.o + (static_cast<size_t>(qi) * H + h) * DIM;
+#pragma unroll
+      for (int c = 0; c < DIM / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tO + 32 * c, v);
+        tmem_ld_wait();
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * i]) * inv,
+                                                    __uint_as_float(v[2 * i + 1]) * inv);
+          w[i] = *reinterpret_cast<uint32_t*>(&b2);
+        }
+        if (row_valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
+          dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+        }
+      }
+      if (row_valid) prm.lse[hT + qi] = (m - 8.f + __log2f(l8)) * kLn2;
+    }
+    if (!ok) sm.abort = 1;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (sm.abort && threadIdx.x == 0) report(prm.status, FLAMIA_DEV_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int DIM>
+flamia_status launch_fwd(const flamia_qtensor* q, const flamia_qtensor* k,
+                         const flamia_qtensor* v, const int32_t* cu, int ndocs, int T, int H,
+                         float softmax_scale, const void* wl, void* o, float* lse, int* status,
+                         cudaStream_t stream) {
+  CUtensorMap mq, mk, mv;
+  const CUtensorMapSwizzle swz = swizzle_for_row_bytes(DIM);
+  if (!make_token_map(&mq, q->codes, T, H, DIM, kTile, swz) ||
+      !make_token_map(&mk, k->codes, T, H, DIM, kTile, swz) ||
+      !make_token_map(&mv, v->codes, T, H, DIM, kTile, swz))
+    return FLAMIA_ERR_CUDA;
+  const WorklistLayout L = worklist_layout(T, ndocs);
+  FwdParams prm;
+  prm.q_scales = q->scales;
+  prm.k_scales = k->scales;
+  prm.v_scales = v->scales;
+  prm.cu = cu;
+  prm.wl_header = static_cast<const int*>(wl);
+  prm.items = reinterpret_cast<const int4*>(static_cast<const char*>(wl) + L.off_fwd);
+  prm.o = static_cast<__nv_bfloat16*>(o);
+  prm.lse = lse;
+  prm.T = T;
+  prm.H = H;
+  prm.ndocs = ndocs;
+  prm.scale_log2 = softmax_scale * 1.4426950408889634f;
+  prm.status = status;
+  const size_t smem = sizeof(FwdSmem<DIM>) + 1024;
+  if (cudaFuncSetAttribute(attn_fwd_kernel<DIM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return FLAMIA_ERR_CUDA;
+  const long long grid = static_cast<long long>(L.cap_fwd) * H;
+  attn_fwd_kernel<DIM><<<static_cast<unsigned>(grid), kFwdThreads, smem, stream>>>(mq, mk, mv, prm);
+  return cudaGetLastError() == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace flamia
+
+using namespace flamia;
+
+extern "C" flamia_status flamia_attn_fwd(const flamia_qtensor* q, const flamia_qtensor* k,
+                                         const flamia_qtensor* v, const int32_t* cu_seqlens,
+                                         int ndocs, int T, int H, int d, float softmax_scale,
+                                         int flags, const void* wl, void* o_bf16, float* lse,
+                                         int* dev_status, void* stream) {
+  if (!supported_dim(d)) return FLAMIA_ERR_UNSUPPORTED;
+  if (flags != 0) return FLAMIA_ERR_UNSUPPORTED;
+  if (!valid_sizes(T, H, d, ndocs) || q == nullptr || k == nullptr || v == nullptr ||
+      cu_seqlens == nullptr || wl == nullptr || o_bf16 == nullptr || lse == nullptr ||
+      !(softmax_scale > 0.f))
+    return FLAMIA_ERR_INVALID_ARG;
+  if (!q->codes || !q->scales || !k->codes || !k->scales || !v->codes || !v->scales)
+    return FLAMIA_ERR_INVALID_ARG;
+  if (!aligned(q->codes, 16) || !aligned(k->codes, 16) || !aligned(v->codes, 16) ||
+      !aligned(o_bf16, 16) || !aligned(wl, 256))
+    return FLAMIA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return d == 128 ? launch_fwd<128>(q, k, v, cu_seqlens, ndocs, T, H, softmax_scale, wl, o_bf16,
+                                    lse, dev_status, s)
+                  : launch_fwd<64>(q, k, v, cu_seqlens, ndocs, T, H, softmax_scale, wl, o_bf16,
+                                   lse, dev_status, s);
+}

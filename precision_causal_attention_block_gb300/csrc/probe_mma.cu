@@ -1,0 +1,177 @@
+// Single-tile tensor-core product used by the tests to check operand
+// descriptors and scale-factor placement (declared in flamia_debug.h).
+#include "../../include/flamia_debug.h"
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace flamia {
+namespace {
+
+struct ProbeSmem {
+  alignas(1024) uint8_t a[128 * 128];
+  alignas(1024) uint8_t b[128 * 128];
+  uint64_t bar_load, bar_mma;
+  uint32_t tmem_base;
+};
+
+struct ProbeArgs {
+  int mode, N, a_mn, b_mn, variant;
+  int a_bytes, b_bytes;
+  uint32_t a_rowb, b_rowb;  // bytes per shared-memory row of each operand
+  const uint8_t* sfa;
+  const uint8_t* sfb;
+  float* d;
+  int* status;
+};
+
+__device__ __forceinline__ uint32_t layout_for(uint32_t rowb) {
+  return rowb == 128 ? kLayoutSW128 : rowb == 64 ? kLayoutSW64 : kLayoutSW32;
+}
+
+__global__ void __launch_bounds__(128, 1)
+    probe_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                 const ProbeArgs g) {
+  extern __shared__ uint8_t smem_raw[];
+  ProbeSmem& sm = *reinterpret_cast<ProbeSmem*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&sm.bar_load), 1);
+    mbar_init(smem_u32(&sm.bar_mma), 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&sm.tmem_base), 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  bool ok = true;
+  if (threadIdx.x == 0) {
+    const uint32_t bl = smem_u32(&sm.bar_load);
+    mbar_arrive_expect_tx(bl, g.a_bytes + g.b_bytes);
+    tma_load_2d(smem_u32(sm.a), &map_a, bl, 0, 0);
+    tma_load_2d(smem_u32(sm.b), &map_b, bl, 0, 0);
+  }
+  // scale factors into tensor memory (columns 128.. for A, 132.. for B)
+  if (g.mode != 0) {
+    const int variant = (g.variant >> 1) & 3;
+    uint32_t w[8];
+    for (int c = 0; c < 4; ++c) {
+      int ma, nb;
+      if (variant == 0) {
+        ma = 32 * c + lane;
+        nb = 32 * c + lane;
+      } else {
+        ma = 32 * warp + lane;
+        nb = 32 * warp + lane;
+      }
+      uint32_t wa = 0, wb = 0;
+      for (int kb = 0; kb < 4; ++kb) {
+        wa |= static_cast<uint32_t>(g.sfa[ma * 4 + kb]) << (8 * kb);
+        const uint32_t bb = nb < g.N ? g.sfb[nb * 4 + kb] : (g.mode == 1 ? 127u : 0x38u);
+        wb |= bb << (8 * kb);
+      }
+      w[c] = wa;
+      w[4 + c] = wb;
+    }
+    tmem_st8(tmem + (static_cast<uint32_t>(warp * 32) << 16) + 128, w);
+    tmem_st_wait();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    ok = mbar_wait(smem_u32(&sm.bar_load), 0);
+    tc_fence_after();
+    if (ok) {
+      const uint32_t aa = smem_u32(sm.a), ba = smem_u32(sm.b);
+      const bool swap = g.variant & 1;
+      auto kdesc = [&](uint32_t base, uint32_t rowb, int ks) {  // K-major, ks-th 32-byte slice
+        return smem_desc(base + 32 * ks, 0, 8 * rowb, layout_for(rowb));
+      };
+      auto mdesc = [&](uint32_t base, uint32_t rowb, int ks) {  // MN-major, ks-th 32-row slice
+        const uint32_t off = 8 * rowb;
+        return smem_desc(base + ks * 32 * rowb, swap ? off : 0, swap ? 0 : off, layout_for(rowb));
+      };
+      if (g.mode == 0 || g.mode == 1) {
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t ad = g.a_mn ? mdesc(aa, g.a_rowb, ks) : kdesc(aa, g.a_rowb, ks);
+          const uint64_t bd = g.b_mn ? mdesc(ba, g.b_rowb, ks) : kdesc(ba, g.b_rowb, ks);
+          if (g.mode == 0)
+            mma_f8(tmem, ad, bd, idesc_f8(128, g.N, g.a_mn, g.b_mn), ks > 0);
+          else
+            mma_mxf8(tmem, ad, bd, idesc_mxf8(128, g.N, g.a_mn, g.b_mn, ks, ks), tmem + 128,
+                     tmem + 132, ks > 0);
+        }
+      } else {
+        mma_nvf4(tmem, smem_desc(aa, 0, 8 * g.a_rowb, layout_for(g.a_rowb)),
+                 smem_desc(ba, 0, 8 * g.b_rowb, layout_for(g.b_rowb)), idesc_nvf4(128, g.N),
+                 tmem + 128, tmem + 132, 0);
+      }
+    }
+    tc_commit(smem_u32(&sm.bar_mma));
+    if (!mbar_wait(smem_u32(&sm.bar_mma), 0)) ok = false;
+    if (!ok) report(g.status, FLAMIA_DEV_TIMEOUT);
+  }
+  __syncthreads();
+  tc_fence_after();
+  const int row = warp * 32 + lane;
+  for (int c = 0; c < g.N / 32; ++c) {
+    uint32_t v[32];
+    tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + 32 * c, v);
+    tmem_ld_wait();
+    for (int i = 0; i < 32; ++i) g.d[row * g.N + 32 * c + i] = __uint_as_float(v[i]);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+}  // namespace
+}  // namespace flamia
+
+using namespace flamia;
+
+extern "C" flamia_status flamia_debug_mma_tile(int mode, int N, int a_mn_major, int b_mn_major,
+                                               int variant, const uint8_t* a, const uint8_t* b,
+                                               const uint8_t* sfa, const uint8_t* sfb,
+                                               float* d_out, int* dev_status, void* stream) {
+  if (mode < 0 || mode > 2 || (N != 64 && N != 128) || variant < 0 || variant > 3)
+    return FLAMIA_ERR_UNSUPPORTED;
+  if (!a || !b || !d_out || (mode != 0 && (!sfa || !sfb))) return FLAMIA_ERR_INVALID_ARG;
+  if (mode == 2 && (a_mn_major || b_mn_major)) return FLAMIA_ERR_UNSUPPORTED;
+  if (!aligned(a, 16) || !aligned(b, 16)) return FLAMIA_ERR_INVALID_ARG;
+  const int kbytes = mode == 2 ? 32 : 128;  // K = 128 E4M3 or 64 packed E2M1
+  ProbeArgs g;
+  g.mode = mode;
+  g.N = N;
+  g.a_mn = a_mn_major;
+  g.b_mn = b_mn_major;
+  g.variant = variant;
+  int a_rows, b_rows;
+  if (a_mn_major) { a_rows = 128; g.a_rowb = 128; }   // [K][M]
+  else { a_rows = 128; g.a_rowb = kbytes; }            // [M][K]
+  if (b_mn_major) { b_rows = 128; g.b_rowb = N; }      // [K][N]
+  else { b_rows = N; g.b_rowb = kbytes; }              // [N][K]
+  g.a_bytes = a_rows * g.a_rowb;
+  g.b_bytes = b_rows * g.b_rowb;
+  g.sfa = sfa;
+  g.sfb = sfb;
+  g.d = d_out;
+  g.status = dev_status;
+  CUtensorMap ma, mb;
+  if (!make_matrix_map(&ma, a, a_rows, g.a_rowb, a_rows, swizzle_for_row_bytes(g.a_rowb)) ||
+      !make_matrix_map(&mb, b, b_rows, g.b_rowb, b_rows, swizzle_for_row_bytes(g.b_rowb)))
+    return FLAMIA_ERR_CUDA;
+  const size_t smem = sizeof(ProbeSmem) + 1024;
+  if (cudaFuncSetAttribute(probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return FLAMIA_ERR_CUDA;
+  probe_kernel<<<1, 128, smem, static_cast<cudaStream_t>(stream)>>>(ma, mb, g);
+  return cudaGetLastError() == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
+}

@@ -1,0 +1,215 @@
+// Fused token-block quantiser (FLAMIA review page, sec. 3.1, 3.2 and 3.4
+// "Quantization fusion" / "Packed documents").
+//
+// One CTA owns the 32-token blocks whose first token lies in a 128-token
+// segment of one head.  The rows of those blocks (at most 128 + 31) are read
+// once from HBM into registers, reduced to per-block maxima through shared
+// memory, and written back as E4M3 codes plus the per-token E8M0 scale table,
+// optionally with the NVFP4 copy and with D = dO . O fused in.
+// HBM-bound: 2 bytes read + 1 byte written per element.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace flamia {
+namespace {
+
+constexpr int kSeg = 128;             // tokens per CTA segment
+constexpr int kQThreads = kSeg + 32;  // one thread per token of [seg0, seg0 + 160)
+
+__device__ __forceinline__ int doc_of(const int32_t* __restrict__ cu, int ndocs, int t) {
+  int lo = 0, hi = ndocs;  // cu[lo] <= t < cu[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(cu + mid) <= t) lo = mid;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// 2^e as a float for e in [-127, 127] (2^-127 is a subnormal).
+__device__ __forceinline__ float pow2f(int e) {
+  return e >= -126 ? exp2i(e) : exp2i(-126) * 0.5f;
+}
+
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+template <int DIM>
+__global__ void __launch_bounds__(kQThreads, 2)
+    quantize_kernel(const uint4* __restrict__ x, int T, int H, const int32_t* __restrict__ cu,
+                    int ndocs, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                    uint8_t* __restrict__ f4codes, uint8_t* __restrict__ f4scales,
+                    const uint4* __restrict__ o, float* __restrict__ D, int* dev_status) {
+  constexpr int LPR = DIM / 8;    // lanes per row: 16 bytes (8 BF16) per lane
+  constexpr int RPI = 32 / LPR;   // rows per warp-wide load
+  constexpr int NLD = 32 / RPI;   // loads per 32 rows
+  __shared__ float s_rmax[kQThreads];
+  __shared__ int s_exp[kQThreads];
+  __shared__ int s_bounds[2];
+
+  const int seg0 = blockIdx.x * kSeg;
+  const int h = blockIdx.y;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+
+  // Light validation of cu_seqlens, spread over the CTAs of head 0.
+  if (h == 0) {
+    for (int i = blockIdx.x * kQThreads + tid; i < ndocs; i += gridDim.x * kQThreads)
+      if (__ldg(cu + i) > __ldg(cu + i + 1)) report(dev_status, FLAMIA_DEV_BAD_SEQLENS);
+    if (blockIdx.x == 0 && tid == 0 && (__ldg(cu) != 0 || __ldg(cu + ndocs) != T))
+      report(dev_status, FLAMIA_DEV_BAD_SEQLENS);
+  }
+
+  // Block of this thread's token.
+  const int t = seg0 + tid;
+  int bs = 0, be = 0;
+  if (t < T) {
+    const int b = doc_of(cu, ndocs, t);
+    // clamped so that malformed offsets (flagged above) cannot move any
+    // index outside [t - 31, t + 31] and [0, T)
+    const int s = min(max(__ldg(cu + b), 0), t);
+    const int e = max(min(__ldg(cu + b + 1), T), t + 1);
+    bs = s + ((t - s) & ~(kBlock - 1));
+    be = min(bs + kBlock, e);
+  }
+  // This CTA owns the rows [A, Bend): blocks starting inside [seg0, seg0 + kSeg).
+  if (tid == 0) s_bounds[0] = (bs == seg0) ? seg0 : be;
+  if (tid == min(kSeg, T - seg0) - 1) s_bounds[1] = be;
+  __syncthreads();
+  const int A = s_bounds[0], Bend = s_bounds[1];
+
+  // Phase 1: load the rows of this warp's 32 tokens, per-row maximum.
+  uint4 xr[NLD];
+  const int chunk = lane % LPR;
+#pragma unroll
+  for (int i = 0; i < NLD; ++i) {
+    const int tt = seg0 + warp * 32 + i * RPI + lane / LPR;
+    const bool valid = tt >= A && tt < Bend;
+    xr[i] = valid ? __ldg(x + (static_cast<size_t>(tt) * H + h) * LPR + chunk)
+                  : make_uint4(0, 0, 0, 0);
+    const uint32_t w[4] = {xr[i].x, xr[i].y, xr[i].z, xr[i].w};
+    float m = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16lo(w[j])), fabsf(bf16hi(w[j]))));
+#pragma unroll
+    for (int off = LPR / 2; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if (chunk == 0 && valid) s_rmax[tt - seg0] = m;
+  }
+  __syncthreads();
+
+  // Phase 2: block maximum -> round-up exponent -> dense per-token scale byte.
+  if (t >= A && t < Bend) {
+    float amax = 0.f;
+    for (int r = max(bs, A); r < min(be, Bend); ++r) amax = fmaxf(amax, s_rmax[r - seg0]);
+    const int e = roundup_exponent(amax);
+    s_exp[tid] = e;
+    scales[static_cast<size_t>(h) * T + t] = static_cast<uint8_t>(e + 127);
+  }
+  __syncthreads();
+
+  // Phase 3: codes (+ NVFP4 copy, + D) from the registers.
+#pragma unroll
+  for (int i = 0; i < NLD; ++i) {
+    const int tt = seg0 + warp * 32 + i * RPI + lane / LPR;
+    const bool valid = tt >= A && tt < Bend;
+    const int e = valid ? s_exp[tt - seg0] : 0;
+    const float inv = exp2i(-e);  // e in [-127, 120]: 2^-e is a normal float
+    const uint32_t w[4] = {xr[i].x, xr[i].y, xr[i].z, xr[i].w};
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[2 * j] = bf16lo(w[j]);
+      v[2 * j + 1] = bf16hi(w[j]);
+    }
+    uint32_t c[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) c[j] = cvt_e4m3x2(v[2 * j] * inv, v[2 * j + 1] * inv);
+    const size_t row = static_cast<size_t>(tt) * H + h;
+    if (valid) {
+      uint2 packed = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+      reinterpret_cast<uint2*>(codes + row * DIM)[chunk] = packed;
+    }
+    if (f4codes != nullptr) {
+      // NVFP4: one E4M3 scale per 16 elements = two neighbouring lanes.
+      float m = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(v[j]));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+      const float q = __fdiv_rn(m, 6.0f);
+      uint32_t sc = cvt_e4m3x2(q, 0.f) & 0xFFu;          // nearest E4M3 (saturating)
+      const float sv = e4m3x2_to_float2(sc).x;
+      if (sv < q && sc < 0x7Eu) sc += 1;                  // round up to >= amax / 6
+      const float s = e4m3x2_to_float2(sc).x;
+      uint32_t f4 = 0;
+      if (s > 0.f) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          f4 |= cvt_e2m1x2(__fdiv_rn(v[2 * j], s), __fdiv_rn(v[2 * j + 1], s)) << (8 * j);
+      }
+      if (valid) {
+        reinterpret_cast<uint32_t*>(f4codes + row * (DIM / 2))[chunk] = f4;
+        if ((chunk & 1) == 0) f4scales[row * (DIM / 16) + chunk / 2] = static_cast<uint8_t>(sc);
+      }
+    }
+    if (D != nullptr) {
+      const uint4 ov = valid ? __ldg(o + row * LPR + chunk) : make_uint4(0, 0, 0, 0);
+      const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
+      const float scale = pow2f(e);
+      float acc = 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 dq = e4m3x2_to_float2(c[j]);
+        acc = fmaf(dq.x * scale, bf16lo(ow[j]), acc);
+        acc = fmaf(dq.y * scale, bf16hi(ow[j]), acc);
+      }
+#pragma unroll
+      for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      if (chunk == 0 && valid) D[static_cast<size_t>(h) * T + tt] = acc;
+    }
+  }
+}
+
+}  // namespace
+}  // namespace flamia
+
+using namespace flamia;
+
+extern "C" flamia_status flamia_quantize_tokenblock(const void* x_bf16, int T, int H, int d,
+                                                    const int32_t* cu_seqlens, int ndocs,
+                                                    int format, const void* o_bf16, float* D,
+                                                    const flamia_qtensor* out, int* dev_status,
+                                                    void* stream) {
+  if (!supported_dim(d)) return FLAMIA_ERR_UNSUPPORTED;
+  if (format != FLAMIA_FORMAT_MXFP8 && format != FLAMIA_FORMAT_MXFP8_NVFP4)
+    return FLAMIA_ERR_UNSUPPORTED;
+  if (!valid_sizes(T, H, d, ndocs) || x_bf16 == nullptr || cu_seqlens == nullptr ||
+      out == nullptr || out->codes == nullptr || out->scales == nullptr)
+    return FLAMIA_ERR_INVALID_ARG;
+  if ((o_bf16 == nullptr) != (D == nullptr)) return FLAMIA_ERR_INVALID_ARG;
+  if (!aligned(x_bf16, 16) || !aligned(out->codes, 16) || (o_bf16 && !aligned(o_bf16, 16)))
+    return FLAMIA_ERR_INVALID_ARG;
+  uint8_t* f4c = nullptr;
+  uint8_t* f4s = nullptr;
+  if (format == FLAMIA_FORMAT_MXFP8_NVFP4) {
+    if (out->nvfp4_codes == nullptr || out->nvfp4_scales == nullptr ||
+        !aligned(out->nvfp4_codes, 16))
+      return FLAMIA_ERR_INVALID_ARG;
+    f4c = out->nvfp4_codes;
+    f4s = out->nvfp4_scales;
+  }
+  int* status = dev_status;
+  dim3 grid((T + kSeg - 1) / kSeg, H);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (d == 128)
+    quantize_kernel<128><<<grid, kQThreads, 0, s>>>(
+        static_cast<const uint4*>(x_bf16), T, H, cu_seqlens, ndocs, out->codes, out->scales, f4c,
+        f4s, static_cast<const uint4*>(o_bf16), D, status);
+  else
+    quantize_kernel<64><<<grid, kQThreads, 0, s>>>(
+        static_cast<const uint4*>(x_bf16), T, H, cu_seqlens, ndocs, out->codes, out->scales, f4c,
+        f4s, static_cast<const uint4*>(o_bf16), D, status);
+  return cudaGetLastError() == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
+}

@@ -1,0 +1,202 @@
+"""Python binding of the flamia C ABI (include/flamia.h).
+
+Argument marshalling only: torch tensors supply device pointers and the
+current CUDA stream; every step of the attention path runs in the library's
+own CUDA kernels.  There is no fallback: if the library is missing or a call
+returns an error status, a RuntimeError is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "libflamia.so")
+
+FLAMIA_OK = 0
+FORMAT_MXFP8 = 0
+FORMAT_MXFP8_NVFP4 = 1
+FLAG_NVFP4_QK = 0x1
+DEV_BAD_SEQLENS = 0x1
+DEV_CAPACITY = 0x2
+DEV_TIMEOUT = 0x4
+
+_LIB = None
+
+
+class QTensorStruct(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("nvfp4_codes", ctypes.c_void_p), ("nvfp4_scales", ctypes.c_void_p)]
+
+
+_vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_QP = ctypes.POINTER(QTensorStruct)
+SIGNATURES = {
+    "flamia_quantize_tokenblock": (_i, [_vp, _i, _i, _i, _vp, _i, _i, _vp, _vp, _QP, _vp, _vp]),
+    "flamia_worklist_bytes": (_sz, [_i, _i]),
+    "flamia_build_worklist": (_i, [_vp, _i, _i, _vp, _sz, _vp, _vp]),
+    "flamia_attn_fwd": (_i, [_QP, _QP, _QP, _vp, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp, _vp, _vp]),
+    "flamia_bwd_workspace_bytes": (_sz, [_i, _i, _i]),
+    "flamia_attn_bwd": (_i, [_QP, _QP, _QP, _QP, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp,
+                             _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
+    "flamia_status_str": (ctypes.c_char_p, [_i]),
+    "flamia_debug_mma_tile": (_i, [_i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+}
+
+
+def load(path: str = LIB_PATH):
+    """Loads the built library (raises if it was not built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"flamia CUDA library not built ({path}); "
+                               "run __graft_entry__.build() first")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = lib
+    return _LIB
+
+
+def _check(status: int, what: str):
+    if status != FLAMIA_OK:
+        msg = load().flamia_status_str(status).decode()
+        raise RuntimeError(f"{what} failed: {msg} ({status})")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise RuntimeError("flamia needs CUDA tensors")
+    if not t.is_contiguous():
+        raise RuntimeError("flamia needs contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+class QTensor:
+    """Caller-owned buffers of one quantised operand (allocated by torch)."""
+
+    def __init__(self, T: int, H: int, d: int, nvfp4: bool = False, device="cuda"):
+        self.codes = torch.empty((T, H, d), dtype=torch.uint8, device=device)
+        self.scales = torch.empty((H, T), dtype=torch.uint8, device=device)
+        self.nvfp4_codes = torch.empty((T, H, d // 2), dtype=torch.uint8, device=device) if nvfp4 else None
+        self.nvfp4_scales = torch.empty((T, H, d // 16), dtype=torch.uint8, device=device) if nvfp4 else None
+
+    def struct(self) -> QTensorStruct:
+        s = QTensorStruct()
+        s.codes = self.codes.data_ptr()
+        s.scales = self.scales.data_ptr()
+        s.nvfp4_codes = self.nvfp4_codes.data_ptr() if self.nvfp4_codes is not None else None
+        s.nvfp4_scales = self.nvfp4_scales.data_ptr() if self.nvfp4_scales is not None else None
+        return s
+
+
+def flamia_quantize_tokenblock(x, cu_seqlens, out: QTensor, fmt: int = FORMAT_MXFP8, o=None,
+                               D=None, dev_status=None):
+    T, H, d = x.shape
+    st = out.struct()
+    _check(load().flamia_quantize_tokenblock(
+        _ptr(x), T, H, d, _ptr(cu_seqlens), cu_seqlens.numel() - 1, fmt, _ptr(o), _ptr(D),
+        ctypes.byref(st), _ptr(dev_status), _stream()), "flamia_quantize_tokenblock")
+
+
+def flamia_worklist_bytes(T: int, ndocs: int) -> int:
+    return int(load().flamia_worklist_bytes(T, ndocs))
+
+
+def flamia_build_worklist(cu_seqlens, T: int, wl, dev_status=None):
+    _check(load().flamia_build_worklist(_ptr(cu_seqlens), cu_seqlens.numel() - 1, T, _ptr(wl),
+                                        wl.numel() * wl.element_size(), _ptr(dev_status),
+                                        _stream()), "flamia_build_worklist")
+
+
+def flamia_attn_fwd(q: QTensor, k: QTensor, v: QTensor, cu_seqlens, T, H, d, softmax_scale,
+                    wl, o, lse, flags: int = 0, dev_status=None):
+    sq, sk, sv = q.struct(), k.struct(), v.struct()
+    _check(load().flamia_attn_fwd(ctypes.byref(sq), ctypes.byref(sk), ctypes.byref(sv),
+                                  _ptr(cu_seqlens), cu_seqlens.numel() - 1, T, H, d,
+                                  float(softmax_scale), flags, _ptr(wl), _ptr(o), _ptr(lse),
+                                  _ptr(dev_status), _stream()), "flamia_attn_fwd")
+
+
+def flamia_bwd_workspace_bytes(T: int, H: int, d: int) -> int:
+    return int(load().flamia_bwd_workspace_bytes(T, H, d))
+
+
+def flamia_attn_bwd(q: QTensor, k: QTensor, v: QTensor, dout: QTensor, D, lse, cu_seqlens, T, H,
+                    d, softmax_scale, wl, dq, dk, dv, ws, flags: int = 0, dev_status=None):
+    sq, sk, sv, sd = q.struct(), k.struct(), v.struct(), dout.struct()
+    _check(load().flamia_attn_bwd(ctypes.byref(sq), ctypes.byref(sk), ctypes.byref(sv),
+                                  ctypes.byref(sd), _ptr(D), _ptr(lse), _ptr(cu_seqlens),
+                                  cu_seqlens.numel() - 1, T, H, d, float(softmax_scale), flags,
+                                  _ptr(wl), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws),
+                                  ws.numel() * ws.element_size(), _ptr(dev_status), _stream()),
+           "flamia_attn_bwd")
+
+
+def flamia_debug_mma_tile(mode, N, a_mn, b_mn, variant, a, b, sfa, sfb, d_out, dev_status=None):
+    _check(load().flamia_debug_mma_tile(mode, N, a_mn, b_mn, variant, _ptr(a), _ptr(b), _ptr(sfa),
+                                        _ptr(sfb), _ptr(d_out), _ptr(dev_status), _stream()),
+           "flamia_debug_mma_tile")
+
+
+class TrainingCall:
+    """Buffers and the sequence of C-ABI calls of one attention training call
+    (quantise Q, K, V -> work list -> forward -> quantise dO with D -> backward)
+    for fixed shapes.  All buffers are torch allocations owned by this object."""
+
+    def __init__(self, T, H, d, cu_seqlens, softmax_scale, nvfp4_qk: bool = False, device="cuda"):
+        self.T, self.H, self.d = T, H, d
+        self.scale = softmax_scale
+        self.cu = cu_seqlens
+        self.flags = FLAG_NVFP4_QK if nvfp4_qk else 0
+        self.fmt_qk = FORMAT_MXFP8_NVFP4 if nvfp4_qk else FORMAT_MXFP8
+        self.q = QTensor(T, H, d, nvfp4_qk, device)
+        self.k = QTensor(T, H, d, nvfp4_qk, device)
+        self.v = QTensor(T, H, d, False, device)
+        self.dout = QTensor(T, H, d, False, device)
+        ndocs = cu_seqlens.numel() - 1
+        self.wl = torch.empty(flamia_worklist_bytes(T, ndocs), dtype=torch.uint8, device=device)
+        self.ws = torch.empty(flamia_bwd_workspace_bytes(T, H, d), dtype=torch.uint8, device=device)
+        self.o = torch.empty((T, H, d), dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty((H, T), dtype=torch.float32, device=device)
+        self.D = torch.empty((H, T), dtype=torch.float32, device=device)
+        self.dq = torch.empty((T, H, d), dtype=torch.bfloat16, device=device)
+        self.dk = torch.empty_like(self.dq)
+        self.dv = torch.empty_like(self.dq)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def forward(self, xq, xk, xv):
+        flamia_quantize_tokenblock(xq, self.cu, self.q, self.fmt_qk, dev_status=self.status)
+        flamia_quantize_tokenblock(xk, self.cu, self.k, self.fmt_qk, dev_status=self.status)
+        flamia_quantize_tokenblock(xv, self.cu, self.v, FORMAT_MXFP8, dev_status=self.status)
+        flamia_build_worklist(self.cu, self.T, self.wl, dev_status=self.status)
+        flamia_attn_fwd(self.q, self.k, self.v, self.cu, self.T, self.H, self.d, self.scale,
+                        self.wl, self.o, self.lse, self.flags, dev_status=self.status)
+        return self.o, self.lse
+
+    def backward(self, xdo):
+        flamia_quantize_tokenblock(xdo, self.cu, self.dout, FORMAT_MXFP8, o=self.o, D=self.D,
+                                   dev_status=self.status)
+        flamia_attn_bwd(self.q, self.k, self.v, self.dout, self.D, self.lse, self.cu, self.T,
+                        self.H, self.d, self.scale, self.wl, self.dq, self.dk, self.dv, self.ws,
+                        self.flags, dev_status=self.status)
+        return self.dq, self.dk, self.dv
+
+    def __call__(self, xq, xk, xv, xdo):
+        self.forward(xq, xk, xv)
+        return self.backward(xdo)
+
+    def check_status(self):
+        st = int(self.status.item())
+        if st != 0:
+            raise RuntimeError(f"flamia device status 0x{st:x}")

@@ -1,0 +1,81 @@
+"""The C-ABI library builds, loads without a GPU, exports every declared
+symbol, and rejects bad arguments on the host (no kernel is launched)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def cpu_lib():
+    from precision_causal_attention_block_gb300 import build, flamia
+    build.build()
+    return flamia.load()
+
+
+def declared_symbols():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(flamia_[a-z_0-9]+)\s*\(", src))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(cpu_lib):
+    names = declared_symbols()
+    assert "flamia_attn_fwd" in names and "flamia_quantize_tokenblock" in names
+    for n in names:
+        assert hasattr(cpu_lib, n), n
+
+
+def test_size_queries(cpu_lib):
+    from precision_causal_attention_block_gb300 import flamia as fl
+    assert fl.flamia_bwd_workspace_bytes(16384, 16, 128) == 16384 * 16 * 128 * 4
+    assert fl.flamia_bwd_workspace_bytes(10, 1, 96) == 0
+    wl = fl.flamia_worklist_bytes(65536, 30)
+    assert wl >= 64 + 16 * (65536 // 256 + 31) + 16 * (65536 // 128 + 31)
+    assert fl.flamia_worklist_bytes(0, 1) == 0
+
+
+def test_status_strings(cpu_lib):
+    for s in range(5):
+        assert cpu_lib.flamia_status_str(s)
+    assert cpu_lib.flamia_status_str(99) == b"unknown status"
+
+
+def test_host_side_argument_checks(cpu_lib):
+    from precision_causal_attention_block_gb300 import flamia as fl
+    q = fl.QTensorStruct()
+    null = ctypes.c_void_p(None)
+    # unsupported head dim
+    assert cpu_lib.flamia_quantize_tokenblock(null, 16, 1, 96, null, 1, 0, null, null,
+                                              ctypes.byref(q), null, null) == 2
+    # null input
+    assert cpu_lib.flamia_quantize_tokenblock(null, 16, 1, 64, null, 1, 0, null, null,
+                                              ctypes.byref(q), null, null) == 1
+    # work list: buffer too small / null
+    assert cpu_lib.flamia_build_worklist(null, 1, 16, null, 0, null, null) == 1
+    assert cpu_lib.flamia_build_worklist(ctypes.c_void_p(256), 1, 16, ctypes.c_void_p(256), 8,
+                                         null, null) == 3
+    # flags not supported / bad scale
+    assert cpu_lib.flamia_attn_fwd(ctypes.byref(q), ctypes.byref(q), ctypes.byref(q), null, 1, 16,
+                                   1, 64, ctypes.c_float(0.1), 0x80, null, null, null, null,
+                                   null) == 2
+    assert cpu_lib.flamia_attn_bwd(ctypes.byref(q), ctypes.byref(q), ctypes.byref(q),
+                                   ctypes.byref(q), null, null, null, 1, 16, 1, 64,
+                                   ctypes.c_float(-1.0), 0, null, null, null, null, null, 0, null,
+                                   null) == 1
+
+
+def test_product_path_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "precision_causal_attention_block_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"(import|from)\s+oracle|oracle/|flamia_oracle", src), f

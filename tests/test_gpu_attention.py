@@ -1,0 +1,165 @@
+"""GPU causal forward + backward against the FP64 oracle.
+
+Bar (the review page's accuracy section and the method's numerics): on the
+same quantised inputs O, dQ, dK, dV reach cosine >= 0.9995 and max |err| <=
+2e-2 max |ref| against the oracle; the codes are bit-exact; on plain normal
+inputs the quantised path reaches cosine >= 0.998 against exact attention;
+a future token outside a block changes no earlier O / LSE bit (sec. 3.2, 4.5).
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import flamia_oracle as O
+from precision_causal_attention_block_gb300 import workloads as W
+from tests.gpu_helpers import compare, cu_tensor, dev, np64
+
+pytestmark = pytest.mark.gpu
+
+NAMES = ("q", "k", "v", "do")
+
+
+def run_call(w, x, nvfp4=False):
+    from precision_causal_attention_block_gb300 import flamia as fl
+    call = fl.TrainingCall(w.T, w.H, w.d, cu_tensor(w.cu_seqlens), w.sm_scale, nvfp4_qk=nvfp4)
+    xd = {n: dev(t) for n, t in x.items()}
+    call.forward(xd["q"], xd["k"], xd["v"])
+    call.backward(xd["do"])
+    torch.cuda.synchronize()
+    call.check_status()
+    return call
+
+
+def check_against(call, ref, tok, heads, what=("O", "dQ", "dK", "dV")):
+    """Compare GPU outputs on tokens `tok` (slice) and `heads` with an oracle
+    result computed on exactly that slice."""
+    gpu = {"O": call.o, "dQ": call.dq, "dK": call.dk, "dV": call.dv}
+    for n in what:
+        compare(n, np64(gpu[n][tok][:, heads]), ref[n])
+    lse = call.lse[heads][:, tok].cpu().numpy().astype(np.float64)
+    assert np.abs(lse - ref["lse"]).max() <= 1e-4 * max(1.0, np.abs(ref["lse"]).max())
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_ragged_small_elementwise(lib, d):
+    w = W.custom("ragged_attn", [300, 1, 129, 0, 270, 33, 256], 2, d, seed=7,
+                 structure="outlier16x2")
+    x = W.make_inputs_bf16(w)
+    call = run_call(w, x)
+    ref = O.attention(*[x[n].double().numpy() for n in NAMES], w.cu_seqlens, w.sm_scale)
+    qz = ref["quantized"]
+    assert np.array_equal(call.q.codes.cpu().numpy(), qz.qc)
+    assert np.array_equal(call.v.scales.cpu().numpy(), qz.vs)
+    assert np.array_equal(call.dout.codes.cpu().numpy(), qz.doc)
+    check_against(call, ref, slice(0, w.T), list(range(w.H)))
+    compare("D", call.D.cpu().numpy(), ref["D"], cos_min=0.99999, rel_max=1e-3)
+
+
+def test_tiny_config(lib):
+    w = W.tiny()
+    x = W.make_inputs_bf16(w)
+    call = run_call(w, x)
+    ref = O.attention(*[x[n].double().numpy() for n in NAMES], w.cu_seqlens, w.sm_scale)
+    check_against(call, ref, slice(0, w.T), [0, 1])
+
+
+def test_fixed4x4096_one_document_two_heads(lib):
+    w = W.fixed4x4096()
+    x = W.make_inputs_bf16(w)
+    call = run_call(w, x)
+    heads = [0, 9]
+    s, e = 4096, 8192  # document 1
+    ref = O.attention(*[x[n][s:e][:, heads].double().numpy() for n in NAMES], [0, e - s],
+                      w.sm_scale)
+    check_against(call, ref, slice(s, e), heads)
+
+
+def test_varlen65536_sampled(lib):
+    w = W.varlen65536()
+    x = W.make_inputs_bf16(w)
+    call = run_call(w, x)
+    cu = list(w.cu_seqlens)
+    lens = np.diff(cu)
+    # one mid-size document in full, plus exact-attention cosine on it
+    b = int(np.argmin(np.abs(lens - 2000)))
+    s, e = cu[b], cu[b + 1]
+    heads = [3]
+    sl = [x[n][s:e][:, heads].double().numpy() for n in NAMES]
+    ref = O.attention(*sl, [0, e - s], w.sm_scale)
+    check_against(call, ref, slice(s, e), heads)
+    exact = O.attention(*sl, [0, e - s], w.sm_scale, quant=False)
+    for n, t in (("O", call.o), ("dQ", call.dq), ("dK", call.dk), ("dV", call.dv)):
+        cos = O.cosine(np64(t[s:e][:, heads]), exact[n])
+        assert cos >= 0.998, (n, cos)
+    # the longest document: its first and last query blocks, last key blocks
+    b = int(np.argmax(lens))
+    s, e = cu[b], cu[b + 1]
+    L = e - s
+    qz = O.Quantized(*[x[n][s:e][:, heads].double().numpy() for n in NAMES], [0, L])
+    nb = (L + 31) // 32
+    res = O.sampled_rows(qz, 0, 0, w.sm_scale, qblocks=[0, 1, nb - 1], kblocks=[nb - 2, nb - 1])
+    for qb in res["O"]:
+        rows = slice(s + 32 * qb, min(s + 32 * qb + 32, e))
+        compare(f"O[{qb}]", np64(call.o[rows][:, heads[0]]), res["O"][qb])
+        compare(f"dQ[{qb}]", np64(call.dq[rows][:, heads[0]]), res["dQ"][qb])
+    for kb in res["dK"]:
+        rows = slice(s + 32 * kb, min(s + 32 * kb + 32, e))
+        compare(f"dK[{kb}]", np64(call.dk[rows][:, heads[0]]), res["dK"][kb])
+        compare(f"dV[{kb}]", np64(call.dv[rows][:, heads[0]]), res["dV"][kb])
+
+
+def test_onetoken131072_slice(lib):
+    w = W.onetoken131072()
+    x = W.make_inputs_bf16(w)
+    call = run_call(w, x)
+    for (s, e) in ((0, 256), (w.T - 256, w.T)):
+        sl = [x[n][s:e].double().numpy() for n in NAMES]
+        ref = O.attention(*sl, list(range(e - s + 1)), w.sm_scale)
+        check_against(call, ref, slice(s, e), list(range(w.H)))
+        exact = O.attention(*sl, list(range(e - s + 1)), w.sm_scale, quant=False)
+        assert O.cosine(np64(call.o[s:e]), exact["O"]) >= 0.998
+
+
+def test_long131072_sampled(lib):
+    w = W.long131072()
+    x = W.make_inputs_bf16(w)
+    call = run_call(w, x)
+    heads = [0, 17]
+    for h in heads:
+        qz = O.Quantized(*[x[n][:, [h]].double().numpy() for n in NAMES], [0, w.T])
+        nb = w.T // 32
+        res = O.sampled_rows(qz, 0, 0, w.sm_scale, qblocks=[0, 5, nb // 2, nb - 1],
+                             kblocks=[nb - 3, nb - 1])
+        for qb in res["O"]:
+            rows = slice(32 * qb, 32 * qb + 32)
+            compare(f"O[{qb}]", np64(call.o[rows][:, h]), res["O"][qb])
+            compare(f"dQ[{qb}]", np64(call.dq[rows][:, h]), res["dQ"][qb])
+            lse = call.lse[h, rows].cpu().numpy().astype(np.float64)
+            assert np.abs(lse - res["lse"][qb]).max() <= 1e-4 * np.abs(res["lse"][qb]).max()
+        for kb in res["dK"]:
+            rows = slice(32 * kb, 32 * kb + 32)
+            compare(f"dK[{kb}]", np64(call.dk[rows][:, h]), res["dK"][kb])
+            compare(f"dV[{kb}]", np64(call.dv[rows][:, h]), res["dV"][kb])
+
+
+def test_leakage_probe_bitwise(lib):
+    """Perturbing a future token outside the victim's 32-token block (and in
+    another document) leaves every earlier O and LSE bit unchanged; dQ of the
+    earlier rows changes by no more than the float32 atomic-order noise."""
+    w = W.custom("probe", [600, 200], 2, 128, seed=9)
+    x = W.make_inputs_bf16(w)
+    base = run_call(w, x)
+    o0, l0, dq0 = base.o.clone(), base.lse.clone(), base.dq.clone()
+    base2 = run_call(w, x)
+    noise = (base2.dq.float() - dq0.float()).abs().max().item()
+    t = 450  # block [448, 480) of document 0
+    for name in NAMES:
+        y = {n: v.clone() for n, v in x.items()}
+        y[name][t] = (y[name][t].float() * 1000.0).to(torch.bfloat16)
+        y[name][t, :, 5] += 50.0
+        r = run_call(w, y)
+        assert torch.equal(r.o[:448], o0[:448]), name
+        assert torch.equal(r.lse[:, :448], l0[:, :448]), name
+        assert torch.equal(r.o[600:], o0[600:]), name
+        d = (r.dq[:448].float() - dq0[:448].float()).abs().max().item()
+        assert d <= max(noise, 0.0) * 4 + 1e-30, (name, d, noise)

@@ -1,0 +1,88 @@
+"""Single-tile tensor-core products against a float64 reference: every
+operand major-ness and scale placement the attention kernels use (the review
+page, sec. 3.1: one E4M3 payload serves K-major and MN-major products; block
+scales per 32 elements; the mixed path's NVFP4 product)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import flamia_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+def _codes_e4m3(rng, shape):
+    c = rng.integers(0, 256, size=shape, dtype=np.uint8)
+    c[(c & 0x7F) == 0x7F] = 0x38  # no NaN codes
+    return c
+
+
+def _run(fl, mode, N, a_mn, b_mn, variant, a, b, sfa, sfb):
+    d = torch.empty((128, N), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t = lambda z: torch.from_numpy(np.ascontiguousarray(z)).cuda()
+    fl.flamia_debug_mma_tile(mode, N, a_mn, b_mn, variant, t(a), t(b),
+                             t(sfa) if sfa is not None else None,
+                             t(sfb) if sfb is not None else None, d, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    return d.cpu().numpy().astype(np.float64)
+
+
+def _reference(mode, N, a_mn, b_mn, a, b, sfa, sfb):
+    if mode == 2:
+        def unpack(p):
+            c = np.empty((p.shape[0], 64), dtype=np.uint8)
+            c[:, 0::2] = p & 0xF
+            c[:, 1::2] = p >> 4
+            return O.e2m1_decode(c)
+        A = unpack(a) * np.repeat(O.E4M3_TABLE[sfa], 16, axis=1)
+        B = unpack(b) * np.repeat(O.E4M3_TABLE[sfb], 16, axis=1)
+        return A @ B.T
+    A = O.e4m3_decode(a.T if a_mn else a)          # [128][K]
+    B = O.e4m3_decode(b.T if b_mn else b)          # [N][K]
+    if mode == 1:
+        A = A * np.repeat(np.ldexp(1.0, sfa.astype(int) - 127), 32, axis=1)
+        B = B * np.repeat(np.ldexp(1.0, sfb.astype(int) - 127), 32, axis=1)
+    return A @ B.T
+
+
+CASES = [
+    # mode, N, a_mn, b_mn
+    (0, 128, 0, 0),   # S = Q K^T, d = 128
+    (0, 128, 1, 1),
+    (1, 128, 0, 1),   # O += P V, d = 128 (V read MN-major)
+    (1, 64, 0, 1),    # O += P V, d = 64
+    (1, 128, 1, 1),   # dQ = dS K (dS read MN-major)
+    (1, 128, 0, 0),
+    (2, 128, 0, 0),   # NVFP4 S = Q K^T, d = 64
+]
+
+
+@pytest.mark.parametrize("mode,N,a_mn,b_mn", CASES)
+def test_tile_product(lib, mode, N, a_mn, b_mn):
+    from precision_causal_attention_block_gb300 import flamia as fl
+    rng = np.random.default_rng(mode * 100 + N + 10 * a_mn + b_mn)
+    if mode == 2:
+        a = rng.integers(0, 256, size=(128, 32), dtype=np.uint8)
+        b = rng.integers(0, 256, size=(N, 32), dtype=np.uint8)
+        sfa = rng.integers(0x30, 0x48, size=(128, 4), dtype=np.uint8)
+        sfb = rng.integers(0x30, 0x48, size=(N, 4), dtype=np.uint8)
+    else:
+        a = _codes_e4m3(rng, (128, 128))
+        b = _codes_e4m3(rng, (128, N) if b_mn else (N, 128))
+        sfa = rng.integers(122, 133, size=(128, 4), dtype=np.uint8) if mode == 1 else None
+        sfb = rng.integers(122, 133, size=(N, 4), dtype=np.uint8) if mode == 1 else None
+    ref = _reference(mode, N, a_mn, b_mn, a, b, sfa, sfb)
+    tol = 1e-5 * np.abs(ref).max()
+    got = _run(fl, mode, N, a_mn, b_mn, 0, a, b, sfa, sfb)
+    if np.abs(got - ref).max() > tol:
+        report = {}
+        for var in (1, 2, 3):
+            try:
+                g = _run(fl, mode, N, a_mn, b_mn, var, a, b, sfa, sfb)
+                report[var] = float(np.abs(g - ref).max() / np.abs(ref).max())
+            except Exception as ex:  # pragma: no cover - diagnostics only
+                report[var] = str(ex)
+        pytest.fail(f"variant 0 max rel err {np.abs(got - ref).max() / np.abs(ref).max():.3e}; "
+                    f"other variants: {report}")
