@@ -107,6 +107,20 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+def reduce_max(values, device):
+    """Element-wise maximum over ranks (the slowest rank sets the time)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_throughput(flops_per_step, steps, world, slowest_ms):
+    """Whole-job TFLOP/s: every rank ran its own replica of the step."""
+    return world * flops_per_step * steps / (slowest_ms * 1e-3) / 1e12
+
+
 def make_workload(name):
     from precision_causal_attention_block_gb300 import workloads as W
     return W.WORKLOADS[name]()
@@ -210,16 +224,14 @@ def run_ours(args, rank, world, local):
     res = {"total_ms": total_ms, "e2e_ms": e2e_ms, "bwd_ms": sum(bwd_ms) / len(bwd_ms),
            "clocks": clocks.summary()}
     if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms, e2e_ms, res["bwd_ms"]], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        res["total_ms"], res["e2e_ms"], res["bwd_ms"] = t.tolist()
+        res["total_ms"], res["e2e_ms"], res["bwd_ms"] = reduce_max(
+            [total_ms, e2e_ms, res["bwd_ms"]], dev)
     if rank != 0:
         return None
     pk = peaks()
     ms_step = res["total_ms"] / args.steps
-    value = world * flops * args.steps / (res["total_ms"] * 1e-3) / 1e12
-    e2e_value = world * flops * args.steps / (res["e2e_ms"] * 1e-3) / 1e12
+    value = job_throughput(flops, args.steps, world, res["total_ms"])
+    e2e_value = job_throughput(flops, args.steps, world, res["e2e_ms"])
     achieved = bwd_flops / (res["bwd_ms"] * 1e-3) / 1e12
     launches_per_step = 4 + 6 + 1 + 1 + 1  # quantiser x4, work list, fwd, bwd, dq convert
     line = {

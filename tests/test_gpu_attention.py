@@ -90,7 +90,10 @@ def test_varlen65536_sampled(lib):
     exact = O.attention(*sl, [0, e - s], w.sm_scale, quant=False)
     for n, t in (("O", call.o), ("dQ", call.dq), ("dK", call.dk), ("dV", call.dv)):
         cos = O.cosine(np64(t[s:e][:, heads]), exact[n])
-        assert cos >= 0.998, (n, cos)
+        # the method itself (the oracle) sets how close to exact attention a
+        # quantised result can be; the pages report dQ cosine 0.9979 for it
+        method = O.cosine(ref[n], exact[n])
+        assert cos >= min(0.998, method - 2e-4), (n, cos, method)
     # the longest document: its first and last query blocks, last key blocks
     b = int(np.argmax(lens))
     s, e = cu[b], cu[b + 1]
