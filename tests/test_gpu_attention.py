@@ -164,5 +164,9 @@ def test_leakage_probe_bitwise(lib):
         assert torch.equal(r.o[:448], o0[:448]), name
         assert torch.equal(r.lse[:, :448], l0[:, :448]), name
         assert torch.equal(r.o[600:], o0[600:]), name
+        # dQ is summed with float32 atomics in no fixed order: allow the
+        # run-to-run noise floor (at most ~1 BF16 ulp); a leak from a x1000
+        # perturbation would be orders of magnitude larger
         d = (r.dq[:448].float() - dq0[:448].float()).abs().max().item()
-        assert d <= max(noise, 0.0) * 4 + 1e-30, (name, d, noise)
+        floor = max(4 * noise, 2.0 ** -7 * dq0[:448].float().abs().max().item())
+        assert d <= floor, (name, d, noise)
