@@ -128,6 +128,34 @@ flamia_status flamia_build_worklist(const int32_t* cu_seqlens, int ndocs, int T,
                                     void* stream);
 
 /*
+ * Work list without any device allocation, for callers that cannot allocate:
+ * a framework whose caching allocator owns the device memory and hands the
+ * library only its output tensors, a plugin host that gives the library no
+ * allocator, or a latency-critical loop that cannot afford the implicit device
+ * synchronisation of cudaMalloc / cudaFree.  The paper has no counterpart:
+ * it is a convenience of this library's interface.
+ *
+ * Same inputs and the same output as flamia_build_worklist, but `wl` only
+ * needs the header and the two item arrays (the layout above up to the end of
+ * bwd_items; a flamia_worklist_bytes-sized buffer always suffices).  The
+ * builder's scratch lives in an 8 MiB array in the library's own device
+ * memory, allocated on every GPU that loads the library and held until the
+ * process exits.  The scratch grows mainly with the number of documents: any
+ * document mix of up to 131,072 tokens fits, and at the 1,048,576-token
+ * maximum up to 65,536 documents do; a layout whose scratch would exceed
+ * 8 MiB returns FLAMIA_ERR_WORKSPACE without launching.
+ * No cudaMalloc / cudaFree is called.  The first call on a device looks up the
+ * array's device address (with that device current) and caches it; make that
+ * first call before any stream capture.  All calls share the one array:
+ * calls whose kernels overlap on the GPU (different streams, or different
+ * host threads without ordering) race and produce garbage; serialise them.
+ * Nothing left in the array by an earlier call is read by a later one.
+ */
+flamia_status flamia_build_worklist_static(const int32_t* cu_seqlens, int ndocs, int T,
+                                           void* wl, size_t wl_bytes, int* dev_status,
+                                           void* stream);
+
+/*
  * Causal forward.  Source: review page sec. 1.2 (S = QK^T scale, P =
  * softmax(S), O = PV, row statistics saved), sec. 3.1 (unscaled E4M3 product
  * for QK^T with the query factor folded into the softmax scale and the key

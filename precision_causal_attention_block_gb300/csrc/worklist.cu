@@ -8,6 +8,8 @@
 //   count per document -> exclusive scan -> emit in generation order with a
 //   per-chunk cost histogram -> per-bucket scan over chunks -> scan over
 //   buckets in descending cost -> stable scatter (rank inside a chunk).
+#include <mutex>
+
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -252,6 +254,94 @@ extern "C" flamia_status flamia_build_worklist(const int32_t* cu_seqlens, int nd
     cudaFuncSetAttribute(wl_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(smem));
   }
+  wl_count<<<(ndocs + 255) / 256, 256, 0, s>>>(cu_seqlens, ndocs, T, p, dev_status);
+  wl_scan_docs<<<1, kScanThreads, 0, s>>>(ndocs, L.cap_fwd, L.cap_bwd, p, dev_status);
+  wl_emit<<<L.chunks_fwd + L.chunks_bwd, kSortChunk, smem, s>>>(cu_seqlens, ndocs, L.chunks_fwd,
+                                                               L.nbuckets, p);
+  wl_scan_chunks<<<(2 * L.nbuckets + 255) / 256, 256, 0, s>>>(L.nbuckets, L.chunks_fwd,
+                                                              L.chunks_bwd, p);
+  wl_scan_buckets<<<2, kScanThreads, 0, s>>>(L.nbuckets, p);
+  wl_scatter<<<L.chunks_fwd + L.chunks_bwd, kSortChunk, smem, s>>>(L.chunks_fwd, L.nbuckets, p);
+  return cudaGetLastError() == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant of the work-list builder.
+//
+// Some callers cannot allocate device memory for the builder's scratch: a
+// framework whose caching allocator owns the device memory and hands the
+// library only the output tensors, a plugin host that gives the library no
+// allocator at all, or a latency-critical loop where the implicit device
+// synchronisation of cudaMalloc / cudaFree is not acceptable.  This entry point
+// keeps the scratch (per-document counts and offsets, items in generation
+// order, per-chunk cost histograms, bucket starts) in a fixed array in the
+// library's own device memory instead.
+namespace flamia {
+namespace {
+
+constexpr size_t kStaticScratchBytes = 8u << 20;  // 8 MiB per GPU, held until exit
+static __device__ __align__(256) unsigned char g_wl_scratch[kStaticScratchBytes];
+
+std::mutex g_scratch_mu;
+void* g_scratch_addr[128] = {};
+
+// Device address of g_wl_scratch on the current device (looked up once per
+// device; the name is only a host-side stand-in).
+void* static_scratch_address() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_wl_scratch) != cudaSuccess) return nullptr;
+    g_scratch_addr[dev] = p;
+  }
+  return g_scratch_addr[dev];
+}
+
+}  // namespace
+}  // namespace flamia
+
+extern "C" flamia_status flamia_build_worklist_static(const int32_t* cu_seqlens, int ndocs,
+                                                      int T, void* wl, size_t wl_bytes,
+                                                      int* dev_status, void* stream) {
+  if (cu_seqlens == nullptr || wl == nullptr || T <= 0 || ndocs <= 0 || ndocs > T + 1 ||
+      T > (1 << 20))
+    return FLAMIA_ERR_INVALID_ARG;
+  if (!aligned(wl, 256)) return FLAMIA_ERR_INVALID_ARG;
+  const WorklistLayout L = worklist_layout(T, ndocs);
+  // the caller's buffer holds the header and both item arrays
+  if (wl_bytes < L.off_doc_counts) return FLAMIA_ERR_WORKSPACE;
+  // everything after the item arrays lives in the static scratch
+  if (L.total - L.off_doc_counts > kStaticScratchBytes) return FLAMIA_ERR_WORKSPACE;
+  char* scratch = static_cast<char*>(static_scratch_address());
+  if (scratch == nullptr) return FLAMIA_ERR_CUDA;
+  char* base = static_cast<char*>(wl);
+  // scratch keeps the layout's spacing, shifted to the start of the array
+  auto at = [&](size_t off) { return scratch + (off - L.off_doc_counts); };
+  WlPtrs p;
+  p.header = reinterpret_cast<int*>(base);
+  p.fwd = reinterpret_cast<int4*>(base + L.off_fwd);
+  p.bwd = reinterpret_cast<int4*>(base + L.off_bwd);
+  p.counts = reinterpret_cast<int*>(at(L.off_doc_counts));
+  p.offsets = reinterpret_cast<int*>(at(L.off_doc_offsets));
+  p.gen_fwd = reinterpret_cast<int4*>(at(L.off_gen_fwd));
+  p.gen_bwd = reinterpret_cast<int4*>(at(L.off_gen_bwd));
+  p.hist_fwd = reinterpret_cast<int*>(at(L.off_hist_fwd));
+  p.hist_bwd = reinterpret_cast<int*>(at(L.off_hist_bwd));
+  p.bucket_fwd = reinterpret_cast<int*>(at(L.off_buckets));
+  p.bucket_bwd = p.bucket_fwd + L.nbuckets;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t smem = static_cast<size_t>(L.nbuckets) * sizeof(int);
+  if (smem > 200 * 1024) return FLAMIA_ERR_UNSUPPORTED;
+  if (smem > 48 * 1024) {
+    cudaFuncSetAttribute(wl_emit, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(smem));
+    cudaFuncSetAttribute(wl_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(smem));
+  }
+  // Every buffer of scratch is fully written before it is read within one
+  // call, so nothing left by an earlier call needs clearing.
   wl_count<<<(ndocs + 255) / 256, 256, 0, s>>>(cu_seqlens, ndocs, T, p, dev_status);
   wl_scan_docs<<<1, kScanThreads, 0, s>>>(ndocs, L.cap_fwd, L.cap_bwd, p, dev_status);
   wl_emit<<<L.chunks_fwd + L.chunks_bwd, kSortChunk, smem, s>>>(cu_seqlens, ndocs, L.chunks_fwd,

@@ -41,6 +41,7 @@ SIGNATURES = {
     "flamia_bwd_workspace_bytes": (_sz, [_i, _i, _i]),
     "flamia_attn_bwd": (_i, [_QP, _QP, _QP, _QP, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp,
                              _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
+    "flamia_build_worklist_static": (_i, [_vp, _i, _i, _vp, _sz, _vp, _vp]),
     "flamia_status_str": (ctypes.c_char_p, [_i]),
     "flamia_debug_mma_tile": (_i, [_i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
 }
@@ -117,6 +118,15 @@ def flamia_build_worklist(cu_seqlens, T: int, wl, dev_status=None):
     _check(load().flamia_build_worklist(_ptr(cu_seqlens), cu_seqlens.numel() - 1, T, _ptr(wl),
                                         wl.numel() * wl.element_size(), _ptr(dev_status),
                                         _stream()), "flamia_build_worklist")
+
+
+def flamia_build_worklist_static(cu_seqlens, T: int, wl, dev_status=None):
+    """Work list with the builder's scratch in the library's static device
+    array (no allocation); same output as flamia_build_worklist."""
+    _check(load().flamia_build_worklist_static(_ptr(cu_seqlens), cu_seqlens.numel() - 1, T,
+                                               _ptr(wl), wl.numel() * wl.element_size(),
+                                               _ptr(dev_status), _stream()),
+           "flamia_build_worklist_static")
 
 
 def flamia_attn_fwd(q: QTensor, k: QTensor, v: QTensor, cu_seqlens, T, H, d, softmax_scale,
