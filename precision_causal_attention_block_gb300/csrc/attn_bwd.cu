@@ -2,21 +2,26 @@
 // 1.2, 3.1, 3.3, 3.4 "Backward pass").
 //
 // One CTA = one 128-key tile of a document x one head; it walks the 128-query
-// tiles of the same document from the diagonal to the document end.  Warp
-// roles:
-//   warp 0      TMA producer: K, V once; Q, dO tiles through a ring.
-//   warp 1      tensor-memory owner and single-thread tcgen05 MMA issuer.
-//   warps 4-7   compute group: thread = key row of S^T / dP^T, and query row
-//               of the dQ partial.
+// tiles of the same document from the diagonal to the document end.  CTAs are
+// ordered head-major (all key tiles of a head, longest first, then the next
+// head), so the Q / dO tiles and the dQ rows a wave of CTAs touches belong to
+// few heads and stay in L2.  Warp roles:
+//   warp 0       TMA producer: K, V once; Q, dO tiles through a 2-stage ring.
+//   warp 1       tensor-memory owner and single-thread tcgen05 MMA issuer.
+//   warps 4-7    compute group 0: query columns 0..63 of every tile
+//   warps 8-11   compute group 1: query columns 64..127
+//   (thread = key row of S^T / dP^T; for the dQ partial thread = query row,
+//   the two groups splitting the head dimension).
 // Per query tile u:
 //   S^T = K Q^T and dP^T = V dO^T (unscaled E4M3, f32 in TMEM);
-//   the compute group recomputes P = exp2(s - lse2) with the forward's
-//   factors and masks, writes the dV operand RNE_E4M3(2^8 P) and the dS
-//   codes (one round-up exponent per document-aligned 32x32 block) to shared
+//   the compute groups recompute P = exp2(s - lse2) with the forward's
+//   factors and masks, write the dV operand RNE_E4M3(2^8 P) and the dS codes
+//   (one round-up exponent per document-aligned 32x32 block) to shared
 //   memory, and the block scales of the three products to TMEM;
 //   dV += P^b^T dO, dK += dS^T Q (both stay in TMEM over all u) and
 //   dQ_u = dS K (into the columns of S^T) are block-scaled MMAs;
-//   dQ_u is read back and added in float32 to a global accumulator.
+//   dQ_u is scaled, staged in shared memory and added in float32 to the
+//   global accumulator by bulk tensor reduce-adds.
 // Tensor memory (512 columns): S^T / dQ_u [0,128), dP^T and the scale
 // factors [128,256), dV [256,256+d), dK [256+d,256+2d).
 #include <cuda_bf16.h>
@@ -28,7 +33,8 @@ namespace flamia {
 namespace {
 
 constexpr int kBStages = 2;
-constexpr int kBwdThreads = 256;
+constexpr int kBwdThreads = 384;
+constexpr int kComputeThreads = 256;
 constexpr uint32_t kColSP = 0, kColDP = 128, kColDV = 256;
 // scale-factor columns inside the dP^T region (written after dP^T is read)
 constexpr uint32_t kSfDvA = 128, kSfDvB = 132, kSfDkA = 136, kSfDkB = 140, kSfDqA = 144,
@@ -43,10 +49,12 @@ struct BwdSmem {
   alignas(1024) uint8_t dout[kBStages][kTileBytes];
   alignas(1024) uint8_t pb[kTile * kTile];  // [key][query] E4M3, 128B-swizzled rows
   alignas(1024) uint8_t ds[kTile * kTile];  // [key][query] E4M3, 128B-swizzled rows
-  float nl[kTile];        // 8 - lse2 of each query column (-inf outside the document)
-  float dd[kTile];        // D of each query column (0 outside)
+  // dQ_u staging: DIM/32 boxes of [128 query rows][32 floats], 128B-swizzled
+  alignas(1024) float dqs[DIM / 32][kTile * 32];
+  alignas(16) float nl[kTile];  // 8 - lse2 of each query column (-inf outside the document)
+  alignas(16) float dd[kTile];  // D of each query column (0 outside)
   uint32_t qbyte[4], dobyte[4];  // E8M0 bytes of the 4 query blocks of Q and dO
-  uint32_t eds[4][4];     // dS block bytes [query block][key block]
+  uint32_t eds[4][4];            // dS block bytes [query block][key block]
   uint64_t bar_kv;
   uint64_t bar_qd_full[kBStages];
   uint64_t bar_qd_empty[kBStages];
@@ -65,10 +73,9 @@ struct BwdParams {
   const int32_t* cu;
   const int* wl_header;
   const int4* items;
-  float* dq_acc;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
-  int T, H, ndocs;
+  int T, H, ndocs, cap;
   float scale_log2;  // softmax_scale * log2(e)
   float sm_scale;
   int* status;
@@ -81,10 +88,45 @@ __host__ __device__ constexpr uint32_t operand_layout() {
 
 __device__ __forceinline__ float pow2_or_zero(int k) { return k < -126 ? 0.f : exp2i(k); }
 
-__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
-  asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a),
-               "f"(b), "f"(c), "f"(d)
-               : "memory");
+// One 32-column chunk of a key row: P (operand codes), dS (float, 2^8-scaled)
+// and the chunk's |dS| maximum.  MASK: diagonal tile, query < key is masked.
+template <bool MASK>
+__device__ __forceinline__ float bwd_chunk(const uint32_t (&sv)[32], uint32_t (&dv)[32],
+                                           const float* nl, const float* dd, float fS, float fP,
+                                           int col0, int key, uint32_t (&pw)[8]) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; i += 4) {
+    const float4 n4 = *reinterpret_cast<const float4*>(nl + i);
+    const float4 d4 = *reinterpret_cast<const float4*>(dd + i);
+    float2 s01 = __ffma2_rn(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])),
+                            make_float2(fS, fS), make_float2(n4.x, n4.y));
+    float2 s23 = __ffma2_rn(make_float2(__uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3])),
+                            make_float2(fS, fS), make_float2(n4.z, n4.w));
+    if (MASK) {
+      if (col0 + i + 0 < key) s01.x = -INFINITY;
+      if (col0 + i + 1 < key) s01.y = -INFINITY;
+      if (col0 + i + 2 < key) s23.x = -INFINITY;
+      if (col0 + i + 3 < key) s23.y = -INFINITY;
+    }
+    const float2 p01 = make_float2(ex2_approx(s01.x), ex2_approx(s01.y));
+    const float2 p23 = make_float2(ex2_approx(s23.x), ex2_approx(s23.y));
+    const float2 g01 = __ffma2_rn(make_float2(__uint_as_float(dv[i]), __uint_as_float(dv[i + 1])),
+                                  make_float2(fP, fP), make_float2(-d4.x, -d4.y));
+    const float2 g23 =
+        __ffma2_rn(make_float2(__uint_as_float(dv[i + 2]), __uint_as_float(dv[i + 3])),
+                   make_float2(fP, fP), make_float2(-d4.z, -d4.w));
+    const float2 d01 = __fmul2_rn(p01, g01);
+    const float2 d23 = __fmul2_rn(p23, g23);
+    amax = fmax3(fabsf(d01.x), fabsf(d01.y), amax);
+    amax = fmax3(fabsf(d23.x), fabsf(d23.y), amax);
+    dv[i] = __float_as_uint(d01.x);
+    dv[i + 1] = __float_as_uint(d01.y);
+    dv[i + 2] = __float_as_uint(d23.x);
+    dv[i + 3] = __float_as_uint(d23.y);
+    pw[i / 4] = cvt_e4m3x2(p01.x, p01.y) | (cvt_e4m3x2(p23.x, p23.y) << 16);
+  }
+  return amax;
 }
 
 template <int DIM>
@@ -92,15 +134,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap map_q,
                     const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v,
-                    const __grid_constant__ CUtensorMap map_do, const BwdParams prm) {
+                    const __grid_constant__ CUtensorMap map_do,
+                    const __grid_constant__ CUtensorMap map_dq, const BwdParams prm) {
   extern __shared__ uint8_t smem_raw[];
   BwdSmem<DIM>& sm = *reinterpret_cast<BwdSmem<DIM>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
   const int H = prm.H, T = prm.T;
-  const int item_idx = blockIdx.x / H;
-  const int h = blockIdx.x % H;
-  if (item_idx >= prm.wl_header[kHdrNBwd]) return;
+  const int h = blockIdx.x / prm.cap;          // head-major order
+  const int item_idx = blockIdx.x % prm.cap;
+  if (h >= H || item_idx >= prm.wl_header[kHdrNBwd]) return;  // uniform over the CTA
   const int4 item = prm.items[item_idx];
   // clamped: a malformed work list or offsets cannot index outside [0, T)
   const int doc = min(max(item.x, 0), prm.ndocs - 1);
@@ -118,9 +161,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(smem_u32(&sm.bar_qd_empty[i]), 1);
     }
     mbar_init(smem_u32(&sm.bar_s_full), 1);
-    mbar_init(smem_u32(&sm.bar_ds_full), kTile);
+    mbar_init(smem_u32(&sm.bar_ds_full), kComputeThreads);
     mbar_init(smem_u32(&sm.bar_dq_full), 1);
-    mbar_init(smem_u32(&sm.bar_s_free), kTile);
+    mbar_init(smem_u32(&sm.bar_s_free), kComputeThreads);
     mbar_init(smem_u32(&sm.bar_done), 1);
     sm.abort = 0;
     fence_barrier_init();
@@ -225,16 +268,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!mbar_wait(smem_u32(&sm.bar_done), 0)) sm.abort = 1;
     }
   } else if (warp >= 4) {
-    // ------------------------------------------------------------ compute group
+    // ------------------------------------------------------------ compute groups
+    const int g = (warp - 4) >> 2;   // 0: query columns 0..63, 1: 64..127
     const int quad = warp & 3;
     const int j = quad * 32 + lane;  // key row (S^T, dP^T, dV, dK) / query row (dQ_u)
     const int kj = k0 + j;
     const bool key_valid = kj < k1;
+    const bool issuer = (warp == 4 && lane == 0);
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const size_t hT = static_cast<size_t>(h) * T;
     const int ekj = key_valid ? static_cast<int>(prm.k_scales[hT + kj]) - 127 : 0;
     const int evj = key_valid ? static_cast<int>(prm.v_scales[hT + kj]) - 127 : 0;
-    const float rowf = pow2_or_zero(ekj);
+    const float rowf = pow2_or_zero(ekj) * prm.scale_log2;
     const float rowg = pow2_or_zero(evj);
     // E8M0 bytes of this key tile's 4 key blocks (B scale of dQ_u = dS K)
     uint32_t kword = 0;
@@ -244,10 +289,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       kword |= (kk < e ? static_cast<uint32_t>(prm.k_scales[hT + kk]) : 127u) << (8 * kb);
     }
     const float LOG2E = 1.4426950408889634f;
+    // Every compute thread runs the same sequence of named barriers whatever
+    // happens: a wait that times out only clears `ok`, which skips the work
+    // (never a barrier), so no thread can be left waiting at bar.sync.
     bool ok = true;
     for (int u = 0; u < nq; ++u) {
       const int q0 = k0 + u * kTile;
-      {
+      if (g == 0) {
         const int qi = q0 + j;
         const bool qv = qi < e;
         sm.nl[j] = qv ? 8.f - prm.lse[hT + qi] * LOG2E : -INFINITY;
@@ -257,44 +305,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           sm.dobyte[quad] = qv ? prm.do_scales[hT + qi] : 127u;
         }
       }
-      named_barrier_sync(1, kTile);
-      float fS[4], fP[4];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        fS[c] = rowf * prm.scale_log2 * pow2_or_zero(static_cast<int>(sm.qbyte[c]) - 127);
-        fP[c] = rowg * pow2_or_zero(static_cast<int>(sm.dobyte[c]) - 127);
-      }
-      if (!mbar_wait(smem_u32(&sm.bar_s_full), u & 1) || sm.abort) {
-        ok = false;
-        break;
-      }
+      named_barrier_sync(1, kComputeThreads);
+      ok = ok && !sm.abort && mbar_wait(smem_u32(&sm.bar_s_full), u & 1);
       tc_fence_after();
       uint8_t* pbrow = sm.pb + j * kTile;
       uint8_t* dsrow = sm.ds + j * kTile;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int cc = 0; cc < 2 && ok; ++cc) {
+        const int c = 2 * g + cc;  // 32-query block of this chunk
+        const float fS = rowf * pow2_or_zero(static_cast<int>(sm.qbyte[c]) - 127);
+        const float fP = rowg * pow2_or_zero(static_cast<int>(sm.dobyte[c]) - 127);
         uint32_t sv[32], dv[32];
         tmem_ld32(tmem + lane_off + kColSP + 32 * c, sv);
         tmem_ld32(tmem + lane_off + kColDP + 32 * c, dv);
         tmem_ld_wait();
+        uint32_t pw[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         float amax = 0.f;
-        uint32_t pw[8];
+        if (!key_valid) {
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float p8[2], d8[2];
-#pragma unroll
-          for (int w = 0; w < 2; ++w) {
-            const int col = 32 * c + i + w;
-            const bool vis = key_valid && (u > 0 || col >= j);
-            const float x = vis ? fmaf(__uint_as_float(sv[i + w]), fS[c], sm.nl[col]) : -INFINITY;
-            p8[w] = ex2_approx(x);
-            d8[w] = p8[w] * fmaf(__uint_as_float(dv[i + w]), fP[c], -sm.dd[col]);
-            amax = fmaxf(amax, fabsf(d8[w]));
-            dv[i + w] = __float_as_uint(d8[w]);
-          }
-          const uint32_t pc = cvt_e4m3x2(p8[0], p8[1]);
-          if ((i & 2) == 0) pw[i / 4] = pc;
-          else pw[i / 4] |= pc << 16;
+          for (int i = 0; i < 32; ++i) dv[i] = 0u;
+        } else if (u == 0) {
+          amax = bwd_chunk<true>(sv, dv, sm.nl + 32 * c, sm.dd + 32 * c, fS, fP, 32 * c, j, pw);
+        } else {
+          amax = bwd_chunk<false>(sv, dv, sm.nl + 32 * c, sm.dd + 32 * c, fS, fP, 32 * c, j, pw);
         }
         // one exponent per 32x32 block: this warp's 32 key rows x these 32 queries
 #pragma unroll
@@ -302,13 +335,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
         const int eb = max(roundup_exponent(amax) - 8, -127);  // exponent of dS = 2^-8 dS8
         const float inv = exp2i(-(eb + 8));
+        const float2 inv2 = make_float2(inv, inv);
         uint32_t dw[8];
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
-          dw[i / 4] = cvt_e4m3x2(__uint_as_float(dv[i]) * inv, __uint_as_float(dv[i + 1]) * inv) |
-                      (cvt_e4m3x2(__uint_as_float(dv[i + 2]) * inv,
-                                  __uint_as_float(dv[i + 3]) * inv)
-                       << 16);
+          const float2 a =
+              __fmul2_rn(make_float2(__uint_as_float(dv[i]), __uint_as_float(dv[i + 1])), inv2);
+          const float2 b =
+              __fmul2_rn(make_float2(__uint_as_float(dv[i + 2]), __uint_as_float(dv[i + 3])), inv2);
+          dw[i / 4] = cvt_e4m3x2(a.x, a.y) | (cvt_e4m3x2(b.x, b.y) << 16);
         }
         const int ch0 = (2 * c) ^ (j & 7), ch1 = (2 * c + 1) ^ (j & 7);
         *reinterpret_cast<uint4*>(pbrow + 16 * ch0) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
@@ -317,63 +352,86 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         *reinterpret_cast<uint4*>(dsrow + 16 * ch1) = make_uint4(dw[4], dw[5], dw[6], dw[7]);
         if (lane == 0) sm.eds[c][quad] = static_cast<uint32_t>(eb + 127);
       }
-      named_barrier_sync(1, kTile);
-      {
+      named_barrier_sync(1, kComputeThreads);
+      if (ok) {
         // block scales of the three products; every lane quadrant holds the
         // same words: column (base + m/32) of an A scale holds the 4 K-block
         // bytes of rows m/32*32 .. +31
-        uint32_t w0[8], w1[8], w2[8];
-        const uint32_t dow = sm.dobyte[0] | (sm.dobyte[1] << 8) | (sm.dobyte[2] << 16) |
-                             (sm.dobyte[3] << 24);
-        const uint32_t qw = sm.qbyte[0] | (sm.qbyte[1] << 8) | (sm.qbyte[2] << 16) |
-                            (sm.qbyte[3] << 24);
+        uint32_t w[8];
+        if (g == 0) {
+          const uint32_t dow = sm.dobyte[0] | (sm.dobyte[1] << 8) | (sm.dobyte[2] << 16) |
+                               (sm.dobyte[3] << 24);
+          const uint32_t qw = sm.qbyte[0] | (sm.qbyte[1] << 8) | (sm.qbyte[2] << 16) |
+                              (sm.qbyte[3] << 24);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          w0[i] = 0x7F7F7F7Fu;  // dV: A = P^b, scale 2^0
-          w0[4 + i] = dow;      // dV: B = dO, per query block
-          // dK: A = dS^T, row block = key block i, K blocks = query blocks
-          w1[i] = sm.eds[0][i] | (sm.eds[1][i] << 8) | (sm.eds[2][i] << 16) | (sm.eds[3][i] << 24);
-          w1[4 + i] = qw;       // dK: B = Q, per query block
-          // dQ: A = dS, row block = query block i, K blocks = key blocks
-          w2[i] = sm.eds[i][0] | (sm.eds[i][1] << 8) | (sm.eds[i][2] << 16) | (sm.eds[i][3] << 24);
-          w2[4 + i] = kword;    // dQ: B = K, per key block
+          for (int i = 0; i < 4; ++i) {
+            w[i] = 0x7F7F7F7Fu;  // dV: A = P^b, scale 2^0
+            w[4 + i] = dow;      // dV: B = dO, per query block
+          }
+          tmem_st8(tmem + lane_off + kSfDvA, w);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            // dK: A = dS^T, row block = key block i, K blocks = query blocks
+            w[i] = sm.eds[0][i] | (sm.eds[1][i] << 8) | (sm.eds[2][i] << 16) |
+                   (sm.eds[3][i] << 24);
+            w[4 + i] = qw;  // dK: B = Q, per query block
+          }
+          tmem_st8(tmem + lane_off + kSfDkA, w);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            // dQ: A = dS, row block = query block i, K blocks = key blocks
+            w[i] = sm.eds[i][0] | (sm.eds[i][1] << 8) | (sm.eds[i][2] << 16) |
+                   (sm.eds[i][3] << 24);
+            w[4 + i] = kword;  // dQ: B = K, per key block
+          }
+          tmem_st8(tmem + lane_off + kSfDqA, w);
         }
-        tmem_st8(tmem + lane_off + kSfDvA, w0);
-        tmem_st8(tmem + lane_off + kSfDkA, w1);
-        tmem_st8(tmem + lane_off + kSfDqA, w2);
         tmem_st_wait();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&sm.bar_ds_full));
       }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&sm.bar_ds_full));
-      if (!mbar_wait(smem_u32(&sm.bar_dq_full), u & 1) || sm.abort) {
-        ok = false;
-        break;
-      }
+      ok = ok && !sm.abort && mbar_wait(smem_u32(&sm.bar_dq_full), u & 1);
       tc_fence_after();
-      {
-        const int qi = q0 + j;  // TMEM lane j of dQ_u is query row j
-        float* dst = prm.dq_acc + (static_cast<size_t>(qi) * H + h) * DIM;
+      // the previous tile's reduce-adds must have read the staging buffer
+      if (issuer) bulk_wait_group_read0();
+      named_barrier_sync(1, kComputeThreads);
+      if (ok) {
+        const bool qv = q0 + j < e;  // TMEM lane j of dQ_u is query row j
 #pragma unroll 1
-        for (int c = 0; c < DIM / 32; ++c) {
+        for (int c = g * (DIM / 64); c < (g + 1) * (DIM / 64); ++c) {
           uint32_t v[32];
           tmem_ld32(tmem + lane_off + kColSP + 32 * c, v);
           tmem_ld_wait();
-          if (qi < e) {
+          float* row = sm.dqs[c] + j * 32;
 #pragma unroll
-            for (int i = 0; i < 32; i += 4)
-              red_add_v4(dst + 32 * c + i, __uint_as_float(v[i]) * prm.sm_scale,
-                         __uint_as_float(v[i + 1]) * prm.sm_scale,
-                         __uint_as_float(v[i + 2]) * prm.sm_scale,
-                         __uint_as_float(v[i + 3]) * prm.sm_scale);
+          for (int i = 0; i < 8; ++i) {
+            float4 f = make_float4(__uint_as_float(v[4 * i]) * prm.sm_scale,
+                                   __uint_as_float(v[4 * i + 1]) * prm.sm_scale,
+                                   __uint_as_float(v[4 * i + 2]) * prm.sm_scale,
+                                   __uint_as_float(v[4 * i + 3]) * prm.sm_scale);
+            if (!qv) f = make_float4(0.f, 0.f, 0.f, 0.f);  // rows of other documents add 0
+            *reinterpret_cast<float4*>(row + 4 * (i ^ (j & 7))) = f;
           }
         }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&sm.bar_s_free));
       }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&sm.bar_s_free));
+      if (!ok) sm.abort = 1;
+      named_barrier_sync(1, kComputeThreads);
+      if (issuer && !sm.abort) {
+#pragma unroll
+        for (int c = 0; c < DIM / 32; ++c)
+          tma_reduce_add_3d(&map_dq, smem_u32(sm.dqs[c]), 32 * c, h, q0);
+        bulk_commit_group();
+      }
     }
+    if (issuer) bulk_wait_group0();
     if (ok) {
-      // dV = 2^-8 acc, dK = scale * acc, written to the packed buffers
+      // dV = 2^-8 acc, dK = scale * acc, written to the packed buffers; the
+      // groups split the head dimension
       __nv_bfloat16* dvrow = prm.dv + (static_cast<size_t>(kj) * H + h) * DIM;
       __nv_bfloat16* dkrow = prm.dk + (static_cast<size_t>(kj) * H + h) * DIM;
 #pragma unroll 1
@@ -381,7 +439,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const float mul = which == 0 ? (1.f / 256.f) : prm.sm_scale;
         __nv_bfloat16* row = which == 0 ? dvrow : dkrow;
 #pragma unroll 1
-        for (int c = 0; c < DIM / 32; ++c) {
+        for (int c = g * (DIM / 64); c < (g + 1) * (DIM / 64); ++c) {
           uint32_t v[32];
           tmem_ld32(tmem + lane_off + kColDV + which * DIM + 32 * c, v);
           tmem_ld_wait();
@@ -431,12 +489,13 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
                          const float* lse, const int32_t* cu, int ndocs, int T, int H,
                          float softmax_scale, const void* wl, void* dq, void* dk, void* dv,
                          float* acc, int* status, cudaStream_t stream) {
-  CUtensorMap mq, mk, mv, mdo;
+  CUtensorMap mq, mk, mv, mdo, mdq;
   const CUtensorMapSwizzle swz = swizzle_for_row_bytes(DIM);
   if (!make_token_map(&mq, q->codes, T, H, DIM, kTile, swz) ||
       !make_token_map(&mk, k->codes, T, H, DIM, kTile, swz) ||
       !make_token_map(&mv, v->codes, T, H, DIM, kTile, swz) ||
-      !make_token_map(&mdo, dout->codes, T, H, DIM, kTile, swz))
+      !make_token_map(&mdo, dout->codes, T, H, DIM, kTile, swz) ||
+      !make_f32_token_map(&mdq, acc, T, H, DIM, kTile))
     return FLAMIA_ERR_CUDA;
   const WorklistLayout L = worklist_layout(T, ndocs);
   BwdParams prm;
@@ -449,12 +508,12 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
   prm.cu = cu;
   prm.wl_header = static_cast<const int*>(wl);
   prm.items = reinterpret_cast<const int4*>(static_cast<const char*>(wl) + L.off_bwd);
-  prm.dq_acc = acc;
   prm.dk = static_cast<__nv_bfloat16*>(dk);
   prm.dv = static_cast<__nv_bfloat16*>(dv);
   prm.T = T;
   prm.H = H;
   prm.ndocs = ndocs;
+  prm.cap = L.cap_bwd;
   prm.scale_log2 = softmax_scale * 1.4426950408889634f;
   prm.sm_scale = softmax_scale;
   prm.status = status;
@@ -466,7 +525,7 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
     return FLAMIA_ERR_CUDA;
   const long long grid = static_cast<long long>(L.cap_bwd) * H;
   attn_bwd_kernel<DIM>
-      <<<static_cast<unsigned>(grid), kBwdThreads, smem, stream>>>(mq, mk, mv, mdo, prm);
+      <<<static_cast<unsigned>(grid), kBwdThreads, smem, stream>>>(mq, mk, mv, mdo, mdq, prm);
   if (cudaGetLastError() != cudaSuccess) return FLAMIA_ERR_CUDA;
   const size_t n4 = n / 4;
   const int blocks = static_cast<int>(std::min<size_t>((n4 + 255) / 256, 152 * 16));

@@ -56,7 +56,7 @@ struct FwdParams {
   const int4* items;
   __nv_bfloat16* o;
   float* lse;
-  int T, H, ndocs;
+  int T, H, ndocs, cap;
   float scale_log2;  // softmax_scale * log2(e)
   int* status;
 };
@@ -70,6 +70,52 @@ __device__ __forceinline__ float pow2_or_zero(int k) {
   return k < -126 ? 0.f : exp2i(k);
 }
 
+// Maximum of the raw scores of a 32-column chunk; MASK keeps columns <= lim.
+template <bool MASK>
+__device__ __forceinline__ float chunk_max(const uint32_t (&v)[32], int lim) {
+  float a = -INFINITY, b = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < 32; i += 4) {
+    float x0 = __uint_as_float(v[i]), x1 = __uint_as_float(v[i + 1]);
+    float x2 = __uint_as_float(v[i + 2]), x3 = __uint_as_float(v[i + 3]);
+    if (MASK) {
+      if (i + 0 > lim) x0 = -INFINITY;
+      if (i + 1 > lim) x1 = -INFINITY;
+      if (i + 2 > lim) x2 = -INFINITY;
+      if (i + 3 > lim) x3 = -INFINITY;
+    }
+    a = fmax3(x0, x1, a);
+    b = fmax3(x2, x3, b);
+  }
+  return fmaxf(a, b);
+}
+
+// P8 = 2^8 exp2(x cf - m) of a 32-column chunk (masked columns give 0), their
+// running sum, and the E4M3 codes packed four per word.
+template <bool MASK>
+__device__ __forceinline__ void chunk_probs(const uint32_t (&v)[32], float cf, float moff,
+                                            int lim, float2& lsum, uint32_t (&w)[8]) {
+  const float2 cf2 = make_float2(cf, cf), mo2 = make_float2(-moff, -moff);
+#pragma unroll
+  for (int i = 0; i < 32; i += 4) {
+    float2 a = make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+    float2 b = make_float2(__uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+    if (MASK) {
+      if (i + 0 > lim) a.x = -INFINITY;
+      if (i + 1 > lim) a.y = -INFINITY;
+      if (i + 2 > lim) b.x = -INFINITY;
+      if (i + 3 > lim) b.y = -INFINITY;
+    }
+    a = __ffma2_rn(a, cf2, mo2);
+    b = __ffma2_rn(b, cf2, mo2);
+    const float2 pa = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+    const float2 pb = make_float2(ex2_approx(b.x), ex2_approx(b.y));
+    lsum = __fadd2_rn(lsum, pa);
+    lsum = __fadd2_rn(lsum, pb);
+    w[i / 4] = cvt_e4m3x2(pa.x, pa.y) | (cvt_e4m3x2(pb.x, pb.y) << 16);
+  }
+}
+
 template <int DIM>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
@@ -80,9 +126,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
   const int H = prm.H, T = prm.T;
-  const int item_idx = blockIdx.x / H;
-  const int h = blockIdx.x % H;
-  if (item_idx >= prm.wl_header[kHdrNFwd]) return;  // uniform over the CTA
+  const int h = blockIdx.x / prm.cap;  // head-major: K/V of one head are shared by a wave
+  const int item_idx = blockIdx.x % prm.cap;
+  if (h >= H || item_idx >= prm.wl_header[kHdrNFwd]) return;  // uniform over the CTA
   const int4 item = prm.items[item_idx];
   // clamped: a malformed work list or offsets cannot index outside [0, T)
   const int doc = min(max(item.x, 0), prm.ndocs - 1);
@@ -258,12 +304,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         uint32_t v[32];
         tmem_ld32(tS + 32 * c, v);
         tmem_ld_wait();
-        float cm = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float x = __uint_as_float(v[i]);
-          cm = (32 * c + i <= lim) ? fmaxf(cm, x) : cm;
-        }
+        const float cm = diag ? chunk_max<true>(v, lim - 32 * c) : chunk_max<false>(v, 0);
         mx = fmaxf(mx, cm * cf[c]);
       }
       float m_new = (mx == -INFINITY) ? m : fmaxf(m, ceilf(mx));
@@ -287,28 +328,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       m = m_new;
       const float moff = m - 8.f;  // P8 = 2^8 exp2(s - m)
       // pass 2: probabilities, row sum, E4M3 operand
+      float2 lsum = make_float2(0.f, 0.f);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
         tmem_ld32(tS + 32 * c, v);
         tmem_ld_wait();
         uint32_t w[8];
-#pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          float p4[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float x = (32 * c + i + u <= lim) ? __uint_as_float(v[i + u]) : -INFINITY;
-            p4[u] = ex2_approx(fmaf(x, cf[c], -moff));
-            l8 += p4[u];
-          }
-          w[i / 4] = cvt_e4m3x2(p4[0], p4[1]) | (cvt_e4m3x2(p4[2], p4[3]) << 16);
-        }
+        if (diag)
+          chunk_probs<true>(v, cf[c], moff, lim - 32 * c, lsum, w);
+        else
+          chunk_probs<false>(v, cf[c], moff, 0, lsum, w);
         // 32 bytes = 16-byte chunks 2c and 2c+1 of row r, 128B-swizzled
         const int ch0 = (2 * c) ^ (r & 7), ch1 = (2 * c + 1) ^ (r & 7);
         *reinterpret_cast<uint4*>(prow + 16 * ch0) = make_uint4(w[0], w[1], w[2], w[3]);
         *reinterpret_cast<uint4*>(prow + 16 * ch1) = make_uint4(w[4], w[5], w[6], w[7]);
       }
+      l8 += lsum.x + lsum.y;
       // scale factors of P^_t V_j: A (P^) 2^0 for every K block, B = V's block bytes
       const uint32_t sfw[8] = {0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu,
                                sfb, sfb, sfb, sfb};
@@ -383,6 +419,7 @@ flamia_status launch_fwd(const flamia_qtensor* q, const flamia_qtensor* k,
   prm.T = T;
   prm.H = H;
   prm.ndocs = ndocs;
+  prm.cap = L.cap_fwd;
   prm.scale_log2 = softmax_scale * 1.4426950408889634f;
   prm.status = status;
   const size_t smem = sizeof(FwdSmem<DIM>) + 1024;

@@ -3,8 +3,8 @@
 //
 // One CTA owns the 32-token blocks whose first token lies in a 128-token
 // segment of one head.  The rows of those blocks (at most 128 + 31) are read
-// once from HBM into registers, reduced to per-block maxima through shared
-// memory, and written back as E4M3 codes plus the per-token E8M0 scale table,
+// once from HBM by one TMA box into shared memory, reduced to per-block
+// maxima, and written back as E4M3 codes plus the per-token E8M0 scale table,
 // optionally with the NVFP4 copy and with D = dO . O fused in.
 // HBM-bound: 2 bytes read + 1 byte written per element.
 #include <cuda_bf16.h>
@@ -38,22 +38,35 @@ __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w <
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 template <int DIM>
-__global__ void __launch_bounds__(kQThreads, 2)
-    quantize_kernel(const uint4* __restrict__ x, int T, int H, const int32_t* __restrict__ cu,
-                    int ndocs, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
-                    uint8_t* __restrict__ f4codes, uint8_t* __restrict__ f4scales,
-                    const uint4* __restrict__ o, float* __restrict__ D, int* dev_status) {
+__global__ void __launch_bounds__(kQThreads)
+    quantize_kernel(const __grid_constant__ CUtensorMap map_x, int T, int H,
+                    const int32_t* __restrict__ cu, int ndocs, uint8_t* __restrict__ codes,
+                    uint8_t* __restrict__ scales, uint8_t* __restrict__ f4codes,
+                    uint8_t* __restrict__ f4scales, const uint4* __restrict__ o,
+                    float* __restrict__ D, int* dev_status) {
   constexpr int LPR = DIM / 8;    // lanes per row: 16 bytes (8 BF16) per lane
-  constexpr int RPI = 32 / LPR;   // rows per warp-wide load
-  constexpr int NLD = 32 / RPI;   // loads per 32 rows
+  constexpr int RPI = 32 / LPR;   // rows per warp-wide read
+  constexpr int NLD = 32 / RPI;   // reads per 32 rows
+  // the rows [seg0, seg0 + 160) of this head, staged by one TMA box
+  __shared__ alignas(128) uint4 s_x[kQThreads * LPR];
   __shared__ float s_rmax[kQThreads];
   __shared__ int s_exp[kQThreads];
   __shared__ int s_bounds[2];
+  __shared__ alignas(8) uint64_t s_bar;
 
   const int seg0 = blockIdx.x * kSeg;
   const int h = blockIdx.y;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    mbar_init(smem_u32(&s_bar), 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    mbar_arrive_expect_tx(smem_u32(&s_bar), kQThreads * DIM * 2);
+    tma_load_3d(smem_u32(s_x), &map_x, smem_u32(&s_bar), 0, h, seg0);
+  }
 
   // Light validation of cu_seqlens, spread over the CTAs of head 0.
   if (h == 0) {
@@ -80,17 +93,21 @@ __global__ void __launch_bounds__(kQThreads, 2)
   if (tid == min(kSeg, T - seg0) - 1) s_bounds[1] = be;
   __syncthreads();
   const int A = s_bounds[0], Bend = s_bounds[1];
+  // every thread waits for the staged rows (bounded: a timeout is reported)
+  if (!mbar_wait(smem_u32(&s_bar), 0)) {
+    if (tid == 0) report(dev_status, FLAMIA_DEV_TIMEOUT);
+    return;
+  }
 
-  // Phase 1: load the rows of this warp's 32 tokens, per-row maximum.
-  uint4 xr[NLD];
+  // Phase 1: per-row maximum of this warp's 32 tokens.
   const int chunk = lane % LPR;
 #pragma unroll
   for (int i = 0; i < NLD; ++i) {
-    const int tt = seg0 + warp * 32 + i * RPI + lane / LPR;
+    const int rl = warp * 32 + i * RPI + lane / LPR;  // row inside the staged box
+    const int tt = seg0 + rl;
     const bool valid = tt >= A && tt < Bend;
-    xr[i] = valid ? __ldg(x + (static_cast<size_t>(tt) * H + h) * LPR + chunk)
-                  : make_uint4(0, 0, 0, 0);
-    const uint32_t w[4] = {xr[i].x, xr[i].y, xr[i].z, xr[i].w};
+    const uint4 xv = s_x[rl * LPR + chunk];
+    const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
     float m = 0.f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16lo(w[j])), fabsf(bf16hi(w[j]))));
@@ -111,13 +128,15 @@ __global__ void __launch_bounds__(kQThreads, 2)
   __syncthreads();
 
   // Phase 3: codes (+ NVFP4 copy, + D) from the registers.
-#pragma unroll
+#pragma unroll 4
   for (int i = 0; i < NLD; ++i) {
-    const int tt = seg0 + warp * 32 + i * RPI + lane / LPR;
+    const int rl = warp * 32 + i * RPI + lane / LPR;
+    const int tt = seg0 + rl;
     const bool valid = tt >= A && tt < Bend;
-    const int e = valid ? s_exp[tt - seg0] : 0;
+    const int e = valid ? s_exp[rl] : 0;
     const float inv = exp2i(-e);  // e in [-127, 120]: 2^-e is a normal float
-    const uint32_t w[4] = {xr[i].x, xr[i].y, xr[i].z, xr[i].w};
+    const uint4 xv = s_x[rl * LPR + chunk];
+    const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
     float v[8];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -201,15 +220,30 @@ extern "C" flamia_status flamia_quantize_tokenblock(const void* x_bf16, int T, i
     f4s = out->nvfp4_scales;
   }
   int* status = dev_status;
+  // BF16 rows seen as 2-byte elements (dim, head, token); box = one head x 160 rows
+  CUtensorMap map;
+  {
+    EncodeTiledFn enc = get_encode_tiled();
+    if (!enc) return FLAMIA_ERR_CUDA;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                          static_cast<cuuint64_t>(T)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(d) * 2 * H};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(d), 1u, static_cast<cuuint32_t>(kQThreads)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(x_bf16), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return FLAMIA_ERR_CUDA;
+  }
   dim3 grid((T + kSeg - 1) / kSeg, H);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (d == 128)
     quantize_kernel<128><<<grid, kQThreads, 0, s>>>(
-        static_cast<const uint4*>(x_bf16), T, H, cu_seqlens, ndocs, out->codes, out->scales, f4c,
-        f4s, static_cast<const uint4*>(o_bf16), D, status);
+        map, T, H, cu_seqlens, ndocs, out->codes, out->scales, f4c, f4s,
+        static_cast<const uint4*>(o_bf16), D, status);
   else
     quantize_kernel<64><<<grid, kQThreads, 0, s>>>(
-        static_cast<const uint4*>(x_bf16), T, H, cu_seqlens, ndocs, out->codes, out->scales, f4c,
-        f4s, static_cast<const uint4*>(o_bf16), D, status);
+        map, T, H, cu_seqlens, ndocs, out->codes, out->scales, f4c, f4s,
+        static_cast<const uint4*>(o_bf16), D, status);
   return cudaGetLastError() == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
 }

@@ -34,6 +34,12 @@ def _generated(cu):
     return fwd, bwd
 
 
+def test_varlen_recipe_facts():
+    w = W.varlen65536()
+    assert w.ndocs == 30 and max(w.doc_lengths) == 15946 and w.sum_sq_len == 620059716
+    assert w.T == 65536 and min(w.doc_lengths) >= 1
+
+
 def test_invariants_on_the_varlen_workload():
     cu = list(W.varlen65536().cu_seqlens)
     fwd, bwd = O.build_worklist(cu)
