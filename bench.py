@@ -147,7 +147,7 @@ def run_ours(args, rank, world, local):
     x = W.make_inputs_bf16(w)
     xd = {n: t.to(dev) for n, t in x.items()}
     cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev)
-    call = fl.TrainingCall(w.T, w.H, w.d, cu, w.sm_scale, device=dev)
+    call = fl.TrainingCall(w.T, w.H, w.d, cu, w.sm_scale, nvfp4_qk=args.nvfp4, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -219,6 +219,8 @@ def run_ours(args, rank, world, local):
     barrier()
     e2e_ms = sum(a.elapsed_time(b) for a, b in ee)
 
+    breakdown = stage_breakdown(call, xd, stream, flush, w)
+
     flops = w.causal_flops()
     bwd_flops = 5.0 * w.H * w.d * w.sum_sq_len  # 10 * H * d * L^2 / 2
     res = {"total_ms": total_ms, "e2e_ms": e2e_ms, "bwd_ms": sum(bwd_ms) / len(bwd_ms),
@@ -248,6 +250,7 @@ def run_ours(args, rank, world, local):
         "dtype": "e4m3 (mxfp8 operands, f32 accumulate)",
         "data": "synthetic (seeded bf16 normals, 1% outlier channels x20)",
         "config": {"workload": w.name, "T": w.T, "H": w.H, "d": w.d, "docs": w.ndocs,
+                   "qk_product": "nvfp4 (mixed path)" if args.nvfp4 else "mxfp8",
                    "flops_per_step": flops, "l2": "flushed (256 MB write) before every step",
                    "parallelism": f"replicas x{world}"},
         "pct_of_fp8_peak": round(100.0 * value / world / pk["fp8_tflops"], 2),
@@ -259,11 +262,61 @@ def run_ours(args, rank, world, local):
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
+        "breakdown": breakdown,
         "clocks": res["clocks"],
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
     return line
+
+
+def stage_breakdown(call, xd, stream, flush, w, reps=10):
+    """Device time of each stage of the call (median of reps, L2 flushed before
+    each), the quantiser's HBM throughput and the call's working memory."""
+    import torch
+
+    from precision_causal_attention_block_gb300 import flamia as fl
+
+    stages = {
+        "quantize_q_ms": lambda: fl.flamia_quantize_tokenblock(xd["q"], call.cu, call.q,
+                                                               call.fmt_qk,
+                                                               dev_status=call.status),
+        "worklist_ms": lambda: fl.flamia_build_worklist(call.cu, call.T, call.wl,
+                                                        dev_status=call.status),
+        "fwd_ms": lambda: fl.flamia_attn_fwd(call.q, call.k, call.v, call.cu, call.T, call.H,
+                                             call.d, call.scale, call.wl, call.o, call.lse,
+                                             call.flags, dev_status=call.status),
+        "quantize_do_ms": lambda: fl.flamia_quantize_tokenblock(
+            xd["do"], call.cu, call.dout, fl.FORMAT_MXFP8, o=call.o, D=call.D,
+            dev_status=call.status),
+        "bwd_ms": lambda: fl.flamia_attn_bwd(call.q, call.k, call.v, call.dout, call.D,
+                                             call.lse, call.cu, call.T, call.H, call.d,
+                                             call.scale, call.wl, call.dq, call.dk, call.dv,
+                                             call.ws, call.flags, dev_status=call.status),
+    }
+    out = {}
+    for name, fn in stages.items():
+        times = []
+        for _ in range(reps):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b))
+        out[name] = round(statistics.median(times), 4)
+    elems = w.T * w.H * w.d
+    qbytes = elems * 3 + w.T * w.H + (elems // 2 + elems // 16 if call.fmt_qk else 0)
+    out["quantize_q_GBps"] = round(qbytes / (out["quantize_q_ms"] * 1e-3) / 1e9, 1)
+    out["worklist_us"] = round(out["worklist_ms"] * 1e3, 2)
+    bufs = [call.q.codes, call.q.scales, call.k.codes, call.k.scales, call.v.codes,
+            call.v.scales, call.dout.codes, call.dout.scales, call.wl, call.ws, call.o, call.lse,
+            call.D, call.dq, call.dk, call.dv]
+    bufs += [t for t in (call.q.nvfp4_codes, call.q.nvfp4_scales, call.k.nvfp4_codes,
+                         call.k.nvfp4_scales) if t is not None]
+    out["call_memory_GB"] = round(sum(t.numel() * t.element_size() for t in bufs) / 1e9, 3)
+    return out
 
 
 def cpu_baseline(w, budget_s=20.0):
@@ -329,6 +382,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="fixed4x4096")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--nvfp4", action="store_true",
+                    help="mixed path: QK^T from NVFP4 copies of Q and K (head dim 64)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

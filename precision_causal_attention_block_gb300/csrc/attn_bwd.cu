@@ -40,9 +40,10 @@ constexpr uint32_t kColSP = 0, kColDP = 128, kColDV = 256;
 constexpr uint32_t kSfDvA = 128, kSfDvB = 132, kSfDkA = 136, kSfDkB = 140, kSfDqA = 144,
                    kSfDqB = 148;
 
-template <int DIM>
+template <int DIM, bool NVF4>
 struct BwdSmem {
   static constexpr int kTileBytes = kTile * DIM;
+  static constexpr int kTile4Bytes = NVF4 ? kTile * DIM / 2 : 16;  // packed E2M1 tile
   alignas(1024) uint8_t k[kTileBytes];
   alignas(1024) uint8_t v[kTileBytes];
   alignas(1024) uint8_t q[kBStages][kTileBytes];
@@ -51,14 +52,18 @@ struct BwdSmem {
   alignas(1024) uint8_t ds[kTile * kTile];  // [key][query] E4M3, 128B-swizzled rows
   // dQ_u staging: DIM/32 boxes of [128 query rows][32 floats], 128B-swizzled
   alignas(1024) float dqs[DIM / 32][kTile * 32];
-  alignas(16) float nl[kTile];  // 8 - lse2 of each query column (-inf outside the document)
-  alignas(16) float dd[kTile];  // D of each query column (0 outside)
-  uint32_t qbyte[4], dobyte[4];  // E8M0 bytes of the 4 query blocks of Q and dO
+  alignas(NVF4 ? 1024 : 16) uint8_t k4[kTile4Bytes];
+  alignas(NVF4 ? 1024 : 16) uint8_t q4[kBStages][kTile4Bytes];
+  // per-query-tile inputs, double-buffered by tile parity (the next tile's are
+  // loaded while the current one is processed)
+  alignas(16) float nl[2][kTile];  // 8 - lse2 of each query column (-inf outside the document)
+  alignas(16) float dd[2][kTile];  // D of each query column (0 outside)
+  uint32_t qbyte[2][4], dobyte[2][4];  // E8M0 bytes of the 4 query blocks of Q and dO
   uint32_t eds[4][4];            // dS block bytes [query block][key block]
   uint64_t bar_kv;
   uint64_t bar_qd_full[kBStages];
   uint64_t bar_qd_empty[kBStages];
-  uint64_t bar_s_full, bar_ds_full, bar_dq_full, bar_s_free, bar_done;
+  uint64_t bar_s_full, bar_ds_full, bar_dq_full, bar_s_free, bar_done, bar_sf;
   uint32_t tmem_base;
   volatile int abort;
 };
@@ -68,6 +73,8 @@ struct BwdParams {
   const uint8_t* k_scales;
   const uint8_t* v_scales;
   const uint8_t* do_scales;
+  const uint32_t* q4_scales;  // NVFP4: 4 E4M3 scales per (token, head) as one word (d = 64)
+  const uint32_t* k4_scales;
   const float* D;
   const float* lse;
   const int32_t* cu;
@@ -129,15 +136,22 @@ __device__ __forceinline__ float bwd_chunk(const uint32_t (&sv)[32], uint32_t (&
   return amax;
 }
 
-template <int DIM>
+// NVFP4 score product (d = 64): tensor-memory columns of the block scales of
+// K (4 columns) and of Q_u (two 4-column buffers, by u parity).
+constexpr uint32_t kSfK4 = 384, kSfQ4 = 388;
+
+template <int DIM, bool NVF4>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap map_q,
                     const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v,
                     const __grid_constant__ CUtensorMap map_do,
-                    const __grid_constant__ CUtensorMap map_dq, const BwdParams prm) {
+                    const __grid_constant__ CUtensorMap map_dq,
+                    const __grid_constant__ CUtensorMap map_q4,
+                    const __grid_constant__ CUtensorMap map_k4, const BwdParams prm) {
+  static_assert(!NVF4 || DIM == 64, "the NVFP4 score product is built for head dim 64");
   extern __shared__ uint8_t smem_raw[];
-  BwdSmem<DIM>& sm = *reinterpret_cast<BwdSmem<DIM>*>(
+  BwdSmem<DIM, NVF4>& sm = *reinterpret_cast<BwdSmem<DIM, NVF4>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
   const int H = prm.H, T = prm.T;
@@ -165,6 +179,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(smem_u32(&sm.bar_dq_full), 1);
     mbar_init(smem_u32(&sm.bar_s_free), kComputeThreads);
     mbar_init(smem_u32(&sm.bar_done), 1);
+    mbar_init(smem_u32(&sm.bar_sf), kTile);
     sm.abort = 0;
     fence_barrier_init();
   }
@@ -176,7 +191,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-  constexpr uint32_t kTileBytes = BwdSmem<DIM>::kTileBytes;
+  constexpr uint32_t kTileBytes = BwdSmem<DIM, NVF4>::kTileBytes;
+  constexpr uint32_t kPairBytes = 2 * kTileBytes + (NVF4 ? BwdSmem<DIM, NVF4>::kTile4Bytes : 0);
   constexpr uint32_t lay = operand_layout<DIM>();
   constexpr uint32_t sbo = 8 * DIM;
 
@@ -188,9 +204,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       prefetch_tensormap(&map_v);
       prefetch_tensormap(&map_do);
       const uint32_t bkv = smem_u32(&sm.bar_kv);
-      mbar_arrive_expect_tx(bkv, 2 * kTileBytes);
+      mbar_arrive_expect_tx(bkv, kPairBytes);
       tma_load_3d(smem_u32(sm.k), &map_k, bkv, 0, h, k0);
       tma_load_3d(smem_u32(sm.v), &map_v, bkv, 0, h, k0);
+      if (NVF4) tma_load_3d(smem_u32(sm.k4), &map_k4, bkv, 0, h, k0);
       int issued = 0;
       for (int u = 0; u < nq; ++u) {
         const int st = u % kBStages;
@@ -202,9 +219,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
         }
         const uint32_t bf = smem_u32(&sm.bar_qd_full[st]);
-        mbar_arrive_expect_tx(bf, 2 * kTileBytes);
+        mbar_arrive_expect_tx(bf, kPairBytes);
         tma_load_3d(smem_u32(sm.q[st]), &map_q, bf, 0, h, k0 + u * kTile);
         tma_load_3d(smem_u32(sm.dout[st]), &map_do, bf, 0, h, k0 + u * kTile);
+        if (NVF4) tma_load_3d(smem_u32(sm.q4[st]), &map_q4, bf, 0, h, k0 + u * kTile);
         issued = u + 1;
       }
       bool ok = mbar_wait(bkv, 0);
@@ -217,6 +235,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (lane == 0) {
       const uint32_t id_s = idesc_f8(kTile, kTile, 0, 0);
       bool ok = mbar_wait(smem_u32(&sm.bar_kv), 0);
+      if (NVF4) ok = ok && mbar_wait(smem_u32(&sm.bar_sf), 0);
       const uint32_t ka = smem_u32(sm.k), va = smem_u32(sm.v);
       const uint32_t pba = smem_u32(sm.pb), dsa = smem_u32(sm.ds);
       for (int u = 0; ok && u < nq; ++u) {
@@ -228,10 +247,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         tc_fence_after();
         const uint32_t qa = smem_u32(sm.q[st]), da = smem_u32(sm.dout[st]);
+        if (NVF4) {
+          // S^T from the NVFP4 copies: packed E2M1 rows of 32 bytes, one K = 64 product
+          mma_nvf4(tmem + kColSP, smem_desc(smem_u32(sm.k4), 0, 256, kLayoutSW32),
+                   smem_desc(smem_u32(sm.q4[st]), 0, 256, kLayoutSW32), idesc_nvf4(kTile, kTile),
+                   tmem + kSfK4, tmem + kSfQ4 + 4 * (u & 1), 0);
+        } else {
 #pragma unroll
-        for (int ks = 0; ks < DIM / 32; ++ks)
-          mma_f8(tmem + kColSP, smem_desc(ka + 32 * ks, 0, sbo, lay),
-                 smem_desc(qa + 32 * ks, 0, sbo, lay), id_s, ks > 0);
+          for (int ks = 0; ks < DIM / 32; ++ks)
+            mma_f8(tmem + kColSP, smem_desc(ka + 32 * ks, 0, sbo, lay),
+                   smem_desc(qa + 32 * ks, 0, sbo, lay), id_s, ks > 0);
+        }
 #pragma unroll
         for (int ks = 0; ks < DIM / 32; ++ks)
           mma_f8(tmem + kColDP, smem_desc(va + 32 * ks, 0, sbo, lay),
@@ -277,7 +303,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const bool issuer = (warp == 4 && lane == 0);
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const size_t hT = static_cast<size_t>(h) * T;
-    const int ekj = key_valid ? static_cast<int>(prm.k_scales[hT + kj]) - 127 : 0;
+    const int ekj = (key_valid && !NVF4) ? static_cast<int>(prm.k_scales[hT + kj]) - 127 : 0;
     const int evj = key_valid ? static_cast<int>(prm.v_scales[hT + kj]) - 127 : 0;
     const float rowf = pow2_or_zero(ekj) * prm.scale_log2;
     const float rowg = pow2_or_zero(evj);
@@ -289,23 +315,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       kword |= (kk < e ? static_cast<uint32_t>(prm.k_scales[hT + kk]) : 127u) << (8 * kb);
     }
     const float LOG2E = 1.4426950408889634f;
+    // NVFP4 score product: block scales in tensor memory, one 32-bit word (4
+    // E4M3 scales) per row; column c + i of a lane quadrant holds row 32 i +
+    // lane (the same words in every quadrant).  Group 0 writes them.
+    auto write_sf4 = [&](const uint32_t* words, int tok0, uint32_t col) {
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        w[i] = words[static_cast<size_t>(min(tok0 + 32 * i + lane, T - 1)) * H + h];
+      tmem_st4(tmem + lane_off + col, w);
+    };
+    if (NVF4 && g == 0) {
+      write_sf4(prm.k4_scales, k0, kSfK4);
+      write_sf4(prm.q4_scales, k0, kSfQ4);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.bar_sf));
+    }
     // Every compute thread runs the same sequence of named barriers whatever
     // happens: a wait that times out only clears `ok`, which skips the work
     // (never a barrier), so no thread can be left waiting at bar.sync.
+    // group 0 loads the per-query inputs of tile u into buffer u & 1
+    auto load_query_inputs = [&](int u) {
+      const int qi = k0 + u * kTile + j;
+      const bool qv = qi < e;
+      const int b = u & 1;
+      sm.nl[b][j] = qv ? 8.f - prm.lse[hT + qi] * LOG2E : -INFINITY;
+      sm.dd[b][j] = qv ? prm.D[hT + qi] : 0.f;
+      if (lane == 0) {
+        sm.qbyte[b][quad] = qv ? prm.q_scales[hT + qi] : 127u;
+        sm.dobyte[b][quad] = qv ? prm.do_scales[hT + qi] : 127u;
+      }
+    };
+    if (g == 0) load_query_inputs(0);
+    named_barrier_sync(1, kComputeThreads);
     bool ok = true;
     for (int u = 0; u < nq; ++u) {
       const int q0 = k0 + u * kTile;
-      if (g == 0) {
-        const int qi = q0 + j;
-        const bool qv = qi < e;
-        sm.nl[j] = qv ? 8.f - prm.lse[hT + qi] * LOG2E : -INFINITY;
-        sm.dd[j] = qv ? prm.D[hT + qi] : 0.f;
-        if (lane == 0) {
-          sm.qbyte[quad] = qv ? prm.q_scales[hT + qi] : 127u;
-          sm.dobyte[quad] = qv ? prm.do_scales[hT + qi] : 127u;
-        }
-      }
-      named_barrier_sync(1, kComputeThreads);
+      const int ub = u & 1;
       ok = ok && !sm.abort && mbar_wait(smem_u32(&sm.bar_s_full), u & 1);
       tc_fence_after();
       uint8_t* pbrow = sm.pb + j * kTile;
@@ -313,8 +360,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll 1
       for (int cc = 0; cc < 2 && ok; ++cc) {
         const int c = 2 * g + cc;  // 32-query block of this chunk
-        const float fS = rowf * pow2_or_zero(static_cast<int>(sm.qbyte[c]) - 127);
-        const float fP = rowg * pow2_or_zero(static_cast<int>(sm.dobyte[c]) - 127);
+        const float fS =
+            NVF4 ? rowf : rowf * pow2_or_zero(static_cast<int>(sm.qbyte[ub][c]) - 127);
+        const float fP = rowg * pow2_or_zero(static_cast<int>(sm.dobyte[ub][c]) - 127);
         uint32_t sv[32], dv[32];
         tmem_ld32(tmem + lane_off + kColSP + 32 * c, sv);
         tmem_ld32(tmem + lane_off + kColDP + 32 * c, dv);
@@ -325,9 +373,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) dv[i] = 0u;
         } else if (u == 0) {
-          amax = bwd_chunk<true>(sv, dv, sm.nl + 32 * c, sm.dd + 32 * c, fS, fP, 32 * c, j, pw);
+          amax = bwd_chunk<true>(sv, dv, sm.nl[ub] + 32 * c, sm.dd[ub] + 32 * c, fS, fP, 32 * c,
+                                 j, pw);
         } else {
-          amax = bwd_chunk<false>(sv, dv, sm.nl + 32 * c, sm.dd + 32 * c, fS, fP, 32 * c, j, pw);
+          amax = bwd_chunk<false>(sv, dv, sm.nl[ub] + 32 * c, sm.dd[ub] + 32 * c, fS, fP,
+                                  32 * c, j, pw);
         }
         // one exponent per 32x32 block: this warp's 32 key rows x these 32 queries
 #pragma unroll
@@ -359,10 +409,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // bytes of rows m/32*32 .. +31
         uint32_t w[8];
         if (g == 0) {
-          const uint32_t dow = sm.dobyte[0] | (sm.dobyte[1] << 8) | (sm.dobyte[2] << 16) |
-                               (sm.dobyte[3] << 24);
-          const uint32_t qw = sm.qbyte[0] | (sm.qbyte[1] << 8) | (sm.qbyte[2] << 16) |
-                              (sm.qbyte[3] << 24);
+          const uint32_t* db = sm.dobyte[ub];
+          const uint32_t* qb = sm.qbyte[ub];
+          const uint32_t dow = db[0] | (db[1] << 8) | (db[2] << 16) | (db[3] << 24);
+          const uint32_t qw = qb[0] | (qb[1] << 8) | (qb[2] << 16) | (qb[3] << 24);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             w[i] = 0x7F7F7F7Fu;  // dV: A = P^b, scale 2^0
@@ -399,27 +449,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       named_barrier_sync(1, kComputeThreads);
       if (ok) {
         const bool qv = q0 + j < e;  // TMEM lane j of dQ_u is query row j
-#pragma unroll 1
-        for (int c = g * (DIM / 64); c < (g + 1) * (DIM / 64); ++c) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_off + kColSP + 32 * c, v);
-          tmem_ld_wait();
-          float* row = sm.dqs[c] + j * 32;
+        constexpr int kCh = DIM / 64;  // 32-column chunks of dQ_u per group
+        uint32_t v[kCh][32];
+#pragma unroll
+        for (int cc = 0; cc < kCh; ++cc) tmem_ld32(tmem + lane_off + kColSP + 32 * (g * kCh + cc), v[cc]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int cc = 0; cc < kCh; ++cc) {
+          float* row = sm.dqs[g * kCh + cc] + j * 32;
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            float4 f = make_float4(__uint_as_float(v[4 * i]) * prm.sm_scale,
-                                   __uint_as_float(v[4 * i + 1]) * prm.sm_scale,
-                                   __uint_as_float(v[4 * i + 2]) * prm.sm_scale,
-                                   __uint_as_float(v[4 * i + 3]) * prm.sm_scale);
+            float4 f = make_float4(__uint_as_float(v[cc][4 * i]) * prm.sm_scale,
+                                   __uint_as_float(v[cc][4 * i + 1]) * prm.sm_scale,
+                                   __uint_as_float(v[cc][4 * i + 2]) * prm.sm_scale,
+                                   __uint_as_float(v[cc][4 * i + 3]) * prm.sm_scale);
             if (!qv) f = make_float4(0.f, 0.f, 0.f, 0.f);  // rows of other documents add 0
             *reinterpret_cast<float4*>(row + 4 * (i ^ (j & 7))) = f;
           }
+        }
+        // NVFP4: stage the next query tile's block scales (the buffer of
+        // parity u + 1 was last read by S^T of tile u - 1, already complete)
+        if (NVF4 && g == 0 && u + 1 < nq) {
+          write_sf4(prm.q4_scales, q0 + kTile, kSfQ4 + 4 * ((u + 1) & 1));
+          tmem_st_wait();
         }
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(smem_u32(&sm.bar_s_free));
       }
       if (!ok) sm.abort = 1;
+      // the next tile's per-query inputs (its buffer was last read before this
+      // tile's second barrier)
+      if (g == 0 && u + 1 < nq) load_query_inputs(u + 1);
       named_barrier_sync(1, kComputeThreads);
       if (issuer && !sm.abort) {
 #pragma unroll
@@ -483,13 +544,13 @@ __global__ void dq_convert_kernel(const float4* __restrict__ acc, uint2* __restr
   }
 }
 
-template <int DIM>
+template <int DIM, bool NVF4>
 flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
                          const flamia_qtensor* v, const flamia_qtensor* dout, const float* D,
                          const float* lse, const int32_t* cu, int ndocs, int T, int H,
                          float softmax_scale, const void* wl, void* dq, void* dk, void* dv,
                          float* acc, int* status, cudaStream_t stream) {
-  CUtensorMap mq, mk, mv, mdo, mdq;
+  CUtensorMap mq, mk, mv, mdo, mdq, mq4, mk4;
   const CUtensorMapSwizzle swz = swizzle_for_row_bytes(DIM);
   if (!make_token_map(&mq, q->codes, T, H, DIM, kTile, swz) ||
       !make_token_map(&mk, k->codes, T, H, DIM, kTile, swz) ||
@@ -497,12 +558,22 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
       !make_token_map(&mdo, dout->codes, T, H, DIM, kTile, swz) ||
       !make_f32_token_map(&mdq, acc, T, H, DIM, kTile))
     return FLAMIA_ERR_CUDA;
+  if (NVF4) {
+    if (!make_token_map(&mq4, q->nvfp4_codes, T, H, DIM / 2, kTile, CU_TENSOR_MAP_SWIZZLE_32B) ||
+        !make_token_map(&mk4, k->nvfp4_codes, T, H, DIM / 2, kTile, CU_TENSOR_MAP_SWIZZLE_32B))
+      return FLAMIA_ERR_CUDA;
+  } else {
+    mq4 = mq;
+    mk4 = mk;
+  }
   const WorklistLayout L = worklist_layout(T, ndocs);
   BwdParams prm;
   prm.q_scales = q->scales;
   prm.k_scales = k->scales;
   prm.v_scales = v->scales;
   prm.do_scales = dout->scales;
+  prm.q4_scales = reinterpret_cast<const uint32_t*>(q->nvfp4_scales);
+  prm.k4_scales = reinterpret_cast<const uint32_t*>(k->nvfp4_scales);
   prm.D = D;
   prm.lse = lse;
   prm.cu = cu;
@@ -519,13 +590,13 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
   prm.status = status;
   const size_t n = static_cast<size_t>(T) * H * DIM;
   if (cudaMemsetAsync(acc, 0, n * sizeof(float), stream) != cudaSuccess) return FLAMIA_ERR_CUDA;
-  const size_t smem = sizeof(BwdSmem<DIM>) + 1024;
-  if (cudaFuncSetAttribute(attn_bwd_kernel<DIM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const size_t smem = sizeof(BwdSmem<DIM, NVF4>) + 1024;
+  if (cudaFuncSetAttribute(attn_bwd_kernel<DIM, NVF4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return FLAMIA_ERR_CUDA;
   const long long grid = static_cast<long long>(L.cap_bwd) * H;
-  attn_bwd_kernel<DIM>
-      <<<static_cast<unsigned>(grid), kBwdThreads, smem, stream>>>(mq, mk, mv, mdo, mdq, prm);
+  attn_bwd_kernel<DIM, NVF4><<<static_cast<unsigned>(grid), kBwdThreads, smem, stream>>>(
+      mq, mk, mv, mdo, mdq, mq4, mk4, prm);
   if (cudaGetLastError() != cudaSuccess) return FLAMIA_ERR_CUDA;
   const size_t n4 = n / 4;
   const int blocks = static_cast<int>(std::min<size_t>((n4 + 255) / 256, 152 * 16));
@@ -552,7 +623,9 @@ extern "C" flamia_status flamia_attn_bwd(const flamia_qtensor* q, const flamia_q
                                          void* dq_bf16, void* dk_bf16, void* dv_bf16, void* ws,
                                          size_t ws_bytes, int* dev_status, void* stream) {
   if (!supported_dim(d)) return FLAMIA_ERR_UNSUPPORTED;
-  if (flags != 0) return FLAMIA_ERR_UNSUPPORTED;
+  if ((flags & ~FLAMIA_FLAG_NVFP4_QK) != 0) return FLAMIA_ERR_UNSUPPORTED;
+  const bool nvf4 = (flags & FLAMIA_FLAG_NVFP4_QK) != 0;
+  if (nvf4 && d != 64) return FLAMIA_ERR_UNSUPPORTED;
   if (!valid_sizes(T, H, d, ndocs) || !q || !k || !v || !dout || !D || !lse || !cu_seqlens ||
       !wl || !dq_bf16 || !dk_bf16 || !dv_bf16 || !ws || !(softmax_scale > 0.f))
     return FLAMIA_ERR_INVALID_ARG;
@@ -564,11 +637,19 @@ extern "C" flamia_status flamia_attn_bwd(const flamia_qtensor* q, const flamia_q
       !aligned(dv_bf16, 16) || !aligned(ws, 256) || !aligned(wl, 256))
     return FLAMIA_ERR_INVALID_ARG;
   if (ws_bytes < flamia_bwd_workspace_bytes(T, H, d)) return FLAMIA_ERR_WORKSPACE;
+  if (nvf4 && (!q->nvfp4_codes || !q->nvfp4_scales || !k->nvfp4_codes || !k->nvfp4_scales ||
+               !aligned(q->nvfp4_codes, 16) || !aligned(k->nvfp4_codes, 16) ||
+               !aligned(q->nvfp4_scales, 4) || !aligned(k->nvfp4_scales, 4)))
+    return FLAMIA_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* acc = static_cast<float*>(ws);
-  return d == 128 ? launch_bwd<128>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H,
-                                    softmax_scale, wl, dq_bf16, dk_bf16, dv_bf16, acc, dev_status,
-                                    s)
-                  : launch_bwd<64>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, softmax_scale,
-                                   wl, dq_bf16, dk_bf16, dv_bf16, acc, dev_status, s);
+  if (nvf4)
+    return launch_bwd<64, true>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, softmax_scale,
+                                wl, dq_bf16, dk_bf16, dv_bf16, acc, dev_status, s);
+  return d == 128 ? launch_bwd<128, false>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H,
+                                           softmax_scale, wl, dq_bf16, dk_bf16, dv_bf16, acc,
+                                           dev_status, s)
+                  : launch_bwd<64, false>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H,
+                                          softmax_scale, wl, dq_bf16, dk_bf16, dv_bf16, acc,
+                                          dev_status, s);
 }

@@ -29,13 +29,17 @@ constexpr int kStages = 3;
 constexpr int kFwdThreads = 384;
 constexpr float kLn2 = 0.69314718055994530942f;
 
-template <int DIM>
+template <int DIM, bool NVF4>
 struct FwdSmem {
   static constexpr int kTileBytes = kTile * DIM;
+  static constexpr int kTile4Bytes = NVF4 ? kTile * DIM / 2 : 16;  // packed E2M1 tile
   alignas(1024) uint8_t q[2][kTileBytes];
   alignas(1024) uint8_t k[kStages][kTileBytes];
   alignas(1024) uint8_t v[kStages][kTileBytes];
   alignas(1024) uint8_t p[2][kTile * kTile];
+  alignas(NVF4 ? 1024 : 16) uint8_t q4[2][kTile4Bytes];
+  alignas(NVF4 ? 1024 : 16) uint8_t k4[kStages][kTile4Bytes];
+  uint64_t bar_sf;
   uint64_t bar_q;
   uint64_t bar_kv_full[kStages];
   uint64_t bar_kv_empty[kStages];
@@ -51,6 +55,8 @@ struct FwdParams {
   const uint8_t* q_scales;
   const uint8_t* k_scales;
   const uint8_t* v_scales;
+  const uint32_t* q4_scales;  // NVFP4: 4 E4M3 scales per (token, head) as one word (d = 64)
+  const uint32_t* k4_scales;
   const int32_t* cu;
   const int* wl_header;
   const int4* items;
@@ -116,13 +122,20 @@ __device__ __forceinline__ void chunk_probs(const uint32_t (&v)[32], float cf, f
   }
 }
 
-template <int DIM>
+// NVFP4 score product (d = 64): tensor-memory columns of the block scales of
+// Q_0, Q_1 (4 columns each) and of K_j (two 4-column buffers, by j parity).
+constexpr uint32_t kSfQ4 = 384, kSfK4 = 392;
+
+template <int DIM, bool NVF4>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
                     const __grid_constant__ CUtensorMap map_k,
-                    const __grid_constant__ CUtensorMap map_v, const FwdParams prm) {
+                    const __grid_constant__ CUtensorMap map_v,
+                    const __grid_constant__ CUtensorMap map_q4,
+                    const __grid_constant__ CUtensorMap map_k4, const FwdParams prm) {
+  static_assert(!NVF4 || DIM == 64, "the NVFP4 score product is built for head dim 64");
   extern __shared__ uint8_t smem_raw[];
-  FwdSmem<DIM>& sm = *reinterpret_cast<FwdSmem<DIM>*>(
+  FwdSmem<DIM, NVF4>& sm = *reinterpret_cast<FwdSmem<DIM, NVF4>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
   const int H = prm.H, T = prm.T;
@@ -155,6 +168,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(smem_u32(&sm.bar_o_full[t]), 1);
     }
     mbar_init(smem_u32(&sm.bar_done), 1);
+    mbar_init(smem_u32(&sm.bar_sf), 2 * kTile);
     sm.abort = 0;
     fence_barrier_init();
   }
@@ -166,7 +180,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-  constexpr uint32_t kTileBytes = FwdSmem<DIM>::kTileBytes;
+  constexpr uint32_t kTileBytes = FwdSmem<DIM, NVF4>::kTileBytes;
+  constexpr uint32_t kQBytes = kTileBytes + (NVF4 ? FwdSmem<DIM, NVF4>::kTile4Bytes : 0);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -175,9 +190,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       prefetch_tensormap(&map_k);
       prefetch_tensormap(&map_v);
       const uint32_t bq = smem_u32(&sm.bar_q);
-      mbar_arrive_expect_tx(bq, (valid1 ? 2 : 1) * kTileBytes);
+      mbar_arrive_expect_tx(bq, (valid1 ? 2 : 1) * kQBytes);
       tma_load_3d(smem_u32(sm.q[0]), &map_q, bq, 0, h, q0);
       if (valid1) tma_load_3d(smem_u32(sm.q[1]), &map_q, bq, 0, h, q0 + kTile);
+      if (NVF4) {
+        tma_load_3d(smem_u32(sm.q4[0]), &map_q4, bq, 0, h, q0);
+        if (valid1) tma_load_3d(smem_u32(sm.q4[1]), &map_q4, bq, 0, h, q0 + kTile);
+      }
       int issued = 0;
       for (int j = 0; j < nkv; ++j) {
         const int st = j % kStages;
@@ -189,9 +208,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
         }
         const uint32_t bf = smem_u32(&sm.bar_kv_full[st]);
-        mbar_arrive_expect_tx(bf, 2 * kTileBytes);
+        mbar_arrive_expect_tx(bf, kTileBytes + kQBytes);
         tma_load_3d(smem_u32(sm.k[st]), &map_k, bf, 0, h, s + j * kTile);
         tma_load_3d(smem_u32(sm.v[st]), &map_v, bf, 0, h, s + j * kTile);
+        if (NVF4) tma_load_3d(smem_u32(sm.k4[st]), &map_k4, bf, 0, h, s + j * kTile);
         issued = j + 1;
       }
       // Drain: every issued copy has landed before the CTA can exit.
@@ -207,13 +227,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       constexpr uint32_t sbo = 8 * DIM;  // 8 rows of one swizzle atom
       const uint32_t id_qk = idesc_f8(kTile, kTile, 0, 0);
       bool ok = mbar_wait(smem_u32(&sm.bar_q), 0) && mbar_wait(smem_u32(&sm.bar_kv_full[0]), 0);
+      if (NVF4) ok = ok && mbar_wait(smem_u32(&sm.bar_sf), 0);
       tc_fence_after();
-      auto issue_qk = [&](int t, int st) {
-        const uint32_t qa = smem_u32(sm.q[t]), ka = smem_u32(sm.k[st]);
+      // S_t = Q_t K_j^T into columns [128 t, 128 t + 128)
+      auto issue_qk = [&](int t, int jk) {
+        const int st = jk % kStages;
+        if (NVF4) {
+          // packed E2M1 rows of 32 bytes, 32-byte swizzle, one K = 64 product
+          mma_nvf4(tmem + t * kTile, smem_desc(smem_u32(sm.q4[t]), 0, 256, kLayoutSW32),
+                   smem_desc(smem_u32(sm.k4[st]), 0, 256, kLayoutSW32), idesc_nvf4(kTile, kTile),
+                   tmem + kSfQ4 + 4 * t, tmem + kSfK4 + 4 * (jk & 1), 0);
+        } else {
+          const uint32_t qa = smem_u32(sm.q[t]), ka = smem_u32(sm.k[st]);
 #pragma unroll
-        for (int ks = 0; ks < DIM / 32; ++ks)
-          mma_f8(tmem + t * kTile, smem_desc(qa + 32 * ks, 0, sbo, lay),
-                 smem_desc(ka + 32 * ks, 0, sbo, lay), id_qk, ks > 0);
+          for (int ks = 0; ks < DIM / 32; ++ks)
+            mma_f8(tmem + t * kTile, smem_desc(qa + 32 * ks, 0, sbo, lay),
+                   smem_desc(ka + 32 * ks, 0, sbo, lay), id_qk, ks > 0);
+        }
         tc_commit(smem_u32(&sm.bar_s_full[t]));
       };
       if (ok) {
@@ -248,7 +278,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               tc_fence_after();
               kv_ready = j + 2;
             }
-            issue_qk(t, (j + 1) % kStages);
+            issue_qk(t, j + 1);
           } else {
             tc_commit(smem_u32(&sm.bar_o_full[t]));
           }
@@ -273,11 +303,28 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t tS = tmem + lane_off + t * kTile;
     const uint32_t tO = tmem + lane_off + 256 + t * DIM;
     const size_t hT = static_cast<size_t>(h) * T;
-    const int eq = static_cast<int>(prm.q_scales[hT + min(qi, T - 1)]) - 127;
+    const int eq = NVF4 ? 0 : static_cast<int>(prm.q_scales[hT + min(qi, T - 1)]) - 127;
     const float c_row = prm.scale_log2 * pow2_or_zero(eq);
     float m = -INFINITY, l8 = 0.f;
     uint8_t* prow = sm.p[t] + r * kTile;
     bool ok = true;
+    // NVFP4 score product: its block scales live in tensor memory, one 32-bit
+    // word (4 E4M3 scales) per row; column c + i of this lane quadrant holds
+    // row 32 i + lane (the same words in every quadrant).
+    auto write_sf4 = [&](const uint32_t* words, int tok0, uint32_t col) {
+      uint32_t w[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        w[i] = words[static_cast<size_t>(min(tok0 + 32 * i + lane, T - 1)) * H + h];
+      tmem_st4(tmem + lane_off + col, w);
+    };
+    if (NVF4) {
+      write_sf4(prm.q4_scales, qa, kSfQ4 + 4 * t);
+      if (t == 0) write_sf4(prm.k4_scales, s, kSfK4);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.bar_sf));
+    }
     for (int j = 0; j < nt; ++j) {
       if (!mbar_wait(smem_u32(&sm.bar_s_full[t]), j & 1) || sm.abort) {
         ok = false;
@@ -290,21 +337,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
       for (int kb = 0; kb < 4; ++kb) {
         const int kk = k0 + 32 * kb;
-        const int ekb = kk < e ? static_cast<int>(prm.k_scales[hT + kk]) - 127 : 0;
+        const int ekb = (!NVF4 && kk < e) ? static_cast<int>(prm.k_scales[hT + kk]) - 127 : 0;
         cf[kb] = c_row * pow2_or_zero(ekb);
         const uint32_t vb = kk < e ? prm.v_scales[hT + kk] : 127u;
         sfb |= vb << (8 * kb);
       }
       const bool diag = (j == nt - 1);
       const int lim = diag ? min(r, e - 1 - k0) : kTile - 1;  // last visible column
+      // the whole 128-column row of S_t in registers: four loads, one wait
+      uint32_t sv[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, sv[c]);
+      tmem_ld_wait();
       // pass 1: row maximum in the log2 domain
       float mx = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tS + 32 * c, v);
-        tmem_ld_wait();
-        const float cm = diag ? chunk_max<true>(v, lim - 32 * c) : chunk_max<false>(v, 0);
+        const float cm = diag ? chunk_max<true>(sv[c], lim - 32 * c) : chunk_max<false>(sv[c], 0);
         mx = fmaxf(mx, cm * cf[c]);
       }
       float m_new = (mx == -INFINITY) ? m : fmaxf(m, ceilf(mx));
@@ -314,14 +363,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       l8 *= corr;
       if (__any_sync(0xffffffffu, need)) {
         // rescale this warp's O rows by the (exact power-of-two) correction
-#pragma unroll
-        for (int c = 0; c < DIM / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tO + 32 * c, v);
+        // in 8-column pieces: the row of S stays live in registers meanwhile
+#pragma unroll 1
+        for (int c = 0; c < DIM / 8; ++c) {
+          uint32_t v[8];
+          tmem_ld8(tO + 8 * c, v);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * corr);
-          tmem_st32(tO + 32 * c, v);
+          for (int i = 0; i < 8; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * corr);
+          tmem_st8(tO + 8 * c, v);
         }
         tmem_st_wait();
       }
@@ -331,14 +381,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       float2 lsum = make_float2(0.f, 0.f);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tS + 32 * c, v);
-        tmem_ld_wait();
         uint32_t w[8];
         if (diag)
-          chunk_probs<true>(v, cf[c], moff, lim - 32 * c, lsum, w);
+          chunk_probs<true>(sv[c], cf[c], moff, lim - 32 * c, lsum, w);
         else
-          chunk_probs<false>(v, cf[c], moff, 0, lsum, w);
+          chunk_probs<false>(sv[c], cf[c], moff, 0, lsum, w);
         // 32 bytes = 16-byte chunks 2c and 2c+1 of row r, 128B-swizzled
         const int ch0 = (2 * c) ^ (r & 7), ch1 = (2 * c + 1) ^ (r & 7);
         *reinterpret_cast<uint4*>(prow + 16 * ch0) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -349,6 +396,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const uint32_t sfw[8] = {0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu,
                                sfb, sfb, sfb, sfb};
       tmem_st8(tS, sfw);
+      // NVFP4: group 0 stages the block scales of the next key tile (the
+      // buffer of parity j + 1 was last read by the products of tile j - 1,
+      // which completed before S_0 of tile j)
+      if (NVF4 && t == 0 && j + 1 < nkv) write_sf4(prm.k4_scales, k0 + kTile, kSfK4 + 4 * ((j + 1) & 1));
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
@@ -361,7 +412,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tc_fence_after();
       const float inv = 1.f / l8;
       __nv_bfloat16* orow = prm.o + (static_cast<size_t>(qi) * H + h) * DIM;
-#pragma unroll
+#pragma unroll 1
       for (int c = 0; c < DIM / 32; ++c) {
         uint32_t v[32];
         tmem_ld32(tO + 32 * c, v);
@@ -395,22 +446,32 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
-template <int DIM>
+template <int DIM, bool NVF4>
 flamia_status launch_fwd(const flamia_qtensor* q, const flamia_qtensor* k,
                          const flamia_qtensor* v, const int32_t* cu, int ndocs, int T, int H,
                          float softmax_scale, const void* wl, void* o, float* lse, int* status,
                          cudaStream_t stream) {
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mq4, mk4;
   const CUtensorMapSwizzle swz = swizzle_for_row_bytes(DIM);
   if (!make_token_map(&mq, q->codes, T, H, DIM, kTile, swz) ||
       !make_token_map(&mk, k->codes, T, H, DIM, kTile, swz) ||
       !make_token_map(&mv, v->codes, T, H, DIM, kTile, swz))
     return FLAMIA_ERR_CUDA;
+  if (NVF4) {
+    if (!make_token_map(&mq4, q->nvfp4_codes, T, H, DIM / 2, kTile, CU_TENSOR_MAP_SWIZZLE_32B) ||
+        !make_token_map(&mk4, k->nvfp4_codes, T, H, DIM / 2, kTile, CU_TENSOR_MAP_SWIZZLE_32B))
+      return FLAMIA_ERR_CUDA;
+  } else {
+    mq4 = mq;
+    mk4 = mk;
+  }
   const WorklistLayout L = worklist_layout(T, ndocs);
   FwdParams prm;
   prm.q_scales = q->scales;
   prm.k_scales = k->scales;
   prm.v_scales = v->scales;
+  prm.q4_scales = reinterpret_cast<const uint32_t*>(q->nvfp4_scales);
+  prm.k4_scales = reinterpret_cast<const uint32_t*>(k->nvfp4_scales);
   prm.cu = cu;
   prm.wl_header = static_cast<const int*>(wl);
   prm.items = reinterpret_cast<const int4*>(static_cast<const char*>(wl) + L.off_fwd);
@@ -422,12 +483,14 @@ flamia_status launch_fwd(const flamia_qtensor* q, const flamia_qtensor* k,
   prm.cap = L.cap_fwd;
   prm.scale_log2 = softmax_scale * 1.4426950408889634f;
   prm.status = status;
-  const size_t smem = sizeof(FwdSmem<DIM>) + 1024;
-  if (cudaFuncSetAttribute(attn_fwd_kernel<DIM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const size_t smem = sizeof(FwdSmem<DIM, NVF4>) + 1024;
+  if (cudaFuncSetAttribute(attn_fwd_kernel<DIM, NVF4>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return FLAMIA_ERR_CUDA;
   const long long grid = static_cast<long long>(L.cap_fwd) * H;
-  attn_fwd_kernel<DIM><<<static_cast<unsigned>(grid), kFwdThreads, smem, stream>>>(mq, mk, mv, prm);
+  attn_fwd_kernel<DIM, NVF4>
+      <<<static_cast<unsigned>(grid), kFwdThreads, smem, stream>>>(mq, mk, mv, mq4, mk4, prm);
   return cudaGetLastError() == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
 }
 
@@ -442,7 +505,9 @@ extern "C" flamia_status flamia_attn_fwd(const flamia_qtensor* q, const flamia_q
                                          int flags, const void* wl, void* o_bf16, float* lse,
                                          int* dev_status, void* stream) {
   if (!supported_dim(d)) return FLAMIA_ERR_UNSUPPORTED;
-  if (flags != 0) return FLAMIA_ERR_UNSUPPORTED;
+  if ((flags & ~FLAMIA_FLAG_NVFP4_QK) != 0) return FLAMIA_ERR_UNSUPPORTED;
+  const bool nvf4 = (flags & FLAMIA_FLAG_NVFP4_QK) != 0;
+  if (nvf4 && d != 64) return FLAMIA_ERR_UNSUPPORTED;
   if (!valid_sizes(T, H, d, ndocs) || q == nullptr || k == nullptr || v == nullptr ||
       cu_seqlens == nullptr || wl == nullptr || o_bf16 == nullptr || lse == nullptr ||
       !(softmax_scale > 0.f))
@@ -452,9 +517,16 @@ extern "C" flamia_status flamia_attn_fwd(const flamia_qtensor* q, const flamia_q
   if (!aligned(q->codes, 16) || !aligned(k->codes, 16) || !aligned(v->codes, 16) ||
       !aligned(o_bf16, 16) || !aligned(wl, 256))
     return FLAMIA_ERR_INVALID_ARG;
+  if (nvf4 && (!q->nvfp4_codes || !q->nvfp4_scales || !k->nvfp4_codes || !k->nvfp4_scales ||
+               !aligned(q->nvfp4_codes, 16) || !aligned(k->nvfp4_codes, 16) ||
+               !aligned(q->nvfp4_scales, 4) || !aligned(k->nvfp4_scales, 4)))
+    return FLAMIA_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return d == 128 ? launch_fwd<128>(q, k, v, cu_seqlens, ndocs, T, H, softmax_scale, wl, o_bf16,
-                                    lse, dev_status, s)
-                  : launch_fwd<64>(q, k, v, cu_seqlens, ndocs, T, H, softmax_scale, wl, o_bf16,
-                                   lse, dev_status, s);
+  if (nvf4)
+    return launch_fwd<64, true>(q, k, v, cu_seqlens, ndocs, T, H, softmax_scale, wl, o_bf16, lse,
+                                dev_status, s);
+  return d == 128 ? launch_fwd<128, false>(q, k, v, cu_seqlens, ndocs, T, H, softmax_scale, wl,
+                                           o_bf16, lse, dev_status, s)
+                  : launch_fwd<64, false>(q, k, v, cu_seqlens, ndocs, T, H, softmax_scale, wl,
+                                          o_bf16, lse, dev_status, s);
 }

@@ -50,6 +50,7 @@ __global__ void __launch_bounds__(kQThreads)
   // the rows [seg0, seg0 + 160) of this head, staged by one TMA box
   __shared__ alignas(128) uint4 s_x[kQThreads * LPR];
   __shared__ float s_rmax[kQThreads];
+  __shared__ float s_pre[kQThreads], s_suf[kQThreads];
   __shared__ int s_exp[kQThreads];
   __shared__ int s_bounds[2];
   __shared__ alignas(8) uint64_t s_bar;
@@ -113,14 +114,40 @@ __global__ void __launch_bounds__(kQThreads)
     for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16lo(w[j])), fabsf(bf16hi(w[j]))));
 #pragma unroll
     for (int off = LPR / 2; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    if (chunk == 0 && valid) s_rmax[tt - seg0] = m;
+    if (chunk == 0) s_rmax[rl] = valid ? m : 0.f;
   }
   __syncthreads();
 
-  // Phase 2: block maximum -> round-up exponent -> dense per-token scale byte.
+  // Phase 2: block maxima by segmented scans over each warp's 32 rows (lane =
+  // row): prefix maxima restart at block starts, suffix maxima at block ends;
+  // a block's maximum is suffix(first row) max prefix(last row), whether or
+  // not it crosses a warp boundary.  Rows outside [A, Bend) stand alone.
+  {
+    const bool own = t >= A && t < Bend;
+    float pre = s_rmax[tid], suf = pre;
+    int hf = own ? (t == bs) : 1, tf = own ? (t == be - 1) : 1;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float yp = __shfl_up_sync(0xffffffffu, pre, off);
+      const int fp = __shfl_up_sync(0xffffffffu, hf, off);
+      const float ys = __shfl_down_sync(0xffffffffu, suf, off);
+      const int fs = __shfl_down_sync(0xffffffffu, tf, off);
+      if (lane >= off && !hf) {
+        pre = fmaxf(pre, yp);
+        hf |= fp;
+      }
+      if (lane + off < 32 && !tf) {
+        suf = fmaxf(suf, ys);
+        tf |= fs;
+      }
+    }
+    s_pre[tid] = pre;
+    s_suf[tid] = suf;
+  }
+  __syncthreads();
+  // block maximum -> round-up exponent -> dense per-token scale byte
   if (t >= A && t < Bend) {
-    float amax = 0.f;
-    for (int r = max(bs, A); r < min(be, Bend); ++r) amax = fmaxf(amax, s_rmax[r - seg0]);
+    const float amax = fmaxf(s_suf[max(bs, A) - seg0], s_pre[min(be, Bend) - 1 - seg0]);
     const int e = roundup_exponent(amax);
     s_exp[tid] = e;
     scales[static_cast<size_t>(h) * T + t] = static_cast<uint8_t>(e + 127);

@@ -170,3 +170,44 @@ def test_leakage_probe_bitwise(lib):
         d = (r.dq[:448].float() - dq0[:448].float()).abs().max().item()
         floor = max(4 * noise, 2.0 ** -7 * dq0[:448].float().abs().max().item())
         assert d <= floor, (name, d, noise)
+
+
+# ---------------------------------------------------------------- mixed NVFP4 path
+
+def test_nvfp4_mixed_ragged_small(lib):
+    """Scores from the NVFP4 copies of Q and K (review page sec. 3.1 mixed
+    path); every other product stays MXFP8."""
+    w = W.custom("ragged_nvfp4", [300, 1, 129, 0, 270, 33, 256], 2, 64, seed=17)
+    x = W.make_inputs_bf16(w)
+    call = run_call(w, x, nvfp4=True)
+    ref = O.attention(*[x[n].double().numpy() for n in NAMES], w.cu_seqlens, w.sm_scale,
+                      qk_format="nvfp4")
+    check_against(call, ref, slice(0, w.T), list(range(w.H)))
+
+
+def test_nvfp4_mixed_long131072_sampled(lib):
+    w = W.long131072()
+    x = W.make_inputs_bf16(w)
+    call = run_call(w, x, nvfp4=True)
+    h = 5
+    qz = O.Quantized(*[x[n][:, [h]].double().numpy() for n in NAMES], [0, w.T],
+                     qk_format="nvfp4")
+    nb = w.T // 32
+    res = O.sampled_rows(qz, 0, 0, w.sm_scale, qblocks=[0, 7, nb // 3, nb - 1],
+                         kblocks=[nb - 2, nb - 1])
+    for qb in res["O"]:
+        rows = slice(32 * qb, 32 * qb + 32)
+        compare(f"O[{qb}]", np64(call.o[rows][:, h]), res["O"][qb])
+        compare(f"dQ[{qb}]", np64(call.dq[rows][:, h]), res["dQ"][qb])
+    for kb in res["dK"]:
+        rows = slice(32 * kb, 32 * kb + 32)
+        compare(f"dK[{kb}]", np64(call.dk[rows][:, h]), res["dK"][kb])
+        compare(f"dV[{kb}]", np64(call.dv[rows][:, h]), res["dV"][kb])
+
+
+def test_nvfp4_flag_needs_head_dim_64(lib):
+    from precision_causal_attention_block_gb300 import flamia as fl
+    w = W.custom("d128", [64], 1, 128)
+    x = W.make_inputs_bf16(w)
+    with pytest.raises(RuntimeError, match="unsupported"):
+        run_call(w, x, nvfp4=True)
