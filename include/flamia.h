@@ -116,10 +116,16 @@ flamia_status flamia_quantize_tokenblock(const void* x_bf16, int T, int H, int d
  * Buffer layout (device, caller-owned, flamia_worklist_bytes(T, ndocs) bytes,
  * 256-byte aligned):
  *   int32 header[16]: [0] n_fwd, [1] n_bwd, [2] cap_fwd, [3] cap_bwd,
- *                     [4] max cost; the rest reserved.
+ *                     [4] max cost, [5] n_tile_fwd, [6] n_tile_bwd;
+ *                     [7], [8] used by the builder; the rest reserved.
  *   int32x4 fwd_items[cap_fwd] at byte 64: {doc, q_start, q_end, cost}
  *   int32x4 bwd_items[cap_bwd] after it:    {doc, k_start, k_end, cost}
+ *   int32x4 tile_fwd[cap_fwd], tile_bwd[cap_bwd] after them: the same two
+ *     lists without the items of documents of at most 32 tokens (n_tile_*
+ *     entries each); the tensor-core kernels walk these, while documents of
+ *     one 32-token block run on a CUDA-core kernel that needs no list.
  *   followed by the builder's scratch.
+ * Each array starts on a 256-byte boundary.
  * cap_fwd = T/256 + ndocs + 1, cap_bwd = T/128 + ndocs + 1 (upper bounds).
  */
 size_t flamia_worklist_bytes(int T, int ndocs);
@@ -136,8 +142,8 @@ flamia_status flamia_build_worklist(const int32_t* cu_seqlens, int ndocs, int T,
  * it is a convenience of this library's interface.
  *
  * Same inputs and the same output as flamia_build_worklist, but `wl` only
- * needs the header and the two item arrays (the layout above up to the end of
- * bwd_items; a flamia_worklist_bytes-sized buffer always suffices).  The
+ * needs the header and the four item arrays (the layout above up to the end
+ * of tile_bwd; a flamia_worklist_bytes-sized buffer always suffices).  The
  * builder's scratch lives in an 8 MiB array in the library's own device
  * memory, allocated on every GPU that loads the library and held until the
  * process exits.  The scratch grows mainly with the number of documents: any

@@ -1,11 +1,13 @@
 // Causal backward over token-block MXFP8 operands (FLAMIA review page, sec.
-// 1.2, 3.1, 3.3, 3.4 "Backward pass").
+// 1.2, 3.1, 3.3, 3.4 "Backward pass"): the entry point, and the kernel for
+// head dim 64 (MXFP8 or the mixed NVFP4 score product); head dim 128 runs the
+// pipelined kernel of attn_bwd128.cu.
 //
-// One CTA = one 128-key tile of a document x one head; it walks the 128-query
-// tiles of the same document from the diagonal to the document end.  CTAs are
-// ordered head-major (all key tiles of a head, longest first, then the next
-// head), so the Q / dO tiles and the dQ rows a wave of CTAs touches belong to
-// few heads and stay in L2.  Warp roles:
+// One work item = one 128-key tile of a document x one head; it walks the
+// 128-query tiles of the same document from the diagonal to the document end.
+// Items are ordered head-major (all key tiles of a head, longest first, then
+// the next head), so the Q / dO tiles and the dQ rows a wave of CTAs touches
+// belong to few heads and stay in L2.  Warp roles:
 //   warp 0       TMA producer: K, V once; Q, dO tiles through a 2-stage ring.
 //   warp 1       tensor-memory owner and single-thread tcgen05 MMA issuer.
 //   warps 4-7    compute group 0: query columns 0..63 of every tile
@@ -26,8 +28,7 @@
 // factors [128,256), dV [256,256+d), dK [256+d,256+2d).
 #include <cuda_bf16.h>
 
-#include "common.cuh"
-#include "ptx.cuh"
+#include "bwd_common.cuh"
 
 namespace flamia {
 namespace {
@@ -64,76 +65,14 @@ struct BwdSmem {
   uint64_t bar_qd_full[kBStages];
   uint64_t bar_qd_empty[kBStages];
   uint64_t bar_s_full, bar_ds_full, bar_dq_full, bar_s_free, bar_done, bar_sf;
+  uint64_t bar_kv_free, bar_acc_empty;
   uint32_t tmem_base;
   volatile int abort;
-};
-
-struct BwdParams {
-  const uint8_t* q_scales;
-  const uint8_t* k_scales;
-  const uint8_t* v_scales;
-  const uint8_t* do_scales;
-  const uint32_t* q4_scales;  // NVFP4: 4 E4M3 scales per (token, head) as one word (d = 64)
-  const uint32_t* k4_scales;
-  const float* D;
-  const float* lse;
-  const int32_t* cu;
-  const int* wl_header;
-  const int4* items;
-  __nv_bfloat16* dk;
-  __nv_bfloat16* dv;
-  int T, H, ndocs, cap;
-  float scale_log2;  // softmax_scale * log2(e)
-  float sm_scale;
-  int* status;
 };
 
 template <int DIM>
 __host__ __device__ constexpr uint32_t operand_layout() {
   return DIM == 128 ? kLayoutSW128 : kLayoutSW64;
-}
-
-__device__ __forceinline__ float pow2_or_zero(int k) { return k < -126 ? 0.f : exp2i(k); }
-
-// One 32-column chunk of a key row: P (operand codes), dS (float, 2^8-scaled)
-// and the chunk's |dS| maximum.  MASK: diagonal tile, query < key is masked.
-template <bool MASK>
-__device__ __forceinline__ float bwd_chunk(const uint32_t (&sv)[32], uint32_t (&dv)[32],
-                                           const float* nl, const float* dd, float fS, float fP,
-                                           int col0, int key, uint32_t (&pw)[8]) {
-  float amax = 0.f;
-#pragma unroll
-  for (int i = 0; i < 32; i += 4) {
-    const float4 n4 = *reinterpret_cast<const float4*>(nl + i);
-    const float4 d4 = *reinterpret_cast<const float4*>(dd + i);
-    float2 s01 = __ffma2_rn(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])),
-                            make_float2(fS, fS), make_float2(n4.x, n4.y));
-    float2 s23 = __ffma2_rn(make_float2(__uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3])),
-                            make_float2(fS, fS), make_float2(n4.z, n4.w));
-    if (MASK) {
-      if (col0 + i + 0 < key) s01.x = -INFINITY;
-      if (col0 + i + 1 < key) s01.y = -INFINITY;
-      if (col0 + i + 2 < key) s23.x = -INFINITY;
-      if (col0 + i + 3 < key) s23.y = -INFINITY;
-    }
-    const float2 p01 = make_float2(ex2_approx(s01.x), ex2_approx(s01.y));
-    const float2 p23 = make_float2(ex2_approx(s23.x), ex2_approx(s23.y));
-    const float2 g01 = __ffma2_rn(make_float2(__uint_as_float(dv[i]), __uint_as_float(dv[i + 1])),
-                                  make_float2(fP, fP), make_float2(-d4.x, -d4.y));
-    const float2 g23 =
-        __ffma2_rn(make_float2(__uint_as_float(dv[i + 2]), __uint_as_float(dv[i + 3])),
-                   make_float2(fP, fP), make_float2(-d4.z, -d4.w));
-    const float2 d01 = __fmul2_rn(p01, g01);
-    const float2 d23 = __fmul2_rn(p23, g23);
-    amax = fmax3(fabsf(d01.x), fabsf(d01.y), amax);
-    amax = fmax3(fabsf(d23.x), fabsf(d23.y), amax);
-    dv[i] = __float_as_uint(d01.x);
-    dv[i + 1] = __float_as_uint(d01.y);
-    dv[i + 2] = __float_as_uint(d23.x);
-    dv[i + 3] = __float_as_uint(d23.y);
-    pw[i / 4] = cvt_e4m3x2(p01.x, p01.y) | (cvt_e4m3x2(p23.x, p23.y) << 16);
-  }
-  return amax;
 }
 
 // NVFP4 score product (d = 64): tensor-memory columns of the block scales of
@@ -155,21 +94,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
   const int H = prm.H, T = prm.T;
-  const int h = blockIdx.x / prm.cap;          // head-major order
-  const int item_idx = blockIdx.x % prm.cap;
-  if (h >= H || item_idx >= prm.wl_header[kHdrNBwd]) return;  // uniform over the CTA
-  const int4 item = prm.items[item_idx];
-  // clamped: a malformed work list or offsets cannot index outside [0, T)
-  const int doc = min(max(item.x, 0), prm.ndocs - 1);
-  const int s = min(max(prm.cu[doc], 0), T);
-  const int e = min(max(prm.cu[doc + 1], s), T);
-  const int k0 = s + ((min(max(item.y, s), e) - s) & ~(kTile - 1));
-  const int k1 = min(max(item.z, k0), min(k0 + kTile, e));
-  const int nq = (e - k0 + kTile - 1) / kTile;  // query tiles from the diagonal to the end
-
+  const int n_items = min(prm.wl_header[kHdrTileBwd], prm.cap);
+  const int total = n_items * H;
+  if (static_cast<int>(blockIdx.x) >= total) return;  // uniform over the CTA
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&sm.bar_kv), 1);
+    mbar_init(smem_u32(&sm.bar_kv_free), 1);
     for (int i = 0; i < kBStages; ++i) {
       mbar_init(smem_u32(&sm.bar_qd_full[i]), 1);
       mbar_init(smem_u32(&sm.bar_qd_empty[i]), 1);
@@ -178,6 +109,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(smem_u32(&sm.bar_ds_full), kComputeThreads);
     mbar_init(smem_u32(&sm.bar_dq_full), 1);
     mbar_init(smem_u32(&sm.bar_s_free), kComputeThreads);
+    mbar_init(smem_u32(&sm.bar_acc_empty), kComputeThreads);
     mbar_init(smem_u32(&sm.bar_done), 1);
     mbar_init(smem_u32(&sm.bar_sf), kTile);
     sm.abort = 0;
@@ -204,29 +136,41 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       prefetch_tensormap(&map_v);
       prefetch_tensormap(&map_do);
       const uint32_t bkv = smem_u32(&sm.bar_kv);
-      mbar_arrive_expect_tx(bkv, kPairBytes);
-      tma_load_3d(smem_u32(sm.k), &map_k, bkv, 0, h, k0);
-      tma_load_3d(smem_u32(sm.v), &map_v, bkv, 0, h, k0);
-      if (NVF4) tma_load_3d(smem_u32(sm.k4), &map_k4, bkv, 0, h, k0);
-      int issued = 0;
-      for (int u = 0; u < nq; ++u) {
-        const int st = u % kBStages;
-        if (u >= kBStages) {
-          if (!mbar_wait(smem_u32(&sm.bar_qd_empty[st]), ((u / kBStages) - 1) & 1) ||
-              sm.abort) {
-            sm.abort = 1;
+      int nk = 0;  // items whose K / V were loaded
+      int uc = 0;  // query tiles loaded over all items
+      bool ok = true;
+      for (int round = 0; ok; ++round) {
+        const int idx = snake_index_b(round);
+        if (idx >= total) break;
+        BwdItem it;
+        if (!decode_bwd_item(prm, n_items, idx, it)) continue;
+        // the previous item's K / V are free once its last products are done
+        if (nk > 0 && (!mbar_wait(smem_u32(&sm.bar_kv_free), (nk - 1) & 1) || sm.abort)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(bkv, kPairBytes);
+        tma_load_3d(smem_u32(sm.k), &map_k, bkv, 0, it.h, it.k0);
+        tma_load_3d(smem_u32(sm.v), &map_v, bkv, 0, it.h, it.k0);
+        if (NVF4) tma_load_3d(smem_u32(sm.k4), &map_k4, bkv, 0, it.h, it.k0);
+        ++nk;
+        for (int u = 0; u < it.nq; ++u, ++uc) {
+          const int st = uc % kBStages;
+          if (uc >= kBStages &&
+              (!mbar_wait(smem_u32(&sm.bar_qd_empty[st]), ((uc / kBStages) - 1) & 1) ||
+               sm.abort)) {
+            ok = false;
             break;
           }
+          const uint32_t bf = smem_u32(&sm.bar_qd_full[st]);
+          mbar_arrive_expect_tx(bf, kPairBytes);
+          tma_load_3d(smem_u32(sm.q[st]), &map_q, bf, 0, it.h, it.k0 + u * kTile);
+          tma_load_3d(smem_u32(sm.dout[st]), &map_do, bf, 0, it.h, it.k0 + u * kTile);
+          if (NVF4) tma_load_3d(smem_u32(sm.q4[st]), &map_q4, bf, 0, it.h, it.k0 + u * kTile);
         }
-        const uint32_t bf = smem_u32(&sm.bar_qd_full[st]);
-        mbar_arrive_expect_tx(bf, kPairBytes);
-        tma_load_3d(smem_u32(sm.q[st]), &map_q, bf, 0, h, k0 + u * kTile);
-        tma_load_3d(smem_u32(sm.dout[st]), &map_do, bf, 0, h, k0 + u * kTile);
-        if (NVF4) tma_load_3d(smem_u32(sm.q4[st]), &map_q4, bf, 0, h, k0 + u * kTile);
-        issued = u + 1;
       }
-      bool ok = mbar_wait(bkv, 0);
-      for (int u = max(0, issued - kBStages); u < issued; ++u)
+      if (nk > 0) ok &= mbar_wait(bkv, (nk - 1) & 1);
+      for (int u = max(0, uc - kBStages); u < uc; ++u)
         ok &= mbar_wait(smem_u32(&sm.bar_qd_full[u % kBStages]), (u / kBStages) & 1);
       if (!ok) sm.abort = 1;
     }
@@ -234,60 +178,78 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t id_s = idesc_f8(kTile, kTile, 0, 0);
-      bool ok = mbar_wait(smem_u32(&sm.bar_kv), 0);
-      if (NVF4) ok = ok && mbar_wait(smem_u32(&sm.bar_sf), 0);
       const uint32_t ka = smem_u32(sm.k), va = smem_u32(sm.v);
       const uint32_t pba = smem_u32(sm.pb), dsa = smem_u32(sm.ds);
-      for (int u = 0; ok && u < nq; ++u) {
-        const int st = u % kBStages;
-        if (!mbar_wait(smem_u32(&sm.bar_qd_full[st]), (u / kBStages) & 1) ||
-            (u > 0 && !mbar_wait(smem_u32(&sm.bar_s_free), (u - 1) & 1)) || sm.abort) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t qa = smem_u32(sm.q[st]), da = smem_u32(sm.dout[st]);
-        if (NVF4) {
-          // S^T from the NVFP4 copies: packed E2M1 rows of 32 bytes, one K = 64 product
-          mma_nvf4(tmem + kColSP, smem_desc(smem_u32(sm.k4), 0, 256, kLayoutSW32),
-                   smem_desc(smem_u32(sm.q4[st]), 0, 256, kLayoutSW32), idesc_nvf4(kTile, kTile),
-                   tmem + kSfK4, tmem + kSfQ4 + 4 * (u & 1), 0);
-        } else {
+      int nk = 0, uc = 0;  // items and query tiles consumed so far
+      bool ok = true;
+      for (int round = 0; ok; ++round) {
+        const int idx = snake_index_b(round);
+        if (idx >= total) break;
+        BwdItem it;
+        if (!decode_bwd_item(prm, n_items, idx, it)) continue;
+        ok = mbar_wait(smem_u32(&sm.bar_kv), nk & 1);
+        if (NVF4) ok = ok && mbar_wait(smem_u32(&sm.bar_sf), nk & 1);
+        ++nk;
+        for (int u = 0; ok && u < it.nq; ++u, ++uc) {
+          const int st = uc % kBStages;
+          if (!mbar_wait(smem_u32(&sm.bar_qd_full[st]), (uc / kBStages) & 1) ||
+              (uc > 0 && !mbar_wait(smem_u32(&sm.bar_s_free), (uc - 1) & 1)) || sm.abort) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t qa = smem_u32(sm.q[st]), da = smem_u32(sm.dout[st]);
+          if (NVF4) {
+            // S^T from the NVFP4 copies: packed E2M1 rows of 32 bytes, one K = 64 product
+            mma_nvf4(tmem + kColSP, smem_desc(smem_u32(sm.k4), 0, 256, kLayoutSW32),
+                     smem_desc(smem_u32(sm.q4[st]), 0, 256, kLayoutSW32),
+                     idesc_nvf4(kTile, kTile), tmem + kSfK4, tmem + kSfQ4 + 4 * (uc & 1), 0);
+          } else {
+#pragma unroll
+            for (int ks = 0; ks < DIM / 32; ++ks)
+              mma_f8(tmem + kColSP, smem_desc(ka + 32 * ks, 0, sbo, lay),
+                     smem_desc(qa + 32 * ks, 0, sbo, lay), id_s, ks > 0);
+          }
 #pragma unroll
           for (int ks = 0; ks < DIM / 32; ++ks)
-            mma_f8(tmem + kColSP, smem_desc(ka + 32 * ks, 0, sbo, lay),
-                   smem_desc(qa + 32 * ks, 0, sbo, lay), id_s, ks > 0);
+            mma_f8(tmem + kColDP, smem_desc(va + 32 * ks, 0, sbo, lay),
+                   smem_desc(da + 32 * ks, 0, sbo, lay), id_s, ks > 0);
+          tc_commit(smem_u32(&sm.bar_s_full));
+          // dV / dK restart from zero on an item's first tile: the previous
+          // item's epilogue must have read them (its S^T / dP^T products could
+          // already run meanwhile)
+          if (!mbar_wait(smem_u32(&sm.bar_ds_full), uc & 1) ||
+              (u == 0 && nk > 1 && !mbar_wait(smem_u32(&sm.bar_acc_empty), (nk - 2) & 1)) ||
+              sm.abort) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // dV += P^b^T dO : A [key][query] K-major, B = dO tile read MN-major
+#pragma unroll
+          for (int kb = 0; kb < 4; ++kb)
+            mma_mxf8(tmem + kColDV, smem_desc(pba + 32 * kb, 0, 1024, kLayoutSW128),
+                     smem_desc(da + kb * 32 * DIM, 0, sbo, lay),
+                     idesc_mxf8(kTile, DIM, 0, 1, kb, kb), tmem + kSfDvA, tmem + kSfDvB,
+                     (u > 0 || kb > 0));
+          // dK += dS^T Q : A [key][query] K-major, B = Q tile read MN-major
+#pragma unroll
+          for (int kb = 0; kb < 4; ++kb)
+            mma_mxf8(tmem + kColDV + DIM, smem_desc(dsa + 32 * kb, 0, 1024, kLayoutSW128),
+                     smem_desc(qa + kb * 32 * DIM, 0, sbo, lay),
+                     idesc_mxf8(kTile, DIM, 0, 1, kb, kb), tmem + kSfDkA, tmem + kSfDkB,
+                     (u > 0 || kb > 0));
+          // dQ_u = dS K : A = the same dS bytes read MN-major (M = queries), B = K MN-major
+#pragma unroll
+          for (int kb = 0; kb < 4; ++kb)
+            mma_mxf8(tmem + kColSP, smem_desc(dsa + kb * 32 * kTile, 0, 1024, kLayoutSW128),
+                     smem_desc(ka + kb * 32 * DIM, 0, sbo, lay),
+                     idesc_mxf8(kTile, DIM, 1, 1, kb, kb), tmem + kSfDqA, tmem + kSfDqB, kb > 0);
+          tc_commit(smem_u32(&sm.bar_dq_full));
+          tc_commit(smem_u32(&sm.bar_qd_empty[st]));
         }
-#pragma unroll
-        for (int ks = 0; ks < DIM / 32; ++ks)
-          mma_f8(tmem + kColDP, smem_desc(va + 32 * ks, 0, sbo, lay),
-                 smem_desc(da + 32 * ks, 0, sbo, lay), id_s, ks > 0);
-        tc_commit(smem_u32(&sm.bar_s_full));
-        if (!mbar_wait(smem_u32(&sm.bar_ds_full), u & 1) || sm.abort) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        // dV += P^b^T dO : A [key][query] K-major, B = dO tile read MN-major
-#pragma unroll
-        for (int kb = 0; kb < 4; ++kb)
-          mma_mxf8(tmem + kColDV, smem_desc(pba + 32 * kb, 0, 1024, kLayoutSW128),
-                   smem_desc(da + kb * 32 * DIM, 0, sbo, lay), idesc_mxf8(kTile, DIM, 0, 1, kb, kb),
-                   tmem + kSfDvA, tmem + kSfDvB, (u > 0 || kb > 0));
-        // dK += dS^T Q : A [key][query] K-major, B = Q tile read MN-major
-#pragma unroll
-        for (int kb = 0; kb < 4; ++kb)
-          mma_mxf8(tmem + kColDV + DIM, smem_desc(dsa + 32 * kb, 0, 1024, kLayoutSW128),
-                   smem_desc(qa + kb * 32 * DIM, 0, sbo, lay), idesc_mxf8(kTile, DIM, 0, 1, kb, kb),
-                   tmem + kSfDkA, tmem + kSfDkB, (u > 0 || kb > 0));
-        // dQ_u = dS K : A = the same dS bytes read MN-major (M = queries), B = K MN-major
-#pragma unroll
-        for (int kb = 0; kb < 4; ++kb)
-          mma_mxf8(tmem + kColSP, smem_desc(dsa + kb * 32 * kTile, 0, 1024, kLayoutSW128),
-                   smem_desc(ka + kb * 32 * DIM, 0, sbo, lay), idesc_mxf8(kTile, DIM, 1, 1, kb, kb),
-                   tmem + kSfDqA, tmem + kSfDqB, kb > 0);
-        tc_commit(smem_u32(&sm.bar_dq_full));
-        tc_commit(smem_u32(&sm.bar_qd_empty[st]));
+        // this item's K / V may be replaced once its products are done
+        if (ok) tc_commit(smem_u32(&sm.bar_kv_free));
       }
       if (!ok) sm.abort = 1;
       tc_commit(smem_u32(&sm.bar_done));
@@ -298,229 +260,244 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int g = (warp - 4) >> 2;   // 0: query columns 0..63, 1: 64..127
     const int quad = warp & 3;
     const int j = quad * 32 + lane;  // key row (S^T, dP^T, dV, dK) / query row (dQ_u)
-    const int kj = k0 + j;
-    const bool key_valid = kj < k1;
     const bool issuer = (warp == 4 && lane == 0);
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const size_t hT = static_cast<size_t>(h) * T;
-    const int ekj = (key_valid && !NVF4) ? static_cast<int>(prm.k_scales[hT + kj]) - 127 : 0;
-    const int evj = key_valid ? static_cast<int>(prm.v_scales[hT + kj]) - 127 : 0;
-    const float rowf = pow2_or_zero(ekj) * prm.scale_log2;
-    const float rowg = pow2_or_zero(evj);
-    // E8M0 bytes of this key tile's 4 key blocks (B scale of dQ_u = dS K)
-    uint32_t kword = 0;
-#pragma unroll
-    for (int kb = 0; kb < 4; ++kb) {
-      const int kk = k0 + 32 * kb;
-      kword |= (kk < e ? static_cast<uint32_t>(prm.k_scales[hT + kk]) : 127u) << (8 * kb);
-    }
     const float LOG2E = 1.4426950408889634f;
-    // NVFP4 score product: block scales in tensor memory, one 32-bit word (4
-    // E4M3 scales) per row; column c + i of a lane quadrant holds row 32 i +
-    // lane (the same words in every quadrant).  Group 0 writes them.
-    auto write_sf4 = [&](const uint32_t* words, int tok0, uint32_t col) {
-      uint32_t w[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        w[i] = words[static_cast<size_t>(min(tok0 + 32 * i + lane, T - 1)) * H + h];
-      tmem_st4(tmem + lane_off + col, w);
-    };
-    if (NVF4 && g == 0) {
-      write_sf4(prm.k4_scales, k0, kSfK4);
-      write_sf4(prm.q4_scales, k0, kSfQ4);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&sm.bar_sf));
-    }
     // Every compute thread runs the same sequence of named barriers whatever
     // happens: a wait that times out only clears `ok`, which skips the work
     // (never a barrier), so no thread can be left waiting at bar.sync.
-    // group 0 loads the per-query inputs of tile u into buffer u & 1
-    auto load_query_inputs = [&](int u) {
-      const int qi = k0 + u * kTile + j;
-      const bool qv = qi < e;
-      const int b = u & 1;
-      sm.nl[b][j] = qv ? 8.f - prm.lse[hT + qi] * LOG2E : -INFINITY;
-      sm.dd[b][j] = qv ? prm.D[hT + qi] : 0.f;
-      if (lane == 0) {
-        sm.qbyte[b][quad] = qv ? prm.q_scales[hT + qi] : 127u;
-        sm.dobyte[b][quad] = qv ? prm.do_scales[hT + qi] : 127u;
-      }
-    };
-    if (g == 0) load_query_inputs(0);
-    named_barrier_sync(1, kComputeThreads);
     bool ok = true;
-    for (int u = 0; u < nq; ++u) {
-      const int q0 = k0 + u * kTile;
-      const int ub = u & 1;
-      ok = ok && !sm.abort && mbar_wait(smem_u32(&sm.bar_s_full), u & 1);
-      tc_fence_after();
-      uint8_t* pbrow = sm.pb + j * kTile;
-      uint8_t* dsrow = sm.ds + j * kTile;
-#pragma unroll 1
-      for (int cc = 0; cc < 2 && ok; ++cc) {
-        const int c = 2 * g + cc;  // 32-query block of this chunk
-        const float fS =
-            NVF4 ? rowf : rowf * pow2_or_zero(static_cast<int>(sm.qbyte[ub][c]) - 127);
-        const float fP = rowg * pow2_or_zero(static_cast<int>(sm.dobyte[ub][c]) - 127);
-        uint32_t sv[32], dv[32];
-        tmem_ld32(tmem + lane_off + kColSP + 32 * c, sv);
-        tmem_ld32(tmem + lane_off + kColDP + 32 * c, dv);
-        tmem_ld_wait();
-        uint32_t pw[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        float amax = 0.f;
-        if (!key_valid) {
+    int uc = 0;  // query tiles processed over all items (phase and buffer parity)
+    for (int round = 0;; ++round) {
+      const int idx = snake_index_b(round);
+      if (idx >= total) break;
+      BwdItem it;
+      if (!decode_bwd_item(prm, n_items, idx, it)) continue;
+      const int h = it.h, e = it.e, k0 = it.k0, nq = it.nq;
+      const int kj = k0 + j;
+      const bool key_valid = kj < it.k1;
+      const size_t hT = static_cast<size_t>(h) * T;
+      const int ekj = (key_valid && !NVF4) ? static_cast<int>(prm.k_scales[hT + kj]) - 127 : 0;
+      const int evj = key_valid ? static_cast<int>(prm.v_scales[hT + kj]) - 127 : 0;
+      const float rowf = pow2_or_zero(ekj) * prm.scale_log2;
+      const float rowg = pow2_or_zero(evj);
+      // E8M0 bytes of this key tile's 4 key blocks (B scale of dQ_u = dS K)
+      uint32_t kword = 0;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) dv[i] = 0u;
-        } else if (u == 0) {
-          amax = bwd_chunk<true>(sv, dv, sm.nl[ub] + 32 * c, sm.dd[ub] + 32 * c, fS, fP, 32 * c,
-                                 j, pw);
-        } else {
-          amax = bwd_chunk<false>(sv, dv, sm.nl[ub] + 32 * c, sm.dd[ub] + 32 * c, fS, fP,
-                                  32 * c, j, pw);
-        }
-        // one exponent per 32x32 block: this warp's 32 key rows x these 32 queries
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-        const int eb = max(roundup_exponent(amax) - 8, -127);  // exponent of dS = 2^-8 dS8
-        const float inv = exp2i(-(eb + 8));
-        const float2 inv2 = make_float2(inv, inv);
-        uint32_t dw[8];
-#pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          const float2 a =
-              __fmul2_rn(make_float2(__uint_as_float(dv[i]), __uint_as_float(dv[i + 1])), inv2);
-          const float2 b =
-              __fmul2_rn(make_float2(__uint_as_float(dv[i + 2]), __uint_as_float(dv[i + 3])), inv2);
-          dw[i / 4] = cvt_e4m3x2(a.x, a.y) | (cvt_e4m3x2(b.x, b.y) << 16);
-        }
-        const int ch0 = (2 * c) ^ (j & 7), ch1 = (2 * c + 1) ^ (j & 7);
-        *reinterpret_cast<uint4*>(pbrow + 16 * ch0) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-        *reinterpret_cast<uint4*>(pbrow + 16 * ch1) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
-        *reinterpret_cast<uint4*>(dsrow + 16 * ch0) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
-        *reinterpret_cast<uint4*>(dsrow + 16 * ch1) = make_uint4(dw[4], dw[5], dw[6], dw[7]);
-        if (lane == 0) sm.eds[c][quad] = static_cast<uint32_t>(eb + 127);
+      for (int kb = 0; kb < 4; ++kb) {
+        const int kk = k0 + 32 * kb;
+        kword |= (kk < e ? static_cast<uint32_t>(prm.k_scales[hT + kk]) : 127u) << (8 * kb);
       }
-      named_barrier_sync(1, kComputeThreads);
-      if (ok) {
-        // block scales of the three products; every lane quadrant holds the
-        // same words: column (base + m/32) of an A scale holds the 4 K-block
-        // bytes of rows m/32*32 .. +31
-        uint32_t w[8];
-        if (g == 0) {
-          const uint32_t* db = sm.dobyte[ub];
-          const uint32_t* qb = sm.qbyte[ub];
-          const uint32_t dow = db[0] | (db[1] << 8) | (db[2] << 16) | (db[3] << 24);
-          const uint32_t qw = qb[0] | (qb[1] << 8) | (qb[2] << 16) | (qb[3] << 24);
+      // NVFP4 score product: block scales in tensor memory, one 32-bit word (4
+      // E4M3 scales) per row; column c + i of a lane quadrant holds row 32 i +
+      // lane (the same words in every quadrant).  Group 0 writes them.
+      auto write_sf4 = [&](const uint32_t* words, int tok0, uint32_t col) {
+        uint32_t w[4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            w[i] = 0x7F7F7F7Fu;  // dV: A = P^b, scale 2^0
-            w[4 + i] = dow;      // dV: B = dO, per query block
-          }
-          tmem_st8(tmem + lane_off + kSfDvA, w);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            // dK: A = dS^T, row block = key block i, K blocks = query blocks
-            w[i] = sm.eds[0][i] | (sm.eds[1][i] << 8) | (sm.eds[2][i] << 16) |
-                   (sm.eds[3][i] << 24);
-            w[4 + i] = qw;  // dK: B = Q, per query block
-          }
-          tmem_st8(tmem + lane_off + kSfDkA, w);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            // dQ: A = dS, row block = query block i, K blocks = key blocks
-            w[i] = sm.eds[i][0] | (sm.eds[i][1] << 8) | (sm.eds[i][2] << 16) |
-                   (sm.eds[i][3] << 24);
-            w[4 + i] = kword;  // dQ: B = K, per key block
-          }
-          tmem_st8(tmem + lane_off + kSfDqA, w);
-        }
+        for (int i = 0; i < 4; ++i)
+          w[i] = words[static_cast<size_t>(min(tok0 + 32 * i + lane, T - 1)) * H + h];
+        tmem_st4(tmem + lane_off + col, w);
+      };
+      if (NVF4 && g == 0) {
+        // the previous item's products completed before its last dQ was read
+        write_sf4(prm.k4_scales, k0, kSfK4);
+        write_sf4(prm.q4_scales, k0, kSfQ4 + 4 * (uc & 1));
         tmem_st_wait();
-        fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(smem_u32(&sm.bar_ds_full));
+        mbar_arrive(smem_u32(&sm.bar_sf));
       }
-      ok = ok && !sm.abort && mbar_wait(smem_u32(&sm.bar_dq_full), u & 1);
-      tc_fence_after();
-      // the previous tile's reduce-adds must have read the staging buffer
-      if (issuer) bulk_wait_group_read0();
+      // group 0 loads the per-query inputs of the item's tile u into buffer
+      // (global tile index) & 1
+      auto load_query_inputs = [&](int u, int ug) {
+        const int qi = k0 + u * kTile + j;
+        const bool qv = qi < e;
+        const int b = ug & 1;
+        sm.nl[b][j] = qv ? 8.f - prm.lse[hT + qi] * LOG2E : -INFINITY;
+        sm.dd[b][j] = qv ? prm.D[hT + qi] : 0.f;
+        if (lane == 0) {
+          sm.qbyte[b][quad] = qv ? prm.q_scales[hT + qi] : 127u;
+          sm.dobyte[b][quad] = qv ? prm.do_scales[hT + qi] : 127u;
+        }
+      };
+      if (g == 0) load_query_inputs(0, uc);
       named_barrier_sync(1, kComputeThreads);
+      for (int u = 0; u < nq; ++u, ++uc) {
+        const int q0 = k0 + u * kTile;
+        const int ub = uc & 1;
+        ok = ok && !sm.abort && mbar_wait(smem_u32(&sm.bar_s_full), uc & 1);
+        tc_fence_after();
+        uint8_t* pbrow = sm.pb + j * kTile;
+        uint8_t* dsrow = sm.ds + j * kTile;
+#pragma unroll 1
+        for (int cc = 0; cc < 2 && ok; ++cc) {
+          const int c = 2 * g + cc;  // 32-query block of this chunk
+          const float fS =
+              NVF4 ? rowf : rowf * pow2_or_zero(static_cast<int>(sm.qbyte[ub][c]) - 127);
+          const float fP = rowg * pow2_or_zero(static_cast<int>(sm.dobyte[ub][c]) - 127);
+          uint32_t sv[32], dv[32];
+          tmem_ld32(tmem + lane_off + kColSP + 32 * c, sv);
+          tmem_ld32(tmem + lane_off + kColDP + 32 * c, dv);
+          tmem_ld_wait();
+          uint32_t pw[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+          float amax = 0.f;
+          if (!key_valid) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) dv[i] = 0u;
+          } else if (u == 0) {
+            amax = bwd_chunk<true>(sv, dv, sm.nl[ub] + 32 * c, sm.dd[ub] + 32 * c, fS, fP,
+                                   32 * c, j, pw);
+          } else {
+            amax = bwd_chunk<false>(sv, dv, sm.nl[ub] + 32 * c, sm.dd[ub] + 32 * c, fS, fP,
+                                    32 * c, j, pw);
+          }
+          // one exponent per 32x32 block: this warp's 32 key rows x these 32 queries
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+          const int eb = max(roundup_exponent(amax) - 8, -127);  // exponent of dS = 2^-8 dS8
+          const float inv = exp2i(-(eb + 8));
+          const float2 inv2 = make_float2(inv, inv);
+          uint32_t dw[8];
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const float2 a = __fmul2_rn(
+                make_float2(__uint_as_float(dv[i]), __uint_as_float(dv[i + 1])), inv2);
+            const float2 b = __fmul2_rn(
+                make_float2(__uint_as_float(dv[i + 2]), __uint_as_float(dv[i + 3])), inv2);
+            dw[i / 4] = cvt_e4m3x2(a.x, a.y) | (cvt_e4m3x2(b.x, b.y) << 16);
+          }
+          const int ch0 = (2 * c) ^ (j & 7), ch1 = (2 * c + 1) ^ (j & 7);
+          *reinterpret_cast<uint4*>(pbrow + 16 * ch0) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+          *reinterpret_cast<uint4*>(pbrow + 16 * ch1) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
+          *reinterpret_cast<uint4*>(dsrow + 16 * ch0) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
+          *reinterpret_cast<uint4*>(dsrow + 16 * ch1) = make_uint4(dw[4], dw[5], dw[6], dw[7]);
+          if (lane == 0) sm.eds[c][quad] = static_cast<uint32_t>(eb + 127);
+        }
+        named_barrier_sync(1, kComputeThreads);
+        if (ok) {
+          // block scales of the three products; every lane quadrant holds the
+          // same words: column (base + m/32) of an A scale holds the 4 K-block
+          // bytes of rows m/32*32 .. +31
+          uint32_t w[8];
+          if (g == 0) {
+            const uint32_t* db = sm.dobyte[ub];
+            const uint32_t* qb = sm.qbyte[ub];
+            const uint32_t dow = db[0] | (db[1] << 8) | (db[2] << 16) | (db[3] << 24);
+            const uint32_t qw = qb[0] | (qb[1] << 8) | (qb[2] << 16) | (qb[3] << 24);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              w[i] = 0x7F7F7F7Fu;  // dV: A = P^b, scale 2^0
+              w[4 + i] = dow;      // dV: B = dO, per query block
+            }
+            tmem_st8(tmem + lane_off + kSfDvA, w);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              // dK: A = dS^T, row block = key block i, K blocks = query blocks
+              w[i] = sm.eds[0][i] | (sm.eds[1][i] << 8) | (sm.eds[2][i] << 16) |
+                     (sm.eds[3][i] << 24);
+              w[4 + i] = qw;  // dK: B = Q, per query block
+            }
+            tmem_st8(tmem + lane_off + kSfDkA, w);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              // dQ: A = dS, row block = query block i, K blocks = key blocks
+              w[i] = sm.eds[i][0] | (sm.eds[i][1] << 8) | (sm.eds[i][2] << 16) |
+                     (sm.eds[i][3] << 24);
+              w[4 + i] = kword;  // dQ: B = K, per key block
+            }
+            tmem_st8(tmem + lane_off + kSfDqA, w);
+          }
+          tmem_st_wait();
+          fence_proxy_async_smem();
+          tc_fence_before();
+          mbar_arrive(smem_u32(&sm.bar_ds_full));
+        }
+        ok = ok && !sm.abort && mbar_wait(smem_u32(&sm.bar_dq_full), uc & 1);
+        tc_fence_after();
+        // the previous tile's reduce-adds must have read the staging buffer
+        if (issuer) bulk_wait_group_read0();
+        named_barrier_sync(1, kComputeThreads);
+        if (ok) {
+          const bool qv = q0 + j < e;  // TMEM lane j of dQ_u is query row j
+          constexpr int kCh = DIM / 64;  // 32-column chunks of dQ_u per group
+          uint32_t v[kCh][32];
+#pragma unroll
+          for (int cc = 0; cc < kCh; ++cc)
+            tmem_ld32(tmem + lane_off + kColSP + 32 * (g * kCh + cc), v[cc]);
+          tmem_ld_wait();
+#pragma unroll
+          for (int cc = 0; cc < kCh; ++cc) {
+            float* row = sm.dqs[g * kCh + cc] + j * 32;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              float4 f = make_float4(__uint_as_float(v[cc][4 * i]) * prm.sm_scale,
+                                     __uint_as_float(v[cc][4 * i + 1]) * prm.sm_scale,
+                                     __uint_as_float(v[cc][4 * i + 2]) * prm.sm_scale,
+                                     __uint_as_float(v[cc][4 * i + 3]) * prm.sm_scale);
+              if (!qv) f = make_float4(0.f, 0.f, 0.f, 0.f);  // rows of other documents add 0
+              *reinterpret_cast<float4*>(row + 4 * (i ^ (j & 7))) = f;
+            }
+          }
+          // NVFP4: stage the next query tile's block scales (the buffer of the
+          // next tile's parity was last read by S^T two tiles back, complete)
+          if (NVF4 && g == 0 && u + 1 < nq) {
+            write_sf4(prm.q4_scales, q0 + kTile, kSfQ4 + 4 * ((uc + 1) & 1));
+            tmem_st_wait();
+          }
+          fence_proxy_async_smem();
+          tc_fence_before();
+          mbar_arrive(smem_u32(&sm.bar_s_free));
+        }
+        if (!ok) sm.abort = 1;
+        // the next tile's per-query inputs (its buffer was last read before this
+        // tile's second barrier)
+        if (g == 0 && u + 1 < nq) load_query_inputs(u + 1, uc + 1);
+        named_barrier_sync(1, kComputeThreads);
+        if (issuer && !sm.abort) {
+#pragma unroll
+          for (int c = 0; c < DIM / 32; ++c)
+            tma_reduce_add_3d(&map_dq, smem_u32(sm.dqs[c]), 32 * c, h, q0);
+          bulk_commit_group();
+        }
+      }
       if (ok) {
-        const bool qv = q0 + j < e;  // TMEM lane j of dQ_u is query row j
-        constexpr int kCh = DIM / 64;  // 32-column chunks of dQ_u per group
-        uint32_t v[kCh][32];
+        // dV = 2^-8 acc, dK = scale * acc, written to the packed buffers; the
+        // groups split the head dimension (every product of the item completed
+        // before its last dQ was read)
+        __nv_bfloat16* dvrow = prm.dv + (static_cast<size_t>(kj) * H + h) * DIM;
+        __nv_bfloat16* dkrow = prm.dk + (static_cast<size_t>(kj) * H + h) * DIM;
+#pragma unroll 1
+        for (int which = 0; which < 2; ++which) {
+          const float mul = which == 0 ? (1.f / 256.f) : prm.sm_scale;
+          __nv_bfloat16* row = which == 0 ? dvrow : dkrow;
+#pragma unroll 1
+          for (int c = g * (DIM / 64); c < (g + 1) * (DIM / 64); ++c) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_off + kColDV + which * DIM + 32 * c, v);
+            tmem_ld_wait();
+            uint32_t w[16];
 #pragma unroll
-        for (int cc = 0; cc < kCh; ++cc) tmem_ld32(tmem + lane_off + kColSP + 32 * (g * kCh + cc), v[cc]);
-        tmem_ld_wait();
-#pragma unroll
-        for (int cc = 0; cc < kCh; ++cc) {
-          float* row = sm.dqs[g * kCh + cc] + j * 32;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            float4 f = make_float4(__uint_as_float(v[cc][4 * i]) * prm.sm_scale,
-                                   __uint_as_float(v[cc][4 * i + 1]) * prm.sm_scale,
-                                   __uint_as_float(v[cc][4 * i + 2]) * prm.sm_scale,
-                                   __uint_as_float(v[cc][4 * i + 3]) * prm.sm_scale);
-            if (!qv) f = make_float4(0.f, 0.f, 0.f, 0.f);  // rows of other documents add 0
-            *reinterpret_cast<float4*>(row + 4 * (i ^ (j & 7))) = f;
+            for (int i = 0; i < 16; ++i) {
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * i]) * mul,
+                                                        __uint_as_float(v[2 * i + 1]) * mul);
+              w[i] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+            if (key_valid) {
+              uint4* dst = reinterpret_cast<uint4*>(row + 32 * c);
+              dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+              dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+              dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
+              dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+            }
           }
         }
-        // NVFP4: stage the next query tile's block scales (the buffer of
-        // parity u + 1 was last read by S^T of tile u - 1, already complete)
-        if (NVF4 && g == 0 && u + 1 < nq) {
-          write_sf4(prm.q4_scales, q0 + kTile, kSfQ4 + 4 * ((u + 1) & 1));
-          tmem_st_wait();
-        }
-        fence_proxy_async_smem();
+        // dV / dK columns may now be restarted by the next item
         tc_fence_before();
-        mbar_arrive(smem_u32(&sm.bar_s_free));
-      }
-      if (!ok) sm.abort = 1;
-      // the next tile's per-query inputs (its buffer was last read before this
-      // tile's second barrier)
-      if (g == 0 && u + 1 < nq) load_query_inputs(u + 1);
-      named_barrier_sync(1, kComputeThreads);
-      if (issuer && !sm.abort) {
-#pragma unroll
-        for (int c = 0; c < DIM / 32; ++c)
-          tma_reduce_add_3d(&map_dq, smem_u32(sm.dqs[c]), 32 * c, h, q0);
-        bulk_commit_group();
+        mbar_arrive(smem_u32(&sm.bar_acc_empty));
       }
     }
     if (issuer) bulk_wait_group0();
-    if (ok) {
-      // dV = 2^-8 acc, dK = scale * acc, written to the packed buffers; the
-      // groups split the head dimension
-      __nv_bfloat16* dvrow = prm.dv + (static_cast<size_t>(kj) * H + h) * DIM;
-      __nv_bfloat16* dkrow = prm.dk + (static_cast<size_t>(kj) * H + h) * DIM;
-#pragma unroll 1
-      for (int which = 0; which < 2; ++which) {
-        const float mul = which == 0 ? (1.f / 256.f) : prm.sm_scale;
-        __nv_bfloat16* row = which == 0 ? dvrow : dkrow;
-#pragma unroll 1
-        for (int c = g * (DIM / 64); c < (g + 1) * (DIM / 64); ++c) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_off + kColDV + which * DIM + 32 * c, v);
-          tmem_ld_wait();
-          uint32_t w[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * i]) * mul,
-                                                      __uint_as_float(v[2 * i + 1]) * mul);
-            w[i] = *reinterpret_cast<uint32_t*>(&b2);
-          }
-          if (key_valid) {
-            uint4* dst = reinterpret_cast<uint4*>(row + 32 * c);
-            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-            dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
-            dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
-          }
-        }
-      }
-    }
     if (!ok) sm.abort = 1;
   }
 
@@ -552,11 +529,11 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
                          float* acc, int* status, cudaStream_t stream) {
   CUtensorMap mq, mk, mv, mdo, mdq, mq4, mk4;
   const CUtensorMapSwizzle swz = swizzle_for_row_bytes(DIM);
-  if (!make_token_map(&mq, q->codes, T, H, DIM, kTile, swz) ||
+  if (DIM == 64 && (!make_token_map(&mq, q->codes, T, H, DIM, kTile, swz) ||
       !make_token_map(&mk, k->codes, T, H, DIM, kTile, swz) ||
       !make_token_map(&mv, v->codes, T, H, DIM, kTile, swz) ||
       !make_token_map(&mdo, dout->codes, T, H, DIM, kTile, swz) ||
-      !make_f32_token_map(&mdq, acc, T, H, DIM, kTile))
+      !make_f32_token_map(&mdq, acc, T, H, DIM, kTile)))
     return FLAMIA_ERR_CUDA;
   if (NVF4) {
     if (!make_token_map(&mq4, q->nvfp4_codes, T, H, DIM / 2, kTile, CU_TENSOR_MAP_SWIZZLE_32B) ||
@@ -578,7 +555,7 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
   prm.lse = lse;
   prm.cu = cu;
   prm.wl_header = static_cast<const int*>(wl);
-  prm.items = reinterpret_cast<const int4*>(static_cast<const char*>(wl) + L.off_bwd);
+  prm.items = reinterpret_cast<const int4*>(static_cast<const char*>(wl) + L.off_tile_bwd);
   prm.dk = static_cast<__nv_bfloat16*>(dk);
   prm.dv = static_cast<__nv_bfloat16*>(dv);
   prm.T = T;
@@ -590,14 +567,25 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
   prm.status = status;
   const size_t n = static_cast<size_t>(T) * H * DIM;
   if (cudaMemsetAsync(acc, 0, n * sizeof(float), stream) != cudaSuccess) return FLAMIA_ERR_CUDA;
-  const size_t smem = sizeof(BwdSmem<DIM, NVF4>) + 1024;
-  if (cudaFuncSetAttribute(attn_bwd_kernel<DIM, NVF4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem)) != cudaSuccess)
+  // persistent: one CTA per SM (shared memory allows one), items in snake order
+  const long long grid = std::min<long long>(static_cast<long long>(L.cap_bwd) * H, num_sms());
+  if constexpr (DIM == 128 && !NVF4) {
+    if (launch_bwd128_pipelined(prm, q, k, v, dout, acc, static_cast<unsigned>(grid), stream) !=
+        cudaSuccess)
+      return FLAMIA_ERR_CUDA;
+  } else {
+    const size_t smem = sizeof(BwdSmem<DIM, NVF4>) + 1024;
+    if (cudaFuncSetAttribute(attn_bwd_kernel<DIM, NVF4>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return FLAMIA_ERR_CUDA;
+    attn_bwd_kernel<DIM, NVF4><<<static_cast<unsigned>(grid), kBwdThreads, smem, stream>>>(
+        mq, mk, mv, mdo, mdq, mq4, mk4, prm);
+    if (cudaGetLastError() != cudaSuccess) return FLAMIA_ERR_CUDA;
+  }
+  if (launch_bwd_short(q, k, v, dout, D, lse, cu, ndocs, T, H, DIM, softmax_scale, NVF4, acc, dk,
+                       dv, stream) != cudaSuccess)
     return FLAMIA_ERR_CUDA;
-  const long long grid = static_cast<long long>(L.cap_bwd) * H;
-  attn_bwd_kernel<DIM, NVF4><<<static_cast<unsigned>(grid), kBwdThreads, smem, stream>>>(
-      mq, mk, mv, mdo, mdq, mq4, mk4, prm);
-  if (cudaGetLastError() != cudaSuccess) return FLAMIA_ERR_CUDA;
   const size_t n4 = n / 4;
   const int blocks = static_cast<int>(std::min<size_t>((n4 + 255) / 256, 152 * 16));
   dq_convert_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(acc),

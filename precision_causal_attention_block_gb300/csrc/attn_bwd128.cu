@@ -1,0 +1,504 @@
+// Causal backward for head dim 128 over token-block MXFP8 operands (FLAMIA
+// review page, sec. 1.2, 3.1, 3.3, 3.4 "Backward pass"), pipelined so that
+// the tensor core and the CUDA cores work at the same time.
+//
+// One work item = one 128-key tile of a document x one head (persistent CTAs,
+// items in snake order as in the other kernels).  The item's queries are
+// walked in 64-query tiles t from the diagonal to the document end; the two
+// compute groups take alternate tiles, each with its own half of tensor memory:
+//
+//   TMEM columns  [64b, 64b+64)     S^T_t (keys x queries), then dQ^T_t
+//                 [128+64b, +64)    dP^T_t, then the block scales of tile t
+//                 [256, 384)        dV accumulator   [384, 512) dK accumulator
+//   (b = t & 1 = the compute group of tile t)
+//
+// While group b turns S^T_t / dP^T_t into the dV operand RNE_E4M3(2^8 P) and
+// the dS codes, the tensor core runs the products of the other group's tile;
+// its S^T / dP^T for tile t+2 start as soon as dQ^T_t has been read out.
+//   S^T_t = K Q_t^T, dP^T_t = V dO_t^T          (unscaled E4M3, M=128, N=64)
+//   dV += P^b_t^T dO_t, dK += dS_t^T Q_t         (block-scaled, M=128, N=128, K=64)
+//   dQ_t^T = K^T dS_t^T                          (block-scaled, M=128 dims, N=64)
+// dQ_t^T is read with one thread per head-dim row, staged as [query][dim]
+// float32 rows and added to the global accumulator by bulk tensor reduce-adds.
+//
+// Warp roles: warp 0 TMA producer (K, V per item; Q, dO 64-row tiles through a
+// 4-stage ring), warp 1 tensor-memory owner and single-thread MMA issuer,
+// warps 4-7 compute group 0, warps 8-11 compute group 1 (thread = key row for
+// S^T / dP^T / dV / dK, head-dim row for dQ^T).
+#include "bwd_common.cuh"
+
+namespace flamia {
+namespace {
+
+constexpr int kQT = 64;          // queries per tile
+constexpr int kRing = 4;         // Q / dO ring stages
+constexpr int kThreads = 384;
+constexpr int kGroupThreads = 128;
+constexpr int kD = 128;          // head dim
+constexpr uint32_t kColDV = 256, kColDK = 384;
+// block-scale columns inside a dP^T half (written after dP^T is read)
+constexpr uint32_t kSfDvA = 0, kSfDvB = 4, kSfDkA = 8, kSfDkB = 12, kSfDqA = 16, kSfDqB = 20;
+
+__device__ __forceinline__ uint32_t col_s(int b) { return 64u * b; }
+__device__ __forceinline__ uint32_t col_p(int b) { return 128u + 64u * b; }
+
+struct Bwd128Smem {
+  alignas(1024) uint8_t k[kTile * kD];             // [key][dim], 128B-swizzled rows
+  alignas(1024) uint8_t v[kTile * kD];
+  alignas(1024) uint8_t q[kRing][kQT * kD];        // [query][dim], 128B-swizzled rows
+  alignas(1024) uint8_t dout[kRing][kQT * kD];
+  alignas(1024) uint8_t pb[2][kTile * kQT];        // [key][query] E4M3, 64B-swizzled rows
+  alignas(1024) uint8_t ds[2][kTile * kQT];
+  alignas(1024) float dqs[2][kD / 32][kQT * 32];   // per group: 4 boxes [query][32 dims]
+  // per-query inputs of a group's tile, double-buffered by the group's tile count
+  alignas(16) float nl[2][2][kQT];                 // 8 - lse2 (-inf outside the document)
+  alignas(16) float dd[2][2][kQT];                 // D (0 outside)
+  uint32_t qbyte[2][2][2], dobyte[2][2][2];        // [group][buffer][query block]
+  uint32_t eds[2][2][4];                           // [group][query block][key block]
+  uint64_t bar_kv, bar_kv_free;
+  uint64_t bar_qd_full[kRing], bar_qd_empty[kRing];
+  uint64_t bar_s_full[2], bar_ds_full[2], bar_dq_full[2], bar_dq_read[2];
+  uint64_t bar_acc_full, bar_acc_empty, bar_done;
+  uint32_t tmem_base;
+  volatile int abort;
+};
+
+__device__ __forceinline__ int n_tiles64(const BwdItem& it) { return (it.e - it.k0 + kQT - 1) / kQT; }
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd128_kernel(const __grid_constant__ CUtensorMap map_q,
+                       const __grid_constant__ CUtensorMap map_k,
+                       const __grid_constant__ CUtensorMap map_v,
+                       const __grid_constant__ CUtensorMap map_do,
+                       const __grid_constant__ CUtensorMap map_dq, const BwdParams prm) {
+  extern __shared__ uint8_t smem_raw[];
+  Bwd128Smem& sm = *reinterpret_cast<Bwd128Smem*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
+  const int H = prm.H, T = prm.T;
+  const int n_items = min(prm.wl_header[kHdrTileBwd], prm.cap);
+  const int total = n_items * H;
+  if (static_cast<int>(blockIdx.x) >= total) return;  // uniform over the CTA
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&sm.bar_kv), 1);
+    mbar_init(smem_u32(&sm.bar_kv_free), 1);
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(smem_u32(&sm.bar_qd_full[i]), 1);
+      mbar_init(smem_u32(&sm.bar_qd_empty[i]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&sm.bar_s_full[b]), 1);
+      mbar_init(smem_u32(&sm.bar_ds_full[b]), kGroupThreads);
+      mbar_init(smem_u32(&sm.bar_dq_full[b]), 1);
+      mbar_init(smem_u32(&sm.bar_dq_read[b]), kGroupThreads);
+    }
+    mbar_init(smem_u32(&sm.bar_acc_full), 1);
+    mbar_init(smem_u32(&sm.bar_acc_empty), 2 * kGroupThreads);
+    mbar_init(smem_u32(&sm.bar_done), 1);
+    sm.abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sm.tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  constexpr uint32_t kKVBytes = 2 * kTile * kD;
+  constexpr uint32_t kQDBytes = 2 * kQT * kD;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tensormap(&map_q);
+      prefetch_tensormap(&map_k);
+      prefetch_tensormap(&map_v);
+      prefetch_tensormap(&map_do);
+      const uint32_t bkv = smem_u32(&sm.bar_kv);
+      int nk = 0, uc = 0;  // items and query tiles loaded (tiles in the consumers' order)
+      bool ok = true;
+      auto load_qd = [&](int h, int q0) -> bool {
+        const int st = uc % kRing;
+        if (uc >= kRing &&
+            (!mbar_wait(smem_u32(&sm.bar_qd_empty[st]), ((uc / kRing) - 1) & 1) || sm.abort))
+          return false;
+        const uint32_t bf = smem_u32(&sm.bar_qd_full[st]);
+        mbar_arrive_expect_tx(bf, kQDBytes);
+        tma_load_3d(smem_u32(sm.q[st]), &map_q, bf, 0, h, q0);
+        tma_load_3d(smem_u32(sm.dout[st]), &map_do, bf, 0, h, q0);
+        ++uc;
+        return true;
+      };
+      for (int round = 0; ok; ++round) {
+        const int idx = snake_index_b(round);
+        if (idx >= total) break;
+        BwdItem it;
+        if (!decode_bwd_item(prm, n_items, idx, it)) continue;
+        const int nq = n_tiles64(it);
+        const int pre = min(nq, 2);
+        int u = 0;
+        // the item's first query tiles do not depend on the previous K / V
+        for (; u < pre && ok; ++u) ok = load_qd(it.h, it.k0 + u * kQT);
+        if (!ok) break;
+        if (nk > 0 && (!mbar_wait(smem_u32(&sm.bar_kv_free), (nk - 1) & 1) || sm.abort)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(bkv, kKVBytes);
+        tma_load_3d(smem_u32(sm.k), &map_k, bkv, 0, it.h, it.k0);
+        tma_load_3d(smem_u32(sm.v), &map_v, bkv, 0, it.h, it.k0);
+        ++nk;
+        for (; u < nq && ok; ++u) ok = load_qd(it.h, it.k0 + u * kQT);
+      }
+      // drain: every issued copy has landed before the CTA exits
+      if (nk > 0) ok &= mbar_wait(bkv, (nk - 1) & 1);
+      for (int t = max(0, uc - kRing); t < uc; ++t)
+        ok &= mbar_wait(smem_u32(&sm.bar_qd_full[t % kRing]), (t / kRing) & 1);
+      if (!ok) sm.abort = 1;
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t ka = smem_u32(sm.k), va = smem_u32(sm.v);
+      constexpr uint32_t id_s = idesc_f8(kTile, kQT, 0, 0);
+      int nk = 0, ug = 0;
+      bool ok = true;
+      // S^T_t and dP^T_t into the tensor-memory half of tile t
+      auto issue_sdp = [&](int t) -> bool {
+        const int st = t % kRing, b = t & 1;
+        if (!mbar_wait(smem_u32(&sm.bar_qd_full[st]), (t / kRing) & 1)) return false;
+        // the half's previous tile (t - 2) has had its dQ^T read out
+        if (t >= 2 && !mbar_wait(smem_u32(&sm.bar_dq_read[b]), ((t >> 1) - 1) & 1)) return false;
+        if (sm.abort) return false;
+        tc_fence_after();
+        const uint32_t qa = smem_u32(sm.q[st]), da = smem_u32(sm.dout[st]);
+#pragma unroll
+        for (int ks = 0; ks < kD / 32; ++ks)
+          mma_f8(tmem + col_s(b), smem_desc(ka + 32 * ks, 0, 1024, kLayoutSW128),
+                 smem_desc(qa + 32 * ks, 0, 1024, kLayoutSW128), id_s, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < kD / 32; ++ks)
+          mma_f8(tmem + col_p(b), smem_desc(va + 32 * ks, 0, 1024, kLayoutSW128),
+                 smem_desc(da + 32 * ks, 0, 1024, kLayoutSW128), id_s, ks > 0);
+        tc_commit(smem_u32(&sm.bar_s_full[b]));
+        return true;
+      };
+      for (int round = 0; ok; ++round) {
+        const int idx = snake_index_b(round);
+        if (idx >= total) break;
+        BwdItem it;
+        if (!decode_bwd_item(prm, n_items, idx, it)) continue;
+        const int nq = n_tiles64(it);
+        ok = mbar_wait(smem_u32(&sm.bar_kv), nk & 1) && (nq < 1 || issue_sdp(ug)) &&
+             (nq < 2 || issue_sdp(ug + 1));
+        for (int u = 0; ok && u < nq; ++u) {
+          const int t = ug + u, b = t & 1, st = t % kRing;
+          // dV / dK restart from zero on an item's first tile: the previous
+          // item's epilogue must have read them
+          if (!mbar_wait(smem_u32(&sm.bar_ds_full[b]), (t >> 1) & 1) ||
+              (u == 0 && nk > 0 && !mbar_wait(smem_u32(&sm.bar_acc_empty), (nk - 1) & 1)) ||
+              sm.abort) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t qa = smem_u32(sm.q[st]), da = smem_u32(sm.dout[st]);
+          const uint32_t pba = smem_u32(sm.pb[b]), dsa = smem_u32(sm.ds[b]);
+          const uint32_t sf = tmem + col_p(b);
+          // dV += P^b^T dO_t : A [key][query] K-major (64-byte rows), B = dO_t MN-major
+#pragma unroll
+          for (int kb = 0; kb < kQT / 32; ++kb)
+            mma_mxf8(tmem + kColDV, smem_desc(pba + 32 * kb, 0, 512, kLayoutSW64),
+                     smem_desc(da + kb * 32 * kD, 0, 1024, kLayoutSW128),
+                     idesc_mxf8(kTile, kD, 0, 1, kb, kb), sf + kSfDvA, sf + kSfDvB,
+                     (u > 0 || kb > 0));
+          // dK += dS^T Q_t
+#pragma unroll
+          for (int kb = 0; kb < kQT / 32; ++kb)
+            mma_mxf8(tmem + kColDK, smem_desc(dsa + 32 * kb, 0, 512, kLayoutSW64),
+                     smem_desc(qa + kb * 32 * kD, 0, 1024, kLayoutSW128),
+                     idesc_mxf8(kTile, kD, 0, 1, kb, kb), sf + kSfDkA, sf + kSfDkB,
+                     (u > 0 || kb > 0));
+          // dQ^T_t = K^T dS^T : A = K read MN-major (M = dims), B = dS read MN-major
+#pragma unroll
+          for (int kb = 0; kb < kTile / 32; ++kb)
+            mma_mxf8(tmem + col_s(b), smem_desc(ka + kb * 32 * kD, 0, 1024, kLayoutSW128),
+                     smem_desc(dsa + kb * 32 * kQT, 0, 512, kLayoutSW64),
+                     idesc_mxf8(kD, kQT, 1, 1, kb, kb), sf + kSfDqA, sf + kSfDqB, kb > 0);
+          tc_commit(smem_u32(&sm.bar_dq_full[b]));
+          tc_commit(smem_u32(&sm.bar_qd_empty[st]));
+          if (u + 2 < nq && !issue_sdp(t + 2)) {
+            ok = false;
+            break;
+          }
+        }
+        if (!ok) break;
+        tc_commit(smem_u32(&sm.bar_acc_full));
+        tc_commit(smem_u32(&sm.bar_kv_free));
+        ++nk;
+        ug += nq;
+      }
+      if (!ok) sm.abort = 1;
+      tc_commit(smem_u32(&sm.bar_done));
+      if (!mbar_wait(smem_u32(&sm.bar_done), 0)) sm.abort = 1;
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ compute groups
+    const int g = (warp - 4) >> 2;  // tiles t with t & 1 == g
+    const int quad = warp & 3;
+    const int j = quad * 32 + lane;  // key row (S^T, dP^T, dV, dK) / dim row (dQ^T)
+    const bool issuer = (quad == 0 && lane == 0);
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t bar_id = 1 + g;
+    const float LOG2E = 1.4426950408889634f;
+    // Every thread of the group runs the same sequence of named barriers: a
+    // wait that times out only clears `ok`, which skips work, never a barrier.
+    bool ok = true;
+    int ng = 0, ug = 0, nk = 0;  // this group's tiles, all tiles, items
+    // per-query inputs of one tile, fetched into registers ahead of use
+    float r_nl = -INFINITY, r_dd = 0.f;
+    uint32_t r_qb = 127u, r_dob = 127u;
+    auto fetch_inputs = [&](size_t hT, int q0, int e) {
+      if (quad < 2) {
+        const int qi = q0 + j;
+        const bool qv = qi < e;
+        r_nl = qv ? 8.f - prm.lse[hT + qi] * LOG2E : -INFINITY;
+        r_dd = qv ? prm.D[hT + qi] : 0.f;
+      } else if (lane == 0) {
+        const int qi = q0 + 32 * (quad - 2);
+        const bool qv = qi < e;
+        r_qb = qv ? prm.q_scales[hT + qi] : 127u;
+        r_dob = qv ? prm.do_scales[hT + qi] : 127u;
+      }
+    };
+    auto store_inputs = [&](int buf) {
+      if (quad < 2) {
+        sm.nl[g][buf][j] = r_nl;
+        sm.dd[g][buf][j] = r_dd;
+      } else if (lane == 0) {
+        sm.qbyte[g][buf][quad - 2] = r_qb;
+        sm.dobyte[g][buf][quad - 2] = r_dob;
+      }
+    };
+    for (int round = 0;; ++round) {
+      const int idx = snake_index_b(round);
+      if (idx >= total) break;
+      BwdItem it;
+      if (!decode_bwd_item(prm, n_items, idx, it)) continue;
+      const int h = it.h, e = it.e, k0 = it.k0, nq = n_tiles64(it);
+      const size_t hT = static_cast<size_t>(h) * T;
+      const int kj = k0 + j;
+      const bool key_valid = kj < it.k1;
+      const int ekj = key_valid ? static_cast<int>(prm.k_scales[hT + kj]) - 127 : 0;
+      const int evj = key_valid ? static_cast<int>(prm.v_scales[hT + kj]) - 127 : 0;
+      const float rowf = pow2_or_zero(ekj) * prm.scale_log2;
+      const float rowg = pow2_or_zero(evj);
+      // E8M0 bytes of the tile's 4 key blocks (A scale of dQ^T = K^T dS^T)
+      uint32_t kword = 0;
+#pragma unroll
+      for (int kb = 0; kb < 4; ++kb) {
+        const int kk = k0 + 32 * kb;
+        kword |= (kk < e ? static_cast<uint32_t>(prm.k_scales[hT + kk]) : 127u) << (8 * kb);
+      }
+      int u = ((ug & 1) == g) ? 0 : 1;  // this group's first tile of the item
+      if (u < nq) {
+        fetch_inputs(hT, k0 + u * kQT, e);
+        store_inputs(ng & 1);
+      }
+      named_barrier_sync(bar_id, kGroupThreads);
+      for (; u < nq; u += 2, ++ng) {
+        const int q0 = k0 + u * kQT;
+        const int buf = ng & 1;
+        if (u + 2 < nq) fetch_inputs(hT, q0 + 2 * kQT, e);  // lands during this tile
+        ok = ok && !sm.abort && mbar_wait(smem_u32(&sm.bar_s_full[g]), ng & 1);
+        tc_fence_after();
+        uint8_t* pbrow = sm.pb[g] + j * kQT;
+        uint8_t* dsrow = sm.ds[g] + j * kQT;
+        const int sw = (j >> 1) & 3;  // 64-byte swizzle of row j
+#pragma unroll 1
+        for (int c = 0; c < 2 && ok; ++c) {
+          const float fS = rowf * pow2_or_zero(static_cast<int>(sm.qbyte[g][buf][c]) - 127);
+          const float fP = rowg * pow2_or_zero(static_cast<int>(sm.dobyte[g][buf][c]) - 127);
+          uint32_t sv[32], dv[32];
+          tmem_ld32(tmem + lane_off + col_s(g) + 32 * c, sv);
+          tmem_ld32(tmem + lane_off + col_p(g) + 32 * c, dv);
+          tmem_ld_wait();
+          uint32_t pw[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+          float amax = 0.f;
+          const float* nl = sm.nl[g][buf] + 32 * c;
+          const float* dd = sm.dd[g][buf] + 32 * c;
+          if (!key_valid) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) dv[i] = 0u;
+          } else if (u < 2) {  // the tile crosses the diagonal
+            amax = bwd_chunk<true>(sv, dv, nl, dd, fS, fP, u * kQT + 32 * c, j, pw);
+          } else {
+            amax = bwd_chunk<false>(sv, dv, nl, dd, fS, fP, u * kQT + 32 * c, j, pw);
+          }
+          // one exponent per 32x32 block: this warp's 32 key rows x these 32 queries
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+          const int eb = max(roundup_exponent(amax) - 8, -127);  // exponent of dS = 2^-8 dS8
+          const float inv = exp2i(-(eb + 8));
+          const float2 inv2 = make_float2(inv, inv);
+          uint32_t dw[8];
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const float2 a = __fmul2_rn(
+                make_float2(__uint_as_float(dv[i]), __uint_as_float(dv[i + 1])), inv2);
+            const float2 bq = __fmul2_rn(
+                make_float2(__uint_as_float(dv[i + 2]), __uint_as_float(dv[i + 3])), inv2);
+            dw[i / 4] = cvt_e4m3x2(a.x, a.y) | (cvt_e4m3x2(bq.x, bq.y) << 16);
+          }
+          const int ch0 = (2 * c) ^ sw, ch1 = (2 * c + 1) ^ sw;
+          *reinterpret_cast<uint4*>(pbrow + 16 * ch0) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+          *reinterpret_cast<uint4*>(pbrow + 16 * ch1) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
+          *reinterpret_cast<uint4*>(dsrow + 16 * ch0) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
+          *reinterpret_cast<uint4*>(dsrow + 16 * ch1) = make_uint4(dw[4], dw[5], dw[6], dw[7]);
+          if (lane == 0) sm.eds[g][c][quad] = static_cast<uint32_t>(eb + 127);
+        }
+        // the group's previous reduce-add has read the staging buffer
+        if (issuer) bulk_wait_group_read0();
+        named_barrier_sync(bar_id, kGroupThreads);
+        if (ok) {
+          // block scales of the three products (the same words in every lane
+          // quadrant: column base + i covers rows 32 i .. 32 i + 31)
+          const uint32_t qw = sm.qbyte[g][buf][0] | (sm.qbyte[g][buf][1] << 8) | 0x7F7F0000u;
+          const uint32_t dow =
+              sm.dobyte[g][buf][0] | (sm.dobyte[g][buf][1] << 8) | 0x7F7F0000u;
+          uint32_t w[8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            w[i] = 0x7F7F7F7Fu;  // dV: A = P^b, scale 2^0
+            w[4 + i] = dow;      // dV: B = dO_t, per query block
+          }
+          tmem_st8(tmem + lane_off + col_p(g) + kSfDvA, w);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            // dK: A = dS^T, row block = key block i, K blocks = the 2 query blocks
+            w[i] = sm.eds[g][0][i] | (sm.eds[g][1][i] << 8) | 0x7F7F0000u;
+            w[4 + i] = qw;  // dK: B = Q_t, per query block
+          }
+          tmem_st8(tmem + lane_off + col_p(g) + kSfDkA, w);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) w[i] = kword;  // dQ^T: A = K^T, per key block
+#pragma unroll
+          for (int i = 0; i < 2; ++i)  // dQ^T: B = dS^T, row block = query block i
+            w[4 + i] = sm.eds[g][i][0] | (sm.eds[g][i][1] << 8) | (sm.eds[g][i][2] << 16) |
+                       (sm.eds[g][i][3] << 24);
+          w[6] = w[7] = 0x7F7F7F7Fu;
+          tmem_st8(tmem + lane_off + col_p(g) + kSfDqA, w);
+          tmem_st_wait();
+          fence_proxy_async_smem();
+          tc_fence_before();
+          mbar_arrive(smem_u32(&sm.bar_ds_full[g]));
+        }
+        // the next tile's inputs go to the other buffer (last read by the
+        // group's previous tile, before its final barrier)
+        if (u + 2 < nq) store_inputs(buf ^ 1);
+        ok = ok && !sm.abort && mbar_wait(smem_u32(&sm.bar_dq_full[g]), ng & 1);
+        tc_fence_after();
+        if (ok) {
+          uint32_t v0[32], v1[32];
+          tmem_ld32(tmem + lane_off + col_s(g), v0);
+          tmem_ld32(tmem + lane_off + col_s(g) + 32, v1);
+          tmem_ld_wait();
+          // S^T / dP^T of the group's next tile may now be computed
+          tc_fence_before();
+          mbar_arrive(smem_u32(&sm.bar_dq_read[g]));
+          const int nvalid = min(kQT, e - q0);  // queries of other documents add 0
+          float* stg = sm.dqs[g][quad] + lane;  // row = query, element = this dim
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            stg[c * 32] = c < nvalid ? __uint_as_float(v0[c]) * prm.sm_scale : 0.f;
+            stg[(c + 32) * 32] = c + 32 < nvalid ? __uint_as_float(v1[c]) * prm.sm_scale : 0.f;
+          }
+          fence_proxy_async_smem();
+        }
+        if (!ok) sm.abort = 1;
+        named_barrier_sync(bar_id, kGroupThreads);
+        if (issuer && !sm.abort) {
+#pragma unroll
+          for (int c = 0; c < kD / 32; ++c)
+            tma_reduce_add_3d(&map_dq, smem_u32(sm.dqs[g][c]), 32 * c, h, q0);
+          bulk_commit_group();
+        }
+      }
+      ug += nq;
+      // dV = 2^-8 acc, dK = scale * acc; the groups split the head dimension
+      ok = ok && !sm.abort && mbar_wait(smem_u32(&sm.bar_acc_full), nk & 1);
+      tc_fence_after();
+      if (ok) {
+        __nv_bfloat16* dvrow = prm.dv + (static_cast<size_t>(kj) * H + h) * kD;
+        __nv_bfloat16* dkrow = prm.dk + (static_cast<size_t>(kj) * H + h) * kD;
+#pragma unroll 1
+        for (int which = 0; which < 2; ++which) {
+          const float mul = which == 0 ? (1.f / 256.f) : prm.sm_scale;
+          __nv_bfloat16* row = which == 0 ? dvrow : dkrow;
+          const uint32_t col = which == 0 ? kColDV : kColDK;
+#pragma unroll 1
+          for (int c = 2 * g; c < 2 * g + 2; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_off + col + 32 * c, v);
+            tmem_ld_wait();
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * i]) * mul,
+                                                        __uint_as_float(v[2 * i + 1]) * mul);
+              w[i] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+            if (key_valid) {
+              uint4* dst = reinterpret_cast<uint4*>(row + 32 * c);
+              dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+              dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+              dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
+              dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&sm.bar_acc_empty));
+      }
+      ++nk;
+    }
+    if (issuer) bulk_wait_group0();
+    if (!ok) sm.abort = 1;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (sm.abort && threadIdx.x == 0) report(prm.status, FLAMIA_DEV_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd128_pipelined(const BwdParams& prm, const flamia_qtensor* q,
+                                    const flamia_qtensor* k, const flamia_qtensor* v,
+                                    const flamia_qtensor* dout, float* acc, unsigned grid,
+                                    cudaStream_t stream) {
+  CUtensorMap mq, mk, mv, mdo, mdq;
+  const int T = prm.T, H = prm.H;
+  if (!make_token_map(&mq, q->codes, T, H, kD, kQT, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_token_map(&mk, k->codes, T, H, kD, kTile, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_token_map(&mv, v->codes, T, H, kD, kTile, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_token_map(&mdo, dout->codes, T, H, kD, kQT, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_f32_token_map(&mdq, acc, T, H, kD, kQT, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  const size_t smem = sizeof(Bwd128Smem) + 1024;
+  cudaError_t err = cudaFuncSetAttribute(
+      attn_bwd128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (err != cudaSuccess) return err;
+  attn_bwd128_kernel<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mdo, mdq, prm);
+  return cudaGetLastError();
+}
+
+}  // namespace flamia

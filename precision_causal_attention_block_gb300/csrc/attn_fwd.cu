@@ -21,6 +21,7 @@
 
 #include "common.cuh"
 #include "ptx.cuh"
+#include "short_docs.cuh"
 
 namespace flamia {
 namespace {
@@ -40,7 +41,8 @@ struct FwdSmem {
   alignas(NVF4 ? 1024 : 16) uint8_t q4[2][kTile4Bytes];
   alignas(NVF4 ? 1024 : 16) uint8_t k4[kStages][kTile4Bytes];
   uint64_t bar_sf;
-  uint64_t bar_q;
+  uint64_t bar_q, bar_q_empty;
+  uint64_t bar_o_empty[2];
   uint64_t bar_kv_full[kStages];
   uint64_t bar_kv_empty[kStages];
   uint64_t bar_s_full[2];
@@ -126,6 +128,40 @@ __device__ __forceinline__ void chunk_probs(const uint32_t (&v)[32], float cf, f
 // Q_0, Q_1 (4 columns each) and of K_j (two 4-column buffers, by j parity).
 constexpr uint32_t kSfQ4 = 384, kSfK4 = 392;
 
+// One forward work item (256 queries of one document x one head), decoded
+// identically by every role; false for items of short documents, which the
+// CUDA-core kernel handles.
+struct FwdItem {
+  int h, s, e, q0, q1, n0, n1, nkv;
+  bool valid1;
+};
+
+__device__ __forceinline__ bool decode_fwd_item(const FwdParams& prm, int n_items, int idx,
+                                                FwdItem& it) {
+  const int T = prm.T;
+  it.h = idx / n_items;  // head-major: a wave of CTAs shares the K/V of few heads
+  const int4 item = prm.items[idx % n_items];
+  // clamped: a malformed work list or offsets cannot index outside [0, T)
+  const int doc = min(max(item.x, 0), prm.ndocs - 1);
+  it.s = min(max(prm.cu[doc], 0), T);
+  it.e = min(max(prm.cu[doc + 1], it.s), T);
+  if (it.e - it.s <= kShortDoc) return false;
+  it.q0 = it.s + ((min(max(item.y, it.s), it.e) - it.s) & ~(kTile - 1));
+  it.q1 = min(max(item.z, it.q0), it.e);
+  it.valid1 = it.q1 > it.q0 + kTile;
+  it.n0 = (it.q0 - it.s) / kTile + 1;      // key tiles of query tile 0
+  it.n1 = it.valid1 ? it.n0 + 1 : 0;       // key tiles of query tile 1
+  it.nkv = it.valid1 ? it.n1 : it.n0;
+  return true;
+}
+
+// The CTA's items in snake order over the head-major (head, item) list:
+// round r takes index r * G + b (r even) or r * G + G - 1 - b (r odd).
+__device__ __forceinline__ int snake_index(int round) {
+  const int G = gridDim.x, b = blockIdx.x;
+  return round * G + ((round & 1) ? G - 1 - b : b);
+}
+
 template <int DIM, bool NVF4>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
@@ -139,25 +175,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
   const int H = prm.H, T = prm.T;
-  const int h = blockIdx.x / prm.cap;  // head-major: K/V of one head are shared by a wave
-  const int item_idx = blockIdx.x % prm.cap;
-  if (h >= H || item_idx >= prm.wl_header[kHdrNFwd]) return;  // uniform over the CTA
-  const int4 item = prm.items[item_idx];
-  // clamped: a malformed work list or offsets cannot index outside [0, T)
-  const int doc = min(max(item.x, 0), prm.ndocs - 1);
-  const int s = min(max(prm.cu[doc], 0), T);
-  const int e = min(max(prm.cu[doc + 1], s), T);
-  const int q0 = s + ((min(max(item.y, s), e) - s) & ~(kTile - 1));
-  const int q1 = min(max(item.z, q0), e);
-  const bool valid1 = q1 > q0 + kTile;
-  const int n0 = (q0 - s) / kTile + 1;           // key tiles of query tile 0
-  const int n1 = valid1 ? n0 + 1 : 0;            // key tiles of query tile 1
-  const int nkv = valid1 ? n1 : n0;
-
+  const int n_items = min(prm.wl_header[kHdrTileFwd], prm.cap);
+  const int total = n_items * H;
+  if (static_cast<int>(blockIdx.x) >= total) return;  // uniform over the CTA
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&sm.bar_q), 1);
+    mbar_init(smem_u32(&sm.bar_q_empty), 1);
     for (int i = 0; i < kStages; ++i) {
       mbar_init(smem_u32(&sm.bar_kv_full[i]), 1);
       mbar_init(smem_u32(&sm.bar_kv_empty[i]), 1);
@@ -166,6 +191,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(smem_u32(&sm.bar_s_full[t]), 1);
       mbar_init(smem_u32(&sm.bar_p_full[t]), kTile);
       mbar_init(smem_u32(&sm.bar_o_full[t]), 1);
+      mbar_init(smem_u32(&sm.bar_o_empty[t]), kTile);
     }
     mbar_init(smem_u32(&sm.bar_done), 1);
     mbar_init(smem_u32(&sm.bar_sf), 2 * kTile);
@@ -190,33 +216,46 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       prefetch_tensormap(&map_k);
       prefetch_tensormap(&map_v);
       const uint32_t bq = smem_u32(&sm.bar_q);
-      mbar_arrive_expect_tx(bq, (valid1 ? 2 : 1) * kQBytes);
-      tma_load_3d(smem_u32(sm.q[0]), &map_q, bq, 0, h, q0);
-      if (valid1) tma_load_3d(smem_u32(sm.q[1]), &map_q, bq, 0, h, q0 + kTile);
-      if (NVF4) {
-        tma_load_3d(smem_u32(sm.q4[0]), &map_q4, bq, 0, h, q0);
-        if (valid1) tma_load_3d(smem_u32(sm.q4[1]), &map_q4, bq, 0, h, q0 + kTile);
-      }
-      int issued = 0;
-      for (int j = 0; j < nkv; ++j) {
-        const int st = j % kStages;
-        if (j >= kStages) {
-          if (!mbar_wait(smem_u32(&sm.bar_kv_empty[st]), ((j / kStages) - 1) & 1) ||
-              sm.abort) {
-            sm.abort = 1;
+      int nq_loaded = 0;  // items whose Q tiles were loaded
+      int kvc = 0;        // key tiles loaded over all items
+      bool ok = true;
+      for (int round = 0; ok; ++round) {
+        const int idx = snake_index(round);
+        if (idx >= total) break;
+        FwdItem it;
+        if (!decode_fwd_item(prm, n_items, idx, it)) continue;
+        // the previous item's Q tiles are free once its last score product is done
+        if (nq_loaded > 0 && (!mbar_wait(smem_u32(&sm.bar_q_empty), (nq_loaded - 1) & 1) ||
+                              sm.abort)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(bq, (it.valid1 ? 2 : 1) * kQBytes);
+        tma_load_3d(smem_u32(sm.q[0]), &map_q, bq, 0, it.h, it.q0);
+        if (it.valid1) tma_load_3d(smem_u32(sm.q[1]), &map_q, bq, 0, it.h, it.q0 + kTile);
+        if (NVF4) {
+          tma_load_3d(smem_u32(sm.q4[0]), &map_q4, bq, 0, it.h, it.q0);
+          if (it.valid1) tma_load_3d(smem_u32(sm.q4[1]), &map_q4, bq, 0, it.h, it.q0 + kTile);
+        }
+        ++nq_loaded;
+        for (int j = 0; j < it.nkv; ++j, ++kvc) {
+          const int st = kvc % kStages;
+          if (kvc >= kStages &&
+              (!mbar_wait(smem_u32(&sm.bar_kv_empty[st]), ((kvc / kStages) - 1) & 1) ||
+               sm.abort)) {
+            ok = false;
             break;
           }
+          const uint32_t bf = smem_u32(&sm.bar_kv_full[st]);
+          mbar_arrive_expect_tx(bf, kTileBytes + kQBytes);
+          tma_load_3d(smem_u32(sm.k[st]), &map_k, bf, 0, it.h, it.s + j * kTile);
+          tma_load_3d(smem_u32(sm.v[st]), &map_v, bf, 0, it.h, it.s + j * kTile);
+          if (NVF4) tma_load_3d(smem_u32(sm.k4[st]), &map_k4, bf, 0, it.h, it.s + j * kTile);
         }
-        const uint32_t bf = smem_u32(&sm.bar_kv_full[st]);
-        mbar_arrive_expect_tx(bf, kTileBytes + kQBytes);
-        tma_load_3d(smem_u32(sm.k[st]), &map_k, bf, 0, h, s + j * kTile);
-        tma_load_3d(smem_u32(sm.v[st]), &map_v, bf, 0, h, s + j * kTile);
-        if (NVF4) tma_load_3d(smem_u32(sm.k4[st]), &map_k4, bf, 0, h, s + j * kTile);
-        issued = j + 1;
       }
       // Drain: every issued copy has landed before the CTA can exit.
-      bool ok = mbar_wait(bq, 0);
-      for (int j = max(0, issued - kStages); j < issued; ++j)
+      if (nq_loaded > 0) ok &= mbar_wait(bq, (nq_loaded - 1) & 1);
+      for (int j = max(0, kvc - kStages); j < kvc; ++j)
         ok &= mbar_wait(smem_u32(&sm.bar_kv_full[j % kStages]), (j / kStages) & 1);
       if (!ok) sm.abort = 1;
     }
@@ -226,10 +265,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       constexpr uint32_t lay = operand_layout<DIM>();
       constexpr uint32_t sbo = 8 * DIM;  // 8 rows of one swizzle atom
       const uint32_t id_qk = idesc_f8(kTile, kTile, 0, 0);
-      bool ok = mbar_wait(smem_u32(&sm.bar_q), 0) && mbar_wait(smem_u32(&sm.bar_kv_full[0]), 0);
-      if (NVF4) ok = ok && mbar_wait(smem_u32(&sm.bar_sf), 0);
-      tc_fence_after();
-      // S_t = Q_t K_j^T into columns [128 t, 128 t + 128)
+      // running counts of each barrier's completions (phase parity = count & 1)
+      int nq_used = 0, kvc = 0, o_used[2] = {0, 0}, p_seen[2] = {0, 0};
+      bool ok = true;
+      // S_t = Q_t K^T of the key tile with global index jk into columns [128 t, 128 t + 128)
       auto issue_qk = [&](int t, int jk) {
         const int st = jk % kStages;
         if (NVF4) {
@@ -246,44 +285,69 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         tc_commit(smem_u32(&sm.bar_s_full[t]));
       };
-      if (ok) {
-        issue_qk(0, 0);
-        if (valid1) issue_qk(1, 0);
-      }
-      int kv_ready = 1;  // stages known full: tiles [0, kv_ready)
-      for (int j = 0; ok && j < nkv; ++j) {
-        const int st = j % kStages;
-        for (int t = 0; t < 2 && ok; ++t) {
-          const int nt = t == 0 ? n0 : n1;
-          if (j >= nt) continue;
-          if (!mbar_wait(smem_u32(&sm.bar_p_full[t]), j & 1) || sm.abort) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t pa = smem_u32(sm.p[t]), va = smem_u32(sm.v[st]);
-          const uint32_t sf = tmem + t * kTile;  // scale factors live in S_t columns 0..7
-#pragma unroll
-          for (int kb = 0; kb < 4; ++kb)
-            mma_mxf8(tmem + 256 + t * DIM, smem_desc(pa + 32 * kb, 0, 1024, kLayoutSW128),
-                     smem_desc(va + kb * 32 * DIM, 0, sbo, lay),
-                     idesc_mxf8(kTile, DIM, 0, 1, kb, kb), sf, sf + 4, (j > 0 || kb > 0));
-          if (j + 1 < nt) {
-            if (kv_ready <= j + 1) {
-              if (!mbar_wait(smem_u32(&sm.bar_kv_full[(j + 1) % kStages]),
-                             ((j + 1) / kStages) & 1)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              kv_ready = j + 2;
-            }
-            issue_qk(t, j + 1);
-          } else {
-            tc_commit(smem_u32(&sm.bar_o_full[t]));
-          }
+      for (int round = 0; ok; ++round) {
+        const int idx = snake_index(round);
+        if (idx >= total) break;
+        FwdItem it;
+        if (!decode_fwd_item(prm, n_items, idx, it)) continue;
+        ok = mbar_wait(smem_u32(&sm.bar_q), nq_used & 1) &&
+             mbar_wait(smem_u32(&sm.bar_kv_full[kvc % kStages]), (kvc / kStages) & 1);
+        if (NVF4) ok = ok && mbar_wait(smem_u32(&sm.bar_sf), nq_used & 1);
+        ++nq_used;
+        if (!ok || sm.abort) {
+          ok = false;
+          break;
         }
-        if (ok) tc_commit(smem_u32(&sm.bar_kv_empty[st]));
+        tc_fence_after();
+        issue_qk(0, kvc);
+        if (it.valid1) issue_qk(1, kvc);
+        int kv_ready = kvc + 1;  // key tiles known loaded: global indices < kv_ready
+        for (int j = 0; ok && j < it.nkv; ++j) {
+          const int jk = kvc + j, st = jk % kStages;
+          for (int t = 0; t < 2 && ok; ++t) {
+            const int nt = t == 0 ? it.n0 : it.n1;
+            if (j >= nt) continue;
+            if (!mbar_wait(smem_u32(&sm.bar_p_full[t]), p_seen[t] & 1) || sm.abort) {
+              ok = false;
+              break;
+            }
+            ++p_seen[t];
+            // the first P^V of an item overwrites O_t: the previous item's
+            // epilogue must have read it
+            if (j == 0 && o_used[t] > 0 &&
+                !mbar_wait(smem_u32(&sm.bar_o_empty[t]), (o_used[t] - 1) & 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t pa = smem_u32(sm.p[t]), va = smem_u32(sm.v[st]);
+            const uint32_t sf = tmem + t * kTile;  // scale factors live in S_t columns 0..7
+#pragma unroll
+            for (int kb = 0; kb < 4; ++kb)
+              mma_mxf8(tmem + 256 + t * DIM, smem_desc(pa + 32 * kb, 0, 1024, kLayoutSW128),
+                       smem_desc(va + kb * 32 * DIM, 0, sbo, lay),
+                       idesc_mxf8(kTile, DIM, 0, 1, kb, kb), sf, sf + 4, (j > 0 || kb > 0));
+            if (j + 1 < nt) {
+              if (kv_ready <= jk + 1) {
+                if (!mbar_wait(smem_u32(&sm.bar_kv_full[(jk + 1) % kStages]),
+                               ((jk + 1) / kStages) & 1)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                kv_ready = jk + 2;
+              }
+              issue_qk(t, jk + 1);
+            } else {
+              tc_commit(smem_u32(&sm.bar_o_full[t]));
+              ++o_used[t];
+            }
+          }
+          if (ok) tc_commit(smem_u32(&sm.bar_kv_empty[st]));
+        }
+        kvc += it.nkv;
+        // this item's Q tiles may be replaced once its products are done
+        if (ok) tc_commit(smem_u32(&sm.bar_q_empty));
       }
       if (!ok) sm.abort = 1;
       // Drain: all MMAs of this thread complete before tensor memory is freed.
@@ -295,144 +359,175 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int t = (warp - 4) >> 2;
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
-    const int nt = t == 0 ? n0 : n1;
-    const int qa = q0 + t * kTile;
-    const int qi = qa + r;
-    const bool row_valid = qi < q1;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t tS = tmem + lane_off + t * kTile;
     const uint32_t tO = tmem + lane_off + 256 + t * DIM;
-    const size_t hT = static_cast<size_t>(h) * T;
-    const int eq = NVF4 ? 0 : static_cast<int>(prm.q_scales[hT + min(qi, T - 1)]) - 127;
-    const float c_row = prm.scale_log2 * pow2_or_zero(eq);
-    float m = -INFINITY, l8 = 0.f;
     uint8_t* prow = sm.p[t] + r * kTile;
+    int s_seen = 0, o_seen = 0;  // completions of s_full[t] and o_full[t] waited so far
+    int kvc = 0;                 // global index of the current item's first key tile
     bool ok = true;
-    // NVFP4 score product: its block scales live in tensor memory, one 32-bit
-    // word (4 E4M3 scales) per row; column c + i of this lane quadrant holds
-    // row 32 i + lane (the same words in every quadrant).
-    auto write_sf4 = [&](const uint32_t* words, int tok0, uint32_t col) {
-      uint32_t w[4];
+    for (int round = 0; ok; ++round) {
+      const int idx = snake_index(round);
+      if (idx >= total) break;
+      FwdItem it;
+      if (!decode_fwd_item(prm, n_items, idx, it)) continue;
+      const int h = it.h, s = it.s, e = it.e;
+      const int nt = t == 0 ? it.n0 : it.n1;
+      const int kv0 = kvc;
+      kvc += it.nkv;
+      const int qa = it.q0 + t * kTile;
+      const int qi = qa + r;
+      const bool row_valid = qi < it.q1;
+      const size_t hT = static_cast<size_t>(h) * T;
+      const int eq = NVF4 ? 0 : static_cast<int>(prm.q_scales[hT + min(qi, T - 1)]) - 127;
+      const float c_row = prm.scale_log2 * pow2_or_zero(eq);
+      float m = -INFINITY, l8 = 0.f;
+      // NVFP4 score product: its block scales live in tensor memory, one 32-bit
+      // word (4 E4M3 scales) per row; column c + i of this lane quadrant holds
+      // row 32 i + lane (the same words in every quadrant).
+      auto write_sf4 = [&](const uint32_t* words, int tok0, uint32_t col) {
+        uint32_t w[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        w[i] = words[static_cast<size_t>(min(tok0 + 32 * i + lane, T - 1)) * H + h];
-      tmem_st4(tmem + lane_off + col, w);
-    };
-    if (NVF4) {
-      write_sf4(prm.q4_scales, qa, kSfQ4 + 4 * t);
-      if (t == 0) write_sf4(prm.k4_scales, s, kSfK4);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&sm.bar_sf));
-    }
-    for (int j = 0; j < nt; ++j) {
-      if (!mbar_wait(smem_u32(&sm.bar_s_full[t]), j & 1) || sm.abort) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const int k0 = s + j * kTile;
-      float cf[4];
-      uint32_t sfb = 0;
-#pragma unroll
-      for (int kb = 0; kb < 4; ++kb) {
-        const int kk = k0 + 32 * kb;
-        const int ekb = (!NVF4 && kk < e) ? static_cast<int>(prm.k_scales[hT + kk]) - 127 : 0;
-        cf[kb] = c_row * pow2_or_zero(ekb);
-        const uint32_t vb = kk < e ? prm.v_scales[hT + kk] : 127u;
-        sfb |= vb << (8 * kb);
-      }
-      const bool diag = (j == nt - 1);
-      const int lim = diag ? min(r, e - 1 - k0) : kTile - 1;  // last visible column
-      // the whole 128-column row of S_t in registers: four loads, one wait
-      uint32_t sv[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, sv[c]);
-      tmem_ld_wait();
-      // pass 1: row maximum in the log2 domain
-      float mx = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const float cm = diag ? chunk_max<true>(sv[c], lim - 32 * c) : chunk_max<false>(sv[c], 0);
-        mx = fmaxf(mx, cm * cf[c]);
-      }
-      float m_new = (mx == -INFINITY) ? m : fmaxf(m, ceilf(mx));
-      if (m_new == -INFINITY) m_new = 0.f;
-      const bool need = (j > 0) && (m_new > m);
-      const float corr = need ? pow2_or_zero(static_cast<int>(m - m_new)) : 1.f;
-      l8 *= corr;
-      if (__any_sync(0xffffffffu, need)) {
-        // rescale this warp's O rows by the (exact power-of-two) correction
-        // in 8-column pieces: the row of S stays live in registers meanwhile
-#pragma unroll 1
-        for (int c = 0; c < DIM / 8; ++c) {
-          uint32_t v[8];
-          tmem_ld8(tO + 8 * c, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 8; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * corr);
-          tmem_st8(tO + 8 * c, v);
-        }
+        for (int i = 0; i < 4; ++i)
+          w[i] = words[static_cast<size_t>(min(tok0 + 32 * i + lane, T - 1)) * H + h];
+        tmem_st4(tmem + lane_off + col, w);
+      };
+      if (NVF4) {
+        // K scales go to the buffer of the key tile's global parity (it was
+        // last read by the products of the key tile two before, complete once
+        // this group saw the previous item's O_0)
+        write_sf4(prm.q4_scales, qa, kSfQ4 + 4 * t);
+        if (t == 0) write_sf4(prm.k4_scales, s, kSfK4 + 4 * (kv0 & 1));
         tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&sm.bar_sf));
       }
-      m = m_new;
-      const float moff = m - 8.f;  // P8 = 2^8 exp2(s - m)
-      // pass 2: probabilities, row sum, E4M3 operand
-      float2 lsum = make_float2(0.f, 0.f);
+      // scale bytes of the K and V blocks of key tile j, fetched one step ahead
+      uint32_t kbyte[4], vbyte[4];
+      auto fetch_scales = [&](int jj) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t w[8];
-        if (diag)
-          chunk_probs<true>(sv[c], cf[c], moff, lim - 32 * c, lsum, w);
-        else
-          chunk_probs<false>(sv[c], cf[c], moff, 0, lsum, w);
-        // 32 bytes = 16-byte chunks 2c and 2c+1 of row r, 128B-swizzled
-        const int ch0 = (2 * c) ^ (r & 7), ch1 = (2 * c + 1) ^ (r & 7);
-        *reinterpret_cast<uint4*>(prow + 16 * ch0) = make_uint4(w[0], w[1], w[2], w[3]);
-        *reinterpret_cast<uint4*>(prow + 16 * ch1) = make_uint4(w[4], w[5], w[6], w[7]);
-      }
-      l8 += lsum.x + lsum.y;
-      // scale factors of P^_t V_j: A (P^) 2^0 for every K block, B = V's block bytes
-      const uint32_t sfw[8] = {0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu,
-                               sfb, sfb, sfb, sfb};
-      tmem_st8(tS, sfw);
-      // NVFP4: group 0 stages the block scales of the next key tile (the
-      // buffer of parity j + 1 was last read by the products of tile j - 1,
-      // which completed before S_0 of tile j)
-      if (NVF4 && t == 0 && j + 1 < nkv) write_sf4(prm.k4_scales, k0 + kTile, kSfK4 + 4 * ((j + 1) & 1));
-      tmem_st_wait();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&sm.bar_p_full[t]));
-    }
-    if (nt > 0 && ok) {
-      if (!mbar_wait(smem_u32(&sm.bar_o_full[t]), 0) || sm.abort) ok = false;
-    }
-    if (nt > 0 && ok) {
-      tc_fence_after();
-      const float inv = 1.f / l8;
-      __nv_bfloat16* orow = prm.o + (static_cast<size_t>(qi) * H + h) * DIM;
-#pragma unroll 1
-      for (int c = 0; c < DIM / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tO + 32 * c, v);
+        for (int kb = 0; kb < 4; ++kb) {
+          const int kk = s + jj * kTile + 32 * kb;
+          const bool in = jj < nt && kk < e;
+          kbyte[kb] = (in && !NVF4) ? prm.k_scales[hT + kk] : 127u;
+          vbyte[kb] = in ? prm.v_scales[hT + kk] : 127u;
+        }
+      };
+      fetch_scales(0);
+      for (int j = 0; j < nt; ++j) {
+        const int k0 = s + j * kTile;
+        float cf[4];
+        uint32_t sfb = 0;
+#pragma unroll
+        for (int kb = 0; kb < 4; ++kb) {
+          cf[kb] = c_row * pow2_or_zero(static_cast<int>(kbyte[kb]) - 127);
+          sfb |= vbyte[kb] << (8 * kb);
+        }
+        fetch_scales(j + 1);  // in flight while this tile is processed
+        if (!mbar_wait(smem_u32(&sm.bar_s_full[t]), s_seen & 1) || sm.abort) {
+          ok = false;
+          break;
+        }
+        ++s_seen;
+        tc_fence_after();
+        const bool diag = (j == nt - 1);
+        const int lim = diag ? min(r, e - 1 - k0) : kTile - 1;  // last visible column
+        // the whole 128-column row of S_t in registers: four loads, one wait
+        uint32_t sv[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, sv[c]);
         tmem_ld_wait();
-        uint32_t w[16];
+        // pass 1: row maximum in the log2 domain
+        float mx = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * i]) * inv,
-                                                    __uint_as_float(v[2 * i + 1]) * inv);
-          w[i] = *reinterpret_cast<uint32_t*>(&b2);
+        for (int c = 0; c < 4; ++c) {
+          const float cm =
+              diag ? chunk_max<true>(sv[c], lim - 32 * c) : chunk_max<false>(sv[c], 0);
+          mx = fmaxf(mx, cm * cf[c]);
         }
-        if (row_valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
-          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-          dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
-          dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+        float m_new = (mx == -INFINITY) ? m : fmaxf(m, ceilf(mx));
+        if (m_new == -INFINITY) m_new = 0.f;
+        const bool need = (j > 0) && (m_new > m);
+        const float corr = need ? pow2_or_zero(static_cast<int>(m - m_new)) : 1.f;
+        l8 *= corr;
+        if (__any_sync(0xffffffffu, need)) {
+          // rescale this warp's O rows by the (exact power-of-two) correction
+          // in 8-column pieces: the row of S stays live in registers meanwhile
+#pragma unroll 1
+          for (int c = 0; c < DIM / 8; ++c) {
+            uint32_t v[8];
+            tmem_ld8(tO + 8 * c, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * corr);
+            tmem_st8(tO + 8 * c, v);
+          }
+          tmem_st_wait();
         }
+        m = m_new;
+        const float moff = m - 8.f;  // P8 = 2^8 exp2(s - m)
+        // pass 2: probabilities, row sum, E4M3 operand
+        float2 lsum = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t w[8];
+          if (diag)
+            chunk_probs<true>(sv[c], cf[c], moff, lim - 32 * c, lsum, w);
+          else
+            chunk_probs<false>(sv[c], cf[c], moff, 0, lsum, w);
+          // 32 bytes = 16-byte chunks 2c and 2c+1 of row r, 128B-swizzled
+          const int ch0 = (2 * c) ^ (r & 7), ch1 = (2 * c + 1) ^ (r & 7);
+          *reinterpret_cast<uint4*>(prow + 16 * ch0) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(prow + 16 * ch1) = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+        l8 += lsum.x + lsum.y;
+        // scale factors of P^_t V_j: A (P^) 2^0 for every K block, B = V's block bytes
+        const uint32_t sfw[8] = {0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu,
+                                 sfb, sfb, sfb, sfb};
+        tmem_st8(tS, sfw);
+        // NVFP4: group 0 stages the block scales of the next key tile (its
+        // buffer was last read by the products of key tile j - 1, which
+        // completed before S_0 of tile j)
+        if (NVF4 && t == 0 && j + 1 < it.nkv)
+          write_sf4(prm.k4_scales, k0 + kTile, kSfK4 + 4 * ((kv0 + j + 1) & 1));
+        tmem_st_wait();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&sm.bar_p_full[t]));
       }
-      if (row_valid) prm.lse[hT + qi] = (m - 8.f + __log2f(l8)) * kLn2;
+      if (nt > 0 && ok) {
+        if (!mbar_wait(smem_u32(&sm.bar_o_full[t]), o_seen & 1) || sm.abort) ok = false;
+        ++o_seen;
+      }
+      if (nt > 0 && ok) {
+        tc_fence_after();
+        const float inv = 1.f / l8;
+        __nv_bfloat16* orow = prm.o + (static_cast<size_t>(qi) * H + h) * DIM;
+#pragma unroll 1
+        for (int c = 0; c < DIM / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tO + 32 * c, v);
+          tmem_ld_wait();
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * i]) * inv,
+                                                      __uint_as_float(v[2 * i + 1]) * inv);
+            w[i] = *reinterpret_cast<uint32_t*>(&b2);
+          }
+          if (row_valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
+            dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+          }
+        }
+        if (row_valid) prm.lse[hT + qi] = (m - 8.f + __log2f(l8)) * kLn2;
+        // O_t may now be overwritten by the next item
+        tc_fence_before();
+        mbar_arrive(smem_u32(&sm.bar_o_empty[t]));
+      }
     }
     if (!ok) sm.abort = 1;
   }
@@ -474,7 +569,7 @@ flamia_status launch_fwd(const flamia_qtensor* q, const flamia_qtensor* k,
   prm.k4_scales = reinterpret_cast<const uint32_t*>(k->nvfp4_scales);
   prm.cu = cu;
   prm.wl_header = static_cast<const int*>(wl);
-  prm.items = reinterpret_cast<const int4*>(static_cast<const char*>(wl) + L.off_fwd);
+  prm.items = reinterpret_cast<const int4*>(static_cast<const char*>(wl) + L.off_tile_fwd);
   prm.o = static_cast<__nv_bfloat16*>(o);
   prm.lse = lse;
   prm.T = T;
@@ -488,10 +583,15 @@ flamia_status launch_fwd(const flamia_qtensor* q, const flamia_qtensor* k,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return FLAMIA_ERR_CUDA;
-  const long long grid = static_cast<long long>(L.cap_fwd) * H;
+  // persistent: one CTA per SM (shared memory allows one), items in snake order
+  const long long grid = std::min<long long>(static_cast<long long>(L.cap_fwd) * H, num_sms());
   attn_fwd_kernel<DIM, NVF4>
       <<<static_cast<unsigned>(grid), kFwdThreads, smem, stream>>>(mq, mk, mv, mq4, mk4, prm);
-  return cudaGetLastError() == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return FLAMIA_ERR_CUDA;
+  return launch_fwd_short(q, k, v, cu, ndocs, T, H, DIM, softmax_scale, NVF4, o, lse, stream) ==
+                 cudaSuccess
+             ? FLAMIA_OK
+             : FLAMIA_ERR_CUDA;
 }
 
 }  // namespace

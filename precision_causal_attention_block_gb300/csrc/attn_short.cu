@@ -1,0 +1,320 @@
+// Documents of at most 32 tokens (FLAMIA review page, sec. 3.4 "Packed
+// documents"): one 32-token scale block covers the whole document, so every
+// operand of the document has a single power-of-two scale per head and the
+// work is a handful of tiny dot products -- not a dense contraction.  One
+// warp handles one (document, head) on the CUDA cores with the same numerics
+// as the tile kernels: E4M3 codes decoded exactly, float32 sums, the integer
+// running maximum, P^ = RNE_E4M3(2^8 exp2(s - m)), dS rounded with one
+// round-up exponent for the document's single 32x32 block.
+// Lanes split the head dimension (d / 32 consecutive elements per lane).
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+#include "short_docs.cuh"
+
+namespace flamia {
+namespace {
+
+constexpr int kShortWarps = 4;  // warps (documents x heads) per CTA
+
+__device__ __forceinline__ float pow2_or_zero_s(int k) { return k < -126 ? 0.f : exp2i(k); }
+
+struct ShortParams {
+  const uint8_t *qc, *kc, *vc, *doc_;           // E4M3 codes [T, H, d]
+  const uint8_t *qs, *ks, *vs, *dos;            // E8M0 bytes [H, T]
+  const uint8_t *q4c, *k4c;                     // NVFP4 codes [T, H, d/2] (mixed path, d = 64)
+  const uint8_t *q4s, *k4s;                     // NVFP4 E4M3 scales [T, H, d/16]
+  const int32_t* cu;
+  int T, H, ndocs;
+  float scale_log2, sm_scale;
+  // forward
+  __nv_bfloat16* o;
+  float* lse;
+  // backward
+  const float *lse_in, *D;
+  float* dq_acc;                                // float32 [T, H, d]
+  __nv_bfloat16 *dk, *dv;
+};
+
+// d/32 E4M3 codes of one row (this lane's slice) decoded to floats.
+template <int DIM>
+__device__ __forceinline__ void load_codes(const uint8_t* __restrict__ base, size_t row,
+                                           int lane, float (&x)[DIM / 32]) {
+  if constexpr (DIM == 128) {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(base + row * DIM + 4 * lane);
+    const float2 a = e4m3x2_to_float2(w & 0xFFFFu), b = e4m3x2_to_float2(w >> 16);
+    x[0] = a.x;
+    x[1] = a.y;
+    x[2] = b.x;
+    x[3] = b.y;
+  } else {
+    const uint32_t w = *reinterpret_cast<const uint16_t*>(base + row * DIM + 2 * lane);
+    const float2 a = e4m3x2_to_float2(w);
+    x[0] = a.x;
+    x[1] = a.y;
+  }
+}
+
+// d = 64 NVFP4 row slice of this lane: 2 elements (one byte) times the E4M3
+// scale of its 16-element group.
+__device__ __forceinline__ void load_nvfp4(const uint8_t* __restrict__ codes,
+                                           const uint8_t* __restrict__ scales, size_t row,
+                                           int lane, float (&x)[2]) {
+  const float2 v = e2m1x2_to_float2(codes[row * 32 + lane]);
+  const float sc = e4m3x2_to_float2(scales[row * 4 + lane / 8]).x;
+  x[0] = v.x * sc;
+  x[1] = v.y * sc;
+}
+
+// Score operand rows: E4M3 codes, or the NVFP4 values on the mixed path.
+template <int DIM, bool NVF4>
+__device__ __forceinline__ void load_score_rows(const ShortParams& prm, bool is_q, size_t row,
+                                                int lane, float (&x)[DIM / 32]) {
+  if constexpr (NVF4) {
+    static_assert(DIM == 64, "the NVFP4 score product is built for head dim 64");
+    load_nvfp4(is_q ? prm.q4c : prm.k4c, is_q ? prm.q4s : prm.k4s, row, lane, x);
+  } else {
+    load_codes<DIM>(is_q ? prm.qc : prm.kc, row, lane, x);
+  }
+}
+
+template <int DIM>
+__device__ __forceinline__ float warp_dot(const float (&a)[DIM / 32], const float (&b)[DIM / 32]) {
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < DIM / 32; ++i) acc = fmaf(a[i], b[i], acc);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  return acc;
+}
+
+template <int DIM>
+__device__ __forceinline__ void store_bf16(__nv_bfloat16* __restrict__ dst, size_t row, int lane,
+                                           const float (&x)[DIM / 32]) {
+  if constexpr (DIM == 128) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]), b = __floats2bfloat162_rn(x[2], x[3]);
+    *reinterpret_cast<uint2*>(dst + row * DIM + 4 * lane) =
+        make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+  } else {
+    __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]);
+    *reinterpret_cast<uint32_t*>(dst + row * DIM + 2 * lane) = *reinterpret_cast<uint32_t*>(&a);
+  }
+}
+
+
+template <int DIM, bool NVF4>
+__global__ void __launch_bounds__(32 * kShortWarps)
+    attn_fwd_short_kernel(const ShortParams prm) {
+  const int lane = threadIdx.x & 31;
+  const long long wid = static_cast<long long>(blockIdx.x) * kShortWarps + (threadIdx.x >> 5);
+  const int H = prm.H, T = prm.T;
+  if (wid >= static_cast<long long>(prm.ndocs) * H) return;
+  const int doc = static_cast<int>(wid / H), h = static_cast<int>(wid % H);
+  const int s = min(max(prm.cu[doc], 0), T);
+  const int e = min(max(prm.cu[doc + 1], s), T);
+  const int L = e - s;
+  if (L == 0 || L > kShortDoc) return;  // longer documents run on the tile kernels
+  const size_t hT = static_cast<size_t>(h) * T;
+  // one scale block per operand: the exponents of the document's first token
+  // (on the mixed path the NVFP4 values carry their own scales)
+  const float cf = NVF4 ? prm.scale_log2
+                        : prm.scale_log2 * pow2_or_zero_s(static_cast<int>(prm.qs[hT + s]) - 127) *
+                              pow2_or_zero_s(static_cast<int>(prm.ks[hT + s]) - 127);
+  const float vsc = pow2_or_zero_s(static_cast<int>(prm.vs[hT + s]) - 127);
+  for (int i = 0; i < L; ++i) {
+    float q[DIM / 32];
+    load_score_rows<DIM, NVF4>(prm, true, static_cast<size_t>(s + i) * H + h, lane, q);
+    // lane j keeps the raw score of key j (visible keys: j <= i)
+    float sj = 0.f;
+    const bool vis = lane <= i;
+    for (int j = 0; j <= i; ++j) {
+      float k[DIM / 32];
+      load_score_rows<DIM, NVF4>(prm, false, static_cast<size_t>(s + j) * H + h, lane, k);
+      const float dot = warp_dot<DIM>(q, k);
+      if (lane == j) sj = dot;
+    }
+    float mx = vis ? sj * cf : -INFINITY;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    const float m = ceilf(mx);
+    const float p8 = vis ? ex2_approx(fmaf(sj, cf, -(m - 8.f))) : 0.f;
+    float l8 = p8;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) l8 += __shfl_xor_sync(0xffffffffu, l8, off);
+    const float ph = e4m3x2_to_float2(cvt_e4m3x2(p8, 0.f)).x;  // the E4M3 operand value
+    float acc[DIM / 32] = {};
+    for (int j = 0; j <= i; ++j) {
+      const float pj = __shfl_sync(0xffffffffu, ph, j);
+      float v[DIM / 32];
+      load_codes<DIM>(prm.vc, static_cast<size_t>(s + j) * H + h, lane, v);
+#pragma unroll
+      for (int c = 0; c < DIM / 32; ++c) acc[c] = fmaf(pj, v[c], acc[c]);
+    }
+    const float inv = vsc / l8;
+#pragma unroll
+    for (int c = 0; c < DIM / 32; ++c) acc[c] *= inv;
+    store_bf16<DIM>(prm.o, static_cast<size_t>(s + i) * H + h, lane, acc);
+    if (lane == 0) prm.lse[hT + s + i] = (m - 8.f + __log2f(l8)) * 0.69314718055994530942f;
+  }
+}
+
+template <int DIM, bool NVF4>
+__global__ void __launch_bounds__(32 * kShortWarps)
+    attn_bwd_short_kernel(const ShortParams prm) {
+  // per warp: the document's 2^8 P (dV operand before rounding) and dS
+  __shared__ float s_p[kShortWarps][kShortDoc][kShortDoc + 1];
+  __shared__ float s_ds[kShortWarps][kShortDoc][kShortDoc + 1];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const long long wid = static_cast<long long>(blockIdx.x) * kShortWarps + w;
+  const int H = prm.H, T = prm.T;
+  if (wid >= static_cast<long long>(prm.ndocs) * H) return;
+  const int doc = static_cast<int>(wid / H), h = static_cast<int>(wid % H);
+  const int s = min(max(prm.cu[doc], 0), T);
+  const int e = min(max(prm.cu[doc + 1], s), T);
+  const int L = e - s;
+  if (L == 0 || L > kShortDoc) return;
+  const size_t hT = static_cast<size_t>(h) * T;
+  const int eq = static_cast<int>(prm.qs[hT + s]) - 127, ek = static_cast<int>(prm.ks[hT + s]) - 127;
+  const int ev = static_cast<int>(prm.vs[hT + s]) - 127, edo = static_cast<int>(prm.dos[hT + s]) - 127;
+  const float cf = NVF4 ? prm.scale_log2 : prm.scale_log2 * pow2_or_zero_s(eq) * pow2_or_zero_s(ek);
+  const float gp = pow2_or_zero_s(ev) * pow2_or_zero_s(edo);
+  const float LOG2E = 1.4426950408889634f;
+  // P (x 2^8) and dS (x 2^8) of every visible pair, lane = key
+  float amax = 0.f;
+  for (int i = 0; i < L; ++i) {
+    float q[DIM / 32], g[DIM / 32];
+    load_score_rows<DIM, NVF4>(prm, true, static_cast<size_t>(s + i) * H + h, lane, q);
+    load_codes<DIM>(prm.doc_, static_cast<size_t>(s + i) * H + h, lane, g);
+    const float nl = 8.f - prm.lse_in[hT + s + i] * LOG2E;
+    const float Di = prm.D[hT + s + i];
+    for (int j = 0; j <= i; ++j) {
+      float k[DIM / 32], v[DIM / 32];
+      load_score_rows<DIM, NVF4>(prm, false, static_cast<size_t>(s + j) * H + h, lane, k);
+      load_codes<DIM>(prm.vc, static_cast<size_t>(s + j) * H + h, lane, v);
+      const float sd = warp_dot<DIM>(q, k);
+      const float dp = warp_dot<DIM>(g, v);
+      const float p8 = ex2_approx(fmaf(sd, cf, nl));
+      const float d8 = p8 * fmaf(dp, gp, -Di);
+      if (lane == 0) {
+        s_p[w][i][j] = p8;
+        s_ds[w][i][j] = d8;
+      }
+      amax = fmaxf(amax, fabsf(d8));
+    }
+  }
+  __syncwarp();
+  // the document is one 32x32 dS block: one round-up exponent
+  const int eb = max(roundup_exponent(amax) - 8, -127);
+  const float inv = exp2i(-(eb + 8)), dsc = pow2_or_zero_s(eb);
+  // dQ_i = scale * sum_j dS^_ij K^_j  (float32 rows of the accumulator)
+  for (int i = 0; i < L; ++i) {
+    float acc[DIM / 32] = {};
+    for (int j = 0; j <= i; ++j) {
+      const float dsh = e4m3x2_to_float2(cvt_e4m3x2(s_ds[w][i][j] * inv, 0.f)).x * dsc;
+      float k[DIM / 32];
+      load_codes<DIM>(prm.kc, static_cast<size_t>(s + j) * H + h, lane, k);
+#pragma unroll
+      for (int c = 0; c < DIM / 32; ++c) acc[c] = fmaf(dsh, k[c], acc[c]);
+    }
+    const float mul = prm.sm_scale * pow2_or_zero_s(ek);
+    float* dst = prm.dq_acc + (static_cast<size_t>(s + i) * H + h) * DIM + (DIM / 32) * lane;
+#pragma unroll
+    for (int c = 0; c < DIM / 32; ++c) dst[c] = acc[c] * mul;
+  }
+  // dK_j = scale * sum_i dS^_ij Q^_i,  dV_j = 2^-8 sum_i P^b_ij dO^_i
+  for (int j = 0; j < L; ++j) {
+    float ak[DIM / 32] = {}, av[DIM / 32] = {};
+    for (int i = j; i < L; ++i) {
+      const float dsh = e4m3x2_to_float2(cvt_e4m3x2(s_ds[w][i][j] * inv, 0.f)).x * dsc;
+      const float pb = e4m3x2_to_float2(cvt_e4m3x2(s_p[w][i][j], 0.f)).x;
+      float q[DIM / 32], g[DIM / 32];
+      load_codes<DIM>(prm.qc, static_cast<size_t>(s + i) * H + h, lane, q);
+      load_codes<DIM>(prm.doc_, static_cast<size_t>(s + i) * H + h, lane, g);
+#pragma unroll
+      for (int c = 0; c < DIM / 32; ++c) {
+        ak[c] = fmaf(dsh, q[c], ak[c]);
+        av[c] = fmaf(pb, g[c], av[c]);
+      }
+    }
+    const float mk = prm.sm_scale * pow2_or_zero_s(eq), mv = pow2_or_zero_s(edo) * (1.f / 256.f);
+#pragma unroll
+    for (int c = 0; c < DIM / 32; ++c) {
+      ak[c] *= mk;
+      av[c] *= mv;
+    }
+    store_bf16<DIM>(prm.dk, static_cast<size_t>(s + j) * H + h, lane, ak);
+    store_bf16<DIM>(prm.dv, static_cast<size_t>(s + j) * H + h, lane, av);
+  }
+}
+
+ShortParams make_params(const flamia_qtensor* q, const flamia_qtensor* k, const flamia_qtensor* v,
+                        const int32_t* cu, int ndocs, int T, int H, float softmax_scale) {
+  ShortParams p{};
+  p.q4c = q->nvfp4_codes;
+  p.k4c = k->nvfp4_codes;
+  p.q4s = q->nvfp4_scales;
+  p.k4s = k->nvfp4_scales;
+  p.qc = q->codes;
+  p.kc = k->codes;
+  p.vc = v->codes;
+  p.qs = q->scales;
+  p.ks = k->scales;
+  p.vs = v->scales;
+  p.cu = cu;
+  p.T = T;
+  p.H = H;
+  p.ndocs = ndocs;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.sm_scale = softmax_scale;
+  return p;
+}
+
+inline unsigned short_grid(int ndocs, int H) {
+  const long long warps = static_cast<long long>(ndocs) * H;
+  return static_cast<unsigned>((warps + kShortWarps - 1) / kShortWarps);
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_short(const flamia_qtensor* q, const flamia_qtensor* k,
+                             const flamia_qtensor* v, const int32_t* cu, int ndocs, int T, int H,
+                             int d, float softmax_scale, bool nvfp4_qk, void* o, float* lse,
+                             cudaStream_t stream) {
+  ShortParams p = make_params(q, k, v, cu, ndocs, T, H, softmax_scale);
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  const unsigned grid = short_grid(ndocs, H);
+  if (nvfp4_qk)
+    attn_fwd_short_kernel<64, true><<<grid, 32 * kShortWarps, 0, stream>>>(p);
+  else if (d == 128)
+    attn_fwd_short_kernel<128, false><<<grid, 32 * kShortWarps, 0, stream>>>(p);
+  else
+    attn_fwd_short_kernel<64, false><<<grid, 32 * kShortWarps, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_short(const flamia_qtensor* q, const flamia_qtensor* k,
+                             const flamia_qtensor* v, const flamia_qtensor* dout, const float* D,
+                             const float* lse, const int32_t* cu, int ndocs, int T, int H, int d,
+                             float softmax_scale, bool nvfp4_qk, float* dq_acc, void* dk, void* dv,
+                             cudaStream_t stream) {
+  ShortParams p = make_params(q, k, v, cu, ndocs, T, H, softmax_scale);
+  p.doc_ = dout->codes;
+  p.dos = dout->scales;
+  p.lse_in = lse;
+  p.D = D;
+  p.dq_acc = dq_acc;
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  const unsigned grid = short_grid(ndocs, H);
+  if (nvfp4_qk)
+    attn_bwd_short_kernel<64, true><<<grid, 32 * kShortWarps, 0, stream>>>(p);
+  else if (d == 128)
+    attn_bwd_short_kernel<128, false><<<grid, 32 * kShortWarps, 0, stream>>>(p);
+  else
+    attn_bwd_short_kernel<64, false><<<grid, 32 * kShortWarps, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace flamia

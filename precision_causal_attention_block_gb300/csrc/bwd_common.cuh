@@ -1,0 +1,112 @@
+// Pieces shared by the backward kernels (attn_bwd.cu: head dims 64 and the
+// mixed NVFP4 path; attn_bwd128.cu: the pipelined head-dim-128 kernel).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+#include "short_docs.cuh"
+
+namespace flamia {
+
+struct BwdParams {
+  const uint8_t* q_scales;
+  const uint8_t* k_scales;
+  const uint8_t* v_scales;
+  const uint8_t* do_scales;
+  const uint32_t* q4_scales;  // NVFP4: 4 E4M3 scales per (token, head) as one word (d = 64)
+  const uint32_t* k4_scales;
+  const float* D;
+  const float* lse;
+  const int32_t* cu;
+  const int* wl_header;
+  const int4* items;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int T, H, ndocs, cap;
+  float scale_log2;  // softmax_scale * log2(e)
+  float sm_scale;
+  int* status;
+};
+
+__device__ __forceinline__ float pow2_or_zero(int k) { return k < -126 ? 0.f : exp2i(k); }
+
+// One 32-column chunk of a key row: P (operand codes), dS (float, 2^8-scaled)
+// and the chunk's |dS| maximum.  MASK: diagonal tile, query < key is masked.
+template <bool MASK>
+__device__ __forceinline__ float bwd_chunk(const uint32_t (&sv)[32], uint32_t (&dv)[32],
+                                           const float* nl, const float* dd, float fS, float fP,
+                                           int col0, int key, uint32_t (&pw)[8]) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; i += 4) {
+    const float4 n4 = *reinterpret_cast<const float4*>(nl + i);
+    const float4 d4 = *reinterpret_cast<const float4*>(dd + i);
+    float2 s01 = __ffma2_rn(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])),
+                            make_float2(fS, fS), make_float2(n4.x, n4.y));
+    float2 s23 = __ffma2_rn(make_float2(__uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3])),
+                            make_float2(fS, fS), make_float2(n4.z, n4.w));
+    if (MASK) {
+      if (col0 + i + 0 < key) s01.x = -INFINITY;
+      if (col0 + i + 1 < key) s01.y = -INFINITY;
+      if (col0 + i + 2 < key) s23.x = -INFINITY;
+      if (col0 + i + 3 < key) s23.y = -INFINITY;
+    }
+    const float2 p01 = make_float2(ex2_approx(s01.x), ex2_approx(s01.y));
+    const float2 p23 = make_float2(ex2_approx(s23.x), ex2_approx(s23.y));
+    const float2 g01 = __ffma2_rn(make_float2(__uint_as_float(dv[i]), __uint_as_float(dv[i + 1])),
+                                  make_float2(fP, fP), make_float2(-d4.x, -d4.y));
+    const float2 g23 =
+        __ffma2_rn(make_float2(__uint_as_float(dv[i + 2]), __uint_as_float(dv[i + 3])),
+                   make_float2(fP, fP), make_float2(-d4.z, -d4.w));
+    const float2 d01 = __fmul2_rn(p01, g01);
+    const float2 d23 = __fmul2_rn(p23, g23);
+    amax = fmax3(fabsf(d01.x), fabsf(d01.y), amax);
+    amax = fmax3(fabsf(d23.x), fabsf(d23.y), amax);
+    dv[i] = __float_as_uint(d01.x);
+    dv[i + 1] = __float_as_uint(d01.y);
+    dv[i + 2] = __float_as_uint(d23.x);
+    dv[i + 3] = __float_as_uint(d23.y);
+    pw[i / 4] = cvt_e4m3x2(p01.x, p01.y) | (cvt_e4m3x2(p23.x, p23.y) << 16);
+  }
+  return amax;
+}
+
+// One backward work item (128-key tile of one document x one head), decoded
+// identically by every role; false for items of short documents, which the
+// CUDA-core kernel handles.
+struct BwdItem {
+  int h, s, e, k0, k1, nq;
+};
+
+__device__ __forceinline__ bool decode_bwd_item(const BwdParams& prm, int n_items, int idx,
+                                                BwdItem& it) {
+  const int T = prm.T;
+  it.h = idx / n_items;  // head-major: a wave of CTAs touches the Q / dO / dQ of few heads
+  const int4 item = prm.items[idx % n_items];
+  // clamped: a malformed work list or offsets cannot index outside [0, T)
+  const int doc = min(max(item.x, 0), prm.ndocs - 1);
+  it.s = min(max(prm.cu[doc], 0), T);
+  it.e = min(max(prm.cu[doc + 1], it.s), T);
+  if (it.e - it.s <= kShortDoc) return false;
+  it.k0 = it.s + ((min(max(item.y, it.s), it.e) - it.s) & ~(kTile - 1));
+  it.k1 = min(max(item.z, it.k0), min(it.k0 + kTile, it.e));
+  it.nq = (it.e - it.k0 + kTile - 1) / kTile;  // query tiles from the diagonal to the end
+  return true;
+}
+
+// The CTA's items in snake order over the head-major (head, item) list.
+__device__ __forceinline__ int snake_index_b(int round) {
+  const int G = gridDim.x, b = blockIdx.x;
+  return round * G + ((round & 1) ? G - 1 - b : b);
+}
+
+// Pipelined backward for head dim 128 (MXFP8 score product); grid = CTAs.
+cudaError_t launch_bwd128_pipelined(const BwdParams& prm, const flamia_qtensor* q,
+                                    const flamia_qtensor* k, const flamia_qtensor* v,
+                                    const flamia_qtensor* dout, float* acc, unsigned grid,
+                                    cudaStream_t stream);
+
+}  // namespace flamia

@@ -16,6 +16,9 @@ namespace flamia {
 constexpr int kTile = 128;       // query / key tile (MMA M and N)
 constexpr int kBlock = 32;       // token block of the scales
 constexpr int kFwdItem = 256;    // queries per forward work item
+// Documents of at most this many tokens (one 32-token scale block) run on the
+// CUDA-core kernels of attn_short.cu; the tile kernels skip them.
+constexpr int kShortDoc = 32;
 
 // ------------------------------------------------------------------ work list
 
@@ -24,8 +27,9 @@ struct WorklistLayout {
   int nbuckets;                // costs 0 .. nbuckets-1
   int chunks_fwd, chunks_bwd;  // 1024-item chunks of the counting sort
   size_t off_fwd, off_bwd;     // byte offsets of the sorted item arrays
-  size_t off_doc_counts;       // int32 [2][ndocs]: items per document
-  size_t off_doc_offsets;      // int32 [2][ndocs]: exclusive prefix of the counts
+  size_t off_tile_fwd, off_tile_bwd;  // the same lists without short-document items
+  size_t off_doc_counts;       // int32 [4][ndocs]: in-chunk prefixes of 4 per-document counts
+  size_t off_doc_offsets;      // int32 [4][doc chunks]: chunk totals, then chunk offsets
   size_t off_gen_fwd, off_gen_bwd;  // int4 items in generation order
   size_t off_hist_fwd, off_hist_bwd;  // int32 [chunks][nbuckets]
   size_t off_buckets;                 // int32 [2][nbuckets]
@@ -48,10 +52,15 @@ inline WorklistLayout worklist_layout(int T, int ndocs) {
   o = align_up(o + 16ull * L.cap_fwd, 256);
   L.off_bwd = o;
   o = align_up(o + 16ull * L.cap_bwd, 256);
+  L.off_tile_fwd = o;
+  o = align_up(o + 16ull * L.cap_fwd, 256);
+  L.off_tile_bwd = o;
+  o = align_up(o + 16ull * L.cap_bwd, 256);
+  // everything below is the builder's scratch
   L.off_doc_counts = o;
-  o = align_up(o + 8ull * (ndocs + 1), 256);
+  o = align_up(o + 16ull * (ndocs + 1), 256);
   L.off_doc_offsets = o;
-  o = align_up(o + 8ull * (ndocs + 1), 256);
+  o = align_up(o + 16ull * ((ndocs + kSortChunk - 1) / kSortChunk + 1), 256);
   L.off_gen_fwd = o;
   o = align_up(o + 16ull * L.cap_fwd, 256);
   L.off_gen_bwd = o;
@@ -66,8 +75,21 @@ inline WorklistLayout worklist_layout(int T, int ndocs) {
   return L;
 }
 
-// Header words of the work-list buffer.
-enum : int { kHdrNFwd = 0, kHdrNBwd = 1, kHdrCapFwd = 2, kHdrCapBwd = 3, kHdrMaxCost = 4 };
+// Header words of the work-list buffer: list sizes and capacities, the
+// largest cost, the sizes of the tile lists (items of documents longer than
+// kShortDoc, which the tile kernels process) and, internal to the builder, the
+// number of documents with a long cost-1 item in each list.
+enum : int {
+  kHdrNFwd = 0,
+  kHdrNBwd = 1,
+  kHdrCapFwd = 2,
+  kHdrCapBwd = 3,
+  kHdrMaxCost = 4,
+  kHdrTileFwd = 5,
+  kHdrTileBwd = 6,
+  kHdrLong1Fwd = 7,
+  kHdrLong1Bwd = 8
+};
 
 // ------------------------------------------------------------------ checks
 
@@ -80,6 +102,15 @@ inline bool supported_dim(int d) { return d == 64 || d == 128; }
 inline bool valid_sizes(int T, int H, int d, int ndocs) {
   return T > 0 && T < (1 << 24) && H > 0 && H <= 4096 && ndocs >= 1 && ndocs <= T + 1 &&
          static_cast<long long>(T) * H * d < (1ll << 40) && supported_dim(d);
+}
+
+// Streaming multiprocessors of the current device (persistent grids).
+inline int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 148;
+  return n;
 }
 
 // ------------------------------------------------------------------ tensor maps
@@ -127,7 +158,8 @@ inline bool make_matrix_map(CUtensorMap* map, const void* base, int rows, int ro
 // A float32 [T, H, d] tensor seen as 3-D (dim, head, token); box = (32, 1,
 // box_rows) with 128-byte swizzle (one 128-byte row of 32 floats per token).
 inline bool make_f32_token_map(CUtensorMap* map, const void* base, int T, int H, int d,
-                               int box_rows) {
+                               int box_rows,
+                               CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn enc = get_encode_tiled();
   if (!enc) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
@@ -136,7 +168,7 @@ inline bool make_f32_token_map(CUtensorMap* map, const void* base, int T, int H,
   cuuint32_t box[3] = {32u, 1u, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims,
-                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }

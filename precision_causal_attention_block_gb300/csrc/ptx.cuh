@@ -345,6 +345,18 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t codes) {
   return __half22float2(h);
 }
 
+// Two E2M1 codes (bits 0..3 and 4..7) -> two exact floats.
+__device__ __forceinline__ float2 e2m1x2_to_float2(uint32_t codes) {
+  uint32_t h2;
+  asm("{\n\t.reg .b8 t;\n\t"
+      "cvt.u8.u32 t, %1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+      : "=r"(h2)
+      : "r"(codes & 0xFFu));
+  __half2 h = *reinterpret_cast<__half2*>(&h2);
+  return __half22float2(h);
+}
+
 // Two floats -> two E2M1 codes (round to nearest even, saturating): lo in
 // bits 0..3, hi in bits 4..7.
 __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {

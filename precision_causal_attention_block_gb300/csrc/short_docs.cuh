@@ -1,0 +1,23 @@
+// Documents of at most kShortDoc tokens run on the CUDA cores (attn_short.cu);
+// the tile kernels skip them.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "../../include/flamia.h"
+#include "common.cuh"
+
+namespace flamia {
+
+cudaError_t launch_fwd_short(const flamia_qtensor* q, const flamia_qtensor* k,
+                             const flamia_qtensor* v, const int32_t* cu, int ndocs, int T, int H,
+                             int d, float softmax_scale, bool nvfp4_qk, void* o, float* lse,
+                             cudaStream_t stream);
+
+cudaError_t launch_bwd_short(const flamia_qtensor* q, const flamia_qtensor* k,
+                             const flamia_qtensor* v, const flamia_qtensor* dout, const float* D,
+                             const float* lse, const int32_t* cu, int ndocs, int T, int H, int d,
+                             float softmax_scale, bool nvfp4_qk, float* dq_acc, void* dk, void* dv,
+                             cudaStream_t stream);
+
+}  // namespace flamia

@@ -55,6 +55,40 @@ def test_ragged_small_elementwise(lib, d):
     compare("D", call.D.cpu().numpy(), ref["D"], cos_min=0.99999, rel_max=1e-3)
 
 
+SHORT_MIX = [1, 2, 5, 17, 31, 32, 33, 40, 3, 0, 300, 1]
+
+
+@pytest.mark.parametrize("d,nvfp4", [(64, False), (128, False), (64, True)])
+def test_short_documents_elementwise(lib, d, nvfp4):
+    """Documents of at most one 32-token block (one scale per operand) beside
+    longer ones: the packed-document case of the review page, sec. 3.4."""
+    w = W.custom("short_mix", SHORT_MIX, 3, d, seed=21, structure="outlier16x2")
+    x = W.make_inputs_bf16(w)
+    call = run_call(w, x, nvfp4=nvfp4)
+    fmt = "nvfp4" if nvfp4 else "mxfp8"
+    ref = O.attention(*[x[n].double().numpy() for n in NAMES], w.cu_seqlens, w.sm_scale,
+                      qk_format=fmt)
+    check_against(call, ref, slice(0, w.T), list(range(w.H)))
+
+
+def test_all_zero_short_document(lib):
+    """An all-zero query block has the smallest scale exponent; its scores are
+    0 and attention is uniform over the visible keys (no NaN from masking)."""
+    w = W.custom("zero_doc", [7, 20, 45], 2, 128, seed=23)
+    x = W.make_inputs_bf16(w)
+    x["q"][7:27] = 0
+    x["k"][0:7] = 0
+    call = run_call(w, x)
+    for t in (call.o, call.lse, call.dq, call.dk, call.dv):
+        assert torch.isfinite(t.float()).all()
+    ref = O.attention(*[x[n].double().numpy() for n in NAMES], w.cu_seqlens, w.sm_scale)
+    check_against(call, ref, slice(0, w.T), list(range(w.H)))
+    # uniform attention: O_i = mean of the dequantised V rows up to i
+    v = O.dequantize_tokenblock(ref["quantized"].vc, ref["quantized"].vs)
+    want = np.cumsum(v[7:27], 0) / np.arange(1, 21)[:, None, None]
+    compare("O uniform", np64(call.o[7:27]), want)
+
+
 def test_tiny_config(lib):
     w = W.tiny()
     x = W.make_inputs_bf16(w)

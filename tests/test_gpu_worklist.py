@@ -25,9 +25,22 @@ def build(cu, T):
     hdr = raw[:HDR_BYTES].view(np.int32)
     nf, nb, capf, capb = (int(v) for v in hdr[:4])
     fwd = raw[HDR_BYTES:HDR_BYTES + 16 * nf].view(np.int32).reshape(-1, 4)
-    off_bwd = ((HDR_BYTES + 16 * capf) + 255) // 256 * 256
+    al = lambda x: (x + 255) // 256 * 256
+    off_bwd = al(HDR_BYTES + 16 * capf)
     bwd = raw[off_bwd:off_bwd + 16 * nb].view(np.int32).reshape(-1, 4)
-    return fwd, bwd, int(st.item()), int(hdr[4])
+    off_tf = al(off_bwd + 16 * capb)
+    off_tb = al(off_tf + 16 * capf)
+    ntf, ntb = int(hdr[5]), int(hdr[6])
+    tiles = (raw[off_tf:off_tf + 16 * ntf].view(np.int32).reshape(-1, 4),
+             raw[off_tb:off_tb + 16 * ntb].view(np.int32).reshape(-1, 4))
+    return fwd, bwd, int(st.item()), int(hdr[4]), tiles
+
+
+def tile_list(items, cu, short=32):
+    """The lists the tile kernels walk: the same order without the items of
+    documents of at most `short` tokens (those run on the CUDA-core path)."""
+    keep = [i for i, it in enumerate(items) if cu[it[0] + 1] - cu[it[0]] > short]
+    return items[keep]
 
 
 @pytest.mark.parametrize("cu", [
@@ -37,23 +50,26 @@ def build(cu, T):
     [0, 256, 512, 513, 900, 900, 2049],
 ])
 def test_small_lists(lib, cu):
-    fwd, bwd, st, maxc = build(cu, cu[-1])
+    fwd, bwd, st, maxc, (tf, tb) = build(cu, cu[-1])
     rf, rb = O.build_worklist(cu)
     assert st == 0
     assert np.array_equal(fwd, rf) and np.array_equal(bwd, rb)
     assert maxc == (rf[0, 3] if len(rf) else 0)
+    assert np.array_equal(tf, tile_list(rf, cu)) and np.array_equal(tb, tile_list(rb, cu))
 
 
 @pytest.mark.parametrize("name", ["tiny", "fixed4x4096", "varlen65536", "onetoken131072",
                                   "long131072"])
 def test_configs(lib, name):
     w = W.WORKLOADS[name]()
-    fwd, bwd, st, _ = build(list(w.cu_seqlens), w.T)
-    rf, rb = O.build_worklist(w.cu_seqlens)
+    cu = list(w.cu_seqlens)
+    fwd, bwd, st, _, (tf, tb) = build(cu, w.T)
+    rf, rb = O.build_worklist(cu)
     assert st == 0
     assert np.array_equal(fwd, rf) and np.array_equal(bwd, rb)
+    assert np.array_equal(tf, tile_list(rf, cu)) and np.array_equal(tb, tile_list(rb, cu))
 
 
 def test_bad_seqlens_flagged(lib):
-    _, _, st, _ = build([0, 10, 5, 20], 20)
+    _, _, st, _, _ = build([0, 10, 5, 20], 20)
     assert st & 1

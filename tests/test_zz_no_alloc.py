@@ -20,11 +20,18 @@ pytestmark = pytest.mark.gpu
 def _lists(wl_u8):
     raw = wl_u8.cpu().numpy()
     hdr = raw[:64].view(np.int32)
-    nf, nb, capf = int(hdr[0]), int(hdr[1]), int(hdr[2])
+    nf, nb, capf, capb = int(hdr[0]), int(hdr[1]), int(hdr[2]), int(hdr[3])
+    al = lambda x: (x + 255) // 256 * 256
     fwd = raw[64:64 + 16 * nf].view(np.int32).reshape(-1, 4)
-    off_bwd = ((64 + 16 * capf) + 255) // 256 * 256
+    off_bwd = al(64 + 16 * capf)
     bwd = raw[off_bwd:off_bwd + 16 * nb].view(np.int32).reshape(-1, 4)
-    return hdr[:5].copy(), fwd.copy(), bwd.copy()
+    # the lists without short documents follow, sized by header words 5 and 6
+    off_tf = al(off_bwd + 16 * capb)
+    off_tb = al(off_tf + 16 * capf)
+    tf = raw[off_tf:off_tf + 16 * int(hdr[5])]
+    tb = raw[off_tb:off_tb + 16 * int(hdr[6])]
+    return hdr[:7].copy(), np.concatenate([fwd.ravel(), tf.view(np.int32)]), \
+        np.concatenate([bwd.ravel(), tb.view(np.int32)])
 
 
 def _call_both(lib, cu_list, T):
