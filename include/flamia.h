@@ -117,7 +117,9 @@ flamia_status flamia_quantize_tokenblock(const void* x_bf16, int T, int H, int d
  * 256-byte aligned):
  *   int32 header[16]: [0] n_fwd, [1] n_bwd, [2] cap_fwd, [3] cap_bwd,
  *                     [4] max cost, [5] n_tile_fwd, [6] n_tile_bwd;
- *                     [7], [8] used by the builder; the rest reserved.
+ *                     [7], [8] used by the builder; [9] .. [12] item claim
+ *                     counters of the attention kernels (zero between
+ *                     calls); the rest reserved.
  *   int32x4 fwd_items[cap_fwd] at byte 64: {doc, q_start, q_end, cost}
  *   int32x4 bwd_items[cap_bwd] after it:    {doc, k_start, k_end, cost}
  *   int32x4 tile_fwd[cap_fwd], tile_bwd[cap_bwd] after them: the same two
@@ -174,14 +176,19 @@ flamia_status flamia_build_worklist_static(const int32_t* cu_seqlens, int ndocs,
  *
  *  q, k, v      host pointers to quantised operands (E4M3 + scales; with
  *               FLAMIA_FLAG_NVFP4_QK also the NVFP4 copies of q and k).
- *  wl           a work list built for the same cu_seqlens / T.
+ *  wl           a work list built for the same cu_seqlens / T.  Items are
+ *               claimed dynamically in list order (longest first, sec. 3.4:
+ *               the paper's dynamic assignment for causal calls) through a
+ *               counter in the list's header, which the call updates and
+ *               resets before it ends; calls that share one work list must
+ *               not run at the same time (a forward and a backward may).
  *  o_bf16       [T, H, d] BF16 output.   lse  float [H, T] (natural log).
  * Only tokens inside documents are written.
  */
 flamia_status flamia_attn_fwd(const flamia_qtensor* q, const flamia_qtensor* k,
                               const flamia_qtensor* v, const int32_t* cu_seqlens, int ndocs,
                               int T, int H, int d, float softmax_scale, int flags,
-                              const void* wl, void* o_bf16, float* lse, int* dev_status,
+                              void* wl, void* o_bf16, float* lse, int* dev_status,
                               void* stream);
 
 /*
@@ -206,12 +213,13 @@ size_t flamia_bwd_workspace_bytes(int T, int H, int d);
  *  D, lse       float [H, T] from the quantiser and the forward.
  *  dq, dk, dv   [T, H, d] BF16 outputs (only tokens inside documents written).
  *  ws           flamia_bwd_workspace_bytes(T, H, d) bytes, 256-byte aligned.
+ *  wl           as for the forward (its own claim counter).
  */
 flamia_status flamia_attn_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
                               const flamia_qtensor* v, const flamia_qtensor* dout,
                               const float* D, const float* lse,
                               const int32_t* cu_seqlens, int ndocs, int T, int H, int d,
-                              float softmax_scale, int flags, const void* wl,
+                              float softmax_scale, int flags, void* wl,
                               void* dq_bf16, void* dk_bf16, void* dv_bf16,
                               void* ws, size_t ws_bytes, int* dev_status, void* stream);
 

@@ -66,6 +66,8 @@ struct BwdSmem {
   uint64_t bar_qd_empty[kBStages];
   uint64_t bar_s_full, bar_ds_full, bar_dq_full, bar_s_free, bar_done, bar_sf;
   uint64_t bar_kv_free, bar_acc_empty;
+  ItemRing<4> ring;  // claimed items: producer -> MMA issuer, compute leader
+  int item_bc[2];    // the compute leader's copy for the compute groups
   uint32_t tmem_base;
   volatile int abort;
 };
@@ -96,7 +98,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int H = prm.H, T = prm.T;
   const int n_items = min(prm.wl_header[kHdrTileBwd], prm.cap);
   const int total = n_items * H;
-  if (static_cast<int>(blockIdx.x) >= total) return;  // uniform over the CTA
+  if (static_cast<int>(blockIdx.x) >= total) {  // uniform over the CTA
+    if (threadIdx.x == 0) finish_claims(prm.wl_header + kHdrBwdNext, prm.wl_header + kHdrBwdExit);
+    return;
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&sm.bar_kv), 1);
@@ -112,6 +117,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(smem_u32(&sm.bar_acc_empty), kComputeThreads);
     mbar_init(smem_u32(&sm.bar_done), 1);
     mbar_init(smem_u32(&sm.bar_sf), kTile);
+    ring_init(sm.ring, 2);
     sm.abort = 0;
     fence_barrier_init();
   }
@@ -139,11 +145,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int nk = 0;  // items whose K / V were loaded
       int uc = 0;  // query tiles loaded over all items
       bool ok = true;
-      for (int round = 0; ok; ++round) {
-        const int idx = snake_index_b(round);
-        if (idx >= total) break;
+      // items in head-major, longest-first order, claimed one at a time: a CTA
+      // takes the next item when it has issued its current item's last load
+      int* counter = prm.wl_header + kHdrBwdNext;
+      int idx = claim_item(counter);
+      for (int n = 0; ok; ++n) {
+        const bool end = idx >= total;
+        if (!ring_put(sm.ring, n, end ? total : idx) || sm.abort) {
+          ok = false;
+          break;
+        }
+        if (end) break;
         BwdItem it;
-        if (!decode_bwd_item(prm, n_items, idx, it)) continue;
+        if (!decode_bwd_item(prm, n_items, idx, it)) {
+          idx = claim_item(counter);
+          continue;
+        }
         // the previous item's K / V are free once its last products are done
         if (nk > 0 && (!mbar_wait(smem_u32(&sm.bar_kv_free), (nk - 1) & 1) || sm.abort)) {
           ok = false;
@@ -168,6 +185,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tma_load_3d(smem_u32(sm.dout[st]), &map_do, bf, 0, it.h, it.k0 + u * kTile);
           if (NVF4) tma_load_3d(smem_u32(sm.q4[st]), &map_q4, bf, 0, it.h, it.k0 + u * kTile);
         }
+        if (ok) idx = claim_item(counter);
       }
       if (nk > 0) ok &= mbar_wait(bkv, (nk - 1) & 1);
       for (int u = max(0, uc - kBStages); u < uc; ++u)
@@ -182,8 +200,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint32_t pba = smem_u32(sm.pb), dsa = smem_u32(sm.ds);
       int nk = 0, uc = 0;  // items and query tiles consumed so far
       bool ok = true;
-      for (int round = 0; ok; ++round) {
-        const int idx = snake_index_b(round);
+      for (int n = 0; ok; ++n) {
+        const int idx = ring_get(sm.ring, n, true);
+        if (idx < 0) {
+          ok = false;
+          break;
+        }
         if (idx >= total) break;
         BwdItem it;
         if (!decode_bwd_item(prm, n_items, idx, it)) continue;
@@ -268,8 +290,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // (never a barrier), so no thread can be left waiting at bar.sync.
     bool ok = true;
     int uc = 0;  // query tiles processed over all items (phase and buffer parity)
-    for (int round = 0;; ++round) {
-      const int idx = snake_index_b(round);
+    for (int n = 0;; ++n) {
+      if (issuer) sm.item_bc[n & 1] = ring_get(sm.ring, n, true);
+      named_barrier_sync(1, kComputeThreads);
+      const int idx = sm.item_bc[n & 1];
+      if (idx < 0) {
+        ok = false;
+        break;
+      }
       if (idx >= total) break;
       BwdItem it;
       if (!decode_bwd_item(prm, n_items, idx, it)) continue;
@@ -503,7 +531,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (sm.abort && threadIdx.x == 0) report(prm.status, FLAMIA_DEV_TIMEOUT);
+  if (threadIdx.x == 0) {
+    if (sm.abort) report(prm.status, FLAMIA_DEV_TIMEOUT);
+    finish_claims(prm.wl_header + kHdrBwdNext, prm.wl_header + kHdrBwdExit);
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -525,7 +556,7 @@ template <int DIM, bool NVF4>
 flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
                          const flamia_qtensor* v, const flamia_qtensor* dout, const float* D,
                          const float* lse, const int32_t* cu, int ndocs, int T, int H,
-                         float softmax_scale, const void* wl, void* dq, void* dk, void* dv,
+                         float softmax_scale, void* wl, void* dq, void* dk, void* dv,
                          float* acc, int* status, cudaStream_t stream) {
   CUtensorMap mq, mk, mv, mdo, mdq, mq4, mk4;
   const CUtensorMapSwizzle swz = swizzle_for_row_bytes(DIM);
@@ -554,7 +585,7 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
   prm.D = D;
   prm.lse = lse;
   prm.cu = cu;
-  prm.wl_header = static_cast<const int*>(wl);
+  prm.wl_header = static_cast<int*>(wl);
   prm.items = reinterpret_cast<const int4*>(static_cast<const char*>(wl) + L.off_tile_bwd);
   prm.dk = static_cast<__nv_bfloat16*>(dk);
   prm.dv = static_cast<__nv_bfloat16*>(dv);
@@ -607,7 +638,7 @@ extern "C" flamia_status flamia_attn_bwd(const flamia_qtensor* q, const flamia_q
                                          const flamia_qtensor* v, const flamia_qtensor* dout,
                                          const float* D, const float* lse,
                                          const int32_t* cu_seqlens, int ndocs, int T, int H,
-                                         int d, float softmax_scale, int flags, const void* wl,
+                                         int d, float softmax_scale, int flags, void* wl,
                                          void* dq_bf16, void* dk_bf16, void* dv_bf16, void* ws,
                                          size_t ws_bytes, int* dev_status, void* stream) {
   if (!supported_dim(d)) return FLAMIA_ERR_UNSUPPORTED;

@@ -59,6 +59,8 @@ struct Bwd128Smem {
   uint64_t bar_qd_full[kRing], bar_qd_empty[kRing];
   uint64_t bar_s_full[2], bar_ds_full[2], bar_dq_full[2], bar_dq_read[2];
   uint64_t bar_acc_full, bar_acc_empty, bar_done;
+  ItemRing<4> ring;   // claimed items: producer -> MMA issuer, group leaders
+  int item_bc[2][2];  // [group][item parity]: the leader's copy for its group
   uint32_t tmem_base;
   volatile int abort;
 };
@@ -78,7 +80,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int H = prm.H, T = prm.T;
   const int n_items = min(prm.wl_header[kHdrTileBwd], prm.cap);
   const int total = n_items * H;
-  if (static_cast<int>(blockIdx.x) >= total) return;  // uniform over the CTA
+  if (static_cast<int>(blockIdx.x) >= total) {  // uniform over the CTA
+    if (threadIdx.x == 0) finish_claims(prm.wl_header + kHdrBwdNext, prm.wl_header + kHdrBwdExit);
+    return;
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&sm.bar_kv), 1);
@@ -96,6 +101,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&sm.bar_acc_full), 1);
     mbar_init(smem_u32(&sm.bar_acc_empty), 2 * kGroupThreads);
     mbar_init(smem_u32(&sm.bar_done), 1);
+    ring_init(sm.ring, 3);
     sm.abort = 0;
     fence_barrier_init();
   }
@@ -132,11 +138,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++uc;
         return true;
       };
-      for (int round = 0; ok; ++round) {
-        const int idx = snake_index_b(round);
-        if (idx >= total) break;
+      // items in head-major, longest-first order, claimed one at a time: a CTA
+      // takes the next item when it has issued its current item's last load
+      int* counter = prm.wl_header + kHdrBwdNext;
+      int idx = claim_item(counter);
+      for (int n = 0; ok; ++n) {
+        const bool end = idx >= total;
+        if (!ring_put(sm.ring, n, end ? total : idx) || sm.abort) {
+          ok = false;
+          break;
+        }
+        if (end) break;
         BwdItem it;
-        if (!decode_bwd_item(prm, n_items, idx, it)) continue;
+        if (!decode_bwd_item(prm, n_items, idx, it)) {
+          idx = claim_item(counter);
+          continue;
+        }
         const int nq = n_tiles64(it);
         const int pre = min(nq, 2);
         int u = 0;
@@ -152,6 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(smem_u32(sm.v), &map_v, bkv, 0, it.h, it.k0);
         ++nk;
         for (; u < nq && ok; ++u) ok = load_qd(it.h, it.k0 + u * kQT);
+        if (ok) idx = claim_item(counter);
       }
       // drain: every issued copy has landed before the CTA exits
       if (nk > 0) ok &= mbar_wait(bkv, (nk - 1) & 1);
@@ -186,8 +204,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit(smem_u32(&sm.bar_s_full[b]));
         return true;
       };
-      for (int round = 0; ok; ++round) {
-        const int idx = snake_index_b(round);
+      for (int n = 0; ok; ++n) {
+        const int idx = ring_get(sm.ring, n, true);
+        if (idx < 0) {
+          ok = false;
+          break;
+        }
         if (idx >= total) break;
         BwdItem it;
         if (!decode_bwd_item(prm, n_items, idx, it)) continue;
@@ -283,8 +305,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         sm.dobyte[g][buf][quad - 2] = r_dob;
       }
     };
-    for (int round = 0;; ++round) {
-      const int idx = snake_index_b(round);
+    for (int n = 0;; ++n) {
+      if (issuer) sm.item_bc[g][n & 1] = ring_get(sm.ring, n, true);
+      named_barrier_sync(bar_id, kGroupThreads);
+      const int idx = sm.item_bc[g][n & 1];
+      if (idx < 0) {
+        ok = false;
+        break;
+      }
       if (idx >= total) break;
       BwdItem it;
       if (!decode_bwd_item(prm, n_items, idx, it)) continue;
@@ -472,7 +500,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (sm.abort && threadIdx.x == 0) report(prm.status, FLAMIA_DEV_TIMEOUT);
+  if (threadIdx.x == 0) {
+    if (sm.abort) report(prm.status, FLAMIA_DEV_TIMEOUT);
+    finish_claims(prm.wl_header + kHdrBwdNext, prm.wl_header + kHdrBwdExit);
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);

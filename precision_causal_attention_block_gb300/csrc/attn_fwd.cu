@@ -49,6 +49,7 @@ struct FwdSmem {
   uint64_t bar_p_full[2];
   uint64_t bar_o_full[2];
   uint64_t bar_done;
+  ItemRing<4> ring;  // claimed items, producer -> MMA issuer and softmax warps
   uint32_t tmem_base;
   volatile int abort;
 };
@@ -60,7 +61,7 @@ struct FwdParams {
   const uint32_t* q4_scales;  // NVFP4: 4 E4M3 scales per (token, head) as one word (d = 64)
   const uint32_t* k4_scales;
   const int32_t* cu;
-  const int* wl_header;
+  int* wl_header;  // list sizes, and the claim counters this kernel updates
   const int4* items;
   __nv_bfloat16* o;
   float* lse;
@@ -155,12 +156,8 @@ __device__ __forceinline__ bool decode_fwd_item(const FwdParams& prm, int n_item
   return true;
 }
 
-// The CTA's items in snake order over the head-major (head, item) list:
-// round r takes index r * G + b (r even) or r * G + G - 1 - b (r odd).
-__device__ __forceinline__ int snake_index(int round) {
-  const int G = gridDim.x, b = blockIdx.x;
-  return round * G + ((round & 1) ? G - 1 - b : b);
-}
+// Consumers of the item ring: the MMA issuer and the 8 softmax warps.
+constexpr int kFwdRingConsumers = 1 + 8;
 
 template <int DIM, bool NVF4>
 __global__ void __launch_bounds__(kFwdThreads, 1)
@@ -177,7 +174,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int H = prm.H, T = prm.T;
   const int n_items = min(prm.wl_header[kHdrTileFwd], prm.cap);
   const int total = n_items * H;
-  if (static_cast<int>(blockIdx.x) >= total) return;  // uniform over the CTA
+  if (static_cast<int>(blockIdx.x) >= total) {  // uniform over the CTA
+    if (threadIdx.x == 0) finish_claims(prm.wl_header + kHdrFwdNext, prm.wl_header + kHdrFwdExit);
+    return;
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -195,6 +195,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     mbar_init(smem_u32(&sm.bar_done), 1);
     mbar_init(smem_u32(&sm.bar_sf), 2 * kTile);
+    ring_init(sm.ring, kFwdRingConsumers);
     sm.abort = 0;
     fence_barrier_init();
   }
@@ -219,11 +220,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       int nq_loaded = 0;  // items whose Q tiles were loaded
       int kvc = 0;        // key tiles loaded over all items
       bool ok = true;
-      for (int round = 0; ok; ++round) {
-        const int idx = snake_index(round);
-        if (idx >= total) break;
+      // items in head-major, longest-first order, claimed one at a time: a CTA
+      // takes the next item when it has issued its current item's last load
+      int* counter = prm.wl_header + kHdrFwdNext;
+      int idx = claim_item(counter);
+      for (int n = 0; ok; ++n) {
+        const bool end = idx >= total;
+        if (!ring_put(sm.ring, n, end ? total : idx) || sm.abort) {
+          ok = false;
+          break;
+        }
+        if (end) break;
         FwdItem it;
-        if (!decode_fwd_item(prm, n_items, idx, it)) continue;
+        if (!decode_fwd_item(prm, n_items, idx, it)) {
+          idx = claim_item(counter);
+          continue;
+        }
         // the previous item's Q tiles are free once its last score product is done
         if (nq_loaded > 0 && (!mbar_wait(smem_u32(&sm.bar_q_empty), (nq_loaded - 1) & 1) ||
                               sm.abort)) {
@@ -252,6 +264,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           tma_load_3d(smem_u32(sm.v[st]), &map_v, bf, 0, it.h, it.s + j * kTile);
           if (NVF4) tma_load_3d(smem_u32(sm.k4[st]), &map_k4, bf, 0, it.h, it.s + j * kTile);
         }
+        if (ok) idx = claim_item(counter);
       }
       // Drain: every issued copy has landed before the CTA can exit.
       if (nq_loaded > 0) ok &= mbar_wait(bq, (nq_loaded - 1) & 1);
@@ -285,8 +298,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         tc_commit(smem_u32(&sm.bar_s_full[t]));
       };
-      for (int round = 0; ok; ++round) {
-        const int idx = snake_index(round);
+      for (int n = 0; ok; ++n) {
+        const int idx = ring_get(sm.ring, n, true);
+        if (idx < 0) {
+          ok = false;
+          break;
+        }
         if (idx >= total) break;
         FwdItem it;
         if (!decode_fwd_item(prm, n_items, idx, it)) continue;
@@ -366,8 +383,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     int s_seen = 0, o_seen = 0;  // completions of s_full[t] and o_full[t] waited so far
     int kvc = 0;                 // global index of the current item's first key tile
     bool ok = true;
-    for (int round = 0; ok; ++round) {
-      const int idx = snake_index(round);
+    for (int n = 0; ok; ++n) {
+      // the whole warp takes lane 0's copy, so its lanes never disagree
+      const int idx = __shfl_sync(0xffffffffu, ring_get(sm.ring, n, false), 0);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sm.ring.empty[n % 4]));
+      if (idx < 0) {
+        ok = false;
+        break;
+      }
       if (idx >= total) break;
       FwdItem it;
       if (!decode_fwd_item(prm, n_items, idx, it)) continue;
@@ -534,7 +558,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (sm.abort && threadIdx.x == 0) report(prm.status, FLAMIA_DEV_TIMEOUT);
+  if (threadIdx.x == 0) {
+    if (sm.abort) report(prm.status, FLAMIA_DEV_TIMEOUT);
+    finish_claims(prm.wl_header + kHdrFwdNext, prm.wl_header + kHdrFwdExit);
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -544,7 +571,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 template <int DIM, bool NVF4>
 flamia_status launch_fwd(const flamia_qtensor* q, const flamia_qtensor* k,
                          const flamia_qtensor* v, const int32_t* cu, int ndocs, int T, int H,
-                         float softmax_scale, const void* wl, void* o, float* lse, int* status,
+                         float softmax_scale, void* wl, void* o, float* lse, int* status,
                          cudaStream_t stream) {
   CUtensorMap mq, mk, mv, mq4, mk4;
   const CUtensorMapSwizzle swz = swizzle_for_row_bytes(DIM);
@@ -568,7 +595,7 @@ flamia_status launch_fwd(const flamia_qtensor* q, const flamia_qtensor* k,
   prm.q4_scales = reinterpret_cast<const uint32_t*>(q->nvfp4_scales);
   prm.k4_scales = reinterpret_cast<const uint32_t*>(k->nvfp4_scales);
   prm.cu = cu;
-  prm.wl_header = static_cast<const int*>(wl);
+  prm.wl_header = static_cast<int*>(wl);
   prm.items = reinterpret_cast<const int4*>(static_cast<const char*>(wl) + L.off_tile_fwd);
   prm.o = static_cast<__nv_bfloat16*>(o);
   prm.lse = lse;
@@ -602,7 +629,7 @@ using namespace flamia;
 extern "C" flamia_status flamia_attn_fwd(const flamia_qtensor* q, const flamia_qtensor* k,
                                          const flamia_qtensor* v, const int32_t* cu_seqlens,
                                          int ndocs, int T, int H, int d, float softmax_scale,
-                                         int flags, const void* wl, void* o_bf16, float* lse,
+                                         int flags, void* wl, void* o_bf16, float* lse,
                                          int* dev_status, void* stream) {
   if (!supported_dim(d)) return FLAMIA_ERR_UNSUPPORTED;
   if ((flags & ~FLAMIA_FLAG_NVFP4_QK) != 0) return FLAMIA_ERR_UNSUPPORTED;

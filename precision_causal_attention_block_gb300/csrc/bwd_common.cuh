@@ -21,7 +21,7 @@ struct BwdParams {
   const float* D;
   const float* lse;
   const int32_t* cu;
-  const int* wl_header;
+  int* wl_header;  // list sizes, and the claim counters this kernel updates
   const int4* items;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
@@ -97,11 +97,10 @@ __device__ __forceinline__ bool decode_bwd_item(const BwdParams& prm, int n_item
   return true;
 }
 
-// The CTA's items in snake order over the head-major (head, item) list.
-__device__ __forceinline__ int snake_index_b(int round) {
-  const int G = gridDim.x, b = blockIdx.x;
-  return round * G + ((round & 1) ? G - 1 - b : b);
-}
+// Consumer roles of a backward kernel's item ring: the MMA issuer and one
+// leader thread per compute group (the leader hands the item to its group
+// through shared memory and a named barrier, so a group's warps never
+// disagree on the item and never miss a barrier).
 
 // Pipelined backward for head dim 128 (MXFP8 score product); grid = CTAs.
 cudaError_t launch_bwd128_pipelined(const BwdParams& prm, const flamia_qtensor* q,

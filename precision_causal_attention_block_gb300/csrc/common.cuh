@@ -77,8 +77,9 @@ inline WorklistLayout worklist_layout(int T, int ndocs) {
 
 // Header words of the work-list buffer: list sizes and capacities, the
 // largest cost, the sizes of the tile lists (items of documents longer than
-// kShortDoc, which the tile kernels process) and, internal to the builder, the
-// number of documents with a long cost-1 item in each list.
+// kShortDoc, which the tile kernels process), internal to the builder the
+// number of documents with a long cost-1 item in each list, and the tile
+// kernels' item claim counters.
 enum : int {
   kHdrNFwd = 0,
   kHdrNBwd = 1,
@@ -88,7 +89,13 @@ enum : int {
   kHdrTileFwd = 5,
   kHdrTileBwd = 6,
   kHdrLong1Fwd = 7,
-  kHdrLong1Bwd = 8
+  kHdrLong1Bwd = 8,
+  // claim counters of the forward / backward tile kernels and their CTA exit
+  // counts; zero after the build and after every launch
+  kHdrFwdNext = 9,
+  kHdrFwdExit = 10,
+  kHdrBwdNext = 11,
+  kHdrBwdExit = 12
 };
 
 // ------------------------------------------------------------------ checks

@@ -75,6 +75,62 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// ------------------------------------------------------------------ item ring
+// Work items claimed by a CTA's producer thread are handed to the CTA's other
+// roles in claim order through a small shared-memory ring: item number n
+// (0, 1, ...) sits in slot n % kSlots.  `full` completes once per put, `empty`
+// once every consumer role has taken the slot.
+
+template <int kSlots>
+struct ItemRing {
+  int idx[kSlots];
+  uint64_t full[kSlots];
+  uint64_t empty[kSlots];
+};
+
+template <int kSlots>
+__device__ __forceinline__ void ring_init(ItemRing<kSlots>& r, int consumers) {
+  for (int i = 0; i < kSlots; ++i) {
+    mbar_init(smem_u32(&r.full[i]), 1);
+    mbar_init(smem_u32(&r.empty[i]), consumers);
+  }
+}
+
+// Producer: publishes item number n; false if the slot never came free.
+template <int kSlots>
+__device__ __forceinline__ bool ring_put(ItemRing<kSlots>& r, int n, int v) {
+  const int s = n % kSlots;
+  if (n >= kSlots && !mbar_wait(smem_u32(&r.empty[s]), ((n / kSlots) - 1) & 1)) return false;
+  *static_cast<volatile int*>(&r.idx[s]) = v;
+  mbar_arrive(smem_u32(&r.full[s]));  // release: the value is visible to the waiters
+  return true;
+}
+
+// Consumer role: item number n, or -1 if it never arrived.  With `release`
+// the caller's arrive frees the slot (one arrive per consumer role).
+template <int kSlots>
+__device__ __forceinline__ int ring_get(ItemRing<kSlots>& r, int n, bool release) {
+  const int s = n % kSlots;
+  if (!mbar_wait(smem_u32(&r.full[s]), (n / kSlots) & 1)) return -1;
+  const int v = *static_cast<volatile int*>(&r.idx[s]);
+  if (release) mbar_arrive(smem_u32(&r.empty[s]));
+  return v;
+}
+
+// The next unclaimed item of a launch (items are claimed in list order, so
+// the longest go first wherever a CTA is free).
+__device__ __forceinline__ int claim_item(int* counter) { return atomicAdd(counter, 1); }
+
+// Called by thread 0 of every CTA as its last action: the last CTA of the
+// launch resets the claim counter and the exit count for the next launch.
+__device__ __forceinline__ void finish_claims(int* counter, int* exited) {
+  __threadfence();
+  if (atomicAdd(exited, 1) == static_cast<int>(gridDim.x) - 1) {
+    atomicExch(counter, 0);
+    atomicExch(exited, 0);
+  }
+}
+
 // ------------------------------------------------------------------ proxies
 
 // Generic-proxy writes to shared memory become visible to the async proxy

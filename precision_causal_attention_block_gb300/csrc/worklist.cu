@@ -127,6 +127,10 @@ __global__ void __launch_bounds__(kScanThreads)
   if (threadIdx.x == 0) {
     p.header[kHdrLong1Fwd] = s_tot[kCntLongFwd];
     p.header[kHdrLong1Bwd] = s_tot[kCntLongBwd];
+    p.header[kHdrFwdNext] = 0;
+    p.header[kHdrFwdExit] = 0;
+    p.header[kHdrBwdNext] = 0;
+    p.header[kHdrBwdExit] = 0;
     int nf = s_tot[0], nb = s_tot[1];
     if (nf > cap_fwd || nb > cap_bwd) {
       report(dev_status, FLAMIA_DEV_CAPACITY);
