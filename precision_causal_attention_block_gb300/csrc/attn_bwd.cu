@@ -379,9 +379,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                     32 * c, j, pw);
           }
           // one exponent per 32x32 block: this warp's 32 key rows x these 32 queries
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1)
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+          // (|dS| >= 0: the float order is the order of the bit patterns)
+          amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(amax)));
           const int eb = max(roundup_exponent(amax) - 8, -127);  // exponent of dS = 2^-8 dS8
           const float inv = exp2i(-(eb + 8));
           const float2 inv2 = make_float2(inv, inv);
@@ -459,10 +458,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             float* row = sm.dqs[g * kCh + cc] + j * 32;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              float4 f = make_float4(__uint_as_float(v[cc][4 * i]) * prm.sm_scale,
-                                     __uint_as_float(v[cc][4 * i + 1]) * prm.sm_scale,
-                                     __uint_as_float(v[cc][4 * i + 2]) * prm.sm_scale,
-                                     __uint_as_float(v[cc][4 * i + 3]) * prm.sm_scale);
+              // softmax_scale is applied once, in the float32 -> BF16 conversion
+              float4 f = make_float4(__uint_as_float(v[cc][4 * i]), __uint_as_float(v[cc][4 * i + 1]),
+                                     __uint_as_float(v[cc][4 * i + 2]),
+                                     __uint_as_float(v[cc][4 * i + 3]));
               if (!qv) f = make_float4(0.f, 0.f, 0.f, 0.f);  // rows of other documents add 0
               *reinterpret_cast<float4*>(row + 4 * (i ^ (j & 7))) = f;
             }
@@ -541,13 +540,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
-// float32 dQ accumulator -> BF16 output.
+// float32 dQ accumulator (sums of dS K) -> BF16 dQ = softmax_scale * acc.
 __global__ void dq_convert_kernel(const float4* __restrict__ acc, uint2* __restrict__ out,
-                                  size_t n4) {
+                                  size_t n4, float sm_scale) {
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4;
        i += static_cast<size_t>(gridDim.x) * blockDim.x) {
     const float4 a = acc[i];
-    __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y), hi = __floats2bfloat162_rn(a.z, a.w);
+    __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * sm_scale, a.y * sm_scale),
+                   hi = __floats2bfloat162_rn(a.z * sm_scale, a.w * sm_scale);
     out[i] = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
   }
 }
@@ -620,7 +620,7 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
   const size_t n4 = n / 4;
   const int blocks = static_cast<int>(std::min<size_t>((n4 + 255) / 256, 152 * 16));
   dq_convert_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(acc),
-                                                static_cast<uint2*>(dq), n4);
+                                                static_cast<uint2*>(dq), n4, softmax_scale);
   return cudaGetLastError() == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
 }
 

@@ -367,9 +367,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             amax = bwd_chunk<false>(sv, dv, nl, dd, fS, fP, u * kQT + 32 * c, j, pw);
           }
           // one exponent per 32x32 block: this warp's 32 key rows x these 32 queries
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1)
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+          // (|dS| >= 0: the float order is the order of the bit patterns)
+          amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(amax)));
           const int eb = max(roundup_exponent(amax) - 8, -127);  // exponent of dS = 2^-8 dS8
           const float inv = exp2i(-(eb + 8));
           const float2 inv2 = make_float2(inv, inv);
@@ -438,12 +437,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           // S^T / dP^T of the group's next tile may now be computed
           tc_fence_before();
           mbar_arrive(smem_u32(&sm.bar_dq_read[g]));
+          // raw sums of dS K (softmax_scale is applied in the BF16 conversion)
           const int nvalid = min(kQT, e - q0);  // queries of other documents add 0
           float* stg = sm.dqs[g][quad] + lane;  // row = query, element = this dim
+          if (nvalid == kQT) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            stg[c * 32] = c < nvalid ? __uint_as_float(v0[c]) * prm.sm_scale : 0.f;
-            stg[(c + 32) * 32] = c + 32 < nvalid ? __uint_as_float(v1[c]) * prm.sm_scale : 0.f;
+            for (int c = 0; c < 32; ++c) {
+              stg[c * 32] = __uint_as_float(v0[c]);
+              stg[(c + 32) * 32] = __uint_as_float(v1[c]);
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              stg[c * 32] = c < nvalid ? __uint_as_float(v0[c]) : 0.f;
+              stg[(c + 32) * 32] = c + 32 < nvalid ? __uint_as_float(v1[c]) : 0.f;
+            }
           }
           fence_proxy_async_smem();
         }

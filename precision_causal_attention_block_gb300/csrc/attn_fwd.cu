@@ -109,14 +109,14 @@ __device__ __forceinline__ void chunk_probs(const uint32_t (&v)[32], float cf, f
   for (int i = 0; i < 32; i += 4) {
     float2 a = make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1]));
     float2 b = make_float2(__uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
-    if (MASK) {
+    a = __ffma2_rn(a, cf2, mo2);
+    b = __ffma2_rn(b, cf2, mo2);
+    if (MASK) {  // after the product: cf is 0 for an all-zero key block
       if (i + 0 > lim) a.x = -INFINITY;
       if (i + 1 > lim) a.y = -INFINITY;
       if (i + 2 > lim) b.x = -INFINITY;
       if (i + 3 > lim) b.y = -INFINITY;
     }
-    a = __ffma2_rn(a, cf2, mo2);
-    b = __ffma2_rn(b, cf2, mo2);
     const float2 pa = make_float2(ex2_approx(a.x), ex2_approx(a.y));
     const float2 pb = make_float2(ex2_approx(b.x), ex2_approx(b.y));
     lsum = __fadd2_rn(lsum, pa);
@@ -474,20 +474,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const bool need = (j > 0) && (m_new > m);
         const float corr = need ? pow2_or_zero(static_cast<int>(m - m_new)) : 1.f;
         l8 *= corr;
-        if (__any_sync(0xffffffffu, need)) {
-          // rescale this warp's O rows by the (exact power-of-two) correction
-          // in 8-column pieces: the row of S stays live in registers meanwhile
-#pragma unroll 1
-          for (int c = 0; c < DIM / 8; ++c) {
-            uint32_t v[8];
-            tmem_ld8(tO + 8 * c, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * corr);
-            tmem_st8(tO + 8 * c, v);
-          }
-          tmem_st_wait();
-        }
         m = m_new;
         const float moff = m - 8.f;  // P8 = 2^8 exp2(s - m)
         // pass 2: probabilities, row sum, E4M3 operand
@@ -505,6 +491,32 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           *reinterpret_cast<uint4*>(prow + 16 * ch1) = make_uint4(w[4], w[5], w[6], w[7]);
         }
         l8 += lsum.x + lsum.y;
+        if (__any_sync(0xffffffffu, need)) {
+          // rescale this warp's O rows by the (exact power-of-two) correction,
+          // now that the row of S is consumed (the products of key tile j - 1
+          // into O completed before S_t of tile j); P^_t V_j is issued only
+          // after this group's p_full arrive below
+          const float2 c2 = make_float2(corr, corr);
+#pragma unroll 1
+          for (int c0 = 0; c0 < DIM / 32; c0 += 2) {
+            uint32_t a[32], b[32];
+            tmem_ld32(tO + 32 * c0, a);
+            tmem_ld32(tO + 32 * (c0 + 1), b);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              float2 x = __fmul2_rn(make_float2(__uint_as_float(a[i]), __uint_as_float(a[i + 1])), c2);
+              float2 y = __fmul2_rn(make_float2(__uint_as_float(b[i]), __uint_as_float(b[i + 1])), c2);
+              a[i] = __float_as_uint(x.x);
+              a[i + 1] = __float_as_uint(x.y);
+              b[i] = __float_as_uint(y.x);
+              b[i + 1] = __float_as_uint(y.y);
+            }
+            tmem_st32(tO + 32 * c0, a);
+            tmem_st32(tO + 32 * (c0 + 1), b);
+          }
+          tmem_st_wait();
+        }
         // scale factors of P^_t V_j: A (P^) 2^0 for every K block, B = V's block bytes
         const uint32_t sfw[8] = {0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu,
                                  sfb, sfb, sfb, sfb};

@@ -33,7 +33,7 @@ struct ShortParams {
   float* lse;
   // backward
   const float *lse_in, *D;
-  float* dq_acc;                                // float32 [T, H, d]
+  float* dq_acc;  // float32 [T, H, d]: dS K sums (softmax_scale comes in the conversion)
   __nv_bfloat16 *dk, *dv;
 };
 
@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(32 * kShortWarps)
 #pragma unroll
       for (int c = 0; c < DIM / 32; ++c) acc[c] = fmaf(dsh, k[c], acc[c]);
     }
-    const float mul = prm.sm_scale * pow2_or_zero_s(ek);
+    const float mul = pow2_or_zero_s(ek);  // softmax_scale: in the BF16 conversion
     float* dst = prm.dq_acc + (static_cast<size_t>(s + i) * H + h) * DIM + (DIM / 32) * lane;
 #pragma unroll
     for (int c = 0; c < DIM / 32; ++c) dst[c] = acc[c] * mul;

@@ -89,6 +89,24 @@ def test_all_zero_short_document(lib):
     compare("O uniform", np64(call.o[7:27]), want)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_all_zero_blocks_in_long_documents(lib, d):
+    """All-zero 32-token blocks get the smallest scale exponent (factor 0 in
+    the kernels); on a diagonal tile the masked keys must still give 0, not
+    NaN (a masked score times a zero factor)."""
+    w = W.custom("zero_blocks", [300, 200], 2, d, seed=29)
+    x = W.make_inputs_bf16(w)
+    x["k"][128:160] = 0     # key block on the diagonal of query tile 1
+    x["q"][160:192] = 0     # a query block
+    x["v"][320:352] = 0
+    x["do"][64:96] = 0
+    call = run_call(w, x)
+    for t in (call.o, call.lse, call.dq, call.dk, call.dv):
+        assert torch.isfinite(t.float()).all()
+    ref = O.attention(*[x[n].double().numpy() for n in NAMES], w.cu_seqlens, w.sm_scale)
+    check_against(call, ref, slice(0, w.T), list(range(w.H)))
+
+
 def test_tiny_config(lib):
     w = W.tiny()
     x = W.make_inputs_bf16(w)
