@@ -336,22 +336,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       // group 0 loads the per-query inputs of the item's tile u into buffer
       // (global tile index) & 1
-      auto load_query_inputs = [&](int u, int ug) {
+      // the per-query inputs of tile u: raw loads from clamped (always valid)
+      // addresses, issued a tile ahead and only used when stored
+      float r_lse = 0.f, r_dd = 0.f;
+      uint32_t r_qb = 127u, r_dob = 127u;
+      bool r_qv = false;
+      auto fetch_query_inputs = [&](int u) {
         const int qi = k0 + u * kTile + j;
-        const bool qv = qi < e;
-        const int b = ug & 1;
-        sm.nl[b][j] = qv ? 8.f - prm.lse[hT + qi] * LOG2E : -INFINITY;
-        sm.dd[b][j] = qv ? prm.D[hT + qi] : 0.f;
+        r_qv = qi < e;
+        const size_t at = hT + min(qi, T - 1);
+        r_lse = prm.lse[at];
+        r_dd = prm.D[at];
         if (lane == 0) {
-          sm.qbyte[b][quad] = qv ? prm.q_scales[hT + qi] : 127u;
-          sm.dobyte[b][quad] = qv ? prm.do_scales[hT + qi] : 127u;
+          r_qb = prm.q_scales[at];
+          r_dob = prm.do_scales[at];
         }
       };
-      if (g == 0) load_query_inputs(0, uc);
+      auto store_query_inputs = [&](int ug) {
+        const int b = ug & 1;
+        sm.nl[b][j] = r_qv ? 8.f - r_lse * LOG2E : -INFINITY;
+        sm.dd[b][j] = r_qv ? r_dd : 0.f;
+        if (lane == 0) {
+          sm.qbyte[b][quad] = r_qv ? r_qb : 127u;
+          sm.dobyte[b][quad] = r_qv ? r_dob : 127u;
+        }
+      };
+      if (g == 0) {
+        fetch_query_inputs(0);
+        store_query_inputs(uc);
+      }
       named_barrier_sync(1, kComputeThreads);
       for (int u = 0; u < nq; ++u, ++uc) {
         const int q0 = k0 + u * kTile;
         const int ub = uc & 1;
+        if (g == 0 && u + 1 < nq) fetch_query_inputs(u + 1);  // lands during this tile
         ok = ok && !sm.abort && mbar_wait(smem_u32(&sm.bar_s_full), uc & 1);
         tc_fence_after();
         uint8_t* pbrow = sm.pb + j * kTile;
@@ -479,7 +497,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!ok) sm.abort = 1;
         // the next tile's per-query inputs (its buffer was last read before this
         // tile's second barrier)
-        if (g == 0 && u + 1 < nq) load_query_inputs(u + 1, uc + 1);
+        if (g == 0 && u + 1 < nq) store_query_inputs(uc + 1);
         named_barrier_sync(1, kComputeThreads);
         if (issuer && !sm.abort) {
 #pragma unroll

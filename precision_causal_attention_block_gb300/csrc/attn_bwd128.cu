@@ -280,29 +280,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     // wait that times out only clears `ok`, which skips work, never a barrier.
     bool ok = true;
     int ng = 0, ug = 0, nk = 0;  // this group's tiles, all tiles, items
-    // per-query inputs of one tile, fetched into registers ahead of use
-    float r_nl = -INFINITY, r_dd = 0.f;
+    // per-query inputs of one tile: raw loads issued a tile ahead (from
+    // clamped, always valid addresses) and only used when stored, so their
+    // latency hides behind the tile's work
+    float r_lse = 0.f, r_dd = 0.f;
     uint32_t r_qb = 127u, r_dob = 127u;
+    bool r_qv = false;
     auto fetch_inputs = [&](size_t hT, int q0, int e) {
       if (quad < 2) {
         const int qi = q0 + j;
-        const bool qv = qi < e;
-        r_nl = qv ? 8.f - prm.lse[hT + qi] * LOG2E : -INFINITY;
-        r_dd = qv ? prm.D[hT + qi] : 0.f;
+        r_qv = qi < e;
+        const size_t at = hT + min(qi, T - 1);
+        r_lse = prm.lse[at];
+        r_dd = prm.D[at];
       } else if (lane == 0) {
         const int qi = q0 + 32 * (quad - 2);
-        const bool qv = qi < e;
-        r_qb = qv ? prm.q_scales[hT + qi] : 127u;
-        r_dob = qv ? prm.do_scales[hT + qi] : 127u;
+        r_qv = qi < e;
+        const size_t at = hT + min(qi, T - 1);
+        r_qb = prm.q_scales[at];
+        r_dob = prm.do_scales[at];
       }
     };
     auto store_inputs = [&](int buf) {
       if (quad < 2) {
-        sm.nl[g][buf][j] = r_nl;
-        sm.dd[g][buf][j] = r_dd;
+        sm.nl[g][buf][j] = r_qv ? 8.f - r_lse * LOG2E : -INFINITY;
+        sm.dd[g][buf][j] = r_qv ? r_dd : 0.f;
       } else if (lane == 0) {
-        sm.qbyte[g][buf][quad - 2] = r_qb;
-        sm.dobyte[g][buf][quad - 2] = r_dob;
+        sm.qbyte[g][buf][quad - 2] = r_qv ? r_qb : 127u;
+        sm.dobyte[g][buf][quad - 2] = r_qv ? r_dob : 127u;
       }
     };
     for (int n = 0;; ++n) {
