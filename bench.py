@@ -121,6 +121,30 @@ def job_throughput(flops_per_step, steps, world, slowest_ms):
     return world * flops_per_step * steps / (slowest_ms * 1e-3) / 1e12
 
 
+def profiled_traffic(w, nvfp4):
+    """DRAM bytes per launch of the backward kernel from the committed ncu
+    summary of this workload, if the kernel's sources are unchanged since the
+    capture (else None)."""
+    import hashlib
+    import re
+    if nvfp4 or w.d != 128:
+        return None
+    path = os.path.join(ROOT, "profiles", f"attn_bwd128_kernel_{w.name.replace('_', '', 1)}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    t = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
+    srcs = re.search(r"sources:\s*(.+)", text)
+    sha = re.search(r"sources_sha256:\s*([0-9a-f]+)", text)
+    if not (t and srcs and sha):
+        return None
+    h = hashlib.sha256()
+    for f in srcs.group(1).split():
+        h.update(open(os.path.join(ROOT, "precision_causal_attention_block_gb300", "csrc", f),
+                      "rb").read())
+    return int(t.group(1)) if h.hexdigest() == sha.group(1) else None
+
+
 def make_workload(name):
     from precision_causal_attention_block_gb300 import workloads as W
     return W.WORKLOADS[name]()
@@ -235,7 +259,9 @@ def run_ours(args, rank, world, local):
     value = job_throughput(flops, args.steps, world, res["total_ms"])
     e2e_value = job_throughput(flops, args.steps, world, res["e2e_ms"])
     achieved = bwd_flops / (res["bwd_ms"] * 1e-3) / 1e12
-    launches_per_step = 4 + 6 + 1 + 1 + 1  # quantiser x4, work list, fwd, bwd, dq convert
+    # quantiser x4, work list x6, forward + its short-document kernel, backward + its
+    # short-document kernel, dQ conversion (the dQ accumulator memset is a driver call)
+    launches_per_step = 4 + 6 + 2 + 2 + 1
     line = {
         "metric": "MXFP8 causal attn fwd+bwd TFLOP/s incl. quant; % of GB300 FP8 tensor peak",
         "value": round(value, 3),
@@ -254,11 +280,14 @@ def run_ours(args, rank, world, local):
                    "flops_per_step": flops, "l2": "flushed (256 MB write) before every step",
                    "parallelism": f"replicas x{world}"},
         "pct_of_fp8_peak": round(100.0 * value / world / pk["fp8_tflops"], 2),
-        "roofline": {"kernel": "flamia_attn_bwd (memset + attn_bwd_kernel + dq convert)",
+        "roofline": {"kernel": "flamia_attn_bwd (memset + %s + short-document kernel + dq convert)"
+                               % ("attn_bwd128_kernel" if w.d == 128 and not args.nvfp4
+                                  else "attn_bwd_kernel<64>"),
                      "bound": "tensor", "achieved": round(achieved, 2),
                      "peak": pk["fp8_tflops"], "unit": "TFLOP/s",
                      "frac": round(achieved / pk["fp8_tflops"], 4),
-                     "peak_source": pk["source"], "traffic": None},
+                     "peak_source": pk["source"], "traffic": profiled_traffic(w, args.nvfp4),
+                     "traffic_unit": "bytes per launch of the attention kernel (ncu, DRAM read + write)"},
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,

@@ -103,6 +103,12 @@ def long131072():
     return Workload("long_131072_H32_d64", 131072, 32, 64, (0, 131072), 1.0 / 8.0, "rms")
 
 
+def long16384():
+    """The long-context shape cut to one 16,384-token document (H=32, d=64, per-head
+    RMS in [0.5, 2]): a case small enough for detailed kernel profiles."""
+    return Workload("long_16384_H32_d64", 16384, 32, 64, (0, 16384), 1.0 / 8.0, "rms")
+
+
 def custom(name, lengths, H, d, structure="plain", seed=0, sm_scale=None):
     """Small ragged cases for parity tests."""
     cu = offsets(lengths)
@@ -116,6 +122,7 @@ WORKLOADS = {
     "varlen65536": varlen65536,
     "onetoken131072": onetoken131072,
     "long131072": long131072,
+    "long16384": long16384,
 }
 
 
