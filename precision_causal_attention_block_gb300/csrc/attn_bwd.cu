@@ -8,7 +8,7 @@
 // Items are ordered head-major (all key tiles of a head, longest first, then
 // the next head), so the Q / dO tiles and the dQ rows a wave of CTAs touches
 // belong to few heads and stay in L2.  Warp roles:
-//   warp 0       TMA producer: K, V once; Q, dO tiles through a 2-stage ring.
+//   warp 0       TMA producer: K, V per item; Q, dO tiles through a 2-stage ring.
 //   warp 1       tensor-memory owner and single-thread tcgen05 MMA issuer.
 //   warps 4-7    compute group 0: query columns 0..63 of every tile
 //   warps 8-11   compute group 1: query columns 64..127
@@ -21,11 +21,15 @@
 //   (one round-up exponent per document-aligned 32x32 block) to shared
 //   memory, and the block scales of the three products to TMEM;
 //   dV += P^b^T dO, dK += dS^T Q (both stay in TMEM over all u) and
-//   dQ_u = dS K (into the columns of S^T) are block-scaled MMAs;
-//   dQ_u is scaled, staged in shared memory and added in float32 to the
-//   global accumulator by bulk tensor reduce-adds.
-// Tensor memory (512 columns): S^T / dQ_u [0,128), dP^T and the scale
-// factors [128,256), dV [256,256+d), dK [256+d,256+2d).
+//   dQ_u = dS K are block-scaled MMAs;
+//   dQ_u is staged in shared memory and added in float32 to the global
+//   accumulator by bulk tensor reduce-adds.
+// Tensor memory (512 columns): S^T [0,128), dP^T and the scale factors
+// [128,256), dV [256,320), dK [320,384), the NVFP4 score scales [384,396),
+// dQ_u [448,512).  dQ_u has its own columns, so the next tile's S^T / dP^T are
+// issued right behind this tile's products (one thread's MMAs run in order,
+// so dP^T_{u+1} cannot overwrite the scales they read) and compute while the
+// groups read dQ_u out.
 #include <cuda_bf16.h>
 
 #include "bwd_common.cuh"
@@ -36,7 +40,7 @@ namespace {
 constexpr int kBStages = 2;
 constexpr int kBwdThreads = 384;
 constexpr int kComputeThreads = 256;
-constexpr uint32_t kColSP = 0, kColDP = 128, kColDV = 256;
+constexpr uint32_t kColSP = 0, kColDP = 128, kColDV = 256, kColDQ = 448;
 // scale-factor columns inside the dP^T region (written after dP^T is read)
 constexpr uint32_t kSfDvA = 128, kSfDvB = 132, kSfDkA = 136, kSfDkB = 140, kSfDqA = 144,
                    kSfDqB = 148;
@@ -64,7 +68,7 @@ struct BwdSmem {
   uint64_t bar_kv;
   uint64_t bar_qd_full[kBStages];
   uint64_t bar_qd_empty[kBStages];
-  uint64_t bar_s_full, bar_ds_full, bar_dq_full, bar_s_free, bar_done, bar_sf;
+  uint64_t bar_s_full, bar_ds_full, bar_dq_full, bar_dq_read, bar_done, bar_sf;
   uint64_t bar_kv_free, bar_acc_empty;
   ItemRing<4> ring;  // claimed items: producer -> MMA issuer, compute leader
   int item_bc[2];    // the compute leader's copy for the compute groups
@@ -113,7 +117,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(smem_u32(&sm.bar_s_full), 1);
     mbar_init(smem_u32(&sm.bar_ds_full), kComputeThreads);
     mbar_init(smem_u32(&sm.bar_dq_full), 1);
-    mbar_init(smem_u32(&sm.bar_s_free), kComputeThreads);
+    mbar_init(smem_u32(&sm.bar_dq_read), kComputeThreads);
     mbar_init(smem_u32(&sm.bar_acc_empty), kComputeThreads);
     mbar_init(smem_u32(&sm.bar_done), 1);
     mbar_init(smem_u32(&sm.bar_sf), kTile);
@@ -212,20 +216,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ok = mbar_wait(smem_u32(&sm.bar_kv), nk & 1);
         if (NVF4) ok = ok && mbar_wait(smem_u32(&sm.bar_sf), nk & 1);
         ++nk;
-        for (int u = 0; ok && u < it.nq; ++u, ++uc) {
-          const int st = uc % kBStages;
-          if (!mbar_wait(smem_u32(&sm.bar_qd_full[st]), (uc / kBStages) & 1) ||
-              (uc > 0 && !mbar_wait(smem_u32(&sm.bar_s_free), (uc - 1) & 1)) || sm.abort) {
-            ok = false;
-            break;
-          }
+        // S^T_u and dP^T_u (tile u's Q / dO have landed)
+        auto issue_sdp = [&](int uq) -> bool {
+          const int st = uq % kBStages;
+          if (!mbar_wait(smem_u32(&sm.bar_qd_full[st]), (uq / kBStages) & 1) || sm.abort)
+            return false;
           tc_fence_after();
           const uint32_t qa = smem_u32(sm.q[st]), da = smem_u32(sm.dout[st]);
           if (NVF4) {
             // S^T from the NVFP4 copies: packed E2M1 rows of 32 bytes, one K = 64 product
             mma_nvf4(tmem + kColSP, smem_desc(smem_u32(sm.k4), 0, 256, kLayoutSW32),
                      smem_desc(smem_u32(sm.q4[st]), 0, 256, kLayoutSW32),
-                     idesc_nvf4(kTile, kTile), tmem + kSfK4, tmem + kSfQ4 + 4 * (uc & 1), 0);
+                     idesc_nvf4(kTile, kTile), tmem + kSfK4, tmem + kSfQ4 + 4 * (uq & 1), 0);
           } else {
 #pragma unroll
             for (int ks = 0; ks < DIM / 32; ++ks)
@@ -237,6 +239,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mma_f8(tmem + kColDP, smem_desc(va + 32 * ks, 0, sbo, lay),
                    smem_desc(da + 32 * ks, 0, sbo, lay), id_s, ks > 0);
           tc_commit(smem_u32(&sm.bar_s_full));
+          return true;
+        };
+        if (it.nq > 0) ok = ok && issue_sdp(uc);
+        for (int u = 0; ok && u < it.nq; ++u, ++uc) {
+          const int st = uc % kBStages;
+          const uint32_t qa = smem_u32(sm.q[st]), da = smem_u32(sm.dout[st]);
           // dV / dK restart from zero on an item's first tile: the previous
           // item's epilogue must have read them (its S^T / dP^T products could
           // already run meanwhile)
@@ -261,14 +269,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                      smem_desc(qa + kb * 32 * DIM, 0, sbo, lay),
                      idesc_mxf8(kTile, DIM, 0, 1, kb, kb), tmem + kSfDkA, tmem + kSfDkB,
                      (u > 0 || kb > 0));
-          // dQ_u = dS K : A = the same dS bytes read MN-major (M = queries), B = K MN-major
+          // dQ_u = dS K into its own columns, once the groups have read dQ_{u-1}:
+          // A = the same dS bytes read MN-major (M = queries), B = K MN-major
+          if (uc > 0 && (!mbar_wait(smem_u32(&sm.bar_dq_read), (uc - 1) & 1) || sm.abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll
           for (int kb = 0; kb < 4; ++kb)
-            mma_mxf8(tmem + kColSP, smem_desc(dsa + kb * 32 * kTile, 0, 1024, kLayoutSW128),
+            mma_mxf8(tmem + kColDQ, smem_desc(dsa + kb * 32 * kTile, 0, 1024, kLayoutSW128),
                      smem_desc(ka + kb * 32 * DIM, 0, sbo, lay),
                      idesc_mxf8(kTile, DIM, 1, 1, kb, kb), tmem + kSfDqA, tmem + kSfDqB, kb > 0);
           tc_commit(smem_u32(&sm.bar_dq_full));
           tc_commit(smem_u32(&sm.bar_qd_empty[st]));
+          // the next tile's S^T / dP^T right behind
+          if (u + 1 < it.nq && !issue_sdp(uc + 1)) {
+            ok = false;
+            break;
+          }
         }
         // this item's K / V may be replaced once its products are done
         if (ok) tc_commit(smem_u32(&sm.bar_kv_free));
@@ -453,6 +472,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             tmem_st8(tmem + lane_off + kSfDqA, w);
           }
+          // NVFP4: the next query tile's block scales, before this tile's dS is
+          // released (the next S^T is issued right behind this tile's products;
+          // the buffer of its parity was last read by S^T two tiles back,
+          // complete before this tile's S^T was)
+          if (NVF4 && g == 0 && u + 1 < nq)
+            write_sf4(prm.q4_scales, q0 + kTile, kSfQ4 + 4 * ((uc + 1) & 1));
           tmem_st_wait();
           fence_proxy_async_smem();
           tc_fence_before();
@@ -469,8 +494,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           uint32_t v[kCh][32];
 #pragma unroll
           for (int cc = 0; cc < kCh; ++cc)
-            tmem_ld32(tmem + lane_off + kColSP + 32 * (g * kCh + cc), v[cc]);
+            tmem_ld32(tmem + lane_off + kColDQ + 32 * (g * kCh + cc), v[cc]);
           tmem_ld_wait();
+          // dQ of the next tile may now be written
+          tc_fence_before();
+          mbar_arrive(smem_u32(&sm.bar_dq_read));
 #pragma unroll
           for (int cc = 0; cc < kCh; ++cc) {
             float* row = sm.dqs[g * kCh + cc] + j * 32;
@@ -484,15 +512,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               *reinterpret_cast<float4*>(row + 4 * (i ^ (j & 7))) = f;
             }
           }
-          // NVFP4: stage the next query tile's block scales (the buffer of the
-          // next tile's parity was last read by S^T two tiles back, complete)
-          if (NVF4 && g == 0 && u + 1 < nq) {
-            write_sf4(prm.q4_scales, q0 + kTile, kSfQ4 + 4 * ((uc + 1) & 1));
-            tmem_st_wait();
-          }
           fence_proxy_async_smem();
-          tc_fence_before();
-          mbar_arrive(smem_u32(&sm.bar_s_free));
         }
         if (!ok) sm.abort = 1;
         // the next tile's per-query inputs (its buffer was last read before this
