@@ -27,6 +27,8 @@ extern "C" {
  *  mode 2: E2M1 x E2M1 block-scaled, E4M3 scale per 16 along K (K = 64,
  *          two codes per byte, element 2i in the low nibble); sfa u8 [128][4],
  *          sfb u8 [N][4]; both operands K-major.
+ *  mode 3: as mode 1, with A read from tensor memory (row m in lane m, four
+ *          E4M3 elements per 32-bit column along K); A must be K-major.
  *  a: a_mn_major == 0 -> u8 [128][K bytes] (rows = M); 1 -> u8 [K][128].
  *  b: b_mn_major == 0 -> u8 [N][K bytes]   (rows = N); 1 -> u8 [K][N].
  *  N in {64, 128}.  variant: bit 0 swaps the leading / stride byte offsets of

@@ -9,14 +9,16 @@
 //   warps 8-11  softmax of query tile 1
 // Per key tile j the MMA warp issues S_t = Q_t K_j^T (unscaled E4M3, f32 in
 // TMEM) and, once the softmax group has written the E4M3 probability tile
-// P^_t to shared memory, O_t += P^_t V_j as a block-scaled MMA whose B scale
-// is the per-32-key E8M0 scale of V.  The two query tiles ping-pong so the
-// tensor core works on one while the other tile's softmax runs.
+// P^_t back into the consumed columns of S_t, O_t += P^_t V_j as a
+// block-scaled MMA with A read from tensor memory and B = V_j (its per-32-key
+// E8M0 scale).  The two query tiles ping-pong so the tensor core works on one
+// while the other tile's softmax runs.
 //
 // Tensor memory (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+d),
-// O_1 [256+d, 256+2d).  The scale factors of P^_t V_j are written into the
-// first 8 columns of S_t after the softmax has read S_t; the next S_t MMA is
-// issued after P^_t V_j, and tcgen05 MMAs of one thread execute in order.
+// O_1 [256+d, 256+2d).  After the softmax has read S_t, columns 0..7 of S_t
+// take the scale factors of P^_t V_j and columns 8..39 the P^_t codes (four
+// per column); the next S_t MMA is issued after P^_t V_j, and tcgen05 MMAs of
+// one thread execute in order.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -27,6 +29,8 @@ namespace flamia {
 namespace {
 
 constexpr int kStages = 3;
+// first column of P^_t inside S_t (columns 0..7 hold the scale factors of P^V)
+constexpr uint32_t kColP = 8;
 constexpr int kFwdThreads = 384;
 constexpr float kLn2 = 0.69314718055994530942f;
 
@@ -37,7 +41,6 @@ struct FwdSmem {
   alignas(1024) uint8_t q[2][kTileBytes];
   alignas(1024) uint8_t k[kStages][kTileBytes];
   alignas(1024) uint8_t v[kStages][kTileBytes];
-  alignas(1024) uint8_t p[2][kTile * kTile];
   alignas(NVF4 ? 1024 : 16) uint8_t q4[2][kTile4Bytes];
   alignas(NVF4 ? 1024 : 16) uint8_t k4[kStages][kTile4Bytes];
   uint64_t bar_sf;
@@ -337,13 +340,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               break;
             }
             tc_fence_after();
-            const uint32_t pa = smem_u32(sm.p[t]), va = smem_u32(sm.v[st]);
-            const uint32_t sf = tmem + t * kTile;  // scale factors live in S_t columns 0..7
+            const uint32_t va = smem_u32(sm.v[st]);
+            // S_t columns 0..7 hold the scale factors, 8..39 the E4M3 P^_t (A
+            // from tensor memory: 4 keys per column, 8 columns per 32-key step)
+            const uint32_t sf = tmem + t * kTile;
 #pragma unroll
             for (int kb = 0; kb < 4; ++kb)
-              mma_mxf8(tmem + 256 + t * DIM, smem_desc(pa + 32 * kb, 0, 1024, kLayoutSW128),
-                       smem_desc(va + kb * 32 * DIM, 0, sbo, lay),
-                       idesc_mxf8(kTile, DIM, 0, 1, kb, kb), sf, sf + 4, (j > 0 || kb > 0));
+              mma_mxf8_ts(tmem + 256 + t * DIM, sf + kColP + 8 * kb,
+                          smem_desc(va + kb * 32 * DIM, 0, sbo, lay),
+                          idesc_mxf8(kTile, DIM, 0, 1, kb, kb), sf, sf + 4, (j > 0 || kb > 0));
             if (j + 1 < nt) {
               if (kv_ready <= jk + 1) {
                 if (!mbar_wait(smem_u32(&sm.bar_kv_full[(jk + 1) % kStages]),
@@ -379,7 +384,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t tS = tmem + lane_off + t * kTile;
     const uint32_t tO = tmem + lane_off + 256 + t * DIM;
-    uint8_t* prow = sm.p[t] + r * kTile;
     int s_seen = 0, o_seen = 0;  // completions of s_full[t] and o_full[t] waited so far
     int kvc = 0;                 // global index of the current item's first key tile
     bool ok = true;
@@ -485,10 +489,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             chunk_probs<true>(sv[c], cf[c], moff, lim - 32 * c, lsum, w);
           else
             chunk_probs<false>(sv[c], cf[c], moff, 0, lsum, w);
-          // 32 bytes = 16-byte chunks 2c and 2c+1 of row r, 128B-swizzled
-          const int ch0 = (2 * c) ^ (r & 7), ch1 = (2 * c + 1) ^ (r & 7);
-          *reinterpret_cast<uint4*>(prow + 16 * ch0) = make_uint4(w[0], w[1], w[2], w[3]);
-          *reinterpret_cast<uint4*>(prow + 16 * ch1) = make_uint4(w[4], w[5], w[6], w[7]);
+          // the 32 codes of this chunk: row r of P^_t, keys 32 c .. 32 c + 31, into
+          // the consumed columns of S_t (the row was read into registers)
+          tmem_st8(tS + kColP + 8 * c, w);
         }
         l8 += lsum.x + lsum.y;
         if (__any_sync(0xffffffffu, need)) {
@@ -527,7 +530,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (NVF4 && t == 0 && j + 1 < it.nkv)
           write_sf4(prm.k4_scales, k0 + kTile, kSfK4 + 4 * ((kv0 + j + 1) & 1));
         tmem_st_wait();
-        fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(smem_u32(&sm.bar_p_full[t]));
       }

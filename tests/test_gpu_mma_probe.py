@@ -41,7 +41,7 @@ def _reference(mode, N, a_mn, b_mn, a, b, sfa, sfb):
         return A @ B.T
     A = O.e4m3_decode(a.T if a_mn else a)          # [128][K]
     B = O.e4m3_decode(b.T if b_mn else b)          # [N][K]
-    if mode == 1:
+    if mode in (1, 3):
         A = A * np.repeat(np.ldexp(1.0, sfa.astype(int) - 127), 32, axis=1)
         B = B * np.repeat(np.ldexp(1.0, sfb.astype(int) - 127), 32, axis=1)
     return A @ B.T
@@ -56,6 +56,9 @@ CASES = [
     (1, 128, 1, 1),   # dQ = dS K (dS read MN-major)
     (1, 128, 0, 0),
     (2, 128, 0, 0),   # NVFP4 S = Q K^T, d = 64
+    (3, 128, 0, 1),   # O += P V with P from tensor memory, d = 128
+    (3, 64, 0, 1),    # the same, d = 64
+    (3, 128, 0, 0),
 ]
 
 
@@ -71,8 +74,8 @@ def test_tile_product(lib, mode, N, a_mn, b_mn):
     else:
         a = _codes_e4m3(rng, (128, 128))
         b = _codes_e4m3(rng, (128, N) if b_mn else (N, 128))
-        sfa = rng.integers(122, 133, size=(128, 4), dtype=np.uint8) if mode == 1 else None
-        sfb = rng.integers(122, 133, size=(N, 4), dtype=np.uint8) if mode == 1 else None
+        sfa = rng.integers(122, 133, size=(128, 4), dtype=np.uint8) if mode in (1, 3) else None
+        sfb = rng.integers(122, 133, size=(N, 4), dtype=np.uint8) if mode in (1, 3) else None
     ref = _reference(mode, N, a_mn, b_mn, a, b, sfa, sfb)
     tol = 1e-5 * np.abs(ref).max()
     got = _run(fl, mode, N, a_mn, b_mn, 0, a, b, sfa, sfb)
