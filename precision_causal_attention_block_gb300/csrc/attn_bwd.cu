@@ -255,6 +255,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             break;
           }
           tc_fence_after();
+          // dQ_u = dS K into its own columns, once the groups have read dQ_{u-1}:
+          // A = the same dS bytes read MN-major (M = queries), B = K MN-major
+          if (uc > 0 && (!mbar_wait(smem_u32(&sm.bar_dq_read), (uc - 1) & 1) || sm.abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int kb = 0; kb < 4; ++kb)
+            mma_mxf8(tmem + kColDQ, smem_desc(dsa + kb * 32 * kTile, 0, 1024, kLayoutSW128),
+                     smem_desc(ka + kb * 32 * DIM, 0, sbo, lay),
+                     idesc_mxf8(kTile, DIM, 1, 1, kb, kb), tmem + kSfDqA, tmem + kSfDqB, kb > 0);
+          // dQ first: the groups read it out while dV / dK run
+          tc_commit(smem_u32(&sm.bar_dq_full));
           // dV += P^b^T dO : A [key][query] K-major, B = dO tile read MN-major
 #pragma unroll
           for (int kb = 0; kb < 4; ++kb)
@@ -269,19 +283,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                      smem_desc(qa + kb * 32 * DIM, 0, sbo, lay),
                      idesc_mxf8(kTile, DIM, 0, 1, kb, kb), tmem + kSfDkA, tmem + kSfDkB,
                      (u > 0 || kb > 0));
-          // dQ_u = dS K into its own columns, once the groups have read dQ_{u-1}:
-          // A = the same dS bytes read MN-major (M = queries), B = K MN-major
-          if (uc > 0 && (!mbar_wait(smem_u32(&sm.bar_dq_read), (uc - 1) & 1) || sm.abort)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll
-          for (int kb = 0; kb < 4; ++kb)
-            mma_mxf8(tmem + kColDQ, smem_desc(dsa + kb * 32 * kTile, 0, 1024, kLayoutSW128),
-                     smem_desc(ka + kb * 32 * DIM, 0, sbo, lay),
-                     idesc_mxf8(kTile, DIM, 1, 1, kb, kb), tmem + kSfDqA, tmem + kSfDqB, kb > 0);
-          tc_commit(smem_u32(&sm.bar_dq_full));
           tc_commit(smem_u32(&sm.bar_qd_empty[st]));
           // the next tile's S^T / dP^T right behind
           if (u + 1 < it.nq && !issue_sdp(uc + 1)) {

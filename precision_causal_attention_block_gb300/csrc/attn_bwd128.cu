@@ -230,6 +230,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t qa = smem_u32(sm.q[st]), da = smem_u32(sm.dout[st]);
           const uint32_t pba = smem_u32(sm.pb[b]), dsa = smem_u32(sm.ds[b]);
           const uint32_t sf = tmem + col_p(b);
+          // dQ^T_t = K^T dS^T : A = K read MN-major (M = dims), B = dS read MN-major
+#pragma unroll
+          for (int kb = 0; kb < kTile / 32; ++kb)
+            mma_mxf8(tmem + col_s(b), smem_desc(ka + kb * 32 * kD, 0, 1024, kLayoutSW128),
+                     smem_desc(dsa + kb * 32 * kQT, 0, 512, kLayoutSW64),
+                     idesc_mxf8(kD, kQT, 1, 1, kb, kb), sf + kSfDqA, sf + kSfDqB, kb > 0);
+          // dQ^T first: the group reads it out while dV / dK run
+          tc_commit(smem_u32(&sm.bar_dq_full[b]));
           // dV += P^b^T dO_t : A [key][query] K-major (64-byte rows), B = dO_t MN-major
 #pragma unroll
           for (int kb = 0; kb < kQT / 32; ++kb)
@@ -244,13 +252,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                      smem_desc(qa + kb * 32 * kD, 0, 1024, kLayoutSW128),
                      idesc_mxf8(kTile, kD, 0, 1, kb, kb), sf + kSfDkA, sf + kSfDkB,
                      (u > 0 || kb > 0));
-          // dQ^T_t = K^T dS^T : A = K read MN-major (M = dims), B = dS read MN-major
-#pragma unroll
-          for (int kb = 0; kb < kTile / 32; ++kb)
-            mma_mxf8(tmem + col_s(b), smem_desc(ka + kb * 32 * kD, 0, 1024, kLayoutSW128),
-                     smem_desc(dsa + kb * 32 * kQT, 0, 512, kLayoutSW64),
-                     idesc_mxf8(kD, kQT, 1, 1, kb, kb), sf + kSfDqA, sf + kSfDqB, kb > 0);
-          tc_commit(smem_u32(&sm.bar_dq_full[b]));
           tc_commit(smem_u32(&sm.bar_qd_empty[st]));
           if (u + 2 < nq && !issue_sdp(t + 2)) {
             ok = false;
