@@ -29,9 +29,10 @@ extern "C" {
  *          sfb u8 [N][4]; both operands K-major.
  *  mode 3: as mode 1, with A read from tensor memory (row m in lane m, four
  *          E4M3 elements per 32-bit column along K); A must be K-major.
+ *  mode 4: as mode 0, with A read from tensor memory as in mode 3.
  *  a: a_mn_major == 0 -> u8 [128][K bytes] (rows = M); 1 -> u8 [K][128].
  *  b: b_mn_major == 0 -> u8 [N][K bytes]   (rows = N); 1 -> u8 [K][N].
- *  N in {64, 128}.  variant: bit 0 swaps the leading / stride byte offsets of
+ *  N in {32, 64, 128}.  variant: bit 0 swaps the leading / stride byte offsets of
  *  MN-major descriptors; bits 1..2 select the scale-factor placement in
  *  tensor memory (0: column = row / 32, lane = row % 32, replicated in all
  *  lane quadrants; 1: lane = row).

@@ -15,7 +15,7 @@ struct ProbeSmem {
 };
 
 struct ProbeArgs {
-  int mode, N, a_mn, b_mn, variant;  // mode 3: mode 1 with A from tensor memory
+  int mode, N, a_mn, b_mn, variant;  // modes 3 / 4: modes 1 / 0 with A from tensor memory
   const uint8_t* a_g;                 // A in global memory ([128][128] K-major, mode 3)
   int a_bytes, b_bytes;
   uint32_t a_rowb, b_rowb;  // bytes per shared-memory row of each operand
@@ -57,7 +57,7 @@ __global__ void __launch_bounds__(128, 1)
     tma_load_2d(smem_u32(sm.b), &map_b, bl, 0, 0);
   }
   // scale factors into tensor memory (columns 128.. for A, 132.. for B)
-  if (g.mode != 0) {
+  if (g.mode == 1 || g.mode == 2 || g.mode == 3) {
     const int variant = (g.variant >> 1) & 3;
     uint32_t w[8];
     for (int c = 0; c < 4; ++c) {
@@ -79,13 +79,14 @@ __global__ void __launch_bounds__(128, 1)
       w[4 + c] = wb;
     }
     tmem_st8(tmem + (static_cast<uint32_t>(warp * 32) << 16) + 128, w);
-    if (g.mode == 3) {
-      // A row (warp * 32 + lane) into columns 160..191: 4 K elements per column
-      uint32_t r[32];
-      const uint32_t* src = reinterpret_cast<const uint32_t*>(g.a_g) + (warp * 32 + lane) * 32;
-      for (int i = 0; i < 32; ++i) r[i] = src[i];
-      tmem_st32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + 160, r);
-    }
+    tmem_st_wait();
+  }
+  if (g.mode >= 3) {
+    // A row (warp * 32 + lane) into columns 160..191: 4 K elements per column
+    uint32_t r[32];
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(g.a_g) + (warp * 32 + lane) * 32;
+    for (int i = 0; i < 32; ++i) r[i] = src[i];
+    tmem_st32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + 160, r);
     tmem_st_wait();
   }
   tc_fence_before();
@@ -103,11 +104,14 @@ __global__ void __launch_bounds__(128, 1)
         const uint32_t off = 8 * rowb;
         return smem_desc(base + ks * 32 * rowb, swap ? off : 0, swap ? 0 : off, layout_for(rowb));
       };
-      if (g.mode == 3) {
+      if (g.mode >= 3) {
         for (int ks = 0; ks < 4; ++ks) {
           const uint64_t bd = g.b_mn ? mdesc(ba, g.b_rowb, ks) : kdesc(ba, g.b_rowb, ks);
-          mma_mxf8_ts(tmem, tmem + 160 + 8 * ks, bd, idesc_mxf8(128, g.N, 0, g.b_mn, ks, ks),
-                      tmem + 128, tmem + 132, ks > 0);
+          if (g.mode == 3)
+            mma_mxf8_ts(tmem, tmem + 160 + 8 * ks, bd, idesc_mxf8(128, g.N, 0, g.b_mn, ks, ks),
+                        tmem + 128, tmem + 132, ks > 0);
+          else
+            mma_f8_ts(tmem, tmem + 160 + 8 * ks, bd, idesc_f8(128, g.N, 0, g.b_mn), ks > 0);
         }
       } else if (g.mode == 0 || g.mode == 1) {
         for (int ks = 0; ks < 4; ++ks) {
@@ -155,11 +159,12 @@ extern "C" flamia_status flamia_debug_mma_tile(int mode, int N, int a_mn_major, 
                                                int variant, const uint8_t* a, const uint8_t* b,
                                                const uint8_t* sfa, const uint8_t* sfb,
                                                float* d_out, int* dev_status, void* stream) {
-  if (mode < 0 || mode > 3 || (N != 64 && N != 128) || variant < 0 || variant > 3)
+  if (mode < 0 || mode > 4 || (N != 32 && N != 64 && N != 128) || variant < 0 || variant > 3)
     return FLAMIA_ERR_UNSUPPORTED;
-  if (!a || !b || !d_out || (mode != 0 && (!sfa || !sfb))) return FLAMIA_ERR_INVALID_ARG;
+  if (!a || !b || !d_out || ((mode == 1 || mode == 2 || mode == 3) && (!sfa || !sfb)))
+    return FLAMIA_ERR_INVALID_ARG;
   if (mode == 2 && (a_mn_major || b_mn_major)) return FLAMIA_ERR_UNSUPPORTED;
-  if (mode == 3 && a_mn_major) return FLAMIA_ERR_UNSUPPORTED;
+  if (mode >= 3 && a_mn_major) return FLAMIA_ERR_UNSUPPORTED;
   if (!aligned(a, 16) || !aligned(b, 16)) return FLAMIA_ERR_INVALID_ARG;
   const int kbytes = mode == 2 ? 32 : 128;  // K = 128 E4M3 or 64 packed E2M1
   ProbeArgs g;

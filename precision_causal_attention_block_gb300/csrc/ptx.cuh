@@ -270,6 +270,18 @@ __device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64
       : "memory");
 }
 
+// D (+)= A * B, E4M3 x E4M3 -> F32, A read from tensor memory (row m in lane
+// m, four elements per 32-bit column along K), B in shared memory.
+__device__ __forceinline__ void mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // The same product with A read from tensor memory: row m of A in lane m,
 // four E4M3 elements per 32-bit column along K (a_tmem = the first column of
 // this K step's 32 elements).

@@ -59,6 +59,11 @@ CASES = [
     (3, 128, 0, 1),   # O += P V with P from tensor memory, d = 128
     (3, 64, 0, 1),    # the same, d = 64
     (3, 128, 0, 0),
+    (0, 32, 0, 0),    # S^T = K Q^T with 32-query tiles
+    (4, 32, 0, 0),    # the same with K from tensor memory
+    (4, 128, 0, 0),
+    (1, 32, 1, 1),    # dQ^T = K^T dS^T with 32-query tiles (both MN-major)
+    (1, 32, 0, 1),
 ]
 
 
