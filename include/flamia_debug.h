@@ -35,7 +35,8 @@ extern "C" {
  *  N in {32, 64, 128}.  variant: bit 0 swaps the leading / stride byte offsets of
  *  MN-major descriptors; bits 1..2 select the scale-factor placement in
  *  tensor memory (0: column = row / 32, lane = row % 32, replicated in all
- *  lane quadrants; 1: lane = row).
+ *  lane quadrants; 1: lane = row; 2: as 0 for B, while each lane quadrant q
+ *  holds only A's rows 32 q .. 32 q + 31, in column q, and zeros elsewhere).
  * All pointers are device pointers, 16-byte aligned.
  */
 flamia_status flamia_debug_mma_tile(int mode, int N, int a_mn_major, int b_mn_major, int variant,

@@ -62,12 +62,12 @@ __global__ void __launch_bounds__(128, 1)
     uint32_t w[8];
     for (int c = 0; c < 4; ++c) {
       int ma, nb;
-      if (variant == 0) {
-        ma = 32 * c + lane;
-        nb = 32 * c + lane;
-      } else {
+      if (variant == 1) {
         ma = 32 * warp + lane;
         nb = 32 * warp + lane;
+      } else {  // 0: every lane quadrant holds all rows; 2: only the rows of this warp
+        ma = 32 * c + lane;
+        nb = 32 * c + lane;
       }
       uint32_t wa = 0, wb = 0;
       for (int kb = 0; kb < 4; ++kb) {
@@ -75,7 +75,9 @@ __global__ void __launch_bounds__(128, 1)
         const uint32_t bb = nb < g.N ? g.sfb[nb * 4 + kb] : ((g.mode == 1 || g.mode == 3) ? 127u : 0x38u);
         wb |= bb << (8 * kb);
       }
-      w[c] = wa;
+      // placement 2: A's columns of other warps' rows hold 0 (2^-127), which
+      // a product reading them would show; B stays replicated
+      w[c] = (variant != 2 || c == warp) ? wa : 0u;
       w[4 + c] = wb;
     }
     tmem_st8(tmem + (static_cast<uint32_t>(warp * 32) << 16) + 128, w);
@@ -159,7 +161,7 @@ extern "C" flamia_status flamia_debug_mma_tile(int mode, int N, int a_mn_major, 
                                                int variant, const uint8_t* a, const uint8_t* b,
                                                const uint8_t* sfa, const uint8_t* sfb,
                                                float* d_out, int* dev_status, void* stream) {
-  if (mode < 0 || mode > 4 || (N != 32 && N != 64 && N != 128) || variant < 0 || variant > 3)
+  if (mode < 0 || mode > 4 || (N != 32 && N != 64 && N != 128) || variant < 0 || variant > 5)
     return FLAMIA_ERR_UNSUPPORTED;
   if (!a || !b || !d_out || ((mode == 1 || mode == 2 || mode == 3) && (!sfa || !sfb)))
     return FLAMIA_ERR_INVALID_ARG;

@@ -94,3 +94,19 @@ def test_tile_product(lib, mode, N, a_mn, b_mn):
                 report[var] = str(ex)
         pytest.fail(f"variant 0 max rel err {np.abs(got - ref).max() / np.abs(ref).max():.3e}; "
                     f"other variants: {report}")
+
+
+@pytest.mark.parametrize("mode,N", [(1, 128), (3, 128), (3, 64)])
+def test_row_scales_from_own_lane_quadrant(lib, mode, N):
+    """A's per-row block scales need only be present in the lane quadrant of
+    the warp that owns the row (placement 2): each softmax warp can then set
+    the scale of its own rows without exchanging them."""
+    from precision_causal_attention_block_gb300 import flamia as fl
+    rng = np.random.default_rng(7 + mode + N)
+    a = _codes_e4m3(rng, (128, 128))
+    b = _codes_e4m3(rng, (128, N))
+    sfa = rng.integers(118, 137, size=(128, 4), dtype=np.uint8)
+    sfb = rng.integers(122, 133, size=(N, 4), dtype=np.uint8)
+    ref = _reference(mode, N, 0, 1, a, b, sfa, sfb)
+    got = _run(fl, mode, N, 0, 1, 2 << 1, a, b, sfa, sfb)
+    assert np.abs(got - ref).max() <= 1e-5 * np.abs(ref).max()
