@@ -429,7 +429,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 make_float2(__uint_as_float(dv[i]), __uint_as_float(dv[i + 1])), inv2);
             const float2 b = __fmul2_rn(
                 make_float2(__uint_as_float(dv[i + 2]), __uint_as_float(dv[i + 3])), inv2);
-            dw[i / 4] = cvt_e4m3x2(a.x, a.y) | (cvt_e4m3x2(b.x, b.y) << 16);
+            dw[i / 4] = cvt_e4m3x4(a.x, a.y, b.x, b.y);
           }
           const int ch0 = (2 * c) ^ (j & 7), ch1 = (2 * c + 1) ^ (j & 7);
           *reinterpret_cast<uint4*>(pbrow + 16 * ch0) = make_uint4(pw[0], pw[1], pw[2], pw[3]);

@@ -385,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 make_float2(__uint_as_float(dv[i]), __uint_as_float(dv[i + 1])), inv2);
             const float2 bq = __fmul2_rn(
                 make_float2(__uint_as_float(dv[i + 2]), __uint_as_float(dv[i + 3])), inv2);
-            dw[i / 4] = cvt_e4m3x2(a.x, a.y) | (cvt_e4m3x2(bq.x, bq.y) << 16);
+            dw[i / 4] = cvt_e4m3x4(a.x, a.y, bq.x, bq.y);
           }
           const int ch0 = (2 * c) ^ sw, ch1 = (2 * c + 1) ^ sw;
           *reinterpret_cast<uint4*>(pbrow + 16 * ch0) = make_uint4(pw[0], pw[1], pw[2], pw[3]);

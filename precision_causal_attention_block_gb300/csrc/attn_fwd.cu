@@ -13,6 +13,9 @@
 // block-scaled MMA with A read from tensor memory and B = V_j (its per-32-key
 // E8M0 scale).  The two query tiles ping-pong so the tensor core works on one
 // while the other tile's softmax runs.
+// The growth of the running maximum is not applied to O in tensor memory: the
+// A scale of P^_t (one E8M0 per row) carries 2^(m - m_ref) instead, and the
+// epilogue divides by 2^(m - m_ref) l.
 //
 // Tensor memory (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+d),
 // O_1 [256+d, 256+2d).  After the softmax has read S_t, columns 0..7 of S_t
@@ -33,6 +36,9 @@ constexpr int kStages = 3;
 constexpr uint32_t kColP = 8;
 constexpr int kFwdThreads = 384;
 constexpr float kLn2 = 0.69314718055994530942f;
+// Largest exponent of the per-row block scale of P^ before O is rescaled: it
+// bounds O's growth over the true scale to 2^32, far inside float32 range.
+constexpr int kRefSpan = 32;
 
 template <int DIM, bool NVF4>
 struct FwdSmem {
@@ -124,7 +130,7 @@ __device__ __forceinline__ void chunk_probs(const uint32_t (&v)[32], float cf, f
     const float2 pb = make_float2(ex2_approx(b.x), ex2_approx(b.y));
     lsum = __fadd2_rn(lsum, pa);
     lsum = __fadd2_rn(lsum, pb);
-    w[i / 4] = cvt_e4m3x2(pa.x, pa.y) | (cvt_e4m3x2(pb.x, pb.y) << 16);
+    w[i / 4] = cvt_e4m3x4(pa.x, pa.y, pb.x, pb.y);
   }
 }
 
@@ -409,7 +415,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const size_t hT = static_cast<size_t>(h) * T;
       const int eq = NVF4 ? 0 : static_cast<int>(prm.q_scales[hT + min(qi, T - 1)]) - 127;
       const float c_row = prm.scale_log2 * pow2_or_zero(eq);
-      float m = -INFINITY, l8 = 0.f;
+      // m: running integer row maximum (log2 units); l8 = sum of 2^8 exp2(s - m);
+      // m_ref: the maximum whose scale O_t is kept in (see the block scale of P^ below)
+      float m = -INFINITY, l8 = 0.f, m_ref = 0.f;
       // NVFP4 score product: its block scales live in tensor memory, one 32-bit
       // word (4 E4M3 scales) per row; column c + i of this lane quadrant holds
       // row 32 i + lane (the same words in every quadrant).
@@ -475,9 +483,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         float m_new = (mx == -INFINITY) ? m : fmaxf(m, ceilf(mx));
         if (m_new == -INFINITY) m_new = 0.f;
-        const bool need = (j > 0) && (m_new > m);
-        const float corr = need ? pow2_or_zero(static_cast<int>(m - m_new)) : 1.f;
-        l8 *= corr;
+        if (j == 0) m_ref = m_new;
+        if (j > 0 && m_new > m) l8 *= pow2_or_zero(static_cast<int>(m - m_new));
         m = m_new;
         const float moff = m - 8.f;  // P8 = 2^8 exp2(s - m)
         // pass 2: probabilities, row sum, E4M3 operand
@@ -494,12 +501,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           tmem_st8(tS + kColP + 8 * c, w);
         }
         l8 += lsum.x + lsum.y;
-        if (__any_sync(0xffffffffu, need)) {
-          // rescale this warp's O rows by the (exact power-of-two) correction,
-          // now that the row of S is consumed (the products of key tile j - 1
-          // into O completed before S_t of tile j); P^_t V_j is issued only
-          // after this group's p_full arrive below
-          const float2 c2 = make_float2(corr, corr);
+        // P^_t V_j enters O_t with the block scale 2^(m - m_ref) on P^'s row:
+        // O_t stays in the scale of m_ref and needs no rescaling when the
+        // maximum grows (powers of two: the same sums, exactly).  Only a growth
+        // past kRefSpan moves m_ref, rescaling O_t once; the products into O_t
+        // of key tile j - 1 completed before S_t of tile j.
+        int dm = static_cast<int>(m - m_ref);
+        if (__any_sync(0xffffffffu, dm > kRefSpan)) {
+          const float c = pow2_or_zero(-dm);
+          const float2 c2 = make_float2(c, c);
 #pragma unroll 1
           for (int c0 = 0; c0 < DIM / 32; c0 += 2) {
             uint32_t a[32], b[32];
@@ -518,11 +528,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             tmem_st32(tO + 32 * c0, a);
             tmem_st32(tO + 32 * (c0 + 1), b);
           }
-          tmem_st_wait();
+          m_ref = m;
+          dm = 0;
         }
-        // scale factors of P^_t V_j: A (P^) 2^0 for every K block, B = V's block bytes
-        const uint32_t sfw[8] = {0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu,
-                                 sfb, sfb, sfb, sfb};
+        // scale factors of P^_t V_j: A (P^, this row) 2^dm for every K block
+        // (each lane quadrant holds its own rows), B = V's block bytes
+        const uint32_t sa = static_cast<uint32_t>(127 + dm) * 0x01010101u;
+        const uint32_t sfw[8] = {sa, sa, sa, sa, sfb, sfb, sfb, sfb};
         tmem_st8(tS, sfw);
         // NVFP4: group 0 stages the block scales of the next key tile (its
         // buffer was last read by the products of key tile j - 1, which
@@ -539,7 +551,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       if (nt > 0 && ok) {
         tc_fence_after();
-        const float inv = 1.f / l8;
+        const float inv = pow2_or_zero(static_cast<int>(m_ref - m)) / l8;
         __nv_bfloat16* orow = prm.o + (static_cast<size_t>(qi) * H + h) * DIM;
 #pragma unroll 1
         for (int c = 0; c < DIM / 32; ++c) {

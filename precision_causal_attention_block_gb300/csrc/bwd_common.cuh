@@ -69,7 +69,7 @@ __device__ __forceinline__ float bwd_chunk(const uint32_t (&sv)[32], uint32_t (&
     dv[i + 1] = __float_as_uint(d01.y);
     dv[i + 2] = __float_as_uint(d23.x);
     dv[i + 3] = __float_as_uint(d23.y);
-    pw[i / 4] = cvt_e4m3x2(p01.x, p01.y) | (cvt_e4m3x2(p23.x, p23.y) << 16);
+    pw[i / 4] = cvt_e4m3x4(p01.x, p01.y, p23.x, p23.y);
   }
   return amax;
 }

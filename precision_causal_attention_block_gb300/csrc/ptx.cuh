@@ -443,6 +443,19 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
   return r;
 }
 
+// Four floats -> four E4M3 codes in one word (a in bits 0..7, ..., d in 24..31),
+// each rounded to nearest even and saturated as cvt_e4m3x2 does.
+__device__ __forceinline__ uint32_t cvt_e4m3x4(float a, float b, float c, float d) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(a), "f"(b), "f"(c), "f"(d));
+  return r;
+}
+
 // Two E4M3 codes (bits 0..7 and 8..15) -> two exact floats.
 __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t codes) {
   uint32_t h2;
