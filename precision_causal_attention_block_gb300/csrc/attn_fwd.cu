@@ -438,27 +438,28 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tc_fence_before();
         mbar_arrive(smem_u32(&sm.bar_sf));
       }
-      // scale bytes of the K and V blocks of key tile j, fetched one step ahead
-      uint32_t kbyte[4], vbyte[4];
+      // E8M0 bytes of the 4 key blocks of key tile jj, fetched a step ahead:
+      // lane kb loads K block kb's byte, lane 4 + kb V block kb's (the same
+      // bytes serve every row, so one load per lane and the warp shares them)
+      uint32_t sbyte = 127u;
       auto fetch_scales = [&](int jj) {
-#pragma unroll
-        for (int kb = 0; kb < 4; ++kb) {
-          const int kk = s + jj * kTile + 32 * kb;
-          const bool in = jj < nt && kk < e;
-          kbyte[kb] = (in && !NVF4) ? prm.k_scales[hT + kk] : 127u;
-          vbyte[kb] = in ? prm.v_scales[hT + kk] : 127u;
-        }
+        const int kk = s + jj * kTile + 32 * (lane & 3);
+        const bool in = lane < 8 && (lane >= 4 || !NVF4) && jj < nt && kk < e;
+        sbyte = in ? (lane < 4 ? prm.k_scales : prm.v_scales)[hT + kk] : 127u;
       };
       fetch_scales(0);
       for (int j = 0; j < nt; ++j) {
         const int k0 = s + j * kTile;
+        // lanes 0..3 gather the K word, lanes 4..7 the V word (byte kb = block kb)
+        uint32_t sw = sbyte << (8 * (lane & 3));
+        sw |= __shfl_xor_sync(0xffffffffu, sw, 1);
+        sw |= __shfl_xor_sync(0xffffffffu, sw, 2);
+        const uint32_t kword = __shfl_sync(0xffffffffu, sw, 0);
+        const uint32_t sfb = __shfl_sync(0xffffffffu, sw, 4);
         float cf[4];
-        uint32_t sfb = 0;
 #pragma unroll
-        for (int kb = 0; kb < 4; ++kb) {
-          cf[kb] = c_row * pow2_or_zero(static_cast<int>(kbyte[kb]) - 127);
-          sfb |= vbyte[kb] << (8 * kb);
-        }
+        for (int kb = 0; kb < 4; ++kb)  // c_row 2^(byte - 127); byte 0 gives 0
+          cf[kb] = c_row * __int_as_float(((kword >> (8 * kb)) & 0xFFu) << 23);
         fetch_scales(j + 1);  // in flight while this tile is processed
         if (!mbar_wait(smem_u32(&sm.bar_s_full[t]), s_seen & 1) || sm.abort) {
           ok = false;
