@@ -179,33 +179,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t ka = smem_u32(sm.k), va = smem_u32(sm.v);
+    // The whole warp runs this role on warp-uniform values; one elected lane
+    // issues each tcgen05 instruction.
+    {
       constexpr uint32_t id_s = idesc_f8(kTile, kQT, 0, 0);
+      // operand descriptors, built once: a K step or a ring stage moves only
+      // the start address (bits 0..13, address / 16), which never carries out
+      // of its field inside shared memory
+      const uint64_t dk = smem_desc(smem_u32(sm.k), 0, 1024, kLayoutSW128);
+      const uint64_t dv = smem_desc(smem_u32(sm.v), 0, 1024, kLayoutSW128);
+      const uint64_t dq0 = smem_desc(smem_u32(sm.q[0]), 0, 1024, kLayoutSW128);
+      const uint64_t ddo0 = smem_desc(smem_u32(sm.dout[0]), 0, 1024, kLayoutSW128);
+      const uint64_t dpb0 = smem_desc(smem_u32(sm.pb[0]), 0, 512, kLayoutSW64);
+      const uint64_t dds0 = smem_desc(smem_u32(sm.ds[0]), 0, 512, kLayoutSW64);
+      constexpr uint32_t kQStep = kQT * kD / 16, kPStep = kTile * kQT / 16;  // stage strides
       int nk = 0, ug = 0;
       bool ok = true;
       // S^T_t and dP^T_t into the tensor-memory half of tile t
       auto issue_sdp = [&](int t) -> bool {
         const int st = t % kRing, b = t & 1;
-        if (!mbar_wait(smem_u32(&sm.bar_qd_full[st]), (t / kRing) & 1)) return false;
+        if (!mbar_wait_w(smem_u32(&sm.bar_qd_full[st]), (t / kRing) & 1)) return false;
         // the half's previous tile (t - 2) has had its dQ^T read out
-        if (t >= 2 && !mbar_wait(smem_u32(&sm.bar_dq_read[b]), ((t >> 1) - 1) & 1)) return false;
-        if (sm.abort) return false;
+        if (t >= 2 && !mbar_wait_w(smem_u32(&sm.bar_dq_read[b]), ((t >> 1) - 1) & 1)) return false;
+        if (__any_sync(0xffffffffu, sm.abort)) return false;
         tc_fence_after();
-        const uint32_t qa = smem_u32(sm.q[st]), da = smem_u32(sm.dout[st]);
+        const uint64_t dq = dq0 + st * kQStep, ddo = ddo0 + st * kQStep;
 #pragma unroll
         for (int ks = 0; ks < kD / 32; ++ks)
-          mma_f8(tmem + col_s(b), smem_desc(ka + 32 * ks, 0, 1024, kLayoutSW128),
-                 smem_desc(qa + 32 * ks, 0, 1024, kLayoutSW128), id_s, ks > 0);
+          mma_f8_w(tmem + col_s(b), dk + 2 * ks, dq + 2 * ks, id_s, ks > 0);
 #pragma unroll
         for (int ks = 0; ks < kD / 32; ++ks)
-          mma_f8(tmem + col_p(b), smem_desc(va + 32 * ks, 0, 1024, kLayoutSW128),
-                 smem_desc(da + 32 * ks, 0, 1024, kLayoutSW128), id_s, ks > 0);
-        tc_commit(smem_u32(&sm.bar_s_full[b]));
+          mma_f8_w(tmem + col_p(b), dv + 2 * ks, ddo + 2 * ks, id_s, ks > 0);
+        tc_commit_w(smem_u32(&sm.bar_s_full[b]));
         return true;
       };
       for (int n = 0; ok; ++n) {
-        const int idx = ring_get(sm.ring, n, true);
+        // every lane takes lane 0's copy; one arrive frees the slot
+        const int idx = __shfl_sync(0xffffffffu, ring_get(sm.ring, n, false), 0);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm.ring.empty[n % 4]));
         if (idx < 0) {
           ok = false;
           break;
@@ -214,59 +226,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         BwdItem it;
         if (!decode_bwd_item(prm, n_items, idx, it)) continue;
         const int nq = n_tiles64(it);
-        ok = mbar_wait(smem_u32(&sm.bar_kv), nk & 1) && (nq < 1 || issue_sdp(ug)) &&
+        ok = mbar_wait_w(smem_u32(&sm.bar_kv), nk & 1) && (nq < 1 || issue_sdp(ug)) &&
              (nq < 2 || issue_sdp(ug + 1));
         for (int u = 0; ok && u < nq; ++u) {
           const int t = ug + u, b = t & 1, st = t % kRing;
           // dV / dK restart from zero on an item's first tile: the previous
           // item's epilogue must have read them
-          if (!mbar_wait(smem_u32(&sm.bar_ds_full[b]), (t >> 1) & 1) ||
-              (u == 0 && nk > 0 && !mbar_wait(smem_u32(&sm.bar_acc_empty), (nk - 1) & 1)) ||
-              sm.abort) {
+          if (!mbar_wait_w(smem_u32(&sm.bar_ds_full[b]), (t >> 1) & 1) ||
+              (u == 0 && nk > 0 && !mbar_wait_w(smem_u32(&sm.bar_acc_empty), (nk - 1) & 1)) ||
+              __any_sync(0xffffffffu, sm.abort)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t qa = smem_u32(sm.q[st]), da = smem_u32(sm.dout[st]);
-          const uint32_t pba = smem_u32(sm.pb[b]), dsa = smem_u32(sm.ds[b]);
+          const uint64_t dq = dq0 + st * kQStep, ddo = ddo0 + st * kQStep;
+          const uint64_t dpb = dpb0 + b * kPStep, dds = dds0 + b * kPStep;
           const uint32_t sf = tmem + col_p(b);
           // dQ^T_t = K^T dS^T : A = K read MN-major (M = dims), B = dS read MN-major
 #pragma unroll
           for (int kb = 0; kb < kTile / 32; ++kb)
-            mma_mxf8(tmem + col_s(b), smem_desc(ka + kb * 32 * kD, 0, 1024, kLayoutSW128),
-                     smem_desc(dsa + kb * 32 * kQT, 0, 512, kLayoutSW64),
+            mma_mxf8_w(tmem + col_s(b), dk + kb * (32 * kD / 16), dds + kb * (32 * kQT / 16),
                      idesc_mxf8(kD, kQT, 1, 1, kb, kb), sf + kSfDqA, sf + kSfDqB, kb > 0);
           // dQ^T first: the group reads it out while dV / dK run
-          tc_commit(smem_u32(&sm.bar_dq_full[b]));
+          tc_commit_w(smem_u32(&sm.bar_dq_full[b]));
           // dV += P^b^T dO_t : A [key][query] K-major (64-byte rows), B = dO_t MN-major
 #pragma unroll
           for (int kb = 0; kb < kQT / 32; ++kb)
-            mma_mxf8(tmem + kColDV, smem_desc(pba + 32 * kb, 0, 512, kLayoutSW64),
-                     smem_desc(da + kb * 32 * kD, 0, 1024, kLayoutSW128),
+            mma_mxf8_w(tmem + kColDV, dpb + 2 * kb, ddo + kb * (32 * kD / 16),
                      idesc_mxf8(kTile, kD, 0, 1, kb, kb), sf + kSfDvA, sf + kSfDvB,
                      (u > 0 || kb > 0));
           // dK += dS^T Q_t
 #pragma unroll
           for (int kb = 0; kb < kQT / 32; ++kb)
-            mma_mxf8(tmem + kColDK, smem_desc(dsa + 32 * kb, 0, 512, kLayoutSW64),
-                     smem_desc(qa + kb * 32 * kD, 0, 1024, kLayoutSW128),
+            mma_mxf8_w(tmem + kColDK, dds + 2 * kb, dq + kb * (32 * kD / 16),
                      idesc_mxf8(kTile, kD, 0, 1, kb, kb), sf + kSfDkA, sf + kSfDkB,
                      (u > 0 || kb > 0));
-          tc_commit(smem_u32(&sm.bar_qd_empty[st]));
+          tc_commit_w(smem_u32(&sm.bar_qd_empty[st]));
           if (u + 2 < nq && !issue_sdp(t + 2)) {
             ok = false;
             break;
           }
         }
         if (!ok) break;
-        tc_commit(smem_u32(&sm.bar_acc_full));
-        tc_commit(smem_u32(&sm.bar_kv_free));
+        tc_commit_w(smem_u32(&sm.bar_acc_full));
+        tc_commit_w(smem_u32(&sm.bar_kv_free));
         ++nk;
         ug += nq;
       }
       if (!ok) sm.abort = 1;
-      tc_commit(smem_u32(&sm.bar_done));
-      if (!mbar_wait(smem_u32(&sm.bar_done), 0)) sm.abort = 1;
+      tc_commit_w(smem_u32(&sm.bar_done));
+      if (!mbar_wait_w(smem_u32(&sm.bar_done), 0)) sm.abort = 1;
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ compute groups

@@ -283,10 +283,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this role on warp-uniform values; one elected lane
+    // issues each tcgen05 instruction.
+    {
       constexpr uint32_t lay = operand_layout<DIM>();
       constexpr uint32_t sbo = 8 * DIM;  // 8 rows of one swizzle atom
       const uint32_t id_qk = idesc_f8(kTile, kTile, 0, 0);
+      // operand descriptors, built once: a K step, tile or ring stage moves only
+      // the start address (bits 0..13, address / 16), which never carries out
+      // of its field inside shared memory
+      const uint64_t dq0 = smem_desc(smem_u32(sm.q[0]), 0, sbo, lay);
+      const uint64_t dk0 = smem_desc(smem_u32(sm.k[0]), 0, sbo, lay);
+      const uint64_t dv0 = smem_desc(smem_u32(sm.v[0]), 0, sbo, lay);
+      constexpr uint32_t kStep = kTile * DIM / 16;  // one tile's bytes / 16
       // running counts of each barrier's completions (phase parity = count & 1)
       int nq_used = 0, kvc = 0, o_used[2] = {0, 0}, p_seen[2] = {0, 0};
       bool ok = true;
@@ -295,20 +304,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int st = jk % kStages;
         if (NVF4) {
           // packed E2M1 rows of 32 bytes, 32-byte swizzle, one K = 64 product
-          mma_nvf4(tmem + t * kTile, smem_desc(smem_u32(sm.q4[t]), 0, 256, kLayoutSW32),
+          mma_nvf4_w(tmem + t * kTile, smem_desc(smem_u32(sm.q4[t]), 0, 256, kLayoutSW32),
                    smem_desc(smem_u32(sm.k4[st]), 0, 256, kLayoutSW32), idesc_nvf4(kTile, kTile),
                    tmem + kSfQ4 + 4 * t, tmem + kSfK4 + 4 * (jk & 1), 0);
         } else {
-          const uint32_t qa = smem_u32(sm.q[t]), ka = smem_u32(sm.k[st]);
+          const uint64_t dq = dq0 + t * kStep, dk = dk0 + st * kStep;
 #pragma unroll
           for (int ks = 0; ks < DIM / 32; ++ks)
-            mma_f8(tmem + t * kTile, smem_desc(qa + 32 * ks, 0, sbo, lay),
-                   smem_desc(ka + 32 * ks, 0, sbo, lay), id_qk, ks > 0);
+            mma_f8_w(tmem + t * kTile, dq + 2 * ks, dk + 2 * ks, id_qk, ks > 0);
         }
-        tc_commit(smem_u32(&sm.bar_s_full[t]));
+        tc_commit_w(smem_u32(&sm.bar_s_full[t]));
       };
       for (int n = 0; ok; ++n) {
-        const int idx = ring_get(sm.ring, n, true);
+        // every lane takes lane 0's copy; one arrive frees the slot
+        const int idx = __shfl_sync(0xffffffffu, ring_get(sm.ring, n, false), 0);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm.ring.empty[n % 4]));
         if (idx < 0) {
           ok = false;
           break;
@@ -316,11 +327,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (idx >= total) break;
         FwdItem it;
         if (!decode_fwd_item(prm, n_items, idx, it)) continue;
-        ok = mbar_wait(smem_u32(&sm.bar_q), nq_used & 1) &&
-             mbar_wait(smem_u32(&sm.bar_kv_full[kvc % kStages]), (kvc / kStages) & 1);
-        if (NVF4) ok = ok && mbar_wait(smem_u32(&sm.bar_sf), nq_used & 1);
+        ok = mbar_wait_w(smem_u32(&sm.bar_q), nq_used & 1) &&
+             mbar_wait_w(smem_u32(&sm.bar_kv_full[kvc % kStages]), (kvc / kStages) & 1);
+        if (NVF4) ok = ok && mbar_wait_w(smem_u32(&sm.bar_sf), nq_used & 1);
         ++nq_used;
-        if (!ok || sm.abort) {
+        if (!ok || __any_sync(0xffffffffu, sm.abort)) {
           ok = false;
           break;
         }
@@ -333,7 +344,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           for (int t = 0; t < 2 && ok; ++t) {
             const int nt = t == 0 ? it.n0 : it.n1;
             if (j >= nt) continue;
-            if (!mbar_wait(smem_u32(&sm.bar_p_full[t]), p_seen[t] & 1) || sm.abort) {
+            if (!mbar_wait_w(smem_u32(&sm.bar_p_full[t]), p_seen[t] & 1) ||
+                __any_sync(0xffffffffu, sm.abort)) {
               ok = false;
               break;
             }
@@ -341,24 +353,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             // the first P^V of an item overwrites O_t: the previous item's
             // epilogue must have read it
             if (j == 0 && o_used[t] > 0 &&
-                !mbar_wait(smem_u32(&sm.bar_o_empty[t]), (o_used[t] - 1) & 1)) {
+                !mbar_wait_w(smem_u32(&sm.bar_o_empty[t]), (o_used[t] - 1) & 1)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t va = smem_u32(sm.v[st]);
+            const uint64_t dv = dv0 + st * kStep;
             // S_t columns 0..7 hold the scale factors, 8..39 the E4M3 P^_t (A
             // from tensor memory: 4 keys per column, 8 columns per 32-key step)
             const uint32_t sf = tmem + t * kTile;
 #pragma unroll
             for (int kb = 0; kb < 4; ++kb)
-              mma_mxf8_ts(tmem + 256 + t * DIM, sf + kColP + 8 * kb,
-                          smem_desc(va + kb * 32 * DIM, 0, sbo, lay),
+              mma_mxf8_ts_w(tmem + 256 + t * DIM, sf + kColP + 8 * kb, dv + kb * (32 * DIM / 16),
                           idesc_mxf8(kTile, DIM, 0, 1, kb, kb), sf, sf + 4, (j > 0 || kb > 0));
             if (j + 1 < nt) {
               if (kv_ready <= jk + 1) {
-                if (!mbar_wait(smem_u32(&sm.bar_kv_full[(jk + 1) % kStages]),
-                               ((jk + 1) / kStages) & 1)) {
+                if (!mbar_wait_w(smem_u32(&sm.bar_kv_full[(jk + 1) % kStages]),
+                                 ((jk + 1) / kStages) & 1)) {
                   ok = false;
                   break;
                 }
@@ -367,20 +378,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               }
               issue_qk(t, jk + 1);
             } else {
-              tc_commit(smem_u32(&sm.bar_o_full[t]));
+              tc_commit_w(smem_u32(&sm.bar_o_full[t]));
               ++o_used[t];
             }
           }
-          if (ok) tc_commit(smem_u32(&sm.bar_kv_empty[st]));
+          if (ok) tc_commit_w(smem_u32(&sm.bar_kv_empty[st]));
         }
         kvc += it.nkv;
         // this item's Q tiles may be replaced once its products are done
-        if (ok) tc_commit(smem_u32(&sm.bar_q_empty));
+        if (ok) tc_commit_w(smem_u32(&sm.bar_q_empty));
       }
       if (!ok) sm.abort = 1;
       // Drain: all MMAs of this thread complete before tensor memory is freed.
-      tc_commit(smem_u32(&sm.bar_done));
-      if (!mbar_wait(smem_u32(&sm.bar_done), 0)) sm.abort = 1;
+      tc_commit_w(smem_u32(&sm.bar_done));
+      if (!mbar_wait_w(smem_u32(&sm.bar_done), 0)) sm.abort = 1;
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
