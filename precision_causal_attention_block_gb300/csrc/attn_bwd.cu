@@ -198,14 +198,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this role on warp-uniform values; one elected lane
+    // issues each tcgen05 instruction.
+    {
       const uint32_t id_s = idesc_f8(kTile, kTile, 0, 0);
-      const uint32_t ka = smem_u32(sm.k), va = smem_u32(sm.v);
-      const uint32_t pba = smem_u32(sm.pb), dsa = smem_u32(sm.ds);
+      // operand descriptors, built once: a K step or a ring stage moves only
+      // the start address (bits 0..13, address / 16), which never carries out
+      // of its field inside shared memory
+      const uint64_t dk = smem_desc(smem_u32(sm.k), 0, sbo, lay);
+      const uint64_t dv = smem_desc(smem_u32(sm.v), 0, sbo, lay);
+      const uint64_t dq0 = smem_desc(smem_u32(sm.q[0]), 0, sbo, lay);
+      const uint64_t ddo0 = smem_desc(smem_u32(sm.dout[0]), 0, sbo, lay);
+      const uint64_t dpb = smem_desc(smem_u32(sm.pb), 0, 1024, kLayoutSW128);
+      const uint64_t dds = smem_desc(smem_u32(sm.ds), 0, 1024, kLayoutSW128);
+      constexpr uint32_t kStep = kTileBytes / 16;  // one ring stage
       int nk = 0, uc = 0;  // items and query tiles consumed so far
       bool ok = true;
       for (int n = 0; ok; ++n) {
-        const int idx = ring_get(sm.ring, n, true);
+        // every lane takes lane 0's copy; one arrive frees the slot
+        const int idx = __shfl_sync(0xffffffffu, ring_get(sm.ring, n, false), 0);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sm.ring.empty[n % 4]));
         if (idx < 0) {
           ok = false;
           break;
@@ -213,77 +226,74 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (idx >= total) break;
         BwdItem it;
         if (!decode_bwd_item(prm, n_items, idx, it)) continue;
-        ok = mbar_wait(smem_u32(&sm.bar_kv), nk & 1);
-        if (NVF4) ok = ok && mbar_wait(smem_u32(&sm.bar_sf), nk & 1);
+        ok = mbar_wait_w(smem_u32(&sm.bar_kv), nk & 1);
+        if (NVF4) ok = ok && mbar_wait_w(smem_u32(&sm.bar_sf), nk & 1);
         ++nk;
         // S^T_u and dP^T_u (tile u's Q / dO have landed)
         auto issue_sdp = [&](int uq) -> bool {
           const int st = uq % kBStages;
-          if (!mbar_wait(smem_u32(&sm.bar_qd_full[st]), (uq / kBStages) & 1) || sm.abort)
+          if (!mbar_wait_w(smem_u32(&sm.bar_qd_full[st]), (uq / kBStages) & 1) ||
+              __any_sync(0xffffffffu, sm.abort))
             return false;
           tc_fence_after();
-          const uint32_t qa = smem_u32(sm.q[st]), da = smem_u32(sm.dout[st]);
+          const uint64_t dq = dq0 + st * kStep, ddo = ddo0 + st * kStep;
           if (NVF4) {
             // S^T from the NVFP4 copies: packed E2M1 rows of 32 bytes, one K = 64 product
-            mma_nvf4(tmem + kColSP, smem_desc(smem_u32(sm.k4), 0, 256, kLayoutSW32),
+            mma_nvf4_w(tmem + kColSP, smem_desc(smem_u32(sm.k4), 0, 256, kLayoutSW32),
                      smem_desc(smem_u32(sm.q4[st]), 0, 256, kLayoutSW32),
                      idesc_nvf4(kTile, kTile), tmem + kSfK4, tmem + kSfQ4 + 4 * (uq & 1), 0);
           } else {
 #pragma unroll
             for (int ks = 0; ks < DIM / 32; ++ks)
-              mma_f8(tmem + kColSP, smem_desc(ka + 32 * ks, 0, sbo, lay),
-                     smem_desc(qa + 32 * ks, 0, sbo, lay), id_s, ks > 0);
+              mma_f8_w(tmem + kColSP, dk + 2 * ks, dq + 2 * ks, id_s, ks > 0);
           }
 #pragma unroll
           for (int ks = 0; ks < DIM / 32; ++ks)
-            mma_f8(tmem + kColDP, smem_desc(va + 32 * ks, 0, sbo, lay),
-                   smem_desc(da + 32 * ks, 0, sbo, lay), id_s, ks > 0);
-          tc_commit(smem_u32(&sm.bar_s_full));
+            mma_f8_w(tmem + kColDP, dv + 2 * ks, ddo + 2 * ks, id_s, ks > 0);
+          tc_commit_w(smem_u32(&sm.bar_s_full));
           return true;
         };
         if (it.nq > 0) ok = ok && issue_sdp(uc);
         for (int u = 0; ok && u < it.nq; ++u, ++uc) {
           const int st = uc % kBStages;
-          const uint32_t qa = smem_u32(sm.q[st]), da = smem_u32(sm.dout[st]);
+          const uint64_t dq = dq0 + st * kStep, ddo = ddo0 + st * kStep;
           // dV / dK restart from zero on an item's first tile: the previous
           // item's epilogue must have read them (its S^T / dP^T products could
           // already run meanwhile)
-          if (!mbar_wait(smem_u32(&sm.bar_ds_full), uc & 1) ||
-              (u == 0 && nk > 1 && !mbar_wait(smem_u32(&sm.bar_acc_empty), (nk - 2) & 1)) ||
-              sm.abort) {
+          if (!mbar_wait_w(smem_u32(&sm.bar_ds_full), uc & 1) ||
+              (u == 0 && nk > 1 && !mbar_wait_w(smem_u32(&sm.bar_acc_empty), (nk - 2) & 1)) ||
+              __any_sync(0xffffffffu, sm.abort)) {
             ok = false;
             break;
           }
           tc_fence_after();
           // dQ_u = dS K into its own columns, once the groups have read dQ_{u-1}:
           // A = the same dS bytes read MN-major (M = queries), B = K MN-major
-          if (uc > 0 && (!mbar_wait(smem_u32(&sm.bar_dq_read), (uc - 1) & 1) || sm.abort)) {
+          if (uc > 0 && (!mbar_wait_w(smem_u32(&sm.bar_dq_read), (uc - 1) & 1) ||
+                         __any_sync(0xffffffffu, sm.abort))) {
             ok = false;
             break;
           }
           tc_fence_after();
 #pragma unroll
           for (int kb = 0; kb < 4; ++kb)
-            mma_mxf8(tmem + kColDQ, smem_desc(dsa + kb * 32 * kTile, 0, 1024, kLayoutSW128),
-                     smem_desc(ka + kb * 32 * DIM, 0, sbo, lay),
+            mma_mxf8_w(tmem + kColDQ, dds + kb * (32 * kTile / 16), dk + kb * (32 * DIM / 16),
                      idesc_mxf8(kTile, DIM, 1, 1, kb, kb), tmem + kSfDqA, tmem + kSfDqB, kb > 0);
           // dQ first: the groups read it out while dV / dK run
-          tc_commit(smem_u32(&sm.bar_dq_full));
+          tc_commit_w(smem_u32(&sm.bar_dq_full));
           // dV += P^b^T dO : A [key][query] K-major, B = dO tile read MN-major
 #pragma unroll
           for (int kb = 0; kb < 4; ++kb)
-            mma_mxf8(tmem + kColDV, smem_desc(pba + 32 * kb, 0, 1024, kLayoutSW128),
-                     smem_desc(da + kb * 32 * DIM, 0, sbo, lay),
+            mma_mxf8_w(tmem + kColDV, dpb + 2 * kb, ddo + kb * (32 * DIM / 16),
                      idesc_mxf8(kTile, DIM, 0, 1, kb, kb), tmem + kSfDvA, tmem + kSfDvB,
                      (u > 0 || kb > 0));
           // dK += dS^T Q : A [key][query] K-major, B = Q tile read MN-major
 #pragma unroll
           for (int kb = 0; kb < 4; ++kb)
-            mma_mxf8(tmem + kColDV + DIM, smem_desc(dsa + 32 * kb, 0, 1024, kLayoutSW128),
-                     smem_desc(qa + kb * 32 * DIM, 0, sbo, lay),
+            mma_mxf8_w(tmem + kColDV + DIM, dds + 2 * kb, dq + kb * (32 * DIM / 16),
                      idesc_mxf8(kTile, DIM, 0, 1, kb, kb), tmem + kSfDkA, tmem + kSfDkB,
                      (u > 0 || kb > 0));
-          tc_commit(smem_u32(&sm.bar_qd_empty[st]));
+          tc_commit_w(smem_u32(&sm.bar_qd_empty[st]));
           // the next tile's S^T / dP^T right behind
           if (u + 1 < it.nq && !issue_sdp(uc + 1)) {
             ok = false;
@@ -291,11 +301,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
         }
         // this item's K / V may be replaced once its products are done
-        if (ok) tc_commit(smem_u32(&sm.bar_kv_free));
+        if (ok) tc_commit_w(smem_u32(&sm.bar_kv_free));
       }
       if (!ok) sm.abort = 1;
-      tc_commit(smem_u32(&sm.bar_done));
-      if (!mbar_wait(smem_u32(&sm.bar_done), 0)) sm.abort = 1;
+      tc_commit_w(smem_u32(&sm.bar_done));
+      if (!mbar_wait_w(smem_u32(&sm.bar_done), 0)) sm.abort = 1;
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ compute groups
