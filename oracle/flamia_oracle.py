@@ -28,6 +28,10 @@ What it follows (citations name the page and its section):
 * same page, sec. 3.4 "Work scheduling": a work item is 256 consecutive
   queries of one document, its cost the number of key blocks it visits,
   sorted by descending cost.
+* same page, sec. 3.4 "Hadamard rotation" and "Quantization fusion": the
+  head-dimension channels of Q and K are mixed by a normalised orthogonal
+  transform inside the quantiser (dot products preserved, token positions
+  not mixed), on by default at head dim 128.
 * same page, sec. 2 "A small example": the floor exponent rule
   e = floor(log2 amax) - emax with clipping at 448, used here only as the
   negative control of the leakage probe.
@@ -46,6 +50,13 @@ Readings where the pages are silent (each listed in the design doc):
   dQ / dK products;
 * the NVFP4 scale is the smallest E4M3 value >= amax / 6, no tensor-wide
   scale;
+* the rotation is the unnormalised Sylvester-Hadamard matrix H_d (entries
+  +-1, H_d H_d = d I), applied to each (token, head) row of Q and K in float32
+  by butterflies of stride 1, 2, ..., d/2 in that order (the GPU quantiser
+  takes the same steps, so the codes match bit for bit); the 1/d that
+  normalises it is folded into the softmax scale (exact for d a power of
+  two), and the backward returns dQ = dQ_r H_d, dK = dK_r H_d for the
+  gradients dQ_r, dK_r of the rotated operands;
 * work items: forward q0 = s + 256k, q1 = min(q0 + 256, e), cost =
   ceil((q1 - s) / 128); backward k0 = s + 128k, k1 = min(k0 + 128, e),
   cost = ceil((e - k0) / 128); stable sort by descending cost.
@@ -163,6 +174,33 @@ def bf16_round(x) -> np.ndarray:
     x = np.asarray(x, dtype=np.float64)
     f, e = np.frexp(x)
     return np.ldexp(np.rint(f * 256.0) / 256.0, e)
+
+
+def hadamard_fp32(x) -> np.ndarray:
+    """x H_d along the last axis (H_d the unnormalised Sylvester-Hadamard
+    matrix, d a power of two), computed in float32 by butterflies of stride
+    1, 2, ..., d/2 in that order: within each pair (i, i + s) with
+    i mod 2s < s the new values are (x_i + x_{i+s}, x_i - x_{i+s}).
+    Returns float64 (exact copies of the float32 results)."""
+    y = np.asarray(x, dtype=np.float32)
+    d = y.shape[-1]
+    assert d > 0 and d & (d - 1) == 0, d
+    lead = y.shape[:-1]
+    s = 1
+    while s < d:
+        z = y.reshape(lead + (d // (2 * s), 2, s))
+        a, b = z[..., 0, :], z[..., 1, :]
+        y = np.stack([a + b, a - b], axis=-2).reshape(lead + (d,))
+        s *= 2
+    return y.astype(np.float64)
+
+
+def sylvester(d: int) -> np.ndarray:
+    """H_1 = [1], H_2n = [[H_n, H_n], [H_n, -H_n]] (float64)."""
+    h = np.ones((1, 1))
+    while h.shape[0] < d:
+        h = np.block([[h, h], [h, -h]])
+    return h
 
 
 # ----------------------------------------------------------------------------
@@ -438,14 +476,26 @@ def exact_dochead(q, k, v, do, cu, b, h) -> DocHead:
 
 def attention(q, k, v, do, cu_seqlens, sm_scale: float, quant: bool = True,
               qk_format: str = "mxfp8", rule: str = "up", group: str = "block",
-              heads=None, docs=None, backward: bool = True):
+              heads=None, docs=None, backward: bool = True, hadamard: bool = False):
     """Full forward (+ backward) over packed [T, H, d] float64 inputs.
 
     Returns a dict with O [T, H, d] (float64), O_bf16, lse [H, T] (natural log,
     +inf where not computed) and, with backward, dQ, dK, dV [T, H, d] and D
-    [H, T].  ``heads`` / ``docs`` restrict the work (other entries stay 0)."""
+    [H, T].  ``heads`` / ``docs`` restrict the work (other entries stay 0).
+    ``hadamard``: Q and K are rotated by H_d before quantisation (float32
+    butterflies; exactly, in float64, when quant is False), the scores use
+    sm_scale / d, and dQ, dK are rotated back by H_d."""
     q = np.asarray(q, dtype=np.float64)
     T, H, d = q.shape
+    if hadamard:
+        rot = hadamard_fp32 if quant else (lambda x: np.asarray(x, dtype=np.float64) @ sylvester(d))
+        r = attention(rot(q), rot(k), v, do, cu_seqlens, sm_scale / d, quant, qk_format, rule,
+                      group, heads, docs, backward, hadamard=False)
+        if backward:
+            hd = sylvester(d)
+            r["dQ"] = r["dQ"] @ hd
+            r["dK"] = r["dK"] @ hd
+        return r
     cu = [int(c) for c in cu_seqlens]
     heads = range(H) if heads is None else heads
     docs = range(len(cu) - 1) if docs is None else docs
