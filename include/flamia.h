@@ -56,10 +56,17 @@ typedef enum {
 /* Quantiser output formats. */
 #define FLAMIA_FORMAT_MXFP8       0 /* E4M3 codes + per-token E8M0 scales          */
 #define FLAMIA_FORMAT_MXFP8_NVFP4 1 /* the above plus NVFP4 codes and scales       */
+#define FLAMIA_FORMAT_HADAMARD 0x10 /* OR-ed into FLAMIA_FORMAT_MXFP8: rotate each
+                                       (token, head) row by H_d before the block
+                                       statistics (for Q and K; see below)       */
 
 /* Attention flags. */
 #define FLAMIA_FLAG_NVFP4_QK 0x1    /* score product QK^T (fwd and bwd recompute)
                                        from the NVFP4 copy of Q and K (d == 64)   */
+#define FLAMIA_FLAG_HADAMARD 0x2    /* q and k were quantised with
+                                       FLAMIA_FORMAT_HADAMARD: scores use
+                                       softmax_scale / d; the backward returns
+                                       dQ and dK rotated back by H_d            */
 
 /*
  * One quantised operand, all device pointers owned by the caller.
@@ -92,6 +99,13 @@ typedef struct {
  * With format FLAMIA_FORMAT_MXFP8_NVFP4 the same pass also writes the NVFP4
  * copy (sec. 3.1 mixed path): per token and 16-element group, scale = the
  * smallest E4M3 value >= amax / 6, codes = RNE_E2M1(x / scale).
+ * With FLAMIA_FORMAT_HADAMARD (sec. 3.4 "Hadamard rotation": the head-dim
+ * channels of Q and K are mixed by an orthogonal transform inside the
+ * quantiser) each row x is first replaced by x H_d, H_d the unnormalised
+ * Sylvester-Hadamard matrix (entries +-1, H_d H_d = d I), computed in float32
+ * by butterflies of stride 1, 2, .., d/2 in that order; the statistics and
+ * codes are those of the rotated rows.  Not combinable with the NVFP4 copy
+ * (FLAMIA_ERR_UNSUPPORTED) nor with o_bf16 / D.
  *
  *  x_bf16     [T, H, d] BF16 input (finite values).
  *  o_bf16, D  optional (both NULL or both set): the forward output O [T, H, d]
@@ -173,6 +187,9 @@ flamia_status flamia_build_worklist_static(const int32_t* cu_seqlens, int ndocs,
  * running integer row maximum m_i = ceil(max_j s_ij), P~ = exp2(s - m),
  * l = sum P~, operand P^ = RNE_E4M3(2^8 P~), O = 2^-8 sum_j P^ V^_j / l,
  * LSE = (m + log2 l) ln 2.
+ * FLAMIA_FLAG_HADAMARD: q and k hold Q H_d and K H_d, so the call uses
+ * softmax_scale / d for the scores (the same S exactly, d a power of two).
+ * Not combinable with FLAMIA_FLAG_NVFP4_QK.
  *
  *  q, k, v      host pointers to quantised operands (E4M3 + scales; with
  *               FLAMIA_FLAG_NVFP4_QK also the NVFP4 copies of q and k).
@@ -207,6 +224,10 @@ size_t flamia_bwd_workspace_bytes(int T, int H, int d);
  * from the unquantised P; dS exponent = round-up rule on each document-aligned
  * 32x32 block maximum; dQ and dK scaled by softmax_scale after the products;
  * dQ partial sums are added in float32 (no prescale), then converted to BF16.
+ * FLAMIA_FLAG_HADAMARD: as for the forward, with softmax_scale / d, and the
+ * gradients of the rotated operands are rotated back before the BF16
+ * conversion: dQ = dQ_r H_d, dK = dK_r H_d (float32 butterflies as in the
+ * quantiser).
  *
  *  dout         host pointer to the quantised dO (from the quantiser run with
  *               o_bf16 = the forward output, which also produced D).

@@ -537,7 +537,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           bulk_commit_group();
         }
       }
-      if (ok) {
+      if (ok && prm.hadamard) {
+        // Q and K were rotated: group 0 writes whole rows of dK = dK_r H_d
+        // (the butterflies need all DIM columns of a row), group 1 of dV
+        __nv_bfloat16* out = (g == 0 ? prm.dk : prm.dv) + (static_cast<size_t>(kj) * H + h) * DIM;
+        const float mul = g == 0 ? prm.sm_scale : (1.f / 256.f);
+        uint32_t u[DIM / 32][32];
+#pragma unroll
+        for (int c = 0; c < DIM / 32; ++c)
+          tmem_ld32(tmem + lane_off + kColDV + (g == 0 ? DIM : 0) + 32 * c, u[c]);
+        tmem_ld_wait();
+        float x[DIM];
+#pragma unroll
+        for (int i = 0; i < DIM; ++i) x[i] = __uint_as_float(u[i / 32][i % 32]) * mul;
+        if (g == 0) fwht_row<DIM, 1>(x, 0);
+        if (key_valid) {
+#pragma unroll
+          for (int i = 0; i < DIM; i += 8) {
+            uint32_t w[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(x[i + 2 * t], x[i + 2 * t + 1]);
+              w[t] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+            *reinterpret_cast<uint4*>(out + i) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+        // dV / dK columns may now be restarted by the next item
+        tc_fence_before();
+        mbar_arrive(smem_u32(&sm.bar_acc_empty));
+      } else if (ok) {
         // dV = 2^-8 acc, dK = scale * acc, written to the packed buffers; the
         // groups split the head dimension (every product of the item completed
         // before its last dQ was read)
@@ -590,6 +619,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // float32 dQ accumulator (sums of dS K) -> BF16 dQ = softmax_scale * acc.
+// dQ = (sm_scale acc) H_d, one warp per (token, head) row: lane l holds the
+// DIM/32 consecutive elements [DIM/32 l, DIM/32 (l + 1)).
+template <int DIM>
+__global__ void dq_convert_rotate_kernel(const float* __restrict__ acc,
+                                         __nv_bfloat16* __restrict__ out, size_t rows,
+                                         float sm_scale) {
+  constexpr int N = DIM / 32;
+  const int lane = threadIdx.x & 31;
+  const size_t warps = static_cast<size_t>(gridDim.x) * (blockDim.x >> 5);
+  for (size_t r = blockIdx.x * static_cast<size_t>(blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
+       r += warps) {
+    float v[N];
+    const float* src = acc + r * DIM + N * lane;
+#pragma unroll
+    for (int i = 0; i < N; ++i) v[i] = src[i] * sm_scale;
+    fwht_row<N, 32>(v, lane);
+    __nv_bfloat16* dst = out + r * DIM + N * lane;
+#pragma unroll
+    for (int i = 0; i < N; i += 2)
+      *reinterpret_cast<__nv_bfloat162*>(dst + i) = __floats2bfloat162_rn(v[i], v[i + 1]);
+  }
+}
+
 __global__ void dq_convert_kernel(const float4* __restrict__ acc, uint2* __restrict__ out,
                                   size_t n4, float sm_scale) {
   for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n4;
@@ -605,7 +657,7 @@ template <int DIM, bool NVF4>
 flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
                          const flamia_qtensor* v, const flamia_qtensor* dout, const float* D,
                          const float* lse, const int32_t* cu, int ndocs, int T, int H,
-                         float softmax_scale, void* wl, void* dq, void* dk, void* dv,
+                         float softmax_scale, bool had, void* wl, void* dq, void* dk, void* dv,
                          float* acc, int* status, cudaStream_t stream) {
   CUtensorMap mq, mk, mv, mdo, mdq, mq4, mk4;
   const CUtensorMapSwizzle swz = swizzle_for_row_bytes(DIM);
@@ -644,6 +696,7 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
   prm.cap = L.cap_bwd;
   prm.scale_log2 = softmax_scale * 1.4426950408889634f;
   prm.sm_scale = softmax_scale;
+  prm.hadamard = had ? 1 : 0;
   prm.status = status;
   const size_t n = static_cast<size_t>(T) * H * DIM;
   if (cudaMemsetAsync(acc, 0, n * sizeof(float), stream) != cudaSuccess) return FLAMIA_ERR_CUDA;
@@ -663,9 +716,16 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
         mq, mk, mv, mdo, mdq, mq4, mk4, prm);
     if (cudaGetLastError() != cudaSuccess) return FLAMIA_ERR_CUDA;
   }
-  if (launch_bwd_short(q, k, v, dout, D, lse, cu, ndocs, T, H, DIM, softmax_scale, NVF4, acc, dk,
-                       dv, stream) != cudaSuccess)
+  if (launch_bwd_short(q, k, v, dout, D, lse, cu, ndocs, T, H, DIM, softmax_scale, NVF4, had, acc,
+                       dk, dv, stream) != cudaSuccess)
     return FLAMIA_ERR_CUDA;
+  if (had) {
+    const size_t rows = static_cast<size_t>(T) * H;
+    const int blocks = static_cast<int>(std::min<size_t>((rows + 7) / 8, 152 * 16));
+    dq_convert_rotate_kernel<DIM><<<blocks, 256, 0, stream>>>(
+        acc, static_cast<__nv_bfloat16*>(dq), rows, softmax_scale);
+    return cudaGetLastError() == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
+  }
   const size_t n4 = n / 4;
   const int blocks = static_cast<int>(std::min<size_t>((n4 + 255) / 256, 152 * 16));
   dq_convert_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(acc),
@@ -691,9 +751,10 @@ extern "C" flamia_status flamia_attn_bwd(const flamia_qtensor* q, const flamia_q
                                          void* dq_bf16, void* dk_bf16, void* dv_bf16, void* ws,
                                          size_t ws_bytes, int* dev_status, void* stream) {
   if (!supported_dim(d)) return FLAMIA_ERR_UNSUPPORTED;
-  if ((flags & ~FLAMIA_FLAG_NVFP4_QK) != 0) return FLAMIA_ERR_UNSUPPORTED;
+  if ((flags & ~(FLAMIA_FLAG_NVFP4_QK | FLAMIA_FLAG_HADAMARD)) != 0) return FLAMIA_ERR_UNSUPPORTED;
   const bool nvf4 = (flags & FLAMIA_FLAG_NVFP4_QK) != 0;
-  if (nvf4 && d != 64) return FLAMIA_ERR_UNSUPPORTED;
+  const bool had = (flags & FLAMIA_FLAG_HADAMARD) != 0;
+  if ((nvf4 && d != 64) || (nvf4 && had)) return FLAMIA_ERR_UNSUPPORTED;
   if (!valid_sizes(T, H, d, ndocs) || !q || !k || !v || !dout || !D || !lse || !cu_seqlens ||
       !wl || !dq_bf16 || !dk_bf16 || !dv_bf16 || !ws || !(softmax_scale > 0.f))
     return FLAMIA_ERR_INVALID_ARG;
@@ -711,13 +772,13 @@ extern "C" flamia_status flamia_attn_bwd(const flamia_qtensor* q, const flamia_q
     return FLAMIA_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* acc = static_cast<float*>(ws);
+  // rotated Q, K: the same scores with softmax_scale / d (exact: d = 2^k)
+  const float sc = had ? softmax_scale / static_cast<float>(d) : softmax_scale;
   if (nvf4)
-    return launch_bwd<64, true>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, softmax_scale,
-                                wl, dq_bf16, dk_bf16, dv_bf16, acc, dev_status, s);
-  return d == 128 ? launch_bwd<128, false>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H,
-                                           softmax_scale, wl, dq_bf16, dk_bf16, dv_bf16, acc,
-                                           dev_status, s)
-                  : launch_bwd<64, false>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H,
-                                          softmax_scale, wl, dq_bf16, dk_bf16, dv_bf16, acc,
-                                          dev_status, s);
+    return launch_bwd<64, true>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, sc, false, wl,
+                                dq_bf16, dk_bf16, dv_bf16, acc, dev_status, s);
+  return d == 128 ? launch_bwd<128, false>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, sc,
+                                           had, wl, dq_bf16, dk_bf16, dv_bf16, acc, dev_status, s)
+                  : launch_bwd<64, false>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, sc,
+                                          had, wl, dq_bf16, dk_bf16, dv_bf16, acc, dev_status, s);
 }

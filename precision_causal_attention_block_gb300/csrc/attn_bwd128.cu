@@ -483,7 +483,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       // dV = 2^-8 acc, dK = scale * acc; the groups split the head dimension
       ok = ok && !sm.abort && mbar_wait(smem_u32(&sm.bar_acc_full), nk & 1);
       tc_fence_after();
-      if (ok) {
+      if (ok && prm.hadamard) {
+        // Q and K were rotated: group 0 writes whole rows of dK = dK_r H_d
+        // (the butterflies need all 128 columns of a row), group 1 of dV
+        __nv_bfloat16* out = (g == 0 ? prm.dk : prm.dv) + (static_cast<size_t>(kj) * H + h) * kD;
+        const float mul = g == 0 ? prm.sm_scale : (1.f / 256.f);
+        uint32_t u[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_off + (g == 0 ? kColDK : kColDV) + 32 * c, u[c]);
+        tmem_ld_wait();
+        float x[kD];
+#pragma unroll
+        for (int i = 0; i < kD; ++i) x[i] = __uint_as_float(u[i / 32][i % 32]) * mul;
+        if (g == 0) fwht_row<kD, 1>(x, 0);
+        if (key_valid) {
+#pragma unroll
+          for (int i = 0; i < kD; i += 8) {
+            uint32_t w[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(x[i + 2 * t], x[i + 2 * t + 1]);
+              w[t] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+            *reinterpret_cast<uint4*>(out + i) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&sm.bar_acc_empty));
+      } else if (ok) {
         __nv_bfloat16* dvrow = prm.dv + (static_cast<size_t>(kj) * H + h) * kD;
         __nv_bfloat16* dkrow = prm.dk + (static_cast<size_t>(kj) * H + h) * kD;
 #pragma unroll 1

@@ -670,9 +670,12 @@ extern "C" flamia_status flamia_attn_fwd(const flamia_qtensor* q, const flamia_q
                                          int flags, void* wl, void* o_bf16, float* lse,
                                          int* dev_status, void* stream) {
   if (!supported_dim(d)) return FLAMIA_ERR_UNSUPPORTED;
-  if ((flags & ~FLAMIA_FLAG_NVFP4_QK) != 0) return FLAMIA_ERR_UNSUPPORTED;
+  if ((flags & ~(FLAMIA_FLAG_NVFP4_QK | FLAMIA_FLAG_HADAMARD)) != 0) return FLAMIA_ERR_UNSUPPORTED;
   const bool nvf4 = (flags & FLAMIA_FLAG_NVFP4_QK) != 0;
-  if (nvf4 && d != 64) return FLAMIA_ERR_UNSUPPORTED;
+  if ((nvf4 && d != 64) || (nvf4 && (flags & FLAMIA_FLAG_HADAMARD))) return FLAMIA_ERR_UNSUPPORTED;
+  // rotated Q, K (FLAMIA_FLAG_HADAMARD): the same scores with softmax_scale / d
+  // (exact: d = 2^k)
+  if (flags & FLAMIA_FLAG_HADAMARD) softmax_scale /= static_cast<float>(d);
   if (!valid_sizes(T, H, d, ndocs) || q == nullptr || k == nullptr || v == nullptr ||
       cu_seqlens == nullptr || wl == nullptr || o_bf16 == nullptr || lse == nullptr ||
       !(softmax_scale > 0.f))

@@ -35,6 +35,7 @@ struct ShortParams {
   const float *lse_in, *D;
   float* dq_acc;  // float32 [T, H, d]: dS K sums (softmax_scale comes in the conversion)
   __nv_bfloat16 *dk, *dv;
+  int hadamard;  // dK rotated back by H_d (Q and K were quantised rotated)
 };
 
 // d/32 E4M3 codes of one row (this lane's slice) decoded to floats.
@@ -243,6 +244,7 @@ __global__ void __launch_bounds__(32 * kShortWarps)
       ak[c] *= mk;
       av[c] *= mv;
     }
+    if (prm.hadamard) fwht_row<DIM / 32, 32>(ak, lane);  // dK = dK_r H_d (the whole warp)
     store_bf16<DIM>(prm.dk, static_cast<size_t>(s + j) * H + h, lane, ak);
     store_bf16<DIM>(prm.dv, static_cast<size_t>(s + j) * H + h, lane, av);
   }
@@ -297,9 +299,10 @@ cudaError_t launch_fwd_short(const flamia_qtensor* q, const flamia_qtensor* k,
 cudaError_t launch_bwd_short(const flamia_qtensor* q, const flamia_qtensor* k,
                              const flamia_qtensor* v, const flamia_qtensor* dout, const float* D,
                              const float* lse, const int32_t* cu, int ndocs, int T, int H, int d,
-                             float softmax_scale, bool nvfp4_qk, float* dq_acc, void* dk, void* dv,
-                             cudaStream_t stream) {
+                             float softmax_scale, bool nvfp4_qk, bool hadamard, float* dq_acc,
+                             void* dk, void* dv, cudaStream_t stream) {
   ShortParams p = make_params(q, k, v, cu, ndocs, T, H, softmax_scale);
+  p.hadamard = hadamard ? 1 : 0;
   p.doc_ = dout->codes;
   p.dos = dout->scales;
   p.lse_in = lse;

@@ -28,6 +28,7 @@ struct BwdParams {
   int T, H, ndocs, cap;
   float scale_log2;  // softmax_scale * log2(e)
   float sm_scale;
+  int hadamard;  // dK (and, in the conversion, dQ) rotated back by H_d
   int* status;
 };
 

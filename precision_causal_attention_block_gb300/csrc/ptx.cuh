@@ -558,6 +558,36 @@ __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
 
 // Round-up block exponent: smallest e with amax <= 448 * 2^e, clamped to
 // [-127, 127]; amax == 0 (or below the normal range) gives -127.
+// Unnormalised Sylvester-Hadamard butterflies (x H_d) on a row of N * P
+// floats spread over P consecutive lanes: lane `part` (0 .. P-1 inside its
+// aligned group of P lanes) holds elements [N part, N part + N).  Strides 1 ..
+// N/2 run inside the lane, then N, 2N, .. N P / 2 across lanes (partner part ^
+// stride / N), in increasing order; in each pair (i, i + s) the new values are
+// (x_i + x_{i+s}, x_i - x_{i+s}) in float32.  All lanes of the warp must call
+// it together when P > 1.
+template <int N, int P>
+__device__ __forceinline__ void fwht_row(float (&v)[N], int part) {
+#pragma unroll
+  for (int s = 1; s < N; s <<= 1) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      if ((i & s) == 0) {
+        const float a = v[i], b = v[i + s];
+        v[i] = a + b;
+        v[i + s] = a - b;
+      }
+    }
+  }
+#pragma unroll
+  for (int dist = 1; dist < P; dist <<= 1) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      const float o = __shfl_xor_sync(0xffffffffu, v[i], dist);
+      v[i] = (part & dist) ? o - v[i] : v[i] + o;
+    }
+  }
+}
+
 __device__ __forceinline__ int roundup_exponent(float amax) {
   const uint32_t b = __float_as_uint(amax);
   const int E = static_cast<int>((b >> 23) & 0xFF) - 127;

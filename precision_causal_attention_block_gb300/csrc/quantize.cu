@@ -5,7 +5,10 @@
 // segment of one head.  The rows of those blocks (at most 128 + 31) are read
 // once from HBM by one TMA box into shared memory, reduced to per-block
 // maxima, and written back as E4M3 codes plus the per-token E8M0 scale table,
-// optionally with the NVFP4 copy and with D = dO . O fused in.
+// optionally with the NVFP4 copy and with D = dO . O fused in, or with the
+// rows rotated by the Sylvester-Hadamard matrix first (review page, sec. 3.4
+// "Hadamard rotation"; float32 butterflies across the lanes that hold a row,
+// redone where the rows are read, so nothing extra goes through memory).
 // HBM-bound: 2 bytes read + 1 byte written per element.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -37,7 +40,17 @@ __device__ __forceinline__ float pow2f(int e) {
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-template <int DIM>
+// The 8 BF16 elements of one lane's 16-byte chunk as floats.
+__device__ __forceinline__ void unpack8(const uint4& xv, float (&v)[8]) {
+  const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    v[2 * j] = bf16lo(w[j]);
+    v[2 * j + 1] = bf16hi(w[j]);
+  }
+}
+
+template <int DIM, bool HAD>
 __global__ void __launch_bounds__(kQThreads)
     quantize_kernel(const __grid_constant__ CUtensorMap map_x, int T, int H,
                     const int32_t* __restrict__ cu, int ndocs, uint8_t* __restrict__ codes,
@@ -107,11 +120,12 @@ __global__ void __launch_bounds__(kQThreads)
     const int rl = warp * 32 + i * RPI + lane / LPR;  // row inside the staged box
     const int tt = seg0 + rl;
     const bool valid = tt >= A && tt < Bend;
-    const uint4 xv = s_x[rl * LPR + chunk];
-    const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
+    float v[8];
+    unpack8(s_x[rl * LPR + chunk], v);
+    if (HAD) fwht_row<8, LPR>(v, chunk);  // the LPR lanes of a row, all lanes together
     float m = 0.f;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16lo(w[j])), fabsf(bf16hi(w[j]))));
+    for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(v[j]));
 #pragma unroll
     for (int off = LPR / 2; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
     if (chunk == 0) s_rmax[rl] = valid ? m : 0.f;
@@ -162,14 +176,9 @@ __global__ void __launch_bounds__(kQThreads)
     const bool valid = tt >= A && tt < Bend;
     const int e = valid ? s_exp[rl] : 0;
     const float inv = exp2i(-e);  // e in [-127, 120]: 2^-e is a normal float
-    const uint4 xv = s_x[rl * LPR + chunk];
-    const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
     float v[8];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      v[2 * j] = bf16lo(w[j]);
-      v[2 * j + 1] = bf16hi(w[j]);
-    }
+    unpack8(s_x[rl * LPR + chunk], v);
+    if (HAD) fwht_row<8, LPR>(v, chunk);
     uint32_t c[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) c[j] = cvt_e4m3x2(v[2 * j] * inv, v[2 * j + 1] * inv);
@@ -229,7 +238,11 @@ extern "C" flamia_status flamia_quantize_tokenblock(const void* x_bf16, int T, i
                                                     const flamia_qtensor* out, int* dev_status,
                                                     void* stream) {
   if (!supported_dim(d)) return FLAMIA_ERR_UNSUPPORTED;
+  const bool had = (format & FLAMIA_FORMAT_HADAMARD) != 0;
+  format &= ~FLAMIA_FORMAT_HADAMARD;
   if (format != FLAMIA_FORMAT_MXFP8 && format != FLAMIA_FORMAT_MXFP8_NVFP4)
+    return FLAMIA_ERR_UNSUPPORTED;
+  if (had && (format != FLAMIA_FORMAT_MXFP8 || o_bf16 != nullptr || D != nullptr))
     return FLAMIA_ERR_UNSUPPORTED;
   if (!valid_sizes(T, H, d, ndocs) || x_bf16 == nullptr || cu_seqlens == nullptr ||
       out == nullptr || out->codes == nullptr || out->scales == nullptr)
@@ -264,13 +277,9 @@ extern "C" flamia_status flamia_quantize_tokenblock(const void* x_bf16, int T, i
   }
   dim3 grid((T + kSeg - 1) / kSeg, H);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (d == 128)
-    quantize_kernel<128><<<grid, kQThreads, 0, s>>>(
-        map, T, H, cu_seqlens, ndocs, out->codes, out->scales, f4c, f4s,
-        static_cast<const uint4*>(o_bf16), D, status);
-  else
-    quantize_kernel<64><<<grid, kQThreads, 0, s>>>(
-        map, T, H, cu_seqlens, ndocs, out->codes, out->scales, f4c, f4s,
-        static_cast<const uint4*>(o_bf16), D, status);
+  auto kern = d == 128 ? (had ? quantize_kernel<128, true> : quantize_kernel<128, false>)
+                       : (had ? quantize_kernel<64, true> : quantize_kernel<64, false>);
+  kern<<<grid, kQThreads, 0, s>>>(map, T, H, cu_seqlens, ndocs, out->codes, out->scales, f4c, f4s,
+                                  static_cast<const uint4*>(o_bf16), D, status);
   return cudaGetLastError() == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
 }
