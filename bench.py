@@ -171,7 +171,8 @@ def run_ours(args, rank, world, local):
     x = W.make_inputs_bf16(w)
     xd = {n: t.to(dev) for n, t in x.items()}
     cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev)
-    call = fl.TrainingCall(w.T, w.H, w.d, cu, w.sm_scale, nvfp4_qk=args.nvfp4, device=dev)
+    call = fl.TrainingCall(w.T, w.H, w.d, cu, w.sm_scale, nvfp4_qk=args.nvfp4,
+                           hadamard=args.hadamard, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -277,6 +278,7 @@ def run_ours(args, rank, world, local):
         "data": "synthetic (seeded bf16 normals, 1% outlier channels x20)",
         "config": {"workload": w.name, "T": w.T, "H": w.H, "d": w.d, "docs": w.ndocs,
                    "qk_product": "nvfp4 (mixed path)" if args.nvfp4 else "mxfp8",
+                   "qk_rotation": "hadamard" if args.hadamard else "none",
                    "flops_per_step": flops, "l2": "flushed (256 MB write) before every step",
                    "parallelism": f"replicas x{world}"},
         "pct_of_fp8_peak": round(100.0 * value / world / pk["fp8_tflops"], 2),
@@ -286,7 +288,8 @@ def run_ours(args, rank, world, local):
                      "bound": "tensor", "achieved": round(achieved, 2),
                      "peak": pk["fp8_tflops"], "unit": "TFLOP/s",
                      "frac": round(achieved / pk["fp8_tflops"], 4),
-                     "peak_source": pk["source"], "traffic": profiled_traffic(w, args.nvfp4),
+                     "peak_source": pk["source"],
+                     "traffic": None if args.hadamard else profiled_traffic(w, args.nvfp4),
                      "traffic_unit": "bytes per launch of the attention kernel (ncu, DRAM read + write)"},
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -413,6 +416,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--nvfp4", action="store_true",
                     help="mixed path: QK^T from NVFP4 copies of Q and K (head dim 64)")
+    ap.add_argument("--hadamard", action="store_true",
+                    help="Q and K rotated by the Hadamard matrix in the quantiser")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
