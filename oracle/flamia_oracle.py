@@ -32,6 +32,8 @@ What it follows (citations name the page and its section):
   head-dimension channels of Q and K are mixed by a normalised orthogonal
   transform inside the quantiser (dot products preserved, token positions
   not mixed), on by default at head dim 128.
+* same page, sec. 4.8 "Batched and non-causal paths": the non-causal packed
+  call, where every query sees every key of its own document.
 * same page, sec. 2 "A small example": the floor exponent rule
   e = floor(log2 amax) - emax with clipping at 448, used here only as the
   negative control of the leakage probe.
@@ -365,10 +367,11 @@ class DocHead:
         # score operands when they differ from q/k (NVFP4 mixed path): exact values
         self.qs, self.ks = qs, ks
         self.L = q.shape[0]
+        self.causal = True  # False: every query sees every key of the document
 
 
 def _scores(dh: DocHead, rows: np.ndarray, cols: np.ndarray, sm_scale: float) -> np.ndarray:
-    """log2-domain scores s_ij = S_ij * log2(e), -inf where j > i."""
+    """log2-domain scores s_ij = S_ij * log2(e), -inf where j > i (causal)."""
     if dh.qs is not None:
         S = sm_scale * (dh.qs[rows] @ dh.ks[cols].T)
     else:
@@ -376,14 +379,18 @@ def _scores(dh: DocHead, rows: np.ndarray, cols: np.ndarray, sm_scale: float) ->
         S = sm_scale * dots * np.ldexp(1.0, dh.eq[rows])[:, None] \
             * np.ldexp(1.0, dh.ek[cols])[None, :]              # row factor x column factor
     s = S * LOG2E
-    s[cols[None, :] > rows[:, None]] = -np.inf
+    if dh.causal:
+        s[cols[None, :] > rows[:, None]] = -np.inf
     return s
 
 
 def fwd_rows(dh: DocHead, rows: np.ndarray, sm_scale: float, quant: bool = True):
     """Forward output rows: O [R, d], lse2 [R] (log2 units), m [R], l [R]."""
     rows = np.asarray(rows, dtype=np.int64)
-    cols = np.arange(int(rows.max()) + 1 if rows.size else 0)
+    if not dh.causal:
+        cols = np.arange(dh.L)
+    else:
+        cols = np.arange(int(rows.max()) + 1 if rows.size else 0)
     s = _scores(dh, rows, cols, sm_scale)
     m = np.ceil(s.max(axis=1))                                 # integer row maximum
     pt = np.exp2(s - m[:, None])                               # 0 where masked
@@ -476,7 +483,8 @@ def exact_dochead(q, k, v, do, cu, b, h) -> DocHead:
 
 def attention(q, k, v, do, cu_seqlens, sm_scale: float, quant: bool = True,
               qk_format: str = "mxfp8", rule: str = "up", group: str = "block",
-              heads=None, docs=None, backward: bool = True, hadamard: bool = False):
+              heads=None, docs=None, backward: bool = True, hadamard: bool = False,
+              causal: bool = True):
     """Full forward (+ backward) over packed [T, H, d] float64 inputs.
 
     Returns a dict with O [T, H, d] (float64), O_bf16, lse [H, T] (natural log,
@@ -484,13 +492,14 @@ def attention(q, k, v, do, cu_seqlens, sm_scale: float, quant: bool = True,
     [H, T].  ``heads`` / ``docs`` restrict the work (other entries stay 0).
     ``hadamard``: Q and K are rotated by H_d before quantisation (float32
     butterflies; exactly, in float64, when quant is False), the scores use
-    sm_scale / d, and dQ, dK are rotated back by H_d."""
+    sm_scale / d, and dQ, dK are rotated back by H_d.  ``causal=False``: every
+    query sees every key of its document."""
     q = np.asarray(q, dtype=np.float64)
     T, H, d = q.shape
     if hadamard:
         rot = hadamard_fp32 if quant else (lambda x: np.asarray(x, dtype=np.float64) @ sylvester(d))
         r = attention(rot(q), rot(k), v, do, cu_seqlens, sm_scale / d, quant, qk_format, rule,
-                      group, heads, docs, backward, hadamard=False)
+                      group, heads, docs, backward, hadamard=False, causal=causal)
         if backward:
             hd = sylvester(d)
             r["dQ"] = r["dQ"] @ hd
@@ -509,6 +518,7 @@ def attention(q, k, v, do, cu_seqlens, sm_scale: float, quant: bool = True,
             continue
         for h in heads:
             dh = qz.dochead(b, h) if quant else exact_dochead(q, k, v, do, cu, b, h)
+            dh.causal = causal
             rows = np.arange(e - s)
             o, lse2, _, _ = fwd_rows(dh, rows, sm_scale, quant)
             out["O"][s:e, h] = o
@@ -531,7 +541,8 @@ def attention(q, k, v, do, cu_seqlens, sm_scale: float, quant: bool = True,
     return out
 
 
-def sampled_rows(qz: Quantized, b: int, h: int, sm_scale: float, qblocks, kblocks):
+def sampled_rows(qz: Quantized, b: int, h: int, sm_scale: float, qblocks, kblocks,
+                 causal: bool = True):
     """Outputs of selected 32-token query blocks (O, lse, dQ) and 32-token key
     blocks (dK, dV) of document b, head h, each computed from its own
     definition (every key a query row sees, every query row a key sees).
@@ -539,6 +550,7 @@ def sampled_rows(qz: Quantized, b: int, h: int, sm_scale: float, qblocks, kblock
     qblocks / kblocks are doc-local block indices.  Returns dicts keyed by the
     doc-local block index."""
     dh = qz.dochead(b, h)
+    dh.causal = causal
     L = dh.L
     res = {"O": {}, "lse": {}, "dQ": {}, "dK": {}, "dV": {}}
 
@@ -551,12 +563,12 @@ def sampled_rows(qz: Quantized, b: int, h: int, sm_scale: float, qblocks, kblock
     for qb in qblocks:
         rows = np.arange(32 * qb, min(32 * qb + 32, L))
         o, lse2, D = stats(rows)
-        cols = np.arange(0, int(rows[-1]) + 1)
+        cols = np.arange(0, int(rows[-1]) + 1 if causal else L)
         dQ, _, _, _ = bwd_rect(dh, rows, cols, lse2, D, sm_scale, True)
         res["O"][qb], res["lse"][qb], res["dQ"][qb] = o, lse2 * LN2, dQ
     for kb in kblocks:
         cols = np.arange(32 * kb, min(32 * kb + 32, L))
-        rows = np.arange(32 * kb, L)
+        rows = np.arange(32 * kb if causal else 0, L)
         _, lse2, D = stats(rows)
         _, dK, dV, _ = bwd_rect(dh, rows, cols, lse2, D, sm_scale, True)
         res["dK"][kb], res["dV"][kb] = dK, dV

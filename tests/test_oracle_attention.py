@@ -203,3 +203,70 @@ def test_sampled_rows_equal_full_attention():
         rows = slice(s + 32 * kb, min(s + 32 * kb + 32, 300))
         assert np.allclose(res["dK"][kb], r["dK"][rows, 0], rtol=1e-10, atol=1e-13)
         assert np.allclose(res["dV"][kb], r["dV"][rows, 0], rtol=1e-10, atol=1e-13)
+
+
+# ------------------------------------------------------------ non-causal mode
+# (review page, sec. 4.8: the non-causal packed call; every query sees every
+# key of its own document)
+
+def _softmax_attention(q, k, v, do, scale):
+    """Plain dense softmax attention of one document and its gradients,
+    written out from the definition (float64)."""
+    S = scale * q @ k.T
+    P = np.exp(S - S.max(axis=1, keepdims=True))
+    P /= P.sum(axis=1, keepdims=True)
+    o = P @ v
+    dP = do @ v.T
+    dS = P * (dP - (dP * P).sum(axis=1, keepdims=True))
+    return o, scale * dS @ k, scale * dS.T @ q, P.T @ do
+
+
+def test_noncausal_exact_equals_dense_softmax():
+    q, k, v, do = qkvdo(45, 2, 16, seed=31)
+    cu = [0, 20, 45]
+    r = O.attention(q, k, v, do, cu, 0.37, quant=False, causal=False)
+    for b in range(2):
+        s, e = cu[b], cu[b + 1]
+        for h in range(2):
+            o, dq, dk, dv = _softmax_attention(q[s:e, h], k[s:e, h], v[s:e, h], do[s:e, h], 0.37)
+            for got, want in ((r["O"], o), (r["dQ"], dq), (r["dK"], dk), (r["dV"], dv)):
+                assert np.allclose(got[s:e, h], want, rtol=1e-10, atol=1e-12)
+
+
+def test_noncausal_outputs_ignore_key_order():
+    # permuting the keys (with their values) of a document leaves every
+    # non-causal output row unchanged; a causal mask would not
+    q, k, v, do = qkvdo(40, 1, 16, seed=33)
+    perm = np.random.default_rng(1).permutation(40)
+    a = O.attention(q, k, v, do, [0, 40], 0.25, quant=False, causal=False)
+    b = O.attention(q, k[perm], v[perm], do, [0, 40], 0.25, quant=False, causal=False)
+    assert np.allclose(a["O"], b["O"], rtol=1e-12, atol=1e-14)
+    assert np.allclose(a["dQ"], b["dQ"], rtol=1e-10, atol=1e-13)
+    assert np.allclose(a["dK"][perm], b["dK"], rtol=1e-10, atol=1e-13)
+    c = O.attention(q, k[perm], v[perm], do, [0, 40], 0.25, quant=False)
+    assert not np.allclose(a["O"], c["O"])
+
+
+def test_noncausal_quantised_tracks_exact():
+    q, k, v, do = qkvdo(200, 2, 64, seed=35)
+    cu = [0, 77, 200]
+    ex = O.attention(q, k, v, do, cu, 0.125, quant=False, causal=False)
+    qz = O.attention(q, k, v, do, cu, 0.125, causal=False)
+    # the method's own level against FP32 (the pages' summary: dQ cosine
+    # 0.9979 for MXFP8): O, dV above 0.998, dQ, dK above 0.997
+    for n, bar in (("O", 0.998), ("dV", 0.998), ("dQ", 0.997), ("dK", 0.997)):
+        assert O.cosine(qz[n], ex[n]) > bar, n
+    # documents stay isolated: the first document's rows equal a call on it alone
+    one = O.attention(*[x[:77] for x in (q, k, v, do)], [0, 77], 0.125, causal=False)
+    for n in ("O", "dQ", "dK", "dV"):
+        assert np.array_equal(qz[n][:77], one[n]), n
+
+
+def test_noncausal_sampled_rows_match_full():
+    q, k, v, do = qkvdo(96, 1, 32, seed=37)
+    full = O.attention(q, k, v, do, [0, 96], 0.2, causal=False)
+    res = O.sampled_rows(full["quantized"], 0, 0, 0.2, [1], [0, 2], causal=False)
+    assert np.allclose(res["O"][1], full["O"][32:64, 0], rtol=1e-12, atol=1e-14)
+    assert np.allclose(res["dQ"][1], full["dQ"][32:64, 0], rtol=1e-9, atol=1e-12)
+    assert np.allclose(res["dK"][0], full["dK"][0:32, 0], rtol=1e-9, atol=1e-12)
+    assert np.allclose(res["dV"][2], full["dV"][64:96, 0], rtol=1e-9, atol=1e-12)
