@@ -63,6 +63,8 @@ typedef enum {
 /* Attention flags. */
 #define FLAMIA_FLAG_NVFP4_QK 0x1    /* score product QK^T (fwd and bwd recompute)
                                        from the NVFP4 copy of Q and K (d == 64)   */
+#define FLAMIA_FLAG_NONCAUSAL 0x4   /* every query sees every key of its own
+                                       document (no causal mask)                 */
 #define FLAMIA_FLAG_HADAMARD 0x2    /* q and k were quantised with
                                        FLAMIA_FORMAT_HADAMARD: scores use
                                        softmax_scale / d; the backward returns
@@ -190,6 +192,10 @@ flamia_status flamia_build_worklist_static(const int32_t* cu_seqlens, int ndocs,
  * FLAMIA_FLAG_HADAMARD: q and k hold Q H_d and K H_d, so the call uses
  * softmax_scale / d for the scores (the same S exactly, d a power of two).
  * Not combinable with FLAMIA_FLAG_NVFP4_QK.
+ * FLAMIA_FLAG_NONCAUSAL (review page sec. 4.8, the non-causal packed call):
+ * every query sees every key of its own document; the same numerics, the
+ * same work list (its costs are the causal ones: only the order of the items
+ * follows from them).
  *
  *  q, k, v      host pointers to quantised operands (E4M3 + scales; with
  *               FLAMIA_FLAG_NVFP4_QK also the NVFP4 copies of q and k).
@@ -224,6 +230,8 @@ size_t flamia_bwd_workspace_bytes(int T, int H, int d);
  * from the unquantised P; dS exponent = round-up rule on each document-aligned
  * 32x32 block maximum; dQ and dK scaled by softmax_scale after the products;
  * dQ partial sums are added in float32 (no prescale), then converted to BF16.
+ * FLAMIA_FLAG_NONCAUSAL: as for the forward; dS is masked only at the
+ * document ends.
  * FLAMIA_FLAG_HADAMARD: as for the forward, with softmax_scale / d, and the
  * gradients of the rotated operands are rotated back before the BF16
  * conversion: dQ = dQ_r H_d, dK = dK_r H_d (float32 butterflies as in the

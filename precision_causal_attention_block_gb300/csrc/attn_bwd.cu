@@ -185,9 +185,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           const uint32_t bf = smem_u32(&sm.bar_qd_full[st]);
           mbar_arrive_expect_tx(bf, kPairBytes);
-          tma_load_3d(smem_u32(sm.q[st]), &map_q, bf, 0, it.h, it.k0 + u * kTile);
-          tma_load_3d(smem_u32(sm.dout[st]), &map_do, bf, 0, it.h, it.k0 + u * kTile);
-          if (NVF4) tma_load_3d(smem_u32(sm.q4[st]), &map_q4, bf, 0, it.h, it.k0 + u * kTile);
+          tma_load_3d(smem_u32(sm.q[st]), &map_q, bf, 0, it.h, it.qs + u * kTile);
+          tma_load_3d(smem_u32(sm.dout[st]), &map_do, bf, 0, it.h, it.qs + u * kTile);
+          if (NVF4) tma_load_3d(smem_u32(sm.q4[st]), &map_q4, bf, 0, it.h, it.qs + u * kTile);
         }
         if (ok) idx = claim_item(counter);
       }
@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (idx >= total) break;
       BwdItem it;
       if (!decode_bwd_item(prm, n_items, idx, it)) continue;
-      const int h = it.h, e = it.e, k0 = it.k0, nq = it.nq;
+      const int h = it.h, e = it.e, k0 = it.k0, nq = it.nq, qs = it.qs;
       const int kj = k0 + j;
       const bool key_valid = kj < it.k1;
       const size_t hT = static_cast<size_t>(h) * T;
@@ -359,7 +359,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (NVF4 && g == 0) {
         // the previous item's products completed before its last dQ was read
         write_sf4(prm.k4_scales, k0, kSfK4);
-        write_sf4(prm.q4_scales, k0, kSfQ4 + 4 * (uc & 1));
+        write_sf4(prm.q4_scales, qs, kSfQ4 + 4 * (uc & 1));
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(smem_u32(&sm.bar_sf));
@@ -372,7 +372,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint32_t r_qb = 127u, r_dob = 127u;
       bool r_qv = false;
       auto fetch_query_inputs = [&](int u) {
-        const int qi = k0 + u * kTile + j;
+        const int qi = qs + u * kTile + j;
         r_qv = qi < e;
         const size_t at = hT + min(qi, T - 1);
         r_lse = prm.lse[at];
@@ -397,7 +397,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       named_barrier_sync(1, kComputeThreads);
       for (int u = 0; u < nq; ++u, ++uc) {
-        const int q0 = k0 + u * kTile;
+        const int q0 = qs + u * kTile;
         const int ub = uc & 1;
         if (g == 0 && u + 1 < nq) fetch_query_inputs(u + 1);  // lands during this tile
         ok = ok && !sm.abort && mbar_wait(smem_u32(&sm.bar_s_full), uc & 1);
@@ -419,7 +419,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!key_valid) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) dv[i] = 0u;
-          } else if (u == 0) {
+          } else if (prm.causal && u == 0) {
             amax = bwd_chunk<true>(sv, dv, sm.nl[ub] + 32 * c, sm.dd[ub] + 32 * c, fS, fP,
                                    32 * c, j, pw);
           } else {
@@ -657,8 +657,8 @@ template <int DIM, bool NVF4>
 flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
                          const flamia_qtensor* v, const flamia_qtensor* dout, const float* D,
                          const float* lse, const int32_t* cu, int ndocs, int T, int H,
-                         float softmax_scale, bool had, void* wl, void* dq, void* dk, void* dv,
-                         float* acc, int* status, cudaStream_t stream) {
+                         float softmax_scale, bool had, bool causal, void* wl, void* dq,
+                         void* dk, void* dv, float* acc, int* status, cudaStream_t stream) {
   CUtensorMap mq, mk, mv, mdo, mdq, mq4, mk4;
   const CUtensorMapSwizzle swz = swizzle_for_row_bytes(DIM);
   if (DIM == 64 && (!make_token_map(&mq, q->codes, T, H, DIM, kTile, swz) ||
@@ -697,6 +697,7 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
   prm.scale_log2 = softmax_scale * 1.4426950408889634f;
   prm.sm_scale = softmax_scale;
   prm.hadamard = had ? 1 : 0;
+  prm.causal = causal ? 1 : 0;
   prm.status = status;
   const size_t n = static_cast<size_t>(T) * H * DIM;
   if (cudaMemsetAsync(acc, 0, n * sizeof(float), stream) != cudaSuccess) return FLAMIA_ERR_CUDA;
@@ -716,8 +717,8 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
         mq, mk, mv, mdo, mdq, mq4, mk4, prm);
     if (cudaGetLastError() != cudaSuccess) return FLAMIA_ERR_CUDA;
   }
-  if (launch_bwd_short(q, k, v, dout, D, lse, cu, ndocs, T, H, DIM, softmax_scale, NVF4, had, acc,
-                       dk, dv, stream) != cudaSuccess)
+  if (launch_bwd_short(q, k, v, dout, D, lse, cu, ndocs, T, H, DIM, softmax_scale, NVF4, had,
+                       causal, acc, dk, dv, stream) != cudaSuccess)
     return FLAMIA_ERR_CUDA;
   if (had) {
     const size_t rows = static_cast<size_t>(T) * H;
@@ -751,9 +752,11 @@ extern "C" flamia_status flamia_attn_bwd(const flamia_qtensor* q, const flamia_q
                                          void* dq_bf16, void* dk_bf16, void* dv_bf16, void* ws,
                                          size_t ws_bytes, int* dev_status, void* stream) {
   if (!supported_dim(d)) return FLAMIA_ERR_UNSUPPORTED;
-  if ((flags & ~(FLAMIA_FLAG_NVFP4_QK | FLAMIA_FLAG_HADAMARD)) != 0) return FLAMIA_ERR_UNSUPPORTED;
+  if ((flags & ~(FLAMIA_FLAG_NVFP4_QK | FLAMIA_FLAG_HADAMARD | FLAMIA_FLAG_NONCAUSAL)) != 0)
+    return FLAMIA_ERR_UNSUPPORTED;
   const bool nvf4 = (flags & FLAMIA_FLAG_NVFP4_QK) != 0;
   const bool had = (flags & FLAMIA_FLAG_HADAMARD) != 0;
+  const bool causal = (flags & FLAMIA_FLAG_NONCAUSAL) == 0;
   if ((nvf4 && d != 64) || (nvf4 && had)) return FLAMIA_ERR_UNSUPPORTED;
   if (!valid_sizes(T, H, d, ndocs) || !q || !k || !v || !dout || !D || !lse || !cu_seqlens ||
       !wl || !dq_bf16 || !dk_bf16 || !dv_bf16 || !ws || !(softmax_scale > 0.f))
@@ -775,10 +778,12 @@ extern "C" flamia_status flamia_attn_bwd(const flamia_qtensor* q, const flamia_q
   // rotated Q, K: the same scores with softmax_scale / d (exact: d = 2^k)
   const float sc = had ? softmax_scale / static_cast<float>(d) : softmax_scale;
   if (nvf4)
-    return launch_bwd<64, true>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, sc, false, wl,
-                                dq_bf16, dk_bf16, dv_bf16, acc, dev_status, s);
+    return launch_bwd<64, true>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, sc, false,
+                                causal, wl, dq_bf16, dk_bf16, dv_bf16, acc, dev_status, s);
   return d == 128 ? launch_bwd<128, false>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, sc,
-                                           had, wl, dq_bf16, dk_bf16, dv_bf16, acc, dev_status, s)
+                                           had, causal, wl, dq_bf16, dk_bf16, dv_bf16, acc,
+                                           dev_status, s)
                   : launch_bwd<64, false>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, sc,
-                                          had, wl, dq_bf16, dk_bf16, dv_bf16, acc, dev_status, s);
+                                          had, causal, wl, dq_bf16, dk_bf16, dv_bf16, acc,
+                                          dev_status, s);
 }

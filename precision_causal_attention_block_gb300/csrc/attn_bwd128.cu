@@ -65,7 +65,7 @@ struct Bwd128Smem {
   volatile int abort;
 };
 
-__device__ __forceinline__ int n_tiles64(const BwdItem& it) { return (it.e - it.k0 + kQT - 1) / kQT; }
+__device__ __forceinline__ int n_tiles64(const BwdItem& it) { return (it.e - it.qs + kQT - 1) / kQT; }
 
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd128_kernel(const __grid_constant__ CUtensorMap map_q,
@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int pre = min(nq, 2);
         int u = 0;
         // the item's first query tiles do not depend on the previous K / V
-        for (; u < pre && ok; ++u) ok = load_qd(it.h, it.k0 + u * kQT);
+        for (; u < pre && ok; ++u) ok = load_qd(it.h, it.qs + u * kQT);
         if (!ok) break;
         if (nk > 0 && (!mbar_wait(smem_u32(&sm.bar_kv_free), (nk - 1) & 1) || sm.abort)) {
           ok = false;
@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(smem_u32(sm.k), &map_k, bkv, 0, it.h, it.k0);
         tma_load_3d(smem_u32(sm.v), &map_v, bkv, 0, it.h, it.k0);
         ++nk;
-        for (; u < nq && ok; ++u) ok = load_qd(it.h, it.k0 + u * kQT);
+        for (; u < nq && ok; ++u) ok = load_qd(it.h, it.qs + u * kQT);
         if (ok) idx = claim_item(counter);
       }
       // drain: every issued copy has landed before the CTA exits
@@ -348,12 +348,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       int u = ((ug & 1) == g) ? 0 : 1;  // this group's first tile of the item
       if (u < nq) {
-        fetch_inputs(hT, k0 + u * kQT, e);
+        fetch_inputs(hT, it.qs + u * kQT, e);
         store_inputs(ng & 1);
       }
       named_barrier_sync(bar_id, kGroupThreads);
       for (; u < nq; u += 2, ++ng) {
-        const int q0 = k0 + u * kQT;
+        const int q0 = it.qs + u * kQT;
         const int buf = ng & 1;
         if (u + 2 < nq) fetch_inputs(hT, q0 + 2 * kQT, e);  // lands during this tile
         ok = ok && !sm.abort && mbar_wait(smem_u32(&sm.bar_s_full[g]), ng & 1);
@@ -376,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!key_valid) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) dv[i] = 0u;
-          } else if (u < 2) {  // the tile crosses the diagonal
+          } else if (prm.causal && u < 2) {  // the tile crosses the diagonal
             amax = bwd_chunk<true>(sv, dv, nl, dd, fS, fP, u * kQT + 32 * c, j, pw);
           } else {
             amax = bwd_chunk<false>(sv, dv, nl, dd, fS, fP, u * kQT + 32 * c, j, pw);

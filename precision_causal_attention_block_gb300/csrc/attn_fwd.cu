@@ -76,6 +76,7 @@ struct FwdParams {
   float* lse;
   int T, H, ndocs, cap;
   float scale_log2;  // softmax_scale * log2(e)
+  int causal;        // 0: every query sees every key of its document
   int* status;
 };
 
@@ -161,6 +162,10 @@ __device__ __forceinline__ bool decode_fwd_item(const FwdParams& prm, int n_item
   it.valid1 = it.q1 > it.q0 + kTile;
   it.n0 = (it.q0 - it.s) / kTile + 1;      // key tiles of query tile 0
   it.n1 = it.valid1 ? it.n0 + 1 : 0;       // key tiles of query tile 1
+  if (!prm.causal) {  // both tiles see every key tile of the document
+    it.n0 = (it.e - it.s + kTile - 1) / kTile;
+    it.n1 = it.valid1 ? it.n0 : 0;
+  }
   it.nkv = it.valid1 ? it.n1 : it.n0;
   return true;
 }
@@ -478,8 +483,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         ++s_seen;
         tc_fence_after();
+        // the last key tile holds the diagonal (causal) or the document end
         const bool diag = (j == nt - 1);
-        const int lim = diag ? min(r, e - 1 - k0) : kTile - 1;  // last visible column
+        const int lim = diag ? min(prm.causal ? r : kTile - 1, e - 1 - k0) : kTile - 1;
         // the whole 128-column row of S_t in registers: four loads, one wait
         uint32_t sv[4][32];
 #pragma unroll
@@ -609,8 +615,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 template <int DIM, bool NVF4>
 flamia_status launch_fwd(const flamia_qtensor* q, const flamia_qtensor* k,
                          const flamia_qtensor* v, const int32_t* cu, int ndocs, int T, int H,
-                         float softmax_scale, void* wl, void* o, float* lse, int* status,
-                         cudaStream_t stream) {
+                         float softmax_scale, bool causal, void* wl, void* o, float* lse,
+                         int* status, cudaStream_t stream) {
   CUtensorMap mq, mk, mv, mq4, mk4;
   const CUtensorMapSwizzle swz = swizzle_for_row_bytes(DIM);
   if (!make_token_map(&mq, q->codes, T, H, DIM, kTile, swz) ||
@@ -642,6 +648,7 @@ flamia_status launch_fwd(const flamia_qtensor* q, const flamia_qtensor* k,
   prm.ndocs = ndocs;
   prm.cap = L.cap_fwd;
   prm.scale_log2 = softmax_scale * 1.4426950408889634f;
+  prm.causal = causal ? 1 : 0;
   prm.status = status;
   const size_t smem = sizeof(FwdSmem<DIM, NVF4>) + 1024;
   if (cudaFuncSetAttribute(attn_fwd_kernel<DIM, NVF4>,
@@ -653,7 +660,8 @@ flamia_status launch_fwd(const flamia_qtensor* q, const flamia_qtensor* k,
   attn_fwd_kernel<DIM, NVF4>
       <<<static_cast<unsigned>(grid), kFwdThreads, smem, stream>>>(mq, mk, mv, mq4, mk4, prm);
   if (cudaGetLastError() != cudaSuccess) return FLAMIA_ERR_CUDA;
-  return launch_fwd_short(q, k, v, cu, ndocs, T, H, DIM, softmax_scale, NVF4, o, lse, stream) ==
+  return launch_fwd_short(q, k, v, cu, ndocs, T, H, DIM, softmax_scale, NVF4, causal, o, lse,
+                          stream) ==
                  cudaSuccess
              ? FLAMIA_OK
              : FLAMIA_ERR_CUDA;
@@ -670,8 +678,10 @@ extern "C" flamia_status flamia_attn_fwd(const flamia_qtensor* q, const flamia_q
                                          int flags, void* wl, void* o_bf16, float* lse,
                                          int* dev_status, void* stream) {
   if (!supported_dim(d)) return FLAMIA_ERR_UNSUPPORTED;
-  if ((flags & ~(FLAMIA_FLAG_NVFP4_QK | FLAMIA_FLAG_HADAMARD)) != 0) return FLAMIA_ERR_UNSUPPORTED;
+  if ((flags & ~(FLAMIA_FLAG_NVFP4_QK | FLAMIA_FLAG_HADAMARD | FLAMIA_FLAG_NONCAUSAL)) != 0)
+    return FLAMIA_ERR_UNSUPPORTED;
   const bool nvf4 = (flags & FLAMIA_FLAG_NVFP4_QK) != 0;
+  const bool causal = (flags & FLAMIA_FLAG_NONCAUSAL) == 0;
   if ((nvf4 && d != 64) || (nvf4 && (flags & FLAMIA_FLAG_HADAMARD))) return FLAMIA_ERR_UNSUPPORTED;
   // rotated Q, K (FLAMIA_FLAG_HADAMARD): the same scores with softmax_scale / d
   // (exact: d = 2^k)
@@ -691,10 +701,10 @@ extern "C" flamia_status flamia_attn_fwd(const flamia_qtensor* q, const flamia_q
     return FLAMIA_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (nvf4)
-    return launch_fwd<64, true>(q, k, v, cu_seqlens, ndocs, T, H, softmax_scale, wl, o_bf16, lse,
-                                dev_status, s);
-  return d == 128 ? launch_fwd<128, false>(q, k, v, cu_seqlens, ndocs, T, H, softmax_scale, wl,
-                                           o_bf16, lse, dev_status, s)
-                  : launch_fwd<64, false>(q, k, v, cu_seqlens, ndocs, T, H, softmax_scale, wl,
-                                          o_bf16, lse, dev_status, s);
+    return launch_fwd<64, true>(q, k, v, cu_seqlens, ndocs, T, H, softmax_scale, causal, wl,
+                                o_bf16, lse, dev_status, s);
+  return d == 128 ? launch_fwd<128, false>(q, k, v, cu_seqlens, ndocs, T, H, softmax_scale,
+                                           causal, wl, o_bf16, lse, dev_status, s)
+                  : launch_fwd<64, false>(q, k, v, cu_seqlens, ndocs, T, H, softmax_scale,
+                                          causal, wl, o_bf16, lse, dev_status, s);
 }

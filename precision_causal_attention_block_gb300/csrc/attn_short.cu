@@ -36,6 +36,7 @@ struct ShortParams {
   float* dq_acc;  // float32 [T, H, d]: dS K sums (softmax_scale comes in the conversion)
   __nv_bfloat16 *dk, *dv;
   int hadamard;  // dK rotated back by H_d (Q and K were quantised rotated)
+  int causal;    // 0: every query sees every key of its document
 };
 
 // d/32 E4M3 codes of one row (this lane's slice) decoded to floats.
@@ -126,10 +127,11 @@ __global__ void __launch_bounds__(32 * kShortWarps)
   for (int i = 0; i < L; ++i) {
     float q[DIM / 32];
     load_score_rows<DIM, NVF4>(prm, true, static_cast<size_t>(s + i) * H + h, lane, q);
-    // lane j keeps the raw score of key j (visible keys: j <= i)
+    // lane j keeps the raw score of key j (visible keys: j <= i, or j < L)
+    const int last = prm.causal ? i : L - 1;
     float sj = 0.f;
-    const bool vis = lane <= i;
-    for (int j = 0; j <= i; ++j) {
+    const bool vis = lane <= last;
+    for (int j = 0; j <= last; ++j) {
       float k[DIM / 32];
       load_score_rows<DIM, NVF4>(prm, false, static_cast<size_t>(s + j) * H + h, lane, k);
       const float dot = warp_dot<DIM>(q, k);
@@ -145,7 +147,7 @@ __global__ void __launch_bounds__(32 * kShortWarps)
     for (int off = 16; off > 0; off >>= 1) l8 += __shfl_xor_sync(0xffffffffu, l8, off);
     const float ph = e4m3x2_to_float2(cvt_e4m3x2(p8, 0.f)).x;  // the E4M3 operand value
     float acc[DIM / 32] = {};
-    for (int j = 0; j <= i; ++j) {
+    for (int j = 0; j <= last; ++j) {
       const float pj = __shfl_sync(0xffffffffu, ph, j);
       float v[DIM / 32];
       load_codes<DIM>(prm.vc, static_cast<size_t>(s + j) * H + h, lane, v);
@@ -189,7 +191,7 @@ __global__ void __launch_bounds__(32 * kShortWarps)
     load_codes<DIM>(prm.doc_, static_cast<size_t>(s + i) * H + h, lane, g);
     const float nl = 8.f - prm.lse_in[hT + s + i] * LOG2E;
     const float Di = prm.D[hT + s + i];
-    for (int j = 0; j <= i; ++j) {
+    for (int j = 0; j <= (prm.causal ? i : L - 1); ++j) {
       float k[DIM / 32], v[DIM / 32];
       load_score_rows<DIM, NVF4>(prm, false, static_cast<size_t>(s + j) * H + h, lane, k);
       load_codes<DIM>(prm.vc, static_cast<size_t>(s + j) * H + h, lane, v);
@@ -211,7 +213,7 @@ __global__ void __launch_bounds__(32 * kShortWarps)
   // dQ_i = scale * sum_j dS^_ij K^_j  (float32 rows of the accumulator)
   for (int i = 0; i < L; ++i) {
     float acc[DIM / 32] = {};
-    for (int j = 0; j <= i; ++j) {
+    for (int j = 0; j <= (prm.causal ? i : L - 1); ++j) {
       const float dsh = e4m3x2_to_float2(cvt_e4m3x2(s_ds[w][i][j] * inv, 0.f)).x * dsc;
       float k[DIM / 32];
       load_codes<DIM>(prm.kc, static_cast<size_t>(s + j) * H + h, lane, k);
@@ -226,7 +228,7 @@ __global__ void __launch_bounds__(32 * kShortWarps)
   // dK_j = scale * sum_i dS^_ij Q^_i,  dV_j = 2^-8 sum_i P^b_ij dO^_i
   for (int j = 0; j < L; ++j) {
     float ak[DIM / 32] = {}, av[DIM / 32] = {};
-    for (int i = j; i < L; ++i) {
+    for (int i = prm.causal ? j : 0; i < L; ++i) {
       const float dsh = e4m3x2_to_float2(cvt_e4m3x2(s_ds[w][i][j] * inv, 0.f)).x * dsc;
       const float pb = e4m3x2_to_float2(cvt_e4m3x2(s_p[w][i][j], 0.f)).x;
       float q[DIM / 32], g[DIM / 32];
@@ -281,9 +283,10 @@ inline unsigned short_grid(int ndocs, int H) {
 
 cudaError_t launch_fwd_short(const flamia_qtensor* q, const flamia_qtensor* k,
                              const flamia_qtensor* v, const int32_t* cu, int ndocs, int T, int H,
-                             int d, float softmax_scale, bool nvfp4_qk, void* o, float* lse,
-                             cudaStream_t stream) {
+                             int d, float softmax_scale, bool nvfp4_qk, bool causal, void* o,
+                             float* lse, cudaStream_t stream) {
   ShortParams p = make_params(q, k, v, cu, ndocs, T, H, softmax_scale);
+  p.causal = causal ? 1 : 0;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   const unsigned grid = short_grid(ndocs, H);
@@ -299,10 +302,11 @@ cudaError_t launch_fwd_short(const flamia_qtensor* q, const flamia_qtensor* k,
 cudaError_t launch_bwd_short(const flamia_qtensor* q, const flamia_qtensor* k,
                              const flamia_qtensor* v, const flamia_qtensor* dout, const float* D,
                              const float* lse, const int32_t* cu, int ndocs, int T, int H, int d,
-                             float softmax_scale, bool nvfp4_qk, bool hadamard, float* dq_acc,
-                             void* dk, void* dv, cudaStream_t stream) {
+                             float softmax_scale, bool nvfp4_qk, bool hadamard, bool causal,
+                             float* dq_acc, void* dk, void* dv, cudaStream_t stream) {
   ShortParams p = make_params(q, k, v, cu, ndocs, T, H, softmax_scale);
   p.hadamard = hadamard ? 1 : 0;
+  p.causal = causal ? 1 : 0;
   p.doc_ = dout->codes;
   p.dos = dout->scales;
   p.lse_in = lse;

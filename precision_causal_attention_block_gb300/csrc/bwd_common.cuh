@@ -29,6 +29,7 @@ struct BwdParams {
   float scale_log2;  // softmax_scale * log2(e)
   float sm_scale;
   int hadamard;  // dK (and, in the conversion, dQ) rotated back by H_d
+  int causal;    // 0: every query sees every key of its document
   int* status;
 };
 
@@ -79,7 +80,7 @@ __device__ __forceinline__ float bwd_chunk(const uint32_t (&sv)[32], uint32_t (&
 // identically by every role; false for items of short documents, which the
 // CUDA-core kernel handles.
 struct BwdItem {
-  int h, s, e, k0, k1, nq;
+  int h, s, e, k0, k1, qs, nq;  // qs: the first query that sees the key tile
 };
 
 __device__ __forceinline__ bool decode_bwd_item(const BwdParams& prm, int n_items, int idx,
@@ -94,7 +95,9 @@ __device__ __forceinline__ bool decode_bwd_item(const BwdParams& prm, int n_item
   if (it.e - it.s <= kShortDoc) return false;
   it.k0 = it.s + ((min(max(item.y, it.s), it.e) - it.s) & ~(kTile - 1));
   it.k1 = min(max(item.z, it.k0), min(it.k0 + kTile, it.e));
-  it.nq = (it.e - it.k0 + kTile - 1) / kTile;  // query tiles from the diagonal to the end
+  // causal: query tiles from the diagonal to the end; else the whole document
+  it.qs = prm.causal ? it.k0 : it.s;
+  it.nq = (it.e - it.qs + kTile - 1) / kTile;
   return true;
 }
 
