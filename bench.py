@@ -172,7 +172,7 @@ def run_ours(args, rank, world, local):
     xd = {n: t.to(dev) for n, t in x.items()}
     cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev)
     call = fl.TrainingCall(w.T, w.H, w.d, cu, w.sm_scale, nvfp4_qk=args.nvfp4,
-                           hadamard=args.hadamard, device=dev)
+                           hadamard=args.hadamard, causal=not args.noncausal, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -246,8 +246,10 @@ def run_ours(args, rank, world, local):
 
     breakdown = stage_breakdown(call, xd, stream, flush, w)
 
-    flops = w.causal_flops()
-    bwd_flops = 5.0 * w.H * w.d * w.sum_sq_len  # 10 * H * d * L^2 / 2
+    # causal: the visible half of the pairs; non-causal: all L^2 pairs
+    pair_factor = 2.0 if args.noncausal else 1.0
+    flops = w.causal_flops() * pair_factor
+    bwd_flops = 5.0 * w.H * w.d * w.sum_sq_len * pair_factor  # 10 * H * d * L^2 / 2
     res = {"total_ms": total_ms, "e2e_ms": e2e_ms, "bwd_ms": sum(bwd_ms) / len(bwd_ms),
            "clocks": clocks.summary()}
     if world > 1:
@@ -279,6 +281,7 @@ def run_ours(args, rank, world, local):
         "config": {"workload": w.name, "T": w.T, "H": w.H, "d": w.d, "docs": w.ndocs,
                    "qk_product": "nvfp4 (mixed path)" if args.nvfp4 else "mxfp8",
                    "qk_rotation": "hadamard" if args.hadamard else "none",
+                   "mask": "none (non-causal)" if args.noncausal else "causal",
                    "flops_per_step": flops, "l2": "flushed (256 MB write) before every step",
                    "parallelism": f"replicas x{world}"},
         "pct_of_fp8_peak": round(100.0 * value / world / pk["fp8_tflops"], 2),
@@ -289,7 +292,8 @@ def run_ours(args, rank, world, local):
                      "peak": pk["fp8_tflops"], "unit": "TFLOP/s",
                      "frac": round(achieved / pk["fp8_tflops"], 4),
                      "peak_source": pk["source"],
-                     "traffic": None if args.hadamard else profiled_traffic(w, args.nvfp4),
+                     "traffic": None if (args.hadamard or args.noncausal)
+                     else profiled_traffic(w, args.nvfp4),
                      "traffic_unit": "bytes per launch of the attention kernel (ncu, DRAM read + write)"},
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
@@ -418,6 +422,8 @@ def main():
                     help="mixed path: QK^T from NVFP4 copies of Q and K (head dim 64)")
     ap.add_argument("--hadamard", action="store_true",
                     help="Q and K rotated by the Hadamard matrix in the quantiser")
+    ap.add_argument("--noncausal", action="store_true",
+                    help="every query sees its whole document (FLOPs: all L^2 pairs)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
