@@ -32,6 +32,9 @@ What it follows (citations name the page and its section):
   head-dimension channels of Q and K are mixed by a normalised orthogonal
   transform inside the quantiser (dot products preserved, token positions
   not mixed), on by default at head dim 128.
+* survey of the stated API (grouped-query attention, GQA): K and V carry
+  H_kv heads, query head h reads K / V head h // (H / H_kv), and dK, dV of a
+  K / V head sum the contributions of its H / H_kv query heads.
 * same page, sec. 4.8 "Batched and non-causal paths": the non-causal packed
   call, where every query sees every key of its own document.
 * same page, sec. 2 "A small example": the floor exponent rule
@@ -462,23 +465,26 @@ class Quantized:
             self.k4 = dequantize_nvfp4(*quantize_nvfp4(k))
 
     def dochead(self, b: int, h: int) -> DocHead:
+        """Query head h with its K / V head h // (H / H_kv)."""
         s, e = self.cu[b], self.cu[b + 1]
-        ex = lambda sb: sb[h, s:e].astype(np.int64) - 127
-        dh = DocHead(e4m3_decode(self.qc[s:e, h]), ex(self.qs),
-                     e4m3_decode(self.kc[s:e, h]), ex(self.ks),
-                     e4m3_decode(self.vc[s:e, h]), ex(self.vs),
+        hk = h // (self.qc.shape[1] // self.kc.shape[1])
+        ex = lambda sb, hh: sb[hh, s:e].astype(np.int64) - 127
+        dh = DocHead(e4m3_decode(self.qc[s:e, h]), ex(self.qs, h),
+                     e4m3_decode(self.kc[s:e, hk]), ex(self.ks, hk),
+                     e4m3_decode(self.vc[s:e, hk]), ex(self.vs, hk),
                      e4m3_decode(self.doc[s:e, h]) if self.doc is not None else None,
-                     ex(self.dos) if self.doc is not None else None)
+                     ex(self.dos, h) if self.doc is not None else None)
         if self.qk_format == "nvfp4":
-            dh.qs, dh.ks = self.q4[s:e, h], self.k4[s:e, h]
+            dh.qs, dh.ks = self.q4[s:e, h], self.k4[s:e, hk]
         return dh
 
 
 def exact_dochead(q, k, v, do, cu, b, h) -> DocHead:
     s, e = cu[b], cu[b + 1]
+    hk = h // (q.shape[1] // k.shape[1])
     z = np.zeros(e - s, dtype=np.int64)
-    f = lambda x: np.asarray(x[s:e, h], dtype=np.float64)
-    return DocHead(f(q), z, f(k), z, f(v), z, f(do) if do is not None else None, z)
+    f = lambda x, hh: np.asarray(x[s:e, hh], dtype=np.float64)
+    return DocHead(f(q, h), z, f(k, hk), z, f(v, hk), z, f(do, h) if do is not None else None, z)
 
 
 def attention(q, k, v, do, cu_seqlens, sm_scale: float, quant: bool = True,
@@ -493,9 +499,13 @@ def attention(q, k, v, do, cu_seqlens, sm_scale: float, quant: bool = True,
     ``hadamard``: Q and K are rotated by H_d before quantisation (float32
     butterflies; exactly, in float64, when quant is False), the scores use
     sm_scale / d, and dQ, dK are rotated back by H_d.  ``causal=False``: every
-    query sees every key of its document."""
+    query sees every key of its document.  k and v may have H_kv heads (H_kv
+    dividing H): query head h then reads head h // (H / H_kv), and dK, dV
+    ([T, H_kv, d]) sum over the query heads of each K / V head."""
     q = np.asarray(q, dtype=np.float64)
     T, H, d = q.shape
+    Hkv = np.asarray(k).shape[1]
+    assert H % Hkv == 0 and np.asarray(v).shape[1] == Hkv
     if hadamard:
         rot = hadamard_fp32 if quant else (lambda x: np.asarray(x, dtype=np.float64) @ sylvester(d))
         r = attention(rot(q), rot(k), v, do, cu_seqlens, sm_scale / d, quant, qk_format, rule,
@@ -509,7 +519,8 @@ def attention(q, k, v, do, cu_seqlens, sm_scale: float, quant: bool = True,
     heads = range(H) if heads is None else heads
     docs = range(len(cu) - 1) if docs is None else docs
     qz = Quantized(q, k, v, do if backward else None, cu, qk_format, rule, group) if quant else None
-    out = {n: np.zeros((T, H, d)) for n in ("O", "O_bf16", "dQ", "dK", "dV")}
+    out = {n: np.zeros((T, H, d)) for n in ("O", "O_bf16", "dQ")}
+    out.update({n: np.zeros((T, Hkv, d)) for n in ("dK", "dV")})
     out["lse"] = np.full((H, T), np.inf)
     out["D"] = np.zeros((H, T))
     for b in docs:
@@ -533,9 +544,10 @@ def attention(q, k, v, do, cu_seqlens, sm_scale: float, quant: bool = True,
             D = (dohat * o_for_D).sum(axis=1)
             out["D"][h, s:e] = D
             dQ, dK, dV, _ = bwd_rect(dh, rows, rows, lse2, D, sm_scale, quant)
+            hk = h // (H // Hkv)
             out["dQ"][s:e, h] = dQ
-            out["dK"][s:e, h] = dK
-            out["dV"][s:e, h] = dV
+            out["dK"][s:e, hk] += dK
+            out["dV"][s:e, hk] += dV
     if quant:
         out["quantized"] = qz
     return out

@@ -270,3 +270,37 @@ def test_noncausal_sampled_rows_match_full():
     assert np.allclose(res["dQ"][1], full["dQ"][32:64, 0], rtol=1e-9, atol=1e-12)
     assert np.allclose(res["dK"][0], full["dK"][0:32, 0], rtol=1e-9, atol=1e-12)
     assert np.allclose(res["dV"][2], full["dV"][64:96, 0], rtol=1e-9, atol=1e-12)
+
+
+# ------------------------------------------------- grouped-query attention
+# (K / V with H_kv heads shared by groups of H / H_kv query heads)
+
+@pytest.mark.parametrize("quant", [False, True])
+def test_gqa_equals_mha_on_repeated_kv(quant):
+    T, H, Hkv, d = 80, 6, 2, 32
+    rng = np.random.default_rng(41)
+    q, do = [O.bf16_round(rng.standard_normal((T, H, d))) for _ in range(2)]
+    k, v = [O.bf16_round(rng.standard_normal((T, Hkv, d))) for _ in range(2)]
+    cu = [0, 33, 80]
+    g = O.attention(q, k, v, do, cu, 0.2, quant=quant)
+    rep = lambda x: np.repeat(x, H // Hkv, axis=1)   # head h -> kv head h // 3
+    m = O.attention(q, rep(k), rep(v), do, cu, 0.2, quant=quant)
+    assert np.array_equal(g["O"], m["O"]) and np.array_equal(g["dQ"], m["dQ"])
+    assert np.array_equal(g["lse"], m["lse"])
+    for n in ("dK", "dV"):
+        want = m[n].reshape(T, Hkv, H // Hkv, d).sum(axis=2)
+        assert g[n].shape == (T, Hkv, d)
+        assert np.allclose(g[n], want, rtol=1e-12, atol=1e-14 * np.abs(want).max()), n
+
+
+def test_gqa_single_kv_head_gradients_sum_over_queries():
+    # one K / V head for all query heads: dK, dV are the sums over the heads
+    T, H, d = 40, 4, 16
+    rng = np.random.default_rng(43)
+    q, do = [O.bf16_round(rng.standard_normal((T, H, d))) for _ in range(2)]
+    k, v = [O.bf16_round(rng.standard_normal((T, 1, d))) for _ in range(2)]
+    g = O.attention(q, k, v, do, [0, T], 0.3, quant=False)
+    per_head = [O.attention(q[:, h:h + 1], k, v, do[:, h:h + 1], [0, T], 0.3, quant=False)
+                for h in range(H)]
+    for n in ("dK", "dV"):
+        assert np.allclose(g[n][:, 0], sum(r[n][:, 0] for r in per_head), rtol=1e-12, atol=1e-14)
