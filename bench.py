@@ -206,9 +206,10 @@ def run_ours(args, rank, world, local):
             flamia_quant_do(xd["do"], call.cu, call.dout, fl.FORMAT_MXFP8, o=call.o, D=call.D,
                             dev_status=call.status)
             evb[i][0].record(stream)
-            fl.flamia_attn_bwd(call.q, call.k, call.v, call.dout, call.D, call.lse, call.cu,
-                               call.T, call.H, call.d, call.scale, call.wl, call.dq, call.dk,
-                               call.dv, call.ws, call.flags, dev_status=call.status)
+            fl.flamia_attn_bwd_gqa(call.q, call.k, call.v, call.dout, call.D, call.lse, call.cu,
+                                   call.T, call.H, call.H_kv, call.d, call.scale, call.wl,
+                                   call.dq, call.dk, call.dv, call.ws, call.flags,
+                                   dev_status=call.status)
             evb[i][1].record(stream)
             ev[i][1].record(stream)
         torch.cuda.synchronize(dev)
@@ -319,16 +320,17 @@ def stage_breakdown(call, xd, stream, flush, w, reps=10):
                                                                dev_status=call.status),
         "worklist_ms": lambda: fl.flamia_build_worklist(call.cu, call.T, call.wl,
                                                         dev_status=call.status),
-        "fwd_ms": lambda: fl.flamia_attn_fwd(call.q, call.k, call.v, call.cu, call.T, call.H,
-                                             call.d, call.scale, call.wl, call.o, call.lse,
-                                             call.flags, dev_status=call.status),
+        "fwd_ms": lambda: fl.flamia_attn_fwd_gqa(call.q, call.k, call.v, call.cu, call.T, call.H,
+                                                 call.H_kv, call.d, call.scale, call.wl, call.o,
+                                                 call.lse, call.flags, dev_status=call.status),
         "quantize_do_ms": lambda: fl.flamia_quantize_tokenblock(
             xd["do"], call.cu, call.dout, fl.FORMAT_MXFP8, o=call.o, D=call.D,
             dev_status=call.status),
-        "bwd_ms": lambda: fl.flamia_attn_bwd(call.q, call.k, call.v, call.dout, call.D,
-                                             call.lse, call.cu, call.T, call.H, call.d,
-                                             call.scale, call.wl, call.dq, call.dk, call.dv,
-                                             call.ws, call.flags, dev_status=call.status),
+        "bwd_ms": lambda: fl.flamia_attn_bwd_gqa(call.q, call.k, call.v, call.dout, call.D,
+                                                 call.lse, call.cu, call.T, call.H, call.H_kv,
+                                                 call.d, call.scale, call.wl, call.dq, call.dk,
+                                                 call.dv, call.ws, call.flags,
+                                                 dev_status=call.status),
     }
     out = {}
     for name, fn in stages.items():

@@ -215,6 +215,18 @@ flamia_status flamia_attn_fwd(const flamia_qtensor* q, const flamia_qtensor* k,
                               void* stream);
 
 /*
+ * Grouped-query attention: k and v carry H_kv heads (H_kv divides H); query
+ * head h reads K / V head h / (H / H_kv).  k, v codes [T, H_kv, d], scales
+ * [H_kv, T]; q, o [T, H, d]; lse [H, T].  flamia_attn_fwd is this call with
+ * H_kv = H.  FLAMIA_ERR_INVALID_ARG if H_kv does not divide H.
+ */
+flamia_status flamia_attn_fwd_gqa(const flamia_qtensor* q, const flamia_qtensor* k,
+                                  const flamia_qtensor* v, const int32_t* cu_seqlens, int ndocs,
+                                  int T, int H, int H_kv, int d, float softmax_scale, int flags,
+                                  void* wl, void* o_bf16, float* lse, int* dev_status,
+                                  void* stream);
+
+/*
  * Workspace of the backward: a float32 [T, H, d] dQ accumulator plus
  * alignment.  The caller allocates it; the backward clears it itself.
  */
@@ -251,6 +263,20 @@ flamia_status flamia_attn_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
                               float softmax_scale, int flags, void* wl,
                               void* dq_bf16, void* dk_bf16, void* dv_bf16,
                               void* ws, size_t ws_bytes, int* dev_status, void* stream);
+
+/*
+ * Grouped-query backward: as flamia_attn_bwd with K / V heads shared as in
+ * flamia_attn_fwd_gqa; dq [T, H, d], dk and dv [T, H_kv, d] (the gradient of
+ * a K / V head sums over its H / H_kv query heads); dout, D, lse per query
+ * head.  The workspace is flamia_bwd_workspace_bytes(T, H, d).
+ */
+flamia_status flamia_attn_bwd_gqa(const flamia_qtensor* q, const flamia_qtensor* k,
+                                  const flamia_qtensor* v, const flamia_qtensor* dout,
+                                  const float* D, const float* lse, const int32_t* cu_seqlens,
+                                  int ndocs, int T, int H, int H_kv, int d, float softmax_scale,
+                                  int flags, void* wl, void* dq_bf16, void* dk_bf16,
+                                  void* dv_bf16, void* ws, size_t ws_bytes, int* dev_status,
+                                  void* stream);
 
 /* Static description of a status code (never NULL). */
 const char* flamia_status_str(flamia_status s);

@@ -101,7 +101,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   const int H = prm.H, T = prm.T;
   const int n_items = min(prm.wl_header[kHdrTileBwd], prm.cap);
-  const int total = n_items * H;
+  const int total = n_items * prm.Hkv;  // (key tile, K / V head) items
+  const int G = prm.G;
+  // tile v of an item walks the query heads of its K / V head in turn: head
+  // hk G + v / nq, queries qs + (v % nq) kTile
+  auto tile_head = [&](const BwdItem& it, int v) { return G == 1 ? it.hk : it.hk * G + v / it.nq; };
+  auto tile_q0 = [&](const BwdItem& it, int v) {
+    return it.qs + (G == 1 ? v : v % it.nq) * kTile;
+  };
   if (static_cast<int>(blockIdx.x) >= total) {  // uniform over the CTA
     if (threadIdx.x == 0) finish_claims(prm.wl_header + kHdrBwdNext, prm.wl_header + kHdrBwdExit);
     return;
@@ -171,11 +178,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           break;
         }
         mbar_arrive_expect_tx(bkv, kPairBytes);
-        tma_load_3d(smem_u32(sm.k), &map_k, bkv, 0, it.h, it.k0);
-        tma_load_3d(smem_u32(sm.v), &map_v, bkv, 0, it.h, it.k0);
-        if (NVF4) tma_load_3d(smem_u32(sm.k4), &map_k4, bkv, 0, it.h, it.k0);
+        tma_load_3d(smem_u32(sm.k), &map_k, bkv, 0, it.hk, it.k0);
+        tma_load_3d(smem_u32(sm.v), &map_v, bkv, 0, it.hk, it.k0);
+        if (NVF4) tma_load_3d(smem_u32(sm.k4), &map_k4, bkv, 0, it.hk, it.k0);
         ++nk;
-        for (int u = 0; u < it.nq; ++u, ++uc) {
+        for (int u = 0; u < it.nq * G; ++u, ++uc) {
           const int st = uc % kBStages;
           if (uc >= kBStages &&
               (!mbar_wait(smem_u32(&sm.bar_qd_empty[st]), ((uc / kBStages) - 1) & 1) ||
@@ -185,9 +192,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           const uint32_t bf = smem_u32(&sm.bar_qd_full[st]);
           mbar_arrive_expect_tx(bf, kPairBytes);
-          tma_load_3d(smem_u32(sm.q[st]), &map_q, bf, 0, it.h, it.qs + u * kTile);
-          tma_load_3d(smem_u32(sm.dout[st]), &map_do, bf, 0, it.h, it.qs + u * kTile);
-          if (NVF4) tma_load_3d(smem_u32(sm.q4[st]), &map_q4, bf, 0, it.h, it.qs + u * kTile);
+          const int th = tile_head(it, u), tq0 = tile_q0(it, u);
+          tma_load_3d(smem_u32(sm.q[st]), &map_q, bf, 0, th, tq0);
+          tma_load_3d(smem_u32(sm.dout[st]), &map_do, bf, 0, th, tq0);
+          if (NVF4) tma_load_3d(smem_u32(sm.q4[st]), &map_q4, bf, 0, th, tq0);
         }
         if (ok) idx = claim_item(counter);
       }
@@ -253,8 +261,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tc_commit_w(smem_u32(&sm.bar_s_full));
           return true;
         };
-        if (it.nq > 0) ok = ok && issue_sdp(uc);
-        for (int u = 0; ok && u < it.nq; ++u, ++uc) {
+        const int ntot = it.nq * G;  // tiles over the item's query heads
+        if (ntot > 0) ok = ok && issue_sdp(uc);
+        for (int u = 0; ok && u < ntot; ++u, ++uc) {
           const int st = uc % kBStages;
           const uint64_t dq = dq0 + st * kStep, ddo = ddo0 + st * kStep;
           // dV / dK restart from zero on an item's first tile: the previous
@@ -295,7 +304,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                      (u > 0 || kb > 0));
           tc_commit_w(smem_u32(&sm.bar_qd_empty[st]));
           // the next tile's S^T / dP^T right behind
-          if (u + 1 < it.nq && !issue_sdp(uc + 1)) {
+          if (u + 1 < ntot && !issue_sdp(uc + 1)) {
             ok = false;
             break;
           }
@@ -331,10 +340,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (idx >= total) break;
       BwdItem it;
       if (!decode_bwd_item(prm, n_items, idx, it)) continue;
-      const int h = it.h, e = it.e, k0 = it.k0, nq = it.nq, qs = it.qs;
+      const int e = it.e, k0 = it.k0, nt = it.nq, nq = nt * G;
       const int kj = k0 + j;
       const bool key_valid = kj < it.k1;
-      const size_t hT = static_cast<size_t>(h) * T;
+      const size_t hT = static_cast<size_t>(it.hk) * T;  // K / V scale rows
       const int ekj = (key_valid && !NVF4) ? static_cast<int>(prm.k_scales[hT + kj]) - 127 : 0;
       const int evj = key_valid ? static_cast<int>(prm.v_scales[hT + kj]) - 127 : 0;
       const float rowf = pow2_or_zero(ekj) * prm.scale_log2;
@@ -349,17 +358,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // NVFP4 score product: block scales in tensor memory, one 32-bit word (4
       // E4M3 scales) per row; column c + i of a lane quadrant holds row 32 i +
       // lane (the same words in every quadrant).  Group 0 writes them.
-      auto write_sf4 = [&](const uint32_t* words, int tok0, uint32_t col) {
+      auto write_sf4 = [&](const uint32_t* words, int heads, int hh, int tok0, uint32_t col) {
         uint32_t w[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          w[i] = words[static_cast<size_t>(min(tok0 + 32 * i + lane, T - 1)) * H + h];
+          w[i] = words[static_cast<size_t>(min(tok0 + 32 * i + lane, T - 1)) * heads + hh];
         tmem_st4(tmem + lane_off + col, w);
       };
       if (NVF4 && g == 0) {
         // the previous item's products completed before its last dQ was read
-        write_sf4(prm.k4_scales, k0, kSfK4);
-        write_sf4(prm.q4_scales, qs, kSfQ4 + 4 * (uc & 1));
+        write_sf4(prm.k4_scales, prm.Hkv, it.hk, k0, kSfK4);
+        write_sf4(prm.q4_scales, H, tile_head(it, 0), tile_q0(it, 0), kSfQ4 + 4 * (uc & 1));
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(smem_u32(&sm.bar_sf));
@@ -372,9 +381,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       uint32_t r_qb = 127u, r_dob = 127u;
       bool r_qv = false;
       auto fetch_query_inputs = [&](int u) {
-        const int qi = qs + u * kTile + j;
+        const int qi = tile_q0(it, u) + j;
         r_qv = qi < e;
-        const size_t at = hT + min(qi, T - 1);
+        const size_t at = static_cast<size_t>(tile_head(it, u)) * T + min(qi, T - 1);
         r_lse = prm.lse[at];
         r_dd = prm.D[at];
         if (lane == 0) {
@@ -397,7 +406,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       named_barrier_sync(1, kComputeThreads);
       for (int u = 0; u < nq; ++u, ++uc) {
-        const int q0 = qs + u * kTile;
+        const int q0 = tile_q0(it, u), h = tile_head(it, u);
         const int ub = uc & 1;
         if (g == 0 && u + 1 < nq) fetch_query_inputs(u + 1);  // lands during this tile
         ok = ok && !sm.abort && mbar_wait(smem_u32(&sm.bar_s_full), uc & 1);
@@ -419,7 +428,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!key_valid) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) dv[i] = 0u;
-          } else if (prm.causal && u == 0) {
+          } else if (prm.causal && (G == 1 ? u : u % nt) == 0) {
             amax = bwd_chunk<true>(sv, dv, sm.nl[ub] + 32 * c, sm.dd[ub] + 32 * c, fS, fP,
                                    32 * c, j, pw);
           } else {
@@ -488,7 +497,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           // the buffer of its parity was last read by S^T two tiles back,
           // complete before this tile's S^T was)
           if (NVF4 && g == 0 && u + 1 < nq)
-            write_sf4(prm.q4_scales, q0 + kTile, kSfQ4 + 4 * ((uc + 1) & 1));
+            write_sf4(prm.q4_scales, H, tile_head(it, u + 1), tile_q0(it, u + 1),
+                      kSfQ4 + 4 * ((uc + 1) & 1));
           tmem_st_wait();
           fence_proxy_async_smem();
           tc_fence_before();
@@ -540,7 +550,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (ok && prm.hadamard) {
         // Q and K were rotated: group 0 writes whole rows of dK = dK_r H_d
         // (the butterflies need all DIM columns of a row), group 1 of dV
-        __nv_bfloat16* out = (g == 0 ? prm.dk : prm.dv) + (static_cast<size_t>(kj) * H + h) * DIM;
+        __nv_bfloat16* out =
+            (g == 0 ? prm.dk : prm.dv) + (static_cast<size_t>(kj) * prm.Hkv + it.hk) * DIM;
         const float mul = g == 0 ? prm.sm_scale : (1.f / 256.f);
         uint32_t u[DIM / 32][32];
 #pragma unroll
@@ -570,8 +581,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // dV = 2^-8 acc, dK = scale * acc, written to the packed buffers; the
         // groups split the head dimension (every product of the item completed
         // before its last dQ was read)
-        __nv_bfloat16* dvrow = prm.dv + (static_cast<size_t>(kj) * H + h) * DIM;
-        __nv_bfloat16* dkrow = prm.dk + (static_cast<size_t>(kj) * H + h) * DIM;
+        __nv_bfloat16* dvrow = prm.dv + (static_cast<size_t>(kj) * prm.Hkv + it.hk) * DIM;
+        __nv_bfloat16* dkrow = prm.dk + (static_cast<size_t>(kj) * prm.Hkv + it.hk) * DIM;
 #pragma unroll 1
         for (int which = 0; which < 2; ++which) {
           const float mul = which == 0 ? (1.f / 256.f) : prm.sm_scale;
@@ -657,19 +668,19 @@ template <int DIM, bool NVF4>
 flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
                          const flamia_qtensor* v, const flamia_qtensor* dout, const float* D,
                          const float* lse, const int32_t* cu, int ndocs, int T, int H,
-                         float softmax_scale, bool had, bool causal, void* wl, void* dq,
+                         int Hkv, float softmax_scale, bool had, bool causal, void* wl, void* dq,
                          void* dk, void* dv, float* acc, int* status, cudaStream_t stream) {
   CUtensorMap mq, mk, mv, mdo, mdq, mq4, mk4;
   const CUtensorMapSwizzle swz = swizzle_for_row_bytes(DIM);
   if (DIM == 64 && (!make_token_map(&mq, q->codes, T, H, DIM, kTile, swz) ||
-      !make_token_map(&mk, k->codes, T, H, DIM, kTile, swz) ||
-      !make_token_map(&mv, v->codes, T, H, DIM, kTile, swz) ||
+      !make_token_map(&mk, k->codes, T, Hkv, DIM, kTile, swz) ||
+      !make_token_map(&mv, v->codes, T, Hkv, DIM, kTile, swz) ||
       !make_token_map(&mdo, dout->codes, T, H, DIM, kTile, swz) ||
       !make_f32_token_map(&mdq, acc, T, H, DIM, kTile)))
     return FLAMIA_ERR_CUDA;
   if (NVF4) {
     if (!make_token_map(&mq4, q->nvfp4_codes, T, H, DIM / 2, kTile, CU_TENSOR_MAP_SWIZZLE_32B) ||
-        !make_token_map(&mk4, k->nvfp4_codes, T, H, DIM / 2, kTile, CU_TENSOR_MAP_SWIZZLE_32B))
+        !make_token_map(&mk4, k->nvfp4_codes, T, Hkv, DIM / 2, kTile, CU_TENSOR_MAP_SWIZZLE_32B))
       return FLAMIA_ERR_CUDA;
   } else {
     mq4 = mq;
@@ -692,6 +703,8 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
   prm.dv = static_cast<__nv_bfloat16*>(dv);
   prm.T = T;
   prm.H = H;
+  prm.Hkv = Hkv;
+  prm.G = H / Hkv;
   prm.ndocs = ndocs;
   prm.cap = L.cap_bwd;
   prm.scale_log2 = softmax_scale * 1.4426950408889634f;
@@ -702,7 +715,7 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
   const size_t n = static_cast<size_t>(T) * H * DIM;
   if (cudaMemsetAsync(acc, 0, n * sizeof(float), stream) != cudaSuccess) return FLAMIA_ERR_CUDA;
   // persistent: one CTA per SM (shared memory allows one), items in snake order
-  const long long grid = std::min<long long>(static_cast<long long>(L.cap_bwd) * H, num_sms());
+  const long long grid = std::min<long long>(static_cast<long long>(L.cap_bwd) * Hkv, num_sms());
   if constexpr (DIM == 128 && !NVF4) {
     if (launch_bwd128_pipelined(prm, q, k, v, dout, acc, static_cast<unsigned>(grid), stream) !=
         cudaSuccess)
@@ -717,7 +730,7 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
         mq, mk, mv, mdo, mdq, mq4, mk4, prm);
     if (cudaGetLastError() != cudaSuccess) return FLAMIA_ERR_CUDA;
   }
-  if (launch_bwd_short(q, k, v, dout, D, lse, cu, ndocs, T, H, DIM, softmax_scale, NVF4, had,
+  if (launch_bwd_short(q, k, v, dout, D, lse, cu, ndocs, T, H, Hkv, DIM, softmax_scale, NVF4, had,
                        causal, acc, dk, dv, stream) != cudaSuccess)
     return FLAMIA_ERR_CUDA;
   if (had) {
@@ -744,14 +757,16 @@ extern "C" size_t flamia_bwd_workspace_bytes(int T, int H, int d) {
   return align_up(static_cast<size_t>(T) * H * d * sizeof(float), 256);
 }
 
-extern "C" flamia_status flamia_attn_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
-                                         const flamia_qtensor* v, const flamia_qtensor* dout,
-                                         const float* D, const float* lse,
-                                         const int32_t* cu_seqlens, int ndocs, int T, int H,
-                                         int d, float softmax_scale, int flags, void* wl,
-                                         void* dq_bf16, void* dk_bf16, void* dv_bf16, void* ws,
-                                         size_t ws_bytes, int* dev_status, void* stream) {
+extern "C" flamia_status flamia_attn_bwd_gqa(const flamia_qtensor* q, const flamia_qtensor* k,
+                                             const flamia_qtensor* v, const flamia_qtensor* dout,
+                                             const float* D, const float* lse,
+                                             const int32_t* cu_seqlens, int ndocs, int T, int H,
+                                             int H_kv, int d, float softmax_scale, int flags,
+                                             void* wl, void* dq_bf16, void* dk_bf16,
+                                             void* dv_bf16, void* ws, size_t ws_bytes,
+                                             int* dev_status, void* stream) {
   if (!supported_dim(d)) return FLAMIA_ERR_UNSUPPORTED;
+  if (H_kv <= 0 || H <= 0 || H % H_kv != 0) return FLAMIA_ERR_INVALID_ARG;
   if ((flags & ~(FLAMIA_FLAG_NVFP4_QK | FLAMIA_FLAG_HADAMARD | FLAMIA_FLAG_NONCAUSAL)) != 0)
     return FLAMIA_ERR_UNSUPPORTED;
   const bool nvf4 = (flags & FLAMIA_FLAG_NVFP4_QK) != 0;
@@ -778,12 +793,24 @@ extern "C" flamia_status flamia_attn_bwd(const flamia_qtensor* q, const flamia_q
   // rotated Q, K: the same scores with softmax_scale / d (exact: d = 2^k)
   const float sc = had ? softmax_scale / static_cast<float>(d) : softmax_scale;
   if (nvf4)
-    return launch_bwd<64, true>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, sc, false,
-                                causal, wl, dq_bf16, dk_bf16, dv_bf16, acc, dev_status, s);
-  return d == 128 ? launch_bwd<128, false>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, sc,
-                                           had, causal, wl, dq_bf16, dk_bf16, dv_bf16, acc,
+    return launch_bwd<64, true>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, H_kv, sc,
+                                false, causal, wl, dq_bf16, dk_bf16, dv_bf16, acc, dev_status, s);
+  return d == 128 ? launch_bwd<128, false>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, H_kv,
+                                           sc, had, causal, wl, dq_bf16, dk_bf16, dv_bf16, acc,
                                            dev_status, s)
-                  : launch_bwd<64, false>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, sc,
-                                          had, causal, wl, dq_bf16, dk_bf16, dv_bf16, acc,
+                  : launch_bwd<64, false>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, H_kv,
+                                          sc, had, causal, wl, dq_bf16, dk_bf16, dv_bf16, acc,
                                           dev_status, s);
+}
+
+extern "C" flamia_status flamia_attn_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
+                                         const flamia_qtensor* v, const flamia_qtensor* dout,
+                                         const float* D, const float* lse,
+                                         const int32_t* cu_seqlens, int ndocs, int T, int H,
+                                         int d, float softmax_scale, int flags, void* wl,
+                                         void* dq_bf16, void* dk_bf16, void* dv_bf16, void* ws,
+                                         size_t ws_bytes, int* dev_status, void* stream) {
+  return flamia_attn_bwd_gqa(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, H, d, softmax_scale,
+                             flags, wl, dq_bf16, dk_bf16, dv_bf16, ws, ws_bytes, dev_status,
+                             stream);
 }

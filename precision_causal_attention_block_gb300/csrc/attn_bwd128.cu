@@ -67,6 +67,17 @@ struct Bwd128Smem {
 
 __device__ __forceinline__ int n_tiles64(const BwdItem& it) { return (it.e - it.qs + kQT - 1) / kQT; }
 
+// Tile v of an item walks the query heads of its K / V head in turn: head
+// hk G + v / nt, queries qs + (v % nt) kQT (nt = 64-query tiles per head).
+// (G == 1, multi-head attention, needs no division.)
+__device__ __forceinline__ int tile_head(const BwdItem& it, int G, int nt, int v) {
+  return G == 1 ? it.hk : it.hk * G + v / nt;
+}
+__device__ __forceinline__ int tile_u(int G, int nt, int v) { return G == 1 ? v : v % nt; }
+__device__ __forceinline__ int tile_q0(const BwdItem& it, int G, int nt, int v) {
+  return it.qs + tile_u(G, nt, v) * kQT;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd128_kernel(const __grid_constant__ CUtensorMap map_q,
                        const __grid_constant__ CUtensorMap map_k,
@@ -77,9 +88,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   Bwd128Smem& sm = *reinterpret_cast<Bwd128Smem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
-  const int H = prm.H, T = prm.T;
+  const int T = prm.T;
   const int n_items = min(prm.wl_header[kHdrTileBwd], prm.cap);
-  const int total = n_items * H;
+  const int total = n_items * prm.Hkv;  // (key tile, K / V head) items
+  const int G = prm.G;
   if (static_cast<int>(blockIdx.x) >= total) {  // uniform over the CTA
     if (threadIdx.x == 0) finish_claims(prm.wl_header + kHdrBwdNext, prm.wl_header + kHdrBwdExit);
     return;
@@ -154,21 +166,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           idx = claim_item(counter);
           continue;
         }
-        const int nq = n_tiles64(it);
+        const int nt = n_tiles64(it), nq = nt * G;
         const int pre = min(nq, 2);
         int u = 0;
         // the item's first query tiles do not depend on the previous K / V
-        for (; u < pre && ok; ++u) ok = load_qd(it.h, it.qs + u * kQT);
+        for (; u < pre && ok; ++u) ok = load_qd(tile_head(it, G, nt, u), tile_q0(it, G, nt, u));
         if (!ok) break;
         if (nk > 0 && (!mbar_wait(smem_u32(&sm.bar_kv_free), (nk - 1) & 1) || sm.abort)) {
           ok = false;
           break;
         }
         mbar_arrive_expect_tx(bkv, kKVBytes);
-        tma_load_3d(smem_u32(sm.k), &map_k, bkv, 0, it.h, it.k0);
-        tma_load_3d(smem_u32(sm.v), &map_v, bkv, 0, it.h, it.k0);
+        tma_load_3d(smem_u32(sm.k), &map_k, bkv, 0, it.hk, it.k0);
+        tma_load_3d(smem_u32(sm.v), &map_v, bkv, 0, it.hk, it.k0);
         ++nk;
-        for (; u < nq && ok; ++u) ok = load_qd(it.h, it.qs + u * kQT);
+        for (; u < nq && ok; ++u) ok = load_qd(tile_head(it, G, nt, u), tile_q0(it, G, nt, u));
         if (ok) idx = claim_item(counter);
       }
       // drain: every issued copy has landed before the CTA exits
@@ -225,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (idx >= total) break;
         BwdItem it;
         if (!decode_bwd_item(prm, n_items, idx, it)) continue;
-        const int nq = n_tiles64(it);
+        const int nq = n_tiles64(it) * G;  // tiles over the item's query heads
         ok = mbar_wait_w(smem_u32(&sm.bar_kv), nk & 1) && (nq < 1 || issue_sdp(ug)) &&
              (nq < 2 || issue_sdp(ug + 1));
         for (int u = 0; ok && u < nq; ++u) {
@@ -331,8 +343,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (idx >= total) break;
       BwdItem it;
       if (!decode_bwd_item(prm, n_items, idx, it)) continue;
-      const int h = it.h, e = it.e, k0 = it.k0, nq = n_tiles64(it);
-      const size_t hT = static_cast<size_t>(h) * T;
+      const int e = it.e, k0 = it.k0, nt = n_tiles64(it), nq = nt * G;
+      const size_t hT = static_cast<size_t>(it.hk) * T;  // K / V scale rows
+      auto tile_hT = [&](int v) { return static_cast<size_t>(tile_head(it, G, nt, v)) * T; };
       const int kj = k0 + j;
       const bool key_valid = kj < it.k1;
       const int ekj = key_valid ? static_cast<int>(prm.k_scales[hT + kj]) - 127 : 0;
@@ -348,14 +361,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       int u = ((ug & 1) == g) ? 0 : 1;  // this group's first tile of the item
       if (u < nq) {
-        fetch_inputs(hT, it.qs + u * kQT, e);
+        fetch_inputs(tile_hT(u), tile_q0(it, G, nt, u), e);
         store_inputs(ng & 1);
       }
       named_barrier_sync(bar_id, kGroupThreads);
       for (; u < nq; u += 2, ++ng) {
-        const int q0 = it.qs + u * kQT;
+        const int tu = tile_u(G, nt, u);  // the tile's place among its head's tiles
+        const int q0 = it.qs + tu * kQT, h = tile_head(it, G, nt, u);
         const int buf = ng & 1;
-        if (u + 2 < nq) fetch_inputs(hT, q0 + 2 * kQT, e);  // lands during this tile
+        if (u + 2 < nq) fetch_inputs(tile_hT(u + 2), tile_q0(it, G, nt, u + 2), e);  // lands during this tile
         ok = ok && !sm.abort && mbar_wait(smem_u32(&sm.bar_s_full[g]), ng & 1);
         tc_fence_after();
         uint8_t* pbrow = sm.pb[g] + j * kQT;
@@ -376,8 +390,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!key_valid) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) dv[i] = 0u;
-          } else if (prm.causal && u < 2) {  // the tile crosses the diagonal
-            amax = bwd_chunk<true>(sv, dv, nl, dd, fS, fP, u * kQT + 32 * c, j, pw);
+          } else if (prm.causal && tu < 2) {  // the tile crosses the diagonal
+            amax = bwd_chunk<true>(sv, dv, nl, dd, fS, fP, tu * kQT + 32 * c, j, pw);
           } else {
             amax = bwd_chunk<false>(sv, dv, nl, dd, fS, fP, u * kQT + 32 * c, j, pw);
           }
@@ -486,7 +500,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok && prm.hadamard) {
         // Q and K were rotated: group 0 writes whole rows of dK = dK_r H_d
         // (the butterflies need all 128 columns of a row), group 1 of dV
-        __nv_bfloat16* out = (g == 0 ? prm.dk : prm.dv) + (static_cast<size_t>(kj) * H + h) * kD;
+        __nv_bfloat16* out =
+            (g == 0 ? prm.dk : prm.dv) + (static_cast<size_t>(kj) * prm.Hkv + it.hk) * kD;
         const float mul = g == 0 ? prm.sm_scale : (1.f / 256.f);
         uint32_t u[4][32];
 #pragma unroll
@@ -511,8 +526,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(smem_u32(&sm.bar_acc_empty));
       } else if (ok) {
-        __nv_bfloat16* dvrow = prm.dv + (static_cast<size_t>(kj) * H + h) * kD;
-        __nv_bfloat16* dkrow = prm.dk + (static_cast<size_t>(kj) * H + h) * kD;
+        __nv_bfloat16* dvrow = prm.dv + (static_cast<size_t>(kj) * prm.Hkv + it.hk) * kD;
+        __nv_bfloat16* dkrow = prm.dk + (static_cast<size_t>(kj) * prm.Hkv + it.hk) * kD;
 #pragma unroll 1
         for (int which = 0; which < 2; ++which) {
           const float mul = which == 0 ? (1.f / 256.f) : prm.sm_scale;
@@ -569,8 +584,8 @@ cudaError_t launch_bwd128_pipelined(const BwdParams& prm, const flamia_qtensor* 
   CUtensorMap mq, mk, mv, mdo, mdq;
   const int T = prm.T, H = prm.H;
   if (!make_token_map(&mq, q->codes, T, H, kD, kQT, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_token_map(&mk, k->codes, T, H, kD, kTile, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_token_map(&mv, v->codes, T, H, kD, kTile, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_token_map(&mk, k->codes, T, prm.Hkv, kD, kTile, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_token_map(&mv, v->codes, T, prm.Hkv, kD, kTile, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_token_map(&mdo, dout->codes, T, H, kD, kQT, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_f32_token_map(&mdq, acc, T, H, kD, kQT, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;

@@ -75,6 +75,7 @@ struct FwdParams {
   __nv_bfloat16* o;
   float* lse;
   int T, H, ndocs, cap;
+  int Hkv, G;        // K / V heads; query head h reads K / V head h / G (G = H / Hkv)
   float scale_log2;  // softmax_scale * log2(e)
   int causal;        // 0: every query sees every key of its document
   int* status;
@@ -143,7 +144,7 @@ constexpr uint32_t kSfQ4 = 384, kSfK4 = 392;
 // identically by every role; false for items of short documents, which the
 // CUDA-core kernel handles.
 struct FwdItem {
-  int h, s, e, q0, q1, n0, n1, nkv;
+  int h, hk, s, e, q0, q1, n0, n1, nkv;  // h: query head, hk: its K / V head
   bool valid1;
 };
 
@@ -151,6 +152,7 @@ __device__ __forceinline__ bool decode_fwd_item(const FwdParams& prm, int n_item
                                                 FwdItem& it) {
   const int T = prm.T;
   it.h = idx / n_items;  // head-major: a wave of CTAs shares the K/V of few heads
+  it.hk = it.h / prm.G;
   const int4 item = prm.items[idx % n_items];
   // clamped: a malformed work list or offsets cannot index outside [0, T)
   const int doc = min(max(item.x, 0), prm.ndocs - 1);
@@ -274,9 +276,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
           const uint32_t bf = smem_u32(&sm.bar_kv_full[st]);
           mbar_arrive_expect_tx(bf, kTileBytes + kQBytes);
-          tma_load_3d(smem_u32(sm.k[st]), &map_k, bf, 0, it.h, it.s + j * kTile);
-          tma_load_3d(smem_u32(sm.v[st]), &map_v, bf, 0, it.h, it.s + j * kTile);
-          if (NVF4) tma_load_3d(smem_u32(sm.k4[st]), &map_k4, bf, 0, it.h, it.s + j * kTile);
+          tma_load_3d(smem_u32(sm.k[st]), &map_k, bf, 0, it.hk, it.s + j * kTile);
+          tma_load_3d(smem_u32(sm.v[st]), &map_v, bf, 0, it.hk, it.s + j * kTile);
+          if (NVF4) tma_load_3d(smem_u32(sm.k4[st]), &map_k4, bf, 0, it.hk, it.s + j * kTile);
         }
         if (ok) idx = claim_item(counter);
       }
@@ -422,6 +424,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       FwdItem it;
       if (!decode_fwd_item(prm, n_items, idx, it)) continue;
       const int h = it.h, s = it.s, e = it.e;
+      const size_t hkT = static_cast<size_t>(it.hk) * T;  // K / V scale rows
       const int nt = t == 0 ? it.n0 : it.n1;
       const int kv0 = kvc;
       kvc += it.nkv;
@@ -437,19 +440,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // NVFP4 score product: its block scales live in tensor memory, one 32-bit
       // word (4 E4M3 scales) per row; column c + i of this lane quadrant holds
       // row 32 i + lane (the same words in every quadrant).
-      auto write_sf4 = [&](const uint32_t* words, int tok0, uint32_t col) {
+      auto write_sf4 = [&](const uint32_t* words, int heads, int hh, int tok0, uint32_t col) {
         uint32_t w[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          w[i] = words[static_cast<size_t>(min(tok0 + 32 * i + lane, T - 1)) * H + h];
+          w[i] = words[static_cast<size_t>(min(tok0 + 32 * i + lane, T - 1)) * heads + hh];
         tmem_st4(tmem + lane_off + col, w);
       };
       if (NVF4) {
         // K scales go to the buffer of the key tile's global parity (it was
         // last read by the products of the key tile two before, complete once
         // this group saw the previous item's O_0)
-        write_sf4(prm.q4_scales, qa, kSfQ4 + 4 * t);
-        if (t == 0) write_sf4(prm.k4_scales, s, kSfK4 + 4 * (kv0 & 1));
+        write_sf4(prm.q4_scales, H, h, qa, kSfQ4 + 4 * t);
+        if (t == 0) write_sf4(prm.k4_scales, prm.Hkv, it.hk, s, kSfK4 + 4 * (kv0 & 1));
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(smem_u32(&sm.bar_sf));
@@ -461,7 +464,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       auto fetch_scales = [&](int jj) {
         const int kk = s + jj * kTile + 32 * (lane & 3);
         const bool in = lane < 8 && (lane >= 4 || !NVF4) && jj < nt && kk < e;
-        sbyte = in ? (lane < 4 ? prm.k_scales : prm.v_scales)[hT + kk] : 127u;
+        sbyte = in ? (lane < 4 ? prm.k_scales : prm.v_scales)[hkT + kk] : 127u;
       };
       fetch_scales(0);
       for (int j = 0; j < nt; ++j) {
@@ -558,7 +561,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // buffer was last read by the products of key tile j - 1, which
         // completed before S_0 of tile j)
         if (NVF4 && t == 0 && j + 1 < it.nkv)
-          write_sf4(prm.k4_scales, k0 + kTile, kSfK4 + 4 * ((kv0 + j + 1) & 1));
+          write_sf4(prm.k4_scales, prm.Hkv, it.hk, k0 + kTile, kSfK4 + 4 * ((kv0 + j + 1) & 1));
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(smem_u32(&sm.bar_p_full[t]));
@@ -615,17 +618,17 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 template <int DIM, bool NVF4>
 flamia_status launch_fwd(const flamia_qtensor* q, const flamia_qtensor* k,
                          const flamia_qtensor* v, const int32_t* cu, int ndocs, int T, int H,
-                         float softmax_scale, bool causal, void* wl, void* o, float* lse,
+                         int Hkv, float softmax_scale, bool causal, void* wl, void* o, float* lse,
                          int* status, cudaStream_t stream) {
   CUtensorMap mq, mk, mv, mq4, mk4;
   const CUtensorMapSwizzle swz = swizzle_for_row_bytes(DIM);
   if (!make_token_map(&mq, q->codes, T, H, DIM, kTile, swz) ||
-      !make_token_map(&mk, k->codes, T, H, DIM, kTile, swz) ||
-      !make_token_map(&mv, v->codes, T, H, DIM, kTile, swz))
+      !make_token_map(&mk, k->codes, T, Hkv, DIM, kTile, swz) ||
+      !make_token_map(&mv, v->codes, T, Hkv, DIM, kTile, swz))
     return FLAMIA_ERR_CUDA;
   if (NVF4) {
     if (!make_token_map(&mq4, q->nvfp4_codes, T, H, DIM / 2, kTile, CU_TENSOR_MAP_SWIZZLE_32B) ||
-        !make_token_map(&mk4, k->nvfp4_codes, T, H, DIM / 2, kTile, CU_TENSOR_MAP_SWIZZLE_32B))
+        !make_token_map(&mk4, k->nvfp4_codes, T, Hkv, DIM / 2, kTile, CU_TENSOR_MAP_SWIZZLE_32B))
       return FLAMIA_ERR_CUDA;
   } else {
     mq4 = mq;
@@ -645,6 +648,8 @@ flamia_status launch_fwd(const flamia_qtensor* q, const flamia_qtensor* k,
   prm.lse = lse;
   prm.T = T;
   prm.H = H;
+  prm.Hkv = Hkv;
+  prm.G = H / Hkv;
   prm.ndocs = ndocs;
   prm.cap = L.cap_fwd;
   prm.scale_log2 = softmax_scale * 1.4426950408889634f;
@@ -660,8 +665,8 @@ flamia_status launch_fwd(const flamia_qtensor* q, const flamia_qtensor* k,
   attn_fwd_kernel<DIM, NVF4>
       <<<static_cast<unsigned>(grid), kFwdThreads, smem, stream>>>(mq, mk, mv, mq4, mk4, prm);
   if (cudaGetLastError() != cudaSuccess) return FLAMIA_ERR_CUDA;
-  return launch_fwd_short(q, k, v, cu, ndocs, T, H, DIM, softmax_scale, NVF4, causal, o, lse,
-                          stream) ==
+  return launch_fwd_short(q, k, v, cu, ndocs, T, H, Hkv, DIM, softmax_scale, NVF4, causal, o,
+                          lse, stream) ==
                  cudaSuccess
              ? FLAMIA_OK
              : FLAMIA_ERR_CUDA;
@@ -672,12 +677,14 @@ flamia_status launch_fwd(const flamia_qtensor* q, const flamia_qtensor* k,
 
 using namespace flamia;
 
-extern "C" flamia_status flamia_attn_fwd(const flamia_qtensor* q, const flamia_qtensor* k,
-                                         const flamia_qtensor* v, const int32_t* cu_seqlens,
-                                         int ndocs, int T, int H, int d, float softmax_scale,
-                                         int flags, void* wl, void* o_bf16, float* lse,
-                                         int* dev_status, void* stream) {
+extern "C" flamia_status flamia_attn_fwd_gqa(const flamia_qtensor* q, const flamia_qtensor* k,
+                                             const flamia_qtensor* v, const int32_t* cu_seqlens,
+                                             int ndocs, int T, int H, int H_kv, int d,
+                                             float softmax_scale, int flags, void* wl,
+                                             void* o_bf16, float* lse, int* dev_status,
+                                             void* stream) {
   if (!supported_dim(d)) return FLAMIA_ERR_UNSUPPORTED;
+  if (H_kv <= 0 || H <= 0 || H % H_kv != 0) return FLAMIA_ERR_INVALID_ARG;
   if ((flags & ~(FLAMIA_FLAG_NVFP4_QK | FLAMIA_FLAG_HADAMARD | FLAMIA_FLAG_NONCAUSAL)) != 0)
     return FLAMIA_ERR_UNSUPPORTED;
   const bool nvf4 = (flags & FLAMIA_FLAG_NVFP4_QK) != 0;
@@ -701,10 +708,19 @@ extern "C" flamia_status flamia_attn_fwd(const flamia_qtensor* q, const flamia_q
     return FLAMIA_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (nvf4)
-    return launch_fwd<64, true>(q, k, v, cu_seqlens, ndocs, T, H, softmax_scale, causal, wl,
-                                o_bf16, lse, dev_status, s);
-  return d == 128 ? launch_fwd<128, false>(q, k, v, cu_seqlens, ndocs, T, H, softmax_scale,
+    return launch_fwd<64, true>(q, k, v, cu_seqlens, ndocs, T, H, H_kv, softmax_scale, causal,
+                                wl, o_bf16, lse, dev_status, s);
+  return d == 128 ? launch_fwd<128, false>(q, k, v, cu_seqlens, ndocs, T, H, H_kv, softmax_scale,
                                            causal, wl, o_bf16, lse, dev_status, s)
-                  : launch_fwd<64, false>(q, k, v, cu_seqlens, ndocs, T, H, softmax_scale,
+                  : launch_fwd<64, false>(q, k, v, cu_seqlens, ndocs, T, H, H_kv, softmax_scale,
                                           causal, wl, o_bf16, lse, dev_status, s);
+}
+
+extern "C" flamia_status flamia_attn_fwd(const flamia_qtensor* q, const flamia_qtensor* k,
+                                         const flamia_qtensor* v, const int32_t* cu_seqlens,
+                                         int ndocs, int T, int H, int d, float softmax_scale,
+                                         int flags, void* wl, void* o_bf16, float* lse,
+                                         int* dev_status, void* stream) {
+  return flamia_attn_fwd_gqa(q, k, v, cu_seqlens, ndocs, T, H, H, d, softmax_scale, flags, wl,
+                             o_bf16, lse, dev_status, stream);
 }

@@ -27,6 +27,7 @@ struct ShortParams {
   const uint8_t *q4s, *k4s;                     // NVFP4 E4M3 scales [T, H, d/16]
   const int32_t* cu;
   int T, H, ndocs;
+  int Hkv, G;  // K / V heads; query head h reads K / V head h / G
   float scale_log2, sm_scale;
   // forward
   __nv_bfloat16* o;
@@ -118,12 +119,14 @@ __global__ void __launch_bounds__(32 * kShortWarps)
   const int L = e - s;
   if (L == 0 || L > kShortDoc) return;  // longer documents run on the tile kernels
   const size_t hT = static_cast<size_t>(h) * T;
+  const int hk = h / prm.G, Hkv = prm.Hkv;
+  const size_t hkT = static_cast<size_t>(hk) * T;
   // one scale block per operand: the exponents of the document's first token
   // (on the mixed path the NVFP4 values carry their own scales)
   const float cf = NVF4 ? prm.scale_log2
                         : prm.scale_log2 * pow2_or_zero_s(static_cast<int>(prm.qs[hT + s]) - 127) *
-                              pow2_or_zero_s(static_cast<int>(prm.ks[hT + s]) - 127);
-  const float vsc = pow2_or_zero_s(static_cast<int>(prm.vs[hT + s]) - 127);
+                              pow2_or_zero_s(static_cast<int>(prm.ks[hkT + s]) - 127);
+  const float vsc = pow2_or_zero_s(static_cast<int>(prm.vs[hkT + s]) - 127);
   for (int i = 0; i < L; ++i) {
     float q[DIM / 32];
     load_score_rows<DIM, NVF4>(prm, true, static_cast<size_t>(s + i) * H + h, lane, q);
@@ -133,7 +136,7 @@ __global__ void __launch_bounds__(32 * kShortWarps)
     const bool vis = lane <= last;
     for (int j = 0; j <= last; ++j) {
       float k[DIM / 32];
-      load_score_rows<DIM, NVF4>(prm, false, static_cast<size_t>(s + j) * H + h, lane, k);
+      load_score_rows<DIM, NVF4>(prm, false, static_cast<size_t>(s + j) * Hkv + hk, lane, k);
       const float dot = warp_dot<DIM>(q, k);
       if (lane == j) sj = dot;
     }
@@ -150,7 +153,7 @@ __global__ void __launch_bounds__(32 * kShortWarps)
     for (int j = 0; j <= last; ++j) {
       const float pj = __shfl_sync(0xffffffffu, ph, j);
       float v[DIM / 32];
-      load_codes<DIM>(prm.vc, static_cast<size_t>(s + j) * H + h, lane, v);
+      load_codes<DIM>(prm.vc, static_cast<size_t>(s + j) * Hkv + hk, lane, v);
 #pragma unroll
       for (int c = 0; c < DIM / 32; ++c) acc[c] = fmaf(pj, v[c], acc[c]);
     }
@@ -162,98 +165,141 @@ __global__ void __launch_bounds__(32 * kShortWarps)
   }
 }
 
-template <int DIM, bool NVF4>
+// GQA: one warp per (document, K / V head) walks the group's query heads; the
+// dK / dV rows of the document (at most 32) sum over them in this warp's part
+// of the dynamic shared memory (DIM floats per row, lane l owns its DIM / 32
+// columns).  Otherwise one warp per (document, head) and no accumulator.
+template <int DIM, bool NVF4, bool GQA>
 __global__ void __launch_bounds__(32 * kShortWarps)
     attn_bwd_short_kernel(const ShortParams prm) {
   // per warp: the document's 2^8 P (dV operand before rounding) and dS
   __shared__ float s_p[kShortWarps][kShortDoc][kShortDoc + 1];
   __shared__ float s_ds[kShortWarps][kShortDoc][kShortDoc + 1];
+  extern __shared__ float s_acc[];  // GQA: [warp][dK | dV][row][DIM]
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const long long wid = static_cast<long long>(blockIdx.x) * kShortWarps + w;
-  const int H = prm.H, T = prm.T;
-  if (wid >= static_cast<long long>(prm.ndocs) * H) return;
-  const int doc = static_cast<int>(wid / H), h = static_cast<int>(wid % H);
+  const int H = prm.H, T = prm.T, Hkv = prm.Hkv, G = GQA ? prm.G : 1;
+  const int units = GQA ? Hkv : H;
+  if (wid >= static_cast<long long>(prm.ndocs) * units) return;
+  const int doc = static_cast<int>(wid / units), u = static_cast<int>(wid % units);
+  const int hk = GQA ? u : u / prm.G;  // K / V head
   const int s = min(max(prm.cu[doc], 0), T);
   const int e = min(max(prm.cu[doc + 1], s), T);
   const int L = e - s;
   if (L == 0 || L > kShortDoc) return;
-  const size_t hT = static_cast<size_t>(h) * T;
-  const int eq = static_cast<int>(prm.qs[hT + s]) - 127, ek = static_cast<int>(prm.ks[hT + s]) - 127;
-  const int ev = static_cast<int>(prm.vs[hT + s]) - 127, edo = static_cast<int>(prm.dos[hT + s]) - 127;
-  const float cf = NVF4 ? prm.scale_log2 : prm.scale_log2 * pow2_or_zero_s(eq) * pow2_or_zero_s(ek);
-  const float gp = pow2_or_zero_s(ev) * pow2_or_zero_s(edo);
+  constexpr int N = DIM / 32;
+  float* acck = s_acc + static_cast<size_t>(w) * 2 * kShortDoc * DIM;
+  float* accv = acck + kShortDoc * DIM;
+  if (GQA) {
+    for (int j = 0; j < L; ++j)
+#pragma unroll
+      for (int c = 0; c < N; ++c) acck[j * DIM + N * lane + c] = accv[j * DIM + N * lane + c] = 0.f;
+  }
+  const size_t hkT = static_cast<size_t>(hk) * T;
+  const int ek = static_cast<int>(prm.ks[hkT + s]) - 127, ev = static_cast<int>(prm.vs[hkT + s]) - 127;
   const float LOG2E = 1.4426950408889634f;
-  // P (x 2^8) and dS (x 2^8) of every visible pair, lane = key
-  float amax = 0.f;
-  for (int i = 0; i < L; ++i) {
-    float q[DIM / 32], g[DIM / 32];
-    load_score_rows<DIM, NVF4>(prm, true, static_cast<size_t>(s + i) * H + h, lane, q);
-    load_codes<DIM>(prm.doc_, static_cast<size_t>(s + i) * H + h, lane, g);
-    const float nl = 8.f - prm.lse_in[hT + s + i] * LOG2E;
-    const float Di = prm.D[hT + s + i];
-    for (int j = 0; j <= (prm.causal ? i : L - 1); ++j) {
-      float k[DIM / 32], v[DIM / 32];
-      load_score_rows<DIM, NVF4>(prm, false, static_cast<size_t>(s + j) * H + h, lane, k);
-      load_codes<DIM>(prm.vc, static_cast<size_t>(s + j) * H + h, lane, v);
-      const float sd = warp_dot<DIM>(q, k);
-      const float dp = warp_dot<DIM>(g, v);
-      const float p8 = ex2_approx(fmaf(sd, cf, nl));
-      const float d8 = p8 * fmaf(dp, gp, -Di);
-      if (lane == 0) {
-        s_p[w][i][j] = p8;
-        s_ds[w][i][j] = d8;
-      }
-      amax = fmaxf(amax, fabsf(d8));
-    }
-  }
-  __syncwarp();
-  // the document is one 32x32 dS block: one round-up exponent
-  const int eb = max(roundup_exponent(amax) - 8, -127);
-  const float inv = exp2i(-(eb + 8)), dsc = pow2_or_zero_s(eb);
-  // dQ_i = scale * sum_j dS^_ij K^_j  (float32 rows of the accumulator)
-  for (int i = 0; i < L; ++i) {
-    float acc[DIM / 32] = {};
-    for (int j = 0; j <= (prm.causal ? i : L - 1); ++j) {
-      const float dsh = e4m3x2_to_float2(cvt_e4m3x2(s_ds[w][i][j] * inv, 0.f)).x * dsc;
-      float k[DIM / 32];
-      load_codes<DIM>(prm.kc, static_cast<size_t>(s + j) * H + h, lane, k);
-#pragma unroll
-      for (int c = 0; c < DIM / 32; ++c) acc[c] = fmaf(dsh, k[c], acc[c]);
-    }
-    const float mul = pow2_or_zero_s(ek);  // softmax_scale: in the BF16 conversion
-    float* dst = prm.dq_acc + (static_cast<size_t>(s + i) * H + h) * DIM + (DIM / 32) * lane;
-#pragma unroll
-    for (int c = 0; c < DIM / 32; ++c) dst[c] = acc[c] * mul;
-  }
-  // dK_j = scale * sum_i dS^_ij Q^_i,  dV_j = 2^-8 sum_i P^b_ij dO^_i
-  for (int j = 0; j < L; ++j) {
-    float ak[DIM / 32] = {}, av[DIM / 32] = {};
-    for (int i = prm.causal ? j : 0; i < L; ++i) {
-      const float dsh = e4m3x2_to_float2(cvt_e4m3x2(s_ds[w][i][j] * inv, 0.f)).x * dsc;
-      const float pb = e4m3x2_to_float2(cvt_e4m3x2(s_p[w][i][j], 0.f)).x;
-      float q[DIM / 32], g[DIM / 32];
-      load_codes<DIM>(prm.qc, static_cast<size_t>(s + i) * H + h, lane, q);
+  for (int gq = 0; gq < G; ++gq) {
+    const int h = GQA ? hk * G + gq : u;
+    const size_t hT = static_cast<size_t>(h) * T;
+    const int eq = static_cast<int>(prm.qs[hT + s]) - 127;
+    const int edo = static_cast<int>(prm.dos[hT + s]) - 127;
+    const float cf = NVF4 ? prm.scale_log2 : prm.scale_log2 * pow2_or_zero_s(eq) * pow2_or_zero_s(ek);
+    const float gp = pow2_or_zero_s(ev) * pow2_or_zero_s(edo);
+    // P (x 2^8) and dS (x 2^8) of every visible pair, lane = key
+    float amax = 0.f;
+    for (int i = 0; i < L; ++i) {
+      float q[N], g[N];
+      load_score_rows<DIM, NVF4>(prm, true, static_cast<size_t>(s + i) * H + h, lane, q);
       load_codes<DIM>(prm.doc_, static_cast<size_t>(s + i) * H + h, lane, g);
-#pragma unroll
-      for (int c = 0; c < DIM / 32; ++c) {
-        ak[c] = fmaf(dsh, q[c], ak[c]);
-        av[c] = fmaf(pb, g[c], av[c]);
+      const float nl = 8.f - prm.lse_in[hT + s + i] * LOG2E;
+      const float Di = prm.D[hT + s + i];
+      for (int j = 0; j <= (prm.causal ? i : L - 1); ++j) {
+        float k[N], v[N];
+        load_score_rows<DIM, NVF4>(prm, false, static_cast<size_t>(s + j) * Hkv + hk, lane, k);
+        load_codes<DIM>(prm.vc, static_cast<size_t>(s + j) * Hkv + hk, lane, v);
+        const float sd = warp_dot<DIM>(q, k);
+        const float dp = warp_dot<DIM>(g, v);
+        const float p8 = ex2_approx(fmaf(sd, cf, nl));
+        const float d8 = p8 * fmaf(dp, gp, -Di);
+        if (lane == 0) {
+          s_p[w][i][j] = p8;
+          s_ds[w][i][j] = d8;
+        }
+        amax = fmaxf(amax, fabsf(d8));
       }
     }
-    const float mk = prm.sm_scale * pow2_or_zero_s(eq), mv = pow2_or_zero_s(edo) * (1.f / 256.f);
+    __syncwarp();
+    // the document is one 32x32 dS block: one round-up exponent
+    const int eb = max(roundup_exponent(amax) - 8, -127);
+    const float inv = exp2i(-(eb + 8)), dsc = pow2_or_zero_s(eb);
+    // dQ_i = scale * sum_j dS^_ij K^_j  (float32 rows of the accumulator)
+    for (int i = 0; i < L; ++i) {
+      float acc[N] = {};
+      for (int j = 0; j <= (prm.causal ? i : L - 1); ++j) {
+        const float dsh = e4m3x2_to_float2(cvt_e4m3x2(s_ds[w][i][j] * inv, 0.f)).x * dsc;
+        float k[N];
+        load_codes<DIM>(prm.kc, static_cast<size_t>(s + j) * Hkv + hk, lane, k);
 #pragma unroll
-    for (int c = 0; c < DIM / 32; ++c) {
-      ak[c] *= mk;
-      av[c] *= mv;
+        for (int c = 0; c < N; ++c) acc[c] = fmaf(dsh, k[c], acc[c]);
+      }
+      const float mul = pow2_or_zero_s(ek);  // softmax_scale: in the BF16 conversion
+      float* dst = prm.dq_acc + (static_cast<size_t>(s + i) * H + h) * DIM + N * lane;
+#pragma unroll
+      for (int c = 0; c < N; ++c) dst[c] = acc[c] * mul;
     }
-    if (prm.hadamard) fwht_row<DIM / 32, 32>(ak, lane);  // dK = dK_r H_d (the whole warp)
-    store_bf16<DIM>(prm.dk, static_cast<size_t>(s + j) * H + h, lane, ak);
-    store_bf16<DIM>(prm.dv, static_cast<size_t>(s + j) * H + h, lane, av);
+    // dK_j = scale * sum_i dS^_ij Q^_i,  dV_j = 2^-8 sum_i P^b_ij dO^_i
+    for (int j = 0; j < L; ++j) {
+      float ak[N] = {}, av[N] = {};
+      for (int i = prm.causal ? j : 0; i < L; ++i) {
+        const float dsh = e4m3x2_to_float2(cvt_e4m3x2(s_ds[w][i][j] * inv, 0.f)).x * dsc;
+        const float pb = e4m3x2_to_float2(cvt_e4m3x2(s_p[w][i][j], 0.f)).x;
+        float q[N], g[N];
+        load_codes<DIM>(prm.qc, static_cast<size_t>(s + i) * H + h, lane, q);
+        load_codes<DIM>(prm.doc_, static_cast<size_t>(s + i) * H + h, lane, g);
+#pragma unroll
+        for (int c = 0; c < N; ++c) {
+          ak[c] = fmaf(dsh, q[c], ak[c]);
+          av[c] = fmaf(pb, g[c], av[c]);
+        }
+      }
+      const float mk = prm.sm_scale * pow2_or_zero_s(eq), mv = pow2_or_zero_s(edo) * (1.f / 256.f);
+      if (GQA) {
+#pragma unroll
+        for (int c = 0; c < N; ++c) {
+          acck[j * DIM + N * lane + c] += ak[c] * mk;
+          accv[j * DIM + N * lane + c] += av[c] * mv;
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < N; ++c) {
+          ak[c] *= mk;
+          av[c] *= mv;
+        }
+        if (prm.hadamard) fwht_row<N, 32>(ak, lane);  // dK = dK_r H_d (the whole warp)
+        store_bf16<DIM>(prm.dk, static_cast<size_t>(s + j) * Hkv + hk, lane, ak);
+        store_bf16<DIM>(prm.dv, static_cast<size_t>(s + j) * Hkv + hk, lane, av);
+      }
+    }
+    __syncwarp();  // s_p / s_ds are rewritten by the next head
+  }
+  if (GQA) {
+    for (int j = 0; j < L; ++j) {
+      float ak[N], av[N];
+#pragma unroll
+      for (int c = 0; c < N; ++c) {
+        ak[c] = acck[j * DIM + N * lane + c];
+        av[c] = accv[j * DIM + N * lane + c];
+      }
+      if (prm.hadamard) fwht_row<N, 32>(ak, lane);
+      store_bf16<DIM>(prm.dk, static_cast<size_t>(s + j) * Hkv + hk, lane, ak);
+      store_bf16<DIM>(prm.dv, static_cast<size_t>(s + j) * Hkv + hk, lane, av);
+    }
   }
 }
 
 ShortParams make_params(const flamia_qtensor* q, const flamia_qtensor* k, const flamia_qtensor* v,
-                        const int32_t* cu, int ndocs, int T, int H, float softmax_scale) {
+                        const int32_t* cu, int ndocs, int T, int H, int Hkv,
+                        float softmax_scale) {
   ShortParams p{};
   p.q4c = q->nvfp4_codes;
   p.k4c = k->nvfp4_codes;
@@ -268,6 +314,8 @@ ShortParams make_params(const flamia_qtensor* q, const flamia_qtensor* k, const 
   p.cu = cu;
   p.T = T;
   p.H = H;
+  p.Hkv = Hkv;
+  p.G = H / Hkv;
   p.ndocs = ndocs;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   p.sm_scale = softmax_scale;
@@ -283,9 +331,9 @@ inline unsigned short_grid(int ndocs, int H) {
 
 cudaError_t launch_fwd_short(const flamia_qtensor* q, const flamia_qtensor* k,
                              const flamia_qtensor* v, const int32_t* cu, int ndocs, int T, int H,
-                             int d, float softmax_scale, bool nvfp4_qk, bool causal, void* o,
-                             float* lse, cudaStream_t stream) {
-  ShortParams p = make_params(q, k, v, cu, ndocs, T, H, softmax_scale);
+                             int Hkv, int d, float softmax_scale, bool nvfp4_qk, bool causal,
+                             void* o, float* lse, cudaStream_t stream) {
+  ShortParams p = make_params(q, k, v, cu, ndocs, T, H, Hkv, softmax_scale);
   p.causal = causal ? 1 : 0;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
@@ -301,10 +349,10 @@ cudaError_t launch_fwd_short(const flamia_qtensor* q, const flamia_qtensor* k,
 
 cudaError_t launch_bwd_short(const flamia_qtensor* q, const flamia_qtensor* k,
                              const flamia_qtensor* v, const flamia_qtensor* dout, const float* D,
-                             const float* lse, const int32_t* cu, int ndocs, int T, int H, int d,
-                             float softmax_scale, bool nvfp4_qk, bool hadamard, bool causal,
-                             float* dq_acc, void* dk, void* dv, cudaStream_t stream) {
-  ShortParams p = make_params(q, k, v, cu, ndocs, T, H, softmax_scale);
+                             const float* lse, const int32_t* cu, int ndocs, int T, int H,
+                             int Hkv, int d, float softmax_scale, bool nvfp4_qk, bool hadamard,
+                             bool causal, float* dq_acc, void* dk, void* dv, cudaStream_t stream) {
+  ShortParams p = make_params(q, k, v, cu, ndocs, T, H, Hkv, softmax_scale);
   p.hadamard = hadamard ? 1 : 0;
   p.causal = causal ? 1 : 0;
   p.doc_ = dout->codes;
@@ -314,13 +362,37 @@ cudaError_t launch_bwd_short(const flamia_qtensor* q, const flamia_qtensor* k,
   p.dq_acc = dq_acc;
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
-  const unsigned grid = short_grid(ndocs, H);
-  if (nvfp4_qk)
-    attn_bwd_short_kernel<64, true><<<grid, 32 * kShortWarps, 0, stream>>>(p);
-  else if (d == 128)
-    attn_bwd_short_kernel<128, false><<<grid, 32 * kShortWarps, 0, stream>>>(p);
-  else
-    attn_bwd_short_kernel<64, false><<<grid, 32 * kShortWarps, 0, stream>>>(p);
+  if (Hkv == H) {
+    const unsigned grid = short_grid(ndocs, H);
+    if (nvfp4_qk)
+      attn_bwd_short_kernel<64, true, false><<<grid, 32 * kShortWarps, 0, stream>>>(p);
+    else if (d == 128)
+      attn_bwd_short_kernel<128, false, false><<<grid, 32 * kShortWarps, 0, stream>>>(p);
+    else
+      attn_bwd_short_kernel<64, false, false><<<grid, 32 * kShortWarps, 0, stream>>>(p);
+    return cudaGetLastError();
+  }
+  // grouped query heads: one warp per (document, K / V head), dK / dV sums in
+  // dynamic shared memory (2 x 32 rows x d floats per warp)
+  const unsigned grid = short_grid(ndocs, Hkv);
+  const size_t smem = static_cast<size_t>(kShortWarps) * 2 * kShortDoc * d * sizeof(float);
+  cudaError_t err;
+  if (nvfp4_qk) {
+    err = cudaFuncSetAttribute(attn_bwd_short_kernel<64, true, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    attn_bwd_short_kernel<64, true, true><<<grid, 32 * kShortWarps, smem, stream>>>(p);
+  } else if (d == 128) {
+    err = cudaFuncSetAttribute(attn_bwd_short_kernel<128, false, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    attn_bwd_short_kernel<128, false, true><<<grid, 32 * kShortWarps, smem, stream>>>(p);
+  } else {
+    err = cudaFuncSetAttribute(attn_bwd_short_kernel<64, false, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    attn_bwd_short_kernel<64, false, true><<<grid, 32 * kShortWarps, smem, stream>>>(p);
+  }
   return cudaGetLastError();
 }
 

@@ -26,6 +26,7 @@ struct BwdParams {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int T, H, ndocs, cap;
+  int Hkv, G;        // K / V heads; K / V head hk serves query heads hk G .. hk G + G - 1
   float scale_log2;  // softmax_scale * log2(e)
   float sm_scale;
   int hadamard;  // dK (and, in the conversion, dQ) rotated back by H_d
@@ -80,13 +81,14 @@ __device__ __forceinline__ float bwd_chunk(const uint32_t (&sv)[32], uint32_t (&
 // identically by every role; false for items of short documents, which the
 // CUDA-core kernel handles.
 struct BwdItem {
-  int h, s, e, k0, k1, qs, nq;  // qs: the first query that sees the key tile
+  int hk, s, e, k0, k1, qs, nq;  // hk: K / V head; qs: the first query that sees the key
+                                  // tile; nq: 128-query tiles per query head
 };
 
 __device__ __forceinline__ bool decode_bwd_item(const BwdParams& prm, int n_items, int idx,
                                                 BwdItem& it) {
   const int T = prm.T;
-  it.h = idx / n_items;  // head-major: a wave of CTAs touches the Q / dO / dQ of few heads
+  it.hk = idx / n_items;  // head-major: a wave of CTAs touches the Q / dO / dQ of few heads
   const int4 item = prm.items[idx % n_items];
   // clamped: a malformed work list or offsets cannot index outside [0, T)
   const int doc = min(max(item.x, 0), prm.ndocs - 1);

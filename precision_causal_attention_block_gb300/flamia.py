@@ -41,9 +41,13 @@ SIGNATURES = {
     "flamia_worklist_bytes": (_sz, [_i, _i]),
     "flamia_build_worklist": (_i, [_vp, _i, _i, _vp, _sz, _vp, _vp]),
     "flamia_attn_fwd": (_i, [_QP, _QP, _QP, _vp, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp, _vp, _vp]),
+    "flamia_attn_fwd_gqa": (_i, [_QP, _QP, _QP, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp,
+                                 _vp, _vp]),
     "flamia_bwd_workspace_bytes": (_sz, [_i, _i, _i]),
     "flamia_attn_bwd": (_i, [_QP, _QP, _QP, _QP, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp,
                              _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
+    "flamia_attn_bwd_gqa": (_i, [_QP, _QP, _QP, _QP, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i,
+                                 _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
     "flamia_build_worklist_static": (_i, [_vp, _i, _i, _vp, _sz, _vp, _vp]),
     "flamia_status_str": (ctypes.c_char_p, [_i]),
     "flamia_debug_mma_tile": (_i, [_i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
@@ -141,6 +145,15 @@ def flamia_attn_fwd(q: QTensor, k: QTensor, v: QTensor, cu_seqlens, T, H, d, sof
                                   _ptr(dev_status), _stream()), "flamia_attn_fwd")
 
 
+def flamia_attn_fwd_gqa(q: QTensor, k: QTensor, v: QTensor, cu_seqlens, T, H, H_kv, d,
+                        softmax_scale, wl, o, lse, flags: int = 0, dev_status=None):
+    sq, sk, sv = q.struct(), k.struct(), v.struct()
+    _check(load().flamia_attn_fwd_gqa(ctypes.byref(sq), ctypes.byref(sk), ctypes.byref(sv),
+                                      _ptr(cu_seqlens), cu_seqlens.numel() - 1, T, H, H_kv, d,
+                                      float(softmax_scale), flags, _ptr(wl), _ptr(o), _ptr(lse),
+                                      _ptr(dev_status), _stream()), "flamia_attn_fwd_gqa")
+
+
 def flamia_bwd_workspace_bytes(T: int, H: int, d: int) -> int:
     return int(load().flamia_bwd_workspace_bytes(T, H, d))
 
@@ -156,6 +169,18 @@ def flamia_attn_bwd(q: QTensor, k: QTensor, v: QTensor, dout: QTensor, D, lse, c
            "flamia_attn_bwd")
 
 
+def flamia_attn_bwd_gqa(q: QTensor, k: QTensor, v: QTensor, dout: QTensor, D, lse, cu_seqlens,
+                        T, H, H_kv, d, softmax_scale, wl, dq, dk, dv, ws, flags: int = 0,
+                        dev_status=None):
+    sq, sk, sv, sd = q.struct(), k.struct(), v.struct(), dout.struct()
+    _check(load().flamia_attn_bwd_gqa(ctypes.byref(sq), ctypes.byref(sk), ctypes.byref(sv),
+                                      ctypes.byref(sd), _ptr(D), _ptr(lse), _ptr(cu_seqlens),
+                                      cu_seqlens.numel() - 1, T, H, H_kv, d, float(softmax_scale),
+                                      flags, _ptr(wl), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws),
+                                      ws.numel() * ws.element_size(), _ptr(dev_status),
+                                      _stream()), "flamia_attn_bwd_gqa")
+
+
 def flamia_debug_mma_tile(mode, N, a_mn, b_mn, variant, a, b, sfa, sfb, d_out, dev_status=None):
     _check(load().flamia_debug_mma_tile(mode, N, a_mn, b_mn, variant, _ptr(a), _ptr(b), _ptr(sfa),
                                         _ptr(sfb), _ptr(d_out), _ptr(dev_status), _stream()),
@@ -168,8 +193,9 @@ class TrainingCall:
     for fixed shapes.  All buffers are torch allocations owned by this object."""
 
     def __init__(self, T, H, d, cu_seqlens, softmax_scale, nvfp4_qk: bool = False,
-                 hadamard: bool = False, causal: bool = True, device="cuda"):
+                 hadamard: bool = False, causal: bool = True, H_kv=None, device="cuda"):
         self.T, self.H, self.d = T, H, d
+        self.H_kv = H if H_kv is None else H_kv
         self.scale = softmax_scale
         self.cu = cu_seqlens
         self.flags = ((FLAG_NVFP4_QK if nvfp4_qk else 0) | (FLAG_HADAMARD if hadamard else 0) |
@@ -177,8 +203,8 @@ class TrainingCall:
         self.fmt_qk = ((FORMAT_MXFP8_NVFP4 if nvfp4_qk else FORMAT_MXFP8) |
                        (FORMAT_HADAMARD if hadamard else 0))
         self.q = QTensor(T, H, d, nvfp4_qk, device)
-        self.k = QTensor(T, H, d, nvfp4_qk, device)
-        self.v = QTensor(T, H, d, False, device)
+        self.k = QTensor(T, self.H_kv, d, nvfp4_qk, device)
+        self.v = QTensor(T, self.H_kv, d, False, device)
         self.dout = QTensor(T, H, d, False, device)
         ndocs = cu_seqlens.numel() - 1
         self.wl = torch.empty(flamia_worklist_bytes(T, ndocs), dtype=torch.uint8, device=device)
@@ -187,8 +213,8 @@ class TrainingCall:
         self.lse = torch.empty((H, T), dtype=torch.float32, device=device)
         self.D = torch.empty((H, T), dtype=torch.float32, device=device)
         self.dq = torch.empty((T, H, d), dtype=torch.bfloat16, device=device)
-        self.dk = torch.empty_like(self.dq)
-        self.dv = torch.empty_like(self.dq)
+        self.dk = torch.empty((T, self.H_kv, d), dtype=torch.bfloat16, device=device)
+        self.dv = torch.empty_like(self.dk)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
 
     def forward(self, xq, xk, xv):
@@ -196,16 +222,17 @@ class TrainingCall:
         flamia_quantize_tokenblock(xk, self.cu, self.k, self.fmt_qk, dev_status=self.status)
         flamia_quantize_tokenblock(xv, self.cu, self.v, FORMAT_MXFP8, dev_status=self.status)
         flamia_build_worklist(self.cu, self.T, self.wl, dev_status=self.status)
-        flamia_attn_fwd(self.q, self.k, self.v, self.cu, self.T, self.H, self.d, self.scale,
-                        self.wl, self.o, self.lse, self.flags, dev_status=self.status)
+        flamia_attn_fwd_gqa(self.q, self.k, self.v, self.cu, self.T, self.H, self.H_kv, self.d,
+                            self.scale, self.wl, self.o, self.lse, self.flags,
+                            dev_status=self.status)
         return self.o, self.lse
 
     def backward(self, xdo):
         flamia_quantize_tokenblock(xdo, self.cu, self.dout, FORMAT_MXFP8, o=self.o, D=self.D,
                                    dev_status=self.status)
-        flamia_attn_bwd(self.q, self.k, self.v, self.dout, self.D, self.lse, self.cu, self.T,
-                        self.H, self.d, self.scale, self.wl, self.dq, self.dk, self.dv, self.ws,
-                        self.flags, dev_status=self.status)
+        flamia_attn_bwd_gqa(self.q, self.k, self.v, self.dout, self.D, self.lse, self.cu, self.T,
+                            self.H, self.H_kv, self.d, self.scale, self.wl, self.dq, self.dk,
+                            self.dv, self.ws, self.flags, dev_status=self.status)
         return self.dq, self.dk, self.dv
 
     def __call__(self, xq, xk, xv, xdo):
