@@ -169,10 +169,14 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     w = make_workload(args.workload)
     x = W.make_inputs_bf16(w)
+    hkv = args.kv_heads or w.H
+    if hkv != w.H:  # grouped-query attention: the first hkv heads of K and V
+        x["k"], x["v"] = x["k"][:, :hkv].contiguous(), x["v"][:, :hkv].contiguous()
     xd = {n: t.to(dev) for n, t in x.items()}
     cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev)
     call = fl.TrainingCall(w.T, w.H, w.d, cu, w.sm_scale, nvfp4_qk=args.nvfp4,
-                           hadamard=args.hadamard, causal=not args.noncausal, device=dev)
+                           hadamard=args.hadamard, causal=not args.noncausal, H_kv=hkv,
+                           device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -283,6 +287,7 @@ def run_ours(args, rank, world, local):
                    "qk_product": "nvfp4 (mixed path)" if args.nvfp4 else "mxfp8",
                    "qk_rotation": "hadamard" if args.hadamard else "none",
                    "mask": "none (non-causal)" if args.noncausal else "causal",
+                   "kv_heads": hkv,
                    "flops_per_step": flops, "l2": "flushed (256 MB write) before every step",
                    "parallelism": f"replicas x{world}"},
         "pct_of_fp8_peak": round(100.0 * value / world / pk["fp8_tflops"], 2),
@@ -293,7 +298,7 @@ def run_ours(args, rank, world, local):
                      "peak": pk["fp8_tflops"], "unit": "TFLOP/s",
                      "frac": round(achieved / pk["fp8_tflops"], 4),
                      "peak_source": pk["source"],
-                     "traffic": None if (args.hadamard or args.noncausal)
+                     "traffic": None if (args.hadamard or args.noncausal or hkv != w.H)
                      else profiled_traffic(w, args.nvfp4),
                      "traffic_unit": "bytes per launch of the attention kernel (ncu, DRAM read + write)"},
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
@@ -424,6 +429,8 @@ def main():
                     help="mixed path: QK^T from NVFP4 copies of Q and K (head dim 64)")
     ap.add_argument("--hadamard", action="store_true",
                     help="Q and K rotated by the Hadamard matrix in the quantiser")
+    ap.add_argument("--kv-heads", type=int, default=0,
+                    help="grouped-query attention: K / V heads (dividing the query heads)")
     ap.add_argument("--noncausal", action="store_true",
                     help="every query sees its whole document (FLOPs: all L^2 pairs)")
     args = ap.parse_args()
