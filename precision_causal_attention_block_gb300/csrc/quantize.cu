@@ -50,7 +50,7 @@ __device__ __forceinline__ void unpack8(const uint4& xv, float (&v)[8]) {
   }
 }
 
-template <int DIM, bool HAD>
+template <int DIM, bool HAD, bool FUSE_D>
 __global__ void __launch_bounds__(kQThreads)
     quantize_kernel(const __grid_constant__ CUtensorMap map_x, int T, int H,
                     const int32_t* __restrict__ cu, int ndocs, uint8_t* __restrict__ codes,
@@ -80,6 +80,18 @@ __global__ void __launch_bounds__(kQThreads)
   if (tid == 0) {
     mbar_arrive_expect_tx(smem_u32(&s_bar), kQThreads * DIM * 2);
     tma_load_3d(smem_u32(s_x), &map_x, smem_u32(&s_bar), 0, h, seg0);
+  }
+  const int chunk = lane % LPR;
+  // D = dO . O: this lane's O chunks of its rows, loaded while the rows of
+  // dO are staged and reduced (their latency hides behind phases 1 and 2)
+  uint4 ov[FUSE_D ? NLD : 1];
+  if (FUSE_D) {
+#pragma unroll
+    for (int i = 0; i < NLD; ++i) {
+      const int tt = seg0 + warp * 32 + i * RPI + lane / LPR;
+      ov[i] = tt < T ? __ldg(o + (static_cast<size_t>(tt) * H + h) * LPR + chunk)
+                     : make_uint4(0, 0, 0, 0);
+    }
   }
 
   // Light validation of cu_seqlens, spread over the CTAs of head 0.
@@ -114,7 +126,6 @@ __global__ void __launch_bounds__(kQThreads)
   }
 
   // Phase 1: per-row maximum of this warp's 32 tokens.
-  const int chunk = lane % LPR;
 #pragma unroll
   for (int i = 0; i < NLD; ++i) {
     const int rl = warp * 32 + i * RPI + lane / LPR;  // row inside the staged box
@@ -168,8 +179,10 @@ __global__ void __launch_bounds__(kQThreads)
   }
   __syncthreads();
 
-  // Phase 3: codes (+ NVFP4 copy, + D) from the registers.
-#pragma unroll 4
+  // Phase 3: codes (+ NVFP4 copy, + D) from the registers (fully unrolled
+  // with D, so that the prefetched O chunks stay in registers).
+  constexpr int kUnroll = FUSE_D ? NLD : 4;
+#pragma unroll kUnroll
   for (int i = 0; i < NLD; ++i) {
     const int rl = warp * 32 + i * RPI + lane / LPR;
     const int tt = seg0 + rl;
@@ -209,9 +222,9 @@ __global__ void __launch_bounds__(kQThreads)
         if ((chunk & 1) == 0) f4scales[row * (DIM / 16) + chunk / 2] = static_cast<uint8_t>(sc);
       }
     }
-    if (D != nullptr) {
-      const uint4 ov = valid ? __ldg(o + row * LPR + chunk) : make_uint4(0, 0, 0, 0);
-      const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
+    if (FUSE_D) {
+      const uint4 oi = valid ? ov[i] : make_uint4(0, 0, 0, 0);
+      const uint32_t ow[4] = {oi.x, oi.y, oi.z, oi.w};
       const float scale = pow2f(e);
       float acc = 0.f;
 #pragma unroll
@@ -277,8 +290,11 @@ extern "C" flamia_status flamia_quantize_tokenblock(const void* x_bf16, int T, i
   }
   dim3 grid((T + kSeg - 1) / kSeg, H);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  auto kern = d == 128 ? (had ? quantize_kernel<128, true> : quantize_kernel<128, false>)
-                       : (had ? quantize_kernel<64, true> : quantize_kernel<64, false>);
+  const bool fd = D != nullptr;
+  auto kern = d == 128 ? (had ? quantize_kernel<128, true, false>
+                              : fd ? quantize_kernel<128, false, true> : quantize_kernel<128, false, false>)
+                       : (had ? quantize_kernel<64, true, false>
+                              : fd ? quantize_kernel<64, false, true> : quantize_kernel<64, false, false>);
   kern<<<grid, kQThreads, 0, s>>>(map, T, H, cu_seqlens, ndocs, out->codes, out->scales, f4c, f4s,
                                   static_cast<const uint4*>(o_bf16), D, status);
   return cudaGetLastError() == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
