@@ -216,12 +216,21 @@ class TrainingCall:
         self.dk = torch.empty((T, self.H_kv, d), dtype=torch.bfloat16, device=device)
         self.dv = torch.empty_like(self.dk)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        # the work list is built on a side stream while Q, K, V are quantised
+        self.side = torch.cuda.Stream(device)
+        self.wl_ready = torch.cuda.Event()
 
     def forward(self, xq, xk, xv):
+        main = torch.cuda.current_stream()
+        # cu_seqlens is ready and the previous call has finished with the list
+        self.side.wait_stream(main)
+        with torch.cuda.stream(self.side):
+            flamia_build_worklist(self.cu, self.T, self.wl, dev_status=self.status)
+            self.wl_ready.record(self.side)
         flamia_quantize_tokenblock(xq, self.cu, self.q, self.fmt_qk, dev_status=self.status)
         flamia_quantize_tokenblock(xk, self.cu, self.k, self.fmt_qk, dev_status=self.status)
         flamia_quantize_tokenblock(xv, self.cu, self.v, FORMAT_MXFP8, dev_status=self.status)
-        flamia_build_worklist(self.cu, self.T, self.wl, dev_status=self.status)
+        main.wait_event(self.wl_ready)
         flamia_attn_fwd_gqa(self.q, self.k, self.v, self.cu, self.T, self.H, self.H_kv, self.d,
                             self.scale, self.wl, self.o, self.lse, self.flags,
                             dev_status=self.status)
