@@ -32,16 +32,17 @@ What it follows (citations name the page and its section):
   head-dimension channels of Q and K are mixed by a normalised orthogonal
   transform inside the quantiser (dot products preserved, token positions
   not mixed), on by default at head dim 128.
-* survey of the stated API (grouped-query attention, GQA): K and V carry
-  H_kv heads, query head h reads K / V head h // (H / H_kv), and dK, dV of a
-  K / V head sum the contributions of its H / H_kv query heads.
+* grouped-query attention (GQA), part of the attention API the method
+  serves (the pages give no numerics for it): K and V carry H_kv heads,
+  query head h reads K / V head h // (H / H_kv), and dK, dV of a K / V head
+  sum the contributions of its H / H_kv query heads.
 * same page, sec. 4.8 "Batched and non-causal paths": the non-causal packed
   call, where every query sees every key of its own document.
 * same page, sec. 2 "A small example": the floor exponent rule
   e = floor(log2 amax) - emax with clipping at 448, used here only as the
   negative control of the leakage probe.
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent:
 * code rounding is round-to-nearest-even; -0 keeps its sign bit;
 * amax == 0 gives exponent -127 (byte 0) and all-zero codes; exponents are
   clamped to [-127, 127];
