@@ -69,6 +69,10 @@ typedef enum {
                                        FLAMIA_FORMAT_HADAMARD: scores use
                                        softmax_scale / d; the backward returns
                                        dQ and dK rotated back by H_d            */
+#define FLAMIA_FLAG_DETERMINISTIC_DQ 0x8 /* backward only: the float32 dQ
+                                       partials of a query tile are added in
+                                       a fixed key-tile order, so dQ is the
+                                       same bit for bit on every run            */
 
 /*
  * One quantised operand, all device pointers owned by the caller.
@@ -227,8 +231,10 @@ flamia_status flamia_attn_fwd_gqa(const flamia_qtensor* q, const flamia_qtensor*
                                   void* stream);
 
 /*
- * Workspace of the backward: a float32 [T, H, d] dQ accumulator plus
- * alignment.  The caller allocates it; the backward clears it itself.
+ * Workspace of the backward: a float32 [T, H, d] dQ accumulator, then an
+ * int32 [T, H] array of turn counters (used by FLAMIA_FLAG_DETERMINISTIC_DQ),
+ * each part padded to 256 bytes.  The caller allocates it; the backward
+ * clears what it uses itself.
  */
 size_t flamia_bwd_workspace_bytes(int T, int H, int d);
 
@@ -248,6 +254,14 @@ size_t flamia_bwd_workspace_bytes(int T, int H, int d);
  * gradients of the rotated operands are rotated back before the BF16
  * conversion: dQ = dQ_r H_d, dK = dK_r H_d (float32 butterflies as in the
  * quantiser).
+ * FLAMIA_FLAG_DETERMINISTIC_DQ: by default the key tiles' dQ partials reach
+ * the float32 accumulator in whatever order the CTAs finish (the sum varies
+ * in its last bits from run to run).  With the flag, the 128-key tiles of a
+ * document add their partials to a query tile in descending order (a turn
+ * counter per query tile, bounded waits; each head's work items are claimed
+ * shortest first, so a key tile never waits for one claimed after it), and
+ * O, dQ, dK and dV are bitwise reproducible.  A wait that times out (2 s)
+ * sets FLAMIA_DEV_TIMEOUT.
  *
  *  dout         host pointer to the quantised dO (from the quantiser run with
  *               o_bf16 = the forward output, which also produced D).

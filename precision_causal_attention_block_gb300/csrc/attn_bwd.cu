@@ -329,6 +329,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // (never a barrier), so no thread can be left waiting at bar.sync.
     bool ok = true;
     int uc = 0;  // query tiles processed over all items (phase and buffer parity)
+    int* pend = nullptr;  // deterministic dQ: the turn the last reduce-adds pass on
     for (int n = 0;; ++n) {
       if (issuer) sm.item_bc[n & 1] = ring_get(sm.ring, n, true);
       named_barrier_sync(1, kComputeThreads);
@@ -507,7 +508,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ok = ok && !sm.abort && mbar_wait(smem_u32(&sm.bar_dq_full), uc & 1);
         tc_fence_after();
         // the previous tile's reduce-adds must have read the staging buffer
-        if (issuer) bulk_wait_group_read0();
+        // (and, in the deterministic mode, completed: their turn is passed on)
+        if (issuer) {
+          if (prm.dq_turns == nullptr) {
+            bulk_wait_group_read0();
+          } else {
+            bulk_wait_group0();
+            if (pend != nullptr) pass_turn(pend);
+            pend = nullptr;
+          }
+        }
         named_barrier_sync(1, kComputeThreads);
         if (ok) {
           const bool qv = q0 + j < e;  // TMEM lane j of dQ_u is query row j
@@ -541,11 +551,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (g == 0 && u + 1 < nq) store_query_inputs(uc + 1);
         named_barrier_sync(1, kComputeThreads);
         if (issuer && !sm.abort) {
+          int* turn = prm.dq_turns == nullptr
+                          ? nullptr
+                          : prm.dq_turns + static_cast<size_t>(q0) * prm.H + h;
+          if (turn != nullptr && !wait_turn(turn, dq_turn(prm, it, q0))) {
+            sm.abort = 1;
+          } else {
 #pragma unroll
-          for (int c = 0; c < DIM / 32; ++c)
-            tma_reduce_add_3d(&map_dq, smem_u32(sm.dqs[c]), 32 * c, h, q0);
-          bulk_commit_group();
+            for (int c = 0; c < DIM / 32; ++c)
+              tma_reduce_add_3d(&map_dq, smem_u32(sm.dqs[c]), 32 * c, h, q0);
+            bulk_commit_group();
+            pend = turn;
+          }
         }
+      }
+      if (issuer && pend != nullptr) {  // the item's last turn, before the next item
+        bulk_wait_group0();
+        pass_turn(pend);
+        pend = nullptr;
       }
       if (ok && prm.hadamard) {
         // Q and K were rotated: group 0 writes whole rows of dK = dK_r H_d
@@ -668,8 +691,9 @@ template <int DIM, bool NVF4>
 flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
                          const flamia_qtensor* v, const flamia_qtensor* dout, const float* D,
                          const float* lse, const int32_t* cu, int ndocs, int T, int H,
-                         int Hkv, float softmax_scale, bool had, bool causal, void* wl, void* dq,
-                         void* dk, void* dv, float* acc, int* status, cudaStream_t stream) {
+                         int Hkv, float softmax_scale, bool had, bool causal, bool det, void* wl,
+                         void* dq, void* dk, void* dv, float* acc, int* status,
+                         cudaStream_t stream) {
   CUtensorMap mq, mk, mv, mdo, mdq, mq4, mk4;
   const CUtensorMapSwizzle swz = swizzle_for_row_bytes(DIM);
   if (DIM == 64 && (!make_token_map(&mq, q->codes, T, H, DIM, kTile, swz) ||
@@ -713,7 +737,14 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
   prm.causal = causal ? 1 : 0;
   prm.status = status;
   const size_t n = static_cast<size_t>(T) * H * DIM;
-  if (cudaMemsetAsync(acc, 0, n * sizeof(float), stream) != cudaSuccess) return FLAMIA_ERR_CUDA;
+  prm.dq_turns = det ? reinterpret_cast<int*>(reinterpret_cast<char*>(acc) +
+                                              align_up(n * sizeof(float), 256))
+                     : nullptr;
+  // the accumulator and, in the deterministic mode, the turn counters behind it
+  const size_t zero_bytes =
+      det ? align_up(n * sizeof(float), 256) + static_cast<size_t>(T) * H * sizeof(int)
+          : n * sizeof(float);
+  if (cudaMemsetAsync(acc, 0, zero_bytes, stream) != cudaSuccess) return FLAMIA_ERR_CUDA;
   // persistent: one CTA per SM (shared memory allows one), items in snake order
   const long long grid = std::min<long long>(static_cast<long long>(L.cap_bwd) * Hkv, num_sms());
   if constexpr (DIM == 128 && !NVF4) {
@@ -754,7 +785,9 @@ using namespace flamia;
 
 extern "C" size_t flamia_bwd_workspace_bytes(int T, int H, int d) {
   if (T <= 0 || H <= 0 || !supported_dim(d)) return 0;
-  return align_up(static_cast<size_t>(T) * H * d * sizeof(float), 256);
+  // float32 dQ accumulator, then one int turn counter per (token, head)
+  return align_up(static_cast<size_t>(T) * H * d * sizeof(float), 256) +
+         align_up(static_cast<size_t>(T) * H * sizeof(int), 256);
 }
 
 extern "C" flamia_status flamia_attn_bwd_gqa(const flamia_qtensor* q, const flamia_qtensor* k,
@@ -767,9 +800,11 @@ extern "C" flamia_status flamia_attn_bwd_gqa(const flamia_qtensor* q, const flam
                                              int* dev_status, void* stream) {
   if (!supported_dim(d)) return FLAMIA_ERR_UNSUPPORTED;
   if (H_kv <= 0 || H <= 0 || H % H_kv != 0) return FLAMIA_ERR_INVALID_ARG;
-  if ((flags & ~(FLAMIA_FLAG_NVFP4_QK | FLAMIA_FLAG_HADAMARD | FLAMIA_FLAG_NONCAUSAL)) != 0)
+  if ((flags & ~(FLAMIA_FLAG_NVFP4_QK | FLAMIA_FLAG_HADAMARD | FLAMIA_FLAG_NONCAUSAL |
+                 FLAMIA_FLAG_DETERMINISTIC_DQ)) != 0)
     return FLAMIA_ERR_UNSUPPORTED;
   const bool nvf4 = (flags & FLAMIA_FLAG_NVFP4_QK) != 0;
+  const bool det = (flags & FLAMIA_FLAG_DETERMINISTIC_DQ) != 0;
   const bool had = (flags & FLAMIA_FLAG_HADAMARD) != 0;
   const bool causal = (flags & FLAMIA_FLAG_NONCAUSAL) == 0;
   if ((nvf4 && d != 64) || (nvf4 && had)) return FLAMIA_ERR_UNSUPPORTED;
@@ -794,12 +829,12 @@ extern "C" flamia_status flamia_attn_bwd_gqa(const flamia_qtensor* q, const flam
   const float sc = had ? softmax_scale / static_cast<float>(d) : softmax_scale;
   if (nvf4)
     return launch_bwd<64, true>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, H_kv, sc,
-                                false, causal, wl, dq_bf16, dk_bf16, dv_bf16, acc, dev_status, s);
+                                false, causal, det, wl, dq_bf16, dk_bf16, dv_bf16, acc, dev_status, s);
   return d == 128 ? launch_bwd<128, false>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, H_kv,
-                                           sc, had, causal, wl, dq_bf16, dk_bf16, dv_bf16, acc,
+                                           sc, had, causal, det, wl, dq_bf16, dk_bf16, dv_bf16, acc,
                                            dev_status, s)
                   : launch_bwd<64, false>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, H_kv,
-                                          sc, had, causal, wl, dq_bf16, dk_bf16, dv_bf16, acc,
+                                          sc, had, causal, det, wl, dq_bf16, dk_bf16, dv_bf16, acc,
                                           dev_status, s);
 }
 

@@ -61,6 +61,8 @@ struct Bwd128Smem {
   uint64_t bar_acc_full, bar_acc_empty, bar_done;
   ItemRing<4> ring;   // claimed items: producer -> MMA issuer, group leaders
   int item_bc[2][2];  // [group][item parity]: the leader's copy for its group
+  int pend[2];        // deterministic dQ: per group, the turn (index into the counters)
+                      // its last reduce-adds pass on once complete, or -1
   uint32_t tmem_base;
   volatile int abort;
 };
@@ -78,6 +80,8 @@ __device__ __forceinline__ int tile_q0(const BwdItem& it, int G, int nt, int v) 
   return it.qs + tile_u(G, nt, v) * kQT;
 }
 
+// DET: the deterministic dQ mode (ordered reduce-adds through prm.dq_turns).
+template <bool DET>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd128_kernel(const __grid_constant__ CUtensorMap map_q,
                        const __grid_constant__ CUtensorMap map_k,
@@ -115,6 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&sm.bar_done), 1);
     ring_init(sm.ring, 3);
     sm.abort = 0;
+    sm.pend[0] = sm.pend[1] = -1;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -417,8 +422,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4*>(dsrow + 16 * ch1) = make_uint4(dw[4], dw[5], dw[6], dw[7]);
           if (lane == 0) sm.eds[g][c][quad] = static_cast<uint32_t>(eb + 127);
         }
-        // the group's previous reduce-add has read the staging buffer
-        if (issuer) bulk_wait_group_read0();
+        // the group's previous reduce-add has read the staging buffer (and, in
+        // the deterministic mode, completed: its turn is passed on)
+        if (issuer) {
+          if (!DET) {
+            bulk_wait_group_read0();
+          } else {
+            bulk_wait_group0();
+            if (sm.pend[g] >= 0) pass_turn(prm.dq_turns + sm.pend[g]);
+            sm.pend[g] = -1;
+          }
+        }
         named_barrier_sync(bar_id, kGroupThreads);
         if (ok) {
           // block scales of the three products (the same words in every lane
@@ -487,13 +501,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) sm.abort = 1;
         named_barrier_sync(bar_id, kGroupThreads);
         if (issuer && !sm.abort) {
+          const int at = q0 * prm.H + h;
+          if (DET && !wait_turn(prm.dq_turns + at, dq_turn(prm, it, q0))) {
+            sm.abort = 1;
+          } else {
 #pragma unroll
-          for (int c = 0; c < kD / 32; ++c)
-            tma_reduce_add_3d(&map_dq, smem_u32(sm.dqs[g][c]), 32 * c, h, q0);
-          bulk_commit_group();
+            for (int c = 0; c < kD / 32; ++c)
+              tma_reduce_add_3d(&map_dq, smem_u32(sm.dqs[g][c]), 32 * c, h, q0);
+            bulk_commit_group();
+            if (DET) sm.pend[g] = at;
+          }
         }
       }
       ug += nq;
+      if (DET && issuer && sm.pend[g] >= 0) {  // the item's last turn
+        bulk_wait_group0();
+        pass_turn(prm.dq_turns + sm.pend[g]);
+        sm.pend[g] = -1;
+      }
       // dV = 2^-8 acc, dK = scale * acc; the groups split the head dimension
       ok = ok && !sm.abort && mbar_wait(smem_u32(&sm.bar_acc_full), nk & 1);
       tc_fence_after();
@@ -590,10 +615,11 @@ cudaError_t launch_bwd128_pipelined(const BwdParams& prm, const flamia_qtensor* 
       !make_f32_token_map(&mdq, acc, T, H, kD, kQT, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   const size_t smem = sizeof(Bwd128Smem) + 1024;
-  cudaError_t err = cudaFuncSetAttribute(
-      attn_bwd128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  auto kernel = prm.dq_turns != nullptr ? attn_bwd128_kernel<true> : attn_bwd128_kernel<false>;
+  cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  attn_bwd128_kernel<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mdo, mdq, prm);
+  kernel<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mdo, mdq, prm);
   return cudaGetLastError();
 }
 

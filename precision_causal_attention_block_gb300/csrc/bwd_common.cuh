@@ -31,6 +31,7 @@ struct BwdParams {
   float sm_scale;
   int hadamard;  // dK (and, in the conversion, dQ) rotated back by H_d
   int causal;    // 0: every query sees every key of its document
+  int* dq_turns;  // deterministic dQ: [T][H] turn counters (per tile's first query), else null
   int* status;
 };
 
@@ -89,7 +90,11 @@ __device__ __forceinline__ bool decode_bwd_item(const BwdParams& prm, int n_item
                                                 BwdItem& it) {
   const int T = prm.T;
   it.hk = idx / n_items;  // head-major: a wave of CTAs touches the Q / dO / dQ of few heads
-  const int4 item = prm.items[idx % n_items];
+  // each head's list longest first; in the deterministic dQ mode shortest
+  // first, so a document's key tiles are claimed in descending order, the
+  // order of their dQ turns (a turn never waits for an item claimed later)
+  const int pos = idx % n_items;
+  const int4 item = prm.items[prm.dq_turns != nullptr ? n_items - 1 - pos : pos];
   // clamped: a malformed work list or offsets cannot index outside [0, T)
   const int doc = min(max(item.x, 0), prm.ndocs - 1);
   it.s = min(max(prm.cu[doc], 0), T);
@@ -101,6 +106,15 @@ __device__ __forceinline__ bool decode_bwd_item(const BwdParams& prm, int n_item
   it.qs = prm.causal ? it.k0 : it.s;
   it.nq = (it.e - it.qs + kTile - 1) / kTile;
   return true;
+}
+
+// Deterministic dQ: the key tiles of a document add their partials to the
+// query tile starting at q0 in descending key-tile order, the order in which
+// their walks from the diagonal reach it; key tile r waits until the tiles
+// above it have added (causal: the tiles up to the one holding q0; else all).
+__device__ __forceinline__ int dq_turn(const BwdParams& prm, const BwdItem& it, int q0) {
+  const int top = prm.causal ? (q0 - it.s) / kTile : (it.e - it.s - 1) / kTile;
+  return top - (it.k0 - it.s) / kTile;
 }
 
 // Consumer roles of a backward kernel's item ring: the MMA issuer and one

@@ -217,6 +217,42 @@ __device__ __forceinline__ void bulk_wait_group0() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// ------------------------------------------------------- ordered dQ turns
+// In the deterministic dQ mode every 64- or 128-query tile of the float32 dQ
+// accumulator has a turn counter (zeroed before the backward): a key tile
+// adds its partial once the counter reads its turn (the number of key tiles
+// that add before it) and raises the counter by one once its reduce-adds
+// have completed, so the float32 sums run in one fixed order whatever the
+// CTAs' timing.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Bounded wait until *turn >= want (false after kWaitTimeoutNs); the async
+// proxy's later reduce-adds are ordered after the acquiring load.
+__device__ __forceinline__ bool wait_turn(const int* turn, int want) {
+  bool ok = ld_acquire_gpu(turn) >= want;
+  if (!ok) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!(ok = ld_acquire_gpu(turn) >= want)) {
+      if (globaltimer_ns() - t0 > kWaitTimeoutNs) break;
+      __nanosleep(32);
+    }
+  }
+  fence_proxy_async_global();
+  return ok;
+}
+// Passes the turn on: the caller's bulk reduce-adds have completed
+// (bulk_wait_group0), their writes are ordered before the releasing add.
+__device__ __forceinline__ void pass_turn(int* turn) {
+  fence_proxy_async_global();
+  asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(turn) : "memory");
+}
+
 // ------------------------------------------------------------------ tcgen05
 
 // Allocation and deallocation are warp-wide (.sync.aligned): call from one

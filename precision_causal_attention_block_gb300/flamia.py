@@ -22,6 +22,7 @@ FORMAT_HADAMARD = 0x10
 FLAG_NVFP4_QK = 0x1
 FLAG_HADAMARD = 0x2
 FLAG_NONCAUSAL = 0x4
+FLAG_DETERMINISTIC_DQ = 0x8
 DEV_BAD_SEQLENS = 0x1
 DEV_CAPACITY = 0x2
 DEV_TIMEOUT = 0x4
@@ -193,13 +194,15 @@ class TrainingCall:
     for fixed shapes.  All buffers are torch allocations owned by this object."""
 
     def __init__(self, T, H, d, cu_seqlens, softmax_scale, nvfp4_qk: bool = False,
-                 hadamard: bool = False, causal: bool = True, H_kv=None, device="cuda"):
+                 hadamard: bool = False, causal: bool = True, H_kv=None,
+                 deterministic_dq: bool = False, device="cuda"):
         self.T, self.H, self.d = T, H, d
         self.H_kv = H if H_kv is None else H_kv
         self.scale = softmax_scale
         self.cu = cu_seqlens
         self.flags = ((FLAG_NVFP4_QK if nvfp4_qk else 0) | (FLAG_HADAMARD if hadamard else 0) |
-                      (0 if causal else FLAG_NONCAUSAL))
+                      (0 if causal else FLAG_NONCAUSAL) |
+                      (FLAG_DETERMINISTIC_DQ if deterministic_dq else 0))
         self.fmt_qk = ((FORMAT_MXFP8_NVFP4 if nvfp4_qk else FORMAT_MXFP8) |
                        (FORMAT_HADAMARD if hadamard else 0))
         self.q = QTensor(T, H, d, nvfp4_qk, device)
