@@ -38,6 +38,10 @@ What it follows (citations name the page and its section):
   sum the contributions of its H / H_kv query heads.
 * same page, sec. 4.8 "Batched and non-causal paths": the non-causal packed
   call, where every query sees every key of its own document.
+* same page, sec. 3.2 "accumulator leakage" and sec. 3.5.3 "Backward
+  pass": dQ partial sums reduced in FP16 behind a power-of-two prescale set
+  from sequence-wide maxima, or ("causal dQ scaling") from the keys visible
+  to each query row.
 * same page, sec. 2 "A small example": the floor exponent rule
   e = floor(log2 amax) - emax with clipping at 448, used here only as the
   negative control of the leakage probe.
@@ -63,6 +67,10 @@ Readings where the pages are silent:
   normalises it is folded into the softmax scale (exact for d a power of
   two), and the backward returns dQ = dQ_r H_d, dK = dK_r H_d for the
   gradients dQ_r, dK_r of the rotated operands;
+* the FP16 dQ accumulator (an option; float32 is the default): prescale
+  2^p with p = 15 - ceil(log2(16 d 448^3)) - (e_dO + max e_V + max e_K), the
+  maxima sequence-wide or over the keys the row sees, key-tile partials
+  rounded to float32 then FP16 and added in FP16 (see dq_prescale);
 * work items: forward q0 = s + 256k, q1 = min(q0 + 256, e), cost =
   ceil((q1 - s) / 128); backward k0 = s + 128k, k1 = min(k0 + 128, e),
   cost = ceil((e - k0) / 128); stable sort by descending cost.
@@ -422,12 +430,13 @@ def _block_quantize_dS(dS: np.ndarray, r0: int, c0: int) -> np.ndarray:
 
 
 def bwd_rect(dh: DocHead, rows: np.ndarray, cols: np.ndarray, lse2_rows: np.ndarray,
-             D_rows: np.ndarray, sm_scale: float, quant: bool = True):
+             D_rows: np.ndarray, sm_scale: float, quant: bool = True, raw_dq: bool = False):
     """Backward contributions of the rectangle rows x cols.
 
     rows and cols are contiguous doc-local ranges starting on a 32 boundary.
     Returns (dQ partial [R, d] over these cols, dK partial [C, d] and dV
-    partial [C, d] over these rows, dS [R, C])."""
+    partial [C, d] over these rows, dS [R, C]); with raw_dq the dQ partial is
+    the product dS^ K^ before the softmax scale."""
     s = _scores(dh, rows, cols, sm_scale)
     P = np.exp2(s - lse2_rows[:, None])                        # normalised, 0 where masked
     pb = np.ldexp(P, P_SCALE_LOG2)
@@ -441,8 +450,86 @@ def bwd_rect(dh: DocHead, rows: np.ndarray, cols: np.ndarray, lse2_rows: np.ndar
     khat = dh.k[cols] * np.ldexp(1.0, dh.ek[cols])[:, None]
     dV = np.ldexp(pbh.T @ dohat, -P_SCALE_LOG2)
     dK = sm_scale * (dSh.T @ qhat)
-    dQ = sm_scale * (dSh @ khat)
+    dQ = (dSh @ khat) if raw_dq else sm_scale * (dSh @ khat)
     return dQ, dK, dV, dS
+
+
+# ----------------------------------------------------------------------------
+# FP16 dQ accumulation (precision option)
+# ----------------------------------------------------------------------------
+# Review page, sec. 3.2 "accumulator leakage" and sec. 3.5.3 "Backward pass":
+# the dQ partial sums of the key tiles are reduced in FP16 (half the traffic of
+# float32), pre-multiplied by a power of two that keeps them inside FP16's
+# range; by default the power comes from sequence-wide maxima of dO, V and K,
+# so a later token changes the rounding of earlier rows; "causal dQ scaling"
+# takes it from the keys each query row sees.
+# Reading: the magnitudes are the operands' block exponents (every element of
+# a block satisfies |x| <= 448 * 2^e), which bound the raw partial sums
+# rigorously and make the prescale an integer function of the scale tables:
+#   |sum_j dS^_ij K^_jk| <= 16 d 448^3 2^E,  E = e_dO(i) + max e_V + max e_K
+# (|dP_ij|, |D_i| <= d 448^2 2^(e_dO + max e_V) (1 + 2^-4 for O), P sums to 1,
+# RNE_E4M3 of dS adds at most 2^-4 relative plus half a subnormal step per
+# element, which the factor 16 covers up to 2^20 keys), and
+#   p(i) = 15 - ceil(log2(16 d 448^3)) - E   keeps |2^p acc| <= 2^15 < 65504.
+# The maxima run over the head's whole packed sequence ("sequence") or over
+# the keys the row sees ("causal": keys s .. i of its document, all of the
+# document in a non-causal call); p is clamped to [-126, 126].  The 128-key
+# tiles (from the document start) add their partials, rounded to float32 then
+# to FP16, to the FP16 accumulator in descending tile order (the deterministic
+# order; any other order is equally valid); dQ = softmax_scale 2^-p acc.
+
+DQ16_KEY_TILE = 128
+
+
+def dq16_bound_log2(d: int) -> int:
+    """ceil(log2(16 d 448^3)): the raw dQ bound is 2^(this + E)."""
+    return int(math.ceil(math.log2(16 * d * E4M3_MAX ** 3)))
+
+
+def dq_prescale(qz: "Quantized", h: int, mode: str, causal: bool = True) -> np.ndarray:
+    """Prescale exponents p [T] (int64) of query head h; mode "sequence" or
+    "causal" (see above)."""
+    T, H, d = qz.qc.shape
+    hk = h // (H // qz.kc.shape[1])
+    edo = qz.dos[h].astype(np.int64) - 127
+    ev = qz.vs[hk].astype(np.int64) - 127
+    ek = qz.ks[hk].astype(np.int64) - 127
+    if mode == "sequence":
+        E = np.full(T, edo.max() + ev.max() + ek.max() if T else 0, dtype=np.int64)
+    elif mode == "causal":
+        E = np.zeros(T, dtype=np.int64)
+        for b in range(len(qz.cu) - 1):
+            s, e = qz.cu[b], qz.cu[b + 1]
+            if e == s:
+                continue
+            if causal:
+                mv, mk = np.maximum.accumulate(ev[s:e]), np.maximum.accumulate(ek[s:e])
+            else:
+                mv, mk = ev[s:e].max(), ek[s:e].max()
+            E[s:e] = edo[s:e] + mv + mk
+    else:
+        raise ValueError(mode)
+    return np.clip(15 - dq16_bound_log2(d) - E, -126, 126)
+
+
+def fp16_round(x) -> np.ndarray:
+    """Round to the nearest FP16 value (ties to even), returned as float64."""
+    return np.asarray(x, dtype=np.float64).astype(np.float16).astype(np.float64)
+
+
+def dq_fp16_rows(dh: DocHead, rows: np.ndarray, lse2_rows: np.ndarray, D_rows: np.ndarray,
+                 sm_scale: float, p_rows: np.ndarray, return_acc: bool = False):
+    """dQ of the given rows (doc-local, from 0, a multiple-of-32 start)
+    through the prescaled FP16 accumulator."""
+    f = np.ldexp(1.0, np.asarray(p_rows, dtype=np.int64))[:, None]
+    acc = np.zeros((len(rows), dh.q.shape[1]))
+    for t0 in reversed(range(0, dh.L, DQ16_KEY_TILE)):
+        cols = np.arange(t0, min(t0 + DQ16_KEY_TILE, dh.L))
+        part, _, _, _ = bwd_rect(dh, rows, cols, lse2_rows, D_rows, sm_scale, True, raw_dq=True)
+        x = fp16_round((part * f).astype(np.float32))
+        acc = fp16_round(acc + x)                    # the sum of two FP16 values is exact here
+    dq = sm_scale * acc / f
+    return (dq, acc) if return_acc else dq
 
 
 # ----------------------------------------------------------------------------
@@ -491,7 +578,7 @@ def exact_dochead(q, k, v, do, cu, b, h) -> DocHead:
 def attention(q, k, v, do, cu_seqlens, sm_scale: float, quant: bool = True,
               qk_format: str = "mxfp8", rule: str = "up", group: str = "block",
               heads=None, docs=None, backward: bool = True, hadamard: bool = False,
-              causal: bool = True):
+              causal: bool = True, dq_accum: str = "fp32"):
     """Full forward (+ backward) over packed [T, H, d] float64 inputs.
 
     Returns a dict with O [T, H, d] (float64), O_bf16, lse [H, T] (natural log,
@@ -502,7 +589,10 @@ def attention(q, k, v, do, cu_seqlens, sm_scale: float, quant: bool = True,
     sm_scale / d, and dQ, dK are rotated back by H_d.  ``causal=False``: every
     query sees every key of its document.  k and v may have H_kv heads (H_kv
     dividing H): query head h then reads head h // (H / H_kv), and dK, dV
-    ([T, H_kv, d]) sum over the query heads of each K / V head."""
+    ([T, H_kv, d]) sum over the query heads of each K / V head.
+    ``dq_accum``: "fp32" (float32 sums, no prescale), "fp16_sequence" or
+    "fp16_causal" (the prescaled FP16 accumulator of dq_fp16_rows, with the
+    prescale table returned as ``dq_prescale`` [H, T])."""
     q = np.asarray(q, dtype=np.float64)
     T, H, d = q.shape
     Hkv = np.asarray(k).shape[1]
@@ -510,7 +600,8 @@ def attention(q, k, v, do, cu_seqlens, sm_scale: float, quant: bool = True,
     if hadamard:
         rot = hadamard_fp32 if quant else (lambda x: np.asarray(x, dtype=np.float64) @ sylvester(d))
         r = attention(rot(q), rot(k), v, do, cu_seqlens, sm_scale / d, quant, qk_format, rule,
-                      group, heads, docs, backward, hadamard=False, causal=causal)
+                      group, heads, docs, backward, hadamard=False, causal=causal,
+                      dq_accum=dq_accum)
         if backward:
             hd = sylvester(d)
             r["dQ"] = r["dQ"] @ hd
@@ -524,6 +615,13 @@ def attention(q, k, v, do, cu_seqlens, sm_scale: float, quant: bool = True,
     out.update({n: np.zeros((T, Hkv, d)) for n in ("dK", "dV")})
     out["lse"] = np.full((H, T), np.inf)
     out["D"] = np.zeros((H, T))
+    assert dq_accum in ("fp32", "fp16_sequence", "fp16_causal")
+    dq16 = backward and dq_accum != "fp32"
+    if dq16:
+        assert quant, "the FP16 accumulator belongs to the quantised method"
+        out["dq_prescale"] = np.zeros((H, T), dtype=np.int64)
+        for h in heads:
+            out["dq_prescale"][h] = dq_prescale(qz, h, dq_accum[5:], causal)
     for b in docs:
         s, e = cu[b], cu[b + 1]
         if e == s:
@@ -545,6 +643,8 @@ def attention(q, k, v, do, cu_seqlens, sm_scale: float, quant: bool = True,
             D = (dohat * o_for_D).sum(axis=1)
             out["D"][h, s:e] = D
             dQ, dK, dV, _ = bwd_rect(dh, rows, rows, lse2, D, sm_scale, quant)
+            if dq16:
+                dQ = dq_fp16_rows(dh, rows, lse2, D, sm_scale, out["dq_prescale"][h, s:e])
             hk = h // (H // Hkv)
             out["dQ"][s:e, h] = dQ
             out["dK"][s:e, hk] += dK
