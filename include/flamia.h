@@ -73,6 +73,11 @@ typedef enum {
                                        partials of a query tile are added in
                                        a fixed key-tile order, so dQ is the
                                        same bit for bit on every run            */
+#define FLAMIA_FLAG_DQ_FP16 0x10    /* backward only: dQ partials reduce-added
+                                       in FP16 behind a power-of-two prescale
+                                       from sequence-wide maxima                */
+#define FLAMIA_FLAG_DQ_CAUSAL_SCALE 0x20 /* with FLAMIA_FLAG_DQ_FP16: the prescale
+                                       of a query row from the keys it sees     */
 
 /*
  * One quantised operand, all device pointers owned by the caller.
@@ -231,10 +236,12 @@ flamia_status flamia_attn_fwd_gqa(const flamia_qtensor* q, const flamia_qtensor*
                                   void* stream);
 
 /*
- * Workspace of the backward: a float32 [T, H, d] dQ accumulator, then an
- * int32 [T, H] array of turn counters (used by FLAMIA_FLAG_DETERMINISTIC_DQ),
- * each part padded to 256 bytes.  The caller allocates it; the backward
- * clears what it uses itself.
+ * Workspace of the backward, each part padded to 256 bytes: a float32
+ * [T, H, d] dQ accumulator (FLAMIA_FLAG_DQ_FP16 uses its first half as an
+ * FP16 [T, H, d] one), an int32 [T, H] array of turn counters
+ * (FLAMIA_FLAG_DETERMINISTIC_DQ), the int8 [H, T] prescale exponents of the
+ * FP16 accumulator, and 3 H ints of scratch.  The caller allocates it; the
+ * backward clears what it uses itself.
  */
 size_t flamia_bwd_workspace_bytes(int T, int H, int d);
 
@@ -262,6 +269,17 @@ size_t flamia_bwd_workspace_bytes(int T, int H, int d);
  * shortest first, so a key tile never waits for one claimed after it), and
  * O, dQ, dK and dV are bitwise reproducible.  A wait that times out (2 s)
  * sets FLAMIA_DEV_TIMEOUT.
+ * FLAMIA_FLAG_DQ_FP16 (review page, sec. 3.2 "accumulator leakage", sec.
+ * 3.5.3: the FP16 dQ reduce that halves the reduction traffic): each key
+ * tile's float32 dQ partial of query row i is multiplied by 2^p(i), rounded
+ * to FP16 and reduce-added into an FP16 accumulator; dQ = softmax_scale *
+ * 2^-p(i) * acc.  p(i) = 15 - ceil(log2(16 d 448^3)) - (e_dO(i) + max e_V +
+ * max e_K), e the E8M0 block exponents (every element |x| <= 448 2^e), which
+ * bounds |2^p acc| by 2^15; clamped to [-126, 126].  The maxima run over
+ * the head's whole sequence, so a later token changes the rounding of
+ * earlier rows; with FLAMIA_FLAG_DQ_CAUSAL_SCALE they run over the keys the
+ * row sees (its document up to the row; the whole document in a non-causal
+ * call), which removes that dependence.  Combinable with every other flag.
  *
  *  dout         host pointer to the quantised dO (from the quantiser run with
  *               o_bf16 = the forward output, which also produced D).

@@ -63,6 +63,7 @@ struct BwdSmem {
   // loaded while the current one is processed)
   alignas(16) float nl[2][kTile];  // 8 - lse2 of each query column (-inf outside the document)
   alignas(16) float dd[2][kTile];  // D of each query column (0 outside)
+  alignas(16) float pf[2][kTile];  // FP16 dQ: prescale 2^p of each query (0 outside)
   uint32_t qbyte[2][4], dobyte[2][4];  // E8M0 bytes of the 4 query blocks of Q and dO
   uint32_t eds[4][4];            // dS block bytes [query block][key block]
   uint64_t bar_kv;
@@ -380,6 +381,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // addresses, issued a tile ahead and only used when stored
       float r_lse = 0.f, r_dd = 0.f;
       uint32_t r_qb = 127u, r_dob = 127u;
+      int r_pre = 0;
       bool r_qv = false;
       auto fetch_query_inputs = [&](int u) {
         const int qi = tile_q0(it, u) + j;
@@ -387,6 +389,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const size_t at = static_cast<size_t>(tile_head(it, u)) * T + min(qi, T - 1);
         r_lse = prm.lse[at];
         r_dd = prm.D[at];
+        if (prm.dq_pre != nullptr) r_pre = prm.dq_pre[at];
         if (lane == 0) {
           r_qb = prm.q_scales[at];
           r_dob = prm.do_scales[at];
@@ -396,6 +399,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int b = ug & 1;
         sm.nl[b][j] = r_qv ? 8.f - r_lse * LOG2E : -INFINITY;
         sm.dd[b][j] = r_qv ? r_dd : 0.f;
+        sm.pf[b][j] = r_qv ? exp2i(r_pre) : 0.f;
         if (lane == 0) {
           sm.qbyte[b][quad] = r_qv ? r_qb : 127u;
           sm.dobyte[b][quad] = r_qv ? r_dob : 127u;
@@ -530,8 +534,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           // dQ of the next tile may now be written
           tc_fence_before();
           mbar_arrive(smem_u32(&sm.bar_dq_read));
+          if (prm.dq_pre != nullptr) {
+            // x 2^p of the query row (0 outside the document), rounded to FP16,
+            // in DIM / 64 boxes [128 query rows][64 halves], 128B-swizzled
+            const float pf = sm.pf[ub][j];
+            __half* box0 = reinterpret_cast<__half*>(sm.dqs[0]);
 #pragma unroll
-          for (int cc = 0; cc < kCh; ++cc) {
+            for (int t = 0; t < 4 * kCh; ++t) {  // 8-dim chunk t of this group's dims
+              const int dim0 = g * 32 * kCh + 8 * t;
+              const int b = dim0 / 64, ch = (dim0 % 64) / 8;
+              uint32_t w[4];
+#pragma unroll
+              for (int x = 0; x < 4; ++x) {
+                const __half2 h2 = __floats2half2_rn(
+                    __uint_as_float(v[t / 4][8 * (t % 4) + 2 * x]) * pf,
+                    __uint_as_float(v[t / 4][8 * (t % 4) + 2 * x + 1]) * pf);
+                w[x] = *reinterpret_cast<const uint32_t*>(&h2);
+              }
+              *reinterpret_cast<uint4*>(box0 + b * (kTile * 64) + j * 64 + 8 * (ch ^ (j & 7))) =
+                  make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+#pragma unroll
+          for (int cc = 0; cc < kCh && prm.dq_pre == nullptr; ++cc) {
             float* row = sm.dqs[g * kCh + cc] + j * 32;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -557,9 +582,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (turn != nullptr && !wait_turn(turn, dq_turn(prm, it, q0))) {
             sm.abort = 1;
           } else {
+            if (prm.dq_pre != nullptr) {
+              const __half* box0 = reinterpret_cast<const __half*>(sm.dqs[0]);
 #pragma unroll
-            for (int c = 0; c < DIM / 32; ++c)
-              tma_reduce_add_3d(&map_dq, smem_u32(sm.dqs[c]), 32 * c, h, q0);
+              for (int b = 0; b < DIM / 64; ++b)
+                tma_reduce_add_3d(&map_dq, smem_u32(box0 + b * (kTile * 64)), 64 * b, h, q0);
+            } else {
+#pragma unroll
+              for (int c = 0; c < DIM / 32; ++c)
+                tma_reduce_add_3d(&map_dq, smem_u32(sm.dqs[c]), 32 * c, h, q0);
+            }
             bulk_commit_group();
             pend = turn;
           }
@@ -652,27 +684,168 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
-// float32 dQ accumulator (sums of dS K) -> BF16 dQ = softmax_scale * acc.
+// ------------------------------------------------- FP16 dQ accumulator prescale
+// Review page, sec. 3.2 "accumulator leakage", sec. 3.5.3 "Backward pass": the
+// key tiles' dQ partials are reduce-added in FP16 after multiplication by
+// 2^p(i).  Every element of a 32-token block satisfies |x| <= 448 2^e (its
+// E8M0 exponent), which bounds the raw sum: |sum_j dS^_ij K^_jk| <=
+// 16 d 448^3 2^E with E = e_dO(i) + max e_V + max e_K, so
+//   p(i) = 15 - ceil(log2(16 d 448^3)) - E   (clamped to [-126, 126])
+// keeps |2^p acc| <= 2^15.  The maxima run over the head's whole sequence
+// (FLAMIA_FLAG_DQ_FP16) or, with causal dQ scaling, over the keys the row sees.
+__host__ __device__ constexpr int dq16_bound_log2(int d) { return d == 128 ? 38 : 37; }
+
+__device__ __forceinline__ int8_t dq16_prescale(int e_sum_bytes, int cbound) {
+  const int E = e_sum_bytes - 3 * 127;  // three E8M0 bytes
+  return static_cast<int8_t>(min(max(15 - cbound - E, -126), 126));
+}
+
+// Per row of the E8M0 tables, the largest byte: rows 0 .. H-1 dO (query
+// heads), H .. H+Hkv-1 V, H+Hkv .. H+2Hkv-1 K; maxb zeroed by the caller.
+__global__ void scale_max_kernel(const uint8_t* __restrict__ dos, const uint8_t* __restrict__ vs,
+                                 const uint8_t* __restrict__ ks, int T, int H, int Hkv,
+                                 int* __restrict__ maxb) {
+  const int r = blockIdx.y;
+  const uint8_t* row = r < H ? dos + static_cast<size_t>(r) * T
+                       : r < H + Hkv ? vs + static_cast<size_t>(r - H) * T
+                                     : ks + static_cast<size_t>(r - H - Hkv) * T;
+  int m = 0;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < T; i += gridDim.x * blockDim.x)
+    m = max(m, static_cast<int>(row[i]));
+  m = __reduce_max_sync(0xffffffffu, m);
+  if ((threadIdx.x & 31) == 0 && m > 0) atomicMax(maxb + r, m);
+}
+
+// Sequence-wide prescale: one value per query head, written for every token.
+__global__ void dq_prescale_seq_kernel(const int* __restrict__ maxb, int T, int H, int Hkv,
+                                       int cbound, int8_t* __restrict__ pre) {
+  const int G = H / Hkv;
+  const size_t n = static_cast<size_t>(T) * H;
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const int h = static_cast<int>(i / T), hk = h / G;
+    pre[i] = dq16_prescale(maxb[h] + maxb[H + hk] + maxb[H + Hkv + hk], cbound);
+  }
+}
+
+// Causal dQ scaling: one warp per (document, query head) walks the
+// document's 32-token blocks 32 at a time (lane = block): running maxima of
+// the V and K bytes (inclusive prefix over the lanes, plus the carry of the
+// earlier blocks), or the document maxima in a non-causal call, then writes
+// the block's prescale to its tokens.
+__global__ void dq_prescale_causal_kernel(const uint8_t* __restrict__ dos,
+                                          const uint8_t* __restrict__ vs,
+                                          const uint8_t* __restrict__ ks,
+                                          const int32_t* __restrict__ cu, int ndocs, int T, int H,
+                                          int Hkv, int cbound, int causal,
+                                          int8_t* __restrict__ pre) {
+  const int lane = threadIdx.x & 31;
+  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  for (long long w = blockIdx.x * static_cast<long long>(blockDim.x >> 5) + (threadIdx.x >> 5);
+       w < static_cast<long long>(ndocs) * H; w += warps) {
+    const int doc = static_cast<int>(w / H), h = static_cast<int>(w % H), hk = h / (H / Hkv);
+    const int s = min(max(cu[doc], 0), T), e = min(max(cu[doc + 1], s), T);
+    const int nb = (e - s + 31) / 32;
+    const uint8_t* dr = dos + static_cast<size_t>(h) * T;
+    const uint8_t* vr = vs + static_cast<size_t>(hk) * T;
+    const uint8_t* kr = ks + static_cast<size_t>(hk) * T;
+    int mv = 0, mk = 0;  // carries (E8M0 bytes are >= 0)
+    if (!causal) {
+      for (int b = lane; b < nb; b += 32) {
+        mv = max(mv, static_cast<int>(vr[s + 32 * b]));
+        mk = max(mk, static_cast<int>(kr[s + 32 * b]));
+      }
+      mv = __reduce_max_sync(0xffffffffu, mv);
+      mk = __reduce_max_sync(0xffffffffu, mk);
+    }
+    for (int b0 = 0; b0 < nb; b0 += 32) {
+      const int b = b0 + lane;
+      int ev = 0, ek = 0, ed = 0;
+      if (b < nb) {
+        ev = vr[s + 32 * b];
+        ek = kr[s + 32 * b];
+        ed = dr[s + 32 * b];
+      }
+      if (causal) {
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int yv = __shfl_up_sync(0xffffffffu, ev, off);
+          const int yk = __shfl_up_sync(0xffffffffu, ek, off);
+          if (lane >= off) {
+            ev = max(ev, yv);
+            ek = max(ek, yk);
+          }
+        }
+        ev = max(ev, mv);
+        ek = max(ek, mk);
+        mv = __shfl_sync(0xffffffffu, ev, 31);
+        mk = __shfl_sync(0xffffffffu, ek, 31);
+      } else {
+        ev = mv;
+        ek = mk;
+      }
+      const int p = dq16_prescale(ed + ev + ek, cbound);
+      const int nblk = min(32, nb - b0);
+      for (int t = 0; t < nblk; ++t) {
+        const int pt = __shfl_sync(0xffffffffu, p, t);
+        const int tok = s + 32 * (b0 + t) + lane;
+        if (tok < e) pre[static_cast<size_t>(h) * T + tok] = static_cast<int8_t>(pt);
+      }
+    }
+  }
+}
+
+// dQ accumulator -> BF16 dQ = softmax_scale * acc (float32), or
+// softmax_scale * 2^-p * acc (FP16, p of the row).
 // dQ = (sm_scale acc) H_d, one warp per (token, head) row: lane l holds the
 // DIM/32 consecutive elements [DIM/32 l, DIM/32 (l + 1)).
 template <int DIM>
 __global__ void dq_convert_rotate_kernel(const float* __restrict__ acc,
                                          __nv_bfloat16* __restrict__ out, size_t rows,
-                                         float sm_scale) {
+                                         float sm_scale, const int8_t* __restrict__ pre, int T,
+                                         int H) {
   constexpr int N = DIM / 32;
   const int lane = threadIdx.x & 31;
   const size_t warps = static_cast<size_t>(gridDim.x) * (blockDim.x >> 5);
   for (size_t r = blockIdx.x * static_cast<size_t>(blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
        r += warps) {
     float v[N];
-    const float* src = acc + r * DIM + N * lane;
+    if (pre == nullptr) {
+      const float* src = acc + r * DIM + N * lane;
 #pragma unroll
-    for (int i = 0; i < N; ++i) v[i] = src[i] * sm_scale;
+      for (int i = 0; i < N; ++i) v[i] = src[i] * sm_scale;
+    } else {
+      const __half* src = reinterpret_cast<const __half*>(acc) + r * DIM + N * lane;
+      const float f = exp2i(-pre[(r % H) * T + r / H]);
+#pragma unroll
+      for (int i = 0; i < N; ++i) v[i] = (__half2float(src[i]) * f) * sm_scale;
+    }
     fwht_row<N, 32>(v, lane);
     __nv_bfloat16* dst = out + r * DIM + N * lane;
 #pragma unroll
     for (int i = 0; i < N; i += 2)
       *reinterpret_cast<__nv_bfloat162*>(dst + i) = __floats2bfloat162_rn(v[i], v[i + 1]);
+  }
+}
+
+// FP16 accumulator: 8 elements of one row per thread.
+__global__ void dq16_convert_kernel(const uint4* __restrict__ acc, uint4* __restrict__ out,
+                                    size_t n8, int d, int T, int H, float sm_scale,
+                                    const int8_t* __restrict__ pre) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n8;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t r = i * 8 / d;  // (token, head) row
+    const float f = exp2i(-pre[(r % H) * T + r / H]);
+    const uint4 a = acc[i];
+    const uint32_t in[4] = {a.x, a.y, a.z, a.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&in[x]));
+      const __nv_bfloat162 b2 = __floats2bfloat162_rn((v.x * f) * sm_scale, (v.y * f) * sm_scale);
+      o[x] = *reinterpret_cast<const uint32_t*>(&b2);
+    }
+    out[i] = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
@@ -687,20 +860,39 @@ __global__ void dq_convert_kernel(const float4* __restrict__ acc, uint2* __restr
   }
 }
 
+// Backward workspace: float32 [T, H, d] dQ accumulator (the FP16 one uses its
+// first half), int32 [T, H] turn counters, int8 [H, T] prescale table, the
+// per-row byte maxima (H + 2 H_kv <= 3 H ints); each part 256-byte aligned.
+struct BwdWorkspace {
+  size_t off_turns, off_pre, off_max, total;
+};
+inline BwdWorkspace bwd_workspace(int T, int H, int d) {
+  const size_t th = static_cast<size_t>(T) * H;
+  BwdWorkspace w;
+  w.off_turns = align_up(th * d * sizeof(float), 256);
+  w.off_pre = w.off_turns + align_up(th * sizeof(int), 256);
+  w.off_max = w.off_pre + align_up(th, 256);
+  w.total = w.off_max + align_up(3ull * H * sizeof(int), 256);
+  return w;
+}
+
 template <int DIM, bool NVF4>
 flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
                          const flamia_qtensor* v, const flamia_qtensor* dout, const float* D,
                          const float* lse, const int32_t* cu, int ndocs, int T, int H,
-                         int Hkv, float softmax_scale, bool had, bool causal, bool det, void* wl,
-                         void* dq, void* dk, void* dv, float* acc, int* status,
+                         int Hkv, float softmax_scale, bool had, bool causal, bool det, int dq16,
+                         void* wl, void* dq, void* dk, void* dv, void* ws, int* status,
                          cudaStream_t stream) {
   CUtensorMap mq, mk, mv, mdo, mdq, mq4, mk4;
   const CUtensorMapSwizzle swz = swizzle_for_row_bytes(DIM);
+  const BwdWorkspace W = bwd_workspace(T, H, DIM);
+  float* acc = static_cast<float*>(ws);
   if (DIM == 64 && (!make_token_map(&mq, q->codes, T, H, DIM, kTile, swz) ||
       !make_token_map(&mk, k->codes, T, Hkv, DIM, kTile, swz) ||
       !make_token_map(&mv, v->codes, T, Hkv, DIM, kTile, swz) ||
       !make_token_map(&mdo, dout->codes, T, H, DIM, kTile, swz) ||
-      !make_f32_token_map(&mdq, acc, T, H, DIM, kTile)))
+      !(dq16 ? make_f16_token_map(&mdq, acc, T, H, DIM, kTile, CU_TENSOR_MAP_SWIZZLE_128B)
+             : make_f32_token_map(&mdq, acc, T, H, DIM, kTile))))
     return FLAMIA_ERR_CUDA;
   if (NVF4) {
     if (!make_token_map(&mq4, q->nvfp4_codes, T, H, DIM / 2, kTile, CU_TENSOR_MAP_SWIZZLE_32B) ||
@@ -737,14 +929,36 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
   prm.causal = causal ? 1 : 0;
   prm.status = status;
   const size_t n = static_cast<size_t>(T) * H * DIM;
-  prm.dq_turns = det ? reinterpret_cast<int*>(reinterpret_cast<char*>(acc) +
-                                              align_up(n * sizeof(float), 256))
-                     : nullptr;
-  // the accumulator and, in the deterministic mode, the turn counters behind it
-  const size_t zero_bytes =
-      det ? align_up(n * sizeof(float), 256) + static_cast<size_t>(T) * H * sizeof(int)
-          : n * sizeof(float);
-  if (cudaMemsetAsync(acc, 0, zero_bytes, stream) != cudaSuccess) return FLAMIA_ERR_CUDA;
+  char* wsb = static_cast<char*>(ws);
+  prm.dq_turns = det ? reinterpret_cast<int*>(wsb + W.off_turns) : nullptr;
+  int8_t* pre = dq16 ? reinterpret_cast<int8_t*>(wsb + W.off_pre) : nullptr;
+  prm.dq_pre = pre;
+  // the accumulator (float32 or FP16) and, in the deterministic mode, the
+  // turn counters behind it
+  if (cudaMemsetAsync(acc, 0, n * (dq16 ? 2 : 4), stream) != cudaSuccess ||
+      (det && cudaMemsetAsync(wsb + W.off_turns, 0, static_cast<size_t>(T) * H * sizeof(int),
+                              stream) != cudaSuccess))
+    return FLAMIA_ERR_CUDA;
+  if (dq16) {  // the prescale table
+    const int cb = dq16_bound_log2(DIM);
+    if (dq16 == 1) {
+      int* maxb = reinterpret_cast<int*>(wsb + W.off_max);
+      if (cudaMemsetAsync(maxb, 0, sizeof(int) * (H + 2 * Hkv), stream) != cudaSuccess)
+        return FLAMIA_ERR_CUDA;
+      const dim3 g(static_cast<unsigned>(std::min(64, (T + 255) / 256)), H + 2 * Hkv);
+      scale_max_kernel<<<g, 256, 0, stream>>>(dout->scales, v->scales, k->scales, T, H, Hkv, maxb);
+      const size_t nb = static_cast<size_t>(T) * H;
+      const int blocks = static_cast<int>(std::min<size_t>((nb + 255) / 256, 152 * 8));
+      dq_prescale_seq_kernel<<<blocks, 256, 0, stream>>>(maxb, T, H, Hkv, cb, pre);
+    } else {
+      const long long pairs = static_cast<long long>(ndocs) * H;
+      const int blocks = static_cast<int>(std::min<long long>((pairs + 7) / 8, 152 * 8));
+      dq_prescale_causal_kernel<<<blocks, 256, 0, stream>>>(dout->scales, v->scales, k->scales,
+                                                             cu, ndocs, T, H, Hkv, cb,
+                                                             causal ? 1 : 0, pre);
+    }
+    if (cudaGetLastError() != cudaSuccess) return FLAMIA_ERR_CUDA;
+  }
   // persistent: one CTA per SM (shared memory allows one), items in snake order
   const long long grid = std::min<long long>(static_cast<long long>(L.cap_bwd) * Hkv, num_sms());
   if constexpr (DIM == 128 && !NVF4) {
@@ -762,13 +976,21 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
     if (cudaGetLastError() != cudaSuccess) return FLAMIA_ERR_CUDA;
   }
   if (launch_bwd_short(q, k, v, dout, D, lse, cu, ndocs, T, H, Hkv, DIM, softmax_scale, NVF4, had,
-                       causal, acc, dk, dv, stream) != cudaSuccess)
+                       causal, acc, pre, dk, dv, stream) != cudaSuccess)
     return FLAMIA_ERR_CUDA;
   if (had) {
     const size_t rows = static_cast<size_t>(T) * H;
     const int blocks = static_cast<int>(std::min<size_t>((rows + 7) / 8, 152 * 16));
     dq_convert_rotate_kernel<DIM><<<blocks, 256, 0, stream>>>(
-        acc, static_cast<__nv_bfloat16*>(dq), rows, softmax_scale);
+        acc, static_cast<__nv_bfloat16*>(dq), rows, softmax_scale, pre, T, H);
+    return cudaGetLastError() == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
+  }
+  if (dq16) {
+    const size_t n8 = n / 8;
+    const int blocks = static_cast<int>(std::min<size_t>((n8 + 255) / 256, 152 * 16));
+    dq16_convert_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const uint4*>(acc),
+                                                    static_cast<uint4*>(dq), n8, DIM, T, H,
+                                                    softmax_scale, pre);
     return cudaGetLastError() == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
   }
   const size_t n4 = n / 4;
@@ -785,9 +1007,7 @@ using namespace flamia;
 
 extern "C" size_t flamia_bwd_workspace_bytes(int T, int H, int d) {
   if (T <= 0 || H <= 0 || !supported_dim(d)) return 0;
-  // float32 dQ accumulator, then one int turn counter per (token, head)
-  return align_up(static_cast<size_t>(T) * H * d * sizeof(float), 256) +
-         align_up(static_cast<size_t>(T) * H * sizeof(int), 256);
+  return bwd_workspace(T, H, d).total;
 }
 
 extern "C" flamia_status flamia_attn_bwd_gqa(const flamia_qtensor* q, const flamia_qtensor* k,
@@ -801,10 +1021,15 @@ extern "C" flamia_status flamia_attn_bwd_gqa(const flamia_qtensor* q, const flam
   if (!supported_dim(d)) return FLAMIA_ERR_UNSUPPORTED;
   if (H_kv <= 0 || H <= 0 || H % H_kv != 0) return FLAMIA_ERR_INVALID_ARG;
   if ((flags & ~(FLAMIA_FLAG_NVFP4_QK | FLAMIA_FLAG_HADAMARD | FLAMIA_FLAG_NONCAUSAL |
-                 FLAMIA_FLAG_DETERMINISTIC_DQ)) != 0)
+                 FLAMIA_FLAG_DETERMINISTIC_DQ | FLAMIA_FLAG_DQ_FP16 |
+                 FLAMIA_FLAG_DQ_CAUSAL_SCALE)) != 0)
+    return FLAMIA_ERR_UNSUPPORTED;
+  if ((flags & FLAMIA_FLAG_DQ_CAUSAL_SCALE) && !(flags & FLAMIA_FLAG_DQ_FP16))
     return FLAMIA_ERR_UNSUPPORTED;
   const bool nvf4 = (flags & FLAMIA_FLAG_NVFP4_QK) != 0;
   const bool det = (flags & FLAMIA_FLAG_DETERMINISTIC_DQ) != 0;
+  const int dq16 = !(flags & FLAMIA_FLAG_DQ_FP16) ? 0
+                   : (flags & FLAMIA_FLAG_DQ_CAUSAL_SCALE) ? 2 : 1;
   const bool had = (flags & FLAMIA_FLAG_HADAMARD) != 0;
   const bool causal = (flags & FLAMIA_FLAG_NONCAUSAL) == 0;
   if ((nvf4 && d != 64) || (nvf4 && had)) return FLAMIA_ERR_UNSUPPORTED;
@@ -824,18 +1049,18 @@ extern "C" flamia_status flamia_attn_bwd_gqa(const flamia_qtensor* q, const flam
                !aligned(q->nvfp4_scales, 4) || !aligned(k->nvfp4_scales, 4)))
     return FLAMIA_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  float* acc = static_cast<float*>(ws);
   // rotated Q, K: the same scores with softmax_scale / d (exact: d = 2^k)
   const float sc = had ? softmax_scale / static_cast<float>(d) : softmax_scale;
   if (nvf4)
     return launch_bwd<64, true>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, H_kv, sc,
-                                false, causal, det, wl, dq_bf16, dk_bf16, dv_bf16, acc, dev_status, s);
+                                false, causal, det, dq16, wl, dq_bf16, dk_bf16, dv_bf16, ws,
+                                dev_status, s);
   return d == 128 ? launch_bwd<128, false>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, H_kv,
-                                           sc, had, causal, det, wl, dq_bf16, dk_bf16, dv_bf16, acc,
-                                           dev_status, s)
+                                           sc, had, causal, det, dq16, wl, dq_bf16, dk_bf16,
+                                           dv_bf16, ws, dev_status, s)
                   : launch_bwd<64, false>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, H_kv,
-                                          sc, had, causal, det, wl, dq_bf16, dk_bf16, dv_bf16, acc,
-                                          dev_status, s);
+                                          sc, had, causal, det, dq16, wl, dq_bf16, dk_bf16,
+                                          dv_bf16, ws, dev_status, s);
 }
 
 extern "C" flamia_status flamia_attn_bwd(const flamia_qtensor* q, const flamia_qtensor* k,

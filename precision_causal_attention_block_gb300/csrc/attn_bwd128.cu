@@ -53,6 +53,7 @@ struct Bwd128Smem {
   // per-query inputs of a group's tile, double-buffered by the group's tile count
   alignas(16) float nl[2][2][kQT];                 // 8 - lse2 (-inf outside the document)
   alignas(16) float dd[2][2][kQT];                 // D (0 outside)
+  alignas(16) float pf[2][2][kQT];                 // FP16 dQ: prescale 2^p (0 outside)
   uint32_t qbyte[2][2][2], dobyte[2][2][2];        // [group][buffer][query block]
   uint32_t eds[2][2][4];                           // [group][query block][key block]
   uint64_t bar_kv, bar_kv_free;
@@ -81,7 +82,8 @@ __device__ __forceinline__ int tile_q0(const BwdItem& it, int G, int nt, int v) 
 }
 
 // DET: the deterministic dQ mode (ordered reduce-adds through prm.dq_turns).
-template <bool DET>
+// F16: the prescaled FP16 dQ accumulator (prm.dq_pre), else float32.
+template <bool DET, bool F16>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd128_kernel(const __grid_constant__ CUtensorMap map_q,
                        const __grid_constant__ CUtensorMap map_k,
@@ -312,6 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // latency hides behind the tile's work
     float r_lse = 0.f, r_dd = 0.f;
     uint32_t r_qb = 127u, r_dob = 127u;
+    int r_pre = 0;
     bool r_qv = false;
     auto fetch_inputs = [&](size_t hT, int q0, int e) {
       if (quad < 2) {
@@ -320,6 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const size_t at = hT + min(qi, T - 1);
         r_lse = prm.lse[at];
         r_dd = prm.D[at];
+        if (F16) r_pre = prm.dq_pre[at];
       } else if (lane == 0) {
         const int qi = q0 + 32 * (quad - 2);
         r_qv = qi < e;
@@ -332,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (quad < 2) {
         sm.nl[g][buf][j] = r_qv ? 8.f - r_lse * LOG2E : -INFINITY;
         sm.dd[g][buf][j] = r_qv ? r_dd : 0.f;
+        if (F16) sm.pf[g][buf][j] = r_qv ? exp2i(r_pre) : 0.f;
       } else if (lane == 0) {
         sm.qbyte[g][buf][quad - 2] = r_qv ? r_qb : 127u;
         sm.dobyte[g][buf][quad - 2] = r_qv ? r_dob : 127u;
@@ -483,7 +488,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           // raw sums of dS K (softmax_scale is applied in the BF16 conversion)
           const int nvalid = min(kQT, e - q0);  // queries of other documents add 0
           float* stg = sm.dqs[g][quad] + lane;  // row = query, element = this dim
-          if (nvalid == kQT) {
+          if (F16) {
+            // x 2^p of the query (0 outside the document), rounded to FP16, in
+            // two boxes [query][64 dims]
+            const float4* pf4 = reinterpret_cast<const float4*>(sm.pf[g][buf]);
+            __half* st16 = reinterpret_cast<__half*>(sm.dqs[g][0]) + (quad >> 1) * (kQT * 64) +
+                           (quad & 1) * 32 + lane;
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4) {
+              const float4 fa = pf4[c4], fb = pf4[c4 + 8];  // queries 4 c4 + x, 32 + 4 c4 + x
+              const float ma[4] = {fa.x, fa.y, fa.z, fa.w}, mb[4] = {fb.x, fb.y, fb.z, fb.w};
+#pragma unroll
+              for (int x = 0; x < 4; ++x) {
+                const int c = 4 * c4 + x;
+                const __half2 h2 = __floats2half2_rn(__uint_as_float(v0[c]) * ma[x],
+                                                     __uint_as_float(v1[c]) * mb[x]);
+                st16[c * 64] = __low2half(h2);
+                st16[(c + 32) * 64] = __high2half(h2);
+              }
+            }
+          } else if (nvalid == kQT) {
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
               stg[c * 32] = __uint_as_float(v0[c]);
@@ -505,9 +529,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (DET && !wait_turn(prm.dq_turns + at, dq_turn(prm, it, q0))) {
             sm.abort = 1;
           } else {
+            if (F16) {
+              const __half* st16 = reinterpret_cast<const __half*>(sm.dqs[g][0]);
 #pragma unroll
-            for (int c = 0; c < kD / 32; ++c)
-              tma_reduce_add_3d(&map_dq, smem_u32(sm.dqs[g][c]), 32 * c, h, q0);
+              for (int b = 0; b < kD / 64; ++b)
+                tma_reduce_add_3d(&map_dq, smem_u32(st16 + b * (kQT * 64)), 64 * b, h, q0);
+            } else {
+#pragma unroll
+              for (int c = 0; c < kD / 32; ++c)
+                tma_reduce_add_3d(&map_dq, smem_u32(sm.dqs[g][c]), 32 * c, h, q0);
+            }
             bulk_commit_group();
             if (DET) sm.pend[g] = at;
           }
@@ -611,11 +642,15 @@ cudaError_t launch_bwd128_pipelined(const BwdParams& prm, const flamia_qtensor* 
   if (!make_token_map(&mq, q->codes, T, H, kD, kQT, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_token_map(&mk, k->codes, T, prm.Hkv, kD, kTile, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_token_map(&mv, v->codes, T, prm.Hkv, kD, kTile, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_token_map(&mdo, dout->codes, T, H, kD, kQT, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_f32_token_map(&mdq, acc, T, H, kD, kQT, CU_TENSOR_MAP_SWIZZLE_NONE))
+      !make_token_map(&mdo, dout->codes, T, H, kD, kQT, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  const bool f16 = prm.dq_pre != nullptr, det = prm.dq_turns != nullptr;
+  if (f16 ? !make_f16_token_map(&mdq, acc, T, H, kD, kQT, CU_TENSOR_MAP_SWIZZLE_NONE)
+          : !make_f32_token_map(&mdq, acc, T, H, kD, kQT, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   const size_t smem = sizeof(Bwd128Smem) + 1024;
-  auto kernel = prm.dq_turns != nullptr ? attn_bwd128_kernel<true> : attn_bwd128_kernel<false>;
+  auto kernel = det ? (f16 ? attn_bwd128_kernel<true, true> : attn_bwd128_kernel<true, false>)
+                    : (f16 ? attn_bwd128_kernel<false, true> : attn_bwd128_kernel<false, false>);
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;

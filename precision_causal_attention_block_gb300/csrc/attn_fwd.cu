@@ -685,10 +685,11 @@ extern "C" flamia_status flamia_attn_fwd_gqa(const flamia_qtensor* q, const flam
                                              void* stream) {
   if (!supported_dim(d)) return FLAMIA_ERR_UNSUPPORTED;
   if (H_kv <= 0 || H <= 0 || H % H_kv != 0) return FLAMIA_ERR_INVALID_ARG;
-  // FLAMIA_FLAG_DETERMINISTIC_DQ is accepted and has nothing to do here: every
-  // output row of the forward is written by one CTA
+  // the backward's dQ options are accepted and have nothing to do here (every
+  // output row of the forward is written by one CTA)
   if ((flags & ~(FLAMIA_FLAG_NVFP4_QK | FLAMIA_FLAG_HADAMARD | FLAMIA_FLAG_NONCAUSAL |
-                 FLAMIA_FLAG_DETERMINISTIC_DQ)) != 0)
+                 FLAMIA_FLAG_DETERMINISTIC_DQ | FLAMIA_FLAG_DQ_FP16 |
+                 FLAMIA_FLAG_DQ_CAUSAL_SCALE)) != 0)
     return FLAMIA_ERR_UNSUPPORTED;
   const bool nvf4 = (flags & FLAMIA_FLAG_NVFP4_QK) != 0;
   const bool causal = (flags & FLAMIA_FLAG_NONCAUSAL) == 0;

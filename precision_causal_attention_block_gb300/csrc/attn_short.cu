@@ -35,6 +35,7 @@ struct ShortParams {
   // backward
   const float *lse_in, *D;
   float* dq_acc;  // float32 [T, H, d]: dS K sums (softmax_scale comes in the conversion)
+  const int8_t* dq_pre;  // FP16 accumulator: prescale exponents [H, T] (else null: float32)
   __nv_bfloat16 *dk, *dv;
   int hadamard;  // dK rotated back by H_d (Q and K were quantised rotated)
   int causal;    // 0: every query sees every key of its document
@@ -243,9 +244,17 @@ __global__ void __launch_bounds__(32 * kShortWarps)
         for (int c = 0; c < N; ++c) acc[c] = fmaf(dsh, k[c], acc[c]);
       }
       const float mul = pow2_or_zero_s(ek);  // softmax_scale: in the BF16 conversion
-      float* dst = prm.dq_acc + (static_cast<size_t>(s + i) * H + h) * DIM + N * lane;
+      const size_t at = (static_cast<size_t>(s + i) * H + h) * DIM + N * lane;
+      if (prm.dq_pre == nullptr) {
+        float* dst = prm.dq_acc + at;
 #pragma unroll
-      for (int c = 0; c < N; ++c) dst[c] = acc[c] * mul;
+        for (int c = 0; c < N; ++c) dst[c] = acc[c] * mul;
+      } else {  // the document's one key tile: its prescaled sum is the FP16 row
+        const float pre = exp2i(prm.dq_pre[hT + s + i]);
+        __half* dst = reinterpret_cast<__half*>(prm.dq_acc) + at;
+#pragma unroll
+        for (int c = 0; c < N; ++c) dst[c] = __float2half_rn((acc[c] * mul) * pre);
+      }
     }
     // dK_j = scale * sum_i dS^_ij Q^_i,  dV_j = 2^-8 sum_i P^b_ij dO^_i
     for (int j = 0; j < L; ++j) {
@@ -351,7 +360,8 @@ cudaError_t launch_bwd_short(const flamia_qtensor* q, const flamia_qtensor* k,
                              const flamia_qtensor* v, const flamia_qtensor* dout, const float* D,
                              const float* lse, const int32_t* cu, int ndocs, int T, int H,
                              int Hkv, int d, float softmax_scale, bool nvfp4_qk, bool hadamard,
-                             bool causal, float* dq_acc, void* dk, void* dv, cudaStream_t stream) {
+                             bool causal, float* dq_acc, const int8_t* dq_pre, void* dk, void* dv,
+                             cudaStream_t stream) {
   ShortParams p = make_params(q, k, v, cu, ndocs, T, H, Hkv, softmax_scale);
   p.hadamard = hadamard ? 1 : 0;
   p.causal = causal ? 1 : 0;
@@ -360,6 +370,7 @@ cudaError_t launch_bwd_short(const flamia_qtensor* q, const flamia_qtensor* k,
   p.lse_in = lse;
   p.D = D;
   p.dq_acc = dq_acc;
+  p.dq_pre = dq_pre;
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
   if (Hkv == H) {

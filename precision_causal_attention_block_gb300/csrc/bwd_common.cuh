@@ -32,6 +32,7 @@ struct BwdParams {
   int hadamard;  // dK (and, in the conversion, dQ) rotated back by H_d
   int causal;    // 0: every query sees every key of its document
   int* dq_turns;  // deterministic dQ: [T][H] turn counters (per tile's first query), else null
+  const int8_t* dq_pre;  // FP16 dQ accumulator: prescale exponents [H, T], else null (float32)
   int* status;
 };
 

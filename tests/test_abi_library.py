@@ -35,9 +35,11 @@ def test_every_declared_symbol_is_exported(cpu_lib):
 
 def test_size_queries(cpu_lib):
     from precision_causal_attention_block_gb300 import flamia as fl
-    # float32 dQ accumulator, then the int32 turn counters, each 256-byte padded
-    assert fl.flamia_bwd_workspace_bytes(16384, 16, 128) == 16384 * 16 * 128 * 4 + 16384 * 16 * 4
-    assert fl.flamia_bwd_workspace_bytes(3, 1, 64) == 768 + 256
+    # float32 dQ accumulator, int32 turn counters, int8 prescale table, 3 H
+    # ints, each 256-byte padded
+    th = 16384 * 16
+    assert fl.flamia_bwd_workspace_bytes(16384, 16, 128) == th * 128 * 4 + th * 4 + th + 256
+    assert fl.flamia_bwd_workspace_bytes(3, 1, 64) == 768 + 256 + 256 + 256
     assert fl.flamia_bwd_workspace_bytes(10, 1, 96) == 0
     wl = fl.flamia_worklist_bytes(65536, 30)
     assert wl >= 64 + 16 * (65536 // 256 + 31) + 16 * (65536 // 128 + 31)
