@@ -384,6 +384,9 @@ def stage_breakdown(call, xd, stream, flush, w, reps=10):
         "quantize_q_ms": lambda: fl.flamia_quantize_tokenblock(xd["q"], call.cu, call.q,
                                                                call.fmt_qk,
                                                                dev_status=call.status),
+        "quantize_qkv_ms": lambda: fl.flamia_quantize_qkv(xd["q"], xd["k"], xd["v"], call.cu,
+                                                          call.q, call.k, call.v, call.fmt_qk,
+                                                          dev_status=call.status),
         "worklist_ms": lambda: fl.flamia_build_worklist(call.cu, call.T, call.wl,
                                                         dev_status=call.status),
         "fwd_ms": lambda: fl.flamia_attn_fwd_gqa(call.q, call.k, call.v, call.cu, call.T, call.H,
@@ -411,8 +414,12 @@ def stage_breakdown(call, xd, stream, flush, w, reps=10):
             times.append(a.elapsed_time(b))
         out[name] = round(statistics.median(times), 4)
     elems = w.T * w.H * w.d
-    qbytes = elems * 3 + w.T * w.H + (elems // 2 + elems // 16 if call.fmt_qk else 0)
+    qbytes = elems * 3 + w.T * w.H + (elems // 2 + elems // 16 if call.fmt_qk & 0xF else 0)
     out["quantize_q_GBps"] = round(qbytes / (out["quantize_q_ms"] * 1e-3) / 1e9, 1)
+    kv = w.T * call.H_kv * w.d
+    kbytes = kv * 3 + w.T * call.H_kv + (kv // 2 + kv // 16 if call.fmt_qk & 0xF else 0)
+    out["quantize_qkv_GBps"] = round((qbytes + kbytes + kv * 3 + w.T * call.H_kv) /
+                                     (out["quantize_qkv_ms"] * 1e-3) / 1e9, 1)
     out["worklist_us"] = round(out["worklist_ms"] * 1e3, 2)
     bufs = [call.q.codes, call.q.scales, call.k.codes, call.k.scales, call.v.codes,
             call.v.scales, call.dout.codes, call.dout.scales, call.wl, call.ws, call.o, call.lse,

@@ -131,6 +131,23 @@ flamia_status flamia_quantize_tokenblock(const void* x_bf16, int T, int H, int d
                                          void* stream);
 
 /*
+ * Q, K and V of one call quantised by one launch (review page, sec. 3.4
+ * "Quantization fusion": one pass per operand; one launch for the three
+ * fills the GPU for longer and pays one tail).  The results are bit for bit
+ * those of flamia_quantize_tokenblock on q with format_qk (H heads), on k
+ * with format_qk (H_kv heads) and on v with FLAMIA_FORMAT_MXFP8 (H_kv heads).
+ * format_qk: FLAMIA_FORMAT_MXFP8, FLAMIA_FORMAT_MXFP8_NVFP4 or
+ * FLAMIA_FORMAT_MXFP8 | FLAMIA_FORMAT_HADAMARD (then V, never rotated, takes
+ * a second launch).  q_bf16 [T, H, d], k_bf16 and v_bf16 [T, H_kv, d];
+ * H_kv divides H.  Errors as for flamia_quantize_tokenblock.
+ */
+flamia_status flamia_quantize_qkv(const void* q_bf16, const void* k_bf16, const void* v_bf16,
+                                  int T, int H, int H_kv, int d, const int32_t* cu_seqlens,
+                                  int ndocs, int format_qk, const flamia_qtensor* q,
+                                  const flamia_qtensor* k, const flamia_qtensor* v,
+                                  int* dev_status, void* stream);
+
+/*
  * Work list.  Source: review page sec. 3.4 "Work scheduling": a forward item
  * is 256 consecutive queries of one document (two 128-query tiles), its cost
  * the number of 128-key blocks it visits; items are sorted by descending

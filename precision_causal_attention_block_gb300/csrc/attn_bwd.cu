@@ -86,7 +86,9 @@ __host__ __device__ constexpr uint32_t operand_layout() {
 // K (4 columns) and of Q_u (two 4-column buffers, by u parity).
 constexpr uint32_t kSfK4 = 384, kSfQ4 = 388;
 
-template <int DIM, bool NVF4>
+// OPT: the deterministic dQ mode or the FP16 accumulator is on (their code
+// is compiled only into these instances).
+template <int DIM, bool NVF4, bool OPT>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap map_q,
                     const __grid_constant__ CUtensorMap map_k,
@@ -389,7 +391,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const size_t at = static_cast<size_t>(tile_head(it, u)) * T + min(qi, T - 1);
         r_lse = prm.lse[at];
         r_dd = prm.D[at];
-        if (prm.dq_pre != nullptr) r_pre = prm.dq_pre[at];
+        if (OPT && prm.dq_pre != nullptr) r_pre = prm.dq_pre[at];
         if (lane == 0) {
           r_qb = prm.q_scales[at];
           r_dob = prm.do_scales[at];
@@ -399,7 +401,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int b = ug & 1;
         sm.nl[b][j] = r_qv ? 8.f - r_lse * LOG2E : -INFINITY;
         sm.dd[b][j] = r_qv ? r_dd : 0.f;
-        sm.pf[b][j] = r_qv ? exp2i(r_pre) : 0.f;
+        if (OPT) sm.pf[b][j] = r_qv ? exp2i(r_pre) : 0.f;
         if (lane == 0) {
           sm.qbyte[b][quad] = r_qv ? r_qb : 127u;
           sm.dobyte[b][quad] = r_qv ? r_dob : 127u;
@@ -514,7 +516,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // the previous tile's reduce-adds must have read the staging buffer
         // (and, in the deterministic mode, completed: their turn is passed on)
         if (issuer) {
-          if (prm.dq_turns == nullptr) {
+          if (!OPT || prm.dq_turns == nullptr) {
             bulk_wait_group_read0();
           } else {
             bulk_wait_group0();
@@ -534,7 +536,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           // dQ of the next tile may now be written
           tc_fence_before();
           mbar_arrive(smem_u32(&sm.bar_dq_read));
-          if (prm.dq_pre != nullptr) {
+          if (OPT && prm.dq_pre != nullptr) {
             // x 2^p of the query row (0 outside the document), rounded to FP16,
             // in DIM / 64 boxes [128 query rows][64 halves], 128B-swizzled
             const float pf = sm.pf[ub][j];
@@ -556,7 +558,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
           }
 #pragma unroll
-          for (int cc = 0; cc < kCh && prm.dq_pre == nullptr; ++cc) {
+          for (int cc = 0; cc < kCh && !(OPT && prm.dq_pre != nullptr); ++cc) {
             float* row = sm.dqs[g * kCh + cc] + j * 32;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -576,13 +578,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (g == 0 && u + 1 < nq) store_query_inputs(uc + 1);
         named_barrier_sync(1, kComputeThreads);
         if (issuer && !sm.abort) {
-          int* turn = prm.dq_turns == nullptr
+          int* turn = !OPT || prm.dq_turns == nullptr
                           ? nullptr
                           : prm.dq_turns + static_cast<size_t>(q0) * prm.H + h;
           if (turn != nullptr && !wait_turn(turn, dq_turn(prm, it, q0))) {
             sm.abort = 1;
           } else {
-            if (prm.dq_pre != nullptr) {
+            if (OPT && prm.dq_pre != nullptr) {
               const __half* box0 = reinterpret_cast<const __half*>(sm.dqs[0]);
 #pragma unroll
               for (int b = 0; b < DIM / 64; ++b)
@@ -597,7 +599,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
         }
       }
-      if (issuer && pend != nullptr) {  // the item's last turn, before the next item
+      if (OPT && issuer && pend != nullptr) {  // the item's last turn, before the next item
         bulk_wait_group0();
         pass_turn(pend);
         pend = nullptr;
@@ -967,11 +969,11 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
       return FLAMIA_ERR_CUDA;
   } else {
     const size_t smem = sizeof(BwdSmem<DIM, NVF4>) + 1024;
-    if (cudaFuncSetAttribute(attn_bwd_kernel<DIM, NVF4>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto kernel = (det || dq16) ? attn_bwd_kernel<DIM, NVF4, true> : attn_bwd_kernel<DIM, NVF4, false>;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return FLAMIA_ERR_CUDA;
-    attn_bwd_kernel<DIM, NVF4><<<static_cast<unsigned>(grid), kBwdThreads, smem, stream>>>(
+    kernel<<<static_cast<unsigned>(grid), kBwdThreads, smem, stream>>>(
         mq, mk, mv, mdo, mdq, mq4, mk4, prm);
     if (cudaGetLastError() != cudaSuccess) return FLAMIA_ERR_CUDA;
   }

@@ -50,13 +50,26 @@ __device__ __forceinline__ void unpack8(const uint4& xv, float (&v)[8]) {
   }
 }
 
+// Up to three tensors of one call (Q, K, V: the same T, d and documents)
+// quantised by one launch: grid.y runs over the heads of tensor 0, then of
+// tensor 1, then of tensor 2, so one launch fills the GPU three times longer
+// and pays one tail.  f4codes[z] == nullptr: no NVFP4 copy for tensor z.
+struct QuantJob {
+  uint8_t* codes[3];
+  uint8_t* scales[3];
+  uint8_t* f4codes[3];
+  uint8_t* f4scales[3];
+  int H[3];
+  int n;
+};
+
 template <int DIM, bool HAD, bool FUSE_D>
 __global__ void __launch_bounds__(kQThreads)
-    quantize_kernel(const __grid_constant__ CUtensorMap map_x, int T, int H,
-                    const int32_t* __restrict__ cu, int ndocs, uint8_t* __restrict__ codes,
-                    uint8_t* __restrict__ scales, uint8_t* __restrict__ f4codes,
-                    uint8_t* __restrict__ f4scales, const uint4* __restrict__ o,
-                    float* __restrict__ D, int* dev_status) {
+    quantize_kernel(const __grid_constant__ CUtensorMap map0,
+                    const __grid_constant__ CUtensorMap map1,
+                    const __grid_constant__ CUtensorMap map2, int T,
+                    const int32_t* __restrict__ cu, int ndocs, const QuantJob job,
+                    const uint4* __restrict__ o, float* __restrict__ D, int* dev_status) {
   constexpr int LPR = DIM / 8;    // lanes per row: 16 bytes (8 BF16) per lane
   constexpr int RPI = 32 / LPR;   // rows per warp-wide read
   constexpr int NLD = 32 / RPI;   // reads per 32 rows
@@ -69,7 +82,24 @@ __global__ void __launch_bounds__(kQThreads)
   __shared__ alignas(8) uint64_t s_bar;
 
   const int seg0 = blockIdx.x * kSeg;
-  const int h = blockIdx.y;
+  // head h of tensor z (fields picked by selects: no indexed copy of the job)
+  int h = blockIdx.y, z = 0;
+  if (job.n > 1 && h >= job.H[0]) {
+    h -= job.H[0];
+    z = 1;
+    if (job.n > 2 && h >= job.H[1]) {
+      h -= job.H[1];
+      z = 2;
+    }
+  }
+  const int H = z == 0 ? job.H[0] : z == 1 ? job.H[1] : job.H[2];
+  uint8_t* __restrict__ codes = z == 0 ? job.codes[0] : z == 1 ? job.codes[1] : job.codes[2];
+  uint8_t* __restrict__ scales = z == 0 ? job.scales[0] : z == 1 ? job.scales[1] : job.scales[2];
+  uint8_t* __restrict__ f4codes =
+      z == 0 ? job.f4codes[0] : z == 1 ? job.f4codes[1] : job.f4codes[2];
+  uint8_t* __restrict__ f4scales =
+      z == 0 ? job.f4scales[0] : z == 1 ? job.f4scales[1] : job.f4scales[2];
+  const CUtensorMap* map_x = z == 0 ? &map0 : z == 1 ? &map1 : &map2;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -79,7 +109,7 @@ __global__ void __launch_bounds__(kQThreads)
   __syncthreads();
   if (tid == 0) {
     mbar_arrive_expect_tx(smem_u32(&s_bar), kQThreads * DIM * 2);
-    tma_load_3d(smem_u32(s_x), &map_x, smem_u32(&s_bar), 0, h, seg0);
+    tma_load_3d(smem_u32(s_x), map_x, smem_u32(&s_bar), 0, h, seg0);
   }
   const int chunk = lane % LPR;
   // D = dO . O: this lane's O chunks of its rows, loaded while the rows of
@@ -94,8 +124,8 @@ __global__ void __launch_bounds__(kQThreads)
     }
   }
 
-  // Light validation of cu_seqlens, spread over the CTAs of head 0.
-  if (h == 0) {
+  // Light validation of cu_seqlens, spread over the CTAs of the first head.
+  if (blockIdx.y == 0) {
     for (int i = blockIdx.x * kQThreads + tid; i < ndocs; i += gridDim.x * kQThreads)
       if (__ldg(cu + i) > __ldg(cu + i + 1)) report(dev_status, FLAMIA_DEV_BAD_SEQLENS);
     if (blockIdx.x == 0 && tid == 0 && (__ldg(cu) != 0 || __ldg(cu + ndocs) != T))
@@ -240,6 +270,67 @@ __global__ void __launch_bounds__(kQThreads)
   }
 }
 
+// Tensor map of BF16 rows seen as 2-byte elements (dim, head, token); box =
+// one head x 160 rows.
+bool make_rows_map(CUtensorMap* map, const void* x, int T, int H, int d) {
+  EncodeTiledFn enc = get_encode_tiled();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(T)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(d) * 2 * H};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(d), 1u, static_cast<cuuint32_t>(kQThreads)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(x), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Host checks of one tensor's arguments; on success fills its slot of the job.
+flamia_status check_tensor(const void* x, int H, int format, const flamia_qtensor* out,
+                           QuantJob& job, int z) {
+  if (format != FLAMIA_FORMAT_MXFP8 && format != FLAMIA_FORMAT_MXFP8_NVFP4)
+    return FLAMIA_ERR_UNSUPPORTED;
+  if (x == nullptr || out == nullptr || out->codes == nullptr || out->scales == nullptr)
+    return FLAMIA_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(out->codes, 16)) return FLAMIA_ERR_INVALID_ARG;
+  job.codes[z] = out->codes;
+  job.scales[z] = out->scales;
+  job.f4codes[z] = nullptr;
+  job.f4scales[z] = nullptr;
+  if (format == FLAMIA_FORMAT_MXFP8_NVFP4) {
+    if (out->nvfp4_codes == nullptr || out->nvfp4_scales == nullptr ||
+        !aligned(out->nvfp4_codes, 16))
+      return FLAMIA_ERR_INVALID_ARG;
+    job.f4codes[z] = out->nvfp4_codes;
+    job.f4scales[z] = out->nvfp4_scales;
+  }
+  job.H[z] = H;
+  return FLAMIA_OK;
+}
+
+// One launch over the job's tensors (xs[z] their BF16 inputs).
+flamia_status launch_quantize(const void* const* xs, QuantJob& job, int T, int d,
+                              const int32_t* cu, int ndocs, bool had, const void* o_bf16,
+                              float* D, int* dev_status, cudaStream_t s) {
+  CUtensorMap maps[3];
+  int rows = 0;
+  for (int z = 0; z < job.n; ++z) {
+    if (!make_rows_map(&maps[z], xs[z], T, job.H[z], d)) return FLAMIA_ERR_CUDA;
+    rows += job.H[z];
+  }
+  for (int z = job.n; z < 3; ++z) maps[z] = maps[0];
+  if (rows > 65535) return FLAMIA_ERR_UNSUPPORTED;
+  dim3 grid((T + kSeg - 1) / kSeg, rows);
+  const bool fd = D != nullptr;
+  auto kern = d == 128 ? (had ? quantize_kernel<128, true, false>
+                              : fd ? quantize_kernel<128, false, true> : quantize_kernel<128, false, false>)
+                       : (had ? quantize_kernel<64, true, false>
+                              : fd ? quantize_kernel<64, false, true> : quantize_kernel<64, false, false>);
+  kern<<<grid, kQThreads, 0, s>>>(maps[0], maps[1], maps[2], T, cu, ndocs, job,
+                                  static_cast<const uint4*>(o_bf16), D, dev_status);
+  return cudaGetLastError() == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace flamia
 
@@ -253,49 +344,53 @@ extern "C" flamia_status flamia_quantize_tokenblock(const void* x_bf16, int T, i
   if (!supported_dim(d)) return FLAMIA_ERR_UNSUPPORTED;
   const bool had = (format & FLAMIA_FORMAT_HADAMARD) != 0;
   format &= ~FLAMIA_FORMAT_HADAMARD;
-  if (format != FLAMIA_FORMAT_MXFP8 && format != FLAMIA_FORMAT_MXFP8_NVFP4)
-    return FLAMIA_ERR_UNSUPPORTED;
   if (had && (format != FLAMIA_FORMAT_MXFP8 || o_bf16 != nullptr || D != nullptr))
     return FLAMIA_ERR_UNSUPPORTED;
-  if (!valid_sizes(T, H, d, ndocs) || x_bf16 == nullptr || cu_seqlens == nullptr ||
-      out == nullptr || out->codes == nullptr || out->scales == nullptr)
-    return FLAMIA_ERR_INVALID_ARG;
+  if (!valid_sizes(T, H, d, ndocs) || cu_seqlens == nullptr) return FLAMIA_ERR_INVALID_ARG;
   if ((o_bf16 == nullptr) != (D == nullptr)) return FLAMIA_ERR_INVALID_ARG;
-  if (!aligned(x_bf16, 16) || !aligned(out->codes, 16) || (o_bf16 && !aligned(o_bf16, 16)))
-    return FLAMIA_ERR_INVALID_ARG;
-  uint8_t* f4c = nullptr;
-  uint8_t* f4s = nullptr;
-  if (format == FLAMIA_FORMAT_MXFP8_NVFP4) {
-    if (out->nvfp4_codes == nullptr || out->nvfp4_scales == nullptr ||
-        !aligned(out->nvfp4_codes, 16))
-      return FLAMIA_ERR_INVALID_ARG;
-    f4c = out->nvfp4_codes;
-    f4s = out->nvfp4_scales;
-  }
-  int* status = dev_status;
-  // BF16 rows seen as 2-byte elements (dim, head, token); box = one head x 160 rows
-  CUtensorMap map;
-  {
-    EncodeTiledFn enc = get_encode_tiled();
-    if (!enc) return FLAMIA_ERR_CUDA;
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
-                          static_cast<cuuint64_t>(T)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(d) * 2 * H};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(d), 1u, static_cast<cuuint32_t>(kQThreads)};
-    cuuint32_t estr[3] = {1, 1, 1};
-    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(x_bf16), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return FLAMIA_ERR_CUDA;
-  }
-  dim3 grid((T + kSeg - 1) / kSeg, H);
+  if (o_bf16 && !aligned(o_bf16, 16)) return FLAMIA_ERR_INVALID_ARG;
+  QuantJob job{};
+  job.n = 1;
+  const flamia_status st = check_tensor(x_bf16, H, format, out, job, 0);
+  if (st != FLAMIA_OK) return st;
+  const void* xs[1] = {x_bf16};
+  return launch_quantize(xs, job, T, d, cu_seqlens, ndocs, had, o_bf16, D, dev_status,
+                         static_cast<cudaStream_t>(stream));
+}
+
+extern "C" flamia_status flamia_quantize_qkv(const void* q_bf16, const void* k_bf16,
+                                             const void* v_bf16, int T, int H, int H_kv, int d,
+                                             const int32_t* cu_seqlens, int ndocs, int format_qk,
+                                             const flamia_qtensor* q, const flamia_qtensor* k,
+                                             const flamia_qtensor* v, int* dev_status,
+                                             void* stream) {
+  if (!supported_dim(d)) return FLAMIA_ERR_UNSUPPORTED;
+  const bool had = (format_qk & FLAMIA_FORMAT_HADAMARD) != 0;
+  const int fmt = format_qk & ~FLAMIA_FORMAT_HADAMARD;
+  if (had && fmt != FLAMIA_FORMAT_MXFP8) return FLAMIA_ERR_UNSUPPORTED;
+  if (H_kv <= 0 || H <= 0 || H % H_kv != 0) return FLAMIA_ERR_INVALID_ARG;
+  if (!valid_sizes(T, H, d, ndocs) || cu_seqlens == nullptr) return FLAMIA_ERR_INVALID_ARG;
+  QuantJob job{};
+  flamia_status st;
+  if ((st = check_tensor(q_bf16, H, fmt, q, job, 0)) != FLAMIA_OK ||
+      (st = check_tensor(k_bf16, H_kv, fmt, k, job, 1)) != FLAMIA_OK)
+    return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const bool fd = D != nullptr;
-  auto kern = d == 128 ? (had ? quantize_kernel<128, true, false>
-                              : fd ? quantize_kernel<128, false, true> : quantize_kernel<128, false, false>)
-                       : (had ? quantize_kernel<64, true, false>
-                              : fd ? quantize_kernel<64, false, true> : quantize_kernel<64, false, false>);
-  kern<<<grid, kQThreads, 0, s>>>(map, T, H, cu_seqlens, ndocs, out->codes, out->scales, f4c, f4s,
-                                  static_cast<const uint4*>(o_bf16), D, status);
-  return cudaGetLastError() == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
+  if (had) {  // Q and K rotated in one launch, V (never rotated) in its own
+    job.n = 2;
+    const void* xs[2] = {q_bf16, k_bf16};
+    if ((st = launch_quantize(xs, job, T, d, cu_seqlens, ndocs, true, nullptr, nullptr,
+                              dev_status, s)) != FLAMIA_OK)
+      return st;
+    QuantJob jv{};
+    jv.n = 1;
+    if ((st = check_tensor(v_bf16, H_kv, FLAMIA_FORMAT_MXFP8, v, jv, 0)) != FLAMIA_OK) return st;
+    const void* xv[1] = {v_bf16};
+    return launch_quantize(xv, jv, T, d, cu_seqlens, ndocs, false, nullptr, nullptr, dev_status,
+                           s);
+  }
+  if ((st = check_tensor(v_bf16, H_kv, FLAMIA_FORMAT_MXFP8, v, job, 2)) != FLAMIA_OK) return st;
+  job.n = 3;
+  const void* xs[3] = {q_bf16, k_bf16, v_bf16};
+  return launch_quantize(xs, job, T, d, cu_seqlens, ndocs, false, nullptr, nullptr, dev_status, s);
 }

@@ -41,6 +41,8 @@ _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_
 _QP = ctypes.POINTER(QTensorStruct)
 SIGNATURES = {
     "flamia_quantize_tokenblock": (_i, [_vp, _i, _i, _i, _vp, _i, _i, _vp, _vp, _QP, _vp, _vp]),
+    "flamia_quantize_qkv": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _i, _i, _QP, _QP, _QP, _vp,
+                                 _vp]),
     "flamia_worklist_bytes": (_sz, [_i, _i]),
     "flamia_build_worklist": (_i, [_vp, _i, _i, _vp, _sz, _vp, _vp]),
     "flamia_attn_fwd": (_i, [_QP, _QP, _QP, _vp, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp, _vp, _vp]),
@@ -118,6 +120,16 @@ def flamia_quantize_tokenblock(x, cu_seqlens, out: QTensor, fmt: int = FORMAT_MX
     _check(load().flamia_quantize_tokenblock(
         _ptr(x), T, H, d, _ptr(cu_seqlens), cu_seqlens.numel() - 1, fmt, _ptr(o), _ptr(D),
         ctypes.byref(st), _ptr(dev_status), _stream()), "flamia_quantize_tokenblock")
+
+
+def flamia_quantize_qkv(xq, xk, xv, cu_seqlens, q: QTensor, k: QTensor, v: QTensor,
+                        fmt_qk: int = FORMAT_MXFP8, dev_status=None):
+    T, H, d = xq.shape
+    sq, sk, sv = q.struct(), k.struct(), v.struct()
+    _check(load().flamia_quantize_qkv(
+        _ptr(xq), _ptr(xk), _ptr(xv), T, H, xk.shape[1], d, _ptr(cu_seqlens),
+        cu_seqlens.numel() - 1, fmt_qk, ctypes.byref(sq), ctypes.byref(sk), ctypes.byref(sv),
+        _ptr(dev_status), _stream()), "flamia_quantize_qkv")
 
 
 def flamia_worklist_bytes(T: int, ndocs: int) -> int:
@@ -223,8 +235,10 @@ class TrainingCall:
         self.dk = torch.empty((T, self.H_kv, d), dtype=torch.bfloat16, device=device)
         self.dv = torch.empty_like(self.dk)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
-        # the work list is built on a side stream while Q, K, V are quantised
-        self.side = torch.cuda.Stream(device)
+        # the work list is built on a side stream while Q, K, V are quantised;
+        # high priority, so its small launches take SMs ahead of the waiting
+        # CTAs of the quantiser's one large launch
+        self.side = torch.cuda.Stream(device, priority=-1)
         self.wl_ready = torch.cuda.Event()
 
     def forward(self, xq, xk, xv):
@@ -234,9 +248,8 @@ class TrainingCall:
         with torch.cuda.stream(self.side):
             flamia_build_worklist(self.cu, self.T, self.wl, dev_status=self.status)
             self.wl_ready.record(self.side)
-        flamia_quantize_tokenblock(xq, self.cu, self.q, self.fmt_qk, dev_status=self.status)
-        flamia_quantize_tokenblock(xk, self.cu, self.k, self.fmt_qk, dev_status=self.status)
-        flamia_quantize_tokenblock(xv, self.cu, self.v, FORMAT_MXFP8, dev_status=self.status)
+        flamia_quantize_qkv(xq, xk, xv, self.cu, self.q, self.k, self.v, self.fmt_qk,
+                            dev_status=self.status)
         main.wait_event(self.wl_ready)
         flamia_attn_fwd_gqa(self.q, self.k, self.v, self.cu, self.T, self.H, self.H_kv, self.d,
                             self.scale, self.wl, self.o, self.lse, self.flags,

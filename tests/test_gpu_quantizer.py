@@ -108,3 +108,34 @@ def test_bad_seqlens_set_the_status_bit(lib):
     fl.flamia_quantize_tokenblock(x, cu, out, 0, dev_status=st)
     torch.cuda.synchronize()
     assert int(st.item()) & fl.DEV_BAD_SEQLENS
+
+
+@pytest.mark.parametrize("d,fmt,H,Hkv", [(128, 0, 4, 2), (64, 1, 3, 3), (128, 0x10, 2, 1),
+                                         (64, 0, 6, 3)])
+def test_quantize_qkv_one_launch_equals_three_calls(lib, d, fmt, H, Hkv):
+    # flamia_quantize_qkv: Q and K with the call's format, V plain MXFP8, K / V
+    # with H_kv heads; bit for bit the three single calls, which the tests
+    # above pin against the oracle (Q's codes are checked against it here too)
+    from precision_causal_attention_block_gb300 import flamia as fl
+    w = W.custom("qkv", RAGGED, H, d, structure="outlier16x2", seed=5)
+    x = W.make_inputs_bf16(w)
+    xq, xk, xv = dev(x["q"]), dev(x["k"][:, :Hkv].contiguous()), dev(x["v"][:, :Hkv].contiguous())
+    cu = cu_tensor(w.cu_seqlens)
+    nv = (fmt & 0xF) == 1
+    q, k, v = fl.QTensor(w.T, H, d, nv), fl.QTensor(w.T, Hkv, d, nv), fl.QTensor(w.T, Hkv, d)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fl.flamia_quantize_qkv(xq, xk, xv, cu, q, k, v, fmt, dev_status=st)
+    refs = [fl.QTensor(w.T, H, d, nv), fl.QTensor(w.T, Hkv, d, nv), fl.QTensor(w.T, Hkv, d)]
+    for xx, out, f in zip((xq, xk, xv), refs, (fmt, fmt, 0)):
+        fl.flamia_quantize_tokenblock(xx, cu, out, f, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for a, b in zip((q, k, v), refs):
+        assert torch.equal(a.codes, b.codes) and torch.equal(a.scales, b.scales)
+        if a.nvfp4_codes is not None:
+            assert torch.equal(a.nvfp4_codes, b.nvfp4_codes)
+            assert torch.equal(a.nvfp4_scales, b.nvfp4_scales)
+    if fmt != 0x10:
+        codes, sb = O.quantize_tokenblock(x["q"].double().numpy(), w.cu_seqlens)
+        assert np.array_equal(q.codes.cpu().numpy(), codes)
+        assert np.array_equal(q.scales.cpu().numpy(), sb)
