@@ -176,7 +176,8 @@ def run_ours(args, rank, world, local):
     cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev)
     call = fl.TrainingCall(w.T, w.H, w.d, cu, w.sm_scale, nvfp4_qk=args.nvfp4,
                            hadamard=args.hadamard, causal=not args.noncausal, H_kv=hkv,
-                           deterministic_dq=args.deterministic, dq_accum=args.dq_accum, device=dev)
+                           deterministic_dq=args.deterministic, dq_accum=args.dq_accum,
+                           schedule=args.schedule, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -236,7 +237,7 @@ def run_ours(args, rank, world, local):
                                    nvfp4_qk=args.nvfp4, hadamard=args.hadamard,
                                    causal=not args.noncausal, H_kv=hkv,
                                    deterministic_dq=args.deterministic, dq_accum=args.dq_accum,
-                                   device=dev)]
+                                   schedule=args.schedule, device=dev)]
     xin = [xd, {n: torch.empty_like(t) for n, t in xd.items()}]
     outs = lambda c: (c.o, c.dq, c.dk, c.dv)
     hout = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs(c)] for c in calls]
@@ -345,6 +346,7 @@ def run_ours(args, rank, world, local):
                    "kv_heads": hkv,
                    "dq_sum": "ordered (deterministic)" if args.deterministic else "atomic",
                    "dq_accumulator": args.dq_accum,
+                   "schedule": args.schedule,
                    "flops_per_step": flops, "l2": "flushed (256 MB write) before every step",
                    "parallelism": f"replicas x{world}"},
         "pct_of_fp8_peak": round(100.0 * value / world / pk["fp8_tflops"], 2),
@@ -356,7 +358,8 @@ def run_ours(args, rank, world, local):
                      "frac": round(achieved / pk["fp8_tflops"], 4),
                      "peak_source": pk["source"],
                      "traffic": None if (args.hadamard or args.noncausal or hkv != w.H or
-                                         args.deterministic or args.dq_accum != "fp32")
+                                         args.deterministic or args.dq_accum != "fp32" or
+                                         args.schedule != "dynamic")
                      else profiled_traffic(w, args.nvfp4),
                      "traffic_unit": "bytes per launch of the attention kernel (ncu, DRAM read + write)"},
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
@@ -527,6 +530,10 @@ def main():
     ap.add_argument("--dq-accum", default="fp32",
                     choices=["fp32", "fp16_sequence", "fp16_causal"],
                     help="dQ accumulator: float32, or FP16 behind a sequence-wide / causal prescale")
+    ap.add_argument("--schedule", default="dynamic", choices=["dynamic", "rule", "static"],
+                    help="work distribution of the persistent kernels (rule: the pages' choice, "
+                         "dynamic for causal calls, static for non-causal ones unless the "
+                         "longest document is at least 4x the average)")
     ap.add_argument("--deterministic", action="store_true",
                     help="dQ partials added in a fixed key-tile order (bitwise reproducible)")
     args = ap.parse_args()

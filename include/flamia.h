@@ -78,6 +78,17 @@ typedef enum {
                                        from sequence-wide maxima                */
 #define FLAMIA_FLAG_DQ_CAUSAL_SCALE 0x20 /* with FLAMIA_FLAG_DQ_FP16: the prescale
                                        of a query row from the keys it sees     */
+#define FLAMIA_FLAG_SCHEDULE_STATIC 0x40 /* forward / backward: the persistent CTAs
+                                       take their work items in a static snake
+                                       over the cost-sorted list instead of
+                                       claiming the next unclaimed item        */
+#define FLAMIA_FLAG_SCHEDULE_RULE 0x80 /* forward / backward: the pages' rule,
+                                       dynamic claims for causal calls and, for
+                                       non-causal ones, only when the longest
+                                       document is at least 4x the average
+                                       (static snake otherwise).  Default, no
+                                       flag: dynamic claims (measured fastest
+                                       on every workload here)                 */
 
 /*
  * One quantised operand, all device pointers owned by the caller.

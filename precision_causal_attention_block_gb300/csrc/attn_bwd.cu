@@ -161,8 +161,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       bool ok = true;
       // items in head-major, longest-first order, claimed one at a time: a CTA
       // takes the next item when it has issued its current item's last load
-      int* counter = prm.wl_header + kHdrBwdNext;
-      int idx = claim_item(counter);
+      Claims claims{prm.wl_header + kHdrBwdNext,
+                    static_schedule(prm.sched, prm.causal, prm.items, n_items, T, prm.ndocs)};
+      int idx = claims.next();
       for (int n = 0; ok; ++n) {
         const bool end = idx >= total;
         if (!ring_put(sm.ring, n, end ? total : idx) || sm.abort) {
@@ -172,7 +173,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (end) break;
         BwdItem it;
         if (!decode_bwd_item(prm, n_items, idx, it)) {
-          idx = claim_item(counter);
+          idx = claims.next();
           continue;
         }
         // the previous item's K / V are free once its last products are done
@@ -200,7 +201,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tma_load_3d(smem_u32(sm.dout[st]), &map_do, bf, 0, th, tq0);
           if (NVF4) tma_load_3d(smem_u32(sm.q4[st]), &map_q4, bf, 0, th, tq0);
         }
-        if (ok) idx = claim_item(counter);
+        if (ok) idx = claims.next();
       }
       if (nk > 0) ok &= mbar_wait(bkv, (nk - 1) & 1);
       for (int u = max(0, uc - kBStages); u < uc; ++u)
@@ -883,7 +884,7 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
                          const flamia_qtensor* v, const flamia_qtensor* dout, const float* D,
                          const float* lse, const int32_t* cu, int ndocs, int T, int H,
                          int Hkv, float softmax_scale, bool had, bool causal, bool det, int dq16,
-                         void* wl, void* dq, void* dk, void* dv, void* ws, int* status,
+                         int sched, void* wl, void* dq, void* dk, void* dv, void* ws, int* status,
                          cudaStream_t stream) {
   CUtensorMap mq, mk, mv, mdo, mdq, mq4, mk4;
   const CUtensorMapSwizzle swz = swizzle_for_row_bytes(DIM);
@@ -935,6 +936,9 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
   prm.dq_turns = det ? reinterpret_cast<int*>(wsb + W.off_turns) : nullptr;
   int8_t* pre = dq16 ? reinterpret_cast<int8_t*>(wsb + W.off_pre) : nullptr;
   prm.dq_pre = pre;
+  // the deterministic mode needs the claims in list order (a turn only waits
+  // for an item claimed before it)
+  prm.sched = det ? kSchedDynamic : sched;
   // the accumulator (float32 or FP16) and, in the deterministic mode, the
   // turn counters behind it
   if (cudaMemsetAsync(acc, 0, n * (dq16 ? 2 : 4), stream) != cudaSuccess ||
@@ -1024,8 +1028,12 @@ extern "C" flamia_status flamia_attn_bwd_gqa(const flamia_qtensor* q, const flam
   if (H_kv <= 0 || H <= 0 || H % H_kv != 0) return FLAMIA_ERR_INVALID_ARG;
   if ((flags & ~(FLAMIA_FLAG_NVFP4_QK | FLAMIA_FLAG_HADAMARD | FLAMIA_FLAG_NONCAUSAL |
                  FLAMIA_FLAG_DETERMINISTIC_DQ | FLAMIA_FLAG_DQ_FP16 |
-                 FLAMIA_FLAG_DQ_CAUSAL_SCALE)) != 0)
+                 FLAMIA_FLAG_DQ_CAUSAL_SCALE | FLAMIA_FLAG_SCHEDULE_STATIC |
+                 FLAMIA_FLAG_SCHEDULE_RULE)) != 0)
     return FLAMIA_ERR_UNSUPPORTED;
+  const int sched = schedule_of(flags);
+  if (sched < 0) return FLAMIA_ERR_UNSUPPORTED;
+  if ((flags & FLAMIA_FLAG_DETERMINISTIC_DQ) && sched == kSchedStatic) return FLAMIA_ERR_UNSUPPORTED;
   if ((flags & FLAMIA_FLAG_DQ_CAUSAL_SCALE) && !(flags & FLAMIA_FLAG_DQ_FP16))
     return FLAMIA_ERR_UNSUPPORTED;
   const bool nvf4 = (flags & FLAMIA_FLAG_NVFP4_QK) != 0;
@@ -1055,13 +1063,13 @@ extern "C" flamia_status flamia_attn_bwd_gqa(const flamia_qtensor* q, const flam
   const float sc = had ? softmax_scale / static_cast<float>(d) : softmax_scale;
   if (nvf4)
     return launch_bwd<64, true>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, H_kv, sc,
-                                false, causal, det, dq16, wl, dq_bf16, dk_bf16, dv_bf16, ws,
+                                false, causal, det, dq16, sched, wl, dq_bf16, dk_bf16, dv_bf16, ws,
                                 dev_status, s);
   return d == 128 ? launch_bwd<128, false>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, H_kv,
-                                           sc, had, causal, det, dq16, wl, dq_bf16, dk_bf16,
+                                           sc, had, causal, det, dq16, sched, wl, dq_bf16, dk_bf16,
                                            dv_bf16, ws, dev_status, s)
                   : launch_bwd<64, false>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, H_kv,
-                                          sc, had, causal, det, dq16, wl, dq_bf16, dk_bf16,
+                                          sc, had, causal, det, dq16, sched, wl, dq_bf16, dk_bf16,
                                           dv_bf16, ws, dev_status, s);
 }
 

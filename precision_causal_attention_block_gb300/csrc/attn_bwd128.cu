@@ -159,8 +159,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // items in head-major, longest-first order, claimed one at a time: a CTA
       // takes the next item when it has issued its current item's last load
-      int* counter = prm.wl_header + kHdrBwdNext;
-      int idx = claim_item(counter);
+      Claims claims{prm.wl_header + kHdrBwdNext,
+                    static_schedule(prm.sched, prm.causal, prm.items, n_items, T, prm.ndocs)};
+      int idx = claims.next();
       for (int n = 0; ok; ++n) {
         const bool end = idx >= total;
         if (!ring_put(sm.ring, n, end ? total : idx) || sm.abort) {
@@ -170,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (end) break;
         BwdItem it;
         if (!decode_bwd_item(prm, n_items, idx, it)) {
-          idx = claim_item(counter);
+          idx = claims.next();
           continue;
         }
         const int nt = n_tiles64(it), nq = nt * G;
@@ -188,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(smem_u32(sm.v), &map_v, bkv, 0, it.hk, it.k0);
         ++nk;
         for (; u < nq && ok; ++u) ok = load_qd(tile_head(it, G, nt, u), tile_q0(it, G, nt, u));
-        if (ok) idx = claim_item(counter);
+        if (ok) idx = claims.next();
       }
       // drain: every issued copy has landed before the CTA exits
       if (nk > 0) ok &= mbar_wait(bkv, (nk - 1) & 1);

@@ -78,6 +78,7 @@ struct FwdParams {
   int Hkv, G;        // K / V heads; query head h reads K / V head h / G (G = H / Hkv)
   float scale_log2;  // softmax_scale * log2(e)
   int causal;        // 0: every query sees every key of its document
+  int sched;         // kSchedDynamic / kSchedRule / kSchedStatic
   int* status;
 };
 
@@ -238,8 +239,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       bool ok = true;
       // items in head-major, longest-first order, claimed one at a time: a CTA
       // takes the next item when it has issued its current item's last load
-      int* counter = prm.wl_header + kHdrFwdNext;
-      int idx = claim_item(counter);
+      Claims claims{prm.wl_header + kHdrFwdNext,
+                    static_schedule(prm.sched, prm.causal, prm.items, n_items, prm.T, prm.ndocs)};
+      int idx = claims.next();
       for (int n = 0; ok; ++n) {
         const bool end = idx >= total;
         if (!ring_put(sm.ring, n, end ? total : idx) || sm.abort) {
@@ -249,7 +251,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (end) break;
         FwdItem it;
         if (!decode_fwd_item(prm, n_items, idx, it)) {
-          idx = claim_item(counter);
+          idx = claims.next();
           continue;
         }
         // the previous item's Q tiles are free once its last score product is done
@@ -280,7 +282,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           tma_load_3d(smem_u32(sm.v[st]), &map_v, bf, 0, it.hk, it.s + j * kTile);
           if (NVF4) tma_load_3d(smem_u32(sm.k4[st]), &map_k4, bf, 0, it.hk, it.s + j * kTile);
         }
-        if (ok) idx = claim_item(counter);
+        if (ok) idx = claims.next();
       }
       // Drain: every issued copy has landed before the CTA can exit.
       if (nq_loaded > 0) ok &= mbar_wait(bq, (nq_loaded - 1) & 1);
@@ -618,8 +620,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 template <int DIM, bool NVF4>
 flamia_status launch_fwd(const flamia_qtensor* q, const flamia_qtensor* k,
                          const flamia_qtensor* v, const int32_t* cu, int ndocs, int T, int H,
-                         int Hkv, float softmax_scale, bool causal, void* wl, void* o, float* lse,
-                         int* status, cudaStream_t stream) {
+                         int Hkv, float softmax_scale, bool causal, int sched, void* wl, void* o,
+                         float* lse, int* status, cudaStream_t stream) {
   CUtensorMap mq, mk, mv, mq4, mk4;
   const CUtensorMapSwizzle swz = swizzle_for_row_bytes(DIM);
   if (!make_token_map(&mq, q->codes, T, H, DIM, kTile, swz) ||
@@ -654,6 +656,7 @@ flamia_status launch_fwd(const flamia_qtensor* q, const flamia_qtensor* k,
   prm.cap = L.cap_fwd;
   prm.scale_log2 = softmax_scale * 1.4426950408889634f;
   prm.causal = causal ? 1 : 0;
+  prm.sched = sched;
   prm.status = status;
   const size_t smem = sizeof(FwdSmem<DIM, NVF4>) + 1024;
   if (cudaFuncSetAttribute(attn_fwd_kernel<DIM, NVF4>,
@@ -689,8 +692,11 @@ extern "C" flamia_status flamia_attn_fwd_gqa(const flamia_qtensor* q, const flam
   // output row of the forward is written by one CTA)
   if ((flags & ~(FLAMIA_FLAG_NVFP4_QK | FLAMIA_FLAG_HADAMARD | FLAMIA_FLAG_NONCAUSAL |
                  FLAMIA_FLAG_DETERMINISTIC_DQ | FLAMIA_FLAG_DQ_FP16 |
-                 FLAMIA_FLAG_DQ_CAUSAL_SCALE)) != 0)
+                 FLAMIA_FLAG_DQ_CAUSAL_SCALE | FLAMIA_FLAG_SCHEDULE_STATIC |
+                 FLAMIA_FLAG_SCHEDULE_RULE)) != 0)
     return FLAMIA_ERR_UNSUPPORTED;
+  const int sched = schedule_of(flags);
+  if (sched < 0) return FLAMIA_ERR_UNSUPPORTED;
   const bool nvf4 = (flags & FLAMIA_FLAG_NVFP4_QK) != 0;
   const bool causal = (flags & FLAMIA_FLAG_NONCAUSAL) == 0;
   if ((nvf4 && d != 64) || (nvf4 && (flags & FLAMIA_FLAG_HADAMARD))) return FLAMIA_ERR_UNSUPPORTED;
@@ -713,11 +719,11 @@ extern "C" flamia_status flamia_attn_fwd_gqa(const flamia_qtensor* q, const flam
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (nvf4)
     return launch_fwd<64, true>(q, k, v, cu_seqlens, ndocs, T, H, H_kv, softmax_scale, causal,
-                                wl, o_bf16, lse, dev_status, s);
+                                sched, wl, o_bf16, lse, dev_status, s);
   return d == 128 ? launch_fwd<128, false>(q, k, v, cu_seqlens, ndocs, T, H, H_kv, softmax_scale,
-                                           causal, wl, o_bf16, lse, dev_status, s)
+                                           causal, sched, wl, o_bf16, lse, dev_status, s)
                   : launch_fwd<64, false>(q, k, v, cu_seqlens, ndocs, T, H, H_kv, softmax_scale,
-                                          causal, wl, o_bf16, lse, dev_status, s);
+                                          causal, sched, wl, o_bf16, lse, dev_status, s);
 }
 
 extern "C" flamia_status flamia_attn_fwd(const flamia_qtensor* q, const flamia_qtensor* k,

@@ -33,6 +33,7 @@ struct BwdParams {
   int causal;    // 0: every query sees every key of its document
   int* dq_turns;  // deterministic dQ: [T][H] turn counters (per tile's first query), else null
   const int8_t* dq_pre;  // FP16 dQ accumulator: prescale exponents [H, T], else null (float32)
+  int sched;             // kSchedDynamic / kSchedRule / kSchedStatic
   int* status;
 };
 

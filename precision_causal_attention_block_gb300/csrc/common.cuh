@@ -197,6 +197,14 @@ inline bool make_f16_token_map(CUtensorMap* map, const void* base, int T, int H,
   return r == CUDA_SUCCESS;
 }
 
+// The work distribution a call's flags ask for: 0 dynamic (default), 1 the
+// pages' rule, 2 static; -1 if both flags were given.
+inline int schedule_of(int flags) {
+  const bool st = (flags & FLAMIA_FLAG_SCHEDULE_STATIC) != 0;
+  const bool ru = (flags & FLAMIA_FLAG_SCHEDULE_RULE) != 0;
+  return st && ru ? -1 : st ? 2 : ru ? 1 : 0;
+}
+
 inline CUtensorMapSwizzle swizzle_for_row_bytes(int row_bytes) {
   return row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
          : row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B

@@ -143,6 +143,40 @@ __device__ __forceinline__ int ring_get(ItemRing<kSlots>& r, int n, bool release
 // the longest go first wherever a CTA is free).
 __device__ __forceinline__ int claim_item(int* counter) { return atomicAdd(counter, 1); }
 
+// Work distribution of the persistent kernels over their head-major,
+// cost-sorted item list.  Dynamic: the next unclaimed item (claim_item; the
+// review page, sec. 3.4 "Work scheduling", does this with cluster launch
+// control).  Static: the snake over the list, CTA b taking item r P + b in
+// even rounds r and r P + P - 1 - b in odd ones (P CTAs), which deals the
+// longest items out first and needs no atomics.
+enum : int { kSchedDynamic = 0, kSchedRule = 1, kSchedStatic = 2 };
+
+// Static or dynamic for this launch.  kSchedRule is the pages' rule (review
+// page, sec. 4.3 as the summary reports it): dynamic for causal calls; for
+// non-causal calls only when the longest document is at least 4x the average
+// length.  The list's first item carries the longest document's cost in
+// 128-token tiles.
+__device__ __forceinline__ bool static_schedule(int sched, int causal, const int4* items,
+                                                int n_items, int T, int ndocs) {
+  if (sched != kSchedRule) return sched == kSchedStatic;
+  if (causal || n_items <= 0) return false;
+  const long long longest = 128ll * items[0].w;
+  return longest * ndocs < 4ll * T;
+}
+
+struct Claims {
+  int* counter;
+  bool snake;
+  int round = 0;
+  __device__ __forceinline__ int next() {
+    if (!snake) return claim_item(counter);
+    const int P = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
+    const int idx = round * P + ((round & 1) ? P - 1 - b : b);
+    ++round;
+    return idx;
+  }
+};
+
 // Called by thread 0 of every CTA as its last action: the last CTA of the
 // launch resets the claim counter and the exit count for the next launch.
 __device__ __forceinline__ void finish_claims(int* counter, int* exited) {

@@ -66,10 +66,16 @@ def test_host_side_argument_checks(cpu_lib):
     assert cpu_lib.flamia_build_worklist(null, 1, 16, null, 0, null, null) == 1
     assert cpu_lib.flamia_build_worklist(ctypes.c_void_p(256), 1, 16, ctypes.c_void_p(256), 8,
                                          null, null) == 3
-    # flags not supported / bad scale
-    assert cpu_lib.flamia_attn_fwd(ctypes.byref(q), ctypes.byref(q), ctypes.byref(q), null, 1, 16,
-                                   1, 64, ctypes.c_float(0.1), 0x80, null, null, null, null,
-                                   null) == 2
+    # flags not supported (an unknown bit; static and dynamic scheduling at
+    # once; the ordered dQ turns with the static schedule) / bad scale
+    for flags in (0x1000, 0x40 | 0x80):
+        assert cpu_lib.flamia_attn_fwd(ctypes.byref(q), ctypes.byref(q), ctypes.byref(q), null, 1,
+                                       16, 1, 64, ctypes.c_float(0.1), flags, null, null, null,
+                                       null, null) == 2
+    assert cpu_lib.flamia_attn_bwd(ctypes.byref(q), ctypes.byref(q), ctypes.byref(q),
+                                   ctypes.byref(q), null, null, null, 1, 16, 1, 64,
+                                   ctypes.c_float(0.1), 0x8 | 0x40, null, null, null, null, null,
+                                   0, null, null) == 2
     assert cpu_lib.flamia_attn_bwd(ctypes.byref(q), ctypes.byref(q), ctypes.byref(q),
                                    ctypes.byref(q), null, null, null, 1, 16, 1, 64,
                                    ctypes.c_float(-1.0), 0, null, null, null, null, null, 0, null,
