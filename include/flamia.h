@@ -24,8 +24,10 @@
  *   int at `dev_status` (device memory, may be NULL to ignore) as
  *   FLAMIA_DEV_* bits; read it after synchronising the stream.  No kernel
  *   traps or spins without bound.
- * - Support.  head_dim d in {64, 128}; H >= 1; MHA (one K/V head per query
- *   head); causal masking; T < 2^24.
+ * - Support.  head_dim d in {64, 128}; 1 <= H <= 4096; T < 2^24 tokens,
+ *   T * H < 2^31, T * H * d < 2^40; multi-head attention, and grouped K / V
+ *   heads through the _gqa entry points; causal masking, or none with
+ *   FLAMIA_FLAG_NONCAUSAL.  Larger sizes return FLAMIA_ERR_INVALID_ARG.
  * - Formats.  E4M3 = OCP FP8 E4M3FN (bias 7, max 448, subnormals kept).
  *   E8M0 = 2^(byte - 127).  E2M1 = {0, .5, 1, 1.5, 2, 3, 4, 6} with sign,
  *   two codes per byte, element 2i in the low nibble.
