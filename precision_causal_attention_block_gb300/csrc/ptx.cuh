@@ -91,7 +91,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
-// A bounded wait taken by every lane of a converged warp, with one verdict
+// A bounded wait taken by every lane of a converged warp, with one outcome
 // for the whole warp (so the lanes never take different paths).
 __device__ __forceinline__ bool mbar_wait_w(uint32_t bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity));
