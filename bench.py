@@ -323,9 +323,13 @@ def run_ours(args, rank, world, local):
     value = job_throughput(flops, args.steps, world, res["total_ms"])
     e2e_value = job_throughput(flops, args.steps, world, res["e2e_ms"])
     achieved = bwd_flops / (res["bwd_ms"] * 1e-3) / 1e12
-    # quantiser x4, work list x6, forward + its short-document kernel, backward + its
-    # short-document kernel, dQ conversion (the dQ accumulator memset is a driver call)
-    launches_per_step = 4 + 6 + 2 + 2 + 1
+    # quantiser: one launch for Q, K, V (two with the rotation: V is not rotated)
+    # and one for dO; work list x6; forward + its short-document kernel; backward +
+    # its short-document kernel; dQ conversion; the FP16 accumulator's prescale
+    # table (two kernels sequence-wide, one causal).  The dQ accumulator memset
+    # is a driver call.
+    launches_per_step = ((3 if args.hadamard else 2) + 6 + 2 + 2 + 1 +
+                         {"fp32": 0, "fp16_sequence": 2, "fp16_causal": 1}[args.dq_accum])
     line = {
         "metric": "MXFP8 causal attn fwd+bwd TFLOP/s incl. quant; % of GB300 FP8 tensor peak",
         "value": round(value, 3),
