@@ -39,6 +39,9 @@ struct ShortParams {
   __nv_bfloat16 *dk, *dv;
   int hadamard;  // dK rotated back by H_d (Q and K were quantised rotated)
   int causal;    // 0: every query sees every key of its document
+  int skip_single;  // one-token documents were done by the one-thread kernels
+  int ppw;          // (document, head) pairs per warp: 32 when documents average <= 2
+                    // tokens (almost every pair is skipped), else 1
 };
 
 // d/32 E4M3 codes of one row (this lane's slice) decoded to floats.
@@ -107,18 +110,31 @@ __device__ __forceinline__ void store_bf16(__nv_bfloat16* __restrict__ dst, size
 }
 
 
+// The short-document kernels give each warp prm.ppw consecutive (document,
+// head) pairs: each of those lanes reads one pair's length, and the warp then
+// does, one after another, the pairs whose documents it handles (1 .. 32
+// tokens; from 2 when the one-thread kernels took the one-token documents).
+// Many pairs per warp only pay when nearly all are skipped (documents of
+// about one token); otherwise one pair per warp keeps the pairs in parallel.
+// Returns the mask of the lanes whose pair is done.
+__device__ __forceinline__ unsigned short_pairs(const ShortParams& prm, long long p0, int units,
+                                                int lane) {
+  const long long pr = p0 + lane;
+  int L = 0;
+  if (lane < prm.ppw && pr < static_cast<long long>(prm.ndocs) * units) {
+    const int doc = static_cast<int>(pr / units);
+    const int s = min(max(prm.cu[doc], 0), prm.T);
+    L = min(max(prm.cu[doc + 1], s), prm.T) - s;
+  }
+  return __ballot_sync(0xffffffffu, L >= (prm.skip_single ? 2 : 1) && L <= kShortDoc);
+}
+
 template <int DIM, bool NVF4>
-__global__ void __launch_bounds__(32 * kShortWarps)
-    attn_fwd_short_kernel(const ShortParams prm) {
-  const int lane = threadIdx.x & 31;
-  const long long wid = static_cast<long long>(blockIdx.x) * kShortWarps + (threadIdx.x >> 5);
+__device__ __forceinline__ void fwd_short_pair(const ShortParams& prm, int doc, int h, int lane) {
   const int H = prm.H, T = prm.T;
-  if (wid >= static_cast<long long>(prm.ndocs) * H) return;
-  const int doc = static_cast<int>(wid / H), h = static_cast<int>(wid % H);
   const int s = min(max(prm.cu[doc], 0), T);
   const int e = min(max(prm.cu[doc + 1], s), T);
   const int L = e - s;
-  if (L == 0 || L > kShortDoc) return;  // longer documents run on the tile kernels
   const size_t hT = static_cast<size_t>(h) * T;
   const int hk = h / prm.G, Hkv = prm.Hkv;
   const size_t hkT = static_cast<size_t>(hk) * T;
@@ -166,28 +182,35 @@ __global__ void __launch_bounds__(32 * kShortWarps)
   }
 }
 
-// GQA: one warp per (document, K / V head) walks the group's query heads; the
-// dK / dV rows of the document (at most 32) sum over them in this warp's part
-// of the dynamic shared memory (DIM floats per row, lane l owns its DIM / 32
-// columns).  Otherwise one warp per (document, head) and no accumulator.
-template <int DIM, bool NVF4, bool GQA>
+template <int DIM, bool NVF4>
 __global__ void __launch_bounds__(32 * kShortWarps)
-    attn_bwd_short_kernel(const ShortParams prm) {
-  // per warp: the document's 2^8 P (dV operand before rounding) and dS
-  __shared__ float s_p[kShortWarps][kShortDoc][kShortDoc + 1];
-  __shared__ float s_ds[kShortWarps][kShortDoc][kShortDoc + 1];
-  extern __shared__ float s_acc[];  // GQA: [warp][dK | dV][row][DIM]
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const long long wid = static_cast<long long>(blockIdx.x) * kShortWarps + w;
+    attn_fwd_short_kernel(const ShortParams prm) {
+  const int lane = threadIdx.x & 31;
+  const long long p0 =
+      (static_cast<long long>(blockIdx.x) * kShortWarps + (threadIdx.x >> 5)) * prm.ppw;
+  if (p0 >= static_cast<long long>(prm.ndocs) * prm.H) return;
+  for (unsigned todo = short_pairs(prm, p0, prm.H, lane); todo != 0; todo &= todo - 1) {
+    const long long pr = p0 + __ffs(todo) - 1;
+    fwd_short_pair<DIM, NVF4>(prm, static_cast<int>(pr / prm.H), static_cast<int>(pr % prm.H),
+                              lane);
+  }
+}
+
+// One (document, head) pair of the backward, by the whole warp.  GQA: the
+// pair is (document, K / V head) and walks the group's query heads; the dK /
+// dV rows of the document (at most 32) sum over them in this warp's part of
+// the dynamic shared memory (DIM floats per row, lane l owns its DIM / 32
+// columns).  s_p / s_ds: this warp's 2^8 P (the dV operand before rounding)
+// and dS of the document.
+template <int DIM, bool NVF4, bool GQA>
+__device__ __forceinline__ void bwd_short_pair(const ShortParams& prm, int doc, int u, int lane,
+                                               int w, float (*s_p)[kShortDoc + 1],
+                                               float (*s_ds)[kShortDoc + 1], float* s_acc) {
   const int H = prm.H, T = prm.T, Hkv = prm.Hkv, G = GQA ? prm.G : 1;
-  const int units = GQA ? Hkv : H;
-  if (wid >= static_cast<long long>(prm.ndocs) * units) return;
-  const int doc = static_cast<int>(wid / units), u = static_cast<int>(wid % units);
   const int hk = GQA ? u : u / prm.G;  // K / V head
   const int s = min(max(prm.cu[doc], 0), T);
   const int e = min(max(prm.cu[doc + 1], s), T);
   const int L = e - s;
-  if (L == 0 || L > kShortDoc) return;
   constexpr int N = DIM / 32;
   float* acck = s_acc + static_cast<size_t>(w) * 2 * kShortDoc * DIM;
   float* accv = acck + kShortDoc * DIM;
@@ -223,8 +246,8 @@ __global__ void __launch_bounds__(32 * kShortWarps)
         const float p8 = ex2_approx(fmaf(sd, cf, nl));
         const float d8 = p8 * fmaf(dp, gp, -Di);
         if (lane == 0) {
-          s_p[w][i][j] = p8;
-          s_ds[w][i][j] = d8;
+          s_p[i][j] = p8;
+          s_ds[i][j] = d8;
         }
         amax = fmaxf(amax, fabsf(d8));
       }
@@ -237,7 +260,7 @@ __global__ void __launch_bounds__(32 * kShortWarps)
     for (int i = 0; i < L; ++i) {
       float acc[N] = {};
       for (int j = 0; j <= (prm.causal ? i : L - 1); ++j) {
-        const float dsh = e4m3x2_to_float2(cvt_e4m3x2(s_ds[w][i][j] * inv, 0.f)).x * dsc;
+        const float dsh = e4m3x2_to_float2(cvt_e4m3x2(s_ds[i][j] * inv, 0.f)).x * dsc;
         float k[N];
         load_codes<DIM>(prm.kc, static_cast<size_t>(s + j) * Hkv + hk, lane, k);
 #pragma unroll
@@ -260,8 +283,8 @@ __global__ void __launch_bounds__(32 * kShortWarps)
     for (int j = 0; j < L; ++j) {
       float ak[N] = {}, av[N] = {};
       for (int i = prm.causal ? j : 0; i < L; ++i) {
-        const float dsh = e4m3x2_to_float2(cvt_e4m3x2(s_ds[w][i][j] * inv, 0.f)).x * dsc;
-        const float pb = e4m3x2_to_float2(cvt_e4m3x2(s_p[w][i][j], 0.f)).x;
+        const float dsh = e4m3x2_to_float2(cvt_e4m3x2(s_ds[i][j] * inv, 0.f)).x * dsc;
+        const float pb = e4m3x2_to_float2(cvt_e4m3x2(s_p[i][j], 0.f)).x;
         float q[N], g[N];
         load_codes<DIM>(prm.qc, static_cast<size_t>(s + i) * H + h, lane, q);
         load_codes<DIM>(prm.doc_, static_cast<size_t>(s + i) * H + h, lane, g);
@@ -306,6 +329,163 @@ __global__ void __launch_bounds__(32 * kShortWarps)
   }
 }
 
+template <int DIM, bool NVF4, bool GQA>
+__global__ void __launch_bounds__(32 * kShortWarps)
+    attn_bwd_short_kernel(const ShortParams prm) {
+  __shared__ float s_p[kShortWarps][kShortDoc][kShortDoc + 1];
+  __shared__ float s_ds[kShortWarps][kShortDoc][kShortDoc + 1];
+  extern __shared__ float s_acc[];  // GQA: [warp][dK | dV][row][DIM]
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int units = GQA ? prm.Hkv : prm.H;
+  const long long p0 = (static_cast<long long>(blockIdx.x) * kShortWarps + w) * prm.ppw;
+  if (p0 >= static_cast<long long>(prm.ndocs) * units) return;
+  for (unsigned todo = short_pairs(prm, p0, units, lane); todo != 0; todo &= todo - 1) {
+    const long long pr = p0 + __ffs(todo) - 1;
+    bwd_short_pair<DIM, NVF4, GQA>(prm, static_cast<int>(pr / units), static_cast<int>(pr % units),
+                                   lane, w, s_p[w], s_ds[w], s_acc);
+  }
+}
+
+// ------------------------------------------------------ one-token documents
+// A document of one token is one score per head: one thread per (document,
+// head) does it with whole-row loads, the same numerics as the warp kernels
+// (integer maximum, E4M3 P^, the document's one dS exponent); only the order
+// of the float32 dot-product sums differs.  Packed E4M3 codes of a row,
+// 16 at a time.
+template <int DIM>
+__device__ __forceinline__ void decode16(const uint4 w, float (&x)[16]) {
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 a = e4m3x2_to_float2(u[i] & 0xFFFFu), b = e4m3x2_to_float2(u[i] >> 16);
+    x[4 * i] = a.x;
+    x[4 * i + 1] = a.y;
+    x[4 * i + 2] = b.x;
+    x[4 * i + 3] = b.y;
+  }
+}
+
+template <int DIM>
+__device__ __forceinline__ float row_dot(const uint8_t* __restrict__ a, const uint8_t* __restrict__ b) {
+  float acc = 0.f;
+#pragma unroll 4
+  for (int c = 0; c < DIM / 16; ++c) {
+    float x[16], y[16];
+    decode16<DIM>(__ldg(reinterpret_cast<const uint4*>(a) + c), x);
+    decode16<DIM>(__ldg(reinterpret_cast<const uint4*>(b) + c), y);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc = fmaf(x[i], y[i], acc);
+  }
+  return acc;
+}
+
+// f * codes of a row, as BF16, 16 elements (32 bytes) at a time.
+template <int DIM>
+__device__ __forceinline__ void store_scaled_bf16(__nv_bfloat16* __restrict__ dst,
+                                                  const uint8_t* __restrict__ src, float p,
+                                                  float f) {
+#pragma unroll 2
+  for (int c = 0; c < DIM / 16; ++c) {
+    float x[16];
+    decode16<DIM>(__ldg(reinterpret_cast<const uint4*>(src) + c), x);
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      // (p code) rounded as the warp kernels' fmaf(p, code, 0), then times f
+      const __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(p, x[2 * i]) * f,
+                                                      __fmul_rn(p, x[2 * i + 1]) * f);
+      w[i] = *reinterpret_cast<const uint32_t*>(&b2);
+    }
+    uint4* d4 = reinterpret_cast<uint4*>(dst) + 2 * c;
+    d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+}
+
+template <int DIM>
+__global__ void __launch_bounds__(256, 4) attn_fwd_single_kernel(const ShortParams prm) {
+  const long long pair = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int H = prm.H, T = prm.T;
+  if (pair >= static_cast<long long>(prm.ndocs) * H) return;
+  const int doc = static_cast<int>(pair / H), h = static_cast<int>(pair % H);
+  const int s = min(max(prm.cu[doc], 0), T);
+  const int e = min(max(prm.cu[doc + 1], s), T);
+  if (e - s != 1) return;
+  const int hk = h / prm.G;
+  const size_t hT = static_cast<size_t>(h) * T, hkT = static_cast<size_t>(hk) * T;
+  const size_t qrow = static_cast<size_t>(s) * H + h, krow = static_cast<size_t>(s) * prm.Hkv + hk;
+  const float cf = prm.scale_log2 * pow2_or_zero_s(static_cast<int>(prm.qs[hT + s]) - 127) *
+                   pow2_or_zero_s(static_cast<int>(prm.ks[hkT + s]) - 127);
+  const float vsc = pow2_or_zero_s(static_cast<int>(prm.vs[hkT + s]) - 127);
+  const float sj = row_dot<DIM>(prm.qc + qrow * DIM, prm.kc + krow * DIM);
+  const float m = ceilf(sj * cf);
+  const float p8 = ex2_approx(fmaf(sj, cf, -(m - 8.f)));
+  const float ph = e4m3x2_to_float2(cvt_e4m3x2(p8, 0.f)).x;
+  store_scaled_bf16<DIM>(prm.o + qrow * DIM, prm.vc + krow * DIM, ph, vsc / p8);
+  prm.lse[hT + s] = (m - 8.f + __log2f(p8)) * 0.69314718055994530942f;
+}
+
+// Multi-head attention without the rotation (the warp kernel does the rest).
+template <int DIM>
+__global__ void __launch_bounds__(256, 4) attn_bwd_single_kernel(const ShortParams prm) {
+  const long long pair = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int H = prm.H, T = prm.T;
+  if (pair >= static_cast<long long>(prm.ndocs) * H) return;
+  const int doc = static_cast<int>(pair / H), h = static_cast<int>(pair % H);
+  const int s = min(max(prm.cu[doc], 0), T);
+  const int e = min(max(prm.cu[doc + 1], s), T);
+  if (e - s != 1) return;
+  const size_t hT = static_cast<size_t>(h) * T, row = static_cast<size_t>(s) * H + h;
+  const int eq = static_cast<int>(prm.qs[hT + s]) - 127, ek = static_cast<int>(prm.ks[hT + s]) - 127;
+  const int ev = static_cast<int>(prm.vs[hT + s]) - 127, edo = static_cast<int>(prm.dos[hT + s]) - 127;
+  const float cf = prm.scale_log2 * pow2_or_zero_s(eq) * pow2_or_zero_s(ek);
+  const float gp = pow2_or_zero_s(ev) * pow2_or_zero_s(edo);
+  const float sd = row_dot<DIM>(prm.qc + row * DIM, prm.kc + row * DIM);
+  const float dp = row_dot<DIM>(prm.doc_ + row * DIM, prm.vc + row * DIM);
+  const float nl = 8.f - prm.lse_in[hT + s] * 1.4426950408889634f;
+  const float p8 = ex2_approx(fmaf(sd, cf, nl));
+  const float d8 = p8 * fmaf(dp, gp, -prm.D[hT + s]);
+  // the document's one 32x32 dS block holds this one element
+  const int eb = max(roundup_exponent(fabsf(d8)) - 8, -127);
+  const float dsh = e4m3x2_to_float2(cvt_e4m3x2(d8 * exp2i(-(eb + 8)), 0.f)).x * pow2_or_zero_s(eb);
+  const float pb = e4m3x2_to_float2(cvt_e4m3x2(p8, 0.f)).x;
+  // dQ row of the accumulator: dS^ K^ (softmax_scale comes in the conversion)
+  const float mul = pow2_or_zero_s(ek);
+  const uint8_t* kc = prm.kc + row * DIM;
+#pragma unroll 2
+  for (int c = 0; c < DIM / 16; ++c) {
+    float x[16];
+    decode16<DIM>(__ldg(reinterpret_cast<const uint4*>(kc) + c), x);
+    if (prm.dq_pre == nullptr) {
+      float4* d4 = reinterpret_cast<float4*>(prm.dq_acc + row * DIM) + 4 * c;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        d4[i] = make_float4(__fmul_rn(dsh, x[4 * i]) * mul, __fmul_rn(dsh, x[4 * i + 1]) * mul,
+                            __fmul_rn(dsh, x[4 * i + 2]) * mul, __fmul_rn(dsh, x[4 * i + 3]) * mul);
+    } else {
+      const float pre = exp2i(prm.dq_pre[hT + s]);
+      uint32_t w[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const __half2 h2 = __floats2half2_rn((__fmul_rn(dsh, x[2 * i]) * mul) * pre,
+                                             (__fmul_rn(dsh, x[2 * i + 1]) * mul) * pre);
+        w[i] = *reinterpret_cast<const uint32_t*>(&h2);
+      }
+      uint4* d4 = reinterpret_cast<uint4*>(reinterpret_cast<__half*>(prm.dq_acc) + row * DIM) + 2 * c;
+      d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+  }
+  // dK = scale 2^eq dS^ Q^,  dV = 2^(edo - 8) P^b dO^
+  store_scaled_bf16<DIM>(prm.dk + row * DIM, prm.qc + row * DIM, dsh,
+                         prm.sm_scale * pow2_or_zero_s(eq));
+  store_scaled_bf16<DIM>(prm.dv + row * DIM, prm.doc_ + row * DIM, pb,
+                         pow2_or_zero_s(edo) * (1.f / 256.f));
+}
+
+// Pairs per warp of the short-document kernels (see short_pairs).
+inline int short_ppw(int T, int ndocs) { return static_cast<long long>(T) <= 2ll * ndocs ? 32 : 1; }
+
 ShortParams make_params(const flamia_qtensor* q, const flamia_qtensor* k, const flamia_qtensor* v,
                         const int32_t* cu, int ndocs, int T, int H, int Hkv,
                         float softmax_scale) {
@@ -328,11 +508,13 @@ ShortParams make_params(const flamia_qtensor* q, const flamia_qtensor* k, const 
   p.ndocs = ndocs;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
   p.sm_scale = softmax_scale;
+  p.ppw = short_ppw(T, ndocs);
   return p;
 }
 
-inline unsigned short_grid(int ndocs, int H) {
-  const long long warps = static_cast<long long>(ndocs) * H;
+// CTAs of a short-document kernel.
+inline unsigned short_grid(int ndocs, int H, int ppw) {
+  const long long warps = (static_cast<long long>(ndocs) * H + ppw - 1) / ppw;
   return static_cast<unsigned>((warps + kShortWarps - 1) / kShortWarps);
 }
 
@@ -346,7 +528,15 @@ cudaError_t launch_fwd_short(const flamia_qtensor* q, const flamia_qtensor* k,
   p.causal = causal ? 1 : 0;
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
-  const unsigned grid = short_grid(ndocs, H);
+  const unsigned grid = short_grid(ndocs, H, p.ppw);
+  if (!nvfp4_qk) {  // one-token documents: one thread per (document, head)
+    const unsigned g1 = static_cast<unsigned>((static_cast<long long>(ndocs) * H + 255) / 256);
+    if (d == 128)
+      attn_fwd_single_kernel<128><<<g1, 256, 0, stream>>>(p);
+    else
+      attn_fwd_single_kernel<64><<<g1, 256, 0, stream>>>(p);
+    p.skip_single = 1;
+  }
   if (nvfp4_qk)
     attn_fwd_short_kernel<64, true><<<grid, 32 * kShortWarps, 0, stream>>>(p);
   else if (d == 128)
@@ -373,8 +563,16 @@ cudaError_t launch_bwd_short(const flamia_qtensor* q, const flamia_qtensor* k,
   p.dq_pre = dq_pre;
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
+  if (Hkv == H && !nvfp4_qk && !hadamard) {  // one-token documents: one thread each
+    const unsigned g1 = static_cast<unsigned>((static_cast<long long>(ndocs) * H + 255) / 256);
+    if (d == 128)
+      attn_bwd_single_kernel<128><<<g1, 256, 0, stream>>>(p);
+    else
+      attn_bwd_single_kernel<64><<<g1, 256, 0, stream>>>(p);
+    p.skip_single = 1;
+  }
   if (Hkv == H) {
-    const unsigned grid = short_grid(ndocs, H);
+    const unsigned grid = short_grid(ndocs, H, p.ppw);
     if (nvfp4_qk)
       attn_bwd_short_kernel<64, true, false><<<grid, 32 * kShortWarps, 0, stream>>>(p);
     else if (d == 128)
@@ -385,7 +583,7 @@ cudaError_t launch_bwd_short(const flamia_qtensor* q, const flamia_qtensor* k,
   }
   // grouped query heads: one warp per (document, K / V head), dK / dV sums in
   // dynamic shared memory (2 x 32 rows x d floats per warp)
-  const unsigned grid = short_grid(ndocs, Hkv);
+  const unsigned grid = short_grid(ndocs, Hkv, p.ppw);
   const size_t smem = static_cast<size_t>(kShortWarps) * 2 * kShortDoc * d * sizeof(float);
   cudaError_t err;
   if (nvfp4_qk) {

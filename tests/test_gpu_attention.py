@@ -263,3 +263,34 @@ def test_nvfp4_flag_needs_head_dim_64(lib):
     x = W.make_inputs_bf16(w)
     with pytest.raises(RuntimeError, match="unsupported"):
         run_call(w, x, nvfp4=True)
+
+
+@pytest.mark.parametrize("d,H,Hkv,kw", [(128, 3, 3, {}), (64, 2, 2, {"nvfp4_qk": True}),
+                                         (128, 4, 2, {}), (64, 2, 2, {"hadamard": True}),
+                                         (64, 2, 2, {"causal": False})])
+def test_mostly_one_token_documents(lib, d, H, Hkv, kw):
+    """Documents averaging under two tokens (the one-thread kernels take the
+    one-token documents; each warp of the short-document kernels scans 32
+    (document, head) pairs) with a few longer ones mixed in, element by
+    element against the oracle."""
+    from precision_causal_attention_block_gb300 import flamia as fl
+    rng = np.random.default_rng(7)
+    lengths = [1] * 400
+    for L, at in zip((2, 5, 17, 31, 32, 0, 3, 40), rng.choice(400, 8, replace=False)):
+        lengths[at] = L
+    w = W.custom("mostly_one", lengths, H, d, seed=11)
+    assert w.T <= 2 * len(lengths)
+    x = W.make_inputs_bf16(w)
+    x["k"], x["v"] = x["k"][:, :Hkv].contiguous(), x["v"][:, :Hkv].contiguous()
+    call = fl.TrainingCall(w.T, H, d, cu_tensor(w.cu_seqlens), w.sm_scale, H_kv=Hkv, **kw)
+    xd = {n: dev(t) for n, t in x.items()}
+    call.forward(xd["q"], xd["k"], xd["v"])
+    call.backward(xd["do"])
+    torch.cuda.synchronize()
+    call.check_status()
+    ref = O.attention(*[x[n].double().numpy() for n in NAMES], w.cu_seqlens, w.sm_scale,
+                      qk_format="nvfp4" if kw.get("nvfp4_qk") else "mxfp8",
+                      causal=kw.get("causal", True), hadamard=kw.get("hadamard", False))
+    rel = 3e-2 if kw.get("hadamard") else 2e-2
+    for n, t in (("O", call.o), ("dQ", call.dq), ("dK", call.dk), ("dV", call.dv)):
+        compare(n, np64(t), ref[n], rel_max=rel)
