@@ -267,7 +267,9 @@ def test_nvfp4_flag_needs_head_dim_64(lib):
 
 @pytest.mark.parametrize("d,H,Hkv,kw", [(128, 3, 3, {}), (64, 2, 2, {"nvfp4_qk": True}),
                                          (128, 4, 2, {}), (64, 2, 2, {"hadamard": True}),
-                                         (64, 2, 2, {"causal": False})])
+                                         (64, 2, 2, {"causal": False}),
+                                         (128, 2, 2, {"dq_accum": "fp16_causal"}),
+                                         (64, 2, 2, {"deterministic_dq": True})])
 def test_mostly_one_token_documents(lib, d, H, Hkv, kw):
     """Documents averaging under two tokens (the one-thread kernels take the
     one-token documents; each warp of the short-document kernels scans 32
@@ -290,7 +292,8 @@ def test_mostly_one_token_documents(lib, d, H, Hkv, kw):
     call.check_status()
     ref = O.attention(*[x[n].double().numpy() for n in NAMES], w.cu_seqlens, w.sm_scale,
                       qk_format="nvfp4" if kw.get("nvfp4_qk") else "mxfp8",
-                      causal=kw.get("causal", True), hadamard=kw.get("hadamard", False))
+                      causal=kw.get("causal", True), hadamard=kw.get("hadamard", False),
+                      dq_accum=kw.get("dq_accum", "fp32"))
     rel = 3e-2 if kw.get("hadamard") else 2e-2
     for n, t in (("O", call.o), ("dQ", call.dq), ("dK", call.dk), ("dV", call.dv)):
         compare(n, np64(t), ref[n], rel_max=rel)
