@@ -44,6 +44,16 @@ flamia_status flamia_debug_mma_tile(int mode, int N, int a_mn_major, int b_mn_ma
                                     const uint8_t* sfb, float* d_out, int* dev_status,
                                     void* stream);
 
+/*
+ * The library's bounded waits running out on purpose: one thread waits on an
+ * mbarrier that nothing arrives on, then on a dQ turn counter (device int,
+ * zeroed by this call) that nothing passes, with the kernels' own wait
+ * helpers; each gives up after its time limit (2 s) and ORs FLAMIA_DEV_TIMEOUT
+ * into *dev_status.  Nothing hangs or faults, and the context stays usable.
+ * turn: device int the call may write.
+ */
+flamia_status flamia_debug_bounded_waits(int* turn, int* dev_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

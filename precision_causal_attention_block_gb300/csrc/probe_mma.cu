@@ -157,6 +157,29 @@ __global__ void __launch_bounds__(128, 1)
 
 using namespace flamia;
 
+namespace flamia {
+namespace {
+
+__global__ void bounded_waits_kernel(int* turn, int* status) {
+  __shared__ alignas(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(smem_u32(&bar), 1);
+  fence_barrier_init();
+  if (!mbar_wait(smem_u32(&bar), 0)) report(status, FLAMIA_DEV_TIMEOUT);  // nobody arrives
+  if (!wait_turn(turn, 1)) report(status, FLAMIA_DEV_TIMEOUT);           // nobody passes
+}
+
+}  // namespace
+}  // namespace flamia
+
+extern "C" flamia_status flamia_debug_bounded_waits(int* turn, int* dev_status, void* stream) {
+  if (turn == nullptr || dev_status == nullptr) return FLAMIA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(turn, 0, sizeof(int), s) != cudaSuccess) return FLAMIA_ERR_CUDA;
+  flamia::bounded_waits_kernel<<<1, 32, 0, s>>>(turn, dev_status);
+  return cudaGetLastError() == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
+}
+
 extern "C" flamia_status flamia_debug_mma_tile(int mode, int N, int a_mn_major, int b_mn_major,
                                                int variant, const uint8_t* a, const uint8_t* b,
                                                const uint8_t* sfa, const uint8_t* sfb,

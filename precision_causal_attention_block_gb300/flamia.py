@@ -58,6 +58,7 @@ SIGNATURES = {
     "flamia_build_worklist_static": (_i, [_vp, _i, _i, _vp, _sz, _vp, _vp]),
     "flamia_status_str": (ctypes.c_char_p, [_i]),
     "flamia_debug_mma_tile": (_i, [_i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "flamia_debug_bounded_waits": (_i, [_vp, _vp, _vp]),
 }
 
 
@@ -196,6 +197,11 @@ def flamia_attn_bwd_gqa(q: QTensor, k: QTensor, v: QTensor, dout: QTensor, D, ls
                                       flags, _ptr(wl), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws),
                                       ws.numel() * ws.element_size(), _ptr(dev_status),
                                       _stream()), "flamia_attn_bwd_gqa")
+
+
+def flamia_debug_bounded_waits(turn, dev_status):
+    _check(load().flamia_debug_bounded_waits(_ptr(turn), _ptr(dev_status), _stream()),
+           "flamia_debug_bounded_waits")
 
 
 def flamia_debug_mma_tile(mode, N, a_mn, b_mn, variant, a, b, sfa, sfb, d_out, dev_status=None):
