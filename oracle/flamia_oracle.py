@@ -58,6 +58,9 @@ Readings where the pages are silent:
 * the dS block exponent uses the same round-up rule on the 32x32 block
   maximum (masked entries are 0); the softmax scale is applied after the
   dQ / dK products;
+* query-row dS exponents (an option): for the dQ product only, one round-up
+  exponent per query row and 32-key block; dK keeps the 32x32 block ones
+  (only dQ of an earlier row can see a later row through a shared exponent);
 * the NVFP4 scale is the smallest E4M3 value >= amax / 6, no tensor-wide
   scale;
 * the rotation is the unnormalised Sylvester-Hadamard matrix H_d (entries
@@ -429,14 +432,30 @@ def _block_quantize_dS(dS: np.ndarray, r0: int, c0: int) -> np.ndarray:
     return out
 
 
+def _row_quantize_dS(dS: np.ndarray, c0: int) -> np.ndarray:
+    """dS rounded through E4M3 with one round-up exponent per query row and
+    32-column block aligned to the document start (c0: doc-local offset of the
+    first column, a multiple of 32): review page, sec. 3.2, the query-row-wise
+    dS exponents that remove the leakage inside blocks."""
+    assert c0 % 32 == 0
+    out = np.empty_like(dS)
+    for j0 in range(0, dS.shape[1], 32):
+        blk = dS[:, j0:j0 + 32]
+        e = roundup_exponent(np.abs(blk).max(axis=1))[:, None]
+        out[:, j0:j0 + 32] = e4m3_decode(e4m3_encode(blk * np.ldexp(1.0, -e))) * np.ldexp(1.0, e)
+    return out
+
+
 def bwd_rect(dh: DocHead, rows: np.ndarray, cols: np.ndarray, lse2_rows: np.ndarray,
-             D_rows: np.ndarray, sm_scale: float, quant: bool = True, raw_dq: bool = False):
+             D_rows: np.ndarray, sm_scale: float, quant: bool = True, raw_dq: bool = False,
+             ds_rows: bool = False):
     """Backward contributions of the rectangle rows x cols.
 
     rows and cols are contiguous doc-local ranges starting on a 32 boundary.
     Returns (dQ partial [R, d] over these cols, dK partial [C, d] and dV
     partial [C, d] over these rows, dS [R, C]); with raw_dq the dQ partial is
-    the product dS^ K^ before the softmax scale."""
+    the product dS^ K^ before the softmax scale.  ds_rows: the dQ product takes
+    dS rounded with query-row exponents (dK keeps the 32x32 block ones)."""
     s = _scores(dh, rows, cols, sm_scale)
     P = np.exp2(s - lse2_rows[:, None])                        # normalised, 0 where masked
     pb = np.ldexp(P, P_SCALE_LOG2)
@@ -450,7 +469,8 @@ def bwd_rect(dh: DocHead, rows: np.ndarray, cols: np.ndarray, lse2_rows: np.ndar
     khat = dh.k[cols] * np.ldexp(1.0, dh.ek[cols])[:, None]
     dV = np.ldexp(pbh.T @ dohat, -P_SCALE_LOG2)
     dK = sm_scale * (dSh.T @ qhat)
-    dQ = (dSh @ khat) if raw_dq else sm_scale * (dSh @ khat)
+    dSq = _row_quantize_dS(dS, int(cols[0])) if (quant and ds_rows) else dSh
+    dQ = (dSq @ khat) if raw_dq else sm_scale * (dSq @ khat)
     return dQ, dK, dV, dS
 
 
@@ -518,14 +538,16 @@ def fp16_round(x) -> np.ndarray:
 
 
 def dq_fp16_rows(dh: DocHead, rows: np.ndarray, lse2_rows: np.ndarray, D_rows: np.ndarray,
-                 sm_scale: float, p_rows: np.ndarray, return_acc: bool = False):
+                 sm_scale: float, p_rows: np.ndarray, return_acc: bool = False,
+                 ds_rows: bool = False):
     """dQ of the given rows (doc-local, from 0, a multiple-of-32 start)
     through the prescaled FP16 accumulator."""
     f = np.ldexp(1.0, np.asarray(p_rows, dtype=np.int64))[:, None]
     acc = np.zeros((len(rows), dh.q.shape[1]))
     for t0 in reversed(range(0, dh.L, DQ16_KEY_TILE)):
         cols = np.arange(t0, min(t0 + DQ16_KEY_TILE, dh.L))
-        part, _, _, _ = bwd_rect(dh, rows, cols, lse2_rows, D_rows, sm_scale, True, raw_dq=True)
+        part, _, _, _ = bwd_rect(dh, rows, cols, lse2_rows, D_rows, sm_scale, True, raw_dq=True,
+                                 ds_rows=ds_rows)
         x = fp16_round((part * f).astype(np.float32))
         acc = fp16_round(acc + x)                    # the sum of two FP16 values is exact here
     dq = sm_scale * acc / f
@@ -578,7 +600,7 @@ def exact_dochead(q, k, v, do, cu, b, h) -> DocHead:
 def attention(q, k, v, do, cu_seqlens, sm_scale: float, quant: bool = True,
               qk_format: str = "mxfp8", rule: str = "up", group: str = "block",
               heads=None, docs=None, backward: bool = True, hadamard: bool = False,
-              causal: bool = True, dq_accum: str = "fp32"):
+              causal: bool = True, dq_accum: str = "fp32", ds_rows: bool = False):
     """Full forward (+ backward) over packed [T, H, d] float64 inputs.
 
     Returns a dict with O [T, H, d] (float64), O_bf16, lse [H, T] (natural log,
@@ -592,7 +614,8 @@ def attention(q, k, v, do, cu_seqlens, sm_scale: float, quant: bool = True,
     ([T, H_kv, d]) sum over the query heads of each K / V head.
     ``dq_accum``: "fp32" (float32 sums, no prescale), "fp16_sequence" or
     "fp16_causal" (the prescaled FP16 accumulator of dq_fp16_rows, with the
-    prescale table returned as ``dq_prescale`` [H, T])."""
+    prescale table returned as ``dq_prescale`` [H, T]).  ``ds_rows``: dQ from
+    dS rounded with query-row exponents (see _row_quantize_dS)."""
     q = np.asarray(q, dtype=np.float64)
     T, H, d = q.shape
     Hkv = np.asarray(k).shape[1]
@@ -601,7 +624,7 @@ def attention(q, k, v, do, cu_seqlens, sm_scale: float, quant: bool = True,
         rot = hadamard_fp32 if quant else (lambda x: np.asarray(x, dtype=np.float64) @ sylvester(d))
         r = attention(rot(q), rot(k), v, do, cu_seqlens, sm_scale / d, quant, qk_format, rule,
                       group, heads, docs, backward, hadamard=False, causal=causal,
-                      dq_accum=dq_accum)
+                      dq_accum=dq_accum, ds_rows=ds_rows)
         if backward:
             hd = sylvester(d)
             r["dQ"] = r["dQ"] @ hd
@@ -642,9 +665,10 @@ def attention(q, k, v, do, cu_seqlens, sm_scale: float, quant: bool = True,
             o_for_D = out["O_bf16"][s:e, h] if quant else o
             D = (dohat * o_for_D).sum(axis=1)
             out["D"][h, s:e] = D
-            dQ, dK, dV, _ = bwd_rect(dh, rows, rows, lse2, D, sm_scale, quant)
+            dQ, dK, dV, _ = bwd_rect(dh, rows, rows, lse2, D, sm_scale, quant, ds_rows=ds_rows)
             if dq16:
-                dQ = dq_fp16_rows(dh, rows, lse2, D, sm_scale, out["dq_prescale"][h, s:e])
+                dQ = dq_fp16_rows(dh, rows, lse2, D, sm_scale, out["dq_prescale"][h, s:e],
+                                  ds_rows=ds_rows)
             hk = h // (H // Hkv)
             out["dQ"][s:e, h] = dQ
             out["dK"][s:e, hk] += dK

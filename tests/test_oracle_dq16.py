@@ -3,7 +3,8 @@
 exponents set by hand, the range the prescale promises on an input built to
 reach the bound, the leakage the pages attribute to the sequence-wide
 prescale and its removal by causal dQ scaling, and closeness to the float32
-accumulator."""
+accumulator; and of the query-row dS exponents (same page, sec. 3.2: they
+remove the leakage inside blocks): exponents by hand and the in-block leak."""
 import numpy as np
 import pytest
 
@@ -121,3 +122,43 @@ def test_causal_scaling_removes_the_sequence_dependence(mix):
     # ... while the late rows themselves change in every mode
     a, b = run(x, cu, scale, "fp16_causal"), run(y, cu, scale, "fp16_causal")
     assert not np.array_equal(a["dQ"][250:300], b["dQ"][250:300])
+
+
+def test_row_ds_exponents_by_hand():
+    # one 2 x 32 dS block: the block rule gives both rows the large row's
+    # exponent, the row rule gives each row its own.  E4M3 keeps 3 mantissa
+    # bits over its normal range, so a shared exponent only costs precision
+    # where it pushes a row below 2^-6 (the subnormals): here by 2^16.
+    dS = np.zeros((2, 32))
+    dS[0, :] = 1.0 + np.arange(32) / 64.0       # row max 1.484 -> exponent -8
+    dS[1, 5] = 1.5 * 2.0 ** 16                  # row max 98304 -> exponent 8
+    blk = O._block_quantize_dS(dS, 0, 0)
+    row = O._row_quantize_dS(dS, 0)
+    assert O.roundup_exponent(np.array([1.484375]))[0] == -8
+    assert O.roundup_exponent(np.array([1.5 * 2.0 ** 16]))[0] == 8
+    assert np.array_equal(row[0], O.e4m3_decode(O.e4m3_encode(dS[0] * 2.0 ** 8)) * 2.0 ** -8)
+    assert np.array_equal(blk[0], O.e4m3_decode(O.e4m3_encode(dS[0] * 2.0 ** -8)) * 2.0 ** 8)
+    assert np.array_equal(row[1], blk[1])
+    # row 0: within 1/16 relative with its own exponent, subnormal steps of
+    # 2^-9 x 2^8 = 1/2 with the shared one
+    assert np.abs(row[0] - dS[0]).max() <= dS[0].max() / 16
+    assert np.abs(blk[0] - dS[0]).max() >= 0.2
+
+
+def test_row_ds_exponents_remove_the_in_block_leak(mix):
+    # a later query row in the same 32-row block as earlier rows (row 40 of the
+    # first document, block [32, 64)): with the block exponents its dO moves
+    # the rounding of the earlier rows' dQ; with query-row exponents it cannot
+    x, cu, scale = mix
+    y = {n: t.copy() for n, t in x.items()}
+    y["do"][40] *= 64.0
+    early = slice(32, 40)
+    for ds_rows, same in ((False, False), (True, True)):
+        a = O.attention(x["q"], x["k"], x["v"], x["do"], cu, scale, ds_rows=ds_rows)
+        b = O.attention(y["q"], y["k"], y["v"], y["do"], cu, scale, ds_rows=ds_rows)
+        assert np.array_equal(a["dQ"][early], b["dQ"][early]) == same, ds_rows
+        assert np.array_equal(a["dQ"][:32], b["dQ"][:32])  # other blocks: never
+    r = O.attention(x["q"], x["k"], x["v"], x["do"], cu, scale, ds_rows=True)
+    f = O.attention(x["q"], x["k"], x["v"], x["do"], cu, scale)
+    assert O.cosine(r["dQ"], f["dQ"]) >= 0.9999
+    assert np.array_equal(r["dK"], f["dK"]) and np.array_equal(r["dV"], f["dV"])
