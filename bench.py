@@ -177,7 +177,7 @@ def run_ours(args, rank, world, local):
     call = fl.TrainingCall(w.T, w.H, w.d, cu, w.sm_scale, nvfp4_qk=args.nvfp4,
                            hadamard=args.hadamard, causal=not args.noncausal, H_kv=hkv,
                            deterministic_dq=args.deterministic, dq_accum=args.dq_accum,
-                           schedule=args.schedule, device=dev)
+                           schedule=args.schedule, ds_rows=args.ds_rows, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -237,7 +237,7 @@ def run_ours(args, rank, world, local):
                                    nvfp4_qk=args.nvfp4, hadamard=args.hadamard,
                                    causal=not args.noncausal, H_kv=hkv,
                                    deterministic_dq=args.deterministic, dq_accum=args.dq_accum,
-                                   schedule=args.schedule, device=dev)]
+                                   schedule=args.schedule, ds_rows=args.ds_rows, device=dev)]
     xin = [xd, {n: torch.empty_like(t) for n, t in xd.items()}]
     outs = lambda c: (c.o, c.dq, c.dk, c.dv)
     hout = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs(c)] for c in calls]
@@ -351,6 +351,7 @@ def run_ours(args, rank, world, local):
                    "dq_sum": "ordered (deterministic)" if args.deterministic else "atomic",
                    "dq_accumulator": args.dq_accum,
                    "schedule": args.schedule,
+                   "ds_exponents": "query row" if args.ds_rows else "32x32 block",
                    "flops_per_step": flops, "l2": "flushed (256 MB write) before every step",
                    "parallelism": f"replicas x{world}"},
         "pct_of_fp8_peak": round(100.0 * value / world / pk["fp8_tflops"], 2),
@@ -363,7 +364,7 @@ def run_ours(args, rank, world, local):
                      "peak_source": pk["source"],
                      "traffic": None if (args.hadamard or args.noncausal or hkv != w.H or
                                          args.deterministic or args.dq_accum != "fp32" or
-                                         args.schedule != "dynamic")
+                                         args.schedule != "dynamic" or args.ds_rows)
                      else profiled_traffic(w, args.nvfp4),
                      "traffic_unit": "bytes per launch of the attention kernel (ncu, DRAM read + write)"},
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
@@ -538,6 +539,8 @@ def main():
                     help="work distribution of the persistent kernels (rule: the pages' choice, "
                          "dynamic for causal calls, static for non-causal ones unless the "
                          "longest document is at least 4x the average)")
+    ap.add_argument("--ds-rows", action="store_true",
+                    help="dQ's dS operand with one exponent per (query row, 32-key block)")
     ap.add_argument("--deterministic", action="store_true",
                     help="dQ partials added in a fixed key-tile order (bitwise reproducible)")
     args = ap.parse_args()

@@ -84,6 +84,10 @@ typedef enum {
                                        take their work items in a static snake
                                        over the cost-sorted list instead of
                                        claiming the next unclaimed item        */
+#define FLAMIA_FLAG_DS_ROW_EXPONENTS 0x100 /* backward only, head dim 128: dQ's dS
+                                       operand rounded with one exponent per
+                                       (query row, 32-key block) instead of per
+                                       32 x 32 block (dK keeps the block ones) */
 #define FLAMIA_FLAG_SCHEDULE_RULE 0x80 /* forward / backward: the pages' rule,
                                        dynamic claims for causal calls and, for
                                        non-causal ones, only when the longest
@@ -299,6 +303,13 @@ size_t flamia_bwd_workspace_bytes(int T, int H, int d);
  * shortest first, so a key tile never waits for one claimed after it), and
  * O, dQ, dK and dV are bitwise reproducible.  A wait that times out (2 s)
  * sets FLAMIA_DEV_TIMEOUT.
+ * FLAMIA_FLAG_DS_ROW_EXPONENTS (review page, sec. 3.2: the query-row-wise dS
+ * exponents that remove the leakage inside blocks): a 32 x 32 dS block
+ * shares one exponent across 32 query rows, so a later row's gradient moves
+ * the rounding of an earlier row's dQ; with the flag the dQ product takes dS
+ * rounded per (query row, 32-key block), carried as its block scales, while
+ * dK keeps the shared exponents (dK of a key sums every later query anyway).
+ * Head dim 128 only (FLAMIA_ERR_UNSUPPORTED otherwise).
  * FLAMIA_FLAG_DQ_FP16 (review page, sec. 3.2 "accumulator leakage", sec.
  * 3.5.3: the FP16 dQ reduce that halves the reduction traffic): each key
  * tile's float32 dQ partial of query row i is multiplied by 2^p(i), rounded

@@ -884,8 +884,8 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
                          const flamia_qtensor* v, const flamia_qtensor* dout, const float* D,
                          const float* lse, const int32_t* cu, int ndocs, int T, int H,
                          int Hkv, float softmax_scale, bool had, bool causal, bool det, int dq16,
-                         int sched, void* wl, void* dq, void* dk, void* dv, void* ws, int* status,
-                         cudaStream_t stream) {
+                         int sched, bool ds_rows, void* wl, void* dq, void* dk, void* dv, void* ws,
+                         int* status, cudaStream_t stream) {
   CUtensorMap mq, mk, mv, mdo, mdq, mq4, mk4;
   const CUtensorMapSwizzle swz = swizzle_for_row_bytes(DIM);
   const BwdWorkspace W = bwd_workspace(T, H, DIM);
@@ -939,6 +939,7 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
   // the deterministic mode needs the claims in list order (a turn only waits
   // for an item claimed before it)
   prm.sched = det ? kSchedDynamic : sched;
+  prm.ds_rows = ds_rows ? 1 : 0;
   // the accumulator (float32 or FP16) and, in the deterministic mode, the
   // turn counters behind it
   if (cudaMemsetAsync(acc, 0, n * (dq16 ? 2 : 4), stream) != cudaSuccess ||
@@ -982,7 +983,7 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
     if (cudaGetLastError() != cudaSuccess) return FLAMIA_ERR_CUDA;
   }
   if (launch_bwd_short(q, k, v, dout, D, lse, cu, ndocs, T, H, Hkv, DIM, softmax_scale, NVF4, had,
-                       causal, acc, pre, dk, dv, stream) != cudaSuccess)
+                       causal, ds_rows, acc, pre, dk, dv, stream) != cudaSuccess)
     return FLAMIA_ERR_CUDA;
   if (had) {
     const size_t rows = static_cast<size_t>(T) * H;
@@ -1029,8 +1030,10 @@ extern "C" flamia_status flamia_attn_bwd_gqa(const flamia_qtensor* q, const flam
   if ((flags & ~(FLAMIA_FLAG_NVFP4_QK | FLAMIA_FLAG_HADAMARD | FLAMIA_FLAG_NONCAUSAL |
                  FLAMIA_FLAG_DETERMINISTIC_DQ | FLAMIA_FLAG_DQ_FP16 |
                  FLAMIA_FLAG_DQ_CAUSAL_SCALE | FLAMIA_FLAG_SCHEDULE_STATIC |
-                 FLAMIA_FLAG_SCHEDULE_RULE)) != 0)
+                 FLAMIA_FLAG_SCHEDULE_RULE | FLAMIA_FLAG_DS_ROW_EXPONENTS)) != 0)
     return FLAMIA_ERR_UNSUPPORTED;
+  const bool ds_rows = (flags & FLAMIA_FLAG_DS_ROW_EXPONENTS) != 0;
+  if (ds_rows && d != 128) return FLAMIA_ERR_UNSUPPORTED;
   const int sched = schedule_of(flags);
   if (sched < 0) return FLAMIA_ERR_UNSUPPORTED;
   if ((flags & FLAMIA_FLAG_DETERMINISTIC_DQ) && sched == kSchedStatic) return FLAMIA_ERR_UNSUPPORTED;
@@ -1063,13 +1066,13 @@ extern "C" flamia_status flamia_attn_bwd_gqa(const flamia_qtensor* q, const flam
   const float sc = had ? softmax_scale / static_cast<float>(d) : softmax_scale;
   if (nvf4)
     return launch_bwd<64, true>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, H_kv, sc,
-                                false, causal, det, dq16, sched, wl, dq_bf16, dk_bf16, dv_bf16, ws,
+                                false, causal, det, dq16, sched, ds_rows, wl, dq_bf16, dk_bf16, dv_bf16, ws,
                                 dev_status, s);
   return d == 128 ? launch_bwd<128, false>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, H_kv,
-                                           sc, had, causal, det, dq16, sched, wl, dq_bf16, dk_bf16,
+                                           sc, had, causal, det, dq16, sched, ds_rows, wl, dq_bf16, dk_bf16,
                                            dv_bf16, ws, dev_status, s)
                   : launch_bwd<64, false>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, H_kv,
-                                          sc, had, causal, det, dq16, sched, wl, dq_bf16, dk_bf16,
+                                          sc, had, causal, det, dq16, sched, ds_rows, wl, dq_bf16, dk_bf16,
                                           dv_bf16, ws, dev_status, s);
 }
 

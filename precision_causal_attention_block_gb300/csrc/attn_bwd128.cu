@@ -49,6 +49,7 @@ struct Bwd128Smem {
   alignas(1024) uint8_t dout[kRing][kQT * kD];
   alignas(1024) uint8_t pb[2][kTile * kQT];        // [key][query] E4M3, 64B-swizzled rows
   alignas(1024) uint8_t ds[2][kTile * kQT];
+  alignas(1024) uint8_t ds2[2][kTile * kQT];      // query-row dS exponents: dQ's dS codes
   alignas(1024) float dqs[2][kD / 32][kQT * 32];   // per group: 4 boxes [query][32 dims]
   // per-query inputs of a group's tile, double-buffered by the group's tile count
   alignas(16) float nl[2][2][kQT];                 // 8 - lse2 (-inf outside the document)
@@ -56,6 +57,7 @@ struct Bwd128Smem {
   alignas(16) float pf[2][2][kQT];                 // FP16 dQ: prescale 2^p (0 outside)
   uint32_t qbyte[2][2][2], dobyte[2][2][2];        // [group][buffer][query block]
   uint32_t eds[2][2][4];                           // [group][query block][key block]
+  uint8_t erow[2][2][4][32];  // query-row dS bytes [group][query block][key block][query]
   uint64_t bar_kv, bar_kv_free;
   uint64_t bar_qd_full[kRing], bar_qd_empty[kRing];
   uint64_t bar_s_full[2], bar_ds_full[2], bar_dq_full[2], bar_dq_read[2];
@@ -83,7 +85,9 @@ __device__ __forceinline__ int tile_q0(const BwdItem& it, int G, int nt, int v) 
 
 // DET: the deterministic dQ mode (ordered reduce-adds through prm.dq_turns).
 // F16: the prescaled FP16 dQ accumulator (prm.dq_pre), else float32.
-template <bool DET, bool F16>
+// ROWDS: dQ^T's dS operand rounded with one exponent per (query, 32-key block),
+// carried as the product's B scales (dK keeps the 32x32 block exponents).
+template <bool DET, bool F16, bool ROWDS>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd128_kernel(const __grid_constant__ CUtensorMap map_q,
                        const __grid_constant__ CUtensorMap map_k,
@@ -212,6 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t ddo0 = smem_desc(smem_u32(sm.dout[0]), 0, 1024, kLayoutSW128);
       const uint64_t dpb0 = smem_desc(smem_u32(sm.pb[0]), 0, 512, kLayoutSW64);
       const uint64_t dds0 = smem_desc(smem_u32(sm.ds[0]), 0, 512, kLayoutSW64);
+      const uint64_t dqs0 = smem_desc(smem_u32(ROWDS ? sm.ds2[0] : sm.ds[0]), 0, 512, kLayoutSW64);
       constexpr uint32_t kQStep = kQT * kD / 16, kPStep = kTile * kQT / 16;  // stage strides
       int nk = 0, ug = 0;
       bool ok = true;
@@ -261,11 +266,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint64_t dq = dq0 + st * kQStep, ddo = ddo0 + st * kQStep;
           const uint64_t dpb = dpb0 + b * kPStep, dds = dds0 + b * kPStep;
+          const uint64_t ddq = dqs0 + b * kPStep;  // dQ^T's dS operand
           const uint32_t sf = tmem + col_p(b);
           // dQ^T_t = K^T dS^T : A = K read MN-major (M = dims), B = dS read MN-major
 #pragma unroll
           for (int kb = 0; kb < kTile / 32; ++kb)
-            mma_mxf8_w(tmem + col_s(b), dk + kb * (32 * kD / 16), dds + kb * (32 * kQT / 16),
+            mma_mxf8_w(tmem + col_s(b), dk + kb * (32 * kD / 16), ddq + kb * (32 * kQT / 16),
                      idesc_mxf8(kD, kQT, 1, 1, kb, kb), sf + kSfDqA, sf + kSfDqB, kb > 0);
           // dQ^T first: the group reads it out while dV / dK run
           tc_commit_w(smem_u32(&sm.bar_dq_full[b]));
@@ -427,6 +433,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4*>(dsrow + 16 * ch0) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
           *reinterpret_cast<uint4*>(dsrow + 16 * ch1) = make_uint4(dw[4], dw[5], dw[6], dw[7]);
           if (lane == 0) sm.eds[g][c][quad] = static_cast<uint32_t>(eb + 127);
+          if (ROWDS) {
+            // dQ's operand: per query column the maximum over this warp's 32
+            // keys (one key block); lane q keeps query q's and its exponent
+            uint32_t mine = 0u;
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+              const uint32_t m =
+                  __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(__uint_as_float(dv[q]))));
+              if (lane == q) mine = m;
+            }
+            const int er = max(roundup_exponent(__uint_as_float(mine)) - 8, -127);
+            const float invr = exp2i(-(er + 8));
+            sm.erow[g][c][quad][lane] = static_cast<uint8_t>(er + 127);
+            uint32_t dr[8];
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              const float i0 = __shfl_sync(0xffffffffu, invr, i);
+              const float i1 = __shfl_sync(0xffffffffu, invr, i + 1);
+              const float i2 = __shfl_sync(0xffffffffu, invr, i + 2);
+              const float i3 = __shfl_sync(0xffffffffu, invr, i + 3);
+              dr[i / 4] = cvt_e4m3x4(__uint_as_float(dv[i]) * i0, __uint_as_float(dv[i + 1]) * i1,
+                                     __uint_as_float(dv[i + 2]) * i2,
+                                     __uint_as_float(dv[i + 3]) * i3);
+            }
+            uint8_t* ds2row = sm.ds2[g] + j * kQT;
+            *reinterpret_cast<uint4*>(ds2row + 16 * ch0) = make_uint4(dr[0], dr[1], dr[2], dr[3]);
+            *reinterpret_cast<uint4*>(ds2row + 16 * ch1) = make_uint4(dr[4], dr[5], dr[6], dr[7]);
+          }
         }
         // the group's previous reduce-add has read the staging buffer (and, in
         // the deterministic mode, completed: its turn is passed on)
@@ -463,9 +497,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 4; ++i) w[i] = kword;  // dQ^T: A = K^T, per key block
 #pragma unroll
-          for (int i = 0; i < 2; ++i)  // dQ^T: B = dS^T, row block = query block i
-            w[4 + i] = sm.eds[g][i][0] | (sm.eds[g][i][1] << 8) | (sm.eds[g][i][2] << 16) |
-                       (sm.eds[g][i][3] << 24);
+          for (int i = 0; i < 2; ++i) {  // dQ^T: B = dS^T, row block = query block i
+            if (ROWDS)  // this lane's query 32 i + lane: one byte per key block
+              w[4 + i] = static_cast<uint32_t>(sm.erow[g][i][0][lane]) |
+                         (static_cast<uint32_t>(sm.erow[g][i][1][lane]) << 8) |
+                         (static_cast<uint32_t>(sm.erow[g][i][2][lane]) << 16) |
+                         (static_cast<uint32_t>(sm.erow[g][i][3][lane]) << 24);
+            else
+              w[4 + i] = sm.eds[g][i][0] | (sm.eds[g][i][1] << 8) | (sm.eds[g][i][2] << 16) |
+                         (sm.eds[g][i][3] << 24);
+          }
           w[6] = w[7] = 0x7F7F7F7Fu;
           tmem_st8(tmem + lane_off + col_p(g) + kSfDqA, w);
           tmem_st_wait();
@@ -650,8 +691,14 @@ cudaError_t launch_bwd128_pipelined(const BwdParams& prm, const flamia_qtensor* 
           : !make_f32_token_map(&mdq, acc, T, H, kD, kQT, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
   const size_t smem = sizeof(Bwd128Smem) + 1024;
-  auto kernel = det ? (f16 ? attn_bwd128_kernel<true, true> : attn_bwd128_kernel<true, false>)
-                    : (f16 ? attn_bwd128_kernel<false, true> : attn_bwd128_kernel<false, false>);
+  using Kernel = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
+                         const BwdParams);
+  static const Kernel kernels[8] = {
+      attn_bwd128_kernel<false, false, false>, attn_bwd128_kernel<true, false, false>,
+      attn_bwd128_kernel<false, true, false>,  attn_bwd128_kernel<true, true, false>,
+      attn_bwd128_kernel<false, false, true>,  attn_bwd128_kernel<true, false, true>,
+      attn_bwd128_kernel<false, true, true>,   attn_bwd128_kernel<true, true, true>};
+  const Kernel kernel = kernels[(det ? 1 : 0) | (f16 ? 2 : 0) | (prm.ds_rows ? 4 : 0)];
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;

@@ -693,7 +693,7 @@ extern "C" flamia_status flamia_attn_fwd_gqa(const flamia_qtensor* q, const flam
   if ((flags & ~(FLAMIA_FLAG_NVFP4_QK | FLAMIA_FLAG_HADAMARD | FLAMIA_FLAG_NONCAUSAL |
                  FLAMIA_FLAG_DETERMINISTIC_DQ | FLAMIA_FLAG_DQ_FP16 |
                  FLAMIA_FLAG_DQ_CAUSAL_SCALE | FLAMIA_FLAG_SCHEDULE_STATIC |
-                 FLAMIA_FLAG_SCHEDULE_RULE)) != 0)
+                 FLAMIA_FLAG_SCHEDULE_RULE | FLAMIA_FLAG_DS_ROW_EXPONENTS)) != 0)
     return FLAMIA_ERR_UNSUPPORTED;
   const int sched = schedule_of(flags);
   if (sched < 0) return FLAMIA_ERR_UNSUPPORTED;

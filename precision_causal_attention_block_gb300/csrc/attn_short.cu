@@ -40,6 +40,7 @@ struct ShortParams {
   int hadamard;  // dK rotated back by H_d (Q and K were quantised rotated)
   int causal;    // 0: every query sees every key of its document
   int skip_single;  // one-token documents were done by the one-thread kernels
+  int ds_rows;      // dQ from dS rounded with one exponent per query row
   int ppw;          // (document, head) pairs per warp: 32 when documents average <= 2
                     // tokens (almost every pair is skipped), else 1
 };
@@ -259,8 +260,16 @@ __device__ __forceinline__ void bwd_short_pair(const ShortParams& prm, int doc, 
     // dQ_i = scale * sum_j dS^_ij K^_j  (float32 rows of the accumulator)
     for (int i = 0; i < L; ++i) {
       float acc[N] = {};
+      float inv_i = inv, dsc_i = dsc;
+      if (prm.ds_rows) {  // row i's own exponent (the whole document is one key block)
+        float am = 0.f;
+        for (int j = 0; j <= (prm.causal ? i : L - 1); ++j) am = fmaxf(am, fabsf(s_ds[i][j]));
+        const int er = max(roundup_exponent(am) - 8, -127);
+        inv_i = exp2i(-(er + 8));
+        dsc_i = pow2_or_zero_s(er);
+      }
       for (int j = 0; j <= (prm.causal ? i : L - 1); ++j) {
-        const float dsh = e4m3x2_to_float2(cvt_e4m3x2(s_ds[i][j] * inv, 0.f)).x * dsc;
+        const float dsh = e4m3x2_to_float2(cvt_e4m3x2(s_ds[i][j] * inv_i, 0.f)).x * dsc_i;
         float k[N];
         load_codes<DIM>(prm.kc, static_cast<size_t>(s + j) * Hkv + hk, lane, k);
 #pragma unroll
@@ -550,8 +559,8 @@ cudaError_t launch_bwd_short(const flamia_qtensor* q, const flamia_qtensor* k,
                              const flamia_qtensor* v, const flamia_qtensor* dout, const float* D,
                              const float* lse, const int32_t* cu, int ndocs, int T, int H,
                              int Hkv, int d, float softmax_scale, bool nvfp4_qk, bool hadamard,
-                             bool causal, float* dq_acc, const int8_t* dq_pre, void* dk, void* dv,
-                             cudaStream_t stream) {
+                             bool causal, bool ds_rows, float* dq_acc, const int8_t* dq_pre,
+                             void* dk, void* dv, cudaStream_t stream) {
   ShortParams p = make_params(q, k, v, cu, ndocs, T, H, Hkv, softmax_scale);
   p.hadamard = hadamard ? 1 : 0;
   p.causal = causal ? 1 : 0;
@@ -561,6 +570,7 @@ cudaError_t launch_bwd_short(const flamia_qtensor* q, const flamia_qtensor* k,
   p.D = D;
   p.dq_acc = dq_acc;
   p.dq_pre = dq_pre;
+  p.ds_rows = ds_rows ? 1 : 0;
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
   if (Hkv == H && !nvfp4_qk && !hadamard) {  // one-token documents: one thread each

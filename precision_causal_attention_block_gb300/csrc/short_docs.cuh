@@ -18,7 +18,7 @@ cudaError_t launch_bwd_short(const flamia_qtensor* q, const flamia_qtensor* k,
                              const flamia_qtensor* v, const flamia_qtensor* dout, const float* D,
                              const float* lse, const int32_t* cu, int ndocs, int T, int H,
                              int Hkv, int d, float softmax_scale, bool nvfp4_qk, bool hadamard,
-                             bool causal, float* dq_acc, const int8_t* dq_pre, void* dk, void* dv,
-                             cudaStream_t stream);
+                             bool causal, bool ds_rows, float* dq_acc, const int8_t* dq_pre,
+                             void* dk, void* dv, cudaStream_t stream);
 
 }  // namespace flamia

@@ -27,6 +27,7 @@ FLAG_DQ_FP16 = 0x10
 FLAG_DQ_CAUSAL_SCALE = 0x20
 FLAG_SCHEDULE_STATIC = 0x40
 FLAG_SCHEDULE_RULE = 0x80
+FLAG_DS_ROW_EXPONENTS = 0x100
 DEV_BAD_SEQLENS = 0x1
 DEV_CAPACITY = 0x2
 DEV_TIMEOUT = 0x4
@@ -218,7 +219,7 @@ class TrainingCall:
     def __init__(self, T, H, d, cu_seqlens, softmax_scale, nvfp4_qk: bool = False,
                  hadamard: bool = False, causal: bool = True, H_kv=None,
                  deterministic_dq: bool = False, dq_accum: str = "fp32", schedule: str = "dynamic",
-                 device="cuda"):
+                 ds_rows: bool = False, device="cuda"):
         self.T, self.H, self.d = T, H, d
         self.H_kv = H if H_kv is None else H_kv
         self.scale = softmax_scale
@@ -229,7 +230,8 @@ class TrainingCall:
                       {"fp32": 0, "fp16_sequence": FLAG_DQ_FP16,
                        "fp16_causal": FLAG_DQ_FP16 | FLAG_DQ_CAUSAL_SCALE}[dq_accum] |
                       {"dynamic": 0, "rule": FLAG_SCHEDULE_RULE,
-                       "static": FLAG_SCHEDULE_STATIC}[schedule])
+                       "static": FLAG_SCHEDULE_STATIC}[schedule] |
+                      (FLAG_DS_ROW_EXPONENTS if ds_rows else 0))
         self.fmt_qk = ((FORMAT_MXFP8_NVFP4 if nvfp4_qk else FORMAT_MXFP8) |
                        (FORMAT_HADAMARD if hadamard else 0))
         self.q = QTensor(T, H, d, nvfp4_qk, device)

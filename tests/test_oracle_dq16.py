@@ -148,7 +148,10 @@ def test_row_ds_exponents_by_hand():
 def test_row_ds_exponents_remove_the_in_block_leak(mix):
     # a later query row in the same 32-row block as earlier rows (row 40 of the
     # first document, block [32, 64)): with the block exponents its dO moves
-    # the rounding of the earlier rows' dQ; with query-row exponents it cannot
+    # the dS exponent that the earlier rows' dQ is rounded with; with query-row
+    # exponents only the dO block exponent still links them (the per-token
+    # operand scales would remove that), which here shifts a few dO values of
+    # rows 32..39 by less than any dS rounding step: their dQ keeps every bit
     x, cu, scale = mix
     y = {n: t.copy() for n, t in x.items()}
     y["do"][40] *= 64.0
