@@ -84,7 +84,7 @@ typedef enum {
                                        take their work items in a static snake
                                        over the cost-sorted list instead of
                                        claiming the next unclaimed item        */
-#define FLAMIA_FLAG_DS_ROW_EXPONENTS 0x100 /* backward only, head dim 128: dQ's dS
+#define FLAMIA_FLAG_DS_ROW_EXPONENTS 0x100 /* backward only: dQ's dS
                                        operand rounded with one exponent per
                                        (query row, 32-key block) instead of per
                                        32 x 32 block (dK keeps the block ones) */
@@ -309,7 +309,6 @@ size_t flamia_bwd_workspace_bytes(int T, int H, int d);
  * the rounding of an earlier row's dQ; with the flag the dQ product takes dS
  * rounded per (query row, 32-key block), carried as its block scales, while
  * dK keeps the shared exponents (dK of a key sums every later query anyway).
- * Head dim 128 only (FLAMIA_ERR_UNSUPPORTED otherwise).
  * FLAMIA_FLAG_DQ_FP16 (review page, sec. 3.2 "accumulator leakage", sec.
  * 3.5.3: the FP16 dQ reduce that halves the reduction traffic): each key
  * tile's float32 dQ partial of query row i is multiplied by 2^p(i), rounded

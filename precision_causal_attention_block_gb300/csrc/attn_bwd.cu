@@ -55,6 +55,7 @@ struct BwdSmem {
   alignas(1024) uint8_t dout[kBStages][kTileBytes];
   alignas(1024) uint8_t pb[kTile * kTile];  // [key][query] E4M3, 128B-swizzled rows
   alignas(1024) uint8_t ds[kTile * kTile];  // [key][query] E4M3, 128B-swizzled rows
+  alignas(1024) uint8_t ds2[kTile * kTile];  // query-row dS exponents: dQ's dS codes
   // dQ_u staging: DIM/32 boxes of [128 query rows][32 floats], 128B-swizzled
   alignas(1024) float dqs[DIM / 32][kTile * 32];
   alignas(NVF4 ? 1024 : 16) uint8_t k4[kTile4Bytes];
@@ -66,6 +67,7 @@ struct BwdSmem {
   alignas(16) float pf[2][kTile];  // FP16 dQ: prescale 2^p of each query (0 outside)
   uint32_t qbyte[2][4], dobyte[2][4];  // E8M0 bytes of the 4 query blocks of Q and dO
   uint32_t eds[4][4];            // dS block bytes [query block][key block]
+  uint8_t erow[4][4][32];        // query-row dS bytes [query block][key block][query]
   uint64_t bar_kv;
   uint64_t bar_qd_full[kBStages];
   uint64_t bar_qd_empty[kBStages];
@@ -223,6 +225,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const uint64_t ddo0 = smem_desc(smem_u32(sm.dout[0]), 0, sbo, lay);
       const uint64_t dpb = smem_desc(smem_u32(sm.pb), 0, 1024, kLayoutSW128);
       const uint64_t dds = smem_desc(smem_u32(sm.ds), 0, 1024, kLayoutSW128);
+      // dQ's dS operand: the query-row-exponent copy when asked for
+      const uint64_t ddq =
+          smem_desc(smem_u32(OPT && prm.ds_rows ? sm.ds2 : sm.ds), 0, 1024, kLayoutSW128);
       constexpr uint32_t kStep = kTileBytes / 16;  // one ring stage
       int nk = 0, uc = 0;  // items and query tiles consumed so far
       bool ok = true;
@@ -290,7 +295,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int kb = 0; kb < 4; ++kb)
-            mma_mxf8_w(tmem + kColDQ, dds + kb * (32 * kTile / 16), dk + kb * (32 * DIM / 16),
+            mma_mxf8_w(tmem + kColDQ, ddq + kb * (32 * kTile / 16), dk + kb * (32 * DIM / 16),
                      idesc_mxf8(kTile, DIM, 1, 1, kb, kb), tmem + kSfDqA, tmem + kSfDqB, kb > 0);
           // dQ first: the groups read it out while dV / dK run
           tc_commit_w(smem_u32(&sm.bar_dq_full));
@@ -464,6 +469,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           *reinterpret_cast<uint4*>(dsrow + 16 * ch0) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
           *reinterpret_cast<uint4*>(dsrow + 16 * ch1) = make_uint4(dw[4], dw[5], dw[6], dw[7]);
           if (lane == 0) sm.eds[c][quad] = static_cast<uint32_t>(eb + 127);
+          if (OPT && prm.ds_rows) {
+            // dQ's operand: per query column the maximum over this warp's 32
+            // keys (one key block); lane q keeps query q's and its exponent
+            uint32_t mine = 0u;
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+              const uint32_t m =
+                  __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(__uint_as_float(dv[q]))));
+              if (lane == q) mine = m;
+            }
+            const int er = max(roundup_exponent(__uint_as_float(mine)) - 8, -127);
+            const float invr = exp2i(-(er + 8));
+            sm.erow[c][quad][lane] = static_cast<uint8_t>(er + 127);
+            uint32_t dr[8];
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              const float i0 = __shfl_sync(0xffffffffu, invr, i);
+              const float i1 = __shfl_sync(0xffffffffu, invr, i + 1);
+              const float i2 = __shfl_sync(0xffffffffu, invr, i + 2);
+              const float i3 = __shfl_sync(0xffffffffu, invr, i + 3);
+              dr[i / 4] = cvt_e4m3x4(__uint_as_float(dv[i]) * i0, __uint_as_float(dv[i + 1]) * i1,
+                                     __uint_as_float(dv[i + 2]) * i2,
+                                     __uint_as_float(dv[i + 3]) * i3);
+            }
+            uint8_t* ds2row = sm.ds2 + j * kTile;
+            *reinterpret_cast<uint4*>(ds2row + 16 * ch0) = make_uint4(dr[0], dr[1], dr[2], dr[3]);
+            *reinterpret_cast<uint4*>(ds2row + 16 * ch1) = make_uint4(dr[4], dr[5], dr[6], dr[7]);
+          }
         }
         named_barrier_sync(1, kComputeThreads);
         if (ok) {
@@ -494,8 +527,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               // dQ: A = dS, row block = query block i, K blocks = key blocks
-              w[i] = sm.eds[i][0] | (sm.eds[i][1] << 8) | (sm.eds[i][2] << 16) |
-                     (sm.eds[i][3] << 24);
+              if (OPT && prm.ds_rows)  // this lane's query 32 i + lane
+                w[i] = static_cast<uint32_t>(sm.erow[i][0][lane]) |
+                       (static_cast<uint32_t>(sm.erow[i][1][lane]) << 8) |
+                       (static_cast<uint32_t>(sm.erow[i][2][lane]) << 16) |
+                       (static_cast<uint32_t>(sm.erow[i][3][lane]) << 24);
+              else
+                w[i] = sm.eds[i][0] | (sm.eds[i][1] << 8) | (sm.eds[i][2] << 16) |
+                       (sm.eds[i][3] << 24);
               w[4 + i] = kword;  // dQ: B = K, per key block
             }
             tmem_st8(tmem + lane_off + kSfDqA, w);
@@ -974,7 +1013,8 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
       return FLAMIA_ERR_CUDA;
   } else {
     const size_t smem = sizeof(BwdSmem<DIM, NVF4>) + 1024;
-    auto kernel = (det || dq16) ? attn_bwd_kernel<DIM, NVF4, true> : attn_bwd_kernel<DIM, NVF4, false>;
+    auto kernel = (det || dq16 || ds_rows) ? attn_bwd_kernel<DIM, NVF4, true>
+                                           : attn_bwd_kernel<DIM, NVF4, false>;
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return FLAMIA_ERR_CUDA;
@@ -1033,7 +1073,6 @@ extern "C" flamia_status flamia_attn_bwd_gqa(const flamia_qtensor* q, const flam
                  FLAMIA_FLAG_SCHEDULE_RULE | FLAMIA_FLAG_DS_ROW_EXPONENTS)) != 0)
     return FLAMIA_ERR_UNSUPPORTED;
   const bool ds_rows = (flags & FLAMIA_FLAG_DS_ROW_EXPONENTS) != 0;
-  if (ds_rows && d != 128) return FLAMIA_ERR_UNSUPPORTED;
   const int sched = schedule_of(flags);
   if (sched < 0) return FLAMIA_ERR_UNSUPPORTED;
   if ((flags & FLAMIA_FLAG_DETERMINISTIC_DQ) && sched == kSchedStatic) return FLAMIA_ERR_UNSUPPORTED;

@@ -1,8 +1,9 @@
 """GPU query-row dS exponents (FLAMIA_FLAG_DS_ROW_EXPONENTS; review page,
 sec. 3.2: they remove the leakage inside blocks) against the oracle's model:
 dQ from dS rounded per (query row, 32-key block), dK / dV unchanged bit for
-bit, on the head-dim-128 tile kernel and the short-document kernels, with
-the other options; and the in-block leakage probe."""
+bit, on both tile kernels (head dims 128 and 64, the mixed NVFP4 path) and
+the short-document kernels, with the other options; and the in-block
+leakage probe."""
 import numpy as np
 import pytest
 import torch
@@ -28,17 +29,19 @@ def run(w, x, Hkv=None, **kw):
     return call
 
 
-@pytest.mark.parametrize("Hkv,kw", [(None, {}), (None, {"causal": False}), (2, {}),
-                                    (None, {"dq_accum": "fp16_causal"}),
-                                    (None, {"deterministic_dq": True}),
-                                    (None, {"hadamard": True})])
-def test_row_exponents_against_the_oracle(lib, Hkv, kw):
-    w = W.custom("rowds_mix", MIX, 4, 128, seed=43, structure="outlier16x2")
+@pytest.mark.parametrize("d,Hkv,kw", [(128, None, {}), (128, None, {"causal": False}),
+                                      (128, 2, {}), (128, None, {"dq_accum": "fp16_causal"}),
+                                      (128, None, {"deterministic_dq": True}),
+                                      (128, None, {"hadamard": True}), (64, None, {}),
+                                      (64, 2, {"causal": False}), (64, None, {"nvfp4_qk": True})])
+def test_row_exponents_against_the_oracle(lib, d, Hkv, kw):
+    w = W.custom("rowds_mix", MIX, 4, d, seed=43, structure="outlier16x2")
     x = W.make_inputs_bf16(w)
     if Hkv:
         x["k"], x["v"] = x["k"][:, :Hkv].contiguous(), x["v"][:, :Hkv].contiguous()
     call = run(w, x, Hkv, ds_rows=True, **kw)
     ref = O.attention(*[x[n].double().numpy() for n in NAMES], w.cu_seqlens, w.sm_scale,
+                      qk_format="nvfp4" if kw.get("nvfp4_qk") else "mxfp8",
                       causal=kw.get("causal", True), hadamard=kw.get("hadamard", False),
                       dq_accum=kw.get("dq_accum", "fp32"), ds_rows=True)
     rel = 3e-2 if kw.get("hadamard") else 2e-2
@@ -48,20 +51,16 @@ def test_row_exponents_against_the_oracle(lib, Hkv, kw):
     assert torch.equal(base.dk, call.dk) and torch.equal(base.dv, call.dv)
 
 
-def test_row_exponents_need_head_dim_128(lib):
-    from precision_causal_attention_block_gb300 import flamia as fl
-    w = W.custom("rowds64", [100], 1, 64)
-    x = W.make_inputs_bf16(w)
-    with pytest.raises(RuntimeError):
-        run(w, x, ds_rows=True)
-
-
 def test_in_block_leakage_probe(lib):
     # row 40's dO x 64 (block [32, 64) of the first document): the dQ rows 32..39
     # move with the 32 x 32 dS exponents; with query-row exponents they move
     # only through the shared dO block exponent (a few values near the E4M3
-    # subnormals), far less (deterministic mode: one summation order)
-    w = W.custom("rowds_probe", [300, 200], 2, 128, seed=5)
+    # subnormals), far less (deterministic mode: one summation order).  Head
+    # dim 128: there the oracle moves 0 with row exponents; at head dim 64 the
+    # same input moves the oracle's rows through the dO exponent in both modes
+    # (what per-token operand scales would remove), so it tests nothing there
+    d = 128
+    w = W.custom("rowds_probe", [300, 200], 2, d, seed=5)
     x = W.make_inputs_bf16(w)
     y = {n: t.clone() for n, t in x.items()}
     y["do"][40] = (y["do"][40].float() * 64.0).to(torch.bfloat16)
