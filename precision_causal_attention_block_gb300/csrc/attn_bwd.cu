@@ -925,7 +925,8 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
                          int Hkv, float softmax_scale, bool had, bool causal, bool det, int dq16,
                          int sched, bool ds_rows, void* wl, void* dq, void* dk, void* dv, void* ws,
                          int* status, cudaStream_t stream) {
-  CUtensorMap mq, mk, mv, mdo, mdq, mq4, mk4;
+  // (head dim 128 builds its own maps in launch_bwd128_pipelined)
+  CUtensorMap mq{}, mk{}, mv{}, mdo{}, mdq{}, mq4{}, mk4{};
   const CUtensorMapSwizzle swz = swizzle_for_row_bytes(DIM);
   const BwdWorkspace W = bwd_workspace(T, H, DIM);
   float* acc = static_cast<float*>(ws);

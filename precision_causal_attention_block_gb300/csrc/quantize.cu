@@ -312,7 +312,7 @@ flamia_status check_tensor(const void* x, int H, int format, const flamia_qtenso
 flamia_status launch_quantize(const void* const* xs, QuantJob& job, int T, int d,
                               const int32_t* cu, int ndocs, bool had, const void* o_bf16,
                               float* D, int* dev_status, cudaStream_t s) {
-  CUtensorMap maps[3];
+  CUtensorMap maps[3] = {};
   int rows = 0;
   for (int z = 0; z < job.n; ++z) {
     if (!make_rows_map(&maps[z], xs[z], T, job.H[z], d)) return FLAMIA_ERR_CUDA;
