@@ -89,3 +89,18 @@ def test_product_path_does_not_import_the_oracle():
             if f.endswith((".py", ".cu", ".cuh")):
                 src = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"(import|from)\s+oracle|oracle/|flamia_oracle", src), f
+
+
+def test_binding_constants_match_the_header():
+    # every FLAMIA_FLAG_* / FLAMIA_FORMAT_* / FLAMIA_DEV_* macro of flamia.h has
+    # the same value in the Python binding, and the binding declares a
+    # signature for every exported function
+    from precision_causal_attention_block_gb300 import flamia as fl
+    src = open(os.path.join(ROOT, "include", "flamia.h")).read()
+    macros = dict(re.findall(r"#define FLAMIA_((?:FLAG|FORMAT|DEV)_[A-Z0-9_]+)\s+(0x[0-9A-Fa-f]+|\d+)",
+                             src))
+    assert len(macros) >= 14
+    for name, val in macros.items():
+        assert getattr(fl, name, None) == int(val, 0), name
+    for n in declared_symbols():
+        assert n in fl.SIGNATURES, n
