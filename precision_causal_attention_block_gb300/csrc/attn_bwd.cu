@@ -1006,7 +1006,7 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
     }
     if (cudaGetLastError() != cudaSuccess) return FLAMIA_ERR_CUDA;
   }
-  // persistent: one CTA per SM (shared memory allows one), items in snake order
+  // persistent: one CTA per SM (shared memory allows one), items claimed in list order
   const long long grid = std::min<long long>(static_cast<long long>(L.cap_bwd) * Hkv, num_sms());
   if constexpr (DIM == 128 && !NVF4) {
     if (launch_bwd128_pipelined(prm, q, k, v, dout, acc, static_cast<unsigned>(grid), stream) !=

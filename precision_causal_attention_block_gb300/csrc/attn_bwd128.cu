@@ -2,8 +2,8 @@
 // review page, sec. 1.2, 3.1, 3.3, 3.4 "Backward pass"), pipelined so that
 // the tensor core and the CUDA cores work at the same time.
 //
-// One work item = one 128-key tile of a document x one head (persistent CTAs,
-// items in snake order as in the other kernels).  The item's queries are
+// One work item = one 128-key tile of a document x one head (persistent CTAs
+// claiming items as in the other kernels).  The item's queries are
 // walked in 64-query tiles t from the diagonal to the document end; the two
 // compute groups take alternate tiles, each with its own half of tensor memory:
 //

@@ -663,7 +663,7 @@ flamia_status launch_fwd(const flamia_qtensor* q, const flamia_qtensor* k,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return FLAMIA_ERR_CUDA;
-  // persistent: one CTA per SM (shared memory allows one), items in snake order
+  // persistent: one CTA per SM (shared memory allows one), items claimed in list order
   const long long grid = std::min<long long>(static_cast<long long>(L.cap_fwd) * H, num_sms());
   attn_fwd_kernel<DIM, NVF4>
       <<<static_cast<unsigned>(grid), kFwdThreads, smem, stream>>>(mq, mk, mv, mq4, mk4, prm);

@@ -34,7 +34,7 @@ struct BwdParams {
   int* dq_turns;  // deterministic dQ: [T][H] turn counters (per tile's first query), else null
   const int8_t* dq_pre;  // FP16 dQ accumulator: prescale exponents [H, T], else null (float32)
   int sched;             // kSchedDynamic / kSchedRule / kSchedStatic
-  int ds_rows;           // dQ's dS operand with query-row exponents (head dim 128)
+  int ds_rows;           // dQ's dS operand with query-row exponents
   int* status;
 };
 
