@@ -142,10 +142,14 @@ def test_varlen65536_sampled(lib):
     exact = O.attention(*sl, [0, e - s], w.sm_scale, quant=False)
     for n, t in (("O", call.o), ("dQ", call.dq), ("dK", call.dk), ("dV", call.dv)):
         cos = O.cosine(np64(t[s:e][:, heads]), exact[n])
-        # the method itself (the oracle) sets how close to exact attention a
-        # quantised result can be; the pages report dQ cosine 0.9979 for it
         method = O.cosine(ref[n], exact[n])
-        assert cos >= min(0.998, method - 2e-4), (n, cos, method)
+        if n in ("O", "dV"):
+            assert cos >= 0.998, (n, cos, method)
+        else:
+            # the method itself (the oracle) sits at 0.9979 for dQ and dK on
+            # these plain normal inputs, the summary page's own dQ figure for
+            # MXFP8: the kernel must stay within 2e-4 of it
+            assert cos >= method - 2e-4 and cos >= 0.997, (n, cos, method)
     # the longest document: its first and last query blocks, last key blocks
     b = int(np.argmax(lens))
     s, e = cu[b], cu[b + 1]
@@ -197,31 +201,73 @@ def test_long131072_sampled(lib):
             compare(f"dV[{kb}]", np64(call.dv[rows][:, h]), res["dV"][kb])
 
 
-def test_leakage_probe_bitwise(lib):
-    """Perturbing a future token outside the victim's 32-token block (and in
-    another document) leaves every earlier O and LSE bit unchanged; dQ of the
-    earlier rows changes by no more than the float32 atomic-order noise."""
+def perturbed(x, name, t):
+    """A x1000 copy of token t of tensor `name` with one channel shifted by 50."""
+    y = {n: v.clone() for n, v in x.items()}
+    y[name][t] = (y[name][t].float() * 1000.0).to(torch.bfloat16)
+    y[name][t, :, 5] += 50.0
+    return y
+
+
+@pytest.mark.parametrize("d", [128, 64])
+def test_leakage_probe_bitwise(lib, d):
+    """Review page, sec. 3.2 and 4.5: perturbing a future token outside the
+    victim's 32-token block (and in another document) changes no earlier
+    output bit.  The dQ partials are summed in a fixed order (deterministic
+    mode), so every output is compared bit for bit: O, LSE and dQ of the
+    rows before the perturbed token's block, and O, LSE, dQ, dK, dV of the
+    other document, under a perturbation of each of Q, K, V and dO."""
+    from precision_causal_attention_block_gb300 import flamia as fl
+    w = W.custom("probe", [600, 200], 2, d, seed=9)
+    x = W.make_inputs_bf16(w)
+
+    def run(xx):
+        call = fl.TrainingCall(w.T, w.H, w.d, cu_tensor(w.cu_seqlens), w.sm_scale,
+                               deterministic_dq=True)
+        xd = {n: dev(t) for n, t in xx.items()}
+        call.forward(xd["q"], xd["k"], xd["v"])
+        call.backward(xd["do"])
+        torch.cuda.synchronize()
+        call.check_status()
+        return call
+
+    base = run(x)
+    t = 450  # block [448, 480) of document 0
+    for name in NAMES:
+        r = run(perturbed(x, name, t))
+        for what, a, b in (("O", r.o, base.o), ("dQ", r.dq, base.dq)):
+            assert torch.equal(a[:448], b[:448]), (name, what, "earlier rows")
+            assert torch.equal(a[600:], b[600:]), (name, what, "other document")
+        assert torch.equal(r.lse[:, :448], base.lse[:, :448]), name
+        assert torch.equal(r.lse[:, 600:], base.lse[:, 600:]), name
+        assert torch.equal(r.dk[600:], base.dk[600:]), (name, "dK other document")
+        assert torch.equal(r.dv[600:], base.dv[600:]), (name, "dV other document")
+        # the probe has teeth: the perturbation reaches the later rows
+        later, before = (r.dq, base.dq) if name == "do" else (r.o, base.o)
+        assert not torch.equal(later[448:600], before[448:600]), name
+
+
+def test_leakage_probe_atomic_order(lib):
+    """The same probe in the default mode, where dQ partials are summed with
+    float32 reduce-adds in no fixed order: O, LSE, dK and dV compare bit for
+    bit; dQ of the earlier rows may differ from a repeat of the call only by
+    the summation-order noise, bounded per element by two BF16 steps of its
+    value (a leak of the x1000 token would be orders of magnitude larger)."""
     w = W.custom("probe", [600, 200], 2, 128, seed=9)
     x = W.make_inputs_bf16(w)
     base = run_call(w, x)
-    o0, l0, dq0 = base.o.clone(), base.lse.clone(), base.dq.clone()
-    base2 = run_call(w, x)
-    noise = (base2.dq.float() - dq0.float()).abs().max().item()
-    t = 450  # block [448, 480) of document 0
+    o0, l0, dq0 = base.o.clone(), base.lse.clone(), base.dq.float()
+    bound = 2.0 ** -6 * dq0.abs() + 1e-6 * dq0.abs().max()
     for name in NAMES:
-        y = {n: v.clone() for n, v in x.items()}
-        y[name][t] = (y[name][t].float() * 1000.0).to(torch.bfloat16)
-        y[name][t, :, 5] += 50.0
-        r = run_call(w, y)
+        r = run_call(w, perturbed(x, name, 450))
         assert torch.equal(r.o[:448], o0[:448]), name
         assert torch.equal(r.lse[:, :448], l0[:, :448]), name
         assert torch.equal(r.o[600:], o0[600:]), name
-        # dQ is summed with float32 atomics in no fixed order: allow the
-        # run-to-run noise floor (at most ~1 BF16 ulp); a leak from a x1000
-        # perturbation would be orders of magnitude larger
-        d = (r.dq[:448].float() - dq0[:448].float()).abs().max().item()
-        floor = max(4 * noise, 2.0 ** -7 * dq0[:448].float().abs().max().item())
-        assert d <= floor, (name, d, noise)
+        assert torch.equal(r.dk[600:], base.dk[600:]), name
+        assert torch.equal(r.dv[600:], base.dv[600:]), name
+        diff = (r.dq.float() - dq0).abs()
+        assert (diff[:448] <= bound[:448]).all(), (name, diff[:448].max().item())
+        assert (diff[600:] <= bound[600:]).all(), (name, diff[600:].max().item())
 
 
 # ---------------------------------------------------------------- mixed NVFP4 path

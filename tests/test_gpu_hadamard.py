@@ -97,17 +97,28 @@ def test_rotated_attention_tracks_exact_attention(lib, d):
 
 
 def test_rotated_fixed4x4096_one_document(lib):
-    # the full-size shape's kernels (head dim 128, 4096-token documents), the
-    # oracle on one document and two heads
+    """The full-size shape's kernels (head dim 128, 4096-token documents) with
+    the rotation, the pages' default at head dim 128 (review page, sec. 3.4),
+    against the oracle and against exact attention on one document.  Head 1
+    (a x20 channel in dO only) reaches cosine >= 0.998 to exact attention on
+    all four outputs, and so does the kernel.  Head 13 has x20 channels in Q,
+    K and V: there the method itself stays below 0.998 (the rotation spreads
+    the Q and K outliers over every channel; the oracle gives dK 0.911), so
+    the kernel is held to the oracle's own distance from exact attention."""
     w = W.fixed4x4096()
     x = W.make_inputs_bf16(w)
     call = run_call(w, x)
-    tok, heads = slice(4096, 8192), [0, 7]
+    tok, heads = slice(4096, 8192), [1, 13]
     xs = [x[n][tok][:, heads].double().numpy() for n in NAMES]
     ref = O.attention(*xs, [0, 4096], w.sm_scale, hadamard=True)
+    ex = O.attention(*xs, [0, 4096], w.sm_scale, quant=False)
     gpu = {"O": call.o, "dQ": call.dq, "dK": call.dk, "dV": call.dv}
     for n in ("O", "dQ", "dK", "dV"):
-        compare(n, np64(gpu[n][tok][:, heads]), ref[n], rel_max=ROTATED_REL_MAX[n])
+        got = np64(gpu[n][tok][:, heads])
+        compare(n, got, ref[n], rel_max=ROTATED_REL_MAX[n])
+        assert O.cosine(got[:, 0], ex[n][:, 0]) >= 0.998, (n, "head 1")
+        method = O.cosine(ref[n][:, 1], ex[n][:, 1])
+        assert O.cosine(got[:, 1], ex[n][:, 1]) >= method - 2e-4, (n, "head 13", method)
 
 
 # The rotation back makes every element of dQ and dK a +-1 sum over all d
