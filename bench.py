@@ -4,7 +4,10 @@
 inputs, printed as one JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload fixed4x4096]
+                    [--workload long131072]
+
+The default workload is the largest single-GPU configuration: one causal
+document of 131,072 tokens, 32 heads of dimension 64 (MXFP8).
 
 A step is one whole training call over one batch resident in HBM.  FLOPs use
 the causal convention 7 * H * d * sum(L^2) (forward 4, backward 10, over the
@@ -33,18 +36,24 @@ FALLBACK_BF16_SUSTAINED = 1700.0
 FALLBACK_HBM_GBS = 6800.0
 FP8_OVER_BF16 = 2.0               # nominal dense FP8 / BF16 ratio (4.5 / 2.25 PFLOP/s)
 L2_FLUSH_BYTES = 256 << 20
+STRUCTURE_NOTE = {"rms": "per-head RMS drawn in [0.5, 2]",
+                  "outlier20pct1": "1% of channels x20",
+                  "outlier16x2": "2 of 64 channels x16", "plain": "no structure"}
 
 
 def peaks():
+    """FP8 tensor peak = the measured BF16 burst GEMM rate x the nominal FP8 /
+    BF16 ratio: the roofline kernel is timed alone (one launch of well under a
+    second), so the burst figure applies; HBM = the measured copy bandwidth."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             p = json.load(f)
-        bf16 = p.get("bf16_tflops_sustained") or p.get("bf16_tflops")
+        bf16 = p.get("bf16_tflops") or p.get("bf16_tflops_sustained")
         return {"fp8_tflops": float(bf16) * FP8_OVER_BF16, "hbm_gbs": float(p.get("hbm_gbs")),
-                "source": "measured (bf16 x nominal fp8/bf16 ratio)"}
-    return {"fp8_tflops": FALLBACK_BF16_SUSTAINED * FP8_OVER_BF16, "hbm_gbs": FALLBACK_HBM_GBS,
-            "source": "fallback (bf16 sustained x nominal fp8/bf16 ratio)"}
+                "source": "of measured (bf16 burst x nominal fp8/bf16 ratio 2)"}
+    return {"fp8_tflops": FALLBACK_BF16_TFLOPS * FP8_OVER_BF16, "hbm_gbs": FALLBACK_HBM_GBS,
+            "source": "of fallback (bf16 burst x nominal fp8/bf16 ratio 2)"}
 
 
 def dist_env():
@@ -121,15 +130,19 @@ def job_throughput(flops_per_step, steps, world, slowest_ms):
     return world * flops_per_step * steps / (slowest_ms * 1e-3) / 1e12
 
 
+def bwd_kernel_name(w, nvfp4):
+    return ("attn_bwd128_kernel" if w.d == 128 and not nvfp4 else
+            "attn_bwd_kernel_d64_nvfp4" if nvfp4 else f"attn_bwd_kernel_d{w.d}")
+
+
 def profiled_traffic(w, nvfp4):
     """DRAM bytes per launch of the backward kernel from the committed ncu
     summary of this workload, if the kernel's sources are unchanged since the
     capture (else None)."""
     import hashlib
     import re
-    if nvfp4 or w.d != 128:
-        return None
-    path = os.path.join(ROOT, "profiles", f"attn_bwd128_kernel_{w.name.replace('_', '', 1)}.md")
+    path = os.path.join(ROOT, "profiles",
+                        f"{bwd_kernel_name(w, nvfp4)}_{w.name.replace('_', '', 1)}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
@@ -202,6 +215,7 @@ def run_ours(args, rank, world, local):
            for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize(dev)
+    launches0 = fl.flamia_debug_launch_count()
     with ClockSampler(local) as clocks:
         for i in range(args.steps):
             flush.fill_(i & 0xFF)
@@ -218,6 +232,7 @@ def run_ours(args, rank, world, local):
             evb[i][1].record(stream)
             ev[i][1].record(stream)
         torch.cuda.synchronize(dev)
+    launches = fl.flamia_debug_launch_count() - launches0
     barrier()
     call.check_status()
     step_ms = [a.elapsed_time(b) for a, b in ev]
@@ -323,13 +338,6 @@ def run_ours(args, rank, world, local):
     value = job_throughput(flops, args.steps, world, res["total_ms"])
     e2e_value = job_throughput(flops, args.steps, world, res["e2e_ms"])
     achieved = bwd_flops / (res["bwd_ms"] * 1e-3) / 1e12
-    # quantiser: one launch for Q, K, V (two with the rotation: V is not rotated)
-    # and one for dO; work list x6; forward + its short-document kernel; backward +
-    # its short-document kernel; dQ conversion; the FP16 accumulator's prescale
-    # table (two kernels sequence-wide, one causal).  The dQ accumulator memset
-    # is a driver call.
-    launches_per_step = ((3 if args.hadamard else 2) + 6 + 2 + 2 + 1 +
-                         {"fp32": 0, "fp16_sequence": 2, "fp16_causal": 1}[args.dq_accum])
     line = {
         "metric": "MXFP8 causal attn fwd+bwd TFLOP/s incl. quant; % of GB300 FP8 tensor peak",
         "value": round(value, 3),
@@ -342,7 +350,7 @@ def run_ours(args, rank, world, local):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "e4m3 (mxfp8 operands, f32 accumulate)",
-        "data": "synthetic (seeded bf16 normals, 1% outlier channels x20)",
+        "data": "synthetic (seeded bf16 normals, %s)" % STRUCTURE_NOTE.get(w.structure, w.structure),
         "config": {"workload": w.name, "T": w.T, "H": w.H, "d": w.d, "docs": w.ndocs,
                    "qk_product": "nvfp4 (mixed path)" if args.nvfp4 else "mxfp8",
                    "qk_rotation": "hadamard" if args.hadamard else "none",
@@ -357,6 +365,7 @@ def run_ours(args, rank, world, local):
         "pct_of_fp8_peak": round(100.0 * value / world / pk["fp8_tflops"], 2),
         "roofline": {"kernel": "flamia_attn_bwd (memset + %s + short-document kernel + dq convert)"
                                % ("attn_bwd128_kernel" if w.d == 128 and not args.nvfp4
+                                  else "attn_bwd_kernel<64, nvfp4>" if args.nvfp4
                                   else "attn_bwd_kernel<64>"),
                      "bound": "tensor", "achieved": round(achieved, 2),
                      "peak": pk["fp8_tflops"], "unit": "TFLOP/s",
@@ -372,13 +381,84 @@ def run_ours(args, rank, world, local):
                 "copies": "overlapped with compute: 2 buffer sets, copy-in / call / copy-out "
                           "streams ordered by events; 2 untimed warm-up steps",
                 "copy_only_ms_per_step": round(copy_ms, 4)},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": launches,
+        "gpu_launches_counted": "the library's own launch counter read around the timed steps",
         "breakdown": breakdown,
         "clocks": res["clocks"],
     }
+    if not args.no_stress:
+        line["scheduling_stress"] = stress_stats(dev, stream, flush)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
     return line
+
+
+def stress_stats(dev, stream, flush, reps=5):
+    """The scheduling-stress shape (131,072 one-token documents, 16 heads of
+    dimension 128): work-list build time, the call's time, and its peak device
+    memory, the growth of torch's max_memory_allocated from before the call's
+    buffers are allocated to the end of one call (inputs resident beforehand
+    and reported apart)."""
+    import torch
+
+    from precision_causal_attention_block_gb300 import flamia as fl
+    from precision_causal_attention_block_gb300 import workloads as W
+
+    w = W.onetoken131072()
+    xd = {n: t.to(dev) for n, t in W.make_inputs_bf16(w).items()}
+    cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev)
+    torch.cuda.synchronize(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    base = torch.cuda.memory_allocated(dev)
+    call = fl.TrainingCall(w.T, w.H, w.d, cu, w.sm_scale, device=dev)
+    call(xd["q"], xd["k"], xd["v"], xd["do"])
+    torch.cuda.synchronize(dev)
+    peak = torch.cuda.max_memory_allocated(dev) - base
+    call.check_status()
+    times, wl = [], []
+    for _ in range(reps):
+        flush.fill_(3)
+        a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        a.record(stream)
+        fl.flamia_build_worklist(call.cu, call.T, call.wl, dev_status=call.status)
+        b.record(stream)
+        call(xd["q"], xd["k"], xd["v"], xd["do"])
+        c.record(stream)
+        torch.cuda.synchronize(dev)
+        wl.append(a.elapsed_time(b))
+        times.append(b.elapsed_time(c))
+    call.check_status()
+    inputs = sum(t.numel() * t.element_size() for t in xd.values())
+    return {"workload": w.name, "worklist_us": round(1e3 * statistics.median(wl), 2),
+            "call_ms": round(statistics.median(times), 4),
+            "peak_memory_GB": round(peak / 1e9, 3),
+            "peak_memory": "max_memory_allocated growth over buffer allocation + one call",
+            "inputs_GB": round(inputs / 1e9, 3)}
+
+
+def profile_calls(args):
+    """Only the training call, `args.steps` times after `args.warmup` untimed
+    ones, for profiler captures (ncu): no timing, no extra measurements."""
+    import torch
+
+    from precision_causal_attention_block_gb300 import build as B
+    from precision_causal_attention_block_gb300 import flamia as fl
+    from precision_causal_attention_block_gb300 import workloads as W
+
+    if not os.path.exists(B.LIB):
+        B.build()
+    w = make_workload(args.workload)
+    xd = {n: t.cuda() for n, t in W.make_inputs_bf16(w).items()}
+    cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device="cuda")
+    call = fl.TrainingCall(w.T, w.H, w.d, cu, w.sm_scale, nvfp4_qk=args.nvfp4,
+                           hadamard=args.hadamard, causal=not args.noncausal,
+                           deterministic_dq=args.deterministic, dq_accum=args.dq_accum,
+                           schedule=args.schedule, ds_rows=args.ds_rows)
+    for _ in range(args.warmup + args.steps):
+        call(xd["q"], xd["k"], xd["v"], xd["do"])
+    torch.cuda.synchronize()
+    call.check_status()
+    print(json.dumps({"profiled_calls": args.steps, "workload": w.name}))
 
 
 def stage_breakdown(call, xd, stream, flush, w, reps=10):
@@ -519,11 +599,15 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="fixed4x4096")
+    ap.add_argument("--workload", default="long131072")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-stress", action="store_true",
+                    help="skip the one-token-document work-list / peak-memory measurement")
+    ap.add_argument("--profile-calls", action="store_true",
+                    help="run only the training call (for ncu), no timing and no JSON line")
     ap.add_argument("--nvfp4", action="store_true",
                     help="mixed path: QK^T from NVFP4 copies of Q and K (head dim 64)")
     ap.add_argument("--hadamard", action="store_true",
@@ -547,6 +631,8 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     rank, world, local = dist_env()
+    if args.profile_calls:
+        return profile_calls(args)
     line = run_reference(args, rank, world) if args.impl == "reference" else \
         run_ours(args, rank, world, local)
     if line is not None:

@@ -24,7 +24,7 @@
  *   int at `dev_status` (device memory, may be NULL to ignore) as
  *   FLAMIA_DEV_* bits; read it after synchronising the stream.  No kernel
  *   traps or spins without bound.
- * - Support.  head_dim d in {64, 128}; 1 <= H <= 4096; T < 2^24 tokens,
+ * - Support.  head_dim d in {64, 128}; 1 <= H <= 4096; T <= 2^20 tokens,
  *   T * H < 2^31, T * H * d < 2^40; multi-head attention, and grouped K / V
  *   heads through the _gqa entry points; causal masking, or none with
  *   FLAMIA_FLAG_NONCAUSAL.  Larger sizes return FLAMIA_ERR_INVALID_ARG.
@@ -211,9 +211,10 @@ flamia_status flamia_build_worklist(const int32_t* cu_seqlens, int ndocs, int T,
  * document mix of up to 131,072 tokens fits, and at the 1,048,576-token
  * maximum up to 65,536 documents do; a layout whose scratch would exceed
  * 8 MiB returns FLAMIA_ERR_WORKSPACE without launching.
- * No cudaMalloc / cudaFree is called.  The first call on a device looks up the
- * array's device address (with that device current) and caches it; make that
- * first call before any stream capture.  All calls share the one array:
+ * No cudaMalloc / cudaFree is called.  The first call in a CUDA context (with
+ * its device current) looks up the array's device address and caches it under
+ * the context's unique ID; make that first call before any stream capture.  A
+ * context created later (after cudaDeviceReset, say) looks it up again.  All calls share the one array:
  * calls whose kernels overlap on the GPU (different streams, or different
  * host threads without ordering) race and produce garbage; serialise them.
  * Nothing left in the array by an earlier call is read by a later one.
@@ -268,6 +269,14 @@ flamia_status flamia_attn_fwd_gqa(const flamia_qtensor* q, const flamia_qtensor*
                                   int T, int H, int H_kv, int d, float softmax_scale, int flags,
                                   void* wl, void* o_bf16, float* lse, int* dev_status,
                                   void* stream);
+
+/*
+ * Workspace of the forward: 0 bytes for every size (the review page, sec.
+ * 3.4, keeps the forward's running statistics and P^ on chip; O and LSE are
+ * its outputs).  Kept so that a caller sizes both calls the same way;
+ * returns 0 also for unsupported sizes.
+ */
+size_t flamia_fwd_workspace_bytes(int T, int H, int d);
 
 /*
  * Workspace of the backward, each part padded to 256 bytes: a float32

@@ -54,6 +54,14 @@ flamia_status flamia_debug_mma_tile(int mode, int N, int a_mn_major, int b_mn_ma
  */
 flamia_status flamia_debug_bounded_waits(int* turn, int* dev_status, void* stream);
 
+/*
+ * Number of kernel launches the library has enqueued since it was loaded, over
+ * every entry point and host thread (memsets are not kernels and are not
+ * counted).  Read it before and after a region to count that region's
+ * launches.
+ */
+unsigned long long flamia_debug_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,6 +1,7 @@
 // Library-wide pieces of the C ABI: status strings and the driver entry
 // point for tensor-map encoding (resolved at run time, so loading the
 // library needs no libcuda at link time).
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -21,7 +22,15 @@ EncodeTiledFn get_encode_tiled() {
   return fn;
 }
 
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+}
+
+void count_launches(int n) { g_launches.fetch_add(static_cast<unsigned long long>(n)); }
+
 }  // namespace flamia
+
+extern "C" unsigned long long flamia_debug_launch_count(void) { return flamia::g_launches.load(); }
 
 extern "C" const char* flamia_status_str(flamia_status s) {
   switch (s) {

@@ -1005,6 +1005,7 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
                                                              causal ? 1 : 0, pre);
     }
     if (cudaGetLastError() != cudaSuccess) return FLAMIA_ERR_CUDA;
+    count_launches(dq16 == 1 ? 2 : 1);
   }
   // persistent: one CTA per SM (shared memory allows one), items claimed in list order
   const long long grid = std::min<long long>(static_cast<long long>(L.cap_bwd) * Hkv, num_sms());
@@ -1022,6 +1023,7 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
     kernel<<<static_cast<unsigned>(grid), kBwdThreads, smem, stream>>>(
         mq, mk, mv, mdo, mdq, mq4, mk4, prm);
     if (cudaGetLastError() != cudaSuccess) return FLAMIA_ERR_CUDA;
+    count_launches(1);
   }
   if (launch_bwd_short(q, k, v, dout, D, lse, cu, ndocs, T, H, Hkv, DIM, softmax_scale, NVF4, had,
                        causal, ds_rows, acc, pre, dk, dv, stream) != cudaSuccess)
@@ -1031,6 +1033,7 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
     const int blocks = static_cast<int>(std::min<size_t>((rows + 7) / 8, 152 * 16));
     dq_convert_rotate_kernel<DIM><<<blocks, 256, 0, stream>>>(
         acc, static_cast<__nv_bfloat16*>(dq), rows, softmax_scale, pre, T, H);
+    count_launches(1);
     return cudaGetLastError() == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
   }
   if (dq16) {
@@ -1039,12 +1042,14 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
     dq16_convert_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const uint4*>(acc),
                                                     static_cast<uint4*>(dq), n8, DIM, T, H,
                                                     softmax_scale, pre);
+    count_launches(1);
     return cudaGetLastError() == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
   }
   const size_t n4 = n / 4;
   const int blocks = static_cast<int>(std::min<size_t>((n4 + 255) / 256, 152 * 16));
   dq_convert_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(acc),
                                                 static_cast<uint2*>(dq), n4, softmax_scale);
+  count_launches(1);
   return cudaGetLastError() == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
 }
 

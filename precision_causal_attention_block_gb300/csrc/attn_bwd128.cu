@@ -703,6 +703,7 @@ cudaError_t launch_bwd128_pipelined(const BwdParams& prm, const flamia_qtensor* 
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
   kernel<<<grid, kThreads, smem, stream>>>(mq, mk, mv, mdo, mdq, prm);
+  count_launches(1);
   return cudaGetLastError();
 }
 

@@ -668,6 +668,7 @@ flamia_status launch_fwd(const flamia_qtensor* q, const flamia_qtensor* k,
   attn_fwd_kernel<DIM, NVF4>
       <<<static_cast<unsigned>(grid), kFwdThreads, smem, stream>>>(mq, mk, mv, mq4, mk4, prm);
   if (cudaGetLastError() != cudaSuccess) return FLAMIA_ERR_CUDA;
+  count_launches(1);
   return launch_fwd_short(q, k, v, cu, ndocs, T, H, Hkv, DIM, softmax_scale, NVF4, causal, o,
                           lse, stream) ==
                  cudaSuccess
@@ -725,6 +726,10 @@ extern "C" flamia_status flamia_attn_fwd_gqa(const flamia_qtensor* q, const flam
                   : launch_fwd<64, false>(q, k, v, cu_seqlens, ndocs, T, H, H_kv, softmax_scale,
                                           causal, sched, wl, o_bf16, lse, dev_status, s);
 }
+
+// The forward keeps its running statistics and probabilities on chip: no
+// workspace at any size.
+extern "C" size_t flamia_fwd_workspace_bytes(int, int, int) { return 0; }
 
 extern "C" flamia_status flamia_attn_fwd(const flamia_qtensor* q, const flamia_qtensor* k,
                                          const flamia_qtensor* v, const int32_t* cu_seqlens,

@@ -544,6 +544,7 @@ cudaError_t launch_fwd_short(const flamia_qtensor* q, const flamia_qtensor* k,
       attn_fwd_single_kernel<128><<<g1, 256, 0, stream>>>(p);
     else
       attn_fwd_single_kernel<64><<<g1, 256, 0, stream>>>(p);
+    count_launches(1);
     p.skip_single = 1;
   }
   if (nvfp4_qk)
@@ -552,6 +553,7 @@ cudaError_t launch_fwd_short(const flamia_qtensor* q, const flamia_qtensor* k,
     attn_fwd_short_kernel<128, false><<<grid, 32 * kShortWarps, 0, stream>>>(p);
   else
     attn_fwd_short_kernel<64, false><<<grid, 32 * kShortWarps, 0, stream>>>(p);
+  count_launches(1);
   return cudaGetLastError();
 }
 
@@ -579,6 +581,7 @@ cudaError_t launch_bwd_short(const flamia_qtensor* q, const flamia_qtensor* k,
       attn_bwd_single_kernel<128><<<g1, 256, 0, stream>>>(p);
     else
       attn_bwd_single_kernel<64><<<g1, 256, 0, stream>>>(p);
+    count_launches(1);
     p.skip_single = 1;
   }
   if (Hkv == H) {
@@ -589,6 +592,7 @@ cudaError_t launch_bwd_short(const flamia_qtensor* q, const flamia_qtensor* k,
       attn_bwd_short_kernel<128, false, false><<<grid, 32 * kShortWarps, 0, stream>>>(p);
     else
       attn_bwd_short_kernel<64, false, false><<<grid, 32 * kShortWarps, 0, stream>>>(p);
+    count_launches(1);
     return cudaGetLastError();
   }
   // grouped query heads: one warp per (document, K / V head), dK / dV sums in
@@ -612,6 +616,7 @@ cudaError_t launch_bwd_short(const flamia_qtensor* q, const flamia_qtensor* k,
     if (err != cudaSuccess) return err;
     attn_bwd_short_kernel<64, false, true><<<grid, 32 * kShortWarps, smem, stream>>>(p);
   }
+  count_launches(1);
   return cudaGetLastError();
 }
 

@@ -106,14 +106,23 @@ inline bool aligned(const void* p, size_t a) {
 
 inline bool supported_dim(int d) { return d == 64 || d == 128; }
 
+// Largest packed token count of a call.  The work-list builder's per-chunk
+// cost histograms grow with T^2 (chunks x cost buckets), which sets this one
+// limit for every entry point.
+constexpr int kMaxTokens = 1 << 20;
+
 // Sizes the kernels index safely: token x head counts fit an int (per-row
 // tables and counters are indexed by token * H + head in 32 bits), elements
 // in 40 bits (64-bit offsets everywhere else).
 inline bool valid_sizes(int T, int H, int d, int ndocs) {
-  return T > 0 && T < (1 << 24) && H > 0 && H <= 4096 && ndocs >= 1 && ndocs <= T + 1 &&
+  return T > 0 && T <= kMaxTokens && H > 0 && H <= 4096 && ndocs >= 1 && ndocs <= T + 1 &&
          static_cast<long long>(T) * H < (1ll << 31) &&
          static_cast<long long>(T) * H * d < (1ll << 40) && supported_dim(d);
 }
+
+// Kernel launches enqueued by the library since it was loaded (all entry
+// points, all threads); each launch site adds its count after enqueuing.
+void count_launches(int n);  // defined in abi.cu
 
 // Streaming multiprocessors of the current device (persistent grids).
 inline int num_sms() {

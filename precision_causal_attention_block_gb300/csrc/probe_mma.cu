@@ -177,6 +177,7 @@ extern "C" flamia_status flamia_debug_bounded_waits(int* turn, int* dev_status, 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(turn, 0, sizeof(int), s) != cudaSuccess) return FLAMIA_ERR_CUDA;
   flamia::bounded_waits_kernel<<<1, 32, 0, s>>>(turn, dev_status);
+  flamia::count_launches(1);
   return cudaGetLastError() == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
 }
 
@@ -219,5 +220,6 @@ extern "C" flamia_status flamia_debug_mma_tile(int mode, int N, int a_mn_major, 
                            static_cast<int>(smem)) != cudaSuccess)
     return FLAMIA_ERR_CUDA;
   probe_kernel<<<1, 128, smem, static_cast<cudaStream_t>(stream)>>>(ma, mb, g);
+  flamia::count_launches(1);
   return cudaGetLastError() == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
 }

@@ -328,6 +328,7 @@ flamia_status launch_quantize(const void* const* xs, QuantJob& job, int T, int d
                               : fd ? quantize_kernel<64, false, true> : quantize_kernel<64, false, false>);
   kern<<<grid, kQThreads, 0, s>>>(maps[0], maps[1], maps[2], T, cu, ndocs, job,
                                   static_cast<const uint4*>(o_bf16), D, dev_status);
+  count_launches(1);
   return cudaGetLastError() == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
 }
 

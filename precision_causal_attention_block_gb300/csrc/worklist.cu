@@ -18,6 +18,7 @@
 // kShortDoc+1 .. 128 tokens, a backward one (the last key tile) for every
 // document longer than kShortDoc.  Their rank is a per-document prefix count.
 #include <mutex>
+#include <vector>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -320,6 +321,34 @@ __global__ void __launch_bounds__(kSortChunk)
   }
 }
 
+// The six launches of one build; returns FLAMIA_ERR_CUDA if the shared-memory
+// opt-in or a launch fails.
+flamia_status launch_builder(const int32_t* cu_seqlens, int ndocs, int T,
+                             const WorklistLayout& L, const WlPtrs& p, int* dev_status,
+                             cudaStream_t s) {
+  const size_t smem = static_cast<size_t>(L.nbuckets) * sizeof(int);
+  if (smem > 200 * 1024) return FLAMIA_ERR_UNSUPPORTED;
+  if (smem > 48 * 1024) {
+    if (cudaFuncSetAttribute(wl_emit, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess ||
+        cudaFuncSetAttribute(wl_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return FLAMIA_ERR_CUDA;
+  }
+  const int ndchunks = (ndocs + kScanThreads - 1) / kScanThreads;
+  wl_count<<<ndchunks, kScanThreads, 0, s>>>(cu_seqlens, ndocs, T, p, dev_status);
+  wl_scan_docs<<<1, kScanThreads, 0, s>>>(ndchunks, L.cap_fwd, L.cap_bwd, p, dev_status);
+  wl_emit<<<L.chunks_fwd + L.chunks_bwd, kSortChunk, smem, s>>>(cu_seqlens, ndocs, L.chunks_fwd,
+                                                               L.nbuckets, p);
+  wl_scan_chunks<<<(2 * L.nbuckets * 32 + 255) / 256, 256, 0, s>>>(L.nbuckets, L.chunks_fwd,
+                                                                   L.chunks_bwd, p);
+  wl_scan_buckets<<<2, kScanThreads, 0, s>>>(L.nbuckets, p);
+  wl_scatter<<<L.chunks_fwd + L.chunks_bwd, kSortChunk, smem, s>>>(cu_seqlens, ndocs, L.chunks_fwd,
+                                                                  L.nbuckets, p);
+  count_launches(6);
+  return cudaGetLastError() == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace flamia
 
@@ -334,7 +363,7 @@ extern "C" flamia_status flamia_build_worklist(const int32_t* cu_seqlens, int nd
                                                void* wl, size_t wl_bytes, int* dev_status,
                                                void* stream) {
   if (cu_seqlens == nullptr || wl == nullptr || T <= 0 || ndocs <= 0 || ndocs > T + 1 ||
-      T > (1 << 20))
+      T > kMaxTokens)
     return FLAMIA_ERR_INVALID_ARG;
   if (!aligned(wl, 256)) return FLAMIA_ERR_INVALID_ARG;
   const WorklistLayout L = worklist_layout(T, ndocs);
@@ -354,26 +383,8 @@ extern "C" flamia_status flamia_build_worklist(const int32_t* cu_seqlens, int nd
   p.hist_bwd = reinterpret_cast<int*>(base + L.off_hist_bwd);
   p.bucket_fwd = reinterpret_cast<int*>(base + L.off_buckets);
   p.bucket_bwd = p.bucket_fwd + L.nbuckets;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t smem = static_cast<size_t>(L.nbuckets) * sizeof(int);
-  if (smem > 200 * 1024) return FLAMIA_ERR_UNSUPPORTED;
-  if (smem > 48 * 1024) {
-    cudaFuncSetAttribute(wl_emit, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(smem));
-    cudaFuncSetAttribute(wl_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(smem));
-  }
-  const int ndchunks = (ndocs + kScanThreads - 1) / kScanThreads;
-  wl_count<<<ndchunks, kScanThreads, 0, s>>>(cu_seqlens, ndocs, T, p, dev_status);
-  wl_scan_docs<<<1, kScanThreads, 0, s>>>(ndchunks, L.cap_fwd, L.cap_bwd, p, dev_status);
-  wl_emit<<<L.chunks_fwd + L.chunks_bwd, kSortChunk, smem, s>>>(cu_seqlens, ndocs, L.chunks_fwd,
-                                                               L.nbuckets, p);
-  wl_scan_chunks<<<(2 * L.nbuckets * 32 + 255) / 256, 256, 0, s>>>(L.nbuckets, L.chunks_fwd,
-                                                                   L.chunks_bwd, p);
-  wl_scan_buckets<<<2, kScanThreads, 0, s>>>(L.nbuckets, p);
-  wl_scatter<<<L.chunks_fwd + L.chunks_bwd, kSortChunk, smem, s>>>(cu_seqlens, ndocs, L.chunks_fwd,
-                                                                  L.nbuckets, p);
-  return cudaGetLastError() == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
+  return launch_builder(cu_seqlens, ndocs, T, L, p, dev_status,
+                        static_cast<cudaStream_t>(stream));
 }
 
 // ---------------------------------------------------------------------------
@@ -393,21 +404,57 @@ namespace {
 constexpr size_t kStaticScratchBytes = 8u << 20;  // 8 MiB per GPU, held until exit
 static __device__ __align__(256) unsigned char g_wl_scratch[kStaticScratchBytes];
 
-std::mutex g_scratch_mu;
-void* g_scratch_addr[128] = {};
+// Device address of g_wl_scratch in the current context.  The name is only a
+// host-side stand-in; the address belongs to the module instance loaded in one
+// CUDA context, so it is cached per context under the context's unique ID
+// (cuCtxGetId: never reused within a process, unlike a context handle), and a
+// context created after cudaDeviceReset looks the address up afresh.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
 
-// Device address of g_wl_scratch on the current device (looked up once per
-// device; the name is only a host-side stand-in).
+std::mutex g_scratch_mu;
+struct ScratchEntry {
+  unsigned long long ctx_id;
+  void* addr;
+};
+std::vector<ScratchEntry> g_scratch_addr;
+
+template <typename Fn>
+Fn driver_entry(const char* name) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<Fn>(p);
+}
+
+// The unique ID of the calling thread's current context (0 if there is none).
+unsigned long long current_context_id() {
+  static const CtxGetCurrentFn get_current = driver_entry<CtxGetCurrentFn>("cuCtxGetCurrent");
+  static const CtxGetIdFn get_id = driver_entry<CtxGetIdFn>("cuCtxGetId");
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS ||
+      ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
 void* static_scratch_address() {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return nullptr;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_wl_scratch) != cudaSuccess) return nullptr;
-    g_scratch_addr[dev] = p;
-  }
-  return g_scratch_addr[dev];
+  unsigned long long id = current_context_id();
+  for (const ScratchEntry& e : g_scratch_addr)
+    if (id != 0 && e.ctx_id == id) return e.addr;
+  // first call in this context: the lookup also makes the runtime's primary
+  // context current if no context was current yet
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_wl_scratch) != cudaSuccess || p == nullptr) return nullptr;
+  id = current_context_id();
+  if (id != 0) g_scratch_addr.push_back({id, p});
+  return p;
 }
 
 }  // namespace
@@ -417,7 +464,7 @@ extern "C" flamia_status flamia_build_worklist_static(const int32_t* cu_seqlens,
                                                       int T, void* wl, size_t wl_bytes,
                                                       int* dev_status, void* stream) {
   if (cu_seqlens == nullptr || wl == nullptr || T <= 0 || ndocs <= 0 || ndocs > T + 1 ||
-      T > (1 << 20))
+      T > kMaxTokens)
     return FLAMIA_ERR_INVALID_ARG;
   if (!aligned(wl, 256)) return FLAMIA_ERR_INVALID_ARG;
   const WorklistLayout L = worklist_layout(T, ndocs);
@@ -444,26 +491,8 @@ extern "C" flamia_status flamia_build_worklist_static(const int32_t* cu_seqlens,
   p.hist_bwd = reinterpret_cast<int*>(at(L.off_hist_bwd));
   p.bucket_fwd = reinterpret_cast<int*>(at(L.off_buckets));
   p.bucket_bwd = p.bucket_fwd + L.nbuckets;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t smem = static_cast<size_t>(L.nbuckets) * sizeof(int);
-  if (smem > 200 * 1024) return FLAMIA_ERR_UNSUPPORTED;
-  if (smem > 48 * 1024) {
-    cudaFuncSetAttribute(wl_emit, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(smem));
-    cudaFuncSetAttribute(wl_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(smem));
-  }
   // Every buffer of scratch is fully written before it is read within one
   // call, so nothing left by an earlier call needs clearing.
-  const int ndchunks = (ndocs + kScanThreads - 1) / kScanThreads;
-  wl_count<<<ndchunks, kScanThreads, 0, s>>>(cu_seqlens, ndocs, T, p, dev_status);
-  wl_scan_docs<<<1, kScanThreads, 0, s>>>(ndchunks, L.cap_fwd, L.cap_bwd, p, dev_status);
-  wl_emit<<<L.chunks_fwd + L.chunks_bwd, kSortChunk, smem, s>>>(cu_seqlens, ndocs, L.chunks_fwd,
-                                                               L.nbuckets, p);
-  wl_scan_chunks<<<(2 * L.nbuckets * 32 + 255) / 256, 256, 0, s>>>(L.nbuckets, L.chunks_fwd,
-                                                                   L.chunks_bwd, p);
-  wl_scan_buckets<<<2, kScanThreads, 0, s>>>(L.nbuckets, p);
-  wl_scatter<<<L.chunks_fwd + L.chunks_bwd, kSortChunk, smem, s>>>(cu_seqlens, ndocs, L.chunks_fwd,
-                                                                  L.nbuckets, p);
-  return cudaGetLastError() == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
+  return launch_builder(cu_seqlens, ndocs, T, L, p, dev_status,
+                        static_cast<cudaStream_t>(stream));
 }

@@ -51,6 +51,7 @@ SIGNATURES = {
     "flamia_attn_fwd": (_i, [_QP, _QP, _QP, _vp, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp, _vp, _vp]),
     "flamia_attn_fwd_gqa": (_i, [_QP, _QP, _QP, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp,
                                  _vp, _vp]),
+    "flamia_fwd_workspace_bytes": (_sz, [_i, _i, _i]),
     "flamia_bwd_workspace_bytes": (_sz, [_i, _i, _i]),
     "flamia_attn_bwd": (_i, [_QP, _QP, _QP, _QP, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp,
                              _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
@@ -60,6 +61,7 @@ SIGNATURES = {
     "flamia_status_str": (ctypes.c_char_p, [_i]),
     "flamia_debug_mma_tile": (_i, [_i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "flamia_debug_bounded_waits": (_i, [_vp, _vp, _vp]),
+    "flamia_debug_launch_count": (ctypes.c_ulonglong, []),
 }
 
 
@@ -173,6 +175,10 @@ def flamia_attn_fwd_gqa(q: QTensor, k: QTensor, v: QTensor, cu_seqlens, T, H, H_
                                       _ptr(dev_status), _stream()), "flamia_attn_fwd_gqa")
 
 
+def flamia_fwd_workspace_bytes(T: int, H: int, d: int) -> int:
+    return int(load().flamia_fwd_workspace_bytes(T, H, d))
+
+
 def flamia_bwd_workspace_bytes(T: int, H: int, d: int) -> int:
     return int(load().flamia_bwd_workspace_bytes(T, H, d))
 
@@ -198,6 +204,11 @@ def flamia_attn_bwd_gqa(q: QTensor, k: QTensor, v: QTensor, dout: QTensor, D, ls
                                       flags, _ptr(wl), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws),
                                       ws.numel() * ws.element_size(), _ptr(dev_status),
                                       _stream()), "flamia_attn_bwd_gqa")
+
+
+def flamia_debug_launch_count() -> int:
+    """Kernel launches the library has enqueued since it was loaded."""
+    return int(load().flamia_debug_launch_count())
 
 
 def flamia_debug_bounded_waits(turn, dev_status):

@@ -4,6 +4,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -44,6 +45,9 @@ def test_size_queries(cpu_lib):
     wl = fl.flamia_worklist_bytes(65536, 30)
     assert wl >= 64 + 16 * (65536 // 256 + 31) + 16 * (65536 // 128 + 31)
     assert fl.flamia_worklist_bytes(0, 1) == 0
+    # the forward needs no workspace at any size
+    assert fl.flamia_fwd_workspace_bytes(16384, 16, 128) == 0
+    assert fl.flamia_fwd_workspace_bytes(1 << 20, 32, 64) == 0
 
 
 def test_status_strings(cpu_lib):
@@ -62,10 +66,19 @@ def test_host_side_argument_checks(cpu_lib):
     # null input
     assert cpu_lib.flamia_quantize_tokenblock(null, 16, 1, 64, null, 1, 0, null, null,
                                               ctypes.byref(q), null, null) == 1
-    # work list: buffer too small / null
+    # work list: null / buffer too small / more tokens than the one limit
+    # (real, if host-side, buffers: these checks return before any launch)
     assert cpu_lib.flamia_build_worklist(null, 1, 16, null, 0, null, null) == 1
-    assert cpu_lib.flamia_build_worklist(ctypes.c_void_p(256), 1, 16, ctypes.c_void_p(256), 8,
+    cu = np.array([0, 16], dtype=np.int32)
+    big = np.zeros(fl.flamia_worklist_bytes(16, 1) + 256, dtype=np.uint8)
+    big_al = ctypes.c_void_p((big.ctypes.data + 255) // 256 * 256)
+    assert cpu_lib.flamia_build_worklist(cu.ctypes.data_as(ctypes.c_void_p), 1, 16, big_al, 8,
                                          null, null) == 3
+    for fn in (cpu_lib.flamia_build_worklist, cpu_lib.flamia_build_worklist_static):
+        assert fn(cu.ctypes.data_as(ctypes.c_void_p), 1, (1 << 20) + 1, big_al, big.nbytes - 256,
+                  null, null) == 1
+    assert cpu_lib.flamia_quantize_tokenblock(null, (1 << 20) + 1, 1, 64, null, 1, 0, null,
+                                              null, ctypes.byref(q), null, null) == 1
     # flags not supported (an unknown bit; static and dynamic scheduling at
     # once; the ordered dQ turns with the static schedule) / bad scale
     for flags in (0x1000, 0x40 | 0x80):

@@ -54,16 +54,32 @@ def _call_both(lib, cu_list, T):
 
 
 def test_matches_the_allocating_builder_twice_in_a_row(lib):
+    from oracle import flamia_oracle as O
     cases = [list(W.varlen65536().cu_seqlens), [0, 300, 301, 1000], list(W.onetoken131072().cu_seqlens)]
     for cu in cases:  # consecutive calls reuse the same static scratch
         (h0, f0, b0), (h1, f1, b1) = _call_both(lib, cu, cu[-1])
         assert np.array_equal(h0, h1)
         assert np.array_equal(f0, f1) and np.array_equal(b0, b1)
         assert len(f0) > 0
+        # and both are the oracle's lists (the item arrays lead each vector)
+        rf, rb = O.build_worklist(cu)
+        assert np.array_equal(f1[:rf.size], rf.ravel()) and np.array_equal(b1[:rb.size], rb.ravel())
 
 
 def test_rejects_layouts_beyond_the_static_scratch(lib):
+    """A million one-token documents need more scratch than the array holds:
+    the call returns FLAMIA_ERR_WORKSPACE before launching anything.  Every
+    buffer passed is real and of its declared size."""
+    from precision_causal_attention_block_gb300 import flamia as fl
     T = 1 << 20
-    rc = lib.flamia_build_worklist_static(ctypes.c_void_p(256), T + 1 - 1, T, ctypes.c_void_p(256),
-                                          1 << 40, None, None)
-    assert rc == 3  # FLAMIA_ERR_WORKSPACE, nothing launched
+    cu = torch.arange(T + 1, dtype=torch.int32, device="cuda")
+    n = fl.flamia_worklist_bytes(T, T)
+    wl = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = lib.flamia_build_worklist_static(ctypes.c_void_p(cu.data_ptr()), T, T,
+                                          ctypes.c_void_p(wl.data_ptr()), n,
+                                          ctypes.c_void_p(st.data_ptr()),
+                                          ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == 3  # FLAMIA_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and int(wl.count_nonzero().item()) == 0
