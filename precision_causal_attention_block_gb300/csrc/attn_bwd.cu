@@ -8,28 +8,32 @@
 // Items are ordered head-major (all key tiles of a head, longest first, then
 // the next head), so the Q / dO tiles and the dQ rows a wave of CTAs touches
 // belong to few heads and stay in L2.  Warp roles:
-//   warp 0       TMA producer: K, V per item; Q, dO tiles through a 2-stage ring.
+//   warp 0       TMA producer: K, V per item; Q, dO tiles through a 3-stage ring.
 //   warp 1       tensor-memory owner and single-thread tcgen05 MMA issuer.
 //   warps 4-7    compute group 0: query columns 0..63 of every tile
 //   warps 8-11   compute group 1: query columns 64..127
 //   (thread = key row of S^T / dP^T; for the dQ partial thread = query row,
 //   the two groups splitting the head dimension).
-// Per query tile u:
+// Per query tile t:
 //   S^T = K Q^T and dP^T = V dO^T (unscaled E4M3, f32 in TMEM);
 //   the compute groups recompute P = exp2(s - lse2) with the forward's
 //   factors and masks, write the dV operand RNE_E4M3(2^8 P) and the dS codes
 //   (one round-up exponent per document-aligned 32x32 block) to shared
 //   memory, and the block scales of the three products to TMEM;
-//   dV += P^b^T dO, dK += dS^T Q (both stay in TMEM over all u) and
-//   dQ_u = dS K are block-scaled MMAs;
-//   dQ_u is staged in shared memory and added in float32 to the global
+//   dV += P^b^T dO, dK += dS^T Q (both stay in TMEM over all t) and
+//   dQ_t = dS K are block-scaled MMAs;
+//   dQ_t is staged in shared memory and added in float32 to the global
 //   accumulator by bulk tensor reduce-adds.
-// Tensor memory (512 columns): S^T [0,128), dP^T and the scale factors
-// [128,256), dV [256,320), dK [320,384), the NVFP4 score scales [384,396),
-// dQ_u [448,512).  dQ_u has its own columns, so the next tile's S^T / dP^T are
-// issued right behind this tile's products (one thread's MMAs run in order,
-// so dP^T_{u+1} cannot overwrite the scales they read) and compute while the
-// groups read dQ_u out.
+// The tensor core and the compute groups overlap in both directions: the
+// groups signal as soon as they have loaded the last S^T / dP^T columns of
+// tile t into registers, and S^T / dP^T of tile t+1 are issued then, while
+// the groups still turn tile t into P^b and dS; the products of tile t run
+// while the groups compute tile t+1, which reads dQ_t out after its own
+// recompute (the P^b / dS payloads and the block scales are double-buffered
+// by tile parity).
+// Tensor memory (512 columns): S^T [0,128), dP^T [128,256), dV [256,320),
+// dK [320,384), the NVFP4 score scales [384,396), the block scales of the
+// products of even / odd tiles [400,424) / [424,448), dQ_t [448,512).
 #include <cuda_bf16.h>
 
 #include "bwd_common.cuh"
@@ -37,15 +41,16 @@
 namespace flamia {
 namespace {
 
-constexpr int kBStages = 2;
+constexpr int kBStages = 3;
 constexpr int kBwdThreads = 384;
 constexpr int kComputeThreads = 256;
 constexpr uint32_t kColSP = 0, kColDP = 128, kColDV = 256, kColDQ = 448;
-// scale-factor columns inside the dP^T region (written after dP^T is read)
-constexpr uint32_t kSfDvA = 128, kSfDvB = 132, kSfDkA = 136, kSfDkB = 140, kSfDqA = 144,
-                   kSfDqB = 148;
+// block-scale columns of a tile's products, by tile parity
+constexpr uint32_t kColSf = 400;
+constexpr uint32_t kSfDvA = 0, kSfDvB = 4, kSfDkA = 8, kSfDkB = 12, kSfDqA = 16, kSfDqB = 20;
+__device__ __forceinline__ uint32_t col_sf(int t) { return kColSf + 24u * static_cast<uint32_t>(t & 1); }
 
-template <int DIM, bool NVF4>
+template <int DIM, bool NVF4, bool OPT>
 struct BwdSmem {
   static constexpr int kTileBytes = kTile * DIM;
   static constexpr int kTile4Bytes = NVF4 ? kTile * DIM / 2 : 16;  // packed E2M1 tile
@@ -53,10 +58,12 @@ struct BwdSmem {
   alignas(1024) uint8_t v[kTileBytes];
   alignas(1024) uint8_t q[kBStages][kTileBytes];
   alignas(1024) uint8_t dout[kBStages][kTileBytes];
-  alignas(1024) uint8_t pb[kTile * kTile];  // [key][query] E4M3, 128B-swizzled rows
-  alignas(1024) uint8_t ds[kTile * kTile];  // [key][query] E4M3, 128B-swizzled rows
-  alignas(1024) uint8_t ds2[kTile * kTile];  // query-row dS exponents: dQ's dS codes
-  // dQ_u staging: DIM/32 boxes of [128 query rows][32 floats], 128B-swizzled
+  // [key][query] E4M3, 128B-swizzled rows, by tile parity
+  alignas(1024) uint8_t pb[2][kTile * kTile];
+  alignas(1024) uint8_t ds[2][kTile * kTile];
+  // query-row dS exponents (optional-mode instances only): dQ's dS codes
+  alignas(1024) uint8_t ds2[OPT ? 2 : 1][OPT ? kTile * kTile : 1024];
+  // dQ_t staging: DIM/32 boxes of [128 query rows][32 floats], 128B-swizzled
   alignas(1024) float dqs[DIM / 32][kTile * 32];
   alignas(NVF4 ? 1024 : 16) uint8_t k4[kTile4Bytes];
   alignas(NVF4 ? 1024 : 16) uint8_t q4[kBStages][kTile4Bytes];
@@ -64,20 +71,27 @@ struct BwdSmem {
   // loaded while the current one is processed)
   alignas(16) float nl[2][kTile];  // 8 - lse2 of each query column (-inf outside the document)
   alignas(16) float dd[2][kTile];  // D of each query column (0 outside)
-  alignas(16) float pf[2][kTile];  // FP16 dQ: prescale 2^p of each query (0 outside)
+  // FP16 dQ: prescale 2^p of each query (0 outside); three buffers, since a
+  // tile's dQ is staged while the next tile is computed
+  alignas(16) float pf[3][kTile];
   uint32_t qbyte[2][4], dobyte[2][4];  // E8M0 bytes of the 4 query blocks of Q and dO
   uint32_t eds[4][4];            // dS block bytes [query block][key block]
   uint8_t erow[4][4][32];        // query-row dS bytes [query block][key block][query]
   uint64_t bar_kv;
   uint64_t bar_qd_full[kBStages];
   uint64_t bar_qd_empty[kBStages];
-  uint64_t bar_s_full, bar_ds_full, bar_dq_full, bar_dq_read, bar_done, bar_sf;
-  uint64_t bar_kv_free, bar_acc_empty;
+  uint64_t bar_s_full, bar_sdp_read, bar_ds_full, bar_dq_full, bar_dq_read, bar_done, bar_sf;
+  uint64_t bar_kv_free, bar_acc_full, bar_acc_empty;
   ItemRing<4> ring;  // claimed items: producer -> MMA issuer, compute leader
   int item_bc[2];    // the compute leader's copy for the compute groups
   uint32_t tmem_base;
   volatile int abort;
 };
+
+// one CTA per SM: the largest instance fits the 227 KB a CTA may take (with
+// the 1 KB alignment slack of the launch)
+static_assert(sizeof(BwdSmem<64, true, true>) + 1024 <= 232448, "backward shared memory");
+static_assert(sizeof(BwdSmem<64, false, true>) + 1024 <= 232448, "backward shared memory");
 
 template <int DIM>
 __host__ __device__ constexpr uint32_t operand_layout() {
@@ -85,11 +99,11 @@ __host__ __device__ constexpr uint32_t operand_layout() {
 }
 
 // NVFP4 score product (d = 64): tensor-memory columns of the block scales of
-// K (4 columns) and of Q_u (two 4-column buffers, by u parity).
+// K (4 columns) and of Q_t (two 4-column buffers, by t parity).
 constexpr uint32_t kSfK4 = 384, kSfQ4 = 388;
 
-// OPT: the deterministic dQ mode or the FP16 accumulator is on (their code
-// is compiled only into these instances).
+// OPT: the deterministic dQ mode, the FP16 accumulator or the query-row dS
+// exponents are on (their code is compiled only into these instances).
 template <int DIM, bool NVF4, bool OPT>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap map_q,
@@ -99,9 +113,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     const __grid_constant__ CUtensorMap map_dq,
                     const __grid_constant__ CUtensorMap map_q4,
                     const __grid_constant__ CUtensorMap map_k4, const BwdParams prm) {
+  static_assert(DIM == 64, "head dim 128 runs attn_bwd128_kernel (tensor-memory plan for 64)");
   static_assert(!NVF4 || DIM == 64, "the NVFP4 score product is built for head dim 64");
+  using Smem = BwdSmem<DIM, NVF4, OPT>;
   extern __shared__ uint8_t smem_raw[];
-  BwdSmem<DIM, NVF4>& sm = *reinterpret_cast<BwdSmem<DIM, NVF4>*>(
+  Smem& sm = *reinterpret_cast<Smem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
   const int H = prm.H, T = prm.T;
@@ -127,9 +143,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(smem_u32(&sm.bar_qd_empty[i]), 1);
     }
     mbar_init(smem_u32(&sm.bar_s_full), 1);
+    mbar_init(smem_u32(&sm.bar_sdp_read), kComputeThreads);
     mbar_init(smem_u32(&sm.bar_ds_full), kComputeThreads);
     mbar_init(smem_u32(&sm.bar_dq_full), 1);
     mbar_init(smem_u32(&sm.bar_dq_read), kComputeThreads);
+    mbar_init(smem_u32(&sm.bar_acc_full), 1);
     mbar_init(smem_u32(&sm.bar_acc_empty), kComputeThreads);
     mbar_init(smem_u32(&sm.bar_done), 1);
     mbar_init(smem_u32(&sm.bar_sf), kTile);
@@ -145,8 +163,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-  constexpr uint32_t kTileBytes = BwdSmem<DIM, NVF4>::kTileBytes;
-  constexpr uint32_t kPairBytes = 2 * kTileBytes + (NVF4 ? BwdSmem<DIM, NVF4>::kTile4Bytes : 0);
+  constexpr uint32_t kTileBytes = Smem::kTileBytes;
+  constexpr uint32_t kPairBytes = 2 * kTileBytes + (NVF4 ? Smem::kTile4Bytes : 0);
   constexpr uint32_t lay = operand_layout<DIM>();
   constexpr uint32_t sbo = 8 * DIM;
 
@@ -213,24 +231,54 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs this role on warp-uniform values; one elected lane
-    // issues each tcgen05 instruction.
+    // issues each tcgen05 instruction.  Order per tile t: S^T / dP^T of tile
+    // t+1 (once the groups hold tile t's in registers), then dV_t, dK_t and
+    // dQ_t (once tile t's dS is written and dQ_{t-1} has been read out).  Each
+    // barrier phase is waited for before the next one can complete.
     {
       const uint32_t id_s = idesc_f8(kTile, kTile, 0, 0);
-      // operand descriptors, built once: a K step or a ring stage moves only
-      // the start address (bits 0..13, address / 16), which never carries out
-      // of its field inside shared memory
+      // operand descriptors, built once: a K step, a ring stage or a payload
+      // buffer moves only the start address (bits 0..13, address / 16), which
+      // never carries out of its field inside shared memory
       const uint64_t dk = smem_desc(smem_u32(sm.k), 0, sbo, lay);
       const uint64_t dv = smem_desc(smem_u32(sm.v), 0, sbo, lay);
       const uint64_t dq0 = smem_desc(smem_u32(sm.q[0]), 0, sbo, lay);
       const uint64_t ddo0 = smem_desc(smem_u32(sm.dout[0]), 0, sbo, lay);
-      const uint64_t dpb = smem_desc(smem_u32(sm.pb), 0, 1024, kLayoutSW128);
-      const uint64_t dds = smem_desc(smem_u32(sm.ds), 0, 1024, kLayoutSW128);
+      const uint64_t dpb0 = smem_desc(smem_u32(sm.pb[0]), 0, 1024, kLayoutSW128);
+      const uint64_t dds0 = smem_desc(smem_u32(sm.ds[0]), 0, 1024, kLayoutSW128);
       // dQ's dS operand: the query-row-exponent copy when asked for
-      const uint64_t ddq =
-          smem_desc(smem_u32(OPT && prm.ds_rows ? sm.ds2 : sm.ds), 0, 1024, kLayoutSW128);
-      constexpr uint32_t kStep = kTileBytes / 16;  // one ring stage
+      const uint64_t ddq0 =
+          smem_desc(smem_u32(OPT && prm.ds_rows ? sm.ds2[0] : sm.ds[0]), 0, 1024, kLayoutSW128);
+      constexpr uint32_t kStep = kTileBytes / 16;         // one ring stage
+      constexpr uint32_t kPStep = kTile * kTile / 16;     // one payload buffer
       int nk = 0, uc = 0;  // items and query tiles consumed so far
       bool ok = true;
+      // S^T_t and dP^T_t: tile t's Q / dO have landed and the groups have read
+      // tile t-1's S^T / dP^T columns
+      auto issue_sdp = [&](int t) -> bool {
+        const int st = t % kBStages;
+        if (!mbar_wait_w(smem_u32(&sm.bar_qd_full[st]), (t / kBStages) & 1) ||
+            (t > 0 && !mbar_wait_w(smem_u32(&sm.bar_sdp_read), (t - 1) & 1)) ||
+            __any_sync(0xffffffffu, sm.abort))
+          return false;
+        tc_fence_after();
+        const uint64_t dq = dq0 + st * kStep, ddo = ddo0 + st * kStep;
+        if (NVF4) {
+          // S^T from the NVFP4 copies: packed E2M1 rows of 32 bytes, one K = 64 product
+          mma_nvf4_w(tmem + kColSP, smem_desc(smem_u32(sm.k4), 0, 256, kLayoutSW32),
+                     smem_desc(smem_u32(sm.q4[st]), 0, 256, kLayoutSW32),
+                     idesc_nvf4(kTile, kTile), tmem + kSfK4, tmem + kSfQ4 + 4 * (t & 1), 0);
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < DIM / 32; ++ks)
+            mma_f8_w(tmem + kColSP, dk + 2 * ks, dq + 2 * ks, id_s, ks > 0);
+        }
+#pragma unroll
+        for (int ks = 0; ks < DIM / 32; ++ks)
+          mma_f8_w(tmem + kColDP, dv + 2 * ks, ddo + 2 * ks, id_s, ks > 0);
+        tc_commit_w(smem_u32(&sm.bar_s_full));
+        return true;
+      };
       for (int n = 0; ok; ++n) {
         // every lane takes lane 0's copy; one arrive frees the slot
         const int idx = __shfl_sync(0xffffffffu, ring_get(sm.ring, n, false), 0);
@@ -246,38 +294,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ok = mbar_wait_w(smem_u32(&sm.bar_kv), nk & 1);
         if (NVF4) ok = ok && mbar_wait_w(smem_u32(&sm.bar_sf), nk & 1);
         ++nk;
-        // S^T_u and dP^T_u (tile u's Q / dO have landed)
-        auto issue_sdp = [&](int uq) -> bool {
-          const int st = uq % kBStages;
-          if (!mbar_wait_w(smem_u32(&sm.bar_qd_full[st]), (uq / kBStages) & 1) ||
-              __any_sync(0xffffffffu, sm.abort))
-            return false;
-          tc_fence_after();
-          const uint64_t dq = dq0 + st * kStep, ddo = ddo0 + st * kStep;
-          if (NVF4) {
-            // S^T from the NVFP4 copies: packed E2M1 rows of 32 bytes, one K = 64 product
-            mma_nvf4_w(tmem + kColSP, smem_desc(smem_u32(sm.k4), 0, 256, kLayoutSW32),
-                     smem_desc(smem_u32(sm.q4[st]), 0, 256, kLayoutSW32),
-                     idesc_nvf4(kTile, kTile), tmem + kSfK4, tmem + kSfQ4 + 4 * (uq & 1), 0);
-          } else {
-#pragma unroll
-            for (int ks = 0; ks < DIM / 32; ++ks)
-              mma_f8_w(tmem + kColSP, dk + 2 * ks, dq + 2 * ks, id_s, ks > 0);
-          }
-#pragma unroll
-          for (int ks = 0; ks < DIM / 32; ++ks)
-            mma_f8_w(tmem + kColDP, dv + 2 * ks, ddo + 2 * ks, id_s, ks > 0);
-          tc_commit_w(smem_u32(&sm.bar_s_full));
-          return true;
-        };
         const int ntot = it.nq * G;  // tiles over the item's query heads
         if (ntot > 0) ok = ok && issue_sdp(uc);
         for (int u = 0; ok && u < ntot; ++u, ++uc) {
-          const int st = uc % kBStages;
+          const int st = uc % kBStages, b = uc & 1;
           const uint64_t dq = dq0 + st * kStep, ddo = ddo0 + st * kStep;
+          const uint64_t dpb = dpb0 + b * kPStep, dds = dds0 + b * kPStep;
+          const uint64_t ddq = ddq0 + b * kPStep;
+          const uint32_t sf = tmem + col_sf(uc);
+          // the next tile's S^T / dP^T as soon as this tile's are in registers
+          if (u + 1 < ntot && !issue_sdp(uc + 1)) {
+            ok = false;
+            break;
+          }
           // dV / dK restart from zero on an item's first tile: the previous
-          // item's epilogue must have read them (its S^T / dP^T products could
-          // already run meanwhile)
+          // item's epilogue must have read them
           if (!mbar_wait_w(smem_u32(&sm.bar_ds_full), uc & 1) ||
               (u == 0 && nk > 1 && !mbar_wait_w(smem_u32(&sm.bar_acc_empty), (nk - 2) & 1)) ||
               __any_sync(0xffffffffu, sm.abort)) {
@@ -285,7 +316,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             break;
           }
           tc_fence_after();
-          // dQ_u = dS K into its own columns, once the groups have read dQ_{u-1}:
+          // dV += P^b^T dO : A [key][query] K-major, B = dO tile read MN-major
+#pragma unroll
+          for (int kb = 0; kb < 4; ++kb)
+            mma_mxf8_w(tmem + kColDV, dpb + 2 * kb, ddo + kb * (32 * DIM / 16),
+                       idesc_mxf8(kTile, DIM, 0, 1, kb, kb), sf + kSfDvA, sf + kSfDvB,
+                       (u > 0 || kb > 0));
+          // dK += dS^T Q : A [key][query] K-major, B = Q tile read MN-major
+#pragma unroll
+          for (int kb = 0; kb < 4; ++kb)
+            mma_mxf8_w(tmem + kColDV + DIM, dds + 2 * kb, dq + kb * (32 * DIM / 16),
+                       idesc_mxf8(kTile, DIM, 0, 1, kb, kb), sf + kSfDkA, sf + kSfDkB,
+                       (u > 0 || kb > 0));
+          tc_commit_w(smem_u32(&sm.bar_qd_empty[st]));
+          // dQ_t = dS K into its own columns, once the groups have read dQ_{t-1}:
           // A = the same dS bytes read MN-major (M = queries), B = K MN-major
           if (uc > 0 && (!mbar_wait_w(smem_u32(&sm.bar_dq_read), (uc - 1) & 1) ||
                          __any_sync(0xffffffffu, sm.abort))) {
@@ -296,30 +340,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int kb = 0; kb < 4; ++kb)
             mma_mxf8_w(tmem + kColDQ, ddq + kb * (32 * kTile / 16), dk + kb * (32 * DIM / 16),
-                     idesc_mxf8(kTile, DIM, 1, 1, kb, kb), tmem + kSfDqA, tmem + kSfDqB, kb > 0);
-          // dQ first: the groups read it out while dV / dK run
+                       idesc_mxf8(kTile, DIM, 1, 1, kb, kb), sf + kSfDqA, sf + kSfDqB, kb > 0);
           tc_commit_w(smem_u32(&sm.bar_dq_full));
-          // dV += P^b^T dO : A [key][query] K-major, B = dO tile read MN-major
-#pragma unroll
-          for (int kb = 0; kb < 4; ++kb)
-            mma_mxf8_w(tmem + kColDV, dpb + 2 * kb, ddo + kb * (32 * DIM / 16),
-                     idesc_mxf8(kTile, DIM, 0, 1, kb, kb), tmem + kSfDvA, tmem + kSfDvB,
-                     (u > 0 || kb > 0));
-          // dK += dS^T Q : A [key][query] K-major, B = Q tile read MN-major
-#pragma unroll
-          for (int kb = 0; kb < 4; ++kb)
-            mma_mxf8_w(tmem + kColDV + DIM, dds + 2 * kb, dq + kb * (32 * DIM / 16),
-                     idesc_mxf8(kTile, DIM, 0, 1, kb, kb), tmem + kSfDkA, tmem + kSfDkB,
-                     (u > 0 || kb > 0));
-          tc_commit_w(smem_u32(&sm.bar_qd_empty[st]));
-          // the next tile's S^T / dP^T right behind
-          if (u + 1 < ntot && !issue_sdp(uc + 1)) {
-            ok = false;
-            break;
-          }
         }
-        // this item's K / V may be replaced once its products are done
-        if (ok) tc_commit_w(smem_u32(&sm.bar_kv_free));
+        // dV / dK of the item are complete, and its K / V may be replaced
+        if (ok) {
+          tc_commit_w(smem_u32(&sm.bar_acc_full));
+          tc_commit_w(smem_u32(&sm.bar_kv_free));
+        }
       }
       if (!ok) sm.abort = 1;
       tc_commit_w(smem_u32(&sm.bar_done));
@@ -329,7 +357,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------------------ compute groups
     const int g = (warp - 4) >> 2;   // 0: query columns 0..63, 1: 64..127
     const int quad = warp & 3;
-    const int j = quad * 32 + lane;  // key row (S^T, dP^T, dV, dK) / query row (dQ_u)
+    const int j = quad * 32 + lane;  // key row (S^T, dP^T, dV, dK) / query row (dQ_t)
     const bool issuer = (warp == 4 && lane == 0);
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const float LOG2E = 1.4426950408889634f;
@@ -338,7 +366,96 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // (never a barrier), so no thread can be left waiting at bar.sync.
     bool ok = true;
     int uc = 0;  // query tiles processed over all items (phase and buffer parity)
+    int nk = 0;  // items processed
     int* pend = nullptr;  // deterministic dQ: the turn the last reduce-adds pass on
+    // The staging buffer is free once the previous reduce-adds have read it
+    // (deterministic mode: completed, and their turn passed on).
+    auto staging_free = [&]() {
+      if (!issuer) return;
+      if (!OPT || prm.dq_turns == nullptr) {
+        bulk_wait_group_read0();
+      } else {
+        bulk_wait_group0();
+        if (pend != nullptr) pass_turn(pend);
+        pend = nullptr;
+      }
+    };
+    // dQ_t (tile t = ut of the item, global index tg) from tensor memory to the
+    // staging buffer; every compute thread calls it (it arrives on dq_read)
+    auto read_dq = [&](const BwdItem& it, int ut, int tg) {
+      ok = ok && !sm.abort && mbar_wait(smem_u32(&sm.bar_dq_full), tg & 1);
+      tc_fence_after();
+      if (!ok) return;
+      const bool qv = tile_q0(it, ut) + j < it.e;  // TMEM lane j of dQ_t is query row j
+      constexpr int kCh = DIM / 64;  // 32-column chunks of dQ_t per group
+      uint32_t v[kCh][32];
+#pragma unroll
+      for (int cc = 0; cc < kCh; ++cc)
+        tmem_ld32(tmem + lane_off + kColDQ + 32 * (g * kCh + cc), v[cc]);
+      tmem_ld_wait();
+      // dQ of the next tile may now be written
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.bar_dq_read));
+      if (OPT && prm.dq_pre != nullptr) {
+        // x 2^p of the query row (0 outside the document), rounded to FP16,
+        // in DIM / 64 boxes [128 query rows][64 halves], 128B-swizzled
+        const float pf = sm.pf[tg % 3][j];
+        __half* box0 = reinterpret_cast<__half*>(sm.dqs[0]);
+#pragma unroll
+        for (int t = 0; t < 4 * kCh; ++t) {  // 8-dim chunk t of this group's dims
+          const int dim0 = g * 32 * kCh + 8 * t;
+          const int b = dim0 / 64, ch = (dim0 % 64) / 8;
+          uint32_t w[4];
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            const __half2 h2 = __floats2half2_rn(
+                __uint_as_float(v[t / 4][8 * (t % 4) + 2 * x]) * pf,
+                __uint_as_float(v[t / 4][8 * (t % 4) + 2 * x + 1]) * pf);
+            w[x] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
+          *reinterpret_cast<uint4*>(box0 + b * (kTile * 64) + j * 64 + 8 * (ch ^ (j & 7))) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      } else {
+#pragma unroll
+        for (int cc = 0; cc < kCh; ++cc) {
+          float* row = sm.dqs[g * kCh + cc] + j * 32;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            // softmax_scale is applied once, in the float32 -> BF16 conversion
+            float4 f = make_float4(__uint_as_float(v[cc][4 * i]), __uint_as_float(v[cc][4 * i + 1]),
+                                   __uint_as_float(v[cc][4 * i + 2]),
+                                   __uint_as_float(v[cc][4 * i + 3]));
+            if (!qv) f = make_float4(0.f, 0.f, 0.f, 0.f);  // rows of other documents add 0
+            *reinterpret_cast<float4*>(row + 4 * (i ^ (j & 7))) = f;
+          }
+        }
+      }
+    };
+    // the staged dQ_t (after a barrier) reduce-added into the global accumulator
+    auto reduce_dq = [&](const BwdItem& it, int ut) {
+      if (!issuer || sm.abort) return;
+      const int q0 = tile_q0(it, ut), h = tile_head(it, ut);
+      int* turn = !OPT || prm.dq_turns == nullptr
+                      ? nullptr
+                      : prm.dq_turns + static_cast<size_t>(q0) * prm.H + h;
+      if (turn != nullptr && !wait_turn(turn, dq_turn(prm, it, q0))) {
+        sm.abort = 1;
+        return;
+      }
+      if (OPT && prm.dq_pre != nullptr) {
+        const __half* box0 = reinterpret_cast<const __half*>(sm.dqs[0]);
+#pragma unroll
+        for (int b = 0; b < DIM / 64; ++b)
+          tma_reduce_add_3d(&map_dq, smem_u32(box0 + b * (kTile * 64)), 64 * b, h, q0);
+      } else {
+#pragma unroll
+        for (int c = 0; c < DIM / 32; ++c)
+          tma_reduce_add_3d(&map_dq, smem_u32(sm.dqs[c]), 32 * c, h, q0);
+      }
+      bulk_commit_group();
+      pend = turn;
+    };
     for (int n = 0;; ++n) {
       if (issuer) sm.item_bc[n & 1] = ring_get(sm.ring, n, true);
       named_barrier_sync(1, kComputeThreads);
@@ -358,7 +475,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int evj = key_valid ? static_cast<int>(prm.v_scales[hT + kj]) - 127 : 0;
       const float rowf = pow2_or_zero(ekj) * prm.scale_log2;
       const float rowg = pow2_or_zero(evj);
-      // E8M0 bytes of this key tile's 4 key blocks (B scale of dQ_u = dS K)
+      // E8M0 bytes of this key tile's 4 key blocks (B scale of dQ_t = dS K)
       uint32_t kword = 0;
 #pragma unroll
       for (int kb = 0; kb < 4; ++kb) {
@@ -376,17 +493,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tmem_st4(tmem + lane_off + col, w);
       };
       if (NVF4 && g == 0) {
-        // the previous item's products completed before its last dQ was read
+        // the previous item's score products completed before its last tile
+        // was computed
         write_sf4(prm.k4_scales, prm.Hkv, it.hk, k0, kSfK4);
         write_sf4(prm.q4_scales, H, tile_head(it, 0), tile_q0(it, 0), kSfQ4 + 4 * (uc & 1));
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(smem_u32(&sm.bar_sf));
       }
-      // group 0 loads the per-query inputs of the item's tile u into buffer
-      // (global tile index) & 1
       // the per-query inputs of tile u: raw loads from clamped (always valid)
-      // addresses, issued a tile ahead and only used when stored
+      // addresses, issued a tile ahead and only used when stored (group 0)
       float r_lse = 0.f, r_dd = 0.f;
       uint32_t r_qb = 127u, r_dob = 127u;
       int r_pre = 0;
@@ -403,11 +519,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           r_dob = prm.do_scales[at];
         }
       };
-      auto store_query_inputs = [&](int ug) {
-        const int b = ug & 1;
+      auto store_query_inputs = [&](int tg) {
+        const int b = tg & 1;
         sm.nl[b][j] = r_qv ? 8.f - r_lse * LOG2E : -INFINITY;
         sm.dd[b][j] = r_qv ? r_dd : 0.f;
-        if (OPT) sm.pf[b][j] = r_qv ? exp2i(r_pre) : 0.f;
+        if (OPT) sm.pf[tg % 3][j] = r_qv ? exp2i(r_pre) : 0.f;
         if (lane == 0) {
           sm.qbyte[b][quad] = r_qv ? r_qb : 127u;
           sm.dobyte[b][quad] = r_qv ? r_dob : 127u;
@@ -419,13 +535,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       named_barrier_sync(1, kComputeThreads);
       for (int u = 0; u < nq; ++u, ++uc) {
-        const int q0 = tile_q0(it, u), h = tile_head(it, u);
         const int ub = uc & 1;
         if (g == 0 && u + 1 < nq) fetch_query_inputs(u + 1);  // lands during this tile
         ok = ok && !sm.abort && mbar_wait(smem_u32(&sm.bar_s_full), uc & 1);
         tc_fence_after();
-        uint8_t* pbrow = sm.pb + j * kTile;
-        uint8_t* dsrow = sm.ds + j * kTile;
+        uint8_t* pbrow = sm.pb[ub] + j * kTile;
+        uint8_t* dsrow = sm.ds[ub] + j * kTile;
 #pragma unroll 1
         for (int cc = 0; cc < 2 && ok; ++cc) {
           const int c = 2 * g + cc;  // 32-query block of this chunk
@@ -436,6 +551,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tmem_ld32(tmem + lane_off + kColSP + 32 * c, sv);
           tmem_ld32(tmem + lane_off + kColDP + 32 * c, dv);
           tmem_ld_wait();
+          if (cc == 1) {
+            // every S^T / dP^T column this thread needs is in registers: the
+            // next tile's may be computed (its NVFP4 Q scales first)
+            if (NVF4 && g == 0 && u + 1 < nq) {
+              write_sf4(prm.q4_scales, H, tile_head(it, u + 1), tile_q0(it, u + 1),
+                        kSfQ4 + 4 * ((uc + 1) & 1));
+              tmem_st_wait();
+            }
+            tc_fence_before();
+            mbar_arrive(smem_u32(&sm.bar_sdp_read));
+          }
           uint32_t pw[8] = {0, 0, 0, 0, 0, 0, 0, 0};
           float amax = 0.f;
           if (!key_valid) {
@@ -493,16 +619,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                      __uint_as_float(dv[i + 2]) * i2,
                                      __uint_as_float(dv[i + 3]) * i3);
             }
-            uint8_t* ds2row = sm.ds2 + j * kTile;
+            uint8_t* ds2row = sm.ds2[OPT ? ub : 0] + j * kTile;
             *reinterpret_cast<uint4*>(ds2row + 16 * ch0) = make_uint4(dr[0], dr[1], dr[2], dr[3]);
             *reinterpret_cast<uint4*>(ds2row + 16 * ch1) = make_uint4(dr[4], dr[5], dr[6], dr[7]);
           }
         }
+        // the staging buffer must be free before dQ_{t-1} is staged below
+        if (u > 0) staging_free();
         named_barrier_sync(1, kComputeThreads);
         if (ok) {
-          // block scales of the three products; every lane quadrant holds the
-          // same words: column (base + m/32) of an A scale holds the 4 K-block
-          // bytes of rows m/32*32 .. +31
+          // block scales of the three products (this tile's parity buffer,
+          // last read by the products of tile t-2, complete before tile t's
+          // S^T); every lane quadrant holds the same words: column (base +
+          // m/32) of an A scale holds the 4 K-block bytes of rows m/32*32 .. +31
+          const uint32_t sfc = col_sf(uc);
           uint32_t w[8];
           if (g == 0) {
             const uint32_t* db = sm.dobyte[ub];
@@ -514,7 +644,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               w[i] = 0x7F7F7F7Fu;  // dV: A = P^b, scale 2^0
               w[4 + i] = dow;      // dV: B = dO, per query block
             }
-            tmem_st8(tmem + lane_off + kSfDvA, w);
+            tmem_st8(tmem + lane_off + sfc + kSfDvA, w);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               // dK: A = dS^T, row block = key block i, K blocks = query blocks
@@ -522,7 +652,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                      (sm.eds[3][i] << 24);
               w[4 + i] = qw;  // dK: B = Q, per query block
             }
-            tmem_st8(tmem + lane_off + kSfDkA, w);
+            tmem_st8(tmem + lane_off + sfc + kSfDkA, w);
           } else {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -537,113 +667,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                        (sm.eds[i][3] << 24);
               w[4 + i] = kword;  // dQ: B = K, per key block
             }
-            tmem_st8(tmem + lane_off + kSfDqA, w);
+            tmem_st8(tmem + lane_off + sfc + kSfDqA, w);
           }
-          // NVFP4: the next query tile's block scales, before this tile's dS is
-          // released (the next S^T is issued right behind this tile's products;
-          // the buffer of its parity was last read by S^T two tiles back,
-          // complete before this tile's S^T was)
-          if (NVF4 && g == 0 && u + 1 < nq)
-            write_sf4(prm.q4_scales, H, tile_head(it, u + 1), tile_q0(it, u + 1),
-                      kSfQ4 + 4 * ((uc + 1) & 1));
+        }
+        // dQ of the previous tile, computed while this tile was recomputed
+        if (u > 0) read_dq(it, u - 1, uc - 1);
+        if (ok) {
           tmem_st_wait();
           fence_proxy_async_smem();
           tc_fence_before();
           mbar_arrive(smem_u32(&sm.bar_ds_full));
         }
-        ok = ok && !sm.abort && mbar_wait(smem_u32(&sm.bar_dq_full), uc & 1);
-        tc_fence_after();
-        // the previous tile's reduce-adds must have read the staging buffer
-        // (and, in the deterministic mode, completed: their turn is passed on)
-        if (issuer) {
-          if (!OPT || prm.dq_turns == nullptr) {
-            bulk_wait_group_read0();
-          } else {
-            bulk_wait_group0();
-            if (pend != nullptr) pass_turn(pend);
-            pend = nullptr;
-          }
-        }
-        named_barrier_sync(1, kComputeThreads);
-        if (ok) {
-          const bool qv = q0 + j < e;  // TMEM lane j of dQ_u is query row j
-          constexpr int kCh = DIM / 64;  // 32-column chunks of dQ_u per group
-          uint32_t v[kCh][32];
-#pragma unroll
-          for (int cc = 0; cc < kCh; ++cc)
-            tmem_ld32(tmem + lane_off + kColDQ + 32 * (g * kCh + cc), v[cc]);
-          tmem_ld_wait();
-          // dQ of the next tile may now be written
-          tc_fence_before();
-          mbar_arrive(smem_u32(&sm.bar_dq_read));
-          if (OPT && prm.dq_pre != nullptr) {
-            // x 2^p of the query row (0 outside the document), rounded to FP16,
-            // in DIM / 64 boxes [128 query rows][64 halves], 128B-swizzled
-            const float pf = sm.pf[ub][j];
-            __half* box0 = reinterpret_cast<__half*>(sm.dqs[0]);
-#pragma unroll
-            for (int t = 0; t < 4 * kCh; ++t) {  // 8-dim chunk t of this group's dims
-              const int dim0 = g * 32 * kCh + 8 * t;
-              const int b = dim0 / 64, ch = (dim0 % 64) / 8;
-              uint32_t w[4];
-#pragma unroll
-              for (int x = 0; x < 4; ++x) {
-                const __half2 h2 = __floats2half2_rn(
-                    __uint_as_float(v[t / 4][8 * (t % 4) + 2 * x]) * pf,
-                    __uint_as_float(v[t / 4][8 * (t % 4) + 2 * x + 1]) * pf);
-                w[x] = *reinterpret_cast<const uint32_t*>(&h2);
-              }
-              *reinterpret_cast<uint4*>(box0 + b * (kTile * 64) + j * 64 + 8 * (ch ^ (j & 7))) =
-                  make_uint4(w[0], w[1], w[2], w[3]);
-            }
-          }
-#pragma unroll
-          for (int cc = 0; cc < kCh && !(OPT && prm.dq_pre != nullptr); ++cc) {
-            float* row = sm.dqs[g * kCh + cc] + j * 32;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              // softmax_scale is applied once, in the float32 -> BF16 conversion
-              float4 f = make_float4(__uint_as_float(v[cc][4 * i]), __uint_as_float(v[cc][4 * i + 1]),
-                                     __uint_as_float(v[cc][4 * i + 2]),
-                                     __uint_as_float(v[cc][4 * i + 3]));
-              if (!qv) f = make_float4(0.f, 0.f, 0.f, 0.f);  // rows of other documents add 0
-              *reinterpret_cast<float4*>(row + 4 * (i ^ (j & 7))) = f;
-            }
-          }
-          fence_proxy_async_smem();
-        }
         if (!ok) sm.abort = 1;
-        // the next tile's per-query inputs (its buffer was last read before this
-        // tile's second barrier)
+        // the next tile's per-query inputs (its nl / dd / byte buffer was last
+        // read by tile t-1, its prescale buffer by tile t-2's staging)
         if (g == 0 && u + 1 < nq) store_query_inputs(uc + 1);
         named_barrier_sync(1, kComputeThreads);
-        if (issuer && !sm.abort) {
-          int* turn = !OPT || prm.dq_turns == nullptr
-                          ? nullptr
-                          : prm.dq_turns + static_cast<size_t>(q0) * prm.H + h;
-          if (turn != nullptr && !wait_turn(turn, dq_turn(prm, it, q0))) {
-            sm.abort = 1;
-          } else {
-            if (OPT && prm.dq_pre != nullptr) {
-              const __half* box0 = reinterpret_cast<const __half*>(sm.dqs[0]);
-#pragma unroll
-              for (int b = 0; b < DIM / 64; ++b)
-                tma_reduce_add_3d(&map_dq, smem_u32(box0 + b * (kTile * 64)), 64 * b, h, q0);
-            } else {
-#pragma unroll
-              for (int c = 0; c < DIM / 32; ++c)
-                tma_reduce_add_3d(&map_dq, smem_u32(sm.dqs[c]), 32 * c, h, q0);
-            }
-            bulk_commit_group();
-            pend = turn;
-          }
-        }
+        if (u > 0) reduce_dq(it, u - 1);
+      }
+      // the item's last dQ
+      if (nq > 0) {
+        staging_free();
+        named_barrier_sync(1, kComputeThreads);
+        read_dq(it, nq - 1, uc - 1);
+        fence_proxy_async_smem();
+        if (!ok) sm.abort = 1;
+        named_barrier_sync(1, kComputeThreads);
+        reduce_dq(it, nq - 1);
       }
       if (OPT && issuer && pend != nullptr) {  // the item's last turn, before the next item
         bulk_wait_group0();
         pass_turn(pend);
         pend = nullptr;
       }
+      // every product of the item is complete
+      ok = ok && !sm.abort && mbar_wait(smem_u32(&sm.bar_acc_full), nk & 1);
+      tc_fence_after();
+      ++nk;
       if (ok && prm.hadamard) {
         // Q and K were rotated: group 0 writes whole rows of dK = dK_r H_d
         // (the butterflies need all DIM columns of a row), group 1 of dV
@@ -676,8 +736,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_arrive(smem_u32(&sm.bar_acc_empty));
       } else if (ok) {
         // dV = 2^-8 acc, dK = scale * acc, written to the packed buffers; the
-        // groups split the head dimension (every product of the item completed
-        // before its last dQ was read)
+        // groups split the head dimension
         __nv_bfloat16* dvrow = prm.dv + (static_cast<size_t>(kj) * prm.Hkv + it.hk) * DIM;
         __nv_bfloat16* dkrow = prm.dk + (static_cast<size_t>(kj) * prm.Hkv + it.hk) * DIM;
 #pragma unroll 1
@@ -1014,9 +1073,10 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
         cudaSuccess)
       return FLAMIA_ERR_CUDA;
   } else {
-    const size_t smem = sizeof(BwdSmem<DIM, NVF4>) + 1024;
-    auto kernel = (det || dq16 || ds_rows) ? attn_bwd_kernel<DIM, NVF4, true>
-                                           : attn_bwd_kernel<DIM, NVF4, false>;
+    const bool opt = det || dq16 || ds_rows;
+    const size_t smem =
+        (opt ? sizeof(BwdSmem<DIM, NVF4, true>) : sizeof(BwdSmem<DIM, NVF4, false>)) + 1024;
+    auto kernel = opt ? attn_bwd_kernel<DIM, NVF4, true> : attn_bwd_kernel<DIM, NVF4, false>;
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return FLAMIA_ERR_CUDA;
