@@ -268,6 +268,8 @@ def quantize_tokenblock(x, cu_seqlens, rule: str = "up", group: str = "block"):
     """E4M3 codes [T, H, d] and E8M0 scale bytes [H, T] (one byte per token).
 
     group="block": one exponent per (document-local 32-token block, head).
+    group="token": one exponent per (token, head) over its d elements (the
+    per-token operand scales of the precision options).
     group="tensor": one exponent per head over all tokens (negative control).
     rule="up": round-up exponent (never clips); rule="floor": floor rule with
     clipping at 448 (negative control).
@@ -278,6 +280,8 @@ def quantize_tokenblock(x, cu_seqlens, rule: str = "up", group: str = "block"):
     sbytes = np.zeros((H, T), dtype=np.uint8)
     if group == "block":
         blocks = doc_blocks(cu_seqlens, 32)
+    elif group == "token":
+        blocks = doc_blocks(cu_seqlens, 1)
     elif group == "tensor":
         blocks = [(0, T)] if T > 0 else []
     else:
@@ -383,6 +387,9 @@ class DocHead:
         self.qs, self.ks = qs, ks
         self.L = q.shape[0]
         self.causal = True  # False: every query sees every key of the document
+        # per-token operand scales: the per-token factors along a contraction are
+        # folded into the opposite operand before its E4M3 rounding
+        self.token = False
 
 
 def _scores(dh: DocHead, rows: np.ndarray, cols: np.ndarray, sm_scale: float) -> np.ndarray:
@@ -410,11 +417,49 @@ def fwd_rows(dh: DocHead, rows: np.ndarray, sm_scale: float, quant: bool = True)
     m = np.ceil(s.max(axis=1))                                 # integer row maximum
     pt = np.exp2(s - m[:, None])                               # 0 where masked
     l = pt.sum(axis=1)                                         # unquantised sum
+    if quant and dh.token:
+        # V's per-key factor 2^eV(j) folded into P^ relative to the largest
+        # exponent EV(i, b) among the keys of its 32-key block that row i sees
+        EV = _visible_block_max(dh.ev, rows, cols, dh.causal)
+        fold = np.ldexp(1.0, dh.ev[cols][None, :] - EV)
+        ph = e4m3_decode(e4m3_encode(np.ldexp(pt * fold, P_SCALE_LOG2)))
+        o = np.ldexp((ph * np.ldexp(1.0, EV)) @ dh.v[cols], -P_SCALE_LOG2) / l[:, None]
+        return o, m + np.log2(l), m, l
     p8 = np.ldexp(pt, P_SCALE_LOG2)
     ph = e4m3_decode(e4m3_encode(p8)) if quant else p8         # E4M3 probability operand
     vhat = dh.v[cols] * np.ldexp(1.0, dh.ev[cols])[:, None]
     o = np.ldexp(ph @ vhat, -P_SCALE_LOG2) / l[:, None]
     return o, m + np.log2(l), m, l
+
+
+def _visible_block_max(e, rows, cols, causal):
+    """[R, C] int: for row i and column j, the largest e[j'] over the columns j'
+    of j's document-aligned 32-column block that row i sees (j' <= i when
+    causal); 0 where row i sees no column of the block.  rows / cols are
+    doc-local, cols a contiguous range starting on a 32 boundary."""
+    out = np.zeros((len(rows), len(cols)), dtype=np.int64)
+    c0 = int(cols[0]) if len(cols) else 0
+    for j0 in range(0, len(cols), 32):
+        blk = e[cols[j0:j0 + 32]].astype(np.int64)
+        if causal:
+            pm = np.maximum.accumulate(blk)                    # prefix maxima
+            last = np.asarray(rows) - (c0 + j0)                # last visible column in the block
+            vis = last >= 0
+            val = np.where(vis, pm[np.clip(last, 0, len(blk) - 1)], 0)
+        else:
+            val = np.full(len(rows), blk.max())
+        out[:, j0:j0 + 32] = val[:, None]
+    return out
+
+
+def _query_block_max(e, rows):
+    """[R] int: the largest e over each row's document-aligned 32-row block
+    (rows doc-local, contiguous, starting on a 32 boundary, whole blocks
+    except at the document end)."""
+    out = np.empty(len(rows), dtype=np.int64)
+    for i0 in range(0, len(rows), 32):
+        out[i0:i0 + 32] = e[rows[i0:i0 + 32]].max()
+    return out
 
 
 def _block_quantize_dS(dS: np.ndarray, r0: int, c0: int) -> np.ndarray:
@@ -458,6 +503,8 @@ def bwd_rect(dh: DocHead, rows: np.ndarray, cols: np.ndarray, lse2_rows: np.ndar
     dS rounded with query-row exponents (dK keeps the 32x32 block ones)."""
     s = _scores(dh, rows, cols, sm_scale)
     P = np.exp2(s - lse2_rows[:, None])                        # normalised, 0 where masked
+    if quant and dh.token:
+        return _bwd_rect_token(dh, rows, cols, P, D_rows, sm_scale, raw_dq)
     pb = np.ldexp(P, P_SCALE_LOG2)
     pbh = e4m3_decode(e4m3_encode(pb)) if quant else pb        # dV operand
     dohat = dh.do[rows] * np.ldexp(1.0, dh.edo[rows])[:, None]
@@ -472,6 +519,35 @@ def bwd_rect(dh: DocHead, rows: np.ndarray, cols: np.ndarray, lse2_rows: np.ndar
     dSq = _row_quantize_dS(dS, int(cols[0])) if (quant and ds_rows) else dSh
     dQ = (dSq @ khat) if raw_dq else sm_scale * (dSq @ khat)
     return dQ, dK, dV, dS
+
+
+def _bwd_rect_token(dh: DocHead, rows, cols, P, D_rows, sm_scale, raw_dq):
+    """bwd_rect with per-token operand scales: each per-token factor along a
+    contraction is folded into the opposite operand before that operand's
+    E4M3 rounding (review page, sec. 3.2: scales folded into the opposite
+    operand; per-token operand scales with query-row dS exponents close the
+    leakage inside blocks).
+      dV = 2^-8 sum_i P^b_ij 2^EdO(qb) dO_i,  P^b = RNE(2^8 P 2^(e_dO(i) - EdO(qb)));
+      dK = scale sum_i dS^K_ij 2^EQ(qb) Q_i,  dS^K = dS 2^(eQ(i) - EQ(qb)) rounded
+           with one exponent per 32x32 block;
+      dQ = scale sum_j dS^Q_ij K_j (codes),   dS^Q = dS 2^eK(j) rounded with one
+           exponent per (query row, 32-key block);
+    EdO, EQ: the largest exponent of the query's 32-row block (dV and dK sum
+    every later query by definition, so a block-wide choice cannot leak)."""
+    edo_b = _query_block_max(dh.edo, rows)
+    eq_b = _query_block_max(dh.eq, rows)
+    pbh = e4m3_decode(e4m3_encode(np.ldexp(P, P_SCALE_LOG2 + (dh.edo[rows] - edo_b)[:, None])))
+    dohat = dh.do[rows] * np.ldexp(1.0, dh.edo[rows])[:, None]
+    vhat = dh.v[cols] * np.ldexp(1.0, dh.ev[cols])[:, None]
+    dP = dohat @ vhat.T
+    dS = P * (dP - D_rows[:, None])
+    dSk = _block_quantize_dS(np.ldexp(dS, (dh.eq[rows] - eq_b)[:, None]), int(rows[0]),
+                             int(cols[0]))
+    dSq = _row_quantize_dS(np.ldexp(dS, dh.ek[cols][None, :]), int(cols[0]))
+    dV = np.ldexp((pbh * np.ldexp(1.0, edo_b)[:, None]).T @ dh.do[rows], -P_SCALE_LOG2)
+    dK = sm_scale * ((dSk * np.ldexp(1.0, eq_b)[:, None]).T @ dh.q[rows])
+    dQ = dSq @ dh.k[cols]
+    return (dQ if raw_dq else sm_scale * dQ), dK, dV, dS
 
 
 # ----------------------------------------------------------------------------
@@ -564,6 +640,7 @@ class Quantized:
     def __init__(self, q, k, v, do, cu_seqlens, qk_format: str = "mxfp8",
                  rule: str = "up", group: str = "block"):
         self.cu = [int(c) for c in cu_seqlens]
+        self.group = group
         self.qc, self.qs = quantize_tokenblock(q, self.cu, rule, group)
         self.kc, self.ks = quantize_tokenblock(k, self.cu, rule, group)
         self.vc, self.vs = quantize_tokenblock(v, self.cu, rule, group)
@@ -586,6 +663,7 @@ class Quantized:
                      ex(self.dos, h) if self.doc is not None else None)
         if self.qk_format == "nvfp4":
             dh.qs, dh.ks = self.q4[s:e, h], self.k4[s:e, hk]
+        dh.token = self.group == "token"
         return dh
 
 
@@ -615,7 +693,10 @@ def attention(q, k, v, do, cu_seqlens, sm_scale: float, quant: bool = True,
     ``dq_accum``: "fp32" (float32 sums, no prescale), "fp16_sequence" or
     "fp16_causal" (the prescaled FP16 accumulator of dq_fp16_rows, with the
     prescale table returned as ``dq_prescale`` [H, T]).  ``ds_rows``: dQ from
-    dS rounded with query-row exponents (see _row_quantize_dS)."""
+    dS rounded with query-row exponents (see _row_quantize_dS).
+    ``group="token"``: per-token operand scales (one exponent per token and
+    head; the factors along each contraction folded into the opposite operand,
+    see fwd_rows and _bwd_rect_token; dQ always takes query-row exponents)."""
     q = np.asarray(q, dtype=np.float64)
     T, H, d = q.shape
     Hkv = np.asarray(k).shape[1]
