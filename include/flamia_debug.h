@@ -55,6 +55,14 @@ flamia_status flamia_debug_mma_tile(int mode, int N, int a_mn_major, int b_mn_ma
 flamia_status flamia_debug_bounded_waits(int* turn, int* dev_status, void* stream);
 
 /*
+ * The max-reducing tensor-memory load the forward uses on unmasked score
+ * tiles: 128 rows of 32 floats (in, device, row-major [128][32]) are stored to
+ * tensor memory and loaded back; vals receives the loaded values [128][32],
+ * mx the largest value of each row [128] as the load reports it.
+ */
+flamia_status flamia_debug_tmem_ldred(const float* in, float* vals, float* mx, void* stream);
+
+/*
  * Number of kernel launches the library has enqueued since it was loaded, over
  * every entry point and host thread (memsets are not kernels and are not
  * counted).  Read it before and after a region to count that region's

@@ -18,10 +18,17 @@
 // epilogue divides by 2^(m - m_ref) l.
 //
 // Tensor memory (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+d),
-// O_1 [256+d, 256+2d).  After the softmax has read S_t, columns 0..7 of S_t
-// take the scale factors of P^_t V_j and columns 8..39 the P^_t codes (four
-// per column); the next S_t MMA is issued after P^_t V_j, and tcgen05 MMAs of
-// one thread execute in order.
+// O_1 [256+d, 256+2d).  Head dim 128: after the softmax has read S_t, columns
+// 0..7 of S_t take the scale factors of P^_t V_j and columns 8..39 the P^_t
+// codes (four per column); the next S_t MMA is issued after P^_t V_j, and
+// tcgen05 MMAs of one thread execute in order.  Head dim 64: P^_t has columns
+// of its own, [400 + 40 t, 440 + 40 t) in the same arrangement, so the next
+// S_t is issued as soon as the softmax holds the current one in registers and
+// runs while the softmax turns it into P^_t (the pages' split of the next
+// score product around the current P^V); the softmax writes P^_t once the
+// previous P^_t V product has read it.
+// Unmasked tiles take each 32-key chunk's maximum from the max-reducing
+// tensor-memory load (tcgen05.ld.red) instead of 32 comparisons.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -39,6 +46,8 @@ constexpr float kLn2 = 0.69314718055994530942f;
 // Largest exponent of the per-row block scale of P^ before O is rescaled: it
 // bounds O's growth over the true scale to 2^32, far inside float32 range.
 constexpr int kRefSpan = 32;
+// head dim 64: first column of the P^_t region (scale factors, then codes)
+constexpr uint32_t kColPR = 400, kPRStride = 40;
 
 template <int DIM, bool NVF4>
 struct FwdSmem {
@@ -57,6 +66,9 @@ struct FwdSmem {
   uint64_t bar_s_full[2];
   uint64_t bar_p_full[2];
   uint64_t bar_o_full[2];
+  uint64_t bar_s_read[2];   // head dim 64: the softmax holds S_t in registers
+  uint64_t bar_pv_done[2];  // head dim 64: P^_t V_j has read P^_t
+  uint64_t bar_k4;          // head dim 64, NVFP4: the next key tile's block scales written
   uint64_t bar_done;
   ItemRing<4> ring;  // claimed items, producer -> MMA issuer and softmax warps
   uint32_t tmem_base;
@@ -209,9 +221,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(smem_u32(&sm.bar_p_full[t]), kTile);
       mbar_init(smem_u32(&sm.bar_o_full[t]), 1);
       mbar_init(smem_u32(&sm.bar_o_empty[t]), kTile);
+      mbar_init(smem_u32(&sm.bar_s_read[t]), kTile);
+      mbar_init(smem_u32(&sm.bar_pv_done[t]), 1);
     }
     mbar_init(smem_u32(&sm.bar_done), 1);
     mbar_init(smem_u32(&sm.bar_sf), 2 * kTile);
+    mbar_init(smem_u32(&sm.bar_k4), kTile);
     ring_init(sm.ring, kFwdRingConsumers);
     sm.abort = 0;
     fence_barrier_init();
@@ -307,7 +322,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       constexpr uint32_t kStep = kTile * DIM / 16;  // one tile's bytes / 16
       // running counts of each barrier's completions (phase parity = count & 1)
       int nq_used = 0, kvc = 0, o_used[2] = {0, 0}, p_seen[2] = {0, 0};
+      int s_issued[2] = {0, 0}, s_read_seen[2] = {0, 0};  // head dim 64
+      int k4_seen = 0;  // head dim 64, NVFP4: key tiles whose block scales were written
+      constexpr bool kSep = DIM == 64;
       bool ok = true;
+      // head dim 64: S_t may be overwritten once the softmax has read every
+      // S_t issued before (its s_read arrivals)
+      auto wait_s_read = [&](int t) -> bool {
+        while (s_read_seen[t] < s_issued[t]) {
+          if (!mbar_wait_w(smem_u32(&sm.bar_s_read[t]), s_read_seen[t] & 1)) return false;
+          ++s_read_seen[t];
+        }
+        return true;
+      };
       // S_t = Q_t K^T of the key tile with global index jk into columns [128 t, 128 t + 128)
       auto issue_qk = [&](int t, int jk) {
         const int st = jk % kStages;
@@ -323,6 +350,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             mma_f8_w(tmem + t * kTile, dq + 2 * ks, dk + 2 * ks, id_qk, ks > 0);
         }
         tc_commit_w(smem_u32(&sm.bar_s_full[t]));
+        ++s_issued[t];
       };
       for (int n = 0; ok; ++n) {
         // every lane takes lane 0's copy; one arrive frees the slot
@@ -345,10 +373,74 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           break;
         }
         tc_fence_after();
+        if (kSep && (!wait_s_read(0) || (it.valid1 && !wait_s_read(1)))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
         issue_qk(0, kvc);
         if (it.valid1) issue_qk(1, kvc);
         int kv_ready = kvc + 1;  // key tiles known loaded: global indices < kv_ready
-        for (int j = 0; ok && j < it.nkv; ++j) {
+        for (int j = 0; kSep && ok && j < it.nkv; ++j) {
+          const int jk = kvc + j, st = jk % kStages;
+          // NVFP4: the next key tile's block scales are written by group 0 (in
+          // its step j, or in step n0 - 1 for tile 1's last key tile)
+          if (NVF4 && j + 1 < it.nkv) {
+            if (!mbar_wait_w(smem_u32(&sm.bar_k4), k4_seen & 1)) {
+              ok = false;
+              break;
+            }
+            ++k4_seen;
+          }
+          // the next S_t of both tiles, each once its softmax holds the current one
+          for (int t = 0; t < 2 && ok; ++t) {
+            const int nt = t == 0 ? it.n0 : it.n1;
+            if (j + 1 >= nt) continue;
+            if (kv_ready <= jk + 1) {
+              if (!mbar_wait_w(smem_u32(&sm.bar_kv_full[(jk + 1) % kStages]),
+                               ((jk + 1) / kStages) & 1)) {
+                ok = false;
+                break;
+              }
+              kv_ready = jk + 2;
+            }
+            if (!wait_s_read(t) || __any_sync(0xffffffffu, sm.abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_qk(t, jk + 1);
+          }
+          for (int t = 0; t < 2 && ok; ++t) {
+            const int nt = t == 0 ? it.n0 : it.n1;
+            if (j >= nt) continue;
+            if (!mbar_wait_w(smem_u32(&sm.bar_p_full[t]), p_seen[t] & 1) ||
+                __any_sync(0xffffffffu, sm.abort)) {
+              ok = false;
+              break;
+            }
+            ++p_seen[t];
+            if (j == 0 && o_used[t] > 0 &&
+                !mbar_wait_w(smem_u32(&sm.bar_o_empty[t]), (o_used[t] - 1) & 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t dv = dv0 + st * kStep;
+            const uint32_t sf = tmem + kColPR + kPRStride * t;
+#pragma unroll
+            for (int kb = 0; kb < 4; ++kb)
+              mma_mxf8_ts_w(tmem + 256 + t * DIM, sf + kColP + 8 * kb, dv + kb * (32 * DIM / 16),
+                            idesc_mxf8(kTile, DIM, 0, 1, kb, kb), sf, sf + 4, (j > 0 || kb > 0));
+            tc_commit_w(smem_u32(&sm.bar_pv_done[t]));
+            if (j + 1 == nt) {
+              tc_commit_w(smem_u32(&sm.bar_o_full[t]));
+              ++o_used[t];
+            }
+          }
+          if (ok) tc_commit_w(smem_u32(&sm.bar_kv_empty[st]));
+        }
+        for (int j = 0; !kSep && ok && j < it.nkv; ++j) {
           const int jk = kvc + j, st = jk % kStages;
           for (int t = 0; t < 2 && ok; ++t) {
             const int nt = t == 0 ? it.n0 : it.n1;
@@ -411,6 +503,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const uint32_t tS = tmem + lane_off + t * kTile;
     const uint32_t tO = tmem + lane_off + 256 + t * DIM;
     int s_seen = 0, o_seen = 0;  // completions of s_full[t] and o_full[t] waited so far
+    int pv_seen = 0;             // head dim 64: completions of pv_done[t] waited so far
+    constexpr bool kSep = DIM == 64;
+    const uint32_t tP = kSep ? tmem + lane_off + kColPR + kPRStride * t : tS;
     int kvc = 0;                 // global index of the current item's first key tile
     bool ok = true;
     for (int n = 0; ok; ++n) {
@@ -491,17 +586,37 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // the last key tile holds the diagonal (causal) or the document end
         const bool diag = (j == nt - 1);
         const int lim = diag ? min(prm.causal ? r : kTile - 1, e - 1 - k0) : kTile - 1;
-        // the whole 128-column row of S_t in registers: four loads, one wait
+        // the whole 128-column row of S_t in registers: four loads, one wait;
+        // unmasked tiles get each chunk's maximum with the load
         uint32_t sv[4][32];
+        float cmx[4];
+        if (diag) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, sv[c]);
+          for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, sv[c]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_ld32_max(tS + 32 * c, sv[c], cmx[c]);
+        }
         tmem_ld_wait();
+        if (kSep) {
+          // NVFP4: group 0 stages the block scales of the next key tile before
+          // the next S products may be issued (their buffer was last read by
+          // the score products of key tile j - 1, complete before S_0 of tile j)
+          if (NVF4 && t == 0 && j + 1 < it.nkv) {
+            write_sf4(prm.k4_scales, prm.Hkv, it.hk, k0 + kTile, kSfK4 + 4 * ((kv0 + j + 1) & 1));
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&sm.bar_k4));
+          }
+          // S_t is in registers: the next S_t may be computed
+          tc_fence_before();
+          mbar_arrive(smem_u32(&sm.bar_s_read[t]));
+        }
         // pass 1: row maximum in the log2 domain
         float mx = -INFINITY;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          const float cm =
-              diag ? chunk_max<true>(sv[c], lim - 32 * c) : chunk_max<false>(sv[c], 0);
+          const float cm = diag ? chunk_max<true>(sv[c], lim - 32 * c) : cmx[c];
           mx = fmaxf(mx, cm * cf[c]);
         }
         float m_new = (mx == -INFINITY) ? m : fmaxf(m, ceilf(mx));
@@ -510,6 +625,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (j > 0 && m_new > m) l8 *= pow2_or_zero(static_cast<int>(m - m_new));
         m = m_new;
         const float moff = m - 8.f;  // P8 = 2^8 exp2(s - m)
+        // head dim 64: P^_t's columns are free once the previous P^_t V has read them
+        if (kSep && j > 0) {
+          if (!mbar_wait(smem_u32(&sm.bar_pv_done[t]), pv_seen & 1) || sm.abort) {
+            ok = false;
+            break;
+          }
+          ++pv_seen;
+          tc_fence_after();
+        }
         // pass 2: probabilities, row sum, E4M3 operand
         float2 lsum = make_float2(0.f, 0.f);
 #pragma unroll
@@ -520,8 +644,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           else
             chunk_probs<false>(sv[c], cf[c], moff, 0, lsum, w);
           // the 32 codes of this chunk: row r of P^_t, keys 32 c .. 32 c + 31, into
-          // the consumed columns of S_t (the row was read into registers)
-          tmem_st8(tS + kColP + 8 * c, w);
+          // P^_t's columns (head dim 128: the consumed columns of S_t)
+          tmem_st8(tP + kColP + 8 * c, w);
         }
         l8 += lsum.x + lsum.y;
         // P^_t V_j enters O_t with the block scale 2^(m - m_ref) on P^'s row:
@@ -558,11 +682,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // (each lane quadrant holds its own rows), B = V's block bytes
         const uint32_t sa = static_cast<uint32_t>(127 + dm) * 0x01010101u;
         const uint32_t sfw[8] = {sa, sa, sa, sa, sfb, sfb, sfb, sfb};
-        tmem_st8(tS, sfw);
+        tmem_st8(tP, sfw);
         // NVFP4: group 0 stages the block scales of the next key tile (its
         // buffer was last read by the products of key tile j - 1, which
         // completed before S_0 of tile j)
-        if (NVF4 && t == 0 && j + 1 < it.nkv)
+        if (NVF4 && !kSep && t == 0 && j + 1 < it.nkv)
           write_sf4(prm.k4_scales, prm.Hkv, it.hk, k0 + kTile, kSfK4 + 4 * ((kv0 + j + 1) & 1));
         tmem_st_wait();
         tc_fence_before();
@@ -571,6 +695,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       if (nt > 0 && ok) {
         if (!mbar_wait(smem_u32(&sm.bar_o_full[t]), o_seen & 1) || sm.abort) ok = false;
         ++o_seen;
+        // head dim 64: the item's last P^_t V (complete with O_t) consumes its phase
+        if (kSep && ok) {
+          if (!mbar_wait(smem_u32(&sm.bar_pv_done[t]), pv_seen & 1)) ok = false;
+          ++pv_seen;
+        }
       }
       if (nt > 0 && ok) {
         tc_fence_after();

@@ -160,6 +160,39 @@ using namespace flamia;
 namespace flamia {
 namespace {
 
+// tcgen05.ld.red: 128 threads store rows of 32 floats to tensor memory and
+// read them back with the max-reducing load.
+__global__ void ldred_kernel(const float* in, float* vals, float* mx) {
+  __shared__ uint32_t base;
+  const int warp = threadIdx.x >> 5, r = threadIdx.x;
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&base), 32);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t t = base + (static_cast<uint32_t>(warp * 32) << 16);
+  uint32_t w[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(in[r * 32 + i]);
+  tmem_st32(t, w);
+  tmem_st_wait();
+  uint32_t v[32];
+  float m;
+  tmem_ld32_max(t, v, m);
+  tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < 32; ++i) vals[r * 32 + i] = __uint_as_float(v[i]);
+  mx[r] = m;
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(base, 32);
+  }
+}
+
 __global__ void bounded_waits_kernel(int* turn, int* status) {
   __shared__ alignas(8) uint64_t bar;
   if (threadIdx.x != 0) return;
@@ -220,6 +253,14 @@ extern "C" flamia_status flamia_debug_mma_tile(int mode, int N, int a_mn_major, 
                            static_cast<int>(smem)) != cudaSuccess)
     return FLAMIA_ERR_CUDA;
   probe_kernel<<<1, 128, smem, static_cast<cudaStream_t>(stream)>>>(ma, mb, g);
+  flamia::count_launches(1);
+  return cudaGetLastError() == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
+}
+
+extern "C" flamia_status flamia_debug_tmem_ldred(const float* in, float* vals, float* mx,
+                                                 void* stream) {
+  if (in == nullptr || vals == nullptr || mx == nullptr) return FLAMIA_ERR_INVALID_ARG;
+  flamia::ldred_kernel<<<1, 128, 0, static_cast<cudaStream_t>(stream)>>>(in, vals, mx);
   flamia::count_launches(1);
   return cudaGetLastError() == cudaSuccess ? FLAMIA_OK : FLAMIA_ERR_CUDA;
 }

@@ -62,6 +62,7 @@ SIGNATURES = {
     "flamia_debug_mma_tile": (_i, [_i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "flamia_debug_bounded_waits": (_i, [_vp, _vp, _vp]),
     "flamia_debug_launch_count": (ctypes.c_ulonglong, []),
+    "flamia_debug_tmem_ldred": (_i, [_vp, _vp, _vp, _vp]),
 }
 
 
@@ -204,6 +205,11 @@ def flamia_attn_bwd_gqa(q: QTensor, k: QTensor, v: QTensor, dout: QTensor, D, ls
                                       flags, _ptr(wl), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws),
                                       ws.numel() * ws.element_size(), _ptr(dev_status),
                                       _stream()), "flamia_attn_bwd_gqa")
+
+
+def flamia_debug_tmem_ldred(x, vals, mx):
+    _check(load().flamia_debug_tmem_ldred(_ptr(x), _ptr(vals), _ptr(mx), _stream()),
+           "flamia_debug_tmem_ldred")
 
 
 def flamia_debug_launch_count() -> int:

@@ -110,3 +110,24 @@ def test_row_scales_from_own_lane_quadrant(lib, mode, N):
     ref = _reference(mode, N, 0, 1, a, b, sfa, sfb)
     got = _run(fl, mode, N, 0, 1, 2 << 1, a, b, sfa, sfb)
     assert np.abs(got - ref).max() <= 1e-5 * np.abs(ref).max()
+
+
+def test_tmem_max_reducing_load(lib):
+    """tcgen05.ld.red (max) returns each thread's 32 loaded values unchanged
+    and their maximum: the forward takes its row maximum of unmasked score
+    tiles from it (review page, sec. 3.4 "Softmax throughput")."""
+    import torch
+    from precision_causal_attention_block_gb300 import flamia as fl
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((128, 32)).astype(np.float32) * 30.0
+    x[5] = -np.abs(x[5])           # an all-negative row
+    x[9, :] = -np.inf              # a fully masked row
+    x[9, 17] = -3.5
+    x[40, 3] = 1e30                # a huge value
+    xi = torch.from_numpy(x).cuda()
+    vals = torch.empty_like(xi)
+    mx = torch.empty(128, dtype=torch.float32, device="cuda")
+    fl.flamia_debug_tmem_ldred(xi, vals, mx)
+    torch.cuda.synchronize()
+    assert np.array_equal(vals.cpu().numpy(), x)
+    assert np.array_equal(mx.cpu().numpy(), x.max(axis=1))
