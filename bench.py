@@ -190,7 +190,8 @@ def run_ours(args, rank, world, local):
     call = fl.TrainingCall(w.T, w.H, w.d, cu, w.sm_scale, nvfp4_qk=args.nvfp4,
                            hadamard=args.hadamard, causal=not args.noncausal, H_kv=hkv,
                            deterministic_dq=args.deterministic, dq_accum=args.dq_accum,
-                           schedule=args.schedule, ds_rows=args.ds_rows, device=dev)
+                           schedule=args.schedule, ds_rows=args.ds_rows,
+                           token_scales=args.token_scales, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -222,7 +223,7 @@ def run_ours(args, rank, world, local):
             ev[i][0].record(stream)
             call.forward(xd["q"], xd["k"], xd["v"])
             flamia_quant_do = fl.flamia_quantize_tokenblock
-            flamia_quant_do(xd["do"], call.cu, call.dout, fl.FORMAT_MXFP8, o=call.o, D=call.D,
+            flamia_quant_do(xd["do"], call.cu, call.dout, call.fmt_do, o=call.o, D=call.D,
                             dev_status=call.status)
             evb[i][0].record(stream)
             fl.flamia_attn_bwd_gqa(call.q, call.k, call.v, call.dout, call.D, call.lse, call.cu,
@@ -252,7 +253,8 @@ def run_ours(args, rank, world, local):
                                    nvfp4_qk=args.nvfp4, hadamard=args.hadamard,
                                    causal=not args.noncausal, H_kv=hkv,
                                    deterministic_dq=args.deterministic, dq_accum=args.dq_accum,
-                                   schedule=args.schedule, ds_rows=args.ds_rows, device=dev)]
+                                   schedule=args.schedule, ds_rows=args.ds_rows,
+                                   token_scales=args.token_scales, device=dev)]
     xin = [xd, {n: torch.empty_like(t) for n, t in xd.items()}]
     outs = lambda c: (c.o, c.dq, c.dk, c.dv)
     hout = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs(c)] for c in calls]
@@ -359,7 +361,9 @@ def run_ours(args, rank, world, local):
                    "dq_sum": "ordered (deterministic)" if args.deterministic else "atomic",
                    "dq_accumulator": args.dq_accum,
                    "schedule": args.schedule,
-                   "ds_exponents": "query row" if args.ds_rows else "32x32 block",
+                   "ds_exponents": "query row" if (args.ds_rows or args.token_scales)
+                   else "32x32 block",
+                   "operand_scales": "per token" if args.token_scales else "32-token block",
                    "flops_per_step": flops, "l2": "flushed (256 MB write) before every step",
                    "parallelism": f"replicas x{world}"},
         "pct_of_fp8_peak": round(100.0 * value / world / pk["fp8_tflops"], 2),
@@ -373,7 +377,8 @@ def run_ours(args, rank, world, local):
                      "peak_source": pk["source"],
                      "traffic": None if (args.hadamard or args.noncausal or hkv != w.H or
                                          args.deterministic or args.dq_accum != "fp32" or
-                                         args.schedule != "dynamic" or args.ds_rows)
+                                         args.schedule != "dynamic" or args.ds_rows or
+                                         args.token_scales)
                      else profiled_traffic(w, args.nvfp4),
                      "traffic_unit": "bytes per launch of the attention kernel (ncu, DRAM read + write)"},
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
@@ -386,11 +391,36 @@ def run_ours(args, rank, world, local):
         "breakdown": breakdown,
         "clocks": res["clocks"],
     }
+    line["ds_rounded_to_zero"] = ds_zero_stats(w, xd, args, hkv, dev)
     if not args.no_stress:
         line["scheduling_stress"] = stress_stats(dev, stream, flush)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
     return line
+
+
+def ds_zero_stats(w, xd, args, hkv, dev):
+    """One untimed training call with the dS rounded-to-zero diagnostic: the
+    fraction of the nonzero dS entries (pairs the queries see) whose E4M3 code
+    under the 32x32 block exponent is zero (review page, sec. 3.3; the
+    pages' dS-scale ablation: 0.4% with their scale, 29% with an oversized
+    one)."""
+    import torch
+
+    from precision_causal_attention_block_gb300 import flamia as fl
+    if args.deterministic or args.dq_accum != "fp32":
+        return None
+    cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev)
+    call = fl.TrainingCall(w.T, w.H, w.d, cu, w.sm_scale, nvfp4_qk=args.nvfp4,
+                           hadamard=args.hadamard, causal=not args.noncausal, H_kv=hkv,
+                           schedule=args.schedule, ds_rows=args.ds_rows,
+                           token_scales=args.token_scales, ds_zero_count=True, device=dev)
+    call(xd["q"], xd["k"], xd["v"], xd["do"])
+    torch.cuda.synchronize(dev)
+    call.check_status()
+    nz, z = call.ds_zero_counts()
+    del call
+    return {"nonzero": nz, "zero": z, "fraction": z / nz if nz else 0.0}
 
 
 def stress_stats(dev, stream, flush, reps=5):
@@ -453,7 +483,8 @@ def profile_calls(args):
     call = fl.TrainingCall(w.T, w.H, w.d, cu, w.sm_scale, nvfp4_qk=args.nvfp4,
                            hadamard=args.hadamard, causal=not args.noncausal,
                            deterministic_dq=args.deterministic, dq_accum=args.dq_accum,
-                           schedule=args.schedule, ds_rows=args.ds_rows)
+                           schedule=args.schedule, ds_rows=args.ds_rows,
+                           token_scales=args.token_scales)
     for _ in range(args.warmup + args.steps):
         call(xd["q"], xd["k"], xd["v"], xd["do"])
     torch.cuda.synchronize()
@@ -463,7 +494,8 @@ def profile_calls(args):
 
 def stage_breakdown(call, xd, stream, flush, w, reps=10):
     """Device time of each stage of the call (median of reps, L2 flushed before
-    each), the quantiser's HBM throughput and the call's working memory."""
+    each), the quantiser's HBM throughput and the sum of the call's buffer sizes (the
+    measured peak memory is the scheduling-stress entry's)."""
     import torch
 
     from precision_causal_attention_block_gb300 import flamia as fl
@@ -481,7 +513,7 @@ def stage_breakdown(call, xd, stream, flush, w, reps=10):
                                                  call.H_kv, call.d, call.scale, call.wl, call.o,
                                                  call.lse, call.flags, dev_status=call.status),
         "quantize_do_ms": lambda: fl.flamia_quantize_tokenblock(
-            xd["do"], call.cu, call.dout, fl.FORMAT_MXFP8, o=call.o, D=call.D,
+            xd["do"], call.cu, call.dout, call.fmt_do, o=call.o, D=call.D,
             dev_status=call.status),
         "bwd_ms": lambda: fl.flamia_attn_bwd_gqa(call.q, call.k, call.v, call.dout, call.D,
                                                  call.lse, call.cu, call.T, call.H, call.H_kv,
@@ -514,7 +546,7 @@ def stage_breakdown(call, xd, stream, flush, w, reps=10):
             call.D, call.dq, call.dk, call.dv]
     bufs += [t for t in (call.q.nvfp4_codes, call.q.nvfp4_scales, call.k.nvfp4_codes,
                          call.k.nvfp4_scales) if t is not None]
-    out["call_memory_GB"] = round(sum(t.numel() * t.element_size() for t in bufs) / 1e9, 3)
+    out["call_buffers_GB"] = round(sum(t.numel() * t.element_size() for t in bufs) / 1e9, 3)
     return out
 
 
@@ -625,6 +657,9 @@ def main():
                          "longest document is at least 4x the average)")
     ap.add_argument("--ds-rows", action="store_true",
                     help="dQ's dS operand with one exponent per (query row, 32-key block)")
+    ap.add_argument("--token-scales", action="store_true",
+                    help="per-token operand scales (one exponent per token, folded into the "
+                         "opposite operand; with query-row dS exponents)")
     ap.add_argument("--deterministic", action="store_true",
                     help="dQ partials added in a fixed key-tile order (bitwise reproducible)")
     args = ap.parse_args()

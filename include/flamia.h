@@ -54,6 +54,9 @@ typedef enum {
 #define FLAMIA_DEV_BAD_SEQLENS 0x1  /* cu_seqlens not monotone or not ending at T */
 #define FLAMIA_DEV_CAPACITY    0x2  /* more work items than the buffer holds      */
 #define FLAMIA_DEV_TIMEOUT     0x4  /* a bounded wait gave up; outputs invalid    */
+#define FLAMIA_DEV_RANGE       0x8  /* a scale exponent left the E8M0 range a mode
+                                       supports (per-token operand scales with
+                                       |V| near 2^96 or beyond); outputs invalid */
 
 /* Quantiser output formats. */
 #define FLAMIA_FORMAT_MXFP8       0 /* E4M3 codes + per-token E8M0 scales          */
@@ -61,6 +64,11 @@ typedef enum {
 #define FLAMIA_FORMAT_HADAMARD 0x10 /* OR-ed into FLAMIA_FORMAT_MXFP8: rotate each
                                        (token, head) row by H_d before the block
                                        statistics (for Q and K; see below)       */
+#define FLAMIA_FORMAT_TOKEN_SCALES 0x20 /* OR-ed into FLAMIA_FORMAT_MXFP8 (with or
+                                       without FLAMIA_FORMAT_HADAMARD): one
+                                       exponent per (token, head) instead of per
+                                       32-token block (per-token operand scales,
+                                       see FLAMIA_FLAG_TOKEN_SCALES)             */
 
 /* Attention flags. */
 #define FLAMIA_FLAG_NVFP4_QK 0x1    /* score product QK^T (fwd and bwd recompute)
@@ -88,6 +96,24 @@ typedef enum {
                                        operand rounded with one exponent per
                                        (query row, 32-key block) instead of per
                                        32 x 32 block (dK keeps the block ones) */
+#define FLAMIA_FLAG_TOKEN_SCALES 0x200 /* forward / backward: q, k, v and dout were
+                                       quantised with FLAMIA_FORMAT_TOKEN_SCALES
+                                       (one exponent per token); the per-token
+                                       factors along each contraction are folded
+                                       into the opposite operand before its E4M3
+                                       rounding (see the forward and backward);
+                                       the backward implies
+                                       FLAMIA_FLAG_DS_ROW_EXPONENTS.  Not with
+                                       FLAMIA_FLAG_NVFP4_QK                      */
+#define FLAMIA_FLAG_DS_ZERO_COUNT 0x400 /* backward only: count, over every pair
+                                       a query sees, the dS entries that are
+                                       nonzero and, of those, the ones whose
+                                       E4M3 code under the 32 x 32 block exponent
+                                       is zero (rounded to zero), into two uint64
+                                       at flamia_bwd_ds_counts_offset of the
+                                       workspace (cleared by the call); not with
+                                       FLAMIA_FLAG_DETERMINISTIC_DQ or
+                                       FLAMIA_FLAG_DQ_FP16                       */
 #define FLAMIA_FLAG_SCHEDULE_RULE 0x80 /* forward / backward: the pages' rule,
                                        dynamic claims for causal calls and, for
                                        non-causal ones, only when the longest
@@ -283,10 +309,21 @@ size_t flamia_fwd_workspace_bytes(int T, int H, int d);
  * [T, H, d] dQ accumulator (FLAMIA_FLAG_DQ_FP16 uses its first half as an
  * FP16 [T, H, d] one), an int32 [T, H] array of turn counters
  * (FLAMIA_FLAG_DETERMINISTIC_DQ), the int8 [H, T] prescale exponents of the
- * FP16 accumulator, and 3 H ints of scratch.  The caller allocates it; the
+ * FP16 accumulator, 3 H ints of scratch and the two dS counters
+ * (FLAMIA_FLAG_DS_ZERO_COUNT).  The caller allocates it; the
  * backward clears what it uses itself.
  */
 size_t flamia_bwd_workspace_bytes(int T, int H, int d);
+
+/*
+ * Byte offset, inside the backward workspace, of the two uint64 counters that
+ * FLAMIA_FLAG_DS_ZERO_COUNT fills: [0] nonzero dS entries among the pairs the
+ * queries see, [1] those of them whose E4M3 code in the 32 x 32 block payload
+ * is zero.  The review page (sec. 3.3, and the dS-scale ablation of sec. 4)
+ * takes this fraction as the sign of a badly set dS scale.  Read it after the
+ * backward has completed.  0 for unsupported sizes.
+ */
+size_t flamia_bwd_ds_counts_offset(int T, int H, int d);
 
 /*
  * Causal backward.  Source: review page sec. 1.2 (recompute P; dV = P^T dO,

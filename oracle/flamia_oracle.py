@@ -462,19 +462,55 @@ def _query_block_max(e, rows):
     return out
 
 
-def _block_quantize_dS(dS: np.ndarray, r0: int, c0: int) -> np.ndarray:
+def _block_quantize_dS(dS: np.ndarray, r0: int, c0: int, extra: int = 0) -> np.ndarray:
     """dS rounded through E4M3 with one round-up exponent per 32x32 block whose
     origin is aligned to the document start (r0, c0 are doc-local offsets of
-    the rectangle and must be multiples of 32)."""
+    the rectangle and must be multiples of 32).  extra > 0 enlarges every
+    block exponent by that much (the oversized scale of the pages' dS-scale
+    ablation; never used by the method)."""
     assert r0 % 32 == 0 and c0 % 32 == 0
     out = np.empty_like(dS)
     R, C = dS.shape
     for i0 in range(0, R, 32):
         for j0 in range(0, C, 32):
             blk = dS[i0:i0 + 32, j0:j0 + 32]
-            e = int(roundup_exponent(np.abs(blk).max()))
+            e = int(roundup_exponent(np.abs(blk).max())) + extra
             out[i0:i0 + 32, j0:j0 + 32] = e4m3_decode(e4m3_encode(blk * 2.0 ** -e)) * 2.0 ** e
     return out
+
+
+def ds_zero_counts(qz: "Quantized", sm_scale: float, extra: int = 0, heads=None,
+                   causal: bool = True):
+    """Review page, sec. 3.3 and the dS-scale ablation of sec. 4: over every
+    pair a query sees, the number of dS entries that are nonzero, and of those
+    the number whose E4M3 code under the 32x32 block exponent is zero (rounded
+    to zero).  extra: an oversized block exponent (see _block_quantize_dS).
+    With per-token operand scales the block payload is dK's folded operand.
+    Returns (nonzero, zero)."""
+    T, H, _ = qz.qc.shape
+    nz = zero = 0
+    for b in range(len(qz.cu) - 1):
+        s, e = qz.cu[b], qz.cu[b + 1]
+        if e == s:
+            continue
+        for h in (range(H) if heads is None else heads):
+            dh = qz.dochead(b, h)
+            dh.causal = causal
+            rows = np.arange(e - s)
+            o, lse2, _, _ = fwd_rows(dh, rows, sm_scale, True)
+            dohat = dh.do * np.ldexp(1.0, dh.edo)[:, None]
+            D = (dohat * bf16_round(o)).sum(axis=1)
+            _, _, _, dS = bwd_rect(dh, rows, rows, lse2, D, sm_scale, True)
+            if dh.token:  # the block payload is dK's operand, dS 2^(eQ - EQ)
+                dSh = _block_quantize_dS(
+                    np.ldexp(dS, (dh.eq[rows] - _query_block_max(dh.eq, rows))[:, None]), 0, 0,
+                    extra)
+            else:
+                dSh = _block_quantize_dS(dS, 0, 0, extra)
+            live = dS != 0
+            nz += int(live.sum())
+            zero += int((live & (dSh == 0)).sum())
+    return nz, zero
 
 
 def _row_quantize_dS(dS: np.ndarray, c0: int) -> np.ndarray:

@@ -74,6 +74,10 @@ struct BwdSmem {
   // FP16 dQ: prescale 2^p of each query (0 outside); three buffers, since a
   // tile's dQ is staged while the next tile is computed
   alignas(16) float pf[3][kTile];
+  // per-token operand scales, per query and tile parity: 2^eQ, 2^eD (dO),
+  // 2^(eD - EdO) (dV's fold), 2^(eQ - EQ) (dK's fold); EQ, EdO the query
+  // block's largest exponents
+  alignas(16) float tq[OPT && !NVF4 ? 4 : 1][2][OPT && !NVF4 ? kTile : 4];
   uint32_t qbyte[2][4], dobyte[2][4];  // E8M0 bytes of the 4 query blocks of Q and dO
   uint32_t eds[4][4];            // dS block bytes [query block][key block]
   uint8_t erow[4][4][32];        // query-row dS bytes [query block][key block][query]
@@ -84,6 +88,7 @@ struct BwdSmem {
   uint64_t bar_kv_free, bar_acc_full, bar_acc_empty;
   ItemRing<4> ring;  // claimed items: producer -> MMA issuer, compute leader
   int item_bc[2];    // the compute leader's copy for the compute groups
+  unsigned long long dscnt[2];  // dS rounded-to-zero diagnostic of this CTA
   uint32_t tmem_base;
   volatile int abort;
 };
@@ -153,6 +158,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(smem_u32(&sm.bar_sf), kTile);
     ring_init(sm.ring, 2);
     sm.abort = 0;
+    sm.dscnt[0] = sm.dscnt[1] = 0ull;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -514,7 +520,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         r_lse = prm.lse[at];
         r_dd = prm.D[at];
         if (OPT && prm.dq_pre != nullptr) r_pre = prm.dq_pre[at];
-        if (lane == 0) {
+        if (lane == 0 || (OPT && !NVF4 && prm.token)) {
           r_qb = prm.q_scales[at];
           r_dob = prm.do_scales[at];
         }
@@ -524,6 +530,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         sm.nl[b][j] = r_qv ? 8.f - r_lse * LOG2E : -INFINITY;
         sm.dd[b][j] = r_qv ? r_dd : 0.f;
         if (OPT) sm.pf[tg % 3][j] = r_qv ? exp2i(r_pre) : 0.f;
+        if constexpr (OPT && !NVF4) {
+          if (prm.token) {
+            // per-token operand scales: this query's factors and its block's
+            // largest exponents (the B scales of dK and dV)
+            const int eqb = r_qv ? static_cast<int>(r_qb) : 0;
+            const int edb = r_qv ? static_cast<int>(r_dob) : 0;
+            const int EQ = static_cast<int>(__reduce_max_sync(0xffffffffu, static_cast<unsigned>(eqb)));
+            const int ED = static_cast<int>(__reduce_max_sync(0xffffffffu, static_cast<unsigned>(edb)));
+            sm.tq[0][b][j] = r_qv ? pow2_or_zero(eqb - 127) : 0.f;
+            sm.tq[1][b][j] = r_qv ? pow2_or_zero(edb - 127) : 0.f;
+            sm.tq[2][b][j] = r_qv ? pow2_or_zero(edb - ED) : 0.f;
+            sm.tq[3][b][j] = r_qv ? pow2_or_zero(eqb - EQ) : 0.f;
+            if (lane == 0) {
+              sm.qbyte[b][quad] = static_cast<uint32_t>(EQ);
+              sm.dobyte[b][quad] = static_cast<uint32_t>(ED);
+            }
+            return;
+          }
+        }
         if (lane == 0) {
           sm.qbyte[b][quad] = r_qv ? r_qb : 127u;
           sm.dobyte[b][quad] = r_qv ? r_dob : 127u;
@@ -564,9 +589,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           uint32_t pw[8] = {0, 0, 0, 0, 0, 0, 0, 0};
           float amax = 0.f;
+          const bool tok = OPT && !NVF4 && prm.token;
+          // per-token operand scales: dK's operand is dS 2^(eQ - EQ) per query
+          const float* kq = sm.tq[OPT && !NVF4 ? 3 : 0][ub] + 32 * c;
           if (!key_valid) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) dv[i] = 0u;
+          } else if (tok) {
+            const float* q0p = sm.tq[0][ub] + 32 * c;
+            const float* d0p = sm.tq[OPT && !NVF4 ? 1 : 0][ub] + 32 * c;
+            const float* p0p = sm.tq[OPT && !NVF4 ? 2 : 0][ub] + 32 * c;
+            if (prm.causal && (G == 1 ? u : u % nt) == 0)
+              bwd_chunk_tok<true>(sv, dv, sm.nl[ub] + 32 * c, sm.dd[ub] + 32 * c, q0p, d0p, p0p,
+                                  rowf, rowg, 32 * c, j, pw);
+            else
+              bwd_chunk_tok<false>(sv, dv, sm.nl[ub] + 32 * c, sm.dd[ub] + 32 * c, q0p, d0p, p0p,
+                                   rowf, rowg, 32 * c, j, pw);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(__uint_as_float(dv[i]) * kq[i]));
           } else if (prm.causal && (G == 1 ? u : u % nt) == 0) {
             amax = bwd_chunk<true>(sv, dv, sm.nl[ub] + 32 * c, sm.dd[ub] + 32 * c, fS, fP,
                                    32 * c, j, pw);
@@ -583,12 +623,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           uint32_t dw[8];
 #pragma unroll
           for (int i = 0; i < 32; i += 4) {
-            const float2 a = __fmul2_rn(
-                make_float2(__uint_as_float(dv[i]), __uint_as_float(dv[i + 1])), inv2);
-            const float2 b = __fmul2_rn(
-                make_float2(__uint_as_float(dv[i + 2]), __uint_as_float(dv[i + 3])), inv2);
+            float2 a = make_float2(__uint_as_float(dv[i]), __uint_as_float(dv[i + 1]));
+            float2 b = make_float2(__uint_as_float(dv[i + 2]), __uint_as_float(dv[i + 3]));
+            if (tok) {
+              a = __fmul2_rn(a, make_float2(kq[i], kq[i + 1]));
+              b = __fmul2_rn(b, make_float2(kq[i + 2], kq[i + 3]));
+            }
+            a = __fmul2_rn(a, inv2);
+            b = __fmul2_rn(b, inv2);
             dw[i / 4] = cvt_e4m3x4(a.x, a.y, b.x, b.y);
           }
+          if (OPT && prm.ds_count != nullptr) count_ds_zero(dv, dw, sm.dscnt, lane);
           const int ch0 = (2 * c) ^ (j & 7), ch1 = (2 * c + 1) ^ (j & 7);
           *reinterpret_cast<uint4*>(pbrow + 16 * ch0) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
           *reinterpret_cast<uint4*>(pbrow + 16 * ch1) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
@@ -597,7 +642,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (lane == 0) sm.eds[c][quad] = static_cast<uint32_t>(eb + 127);
           if (OPT && prm.ds_rows) {
             // dQ's operand: per query column the maximum over this warp's 32
-            // keys (one key block); lane q keeps query q's and its exponent
+            // keys (one key block); lane q keeps query q's and its exponent.
+            // Per-token operand scales: the operand is dS 2^eK(j) (K's factor
+            // folded in, the key row's own)
+            if (tok) {
+              const float kf = pow2_or_zero(ekj);
+#pragma unroll
+              for (int q = 0; q < 32; ++q) dv[q] = __float_as_uint(__uint_as_float(dv[q]) * kf);
+            }
             uint32_t mine = 0u;
 #pragma unroll
             for (int q = 0; q < 32; ++q) {
@@ -665,7 +717,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               else
                 w[i] = sm.eds[i][0] | (sm.eds[i][1] << 8) | (sm.eds[i][2] << 16) |
                        (sm.eds[i][3] << 24);
-              w[4 + i] = kword;  // dQ: B = K, per key block
+              // dQ: B = K, per key block (2^0: per-token K factors are in dS)
+              w[4 + i] = (OPT && !NVF4 && prm.token) ? 0x7F7F7F7Fu : kword;
             }
             tmem_st8(tmem + lane_off + sfc + kSfDqA, w);
           }
@@ -777,6 +830,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   if (threadIdx.x == 0) {
     if (sm.abort) report(prm.status, FLAMIA_DEV_TIMEOUT);
+    if (OPT && prm.ds_count != nullptr) {
+      atomicAdd(prm.ds_count, sm.dscnt[0]);
+      atomicAdd(prm.ds_count + 1, sm.dscnt[1]);
+    }
     finish_claims(prm.wl_header + kHdrBwdNext, prm.wl_header + kHdrBwdExit);
   }
   if (warp == 1) {
@@ -965,7 +1022,7 @@ __global__ void dq_convert_kernel(const float4* __restrict__ acc, uint2* __restr
 // first half), int32 [T, H] turn counters, int8 [H, T] prescale table, the
 // per-row byte maxima (H + 2 H_kv <= 3 H ints); each part 256-byte aligned.
 struct BwdWorkspace {
-  size_t off_turns, off_pre, off_max, total;
+  size_t off_turns, off_pre, off_max, off_count, total;
 };
 inline BwdWorkspace bwd_workspace(int T, int H, int d) {
   const size_t th = static_cast<size_t>(T) * H;
@@ -973,7 +1030,8 @@ inline BwdWorkspace bwd_workspace(int T, int H, int d) {
   w.off_turns = align_up(th * d * sizeof(float), 256);
   w.off_pre = w.off_turns + align_up(th * sizeof(int), 256);
   w.off_max = w.off_pre + align_up(th, 256);
-  w.total = w.off_max + align_up(3ull * H * sizeof(int), 256);
+  w.off_count = w.off_max + align_up(3ull * H * sizeof(int), 256);
+  w.total = w.off_count + 256;
   return w;
 }
 
@@ -982,8 +1040,9 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
                          const flamia_qtensor* v, const flamia_qtensor* dout, const float* D,
                          const float* lse, const int32_t* cu, int ndocs, int T, int H,
                          int Hkv, float softmax_scale, bool had, bool causal, bool det, int dq16,
-                         int sched, bool ds_rows, void* wl, void* dq, void* dk, void* dv, void* ws,
-                         int* status, cudaStream_t stream) {
+                         int sched, bool ds_rows, bool tok, bool dscount, void* wl, void* dq,
+                         void* dk, void* dv, void* ws, int* status, cudaStream_t stream) {
+  ds_rows = ds_rows || tok;  // per-token operand scales take query-row dS exponents
   // (head dim 128 builds its own maps in launch_bwd128_pipelined)
   CUtensorMap mq{}, mk{}, mv{}, mdo{}, mdq{}, mq4{}, mk4{};
   const CUtensorMapSwizzle swz = swizzle_for_row_bytes(DIM);
@@ -1039,11 +1098,18 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
   // for an item claimed before it)
   prm.sched = det ? kSchedDynamic : sched;
   prm.ds_rows = ds_rows ? 1 : 0;
+  prm.token = tok ? 1 : 0;
+  prm.ds_count = dscount ? reinterpret_cast<unsigned long long*>(static_cast<char*>(ws) +
+                                                                 W.off_count)
+                         : nullptr;
   // the accumulator (float32 or FP16) and, in the deterministic mode, the
   // turn counters behind it
   if (cudaMemsetAsync(acc, 0, n * (dq16 ? 2 : 4), stream) != cudaSuccess ||
       (det && cudaMemsetAsync(wsb + W.off_turns, 0, static_cast<size_t>(T) * H * sizeof(int),
                               stream) != cudaSuccess))
+    return FLAMIA_ERR_CUDA;
+  if (dscount && cudaMemsetAsync(prm.ds_count, 0, 2 * sizeof(unsigned long long), stream) !=
+                     cudaSuccess)
     return FLAMIA_ERR_CUDA;
   if (dq16) {  // the prescale table
     const int cb = dq16_bound_log2(DIM);
@@ -1073,7 +1139,7 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
         cudaSuccess)
       return FLAMIA_ERR_CUDA;
   } else {
-    const bool opt = det || dq16 || ds_rows;
+    const bool opt = det || dq16 || ds_rows || dscount;
     const size_t smem =
         (opt ? sizeof(BwdSmem<DIM, NVF4, true>) : sizeof(BwdSmem<DIM, NVF4, false>)) + 1024;
     auto kernel = opt ? attn_bwd_kernel<DIM, NVF4, true> : attn_bwd_kernel<DIM, NVF4, false>;
@@ -1086,7 +1152,8 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
     count_launches(1);
   }
   if (launch_bwd_short(q, k, v, dout, D, lse, cu, ndocs, T, H, Hkv, DIM, softmax_scale, NVF4, had,
-                       causal, ds_rows, acc, pre, dk, dv, stream) != cudaSuccess)
+                       causal, ds_rows, tok, prm.ds_count, acc, pre, dk, dv, stream) !=
+      cudaSuccess)
     return FLAMIA_ERR_CUDA;
   if (had) {
     const size_t rows = static_cast<size_t>(T) * H;
@@ -1118,6 +1185,11 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
 
 using namespace flamia;
 
+extern "C" size_t flamia_bwd_ds_counts_offset(int T, int H, int d) {
+  if (T <= 0 || H <= 0 || !supported_dim(d)) return 0;
+  return bwd_workspace(T, H, d).off_count;
+}
+
 extern "C" size_t flamia_bwd_workspace_bytes(int T, int H, int d) {
   if (T <= 0 || H <= 0 || !supported_dim(d)) return 0;
   return bwd_workspace(T, H, d).total;
@@ -1136,9 +1208,15 @@ extern "C" flamia_status flamia_attn_bwd_gqa(const flamia_qtensor* q, const flam
   if ((flags & ~(FLAMIA_FLAG_NVFP4_QK | FLAMIA_FLAG_HADAMARD | FLAMIA_FLAG_NONCAUSAL |
                  FLAMIA_FLAG_DETERMINISTIC_DQ | FLAMIA_FLAG_DQ_FP16 |
                  FLAMIA_FLAG_DQ_CAUSAL_SCALE | FLAMIA_FLAG_SCHEDULE_STATIC |
-                 FLAMIA_FLAG_SCHEDULE_RULE | FLAMIA_FLAG_DS_ROW_EXPONENTS)) != 0)
+                 FLAMIA_FLAG_SCHEDULE_RULE | FLAMIA_FLAG_DS_ROW_EXPONENTS |
+                 FLAMIA_FLAG_TOKEN_SCALES | FLAMIA_FLAG_DS_ZERO_COUNT)) != 0)
     return FLAMIA_ERR_UNSUPPORTED;
   const bool ds_rows = (flags & FLAMIA_FLAG_DS_ROW_EXPONENTS) != 0;
+  const bool tok = (flags & FLAMIA_FLAG_TOKEN_SCALES) != 0;
+  const bool dscount = (flags & FLAMIA_FLAG_DS_ZERO_COUNT) != 0;
+  // the diagnostic count runs with the float32, unordered dQ sum
+  if (dscount && (flags & (FLAMIA_FLAG_DETERMINISTIC_DQ | FLAMIA_FLAG_DQ_FP16)))
+    return FLAMIA_ERR_UNSUPPORTED;
   const int sched = schedule_of(flags);
   if (sched < 0) return FLAMIA_ERR_UNSUPPORTED;
   if ((flags & FLAMIA_FLAG_DETERMINISTIC_DQ) && sched == kSchedStatic) return FLAMIA_ERR_UNSUPPORTED;
@@ -1150,7 +1228,7 @@ extern "C" flamia_status flamia_attn_bwd_gqa(const flamia_qtensor* q, const flam
                    : (flags & FLAMIA_FLAG_DQ_CAUSAL_SCALE) ? 2 : 1;
   const bool had = (flags & FLAMIA_FLAG_HADAMARD) != 0;
   const bool causal = (flags & FLAMIA_FLAG_NONCAUSAL) == 0;
-  if ((nvf4 && d != 64) || (nvf4 && had)) return FLAMIA_ERR_UNSUPPORTED;
+  if ((nvf4 && d != 64) || (nvf4 && had) || (nvf4 && tok)) return FLAMIA_ERR_UNSUPPORTED;
   if (!valid_sizes(T, H, d, ndocs) || !q || !k || !v || !dout || !D || !lse || !cu_seqlens ||
       !wl || !dq_bf16 || !dk_bf16 || !dv_bf16 || !ws || !(softmax_scale > 0.f))
     return FLAMIA_ERR_INVALID_ARG;
@@ -1171,14 +1249,14 @@ extern "C" flamia_status flamia_attn_bwd_gqa(const flamia_qtensor* q, const flam
   const float sc = had ? softmax_scale / static_cast<float>(d) : softmax_scale;
   if (nvf4)
     return launch_bwd<64, true>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, H_kv, sc,
-                                false, causal, det, dq16, sched, ds_rows, wl, dq_bf16, dk_bf16, dv_bf16, ws,
-                                dev_status, s);
+                                false, causal, det, dq16, sched, ds_rows, false, dscount, wl, dq_bf16,
+                                dk_bf16, dv_bf16, ws, dev_status, s);
   return d == 128 ? launch_bwd<128, false>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, H_kv,
-                                           sc, had, causal, det, dq16, sched, ds_rows, wl, dq_bf16, dk_bf16,
-                                           dv_bf16, ws, dev_status, s)
+                                           sc, had, causal, det, dq16, sched, ds_rows, tok, dscount, wl,
+                                           dq_bf16, dk_bf16, dv_bf16, ws, dev_status, s)
                   : launch_bwd<64, false>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, H_kv,
-                                          sc, had, causal, det, dq16, sched, ds_rows, wl, dq_bf16, dk_bf16,
-                                          dv_bf16, ws, dev_status, s);
+                                          sc, had, causal, det, dq16, sched, ds_rows, tok, dscount, wl,
+                                          dq_bf16, dk_bf16, dv_bf16, ws, dev_status, s);
 }
 
 extern "C" flamia_status flamia_attn_bwd(const flamia_qtensor* q, const flamia_qtensor* k,

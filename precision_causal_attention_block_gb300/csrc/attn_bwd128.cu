@@ -42,6 +42,7 @@ constexpr uint32_t kSfDvA = 0, kSfDvB = 4, kSfDkA = 8, kSfDkB = 12, kSfDqA = 16,
 __device__ __forceinline__ uint32_t col_s(int b) { return 64u * b; }
 __device__ __forceinline__ uint32_t col_p(int b) { return 128u + 64u * b; }
 
+template <bool TOKS>
 struct Bwd128Smem {
   alignas(1024) uint8_t k[kTile * kD];             // [key][dim], 128B-swizzled rows
   alignas(1024) uint8_t v[kTile * kD];
@@ -55,6 +56,9 @@ struct Bwd128Smem {
   alignas(16) float nl[2][2][kQT];                 // 8 - lse2 (-inf outside the document)
   alignas(16) float dd[2][2][kQT];                 // D (0 outside)
   alignas(16) float pf[2][2][kQT];                 // FP16 dQ: prescale 2^p (0 outside)
+  // per-token operand scales (query-row dS instances), per query of a group's
+  // tile: 2^eQ, 2^eD (dO), 2^(eD - EdO) (dV's fold), 2^(eQ - EQ) (dK's fold)
+  alignas(16) float tq[TOKS ? 4 : 1][2][2][TOKS ? kQT : 4];
   uint32_t qbyte[2][2][2], dobyte[2][2][2];        // [group][buffer][query block]
   uint32_t eds[2][2][4];                           // [group][query block][key block]
   uint8_t erow[2][2][4][32];  // query-row dS bytes [group][query block][key block][query]
@@ -66,6 +70,7 @@ struct Bwd128Smem {
   int item_bc[2][2];  // [group][item parity]: the leader's copy for its group
   int pend[2];        // deterministic dQ: per group, the turn (index into the counters)
                       // its last reduce-adds pass on once complete, or -1
+  unsigned long long dscnt[2];  // dS rounded-to-zero diagnostic of this CTA
   uint32_t tmem_base;
   volatile int abort;
 };
@@ -87,7 +92,10 @@ __device__ __forceinline__ int tile_q0(const BwdItem& it, int G, int nt, int v) 
 // F16: the prescaled FP16 dQ accumulator (prm.dq_pre), else float32.
 // ROWDS: dQ^T's dS operand rounded with one exponent per (query, 32-key block),
 // carried as the product's B scales (dK keeps the 32x32 block exponents).
-template <bool DET, bool F16, bool ROWDS>
+// RD: 0 the 32x32 block dS exponents; 1 query-row exponents for dQ^T's
+// operand (ROWDS); 2 per-token operand scales (TOK, with ROWDS).
+// CNT: the dS rounded-to-zero diagnostic (prm.ds_count).
+template <bool DET, bool F16, int RD, bool CNT>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd128_kernel(const __grid_constant__ CUtensorMap map_q,
                        const __grid_constant__ CUtensorMap map_k,
@@ -95,7 +103,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap map_do,
                        const __grid_constant__ CUtensorMap map_dq, const BwdParams prm) {
   extern __shared__ uint8_t smem_raw[];
-  Bwd128Smem& sm = *reinterpret_cast<Bwd128Smem*>(
+  constexpr bool ROWDS = RD >= 1, TOK = RD == 2;
+  Bwd128Smem<TOK>& sm = *reinterpret_cast<Bwd128Smem<TOK>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
   const int T = prm.T;
@@ -125,6 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&sm.bar_done), 1);
     ring_init(sm.ring, 3);
     sm.abort = 0;
+    sm.dscnt[0] = sm.dscnt[1] = 0ull;
     sm.pend[0] = sm.pend[1] = -1;
     fence_barrier_init();
   }
@@ -323,6 +333,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t r_qb = 127u, r_dob = 127u;
     int r_pre = 0;
     bool r_qv = false;
+    constexpr bool tok = TOK;  // per-token operand scales
+    uint32_t r_qt = 0u, r_dot = 0u;      // this query's own bytes (per-token scales)
     auto fetch_inputs = [&](size_t hT, int q0, int e) {
       if (quad < 2) {
         const int qi = q0 + j;
@@ -331,6 +343,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         r_lse = prm.lse[at];
         r_dd = prm.D[at];
         if (F16) r_pre = prm.dq_pre[at];
+        if (tok) {
+          r_qt = prm.q_scales[at];
+          r_dot = prm.do_scales[at];
+        }
       } else if (lane == 0) {
         const int qi = q0 + 32 * (quad - 2);
         r_qv = qi < e;
@@ -344,7 +360,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         sm.nl[g][buf][j] = r_qv ? 8.f - r_lse * LOG2E : -INFINITY;
         sm.dd[g][buf][j] = r_qv ? r_dd : 0.f;
         if (F16) sm.pf[g][buf][j] = r_qv ? exp2i(r_pre) : 0.f;
-      } else if (lane == 0) {
+        if constexpr (TOK) {
+          {
+            // this query's factors; its block's (this warp's 32 queries) largest
+            // exponents are the B scales of dK and dV
+            const int eqb = r_qv ? static_cast<int>(r_qt) : 0;
+            const int edb = r_qv ? static_cast<int>(r_dot) : 0;
+            const int EQ = static_cast<int>(__reduce_max_sync(0xffffffffu, static_cast<unsigned>(eqb)));
+            const int ED = static_cast<int>(__reduce_max_sync(0xffffffffu, static_cast<unsigned>(edb)));
+            sm.tq[0][g][buf][j] = r_qv ? pow2_or_zero(eqb - 127) : 0.f;
+            sm.tq[1][g][buf][j] = r_qv ? pow2_or_zero(edb - 127) : 0.f;
+            sm.tq[2][g][buf][j] = r_qv ? pow2_or_zero(edb - ED) : 0.f;
+            sm.tq[3][g][buf][j] = r_qv ? pow2_or_zero(eqb - EQ) : 0.f;
+            if (lane == 0) {
+              sm.qbyte[g][buf][quad] = static_cast<uint32_t>(EQ);
+              sm.dobyte[g][buf][quad] = static_cast<uint32_t>(ED);
+            }
+          }
+        }
+      } else if (lane == 0 && !tok) {
         sm.qbyte[g][buf][quad - 2] = r_qv ? r_qb : 127u;
         sm.dobyte[g][buf][quad - 2] = r_qv ? r_dob : 127u;
       }
@@ -404,9 +438,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           float amax = 0.f;
           const float* nl = sm.nl[g][buf] + 32 * c;
           const float* dd = sm.dd[g][buf] + 32 * c;
+          // per-token operand scales: dK's operand is dS 2^(eQ - EQ) per query
+          const float* kq = sm.tq[TOK ? 3 : 0][g][buf] + 32 * c;
           if (!key_valid) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) dv[i] = 0u;
+          } else if (tok) {
+            const float* q0p = sm.tq[0][g][buf] + 32 * c;
+            const float* d0p = sm.tq[TOK ? 1 : 0][g][buf] + 32 * c;
+            const float* p0p = sm.tq[TOK ? 2 : 0][g][buf] + 32 * c;
+            if (prm.causal && tu < 2)
+              bwd_chunk_tok<true>(sv, dv, nl, dd, q0p, d0p, p0p, rowf, rowg, tu * kQT + 32 * c, j,
+                                  pw);
+            else
+              bwd_chunk_tok<false>(sv, dv, nl, dd, q0p, d0p, p0p, rowf, rowg, 0, j, pw);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(__uint_as_float(dv[i]) * kq[i]));
           } else if (prm.causal && tu < 2) {  // the tile crosses the diagonal
             amax = bwd_chunk<true>(sv, dv, nl, dd, fS, fP, tu * kQT + 32 * c, j, pw);
           } else {
@@ -421,12 +468,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t dw[8];
 #pragma unroll
           for (int i = 0; i < 32; i += 4) {
-            const float2 a = __fmul2_rn(
-                make_float2(__uint_as_float(dv[i]), __uint_as_float(dv[i + 1])), inv2);
-            const float2 bq = __fmul2_rn(
-                make_float2(__uint_as_float(dv[i + 2]), __uint_as_float(dv[i + 3])), inv2);
+            float2 a = make_float2(__uint_as_float(dv[i]), __uint_as_float(dv[i + 1]));
+            float2 bq = make_float2(__uint_as_float(dv[i + 2]), __uint_as_float(dv[i + 3]));
+            if (tok) {
+              a = __fmul2_rn(a, make_float2(kq[i], kq[i + 1]));
+              bq = __fmul2_rn(bq, make_float2(kq[i + 2], kq[i + 3]));
+            }
+            a = __fmul2_rn(a, inv2);
+            bq = __fmul2_rn(bq, inv2);
             dw[i / 4] = cvt_e4m3x4(a.x, a.y, bq.x, bq.y);
           }
+          if (CNT) count_ds_zero(dv, dw, sm.dscnt, lane);
           const int ch0 = (2 * c) ^ sw, ch1 = (2 * c + 1) ^ sw;
           *reinterpret_cast<uint4*>(pbrow + 16 * ch0) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
           *reinterpret_cast<uint4*>(pbrow + 16 * ch1) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
@@ -435,7 +487,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) sm.eds[g][c][quad] = static_cast<uint32_t>(eb + 127);
           if (ROWDS) {
             // dQ's operand: per query column the maximum over this warp's 32
-            // keys (one key block); lane q keeps query q's and its exponent
+            // keys (one key block); lane q keeps query q's and its exponent.
+            // Per-token operand scales: the operand is dS 2^eK(j) (K's factor
+            // folded in, the key row's own)
+            if (tok) {
+              const float kf = pow2_or_zero(ekj);
+#pragma unroll
+              for (int q = 0; q < 32; ++q) dv[q] = __float_as_uint(__uint_as_float(dv[q]) * kf);
+            }
             uint32_t mine = 0u;
 #pragma unroll
             for (int q = 0; q < 32; ++q) {
@@ -495,7 +554,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_st8(tmem + lane_off + col_p(g) + kSfDkA, w);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) w[i] = kword;  // dQ^T: A = K^T, per key block
+          // dQ^T: A = K^T, per key block (2^0: per-token K factors are in dS)
+          for (int i = 0; i < 4; ++i) w[i] = tok ? 0x7F7F7F7Fu : kword;
 #pragma unroll
           for (int i = 0; i < 2; ++i) {  // dQ^T: B = dS^T, row block = query block i
             if (ROWDS)  // this lane's query 32 i + lane: one byte per key block
@@ -665,6 +725,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (threadIdx.x == 0) {
     if (sm.abort) report(prm.status, FLAMIA_DEV_TIMEOUT);
+    if (CNT && prm.ds_count != nullptr) {
+      atomicAdd(prm.ds_count, sm.dscnt[0]);
+      atomicAdd(prm.ds_count + 1, sm.dscnt[1]);
+    }
     finish_claims(prm.wl_header + kHdrBwdNext, prm.wl_header + kHdrBwdExit);
   }
   if (warp == 1) {
@@ -690,15 +754,24 @@ cudaError_t launch_bwd128_pipelined(const BwdParams& prm, const flamia_qtensor* 
   if (f16 ? !make_f16_token_map(&mdq, acc, T, H, kD, kQT, CU_TENSOR_MAP_SWIZZLE_NONE)
           : !make_f32_token_map(&mdq, acc, T, H, kD, kQT, CU_TENSOR_MAP_SWIZZLE_NONE))
     return cudaErrorInvalidValue;
-  const size_t smem = sizeof(Bwd128Smem) + 1024;
+  const int rd = prm.token ? 2 : prm.ds_rows ? 1 : 0;
+  const bool cnt = prm.ds_count != nullptr;
+  const size_t smem = (rd == 2 ? sizeof(Bwd128Smem<true>) : sizeof(Bwd128Smem<false>)) + 1024;
   using Kernel = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap,
                          const BwdParams);
-  static const Kernel kernels[8] = {
-      attn_bwd128_kernel<false, false, false>, attn_bwd128_kernel<true, false, false>,
-      attn_bwd128_kernel<false, true, false>,  attn_bwd128_kernel<true, true, false>,
-      attn_bwd128_kernel<false, false, true>,  attn_bwd128_kernel<true, false, true>,
-      attn_bwd128_kernel<false, true, true>,   attn_bwd128_kernel<true, true, true>};
-  const Kernel kernel = kernels[(det ? 1 : 0) | (f16 ? 2 : 0) | (prm.ds_rows ? 4 : 0)];
+  // [rd][f16][det]; the diagnostic count only with the float32, unordered dQ sum
+  static const Kernel kernels[3][2][2] = {
+      {{attn_bwd128_kernel<false, false, 0, false>, attn_bwd128_kernel<true, false, 0, false>},
+       {attn_bwd128_kernel<false, true, 0, false>, attn_bwd128_kernel<true, true, 0, false>}},
+      {{attn_bwd128_kernel<false, false, 1, false>, attn_bwd128_kernel<true, false, 1, false>},
+       {attn_bwd128_kernel<false, true, 1, false>, attn_bwd128_kernel<true, true, 1, false>}},
+      {{attn_bwd128_kernel<false, false, 2, false>, attn_bwd128_kernel<true, false, 2, false>},
+       {attn_bwd128_kernel<false, true, 2, false>, attn_bwd128_kernel<true, true, 2, false>}}};
+  static const Kernel counting[3] = {attn_bwd128_kernel<false, false, 0, true>,
+                                     attn_bwd128_kernel<false, false, 1, true>,
+                                     attn_bwd128_kernel<false, false, 2, true>};
+  if (cnt && (det || f16)) return cudaErrorInvalidValue;
+  const Kernel kernel = cnt ? counting[rd] : kernels[rd][f16 ? 1 : 0][det ? 1 : 0];
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;

@@ -49,7 +49,7 @@ constexpr int kRefSpan = 32;
 // head dim 64: first column of the P^_t region (scale factors, then codes)
 constexpr uint32_t kColPR = 400, kPRStride = 40;
 
-template <int DIM, bool NVF4>
+template <int DIM, bool NVF4, bool TOK>
 struct FwdSmem {
   static constexpr int kTileBytes = kTile * DIM;
   static constexpr int kTile4Bytes = NVF4 ? kTile * DIM / 2 : 16;  // packed E2M1 tile
@@ -71,6 +71,12 @@ struct FwdSmem {
   uint64_t bar_k4;          // head dim 64, NVFP4: the next key tile's block scales written
   uint64_t bar_done;
   ItemRing<4> ring;  // claimed items, producer -> MMA issuer and softmax warps
+  // per-token operand scales: per query tile and step parity, the key factors
+  // 2^eK(j), V's folded factors 2^(eV(j) - EV(block)) and the block maxima
+  // EV as E8M0 bytes
+  alignas(16) float kf[TOK ? 2 : 1][2][TOK ? kTile : 4];
+  alignas(16) float vf[TOK ? 2 : 1][2][TOK ? kTile : 4];
+  int evb[2][2][4];
   uint32_t tmem_base;
   volatile int abort;
 };
@@ -149,6 +155,44 @@ __device__ __forceinline__ void chunk_probs(const uint32_t (&v)[32], float cf, f
   }
 }
 
+// Per-token operand scales: P8 = 2^8 exp2(x cf - m) as in chunk_probs, with
+// v = S 2^eK(j) already carrying the key factors, and the E4M3 operand
+// P8 2^(eV(j) - EV) (vf, the chunk's folded V factors, times gmul for the
+// diagonal block of a causal row, whose EV is the maximum over the keys the
+// row sees).
+template <bool MASK>
+__device__ __forceinline__ void chunk_probs_tok(const uint32_t (&v)[32], float cf, float moff,
+                                                int lim, float2& lsum, uint32_t (&w)[8],
+                                                const float* vf, float gmul) {
+  const float2 cf2 = make_float2(cf, cf), mo2 = make_float2(-moff, -moff);
+  const float2 g2 = make_float2(gmul, gmul);
+#pragma unroll
+  for (int i = 0; i < 32; i += 4) {
+    float2 a = make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+    float2 b = make_float2(__uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+    a = __ffma2_rn(a, cf2, mo2);
+    b = __ffma2_rn(b, cf2, mo2);
+    if (MASK) {
+      if (i + 0 > lim) a.x = -INFINITY;
+      if (i + 1 > lim) a.y = -INFINITY;
+      if (i + 2 > lim) b.x = -INFINITY;
+      if (i + 3 > lim) b.y = -INFINITY;
+    }
+    const float2 pa = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+    const float2 pb = make_float2(ex2_approx(b.x), ex2_approx(b.y));
+    lsum = __fadd2_rn(lsum, pa);
+    lsum = __fadd2_rn(lsum, pb);
+    const float4 f = *reinterpret_cast<const float4*>(vf + i);
+    float2 fa = make_float2(f.x, f.y), fb = make_float2(f.z, f.w);
+    if (MASK) {
+      fa = __fmul2_rn(fa, g2);
+      fb = __fmul2_rn(fb, g2);
+    }
+    const float2 qa = __fmul2_rn(pa, fa), qb = __fmul2_rn(pb, fb);
+    w[i / 4] = cvt_e4m3x4(qa.x, qa.y, qb.x, qb.y);
+  }
+}
+
 // NVFP4 score product (d = 64): tensor-memory columns of the block scales of
 // Q_0, Q_1 (4 columns each) and of K_j (two 4-column buffers, by j parity).
 constexpr uint32_t kSfQ4 = 384, kSfK4 = 392;
@@ -188,7 +232,7 @@ __device__ __forceinline__ bool decode_fwd_item(const FwdParams& prm, int n_item
 // Consumers of the item ring: the MMA issuer and the 8 softmax warps.
 constexpr int kFwdRingConsumers = 1 + 8;
 
-template <int DIM, bool NVF4>
+template <int DIM, bool NVF4, bool TOK>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap map_q,
                     const __grid_constant__ CUtensorMap map_k,
@@ -197,7 +241,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                     const __grid_constant__ CUtensorMap map_k4, const FwdParams prm) {
   static_assert(!NVF4 || DIM == 64, "the NVFP4 score product is built for head dim 64");
   extern __shared__ uint8_t smem_raw[];
-  FwdSmem<DIM, NVF4>& sm = *reinterpret_cast<FwdSmem<DIM, NVF4>*>(
+  FwdSmem<DIM, NVF4, TOK>& sm = *reinterpret_cast<FwdSmem<DIM, NVF4, TOK>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
   const int H = prm.H, T = prm.T;
@@ -239,8 +283,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-  constexpr uint32_t kTileBytes = FwdSmem<DIM, NVF4>::kTileBytes;
-  constexpr uint32_t kQBytes = kTileBytes + (NVF4 ? FwdSmem<DIM, NVF4>::kTile4Bytes : 0);
+  constexpr uint32_t kTileBytes = FwdSmem<DIM, NVF4, TOK>::kTileBytes;
+  constexpr uint32_t kQBytes = kTileBytes + (NVF4 ? FwdSmem<DIM, NVF4, TOK>::kTile4Bytes : 0);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -564,8 +608,37 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         sbyte = in ? (lane < 4 ? prm.k_scales : prm.v_scales)[hkT + kk] : 127u;
       };
       fetch_scales(0);
+      // per-token operand scales: this thread's key r of key tile jj (its K and
+      // V exponent bytes, 0 outside the document), fetched a step ahead
+      int r_ek = 0, r_ev = 0;
+      auto fetch_token_bytes = [&](int jj) {
+        const int kk = s + jj * kTile + r;
+        const bool in = jj < nt && kk < e;
+        r_ek = in ? static_cast<int>(prm.k_scales[hkT + kk]) : 0;
+        r_ev = in ? static_cast<int>(prm.v_scales[hkT + kk]) : 0;
+      };
+      if (TOK) fetch_token_bytes(0);
       for (int j = 0; j < nt; ++j) {
         const int k0 = s + j * kTile;
+        // per-token operand scales: this step's key tables (buffer j & 1, last
+        // read in step j - 2, before the group's barrier of step j - 1)
+        int pm = 0, own_max = 0;  // the row's diagonal-block maxima (bytes)
+        if constexpr (TOK) {
+          const int kk = k0 + r;
+          const bool kin = kk < e;
+          own_max = __reduce_max_sync(0xffffffffu, r_ev);  // this warp's key block
+          pm = r_ev;  // inclusive prefix maximum over lanes 0 .. lane
+#pragma unroll
+          for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, pm, off);
+            if (lane >= off) pm = max(pm, y);
+          }
+          sm.kf[j & 1][t][r] = kin ? pow2_or_zero(r_ek - 127) : 0.f;
+          sm.vf[j & 1][t][r] = kin ? pow2_or_zero(r_ev - own_max) : 0.f;
+          if (lane == 0) sm.evb[j & 1][t][quad] = own_max;
+          fetch_token_bytes(j + 1);
+          named_barrier_sync(1 + t, kTile);
+        }
         // lanes 0..3 gather the K word, lanes 4..7 the V word (byte kb = block kb)
         uint32_t sw = sbyte << (8 * (lane & 3));
         sw |= __shfl_xor_sync(0xffffffffu, sw, 1);
@@ -590,7 +663,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // unmasked tiles get each chunk's maximum with the load
         uint32_t sv[4][32];
         float cmx[4];
-        if (diag) {
+        if (diag || TOK) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, sv[c]);
         } else {
@@ -614,10 +687,34 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         // pass 1: row maximum in the log2 domain
         float mx = -INFINITY;
+        if constexpr (TOK) {
+          // the key factors 2^eK(j) per column, then one row factor
+          const float* kfp = sm.kf[j & 1][t];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const float cm = diag ? chunk_max<true>(sv[c], lim - 32 * c) : cmx[c];
-          mx = fmaxf(mx, cm * cf[c]);
+          for (int c = 0; c < 4; ++c) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              const float4 f = *reinterpret_cast<const float4*>(kfp + 32 * c + i);
+              const float2 a = __fmul2_rn(
+                  make_float2(__uint_as_float(sv[c][i]), __uint_as_float(sv[c][i + 1])),
+                  make_float2(f.x, f.y));
+              const float2 b = __fmul2_rn(
+                  make_float2(__uint_as_float(sv[c][i + 2]), __uint_as_float(sv[c][i + 3])),
+                  make_float2(f.z, f.w));
+              sv[c][i] = __float_as_uint(a.x);
+              sv[c][i + 1] = __float_as_uint(a.y);
+              sv[c][i + 2] = __float_as_uint(b.x);
+              sv[c][i + 3] = __float_as_uint(b.y);
+            }
+            const float cm = diag ? chunk_max<true>(sv[c], lim - 32 * c) : chunk_max<false>(sv[c], 0);
+            mx = fmaxf(mx, cm * c_row);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const float cm = diag ? chunk_max<true>(sv[c], lim - 32 * c) : cmx[c];
+            mx = fmaxf(mx, cm * cf[c]);
+          }
         }
         float m_new = (mx == -INFINITY) ? m : fmaxf(m, ceilf(mx));
         if (m_new == -INFINITY) m_new = 0.f;
@@ -636,13 +733,25 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         // pass 2: probabilities, row sum, E4M3 operand
         float2 lsum = make_float2(0.f, 0.f);
+        // per-token operand scales, causal diagonal tile: the row's own key
+        // block takes EV = the maximum over the keys it sees
+        const bool tdiag = TOK && diag && prm.causal;
+        const float gown = tdiag ? pow2_or_zero(own_max - pm) : 1.f;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t w[8];
-          if (diag)
+          if constexpr (TOK) {
+            const float* vfp = sm.vf[j & 1][t] + 32 * c;
+            if (diag)
+              chunk_probs_tok<true>(sv[c], c_row, moff, lim - 32 * c, lsum, w, vfp,
+                                    (tdiag && c == quad) ? gown : 1.f);
+            else
+              chunk_probs_tok<false>(sv[c], c_row, moff, 0, lsum, w, vfp, 1.f);
+          } else if (diag) {
             chunk_probs<true>(sv[c], cf[c], moff, lim - 32 * c, lsum, w);
-          else
+          } else {
             chunk_probs<false>(sv[c], cf[c], moff, 0, lsum, w);
+          }
           // the 32 codes of this chunk: row r of P^_t, keys 32 c .. 32 c + 31, into
           // P^_t's columns (head dim 128: the consumed columns of S_t)
           tmem_st8(tP + kColP + 8 * c, w);
@@ -680,8 +789,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         // scale factors of P^_t V_j: A (P^, this row) 2^dm for every K block
         // (each lane quadrant holds its own rows), B = V's block bytes
-        const uint32_t sa = static_cast<uint32_t>(127 + dm) * 0x01010101u;
-        const uint32_t sfw[8] = {sa, sa, sa, sa, sfb, sfb, sfb, sfb};
+        uint32_t sa = static_cast<uint32_t>(127 + dm) * 0x01010101u, sb = sfb;
+        if constexpr (TOK) {
+          // A: 2^(dm + EV(block)) per key block (the V factors were folded into
+          // P^ relative to EV); B: 2^0
+          const int* evb = sm.evb[j & 1][t];
+          sa = 0;
+          bool bad = false;
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            const int byte = dm + ((tdiag && b == quad) ? pm : evb[b]);
+            bad |= byte > 254;
+            sa |= static_cast<uint32_t>(min(byte, 254)) << (8 * b);
+          }
+          if (bad) report(prm.status, FLAMIA_DEV_RANGE);
+          sb = 0x7F7F7F7Fu;
+        }
+        const uint32_t sfw[8] = {sa, sa, sa, sa, sb, sb, sb, sb};
         tmem_st8(tP, sfw);
         // NVFP4: group 0 stages the block scales of the next key tile (its
         // buffer was last read by the products of key tile j - 1, which
@@ -746,7 +870,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
-template <int DIM, bool NVF4>
+template <int DIM, bool NVF4, bool TOK>
 flamia_status launch_fwd(const flamia_qtensor* q, const flamia_qtensor* k,
                          const flamia_qtensor* v, const int32_t* cu, int ndocs, int T, int H,
                          int Hkv, float softmax_scale, bool causal, int sched, void* wl, void* o,
@@ -787,19 +911,19 @@ flamia_status launch_fwd(const flamia_qtensor* q, const flamia_qtensor* k,
   prm.causal = causal ? 1 : 0;
   prm.sched = sched;
   prm.status = status;
-  const size_t smem = sizeof(FwdSmem<DIM, NVF4>) + 1024;
-  if (cudaFuncSetAttribute(attn_fwd_kernel<DIM, NVF4>,
+  const size_t smem = sizeof(FwdSmem<DIM, NVF4, TOK>) + 1024;
+  if (cudaFuncSetAttribute(attn_fwd_kernel<DIM, NVF4, TOK>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return FLAMIA_ERR_CUDA;
   // persistent: one CTA per SM (shared memory allows one), items claimed in list order
   const long long grid = std::min<long long>(static_cast<long long>(L.cap_fwd) * H, num_sms());
-  attn_fwd_kernel<DIM, NVF4>
+  attn_fwd_kernel<DIM, NVF4, TOK>
       <<<static_cast<unsigned>(grid), kFwdThreads, smem, stream>>>(mq, mk, mv, mq4, mk4, prm);
   if (cudaGetLastError() != cudaSuccess) return FLAMIA_ERR_CUDA;
   count_launches(1);
-  return launch_fwd_short(q, k, v, cu, ndocs, T, H, Hkv, DIM, softmax_scale, NVF4, causal, o,
-                          lse, stream) ==
+  return launch_fwd_short(q, k, v, cu, ndocs, T, H, Hkv, DIM, softmax_scale, NVF4, causal, TOK,
+                          o, lse, stream) ==
                  cudaSuccess
              ? FLAMIA_OK
              : FLAMIA_ERR_CUDA;
@@ -823,11 +947,14 @@ extern "C" flamia_status flamia_attn_fwd_gqa(const flamia_qtensor* q, const flam
   if ((flags & ~(FLAMIA_FLAG_NVFP4_QK | FLAMIA_FLAG_HADAMARD | FLAMIA_FLAG_NONCAUSAL |
                  FLAMIA_FLAG_DETERMINISTIC_DQ | FLAMIA_FLAG_DQ_FP16 |
                  FLAMIA_FLAG_DQ_CAUSAL_SCALE | FLAMIA_FLAG_SCHEDULE_STATIC |
-                 FLAMIA_FLAG_SCHEDULE_RULE | FLAMIA_FLAG_DS_ROW_EXPONENTS)) != 0)
+                 FLAMIA_FLAG_SCHEDULE_RULE | FLAMIA_FLAG_DS_ROW_EXPONENTS |
+                 FLAMIA_FLAG_TOKEN_SCALES | FLAMIA_FLAG_DS_ZERO_COUNT)) != 0)
     return FLAMIA_ERR_UNSUPPORTED;
   const int sched = schedule_of(flags);
   if (sched < 0) return FLAMIA_ERR_UNSUPPORTED;
   const bool nvf4 = (flags & FLAMIA_FLAG_NVFP4_QK) != 0;
+  const bool tok = (flags & FLAMIA_FLAG_TOKEN_SCALES) != 0;
+  if (tok && nvf4) return FLAMIA_ERR_UNSUPPORTED;
   const bool causal = (flags & FLAMIA_FLAG_NONCAUSAL) == 0;
   if ((nvf4 && d != 64) || (nvf4 && (flags & FLAMIA_FLAG_HADAMARD))) return FLAMIA_ERR_UNSUPPORTED;
   // rotated Q, K (FLAMIA_FLAG_HADAMARD): the same scores with softmax_scale / d
@@ -848,12 +975,21 @@ extern "C" flamia_status flamia_attn_fwd_gqa(const flamia_qtensor* q, const flam
     return FLAMIA_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (nvf4)
-    return launch_fwd<64, true>(q, k, v, cu_seqlens, ndocs, T, H, H_kv, softmax_scale, causal,
-                                sched, wl, o_bf16, lse, dev_status, s);
-  return d == 128 ? launch_fwd<128, false>(q, k, v, cu_seqlens, ndocs, T, H, H_kv, softmax_scale,
-                                           causal, sched, wl, o_bf16, lse, dev_status, s)
-                  : launch_fwd<64, false>(q, k, v, cu_seqlens, ndocs, T, H, H_kv, softmax_scale,
-                                          causal, sched, wl, o_bf16, lse, dev_status, s);
+    return launch_fwd<64, true, false>(q, k, v, cu_seqlens, ndocs, T, H, H_kv, softmax_scale,
+                                       causal, sched, wl, o_bf16, lse, dev_status, s);
+  if (tok)
+    return d == 128 ? launch_fwd<128, false, true>(q, k, v, cu_seqlens, ndocs, T, H, H_kv,
+                                                   softmax_scale, causal, sched, wl, o_bf16, lse,
+                                                   dev_status, s)
+                    : launch_fwd<64, false, true>(q, k, v, cu_seqlens, ndocs, T, H, H_kv,
+                                                  softmax_scale, causal, sched, wl, o_bf16, lse,
+                                                  dev_status, s);
+  return d == 128 ? launch_fwd<128, false, false>(q, k, v, cu_seqlens, ndocs, T, H, H_kv,
+                                                  softmax_scale, causal, sched, wl, o_bf16, lse,
+                                                  dev_status, s)
+                  : launch_fwd<64, false, false>(q, k, v, cu_seqlens, ndocs, T, H, H_kv,
+                                                 softmax_scale, causal, sched, wl, o_bf16, lse,
+                                                 dev_status, s);
 }
 
 // The forward keeps its running statistics and probabilities on chip: no

@@ -43,6 +43,9 @@ struct ShortParams {
   int ds_rows;      // dQ from dS rounded with one exponent per query row
   int ppw;          // (document, head) pairs per warp: 32 when documents average <= 2
                     // tokens (almost every pair is skipped), else 1
+  int token;        // per-token operand scales: one exponent per token, the factors
+                    // along each contraction folded into the opposite operand
+  unsigned long long* ds_count;  // dS rounded-to-zero diagnostic [nonzero, zero], or null
 };
 
 // d/32 E4M3 codes of one row (this lane's slice) decoded to floats.
@@ -141,11 +144,18 @@ __device__ __forceinline__ void fwd_short_pair(const ShortParams& prm, int doc, 
   const size_t hkT = static_cast<size_t>(hk) * T;
   // one scale block per operand: the exponents of the document's first token
   // (on the mixed path the NVFP4 values carry their own scales)
-  const float cf = NVF4 ? prm.scale_log2
-                        : prm.scale_log2 * pow2_or_zero_s(static_cast<int>(prm.qs[hT + s]) - 127) *
-                              pow2_or_zero_s(static_cast<int>(prm.ks[hkT + s]) - 127);
-  const float vsc = pow2_or_zero_s(static_cast<int>(prm.vs[hkT + s]) - 127);
+  const float cf0 = NVF4 ? prm.scale_log2
+                         : prm.scale_log2 * pow2_or_zero_s(static_cast<int>(prm.qs[hT + s]) - 127) *
+                               pow2_or_zero_s(static_cast<int>(prm.ks[hkT + s]) - 127);
+  const float vsc0 = pow2_or_zero_s(static_cast<int>(prm.vs[hkT + s]) - 127);
+  // per-token operand scales: lane j holds key j's K and V exponents
+  const int ekj = prm.token && lane < L ? static_cast<int>(prm.ks[hkT + s + lane]) - 127 : 0;
+  const int evj = prm.token && lane < L ? static_cast<int>(prm.vs[hkT + s + lane]) : 0;  // byte
   for (int i = 0; i < L; ++i) {
+    float cf = cf0, vsc = vsc0;
+    if (prm.token)
+      cf = prm.scale_log2 * pow2_or_zero_s(static_cast<int>(prm.qs[hT + s + i]) - 127) *
+           pow2_or_zero_s(ekj);
     float q[DIM / 32];
     load_score_rows<DIM, NVF4>(prm, true, static_cast<size_t>(s + i) * H + h, lane, q);
     // lane j keeps the raw score of key j (visible keys: j <= i, or j < L)
@@ -166,7 +176,17 @@ __device__ __forceinline__ void fwd_short_pair(const ShortParams& prm, int doc, 
     float l8 = p8;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) l8 += __shfl_xor_sync(0xffffffffu, l8, off);
-    const float ph = e4m3x2_to_float2(cvt_e4m3x2(p8, 0.f)).x;  // the E4M3 operand value
+    float fold = 1.f;
+    if (prm.token) {
+      // V's per-key factor folded into P^ relative to the largest exponent
+      // among the keys row i sees
+      int ev = vis ? evj : 0;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) ev = max(ev, __shfl_xor_sync(0xffffffffu, ev, off));
+      fold = vis ? pow2_or_zero_s(evj - ev) : 0.f;
+      vsc = pow2_or_zero_s(ev - 127);
+    }
+    const float ph = e4m3x2_to_float2(cvt_e4m3x2(p8 * fold, 0.f)).x;  // the E4M3 operand value
     float acc[DIM / 32] = {};
     for (int j = 0; j <= last; ++j) {
       const float pj = __shfl_sync(0xffffffffu, ph, j);
@@ -226,8 +246,22 @@ __device__ __forceinline__ void bwd_short_pair(const ShortParams& prm, int doc, 
   for (int gq = 0; gq < G; ++gq) {
     const int h = GQA ? hk * G + gq : u;
     const size_t hT = static_cast<size_t>(h) * T;
-    const int eq = static_cast<int>(prm.qs[hT + s]) - 127;
-    const int edo = static_cast<int>(prm.dos[hT + s]) - 127;
+    int eq = static_cast<int>(prm.qs[hT + s]) - 127;
+    int edo = static_cast<int>(prm.dos[hT + s]) - 127;
+    // per-token operand scales: eq, edo become the document's largest query
+    // and dO exponents (the scales of Q and dO in dK and dV; each token's own
+    // factor relative to them is folded into dS and P^b)
+    if (prm.token) {
+      int a = lane < L ? static_cast<int>(prm.qs[hT + s + lane]) : 0;
+      int b = lane < L ? static_cast<int>(prm.dos[hT + s + lane]) : 0;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        a = max(a, __shfl_xor_sync(0xffffffffu, a, off));
+        b = max(b, __shfl_xor_sync(0xffffffffu, b, off));
+      }
+      eq = a - 127;
+      edo = b - 127;
+    }
     const float cf = NVF4 ? prm.scale_log2 : prm.scale_log2 * pow2_or_zero_s(eq) * pow2_or_zero_s(ek);
     const float gp = pow2_or_zero_s(ev) * pow2_or_zero_s(edo);
     // P (x 2^8) and dS (x 2^8) of every visible pair, lane = key
@@ -238,19 +272,31 @@ __device__ __forceinline__ void bwd_short_pair(const ShortParams& prm, int doc, 
       load_codes<DIM>(prm.doc_, static_cast<size_t>(s + i) * H + h, lane, g);
       const float nl = 8.f - prm.lse_in[hT + s + i] * LOG2E;
       const float Di = prm.D[hT + s + i];
+      // per-token operand scales: query i's own exponents against the
+      // document's largest (dQ_i / dO_i factors in S and dP, folds for dK, dV)
+      const int eqi = prm.token ? static_cast<int>(prm.qs[hT + s + i]) - 127 : eq;
+      const int edoi = prm.token ? static_cast<int>(prm.dos[hT + s + i]) - 127 : edo;
+      const float fk = pow2_or_zero_s(eqi - eq);
       for (int j = 0; j <= (prm.causal ? i : L - 1); ++j) {
         float k[N], v[N];
         load_score_rows<DIM, NVF4>(prm, false, static_cast<size_t>(s + j) * Hkv + hk, lane, k);
         load_codes<DIM>(prm.vc, static_cast<size_t>(s + j) * Hkv + hk, lane, v);
         const float sd = warp_dot<DIM>(q, k);
         const float dp = warp_dot<DIM>(g, v);
-        const float p8 = ex2_approx(fmaf(sd, cf, nl));
-        const float d8 = p8 * fmaf(dp, gp, -Di);
+        float cfij = cf, gpij = gp;
+        if (prm.token) {
+          const int ekj = static_cast<int>(prm.ks[hkT + s + j]) - 127;
+          const int evj = static_cast<int>(prm.vs[hkT + s + j]) - 127;
+          cfij = prm.scale_log2 * pow2_or_zero_s(eqi) * pow2_or_zero_s(ekj);
+          gpij = pow2_or_zero_s(evj) * pow2_or_zero_s(edoi);
+        }
+        const float p8 = ex2_approx(fmaf(sd, cfij, nl));
+        const float d8 = p8 * fmaf(dp, gpij, -Di);
         if (lane == 0) {
           s_p[i][j] = p8;
           s_ds[i][j] = d8;
         }
-        amax = fmaxf(amax, fabsf(d8));
+        amax = fmaxf(amax, fabsf(d8 * fk));  // dK's operand (fk = 1 without token scales)
       }
     }
     __syncwarp();
@@ -261,21 +307,29 @@ __device__ __forceinline__ void bwd_short_pair(const ShortParams& prm, int doc, 
     for (int i = 0; i < L; ++i) {
       float acc[N] = {};
       float inv_i = inv, dsc_i = dsc;
-      if (prm.ds_rows) {  // row i's own exponent (the whole document is one key block)
+      // per-token operand scales: K's per-key factor folded into dQ's dS
+      // operand, which then takes query-row exponents
+      auto kfold = [&](int j) {
+        return prm.token ? pow2_or_zero_s(static_cast<int>(prm.ks[hkT + s + j]) - 127) : 1.f;
+      };
+      if (prm.ds_rows || prm.token) {  // row i's own exponent (the whole document is one key block)
         float am = 0.f;
-        for (int j = 0; j <= (prm.causal ? i : L - 1); ++j) am = fmaxf(am, fabsf(s_ds[i][j]));
+        for (int j = 0; j <= (prm.causal ? i : L - 1); ++j)
+          am = fmaxf(am, fabsf(s_ds[i][j] * kfold(j)));
         const int er = max(roundup_exponent(am) - 8, -127);
         inv_i = exp2i(-(er + 8));
         dsc_i = pow2_or_zero_s(er);
       }
       for (int j = 0; j <= (prm.causal ? i : L - 1); ++j) {
-        const float dsh = e4m3x2_to_float2(cvt_e4m3x2(s_ds[i][j] * inv_i, 0.f)).x * dsc_i;
+        const float dsh =
+            e4m3x2_to_float2(cvt_e4m3x2(s_ds[i][j] * kfold(j) * inv_i, 0.f)).x * dsc_i;
         float k[N];
         load_codes<DIM>(prm.kc, static_cast<size_t>(s + j) * Hkv + hk, lane, k);
 #pragma unroll
         for (int c = 0; c < N; ++c) acc[c] = fmaf(dsh, k[c], acc[c]);
       }
-      const float mul = pow2_or_zero_s(ek);  // softmax_scale: in the BF16 conversion
+      // softmax_scale: in the BF16 conversion
+      const float mul = prm.token ? 1.f : pow2_or_zero_s(ek);
       const size_t at = (static_cast<size_t>(s + i) * H + h) * DIM + N * lane;
       if (prm.dq_pre == nullptr) {
         float* dst = prm.dq_acc + at;
@@ -289,11 +343,23 @@ __device__ __forceinline__ void bwd_short_pair(const ShortParams& prm, int doc, 
       }
     }
     // dK_j = scale * sum_i dS^_ij Q^_i,  dV_j = 2^-8 sum_i P^b_ij dO^_i
+    unsigned long long cnz = 0, cz = 0;  // dS rounded-to-zero diagnostic
     for (int j = 0; j < L; ++j) {
       float ak[N] = {}, av[N] = {};
       for (int i = prm.causal ? j : 0; i < L; ++i) {
-        const float dsh = e4m3x2_to_float2(cvt_e4m3x2(s_ds[i][j] * inv, 0.f)).x * dsc;
-        const float pb = e4m3x2_to_float2(cvt_e4m3x2(s_p[i][j], 0.f)).x;
+        // per-token operand scales: Q's and dO's per-query factors folded
+        // into dS and P^b relative to the document's largest exponents
+        float fq = 1.f, fdo = 1.f;
+        if (prm.token) {
+          fq = pow2_or_zero_s(static_cast<int>(prm.qs[hT + s + i]) - 127 - eq);
+          fdo = pow2_or_zero_s(static_cast<int>(prm.dos[hT + s + i]) - 127 - edo);
+        }
+        const float dsh = e4m3x2_to_float2(cvt_e4m3x2(s_ds[i][j] * fq * inv, 0.f)).x * dsc;
+        const float pb = e4m3x2_to_float2(cvt_e4m3x2(s_p[i][j] * fdo, 0.f)).x;
+        if (s_ds[i][j] != 0.f) {
+          ++cnz;
+          if (dsh == 0.f) ++cz;
+        }
         float q[N], g[N];
         load_codes<DIM>(prm.qc, static_cast<size_t>(s + i) * H + h, lane, q);
         load_codes<DIM>(prm.doc_, static_cast<size_t>(s + i) * H + h, lane, g);
@@ -320,6 +386,10 @@ __device__ __forceinline__ void bwd_short_pair(const ShortParams& prm, int doc, 
         store_bf16<DIM>(prm.dk, static_cast<size_t>(s + j) * Hkv + hk, lane, ak);
         store_bf16<DIM>(prm.dv, static_cast<size_t>(s + j) * Hkv + hk, lane, av);
       }
+    }
+    if (prm.ds_count != nullptr && lane == 0) {
+      atomicAdd(prm.ds_count, cnz);
+      atomicAdd(prm.ds_count + 1, cz);
     }
     __syncwarp();  // s_p / s_ds are rewritten by the next head
   }
@@ -458,6 +528,15 @@ __global__ void __launch_bounds__(256, 4) attn_bwd_single_kernel(const ShortPara
   const int eb = max(roundup_exponent(fabsf(d8)) - 8, -127);
   const float dsh = e4m3x2_to_float2(cvt_e4m3x2(d8 * exp2i(-(eb + 8)), 0.f)).x * pow2_or_zero_s(eb);
   const float pb = e4m3x2_to_float2(cvt_e4m3x2(p8, 0.f)).x;
+  if (prm.ds_count != nullptr) {  // dS rounded-to-zero diagnostic, one add per warp
+    const unsigned act = __activemask();
+    const unsigned lnz = __ballot_sync(act, d8 != 0.f);
+    const unsigned lz = __ballot_sync(act, d8 != 0.f && dsh == 0.f);
+    if ((threadIdx.x & 31) == __ffs(act) - 1) {
+      atomicAdd(prm.ds_count, static_cast<unsigned long long>(__popc(lnz)));
+      atomicAdd(prm.ds_count + 1, static_cast<unsigned long long>(__popc(lz)));
+    }
+  }
   // dQ row of the accumulator: dS^ K^ (softmax_scale comes in the conversion)
   const float mul = pow2_or_zero_s(ek);
   const uint8_t* kc = prm.kc + row * DIM;
@@ -532,9 +611,10 @@ inline unsigned short_grid(int ndocs, int H, int ppw) {
 cudaError_t launch_fwd_short(const flamia_qtensor* q, const flamia_qtensor* k,
                              const flamia_qtensor* v, const int32_t* cu, int ndocs, int T, int H,
                              int Hkv, int d, float softmax_scale, bool nvfp4_qk, bool causal,
-                             void* o, float* lse, cudaStream_t stream) {
+                             bool token, void* o, float* lse, cudaStream_t stream) {
   ShortParams p = make_params(q, k, v, cu, ndocs, T, H, Hkv, softmax_scale);
   p.causal = causal ? 1 : 0;
+  p.token = token ? 1 : 0;  // (one-token documents: per-token scales are block scales)
   p.o = static_cast<__nv_bfloat16*>(o);
   p.lse = lse;
   const unsigned grid = short_grid(ndocs, H, p.ppw);
@@ -561,8 +641,9 @@ cudaError_t launch_bwd_short(const flamia_qtensor* q, const flamia_qtensor* k,
                              const flamia_qtensor* v, const flamia_qtensor* dout, const float* D,
                              const float* lse, const int32_t* cu, int ndocs, int T, int H,
                              int Hkv, int d, float softmax_scale, bool nvfp4_qk, bool hadamard,
-                             bool causal, bool ds_rows, float* dq_acc, const int8_t* dq_pre,
-                             void* dk, void* dv, cudaStream_t stream) {
+                             bool causal, bool ds_rows, bool token,
+                             unsigned long long* ds_count, float* dq_acc,
+                             const int8_t* dq_pre, void* dk, void* dv, cudaStream_t stream) {
   ShortParams p = make_params(q, k, v, cu, ndocs, T, H, Hkv, softmax_scale);
   p.hadamard = hadamard ? 1 : 0;
   p.causal = causal ? 1 : 0;
@@ -573,6 +654,8 @@ cudaError_t launch_bwd_short(const flamia_qtensor* q, const flamia_qtensor* k,
   p.dq_acc = dq_acc;
   p.dq_pre = dq_pre;
   p.ds_rows = ds_rows ? 1 : 0;
+  p.token = token ? 1 : 0;
+  p.ds_count = ds_count;
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
   if (Hkv == H && !nvfp4_qk && !hadamard) {  // one-token documents: one thread each

@@ -35,8 +35,32 @@ struct BwdParams {
   const int8_t* dq_pre;  // FP16 dQ accumulator: prescale exponents [H, T], else null (float32)
   int sched;             // kSchedDynamic / kSchedRule / kSchedStatic
   int ds_rows;           // dQ's dS operand with query-row exponents
+  int token;             // per-token operand scales (implies ds_rows)
+  unsigned long long* ds_count;  // dS rounded-to-zero diagnostic: [nonzero, zero], else null
   int* status;
 };
+
+// dS rounded-to-zero diagnostic of one 32-column chunk: among the chunk's dS
+// values (float, dv) the nonzero ones, and of those the ones whose E4M3 code
+// in the block payload (dw, four per word) is +-0; summed over the warp and
+// added to a shared-memory pair by lane 0.
+__device__ __forceinline__ void count_ds_zero(const uint32_t (&dv)[32], const uint32_t (&dw)[8],
+                                              unsigned long long* cnt, int lane) {
+  uint32_t nz = 0, z = 0;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const bool live = __uint_as_float(dv[i]) != 0.f;
+    const bool zero = ((dw[i >> 2] >> (8 * (i & 3))) & 0x7Fu) == 0u;
+    nz += live ? 1u : 0u;
+    z += (live && zero) ? 1u : 0u;
+  }
+  nz = __reduce_add_sync(0xffffffffu, nz);
+  z = __reduce_add_sync(0xffffffffu, z);
+  if (lane == 0) {
+    atomicAdd(cnt, static_cast<unsigned long long>(nz));
+    atomicAdd(cnt + 1, static_cast<unsigned long long>(z));
+  }
+}
 
 __device__ __forceinline__ float pow2_or_zero(int k) { return k < -126 ? 0.f : exp2i(k); }
 
@@ -79,6 +103,55 @@ __device__ __forceinline__ float bwd_chunk(const uint32_t (&sv)[32], uint32_t (&
     pw[i / 4] = cvt_e4m3x4(p01.x, p01.y, p23.x, p23.y);
   }
   return amax;
+}
+
+// Per-token operand scales: one 32-column chunk of a key row with per-column
+// (query) factors.  s = S 2^eQ(i) rowf + nl, dP 2^eD(i) rowg - D; dv gets
+// dS (2^8-scaled, unfolded) and pw the dV operand RNE_E4M3(P8 2^(eD(i) -
+// EdO)).  qf, df, pf: the chunk's 2^eQ(i), 2^eD(i), 2^(eD(i) - EdO).
+template <bool MASK>
+__device__ __forceinline__ void bwd_chunk_tok(const uint32_t (&sv)[32], uint32_t (&dv)[32],
+                                              const float* nl, const float* dd, const float* qf,
+                                              const float* df, const float* pf, float rowf,
+                                              float rowg, int col0, int key, uint32_t (&pw)[8]) {
+  const float2 rf2 = make_float2(rowf, rowf), rg2 = make_float2(rowg, rowg);
+#pragma unroll
+  for (int i = 0; i < 32; i += 4) {
+    const float4 n4 = *reinterpret_cast<const float4*>(nl + i);
+    const float4 d4 = *reinterpret_cast<const float4*>(dd + i);
+    const float4 q4 = *reinterpret_cast<const float4*>(qf + i);
+    const float4 g4 = *reinterpret_cast<const float4*>(df + i);
+    const float4 p4 = *reinterpret_cast<const float4*>(pf + i);
+    float2 s01 = __fmul2_rn(make_float2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])),
+                            make_float2(q4.x, q4.y));
+    float2 s23 = __fmul2_rn(make_float2(__uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3])),
+                            make_float2(q4.z, q4.w));
+    s01 = __ffma2_rn(s01, rf2, make_float2(n4.x, n4.y));
+    s23 = __ffma2_rn(s23, rf2, make_float2(n4.z, n4.w));
+    if (MASK) {
+      if (col0 + i + 0 < key) s01.x = -INFINITY;
+      if (col0 + i + 1 < key) s01.y = -INFINITY;
+      if (col0 + i + 2 < key) s23.x = -INFINITY;
+      if (col0 + i + 3 < key) s23.y = -INFINITY;
+    }
+    const float2 p01 = make_float2(ex2_approx(s01.x), ex2_approx(s01.y));
+    const float2 p23 = make_float2(ex2_approx(s23.x), ex2_approx(s23.y));
+    float2 g01 = __fmul2_rn(make_float2(__uint_as_float(dv[i]), __uint_as_float(dv[i + 1])),
+                            make_float2(g4.x, g4.y));
+    float2 g23 = __fmul2_rn(make_float2(__uint_as_float(dv[i + 2]), __uint_as_float(dv[i + 3])),
+                            make_float2(g4.z, g4.w));
+    g01 = __ffma2_rn(g01, rg2, make_float2(-d4.x, -d4.y));
+    g23 = __ffma2_rn(g23, rg2, make_float2(-d4.z, -d4.w));
+    const float2 d01 = __fmul2_rn(p01, g01);
+    const float2 d23 = __fmul2_rn(p23, g23);
+    dv[i] = __float_as_uint(d01.x);
+    dv[i + 1] = __float_as_uint(d01.y);
+    dv[i + 2] = __float_as_uint(d23.x);
+    dv[i + 3] = __float_as_uint(d23.y);
+    const float2 b01 = __fmul2_rn(p01, make_float2(p4.x, p4.y));
+    const float2 b23 = __fmul2_rn(p23, make_float2(p4.z, p4.w));
+    pw[i / 4] = cvt_e4m3x4(b01.x, b01.y, b23.x, b23.y);
+  }
 }
 
 // One backward work item (128-key tile of one document x one head), decoded

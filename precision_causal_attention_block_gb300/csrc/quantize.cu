@@ -61,6 +61,7 @@ struct QuantJob {
   uint8_t* f4scales[3];
   int H[3];
   int n;
+  int blk;  // tokens per scale block: 32, or 1 (per-token operand scales)
 };
 
 template <int DIM, bool HAD, bool FUSE_D>
@@ -141,8 +142,8 @@ __global__ void __launch_bounds__(kQThreads)
     // index outside [t - 31, t + 31] and [0, T)
     const int s = min(max(__ldg(cu + b), 0), t);
     const int e = max(min(__ldg(cu + b + 1), T), t + 1);
-    bs = s + ((t - s) & ~(kBlock - 1));
-    be = min(bs + kBlock, e);
+    bs = s + ((t - s) & ~(job.blk - 1));
+    be = min(bs + job.blk, e);
   }
   // This CTA owns the rows [A, Bend): blocks starting inside [seg0, seg0 + kSeg).
   if (tid == 0) s_bounds[0] = (bs == seg0) ? seg0 : be;
@@ -288,6 +289,7 @@ bool make_rows_map(CUtensorMap* map, const void* x, int T, int H, int d) {
 // Host checks of one tensor's arguments; on success fills its slot of the job.
 flamia_status check_tensor(const void* x, int H, int format, const flamia_qtensor* out,
                            QuantJob& job, int z) {
+  // (FLAMIA_FORMAT_TOKEN_SCALES is taken off by the callers)
   if (format != FLAMIA_FORMAT_MXFP8 && format != FLAMIA_FORMAT_MXFP8_NVFP4)
     return FLAMIA_ERR_UNSUPPORTED;
   if (x == nullptr || out == nullptr || out->codes == nullptr || out->scales == nullptr)
@@ -344,14 +346,17 @@ extern "C" flamia_status flamia_quantize_tokenblock(const void* x_bf16, int T, i
                                                     void* stream) {
   if (!supported_dim(d)) return FLAMIA_ERR_UNSUPPORTED;
   const bool had = (format & FLAMIA_FORMAT_HADAMARD) != 0;
-  format &= ~FLAMIA_FORMAT_HADAMARD;
+  const bool tok = (format & FLAMIA_FORMAT_TOKEN_SCALES) != 0;
+  format &= ~(FLAMIA_FORMAT_HADAMARD | FLAMIA_FORMAT_TOKEN_SCALES);
   if (had && (format != FLAMIA_FORMAT_MXFP8 || o_bf16 != nullptr || D != nullptr))
     return FLAMIA_ERR_UNSUPPORTED;
+  if (tok && format != FLAMIA_FORMAT_MXFP8) return FLAMIA_ERR_UNSUPPORTED;
   if (!valid_sizes(T, H, d, ndocs) || cu_seqlens == nullptr) return FLAMIA_ERR_INVALID_ARG;
   if ((o_bf16 == nullptr) != (D == nullptr)) return FLAMIA_ERR_INVALID_ARG;
   if (o_bf16 && !aligned(o_bf16, 16)) return FLAMIA_ERR_INVALID_ARG;
   QuantJob job{};
   job.n = 1;
+  job.blk = tok ? 1 : kBlock;
   const flamia_status st = check_tensor(x_bf16, H, format, out, job, 0);
   if (st != FLAMIA_OK) return st;
   const void* xs[1] = {x_bf16};
@@ -367,11 +372,14 @@ extern "C" flamia_status flamia_quantize_qkv(const void* q_bf16, const void* k_b
                                              void* stream) {
   if (!supported_dim(d)) return FLAMIA_ERR_UNSUPPORTED;
   const bool had = (format_qk & FLAMIA_FORMAT_HADAMARD) != 0;
-  const int fmt = format_qk & ~FLAMIA_FORMAT_HADAMARD;
+  const bool tok = (format_qk & FLAMIA_FORMAT_TOKEN_SCALES) != 0;
+  const int fmt = format_qk & ~(FLAMIA_FORMAT_HADAMARD | FLAMIA_FORMAT_TOKEN_SCALES);
   if (had && fmt != FLAMIA_FORMAT_MXFP8) return FLAMIA_ERR_UNSUPPORTED;
+  if (tok && fmt != FLAMIA_FORMAT_MXFP8) return FLAMIA_ERR_UNSUPPORTED;
   if (H_kv <= 0 || H <= 0 || H % H_kv != 0) return FLAMIA_ERR_INVALID_ARG;
   if (!valid_sizes(T, H, d, ndocs) || cu_seqlens == nullptr) return FLAMIA_ERR_INVALID_ARG;
   QuantJob job{};
+  job.blk = tok ? 1 : kBlock;  // V takes the same scale blocks as Q and K
   flamia_status st;
   if ((st = check_tensor(q_bf16, H, fmt, q, job, 0)) != FLAMIA_OK ||
       (st = check_tensor(k_bf16, H_kv, fmt, k, job, 1)) != FLAMIA_OK)
@@ -385,6 +393,7 @@ extern "C" flamia_status flamia_quantize_qkv(const void* q_bf16, const void* k_b
       return st;
     QuantJob jv{};
     jv.n = 1;
+    jv.blk = job.blk;
     if ((st = check_tensor(v_bf16, H_kv, FLAMIA_FORMAT_MXFP8, v, jv, 0)) != FLAMIA_OK) return st;
     const void* xv[1] = {v_bf16};
     return launch_quantize(xv, jv, T, d, cu_seqlens, ndocs, false, nullptr, nullptr, dev_status,

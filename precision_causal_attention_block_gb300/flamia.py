@@ -19,6 +19,7 @@ FLAMIA_OK = 0
 FORMAT_MXFP8 = 0
 FORMAT_MXFP8_NVFP4 = 1
 FORMAT_HADAMARD = 0x10
+FORMAT_TOKEN_SCALES = 0x20
 FLAG_NVFP4_QK = 0x1
 FLAG_HADAMARD = 0x2
 FLAG_NONCAUSAL = 0x4
@@ -28,9 +29,12 @@ FLAG_DQ_CAUSAL_SCALE = 0x20
 FLAG_SCHEDULE_STATIC = 0x40
 FLAG_SCHEDULE_RULE = 0x80
 FLAG_DS_ROW_EXPONENTS = 0x100
+FLAG_TOKEN_SCALES = 0x200
+FLAG_DS_ZERO_COUNT = 0x400
 DEV_BAD_SEQLENS = 0x1
 DEV_CAPACITY = 0x2
 DEV_TIMEOUT = 0x4
+DEV_RANGE = 0x8
 
 _LIB = None
 
@@ -52,6 +56,7 @@ SIGNATURES = {
     "flamia_attn_fwd_gqa": (_i, [_QP, _QP, _QP, _vp, _i, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp,
                                  _vp, _vp]),
     "flamia_fwd_workspace_bytes": (_sz, [_i, _i, _i]),
+    "flamia_bwd_ds_counts_offset": (_sz, [_i, _i, _i]),
     "flamia_bwd_workspace_bytes": (_sz, [_i, _i, _i]),
     "flamia_attn_bwd": (_i, [_QP, _QP, _QP, _QP, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp,
                              _vp, _vp, _vp, _vp, _sz, _vp, _vp]),
@@ -176,6 +181,10 @@ def flamia_attn_fwd_gqa(q: QTensor, k: QTensor, v: QTensor, cu_seqlens, T, H, H_
                                       _ptr(dev_status), _stream()), "flamia_attn_fwd_gqa")
 
 
+def flamia_bwd_ds_counts_offset(T: int, H: int, d: int) -> int:
+    return int(load().flamia_bwd_ds_counts_offset(T, H, d))
+
+
 def flamia_fwd_workspace_bytes(T: int, H: int, d: int) -> int:
     return int(load().flamia_fwd_workspace_bytes(T, H, d))
 
@@ -236,7 +245,8 @@ class TrainingCall:
     def __init__(self, T, H, d, cu_seqlens, softmax_scale, nvfp4_qk: bool = False,
                  hadamard: bool = False, causal: bool = True, H_kv=None,
                  deterministic_dq: bool = False, dq_accum: str = "fp32", schedule: str = "dynamic",
-                 ds_rows: bool = False, device="cuda"):
+                 ds_rows: bool = False, token_scales: bool = False,
+                 ds_zero_count: bool = False, device="cuda"):
         self.T, self.H, self.d = T, H, d
         self.H_kv = H if H_kv is None else H_kv
         self.scale = softmax_scale
@@ -248,9 +258,14 @@ class TrainingCall:
                        "fp16_causal": FLAG_DQ_FP16 | FLAG_DQ_CAUSAL_SCALE}[dq_accum] |
                       {"dynamic": 0, "rule": FLAG_SCHEDULE_RULE,
                        "static": FLAG_SCHEDULE_STATIC}[schedule] |
-                      (FLAG_DS_ROW_EXPONENTS if ds_rows else 0))
+                      (FLAG_DS_ROW_EXPONENTS if ds_rows else 0) |
+                      (FLAG_TOKEN_SCALES if token_scales else 0) |
+                      (FLAG_DS_ZERO_COUNT if ds_zero_count else 0))
         self.fmt_qk = ((FORMAT_MXFP8_NVFP4 if nvfp4_qk else FORMAT_MXFP8) |
-                       (FORMAT_HADAMARD if hadamard else 0))
+                       (FORMAT_HADAMARD if hadamard else 0) |
+                       (FORMAT_TOKEN_SCALES if token_scales else 0))
+        # dO takes the same scale blocks as Q, K and V
+        self.fmt_do = FORMAT_MXFP8 | (FORMAT_TOKEN_SCALES if token_scales else 0)
         self.q = QTensor(T, H, d, nvfp4_qk, device)
         self.k = QTensor(T, self.H_kv, d, nvfp4_qk, device)
         self.v = QTensor(T, self.H_kv, d, False, device)
@@ -287,7 +302,7 @@ class TrainingCall:
         return self.o, self.lse
 
     def backward(self, xdo):
-        flamia_quantize_tokenblock(xdo, self.cu, self.dout, FORMAT_MXFP8, o=self.o, D=self.D,
+        flamia_quantize_tokenblock(xdo, self.cu, self.dout, self.fmt_do, o=self.o, D=self.D,
                                    dev_status=self.status)
         flamia_attn_bwd_gqa(self.q, self.k, self.v, self.dout, self.D, self.lse, self.cu, self.T,
                             self.H, self.H_kv, self.d, self.scale, self.wl, self.dq, self.dk,
@@ -297,6 +312,13 @@ class TrainingCall:
     def __call__(self, xq, xk, xv, xdo):
         self.forward(xq, xk, xv)
         return self.backward(xdo)
+
+    def ds_zero_counts(self):
+        """(nonzero dS entries, those rounded to zero) of the last backward
+        with ds_zero_count (reads device memory: call after it completed)."""
+        off = flamia_bwd_ds_counts_offset(self.T, self.H, self.d)
+        c = self.ws[off:off + 16].view(torch.int64).cpu()
+        return int(c[0]), int(c[1])
 
     def check_status(self):
         st = int(self.status.item())

@@ -39,8 +39,10 @@ def test_size_queries(cpu_lib):
     # float32 dQ accumulator, int32 turn counters, int8 prescale table, 3 H
     # ints, each 256-byte padded
     th = 16384 * 16
-    assert fl.flamia_bwd_workspace_bytes(16384, 16, 128) == th * 128 * 4 + th * 4 + th + 256
-    assert fl.flamia_bwd_workspace_bytes(3, 1, 64) == 768 + 256 + 256 + 256
+    # (+ 256 bytes for the two dS counters at the end)
+    assert fl.flamia_bwd_workspace_bytes(16384, 16, 128) == th * 128 * 4 + th * 4 + th + 512
+    assert fl.flamia_bwd_workspace_bytes(3, 1, 64) == 768 + 256 + 256 + 256 + 256
+    assert fl.flamia_bwd_ds_counts_offset(3, 1, 64) == 768 + 256 + 256 + 256
     assert fl.flamia_bwd_workspace_bytes(10, 1, 96) == 0
     wl = fl.flamia_worklist_bytes(65536, 30)
     assert wl >= 64 + 16 * (65536 // 256 + 31) + 16 * (65536 // 128 + 31)
