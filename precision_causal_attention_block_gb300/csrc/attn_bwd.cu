@@ -79,12 +79,15 @@ struct BwdSmem {
   // block's largest exponents
   alignas(16) float tq[OPT && !NVF4 ? 4 : 1][2][OPT && !NVF4 ? kTile : 4];
   uint32_t qbyte[2][4], dobyte[2][4];  // E8M0 bytes of the 4 query blocks of Q and dO
-  uint32_t eds[4][4];            // dS block bytes [query block][key block]
-  uint8_t erow[4][4][32];        // query-row dS bytes [query block][key block][query]
+  // by tile parity (a fast warp may start the next tile's recompute while a
+  // slow one still reads this tile's to write the block scales)
+  uint32_t eds[2][4][4];         // dS block bytes [query block][key block]
+  uint8_t erow[2][4][4][32];     // query-row dS bytes [query block][key block][query]
   uint64_t bar_kv;
   uint64_t bar_qd_full[kBStages];
   uint64_t bar_qd_empty[kBStages];
   uint64_t bar_s_full, bar_sdp_read, bar_ds_full, bar_dq_full, bar_dq_read, bar_done, bar_sf;
+  uint64_t bar_staged, bar_stage_free;  // dQ staging: compute groups <-> reducer warp
   uint64_t bar_kv_free, bar_acc_full, bar_acc_empty;
   ItemRing<4> ring;  // claimed items: producer -> MMA issuer, compute leader
   int item_bc[2];    // the compute leader's copy for the compute groups
@@ -152,11 +155,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(smem_u32(&sm.bar_ds_full), kComputeThreads);
     mbar_init(smem_u32(&sm.bar_dq_full), 1);
     mbar_init(smem_u32(&sm.bar_dq_read), kComputeThreads);
+    mbar_init(smem_u32(&sm.bar_staged), kComputeThreads);
+    mbar_init(smem_u32(&sm.bar_stage_free), 1);
     mbar_init(smem_u32(&sm.bar_acc_full), 1);
     mbar_init(smem_u32(&sm.bar_acc_empty), kComputeThreads);
     mbar_init(smem_u32(&sm.bar_done), 1);
     mbar_init(smem_u32(&sm.bar_sf), kTile);
-    ring_init(sm.ring, 2);
+    ring_init(sm.ring, 3);  // the MMA issuer, the compute leader, the dQ reducer
     sm.abort = 0;
     sm.dscnt[0] = sm.dscnt[1] = 0ull;
     fence_barrier_init();
@@ -359,6 +364,61 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_commit_w(smem_u32(&sm.bar_done));
       if (!mbar_wait_w(smem_u32(&sm.bar_done), 0)) sm.abort = 1;
     }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ dQ reducer
+    // One thread reduce-adds each tile's staged dQ into the global float32 (or
+    // FP16) accumulator, so no compute warp waits for the bulk copies: it
+    // follows the items in claim order, waits for a tile's staging, issues the
+    // reduce-adds and frees the staging buffer once they have read it (in the
+    // deterministic mode: once they are complete, passing the tile's turn on).
+    if (lane == 0) {
+      bool ok = true;
+      int tg = 0;  // query tiles over all items
+      for (int n = 0; ok; ++n) {
+        const int idx = ring_get(sm.ring, n, true);
+        if (idx < 0) {
+          ok = false;
+          break;
+        }
+        if (idx >= total) break;
+        BwdItem it;
+        if (!decode_bwd_item(prm, n_items, idx, it)) continue;
+        for (int u = 0; u < it.nq * G; ++u, ++tg) {
+          if (!mbar_wait(smem_u32(&sm.bar_staged), tg & 1) || sm.abort) {
+            ok = false;
+            break;
+          }
+          const int q0 = tile_q0(it, u), h = tile_head(it, u);
+          int* turn = !OPT || prm.dq_turns == nullptr
+                          ? nullptr
+                          : prm.dq_turns + static_cast<size_t>(q0) * prm.H + h;
+          if (turn != nullptr && !wait_turn(turn, dq_turn(prm, it, q0))) {
+            ok = false;
+            break;
+          }
+          if (OPT && prm.dq_pre != nullptr) {
+            const __half* box0 = reinterpret_cast<const __half*>(sm.dqs[0]);
+#pragma unroll
+            for (int b = 0; b < DIM / 64; ++b)
+              tma_reduce_add_3d(&map_dq, smem_u32(box0 + b * (kTile * 64)), 64 * b, h, q0);
+          } else {
+#pragma unroll
+            for (int c = 0; c < DIM / 32; ++c)
+              tma_reduce_add_3d(&map_dq, smem_u32(sm.dqs[c]), 32 * c, h, q0);
+          }
+          bulk_commit_group();
+          if (turn != nullptr) {
+            bulk_wait_group0();
+            pass_turn(turn);
+          } else {
+            bulk_wait_group_read0();
+          }
+          mbar_arrive(smem_u32(&sm.bar_stage_free));
+        }
+      }
+      bulk_wait_group0();
+      if (!ok) sm.abort = 1;
+    }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ compute groups
     const int g = (warp - 4) >> 2;   // 0: query columns 0..63, 1: 64..127
@@ -373,23 +433,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bool ok = true;
     int uc = 0;  // query tiles processed over all items (phase and buffer parity)
     int nk = 0;  // items processed
-    int* pend = nullptr;  // deterministic dQ: the turn the last reduce-adds pass on
-    // The staging buffer is free once the previous reduce-adds have read it
-    // (deterministic mode: completed, and their turn passed on).
-    auto staging_free = [&]() {
-      if (!issuer) return;
-      if (!OPT || prm.dq_turns == nullptr) {
-        bulk_wait_group_read0();
-      } else {
-        bulk_wait_group0();
-        if (pend != nullptr) pass_turn(pend);
-        pend = nullptr;
-      }
-    };
     // dQ_t (tile t = ut of the item, global index tg) from tensor memory to the
-    // staging buffer; every compute thread calls it (it arrives on dq_read)
+    // staging buffer, for the reducer warp; every compute thread calls it (it
+    // arrives on dq_read, then on staged).  The buffer is free once the
+    // reducer's bulk copies of the previous tile have read it.
     auto read_dq = [&](const BwdItem& it, int ut, int tg) {
-      ok = ok && !sm.abort && mbar_wait(smem_u32(&sm.bar_dq_full), tg & 1);
+      ok = ok && !sm.abort && mbar_wait(smem_u32(&sm.bar_dq_full), tg & 1) &&
+           (tg == 0 || mbar_wait(smem_u32(&sm.bar_stage_free), (tg - 1) & 1));
       tc_fence_after();
       if (!ok) return;
       const bool qv = tile_q0(it, ut) + j < it.e;  // TMEM lane j of dQ_t is query row j
@@ -437,30 +487,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
         }
       }
-    };
-    // the staged dQ_t (after a barrier) reduce-added into the global accumulator
-    auto reduce_dq = [&](const BwdItem& it, int ut) {
-      if (!issuer || sm.abort) return;
-      const int q0 = tile_q0(it, ut), h = tile_head(it, ut);
-      int* turn = !OPT || prm.dq_turns == nullptr
-                      ? nullptr
-                      : prm.dq_turns + static_cast<size_t>(q0) * prm.H + h;
-      if (turn != nullptr && !wait_turn(turn, dq_turn(prm, it, q0))) {
-        sm.abort = 1;
-        return;
-      }
-      if (OPT && prm.dq_pre != nullptr) {
-        const __half* box0 = reinterpret_cast<const __half*>(sm.dqs[0]);
-#pragma unroll
-        for (int b = 0; b < DIM / 64; ++b)
-          tma_reduce_add_3d(&map_dq, smem_u32(box0 + b * (kTile * 64)), 64 * b, h, q0);
-      } else {
-#pragma unroll
-        for (int c = 0; c < DIM / 32; ++c)
-          tma_reduce_add_3d(&map_dq, smem_u32(sm.dqs[c]), 32 * c, h, q0);
-      }
-      bulk_commit_group();
-      pend = turn;
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(&sm.bar_staged));
     };
     for (int n = 0;; ++n) {
       if (issuer) sm.item_bc[n & 1] = ring_get(sm.ring, n, true);
@@ -639,7 +667,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           *reinterpret_cast<uint4*>(pbrow + 16 * ch1) = make_uint4(pw[4], pw[5], pw[6], pw[7]);
           *reinterpret_cast<uint4*>(dsrow + 16 * ch0) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
           *reinterpret_cast<uint4*>(dsrow + 16 * ch1) = make_uint4(dw[4], dw[5], dw[6], dw[7]);
-          if (lane == 0) sm.eds[c][quad] = static_cast<uint32_t>(eb + 127);
+          if (lane == 0) sm.eds[ub][c][quad] = static_cast<uint32_t>(eb + 127);
           if (OPT && prm.ds_rows) {
             // dQ's operand: per query column the maximum over this warp's 32
             // keys (one key block); lane q keeps query q's and its exponent.
@@ -659,7 +687,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             const int er = max(roundup_exponent(__uint_as_float(mine)) - 8, -127);
             const float invr = exp2i(-(er + 8));
-            sm.erow[c][quad][lane] = static_cast<uint8_t>(er + 127);
+            sm.erow[ub][c][quad][lane] = static_cast<uint8_t>(er + 127);
             uint32_t dr[8];
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
@@ -676,8 +704,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             *reinterpret_cast<uint4*>(ds2row + 16 * ch1) = make_uint4(dr[4], dr[5], dr[6], dr[7]);
           }
         }
-        // the staging buffer must be free before dQ_{t-1} is staged below
-        if (u > 0) staging_free();
+        // the next tile's per-query inputs (their nl / dd / byte buffer was last
+        // read by tile t-1, the prescale buffer by tile t-2's staging), visible
+        // after the barrier, which also completes the dS block exponents
+        if (g == 0 && u + 1 < nq) store_query_inputs(uc + 1);
         named_barrier_sync(1, kComputeThreads);
         if (ok) {
           // block scales of the three products (this tile's parity buffer,
@@ -700,8 +730,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               // dK: A = dS^T, row block = key block i, K blocks = query blocks
-              w[i] = sm.eds[0][i] | (sm.eds[1][i] << 8) | (sm.eds[2][i] << 16) |
-                     (sm.eds[3][i] << 24);
+              w[i] = sm.eds[ub][0][i] | (sm.eds[ub][1][i] << 8) | (sm.eds[ub][2][i] << 16) |
+                     (sm.eds[ub][3][i] << 24);
               w[4 + i] = qw;  // dK: B = Q, per query block
             }
             tmem_st8(tmem + lane_off + sfc + kSfDkA, w);
@@ -710,13 +740,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int i = 0; i < 4; ++i) {
               // dQ: A = dS, row block = query block i, K blocks = key blocks
               if (OPT && prm.ds_rows)  // this lane's query 32 i + lane
-                w[i] = static_cast<uint32_t>(sm.erow[i][0][lane]) |
-                       (static_cast<uint32_t>(sm.erow[i][1][lane]) << 8) |
-                       (static_cast<uint32_t>(sm.erow[i][2][lane]) << 16) |
-                       (static_cast<uint32_t>(sm.erow[i][3][lane]) << 24);
+                w[i] = static_cast<uint32_t>(sm.erow[ub][i][0][lane]) |
+                       (static_cast<uint32_t>(sm.erow[ub][i][1][lane]) << 8) |
+                       (static_cast<uint32_t>(sm.erow[ub][i][2][lane]) << 16) |
+                       (static_cast<uint32_t>(sm.erow[ub][i][3][lane]) << 24);
               else
-                w[i] = sm.eds[i][0] | (sm.eds[i][1] << 8) | (sm.eds[i][2] << 16) |
-                       (sm.eds[i][3] << 24);
+                w[i] = sm.eds[ub][i][0] | (sm.eds[ub][i][1] << 8) | (sm.eds[ub][i][2] << 16) |
+                       (sm.eds[ub][i][3] << 24);
               // dQ: B = K, per key block (2^0: per-token K factors are in dS)
               w[4 + i] = (OPT && !NVF4 && prm.token) ? 0x7F7F7F7Fu : kword;
             }
@@ -732,27 +762,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mbar_arrive(smem_u32(&sm.bar_ds_full));
         }
         if (!ok) sm.abort = 1;
-        // the next tile's per-query inputs (its nl / dd / byte buffer was last
-        // read by tile t-1, its prescale buffer by tile t-2's staging)
-        if (g == 0 && u + 1 < nq) store_query_inputs(uc + 1);
-        named_barrier_sync(1, kComputeThreads);
-        if (u > 0) reduce_dq(it, u - 1);
       }
       // the item's last dQ
-      if (nq > 0) {
-        staging_free();
-        named_barrier_sync(1, kComputeThreads);
-        read_dq(it, nq - 1, uc - 1);
-        fence_proxy_async_smem();
-        if (!ok) sm.abort = 1;
-        named_barrier_sync(1, kComputeThreads);
-        reduce_dq(it, nq - 1);
-      }
-      if (OPT && issuer && pend != nullptr) {  // the item's last turn, before the next item
-        bulk_wait_group0();
-        pass_turn(pend);
-        pend = nullptr;
-      }
+      if (nq > 0) read_dq(it, nq - 1, uc - 1);
+      if (!ok) sm.abort = 1;
       // every product of the item is complete
       ok = ok && !sm.abort && mbar_wait(smem_u32(&sm.bar_acc_full), nk & 1);
       tc_fence_after();
@@ -822,7 +835,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_arrive(smem_u32(&sm.bar_acc_empty));
       }
     }
-    if (issuer) bulk_wait_group0();
     if (!ok) sm.abort = 1;
   }
 
