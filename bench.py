@@ -191,7 +191,7 @@ def run_ours(args, rank, world, local):
                            hadamard=args.hadamard, causal=not args.noncausal, H_kv=hkv,
                            deterministic_dq=args.deterministic, dq_accum=args.dq_accum,
                            schedule=args.schedule, ds_rows=args.ds_rows,
-                           token_scales=args.token_scales, device=dev)
+                           token_scales=args.token_scales, bwd_ctas=args.bwd_ctas, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -254,7 +254,8 @@ def run_ours(args, rank, world, local):
                                    causal=not args.noncausal, H_kv=hkv,
                                    deterministic_dq=args.deterministic, dq_accum=args.dq_accum,
                                    schedule=args.schedule, ds_rows=args.ds_rows,
-                                   token_scales=args.token_scales, device=dev)]
+                                   token_scales=args.token_scales, bwd_ctas=args.bwd_ctas,
+                                   device=dev)]
     xin = [xd, {n: torch.empty_like(t) for n, t in xd.items()}]
     outs = lambda c: (c.o, c.dq, c.dk, c.dv)
     hout = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs(c)] for c in calls]
@@ -361,6 +362,7 @@ def run_ours(args, rank, world, local):
                    "dq_sum": "ordered (deterministic)" if args.deterministic else "atomic",
                    "dq_accumulator": args.dq_accum,
                    "schedule": args.schedule,
+                   "bwd_ctas": args.bwd_ctas,
                    "ds_exponents": "query row" if (args.ds_rows or args.token_scales)
                    else "32x32 block",
                    "operand_scales": "per token" if args.token_scales else "32-token block",
@@ -368,7 +370,8 @@ def run_ours(args, rank, world, local):
                    "parallelism": f"replicas x{world}"},
         "pct_of_fp8_peak": round(100.0 * value / world / pk["fp8_tflops"], 2),
         "roofline": {"kernel": "flamia_attn_bwd (memset + %s + short-document kernel + dq convert)"
-                               % ("attn_bwd128_kernel" if w.d == 128 and not args.nvfp4
+                               % (("attn_bwd_pair_kernel (CTA pairs)" if args.bwd_ctas == "pair"
+                                   else "attn_bwd128_kernel") if w.d == 128 and not args.nvfp4
                                   else "attn_bwd_kernel<64, nvfp4>" if args.nvfp4
                                   else "attn_bwd_kernel<64>"),
                      "bound": "tensor", "achieved": round(achieved, 2),
@@ -408,7 +411,7 @@ def ds_zero_stats(w, xd, args, hkv, dev):
     import torch
 
     from precision_causal_attention_block_gb300 import flamia as fl
-    if args.deterministic or args.dq_accum != "fp32":
+    if args.deterministic or args.dq_accum != "fp32" or args.bwd_ctas == "pair":
         return None
     cu = torch.tensor(w.cu_seqlens, dtype=torch.int32, device=dev)
     call = fl.TrainingCall(w.T, w.H, w.d, cu, w.sm_scale, nvfp4_qk=args.nvfp4,
@@ -484,7 +487,7 @@ def profile_calls(args):
                            hadamard=args.hadamard, causal=not args.noncausal,
                            deterministic_dq=args.deterministic, dq_accum=args.dq_accum,
                            schedule=args.schedule, ds_rows=args.ds_rows,
-                           token_scales=args.token_scales)
+                           token_scales=args.token_scales, bwd_ctas=args.bwd_ctas)
     for _ in range(args.warmup + args.steps):
         call(xd["q"], xd["k"], xd["v"], xd["do"])
     torch.cuda.synchronize()
@@ -518,7 +521,7 @@ def stage_breakdown(call, xd, stream, flush, w, reps=10):
         "bwd_ms": lambda: fl.flamia_attn_bwd_gqa(call.q, call.k, call.v, call.dout, call.D,
                                                  call.lse, call.cu, call.T, call.H, call.H_kv,
                                                  call.d, call.scale, call.wl, call.dq, call.dk,
-                                                 call.dv, call.ws, call.flags,
+                                                 call.dv, call.ws, call.bwd_flags,
                                                  dev_status=call.status),
     }
     out = {}
@@ -660,6 +663,9 @@ def main():
     ap.add_argument("--token-scales", action="store_true",
                     help="per-token operand scales (one exponent per token, folded into the "
                          "opposite operand; with query-row dS exponents)")
+    ap.add_argument("--bwd-ctas", default="rule", choices=["rule", "one", "pair"],
+                    help="head dim 128: backward items of one 128-key CTA or of a CTA pair "
+                         "splitting 256 keys (rule: the library's choice by shape)")
     ap.add_argument("--deterministic", action="store_true",
                     help="dQ partials added in a fixed key-tile order (bitwise reproducible)")
     args = ap.parse_args()

@@ -121,6 +121,24 @@ typedef enum {
                                        (static snake otherwise).  Default, no
                                        flag: dynamic claims (measured fastest
                                        on every workload here)                 */
+#define FLAMIA_FLAG_BWD_CTA_PAIR 0x800 /* backward only, head dim 128: the
+                                       2-CTA mode (review page sec. 3.4
+                                       "Backward pass"): clusters of two CTAs,
+                                       each pair splitting 256 keys and running
+                                       its products together; FLAMIA_ERR_
+                                       UNSUPPORTED with the NVFP4 path,
+                                       FLAMIA_FLAG_DETERMINISTIC_DQ,
+                                       FLAMIA_FLAG_DQ_FP16, query-row dS
+                                       exponents, per-token scales, the dS
+                                       diagnostic or a static schedule          */
+#define FLAMIA_FLAG_BWD_ONE_CTA 0x1000 /* backward only: one CTA per 128-key
+                                       tile.  With neither flag the backward
+                                       takes the measured rule, which picks
+                                       one-CTA items on every shape (the pair
+                                       was as fast or slower everywhere it was
+                                       timed: packed 4 x 4096, variable-length
+                                       and skewed packings, non-causal,
+                                       grouped heads)                          */
 
 /*
  * One quantised operand, all device pointers owned by the caller.

@@ -63,6 +63,33 @@ flamia_status flamia_debug_bounded_waits(int* turn, int* dev_status, void* strea
 flamia_status flamia_debug_tmem_ldred(const float* in, float* vals, float* mx, void* stream);
 
 /*
+ * One product of a CTA pair (a cluster of two CTAs whose tensor cores run it
+ * together, tcgen05 .cta_group::2; review page sec. 3.4 "Backward pass": the
+ * 2-CTA mode splits 256 keys between the pair), in the three shapes the pair
+ * backward uses.  CTA r (0, 1) holds A's rows 128 r .. 128 r + 127 and half of
+ * B's columns; D rows of CTA r are returned in d_out[r][128][N] (float32).
+ *  shape 0: E4M3 unscaled, M 256, N 64, K 128 (S^T = K Q^T):
+ *           a u8 [2][128][128] (rows = M, K-major); b u8 [2][32][128]
+ *           (CTA r: columns 32 r .. 32 r + 31, rows = N, K-major).
+ *  shape 1: E4M3 block-scaled, M 256, N 128, K 64 (dV = P^T dO):
+ *           a u8 [2][128][64] (K-major); b u8 [2][64][64] (CTA r: columns
+ *           64 r .. 64 r + 63, [K][N], MN-major); sfa u8 [2][128][2] (per row and
+ *           K block); sfb u8 [2] (per K block, every column).
+ *  shape 2: E4M3 block-scaled, M 256, N 64, K 256 (dQ^T = K^T dS^T):
+ *           a u8 [2][256][128] ([K][M], MN-major); b u8 [2][256][32] ([K][N],
+ *           MN-major); sfa u8 [2][8], sfb u8 [2][8] (per CTA, per K block,
+ *           uniform over M / N).  Only the columns a CTA supplied itself
+ *           (32 r .. 32 r + 31) are products of its own A and B.
+ * variant (diagnostics, shape 1): bit 0 leaves out the copies of A's scales
+ * at column + 4 + row / 32; bit 1 fills B's scales only in the columns of
+ * this CTA's own half.  tmem_cols (device u32 [2]) receives each CTA's
+ * allocated tensor-memory address.  All pointers are device pointers.
+ */
+flamia_status flamia_debug_pair_mma(int shape, int variant, const uint8_t* a, const uint8_t* b,
+                                    const uint8_t* sfa, const uint8_t* sfb, float* d_out,
+                                    uint32_t* tmem_cols, int* dev_status, void* stream);
+
+/*
  * Number of kernel launches the library has enqueued since it was loaded, over
  * every entry point and host thread (memsets are not kernels and are not
  * counted).  Read it before and after a region to count that region's

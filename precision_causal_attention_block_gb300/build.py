@@ -18,6 +18,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libflamia.so")
 SOURCES = ["abi.cu", "quantize.cu", "worklist.cu", "attn_fwd.cu", "attn_bwd.cu", "attn_bwd128.cu",
            "attn_short.cu",
+           "attn_bwd_pair.cu",
            "probe_mma.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]

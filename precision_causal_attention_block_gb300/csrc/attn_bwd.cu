@@ -1052,8 +1052,9 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
                          const flamia_qtensor* v, const flamia_qtensor* dout, const float* D,
                          const float* lse, const int32_t* cu, int ndocs, int T, int H,
                          int Hkv, float softmax_scale, bool had, bool causal, bool det, int dq16,
-                         int sched, bool ds_rows, bool tok, bool dscount, void* wl, void* dq,
-                         void* dk, void* dv, void* ws, int* status, cudaStream_t stream) {
+                         int sched, bool ds_rows, bool tok, bool dscount, int ctas, void* wl,
+                         void* dq, void* dk, void* dv, void* ws, int* status,
+                         cudaStream_t stream) {
   ds_rows = ds_rows || tok;  // per-token operand scales take query-row dS exponents
   // (head dim 128 builds its own maps in launch_bwd128_pipelined)
   CUtensorMap mq{}, mk{}, mv{}, mdo{}, mdq{}, mq4{}, mk4{};
@@ -1147,9 +1148,16 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
   // persistent: one CTA per SM (shared memory allows one), items claimed in list order
   const long long grid = std::min<long long>(static_cast<long long>(L.cap_bwd) * Hkv, num_sms());
   if constexpr (DIM == 128 && !NVF4) {
-    if (launch_bwd128_pipelined(prm, q, k, v, dout, acc, static_cast<unsigned>(grid), stream) !=
-        cudaSuccess)
-      return FLAMIA_ERR_CUDA;
+    // two-CTA items when the caller asks for them; the rule by shape picks
+    // one-CTA items for every call (the pair measured as fast or slower on
+    // every shape: 4 x 4096 0.731 against 0.716 ms, non-causal 1.262 against
+    // 1.253, four K / V heads 0.778 against 0.762, the variable-length 65,536
+    // and the skewed 8,192 + 224 x 256 packings equal)
+    const bool pair = ctas == 2 && bwd_pair_supported(prm);
+    const cudaError_t e =
+        pair ? launch_bwd128_pair(prm, q, k, v, dout, acc, stream)
+             : launch_bwd128_pipelined(prm, q, k, v, dout, acc, static_cast<unsigned>(grid), stream);
+    if (e != cudaSuccess) return FLAMIA_ERR_CUDA;
   } else {
     const bool opt = det || dq16 || ds_rows || dscount;
     const size_t smem =
@@ -1221,7 +1229,19 @@ extern "C" flamia_status flamia_attn_bwd_gqa(const flamia_qtensor* q, const flam
                  FLAMIA_FLAG_DETERMINISTIC_DQ | FLAMIA_FLAG_DQ_FP16 |
                  FLAMIA_FLAG_DQ_CAUSAL_SCALE | FLAMIA_FLAG_SCHEDULE_STATIC |
                  FLAMIA_FLAG_SCHEDULE_RULE | FLAMIA_FLAG_DS_ROW_EXPONENTS |
-                 FLAMIA_FLAG_TOKEN_SCALES | FLAMIA_FLAG_DS_ZERO_COUNT)) != 0)
+                 FLAMIA_FLAG_TOKEN_SCALES | FLAMIA_FLAG_DS_ZERO_COUNT |
+                 FLAMIA_FLAG_BWD_CTA_PAIR | FLAMIA_FLAG_BWD_ONE_CTA)) != 0)
+    return FLAMIA_ERR_UNSUPPORTED;
+  const int ctas = (flags & FLAMIA_FLAG_BWD_CTA_PAIR) ? 2 : (flags & FLAMIA_FLAG_BWD_ONE_CTA) ? 1 : 0;
+  if ((flags & FLAMIA_FLAG_BWD_CTA_PAIR) && (flags & FLAMIA_FLAG_BWD_ONE_CTA))
+    return FLAMIA_ERR_UNSUPPORTED;
+  // the 2-CTA mode runs the default numerics only (head dim 128, MXFP8, float32
+  // unordered dQ, 32 x 32 dS exponents, dynamic claims)
+  if (ctas == 2 && (d != 128 || (flags & (FLAMIA_FLAG_NVFP4_QK | FLAMIA_FLAG_DETERMINISTIC_DQ |
+                                          FLAMIA_FLAG_DQ_FP16 | FLAMIA_FLAG_DS_ROW_EXPONENTS |
+                                          FLAMIA_FLAG_TOKEN_SCALES | FLAMIA_FLAG_DS_ZERO_COUNT |
+                                          FLAMIA_FLAG_SCHEDULE_STATIC)) ||
+                    ((flags & FLAMIA_FLAG_SCHEDULE_RULE) && (flags & FLAMIA_FLAG_NONCAUSAL))))
     return FLAMIA_ERR_UNSUPPORTED;
   const bool ds_rows = (flags & FLAMIA_FLAG_DS_ROW_EXPONENTS) != 0;
   const bool tok = (flags & FLAMIA_FLAG_TOKEN_SCALES) != 0;
@@ -1261,13 +1281,13 @@ extern "C" flamia_status flamia_attn_bwd_gqa(const flamia_qtensor* q, const flam
   const float sc = had ? softmax_scale / static_cast<float>(d) : softmax_scale;
   if (nvf4)
     return launch_bwd<64, true>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, H_kv, sc,
-                                false, causal, det, dq16, sched, ds_rows, false, dscount, wl, dq_bf16,
+                                false, causal, det, dq16, sched, ds_rows, false, dscount, ctas, wl, dq_bf16,
                                 dk_bf16, dv_bf16, ws, dev_status, s);
   return d == 128 ? launch_bwd<128, false>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, H_kv,
-                                           sc, had, causal, det, dq16, sched, ds_rows, tok, dscount, wl,
+                                           sc, had, causal, det, dq16, sched, ds_rows, tok, dscount, ctas, wl,
                                            dq_bf16, dk_bf16, dv_bf16, ws, dev_status, s)
                   : launch_bwd<64, false>(q, k, v, dout, D, lse, cu_seqlens, ndocs, T, H, H_kv,
-                                          sc, had, causal, det, dq16, sched, ds_rows, tok, dscount, wl,
+                                          sc, had, causal, det, dq16, sched, ds_rows, tok, dscount, ctas, wl,
                                           dq_bf16, dk_bf16, dv_bf16, ws, dev_status, s);
 }
 

@@ -198,6 +198,13 @@ __device__ __forceinline__ int dq_turn(const BwdParams& prm, const BwdItem& it, 
 // through shared memory and a named barrier, so a group's warps never
 // disagree on the item and never miss a barrier).
 
+// The 2-CTA backward (head dim 128): whether the call's modes allow it, and
+// its launch (grid: as many CTA pairs as can be resident).
+bool bwd_pair_supported(const BwdParams& prm);
+cudaError_t launch_bwd128_pair(const BwdParams& prm, const flamia_qtensor* q,
+                               const flamia_qtensor* k, const flamia_qtensor* v,
+                               const flamia_qtensor* dout, float* acc, cudaStream_t stream);
+
 // Pipelined backward for head dim 128 (MXFP8 score product); grid = CTAs.
 cudaError_t launch_bwd128_pipelined(const BwdParams& prm, const flamia_qtensor* q,
                                     const flamia_qtensor* k, const flamia_qtensor* v,

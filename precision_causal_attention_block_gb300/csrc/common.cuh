@@ -160,6 +160,24 @@ inline bool make_token_map(CUtensorMap* map, const void* base, int T, int H, int
   return r == CUDA_SUCCESS;
 }
 
+// The same [T, H, row_bytes] byte tensor with a box of box_bytes of a row
+// (a column slice of the head dimension) x box_rows tokens of one head.
+inline bool make_token_slice_map(CUtensorMap* map, const void* base, int T, int H, int row_bytes,
+                                 int box_bytes, int box_rows, CUtensorMapSwizzle swz) {
+  EncodeTiledFn enc = get_encode_tiled();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(T)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_bytes),
+                           static_cast<cuuint64_t>(row_bytes) * H};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_bytes), 1u, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // A plain [rows][row_bytes] byte matrix; box = (row_bytes, box_rows).
 inline bool make_matrix_map(CUtensorMap* map, const void* base, int rows, int row_bytes,
                             int box_rows, CUtensorMapSwizzle swz) {

@@ -31,6 +31,8 @@ FLAG_SCHEDULE_RULE = 0x80
 FLAG_DS_ROW_EXPONENTS = 0x100
 FLAG_TOKEN_SCALES = 0x200
 FLAG_DS_ZERO_COUNT = 0x400
+FLAG_BWD_CTA_PAIR = 0x800
+FLAG_BWD_ONE_CTA = 0x1000
 DEV_BAD_SEQLENS = 0x1
 DEV_CAPACITY = 0x2
 DEV_TIMEOUT = 0x4
@@ -68,6 +70,7 @@ SIGNATURES = {
     "flamia_debug_bounded_waits": (_i, [_vp, _vp, _vp]),
     "flamia_debug_launch_count": (ctypes.c_ulonglong, []),
     "flamia_debug_tmem_ldred": (_i, [_vp, _vp, _vp, _vp]),
+    "flamia_debug_pair_mma": (_i, [_i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
 }
 
 
@@ -221,6 +224,13 @@ def flamia_debug_tmem_ldred(x, vals, mx):
            "flamia_debug_tmem_ldred")
 
 
+def flamia_debug_pair_mma(shape, variant, a, b, sfa, sfb, d_out, tmem_cols, dev_status):
+    _check(load().flamia_debug_pair_mma(shape, variant, _ptr(a), _ptr(b), _ptr(sfa), _ptr(sfb),
+                                        _ptr(d_out), _ptr(tmem_cols), _ptr(dev_status),
+                                        _stream()),
+           "flamia_debug_pair_mma")
+
+
 def flamia_debug_launch_count() -> int:
     """Kernel launches the library has enqueued since it was loaded."""
     return int(load().flamia_debug_launch_count())
@@ -246,7 +256,7 @@ class TrainingCall:
                  hadamard: bool = False, causal: bool = True, H_kv=None,
                  deterministic_dq: bool = False, dq_accum: str = "fp32", schedule: str = "dynamic",
                  ds_rows: bool = False, token_scales: bool = False,
-                 ds_zero_count: bool = False, device="cuda"):
+                 ds_zero_count: bool = False, bwd_ctas: str = "rule", device="cuda"):
         self.T, self.H, self.d = T, H, d
         self.H_kv = H if H_kv is None else H_kv
         self.scale = softmax_scale
@@ -261,6 +271,9 @@ class TrainingCall:
                       (FLAG_DS_ROW_EXPONENTS if ds_rows else 0) |
                       (FLAG_TOKEN_SCALES if token_scales else 0) |
                       (FLAG_DS_ZERO_COUNT if ds_zero_count else 0))
+        # backward only: one- or two-CTA items (head dim 128), or the library's rule
+        self.bwd_flags = self.flags | {"rule": 0, "one": FLAG_BWD_ONE_CTA,
+                                       "pair": FLAG_BWD_CTA_PAIR}[bwd_ctas]
         self.fmt_qk = ((FORMAT_MXFP8_NVFP4 if nvfp4_qk else FORMAT_MXFP8) |
                        (FORMAT_HADAMARD if hadamard else 0) |
                        (FORMAT_TOKEN_SCALES if token_scales else 0))
@@ -306,7 +319,7 @@ class TrainingCall:
                                    dev_status=self.status)
         flamia_attn_bwd_gqa(self.q, self.k, self.v, self.dout, self.D, self.lse, self.cu, self.T,
                             self.H, self.H_kv, self.d, self.scale, self.wl, self.dq, self.dk,
-                            self.dv, self.ws, self.flags, dev_status=self.status)
+                            self.dv, self.ws, self.bwd_flags, dev_status=self.status)
         return self.dq, self.dk, self.dv
 
     def __call__(self, xq, xk, xv, xdo):

@@ -109,6 +109,13 @@ def long16384():
     return Workload("long_16384_H32_d64", 16384, 32, 64, (0, 16384), 1.0 / 8.0, "rms")
 
 
+def skewed8192():
+    """The training-call table's most skewed packing: one 8,192-token document
+    followed by 224 documents of 256 tokens (T = 65,536), H=16, d=128."""
+    return Workload("skewed_8192_224x256_H16_d128", 65536, 16, 128,
+                    offsets([8192] + [256] * 224), 1.0 / math.sqrt(128.0), "plain")
+
+
 def custom(name, lengths, H, d, structure="plain", seed=0, sm_scale=None):
     """Small ragged cases for parity tests."""
     cu = offsets(lengths)
@@ -123,6 +130,7 @@ WORKLOADS = {
     "onetoken131072": onetoken131072,
     "long131072": long131072,
     "long16384": long16384,
+    "skewed8192": skewed8192,
 }
 
 

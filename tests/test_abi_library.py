@@ -83,7 +83,7 @@ def test_host_side_argument_checks(cpu_lib):
                                               null, ctypes.byref(q), null, null) == 1
     # flags not supported (an unknown bit; static and dynamic scheduling at
     # once; the ordered dQ turns with the static schedule) / bad scale
-    for flags in (0x1000, 0x40 | 0x80):
+    for flags in (0x4000, 0x40 | 0x80, 0x800):  # the CTA-pair flag is the backward's
         assert cpu_lib.flamia_attn_fwd(ctypes.byref(q), ctypes.byref(q), ctypes.byref(q), null, 1,
                                        16, 1, 64, ctypes.c_float(0.1), flags, null, null, null,
                                        null, null) == 2
@@ -95,6 +95,13 @@ def test_host_side_argument_checks(cpu_lib):
                                    ctypes.byref(q), null, null, null, 1, 16, 1, 64,
                                    ctypes.c_float(-1.0), 0, null, null, null, null, null, 0, null,
                                    null) == 1
+    # the 2-CTA backward: not with head dim 64, the ordered dQ, query-row dS
+    # exponents, or the one-CTA flag
+    for d, flags in ((64, 0x800), (128, 0x800 | 0x8), (128, 0x800 | 0x100), (128, 0x800 | 0x1000)):
+        assert cpu_lib.flamia_attn_bwd(ctypes.byref(q), ctypes.byref(q), ctypes.byref(q),
+                                       ctypes.byref(q), null, null, null, 1, 16, 1, d,
+                                       ctypes.c_float(0.1), flags, null, null, null, null, null,
+                                       0, null, null) == 2
 
 
 def test_product_path_does_not_import_the_oracle():

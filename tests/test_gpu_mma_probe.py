@@ -131,3 +131,70 @@ def test_tmem_max_reducing_load(lib):
     torch.cuda.synchronize()
     assert np.array_equal(vals.cpu().numpy(), x)
     assert np.array_equal(mx.cpu().numpy(), x.max(axis=1))
+
+
+def _pair_inputs(shape, rng):
+    if shape == 0:
+        a, b = _codes_e4m3(rng, (2, 128, 128)), _codes_e4m3(rng, (2, 32, 128))
+        return a, b, None, None
+    if shape == 1:
+        a, b = _codes_e4m3(rng, (2, 128, 64)), _codes_e4m3(rng, (2, 64, 64))
+        sfa = rng.integers(120, 135, size=(2, 128, 2), dtype=np.uint8)
+        sfb = rng.integers(122, 133, size=(2,), dtype=np.uint8)
+        return a, b, sfa, sfb
+    a, b = _codes_e4m3(rng, (2, 256, 128)), _codes_e4m3(rng, (2, 256, 32))
+    sfa = rng.integers(122, 133, size=(2, 8), dtype=np.uint8)
+    sfb = rng.integers(120, 135, size=(2, 8), dtype=np.uint8)
+    return a, b, sfa, sfb
+
+
+def _pair_reference(shape, a, b, sfa, sfb):
+    """Per CTA r, the rows it holds: [(D_r, checked column range)]."""
+    out = []
+    for r in range(2):
+        if shape == 0:
+            B = O.e4m3_decode(np.concatenate([b[0], b[1]], axis=0))    # [64 N][128 K]
+            out.append((O.e4m3_decode(a[r]) @ B.T, slice(0, 64)))
+        elif shape == 1:
+            A = O.e4m3_decode(a[r]) * np.repeat(np.ldexp(1.0, sfa[r].astype(int) - 127), 32, axis=1)
+            B = O.e4m3_decode(np.concatenate([b[0], b[1]], axis=1))    # [64 K][128 N]
+            B = B * np.ldexp(1.0, np.repeat(sfb.astype(int) - 127, 32))[:, None]
+            out.append((A @ B, slice(0, 128)))
+        else:
+            A = O.e4m3_decode(a[r]).T * np.ldexp(1.0, np.repeat(sfa[r].astype(int) - 127, 32))[None, :]
+            B = O.e4m3_decode(b[r]) * np.ldexp(1.0, np.repeat(sfb[r].astype(int) - 127, 32))[:, None]
+            D = np.zeros((128, 64))
+            D[:, 32 * r:32 * r + 32] = A @ B
+            out.append((D, slice(32 * r, 32 * r + 32)))
+    return out
+
+
+def _pair_run(fl, shape, variant, a, b, sfa, sfb):
+    N = 128 if shape == 1 else 64
+    t = lambda z: torch.from_numpy(np.ascontiguousarray(z)).cuda()
+    d = torch.zeros((2, 128, N), dtype=torch.float32, device="cuda")
+    cols = torch.zeros(2, dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    fl.flamia_debug_pair_mma(shape, variant, t(a), t(b), t(sfa) if sfa is not None else None,
+                             t(sfb) if sfb is not None else None, d, cols, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    return d.cpu().numpy().astype(np.float64), cols.cpu().numpy()
+
+
+@pytest.mark.parametrize("shape", [0, 1, 2])
+def test_cta_pair_products(lib, shape):
+    """The three CTA-pair products of the 2-CTA backward (tcgen05 .cta_group::2;
+    review page sec. 3.4 "Backward pass": the pair splits 256 keys): S^T with
+    each CTA supplying half of the query columns, dV / dK with each supplying
+    half of the head-dimension columns, dQ^T over the pair's 256 keys with each
+    CTA keeping the columns it supplied.  Both CTAs see the same tensor-memory
+    columns, and each holds the 128 rows of its own A."""
+    from precision_causal_attention_block_gb300 import flamia as fl
+    rng = np.random.default_rng(40 + shape)
+    a, b, sfa, sfb = _pair_inputs(shape, rng)
+    got, cols = _pair_run(fl, shape, 0, a, b, sfa, sfb)
+    assert cols[0] == cols[1]
+    for r, (ref, cs) in enumerate(_pair_reference(shape, a, b, sfa, sfb)):
+        err = np.abs(got[r][:, cs] - ref[:, cs]).max() / np.abs(ref[:, cs]).max()
+        assert err <= 1e-5, (r, err)
