@@ -54,6 +54,7 @@ __device__ __forceinline__ void unpack8(const uint4& xv, float (&v)[8]) {
 // quantised by one launch: grid.y runs over the heads of tensor 0, then of
 // tensor 1, then of tensor 2, so one launch fills the GPU three times longer
 // and pays one tail.  f4codes[z] == nullptr: no NVFP4 copy for tensor z.
+// With D fused (one tensor, dO), map1 describes O's rows.
 struct QuantJob {
   uint8_t* codes[3];
   uint8_t* scales[3];
@@ -61,7 +62,9 @@ struct QuantJob {
   uint8_t* f4scales[3];
   int H[3];
   int n;
-  int blk;  // tokens per scale block: 32, or 1 (per-token operand scales)
+  int blk;    // tokens per scale block: 32, or 1 (per-token operand scales)
+  int ahead;  // CTAs resident at once: each CTA brings the rows of the CTA one
+              // wave ahead into L2, so HBM keeps streaming while waves compute
 };
 
 template <int DIM, bool HAD, bool FUSE_D>
@@ -111,6 +114,23 @@ __global__ void __launch_bounds__(kQThreads)
   if (tid == 0) {
     mbar_arrive_expect_tx(smem_u32(&s_bar), kQThreads * DIM * 2);
     tma_load_3d(smem_u32(s_x), map_x, smem_u32(&s_bar), 0, h, seg0);
+    // the rows of the CTA one wave ahead (same grid order: segment fastest)
+    const int nx = static_cast<int>(gridDim.x);
+    const int ahead = static_cast<int>(blockIdx.y) * nx + static_cast<int>(blockIdx.x) + job.ahead;
+    if (job.ahead > 0 && ahead < nx * static_cast<int>(gridDim.y)) {
+      int ha = ahead / nx, za = 0;
+      const int sa = (ahead % nx) * kSeg;
+      if (job.n > 1 && ha >= job.H[0]) {
+        ha -= job.H[0];
+        za = 1;
+        if (job.n > 2 && ha >= job.H[1]) {
+          ha -= job.H[1];
+          za = 2;
+        }
+      }
+      tma_prefetch_l2_3d(za == 0 ? &map0 : za == 1 ? &map1 : &map2, 0, ha, sa);
+      if (FUSE_D) tma_prefetch_l2_3d(&map1, 0, ha, sa);
+    }
   }
   const int chunk = lane % LPR;
   // D = dO . O: this lane's O chunks of its rows, loaded while the rows of
@@ -321,6 +341,8 @@ flamia_status launch_quantize(const void* const* xs, QuantJob& job, int T, int d
     rows += job.H[z];
   }
   for (int z = job.n; z < 3; ++z) maps[z] = maps[0];
+  // D fused: the second map describes O's rows (prefetched one wave ahead)
+  if (D != nullptr && !make_rows_map(&maps[1], o_bf16, T, job.H[0], d)) return FLAMIA_ERR_CUDA;
   if (rows > 65535) return FLAMIA_ERR_UNSUPPORTED;
   dim3 grid((T + kSeg - 1) / kSeg, rows);
   const bool fd = D != nullptr;
@@ -328,6 +350,10 @@ flamia_status launch_quantize(const void* const* xs, QuantJob& job, int T, int d
                               : fd ? quantize_kernel<128, false, true> : quantize_kernel<128, false, false>)
                        : (had ? quantize_kernel<64, true, false>
                               : fd ? quantize_kernel<64, false, true> : quantize_kernel<64, false, false>);
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kQThreads, 0) != cudaSuccess)
+    return FLAMIA_ERR_CUDA;
+  job.ahead = per_sm * num_sms();
   kern<<<grid, kQThreads, 0, s>>>(maps[0], maps[1], maps[2], T, cu, ndocs, job,
                                   static_cast<const uint4*>(o_bf16), D, dev_status);
   count_launches(1);
