@@ -228,7 +228,7 @@ def run_ours(args, rank, world, local):
             evb[i][0].record(stream)
             fl.flamia_attn_bwd_gqa(call.q, call.k, call.v, call.dout, call.D, call.lse, call.cu,
                                    call.T, call.H, call.H_kv, call.d, call.scale, call.wl,
-                                   call.dq, call.dk, call.dv, call.ws, call.flags,
+                                   call.dq, call.dk, call.dv, call.ws, call.bwd_flags,
                                    dev_status=call.status)
             evb[i][1].record(stream)
             ev[i][1].record(stream)

@@ -135,10 +135,9 @@ typedef enum {
                                        tile.  With neither flag the backward
                                        takes the measured rule, which picks
                                        one-CTA items on every shape (the pair
-                                       was as fast or slower everywhere it was
-                                       timed: packed 4 x 4096, variable-length
-                                       and skewed packings, non-causal,
-                                       grouped heads)                          */
+                                       measured about 1.5x slower on the
+                                       packed 4 x 4096 and variable-length
+                                       workloads)                              */
 
 /*
  * One quantised operand, all device pointers owned by the caller.

@@ -1149,10 +1149,10 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
   const long long grid = std::min<long long>(static_cast<long long>(L.cap_bwd) * Hkv, num_sms());
   if constexpr (DIM == 128 && !NVF4) {
     // two-CTA items when the caller asks for them; the rule by shape picks
-    // one-CTA items for every call (the pair measured as fast or slower on
-    // every shape: 4 x 4096 0.731 against 0.716 ms, non-causal 1.262 against
-    // 1.253, four K / V heads 0.778 against 0.762, the variable-length 65,536
-    // and the skewed 8,192 + 224 x 256 packings equal)
+    // one-CTA items for every call (the pair measured slower on every shape:
+    // 4 x 4096 1.064 against 0.716 ms, the variable-length 65,536 packing
+    // 8.50 against 5.60 ms: each 64-query tile hands its products, dS and
+    // dQ read-out between the two SMs four times, about 540 cycles a hop)
     const bool pair = ctas == 2 && bwd_pair_supported(prm);
     const cudaError_t e =
         pair ? launch_bwd128_pair(prm, q, k, v, dout, acc, stream)

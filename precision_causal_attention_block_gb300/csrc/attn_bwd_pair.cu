@@ -20,7 +20,7 @@
 // In the dQ^T product each CTA's A is the K of both CTAs (its own keys
 // first) and the B it supplies is dS^T of its 32 queries over the same 256
 // keys in the same order (its own rows written by itself, the other CTA's
-// rows written there through distributed shared memory); so the 32 columns a
+// rows copied there from the other CTA's shared memory); so the 32 columns a
 // CTA supplied hold dQ^T of its queries over all 256 keys (the other 32
 // columns mix the two orders and are never read).  Each CTA reads out and
 // reduce-adds dQ of its own 32 queries: one reduce-add per element and pair
@@ -30,6 +30,9 @@
 // (column base + row / 32), B's for all N columns (each tensor core forms all
 // N columns of its rows).  The 32 x 32 dS exponents of dQ^T's B come from
 // both CTAs: each sends the other its exponents for the other's 32 queries.
+// The other CTA's dS rows and exponents are written to a local staging buffer
+// and sent with one bulk copy per tile, which completes on the receiving
+// CTA's barrier: no generic-proxy writes cross the CTAs.
 //
 // Warp roles: warp 0 lane 0 the producer (the even CTA claims items and hands
 // each to the odd CTA through a mailbox in the odd CTA's shared memory; each
@@ -73,7 +76,9 @@ struct PairSmem {
   alignas(16) float dd[2][2][kQT];                 // D (0 outside)
   uint32_t qbyte[2][2][2], dobyte[2][2][2];        // [group][buffer][query block]
   uint32_t eds[2][2][4];                           // [group][query block][own key block]
-  uint32_t eds_peer[2][4];  // [group][other CTA's key block]: its exponents, this CTA's queries
+  alignas(256) uint8_t xs[2][kTile * kQH];        // staging of the other CTA's rows (its layout)
+  alignas(16) uint32_t xe[2][4];                   // staging of this CTA's exponents for its queries
+  alignas(16) uint32_t eds_peer[2][4];  // [group][other CTA's key block]: its exponents, this CTA's queries
   uint64_t bar_kv, bar_kv_peer, bar_kv_free;
   uint64_t bar_qd_full[kRing], bar_qd_peer[kRing], bar_qd_empty[kRing];
   uint64_t bar_s_full[2], bar_ds_full[2], bar_dq_full[2], bar_dq_read[2], bar_eds[2];
@@ -133,7 +138,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&sm.bar_ds_full[b]), 8);  // 4 warps of each CTA's group
       mbar_init(smem_u32(&sm.bar_dq_full[b]), 1);
       mbar_init(smem_u32(&sm.bar_dq_read[b]), 8);
-      mbar_init(smem_u32(&sm.bar_eds[b]), 4);      // the other CTA's group
+      mbar_init(smem_u32(&sm.bar_eds[b]), 1);      // own expect_tx + the other CTA's copy
     }
     mbar_init(smem_u32(&sm.bar_acc_full), 1);
     mbar_init(smem_u32(&sm.bar_acc_empty), 16);    // 8 compute warps of each CTA
@@ -181,7 +186,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       auto load_qd = [&](int h, int q0) -> bool {
         const int st = uc % kRing;
         if (uc >= kRing &&
-            (!mbar_wait_cl(smem_u32(&sm.bar_qd_empty[st]), ((uc / kRing) - 1) & 1) || sm.abort))
+            (!mbar_wait(smem_u32(&sm.bar_qd_empty[st]), ((uc / kRing) - 1) & 1) || sm.abort))
           return false;
         const uint32_t bf = smem_u32(&sm.bar_qd_full[st]);
         mbar_arrive_expect_tx(bf, kQDBytes);
@@ -235,7 +240,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         int u = 0;
         for (; u < pre && ok; ++u) ok = load_qd(tile_head(it, G, nt, u), tile_q0(it, G, nt, u));
         if (!ok) break;
-        if (nk > 0 && (!mbar_wait_cl(smem_u32(&sm.bar_kv_free), (nk - 1) & 1) || sm.abort)) {
+        if (nk > 0 && (!mbar_wait(smem_u32(&sm.bar_kv_free), (nk - 1) & 1) || sm.abort)) {
           ok = false;
           break;
         }
@@ -287,7 +292,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     if (!ok && lane == 0) abort_pair();
     // every product of the pair has completed before the tensor memory is freed
-    if (!mbar_wait_cl_w(smem_u32(&sm.bar_done), 0) && lane == 0) abort_pair();
+    if (!mbar_wait_w(smem_u32(&sm.bar_done), 0) && lane == 0) abort_pair();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (even CTA)
     {
@@ -306,7 +311,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       int nk = 0, ug = 0;
       bool ok = true;
       // S^T_t and dP^T_t into the tensor-memory half of tile t, once both
-      // CTAs' halves of Q_t / dO_t have landed
+      // CTAs' halves of Q_t / dO_t have landed (the odd CTA's phases, arrived
+      // from there with cluster-scope release, are waited at cluster scope)
       auto issue_sdp = [&](int t) -> bool {
         const int st = t % kRing, b = t & 1;
         if (!mbar_wait_w(smem_u32(&sm.bar_qd_full[st]), (t / kRing) & 1) ||
@@ -391,7 +397,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       if (!ok && lane == 0) abort_pair();
       tc_commit2_w(smem_u32(&sm.bar_done), 3);
-      if (!mbar_wait_cl_w(smem_u32(&sm.bar_done), 0) && lane == 0) abort_pair();
+      if (!mbar_wait_w(smem_u32(&sm.bar_done), 0) && lane == 0) abort_pair();
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ compute groups
@@ -433,15 +439,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     };
     // one arrive per warp, on the even CTA's barrier, after the warp's writes
+    // (cluster scope from the odd CTA only)
     auto warp_arrive_leader = [&](uint64_t* bar) {
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(at_leader(bar));
+      if (lane == 0) {
+        if (rank == 0) mbar_arrive(smem_u32(bar));
+        else mbar_arrive_cluster(at_leader(bar));
+      }
     };
     // `ok` stays uniform over each warp (the tensor-memory accesses and the
     // arrives are warp-wide): the abort flag and every wait are decided for
-    // the whole warp
+    // the whole warp.  These phases are completed by the tensor core (pair
+    // commits) or by the other CTA's bulk copy: CTA-scope waits
     auto wait_w = [&](uint64_t* bar, int parity) {
-      ok = __all_sync(0xffffffffu, ok && !sm.abort) && mbar_wait_cl_w(smem_u32(bar), parity);
+      ok = __all_sync(0xffffffffu, ok && !sm.abort) && mbar_wait_w(smem_u32(bar), parity);
     };
     for (int n = 0;; ++n) {
       if (issuer) sm.item_bc[g][n & 1] = ring_get(sm.ring, n, true);
@@ -485,6 +496,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int q0 = it.qs + tu * kQT, h = tile_head(it, G, nt, u);
         const int buf = ng & 1;
         if (u + 2 < nq) fetch_inputs(tile_hT(u + 2), tile_q0(it, G, nt, u + 2), e);
+        // this tile's rows and exponents from the other CTA arrive as one copy
+        if (issuer) mbar_arrive_expect_tx(smem_u32(&sm.bar_eds[g]), kTile * kQH + 16);
         wait_w(&sm.bar_s_full[g], ng & 1);
         tc_fence_after();
         uint8_t* pbrow = sm.pb[g] + j * kQT;
@@ -493,9 +506,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // the tile crosses or lies below this CTA's diagonal (keys 128 r + j)
         const bool masked = prm.causal && tu < 2 + 2 * r;
 #pragma unroll 1
-        for (int cc = 0; cc < 2 && ok; ++cc) {
-          // the other CTA's query block first: it waits for these exponents
+        for (int cc = 0; cc < 2; ++cc) {
+          // the other CTA's query block first: its rows and exponents travel
+          // while this CTA computes its own block
           const int c = cc ^ (1 - r);
+          if (ok) {
           const float fS = rowf * pow2_or_zero(static_cast<int>(sm.qbyte[g][buf][c]) - 127);
           const float fP = rowg * pow2_or_zero(static_cast<int>(sm.dobyte[g][buf][c]) - 127);
           uint32_t sv[32], dv[32];
@@ -532,30 +547,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4*>(dsrow + 16 * ch0) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
           *reinterpret_cast<uint4*>(dsrow + 16 * ch1) = make_uint4(dw[4], dw[5], dw[6], dw[7]);
           // dQ^T's operand: the same codes in query block c's CTA, row j there
-          // for its own keys, 128 + j for the other's (32-byte swizzle)
-          const int R = c == r ? j : kTile + j;
-          const int s32 = (R >> 2) & 1;
-          uint8_t* qrow = sm.dsq[g] + R * kQH;
-          const uint4 lo = make_uint4(dw[0], dw[1], dw[2], dw[3]);
-          const uint4 hi = make_uint4(dw[4], dw[5], dw[6], dw[7]);
-          if (c == r) {
-            *reinterpret_cast<uint4*>(qrow + 16 * s32) = lo;
-            *reinterpret_cast<uint4*>(qrow + 16 * (1 ^ s32)) = hi;
-            if (lane == 0) sm.eds[g][c][quad] = static_cast<uint32_t>(eb + 127);
-          } else {
-            st_cluster_v4(at_peer(qrow + 16 * s32), lo);
-            st_cluster_v4(at_peer(qrow + 16 * (1 ^ s32)), hi);
-            if (lane == 0) {
-              sm.eds[g][c][quad] = static_cast<uint32_t>(eb + 127);
-              st_cluster_u32(at_peer(&sm.eds_peer[g][quad]), static_cast<uint32_t>(eb + 127));
-              mbar_arrive_cluster(at_peer(&sm.bar_eds[g]));
+          // for its own keys, 128 + j for the other's (32-byte swizzle; the
+          // staging buffer holds the other CTA's rows 128 .. 255 in its layout)
+          const int s32 = (j >> 2) & 1;
+          uint8_t* qrow = c == r ? sm.dsq[g] + j * kQH : sm.xs[g] + j * kQH;
+          *reinterpret_cast<uint4*>(qrow + 16 * s32) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
+          *reinterpret_cast<uint4*>(qrow + 16 * (1 ^ s32)) = make_uint4(dw[4], dw[5], dw[6], dw[7]);
+          if (lane == 0) {
+            sm.eds[g][c][quad] = static_cast<uint32_t>(eb + 127);
+            if (c != r) sm.xe[g][quad] = static_cast<uint32_t>(eb + 127);
+          }
+          }
+          if (cc == 0) {
+            // the other CTA's rows 128 .. 255 of its dQ^T operand and the
+            // exponents of its query block are staged: one copy sends them
+            fence_proxy_async_smem();
+            named_barrier_sync(bar_id, kGroupThreads);
+            if (issuer && ok) {
+              bulk_copy_to_cluster(at_peer(sm.dsq[g] + kTile * kQH), smem_u32(sm.xs[g]),
+                                   kTile * kQH, at_peer(&sm.bar_eds[g]));
+              bulk_copy_to_cluster(at_peer(sm.eds_peer[g]), smem_u32(sm.xe[g]), 16,
+                                   at_peer(&sm.bar_eds[g]));
             }
           }
         }
+        fence_proxy_async_smem();
         // the group's previous reduce-add has read the staging buffer
         if (issuer) bulk_wait_group_read0();
         named_barrier_sync(bar_id, kGroupThreads);
-        // the other CTA's exponents for this CTA's queries
+        // the other CTA's copy to this one
         wait_w(&sm.bar_eds[g], ng & 1);
         if (ok) {
           const uint32_t qw = sm.qbyte[g][buf][0] | (sm.qbyte[g][buf][1] << 8) | 0x7F7F0000u;
@@ -591,8 +611,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tmem_st4(tmem + lane_off + col_p(g) + kSfDqB, w4);
           tmem_st_wait();
         }
-        fence_proxy_async_smem();
-        fence_proxy_async_cluster();
         tc_fence_before();
         if (ok) warp_arrive_leader(&sm.bar_ds_full[g]);
         if (u + 2 < nq) store_inputs(buf ^ 1);

@@ -568,20 +568,21 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cl_bar) {
                : "memory");
 }
 
-__device__ __forceinline__ void st_cluster_v4(uint32_t cl_addr, uint4 v) {
-  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(cl_addr), "r"(v.x),
-               "r"(v.y), "r"(v.z), "r"(v.w)
-               : "memory");
+// Bulk copy from this CTA's shared memory to the shared memory of a CTA of the
+// cluster (async proxy); the destination CTA's mbarrier (a shared::cluster
+// address) receives the bytes as transaction count.  Both addresses and the
+// size are multiples of 16 bytes.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cl, uint32_t src, uint32_t bytes,
+                                                     uint32_t bar_cl) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+      "[%3];" ::"r"(dst_cl),
+      "r"(src), "r"(bytes), "r"(bar_cl)
+      : "memory");
 }
 
 __device__ __forceinline__ void st_cluster_u32(uint32_t cl_addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cl_addr), "r"(v) : "memory");
-}
-
-// Generic-proxy writes to the shared memory of either CTA of the cluster
-// become visible to the tensor core's (async proxy) reads.
-__device__ __forceinline__ void fence_proxy_async_cluster() {
-  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
 }
 
 // As mbar_wait, acquiring at cluster scope (for phases completed by the other
