@@ -381,7 +381,8 @@ def run_ours(args, rank, world, local):
                      "traffic": None if (args.hadamard or args.noncausal or hkv != w.H or
                                          args.deterministic or args.dq_accum != "fp32" or
                                          args.schedule != "dynamic" or args.ds_rows or
-                                         args.token_scales)
+                                         args.token_scales or
+                                         (args.bwd_ctas == "pair" and w.d == 128))
                      else profiled_traffic(w, args.nvfp4),
                      "traffic_unit": "bytes per launch of the attention kernel (ncu, DRAM read + write)"},
         "e2e": {"value": round(e2e_value, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
