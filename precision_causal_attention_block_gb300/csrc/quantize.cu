@@ -32,6 +32,34 @@ __device__ __forceinline__ int doc_of(const int32_t* __restrict__ cu, int ndocs,
   return lo;
 }
 
+// The same document index found by a whole warp: each step the 32 lanes probe
+// 32 points inside [lo, hi) and keep the interval between the last probe
+// with cu <= t and the next, so a search over any number of documents takes
+// about four dependent loads (log_33).  Every step shrinks the interval, so
+// it ends on malformed offsets too (which the callers flag and clamp).
+__device__ __forceinline__ int warp_doc_of(const int32_t* __restrict__ cu, int ndocs, int t,
+                                           int lane) {
+  int lo = 0, hi = ndocs;
+  while (hi - lo > 1) {
+    const int span = hi - lo;
+    const int p = span <= 33 ? lo + 1 + lane : lo + ((lane + 1) * span) / 33;
+    const bool in = span <= 33 ? p < hi : true;
+    const unsigned below = __ballot_sync(0xffffffffu, in && __ldg(cu + p) <= t);
+    const int k = __popc(below);
+    const int last = k == 0 ? lo : __shfl_sync(0xffffffffu, p, k - 1);
+    const int next = __shfl_sync(0xffffffffu, p, min(k, 31));
+    hi = (k == 32 || (span <= 33 && k >= span - 1)) ? hi : next;
+    lo = last;
+  }
+  return lo;
+}
+
+// Offsets of the documents a CTA's staged rows can belong to, cached in
+// shared memory (one-token documents: about 160 of them), when the call has
+// more than kFewDocs documents.
+constexpr int kCuCache = 192;
+constexpr int kFewDocs = 64;
+
 // 2^e as a float for e in [-127, 127] (2^-127 is a subnormal).
 __device__ __forceinline__ float pow2f(int e) {
   return e >= -126 ? exp2i(e) : exp2i(-126) * 0.5f;
@@ -83,6 +111,8 @@ __global__ void __launch_bounds__(kQThreads)
   __shared__ float s_pre[kQThreads], s_suf[kQThreads];
   __shared__ int s_exp[kQThreads];
   __shared__ int s_bounds[2];
+  __shared__ int s_doc[2];
+  __shared__ int s_cu[kCuCache];
   __shared__ alignas(8) uint64_t s_bar;
 
   const int seg0 = blockIdx.x * kSeg;
@@ -153,15 +183,53 @@ __global__ void __launch_bounds__(kQThreads)
       report(dev_status, FLAMIA_DEV_BAD_SEQLENS);
   }
 
+  // Documents of the staged rows.  With many documents, warps 0 and 1 find
+  // those of the first and the last row, the offsets between them are cached
+  // in shared memory once, and each thread searches there (17 dependent
+  // loads per thread on 131,072 one-token documents otherwise); with a few,
+  // each thread's own search is shorter than the extra step.
+  int d0 = 0, nd = 0;
+  bool cached = false;
+  if (ndocs > kFewDocs) {  // uniform over the grid
+    const int tlast = min(seg0 + kQThreads, T) - 1;
+    if (warp < 2) {
+      const int d = warp_doc_of(cu, ndocs, warp == 0 ? seg0 : tlast, lane);
+      if (lane == 0) s_doc[warp] = d;
+    }
+    __syncthreads();
+    d0 = s_doc[0];
+    const int d1 = s_doc[1];
+    nd = d1 - d0 + 2;  // offsets cu[d0 .. d1 + 1]
+    cached = d1 >= d0 && nd <= kCuCache;
+    if (cached)
+      for (int i = tid; i < nd; i += kQThreads) s_cu[i] = __ldg(cu + d0 + i);
+    __syncthreads();
+  }
   // Block of this thread's token.
   const int t = seg0 + tid;
   int bs = 0, be = 0;
   if (t < T) {
-    const int b = doc_of(cu, ndocs, t);
+    int sraw, eraw;
+    if (cached) {
+      // s_cu[0] <= seg0 <= t < s_cu[nd - 1] for well-formed offsets: the
+      // same largest document with cu <= t as the search over all of them
+      int lo = 0, hi = nd - 1;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_cu[mid] <= t) lo = mid;
+        else hi = mid;
+      }
+      sraw = s_cu[lo];
+      eraw = s_cu[lo + 1];
+    } else {
+      const int b = doc_of(cu, ndocs, t);
+      sraw = __ldg(cu + b);
+      eraw = __ldg(cu + b + 1);
+    }
     // clamped so that malformed offsets (flagged above) cannot move any
     // index outside [t - 31, t + 31] and [0, T)
-    const int s = min(max(__ldg(cu + b), 0), t);
-    const int e = max(min(__ldg(cu + b + 1), T), t + 1);
+    const int s = min(max(sraw, 0), t);
+    const int e = max(min(eraw, T), t + 1);
     bs = s + ((t - s) & ~(job.blk - 1));
     be = min(bs + job.blk, e);
   }

@@ -42,6 +42,25 @@ def test_ragged_documents_bit_exact(lib, d, fmt):
         assert np.array_equal(out.nvfp4_codes.cpu().numpy(), pk)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_many_documents_per_segment(lib, d):
+    """Each CTA finds the documents of its rows with a warp-wide search and a
+    shared-memory copy of their offsets, or, when its rows span more
+    documents than the copy holds (here: runs of 300 empty documents), with a
+    per-token search: both give the codes of the oracle bit for bit, for
+    one-token documents too."""
+    # 1,100 tokens, 757 documents (at most T + 1); the rows staged by the
+    # CTA of tokens 128 .. 287 span about 380 of them
+    lens = [1] * 200 + [0] * 300 + [5, 1, 1] + [40] + [1] * 150 + [0] * 100 + [70, 33] + [600]
+    w = W.custom("manydocs", lens, 2, d, structure="outlier16x2", seed=8)
+    xs = W.make_inputs_bf16(w)
+    x = xs["q"]
+    out, D = run_quant(x, w.cu_seqlens, 0, o=xs["k"])
+    codes, sb = O.quantize_tokenblock(x.double().numpy(), w.cu_seqlens)
+    assert np.array_equal(out.codes.cpu().numpy(), codes)
+    assert np.array_equal(out.scales.cpu().numpy(), sb)
+
+
 def test_extreme_magnitudes_and_zeros(lib):
     w = W.custom("extreme", [40, 70, 1], 2, 64, seed=4)
     x = W.make_inputs_f32(w)["q"]
