@@ -16,7 +16,8 @@ pytestmark = pytest.mark.gpu
 EDGES = [0, 1, 2, 31, 32, 33, 63, 64, 65, 127, 128, 129, 255, 256, 257, 383, 384, 385]
 OPTIONS = [{}, {"causal": False}, {"nvfp4_qk": True}, {"hadamard": True},
            {"deterministic_dq": True}, {"dq_accum": "fp16_causal"},
-           {"dq_accum": "fp16_sequence", "causal": False}, {"schedule": "static"}]
+           {"dq_accum": "fp16_sequence", "causal": False}, {"schedule": "static"},
+           {"ds_rows": True}, {"token_scales": True}, {"bwd_ctas": "pair"}]
 
 
 def case(seed):
@@ -27,14 +28,18 @@ def case(seed):
     if sum(lengths) == 0:
         lengths.append(1)
     opts = dict(OPTIONS[seed % len(OPTIONS)])
-    d = 64 if opts.get("nvfp4_qk") else int(rng.choice([64, 128]))
+    d = int(rng.choice([64, 128]))
+    if opts.get("nvfp4_qk"):
+        d = 64
+    if opts.get("bwd_ctas") == "pair":  # the 2-CTA backward is head dim 128's
+        d = 128
     H = int(rng.choice([1, 2, 4]))
     Hkv = int(rng.choice([h for h in (1, 2, 4) if H % h == 0 and h <= H]))
     structure = str(rng.choice(["plain", "rms"]))
     return lengths, H, Hkv, d, structure, opts
 
 
-@pytest.mark.parametrize("seed", range(32))
+@pytest.mark.parametrize("seed", range(4 * len(OPTIONS)))
 def test_random_case_against_the_oracle(lib, seed):
     from precision_causal_attention_block_gb300 import flamia as fl
     lengths, H, Hkv, d, structure, opts = case(seed)
@@ -50,7 +55,8 @@ def test_random_case_against_the_oracle(lib, seed):
     ref = O.attention(*[x[n].double().numpy() for n in ("q", "k", "v", "do")], w.cu_seqlens,
                       w.sm_scale, qk_format="nvfp4" if opts.get("nvfp4_qk") else "mxfp8",
                       causal=opts.get("causal", True), hadamard=opts.get("hadamard", False),
-                      dq_accum=opts.get("dq_accum", "fp32"))
+                      dq_accum=opts.get("dq_accum", "fp32"), ds_rows=opts.get("ds_rows", False),
+                      group="token" if opts.get("token_scales") else "block")
     what = f"case {lengths} H={H} H_kv={Hkv} d={d} {structure} {opts}"
     rel = 3e-2 if opts.get("hadamard") else 2e-2
     for n, t in (("O", call.o), ("dQ", call.dq), ("dK", call.dk), ("dV", call.dv)):
