@@ -71,14 +71,17 @@ struct BwdSmem {
   // loaded while the current one is processed)
   alignas(16) float nl[2][kTile];  // 8 - lse2 of each query column (-inf outside the document)
   alignas(16) float dd[2][kTile];  // D of each query column (0 outside)
-  // FP16 dQ: prescale 2^p of each query (0 outside); three buffers, since a
-  // tile's dQ is staged while the next tile is computed
-  alignas(16) float pf[3][kTile];
+  // FP16 dQ: prescale 2^p of each query (0 outside); four buffers: written a
+  // tile ahead, and a tile's dQ is staged during the next tile, after the
+  // compute threads' arrival on bar_tile of that tile
+  alignas(16) float pf[4][kTile];
   // per-token operand scales, per query and tile parity: 2^eQ, 2^eD (dO),
   // 2^(eD - EdO) (dV's fold), 2^(eQ - EQ) (dK's fold); EQ, EdO the query
   // block's largest exponents
   alignas(16) float tq[OPT && !NVF4 ? 4 : 1][2][OPT && !NVF4 ? kTile : 4];
-  uint32_t qbyte[2][4], dobyte[2][4];  // E8M0 bytes of the 4 query blocks of Q and dO
+  // E8M0 bytes of the 4 query blocks of Q and dO, three buffers (written a
+  // tile ahead; read for the block scales after the wait on bar_tile)
+  uint32_t qbyte[3][4], dobyte[3][4];
   // by tile parity (a fast warp may start the next tile's recompute while a
   // slow one still reads this tile's to write the block scales)
   uint32_t eds[2][4][4];         // dS block bytes [query block][key block]
@@ -89,6 +92,9 @@ struct BwdSmem {
   uint64_t bar_s_full, bar_sdp_read, bar_ds_full, bar_dq_full, bar_dq_read, bar_done, bar_sf;
   uint64_t bar_staged, bar_stage_free;  // dQ staging: compute groups <-> reducer warp
   uint64_t bar_kv_free, bar_acc_full, bar_acc_empty;
+  // once per query tile: every compute thread has written its dS block bytes
+  // and the next tile's per-query inputs
+  uint64_t bar_tile;
   ItemRing<4> ring;  // claimed items: producer -> MMA issuer, compute leader
   int item_bc[2];    // the compute leader's copy for the compute groups
   unsigned long long dscnt[2];  // dS rounded-to-zero diagnostic of this CTA
@@ -159,6 +165,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(smem_u32(&sm.bar_stage_free), 1);
     mbar_init(smem_u32(&sm.bar_acc_full), 1);
     mbar_init(smem_u32(&sm.bar_acc_empty), kComputeThreads);
+    mbar_init(smem_u32(&sm.bar_tile), kComputeThreads);
     mbar_init(smem_u32(&sm.bar_done), 1);
     mbar_init(smem_u32(&sm.bar_sf), kTile);
     ring_init(sm.ring, 3);  // the MMA issuer, the compute leader, the dQ reducer
@@ -455,7 +462,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (OPT && prm.dq_pre != nullptr) {
         // x 2^p of the query row (0 outside the document), rounded to FP16,
         // in DIM / 64 boxes [128 query rows][64 halves], 128B-swizzled
-        const float pf = sm.pf[tg % 3][j];
+        const float pf = sm.pf[tg & 3][j];
         __half* box0 = reinterpret_cast<__half*>(sm.dqs[0]);
 #pragma unroll
         for (int t = 0; t < 4 * kCh; ++t) {  // 8-dim chunk t of this group's dims
@@ -554,10 +561,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
       };
       auto store_query_inputs = [&](int tg) {
-        const int b = tg & 1;
+        const int b = tg & 1, b3 = tg % 3;
         sm.nl[b][j] = r_qv ? 8.f - r_lse * LOG2E : -INFINITY;
         sm.dd[b][j] = r_qv ? r_dd : 0.f;
-        if (OPT) sm.pf[tg % 3][j] = r_qv ? exp2i(r_pre) : 0.f;
+        if (OPT) sm.pf[tg & 3][j] = r_qv ? exp2i(r_pre) : 0.f;
         if constexpr (OPT && !NVF4) {
           if (prm.token) {
             // per-token operand scales: this query's factors and its block's
@@ -571,15 +578,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             sm.tq[2][b][j] = r_qv ? pow2_or_zero(edb - ED) : 0.f;
             sm.tq[3][b][j] = r_qv ? pow2_or_zero(eqb - EQ) : 0.f;
             if (lane == 0) {
-              sm.qbyte[b][quad] = static_cast<uint32_t>(EQ);
-              sm.dobyte[b][quad] = static_cast<uint32_t>(ED);
+              sm.qbyte[b3][quad] = static_cast<uint32_t>(EQ);
+              sm.dobyte[b3][quad] = static_cast<uint32_t>(ED);
             }
             return;
           }
         }
         if (lane == 0) {
-          sm.qbyte[b][quad] = r_qv ? r_qb : 127u;
-          sm.dobyte[b][quad] = r_qv ? r_dob : 127u;
+          sm.qbyte[b3][quad] = r_qv ? r_qb : 127u;
+          sm.dobyte[b3][quad] = r_qv ? r_dob : 127u;
         }
       };
       if (g == 0) {
@@ -588,7 +595,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       named_barrier_sync(1, kComputeThreads);
       for (int u = 0; u < nq; ++u, ++uc) {
-        const int ub = uc & 1;
+        const int ub = uc & 1, ub3 = uc % 3;
         if (g == 0 && u + 1 < nq) fetch_query_inputs(u + 1);  // lands during this tile
         ok = ok && !sm.abort && mbar_wait(smem_u32(&sm.bar_s_full), uc & 1);
         tc_fence_after();
@@ -598,8 +605,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int cc = 0; cc < 2 && ok; ++cc) {
           const int c = 2 * g + cc;  // 32-query block of this chunk
           const float fS =
-              NVF4 ? rowf : rowf * pow2_or_zero(static_cast<int>(sm.qbyte[ub][c]) - 127);
-          const float fP = rowg * pow2_or_zero(static_cast<int>(sm.dobyte[ub][c]) - 127);
+              NVF4 ? rowf : rowf * pow2_or_zero(static_cast<int>(sm.qbyte[ub3][c]) - 127);
+          const float fP = rowg * pow2_or_zero(static_cast<int>(sm.dobyte[ub3][c]) - 127);
           uint32_t sv[32], dv[32];
           tmem_ld32(tmem + lane_off + kColSP + 32 * c, sv);
           tmem_ld32(tmem + lane_off + kColDP + 32 * c, dv);
@@ -704,11 +711,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             *reinterpret_cast<uint4*>(ds2row + 16 * ch1) = make_uint4(dr[4], dr[5], dr[6], dr[7]);
           }
         }
-        // the next tile's per-query inputs (their nl / dd / byte buffer was last
-        // read by tile t-1, the prescale buffer by tile t-2's staging), visible
-        // after the barrier, which also completes the dS block exponents
+        // the next tile's per-query inputs (their nl / dd buffer was last read
+        // by tile t-1's recompute, the byte buffer by tile t-2's block scales,
+        // the prescale buffer by tile t-3's staging), visible after the wait on
+        // bar_tile, which also completes the dS block exponents.  Split
+        // arrive / wait: the previous tile's dQ is read out in between, so a
+        // fast warp does that instead of waiting for the slowest one.  Every
+        // compute thread arrives once per tile, whatever happened.
         if (g == 0 && u + 1 < nq) store_query_inputs(uc + 1);
-        named_barrier_sync(1, kComputeThreads);
+        mbar_arrive(smem_u32(&sm.bar_tile));
+        // dQ of the previous tile, computed while this tile was recomputed
+        if (u > 0) read_dq(it, u - 1, uc - 1);
+        ok = ok && !sm.abort && mbar_wait(smem_u32(&sm.bar_tile), uc & 1);
         if (ok) {
           // block scales of the three products (this tile's parity buffer,
           // last read by the products of tile t-2, complete before tile t's
@@ -717,8 +731,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           const uint32_t sfc = col_sf(uc);
           uint32_t w[8];
           if (g == 0) {
-            const uint32_t* db = sm.dobyte[ub];
-            const uint32_t* qb = sm.qbyte[ub];
+            const uint32_t* db = sm.dobyte[ub3];
+            const uint32_t* qb = sm.qbyte[ub3];
             const uint32_t dow = db[0] | (db[1] << 8) | (db[2] << 16) | (db[3] << 24);
             const uint32_t qw = qb[0] | (qb[1] << 8) | (qb[2] << 16) | (qb[3] << 24);
 #pragma unroll
@@ -753,8 +767,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tmem_st8(tmem + lane_off + sfc + kSfDqA, w);
           }
         }
-        // dQ of the previous tile, computed while this tile was recomputed
-        if (u > 0) read_dq(it, u - 1, uc - 1);
         if (ok) {
           tmem_st_wait();
           fence_proxy_async_smem();
