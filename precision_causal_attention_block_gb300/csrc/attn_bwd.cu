@@ -275,9 +275,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       // tile t-1's S^T / dP^T columns
       auto issue_sdp = [&](int t) -> bool {
         const int st = t % kBStages;
-        if (!mbar_wait_w(smem_u32(&sm.bar_qd_full[st]), (t / kBStages) & 1) ||
-            (t > 0 && !mbar_wait_w(smem_u32(&sm.bar_sdp_read), (t - 1) & 1)) ||
-            __any_sync(0xffffffffu, sm.abort))
+        if (!mbar_wait_w_ab(smem_u32(&sm.bar_qd_full[st]), (t / kBStages) & 1, &sm.abort) ||
+            (t > 0 && !mbar_wait_w_ab(smem_u32(&sm.bar_sdp_read), (t - 1) & 1, &sm.abort)))
           return false;
         tc_fence_after();
         const uint64_t dq = dq0 + st * kStep, ddo = ddo0 + st * kStep;
@@ -327,9 +326,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           // dV / dK restart from zero on an item's first tile: the previous
           // item's epilogue must have read them
-          if (!mbar_wait_w(smem_u32(&sm.bar_ds_full), uc & 1) ||
-              (u == 0 && nk > 1 && !mbar_wait_w(smem_u32(&sm.bar_acc_empty), (nk - 2) & 1)) ||
-              __any_sync(0xffffffffu, sm.abort)) {
+          if (!mbar_wait_w_ab(smem_u32(&sm.bar_ds_full), uc & 1, &sm.abort) ||
+              (u == 0 && nk > 1 &&
+               !mbar_wait_w_ab(smem_u32(&sm.bar_acc_empty), (nk - 2) & 1, &sm.abort))) {
             ok = false;
             break;
           }
@@ -349,8 +348,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tc_commit_w(smem_u32(&sm.bar_qd_empty[st]));
           // dQ_t = dS K into its own columns, once the groups have read dQ_{t-1}:
           // A = the same dS bytes read MN-major (M = queries), B = K MN-major
-          if (uc > 0 && (!mbar_wait_w(smem_u32(&sm.bar_dq_read), (uc - 1) & 1) ||
-                         __any_sync(0xffffffffu, sm.abort))) {
+          if (uc > 0 && !mbar_wait_w_ab(smem_u32(&sm.bar_dq_read), (uc - 1) & 1, &sm.abort)) {
             ok = false;
             break;
           }
@@ -445,8 +443,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // arrives on dq_read, then on staged).  The buffer is free once the
     // reducer's bulk copies of the previous tile have read it.
     auto read_dq = [&](const BwdItem& it, int ut, int tg) {
-      ok = ok && !sm.abort && mbar_wait(smem_u32(&sm.bar_dq_full), tg & 1) &&
-           (tg == 0 || mbar_wait(smem_u32(&sm.bar_stage_free), (tg - 1) & 1));
+      ok = ok && mbar_wait_ab(smem_u32(&sm.bar_dq_full), tg & 1, &sm.abort) &&
+           (tg == 0 || mbar_wait_ab(smem_u32(&sm.bar_stage_free), (tg - 1) & 1, &sm.abort));
       tc_fence_after();
       if (!ok) return;
       const bool qv = tile_q0(it, ut) + j < it.e;  // TMEM lane j of dQ_t is query row j
@@ -597,7 +595,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int u = 0; u < nq; ++u, ++uc) {
         const int ub = uc & 1, ub3 = uc % 3;
         if (g == 0 && u + 1 < nq) fetch_query_inputs(u + 1);  // lands during this tile
-        ok = ok && !sm.abort && mbar_wait(smem_u32(&sm.bar_s_full), uc & 1);
+        ok = ok && mbar_wait_ab(smem_u32(&sm.bar_s_full), uc & 1, &sm.abort);
         tc_fence_after();
         uint8_t* pbrow = sm.pb[ub] + j * kTile;
         uint8_t* dsrow = sm.ds[ub] + j * kTile;
@@ -722,7 +720,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_arrive(smem_u32(&sm.bar_tile));
         // dQ of the previous tile, computed while this tile was recomputed
         if (u > 0) read_dq(it, u - 1, uc - 1);
-        ok = ok && !sm.abort && mbar_wait(smem_u32(&sm.bar_tile), uc & 1);
+        ok = ok && mbar_wait_ab(smem_u32(&sm.bar_tile), uc & 1, &sm.abort);
         if (ok) {
           // block scales of the three products (this tile's parity buffer,
           // last read by the products of tile t-2, complete before tile t's

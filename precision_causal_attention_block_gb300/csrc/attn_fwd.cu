@@ -374,7 +374,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // S_t issued before (its s_read arrivals)
       auto wait_s_read = [&](int t) -> bool {
         while (s_read_seen[t] < s_issued[t]) {
-          if (!mbar_wait_w(smem_u32(&sm.bar_s_read[t]), s_read_seen[t] & 1)) return false;
+          if (!mbar_wait_w_ab(smem_u32(&sm.bar_s_read[t]), s_read_seen[t] & 1, &sm.abort))
+            return false;
           ++s_read_seen[t];
         }
         return true;
@@ -448,7 +449,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
               }
               kv_ready = jk + 2;
             }
-            if (!wait_s_read(t) || __any_sync(0xffffffffu, sm.abort)) {
+            if (!wait_s_read(t)) {
               ok = false;
               break;
             }
@@ -458,8 +459,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           for (int t = 0; t < 2 && ok; ++t) {
             const int nt = t == 0 ? it.n0 : it.n1;
             if (j >= nt) continue;
-            if (!mbar_wait_w(smem_u32(&sm.bar_p_full[t]), p_seen[t] & 1) ||
-                __any_sync(0xffffffffu, sm.abort)) {
+            if (!mbar_wait_w_ab(smem_u32(&sm.bar_p_full[t]), p_seen[t] & 1, &sm.abort)) {
               ok = false;
               break;
             }
@@ -489,8 +489,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           for (int t = 0; t < 2 && ok; ++t) {
             const int nt = t == 0 ? it.n0 : it.n1;
             if (j >= nt) continue;
-            if (!mbar_wait_w(smem_u32(&sm.bar_p_full[t]), p_seen[t] & 1) ||
-                __any_sync(0xffffffffu, sm.abort)) {
+            if (!mbar_wait_w_ab(smem_u32(&sm.bar_p_full[t]), p_seen[t] & 1, &sm.abort)) {
               ok = false;
               break;
             }
@@ -650,7 +649,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         for (int kb = 0; kb < 4; ++kb)  // c_row 2^(byte - 127); byte 0 gives 0
           cf[kb] = c_row * __int_as_float(((kword >> (8 * kb)) & 0xFFu) << 23);
         fetch_scales(j + 1);  // in flight while this tile is processed
-        if (!mbar_wait(smem_u32(&sm.bar_s_full[t]), s_seen & 1) || sm.abort) {
+        if (!mbar_wait_ab(smem_u32(&sm.bar_s_full[t]), s_seen & 1, &sm.abort)) {
           ok = false;
           break;
         }
@@ -724,7 +723,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const float moff = m - 8.f;  // P8 = 2^8 exp2(s - m)
         // head dim 64: P^_t's columns are free once the previous P^_t V has read them
         if (kSep && j > 0) {
-          if (!mbar_wait(smem_u32(&sm.bar_pv_done[t]), pv_seen & 1) || sm.abort) {
+          if (!mbar_wait_ab(smem_u32(&sm.bar_pv_done[t]), pv_seen & 1, &sm.abort)) {
             ok = false;
             break;
           }
@@ -817,7 +816,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         mbar_arrive(smem_u32(&sm.bar_p_full[t]));
       }
       if (nt > 0 && ok) {
-        if (!mbar_wait(smem_u32(&sm.bar_o_full[t]), o_seen & 1) || sm.abort) ok = false;
+        if (!mbar_wait_ab(smem_u32(&sm.bar_o_full[t]), o_seen & 1, &sm.abort)) ok = false;
         ++o_seen;
         // head dim 64: the item's last P^_t V (complete with O_t) consumes its phase
         if (kSep && ok) {

@@ -97,6 +97,28 @@ __device__ __forceinline__ bool mbar_wait_w(uint32_t bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
+// mbar_wait that also gives up once *abort is set (another role of the CTA
+// unwinding).  The flag is read only while the phase is incomplete, so a
+// completed phase costs one try_wait and no extra shared-memory round trip.
+__device__ __forceinline__ bool mbar_wait_ab(uint32_t bar, uint32_t parity,
+                                             const volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > kWaitTimeoutNs) return false;
+  }
+}
+
+// The same for every lane of a converged warp, with one outcome for the warp.
+__device__ __forceinline__ bool mbar_wait_w_ab(uint32_t bar, uint32_t parity,
+                                               const volatile int* abort) {
+  return __all_sync(0xffffffffu, mbar_wait_ab(bar, parity, abort));
+}
+
 // ------------------------------------------------------------------ item ring
 // Work items claimed by a CTA's producer thread are handed to the CTA's other
 // roles in claim order through a small shared-memory ring: item number n
