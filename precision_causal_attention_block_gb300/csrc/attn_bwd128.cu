@@ -233,10 +233,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // S^T_t and dP^T_t into the tensor-memory half of tile t
       auto issue_sdp = [&](int t) -> bool {
         const int st = t % kRing, b = t & 1;
-        if (!mbar_wait_w(smem_u32(&sm.bar_qd_full[st]), (t / kRing) & 1)) return false;
+        if (!mbar_wait_w_ab(smem_u32(&sm.bar_qd_full[st]), (t / kRing) & 1, &sm.abort))
+          return false;
         // the half's previous tile (t - 2) has had its dQ^T read out
-        if (t >= 2 && !mbar_wait_w(smem_u32(&sm.bar_dq_read[b]), ((t >> 1) - 1) & 1)) return false;
-        if (__any_sync(0xffffffffu, sm.abort)) return false;
+        if (t >= 2 &&
+            !mbar_wait_w_ab(smem_u32(&sm.bar_dq_read[b]), ((t >> 1) - 1) & 1, &sm.abort))
+          return false;
         tc_fence_after();
         const uint64_t dq = dq0 + st * kQStep, ddo = ddo0 + st * kQStep;
 #pragma unroll
@@ -267,9 +269,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int t = ug + u, b = t & 1, st = t % kRing;
           // dV / dK restart from zero on an item's first tile: the previous
           // item's epilogue must have read them
-          if (!mbar_wait_w(smem_u32(&sm.bar_ds_full[b]), (t >> 1) & 1) ||
-              (u == 0 && nk > 0 && !mbar_wait_w(smem_u32(&sm.bar_acc_empty), (nk - 1) & 1)) ||
-              __any_sync(0xffffffffu, sm.abort)) {
+          if (!mbar_wait_w_ab(smem_u32(&sm.bar_ds_full[b]), (t >> 1) & 1, &sm.abort) ||
+              (u == 0 && nk > 0 &&
+               !mbar_wait_w_ab(smem_u32(&sm.bar_acc_empty), (nk - 1) & 1, &sm.abort))) {
             ok = false;
             break;
           }
@@ -421,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q0 = it.qs + tu * kQT, h = tile_head(it, G, nt, u);
         const int buf = ng & 1;
         if (u + 2 < nq) fetch_inputs(tile_hT(u + 2), tile_q0(it, G, nt, u + 2), e);  // lands during this tile
-        ok = ok && !sm.abort && mbar_wait(smem_u32(&sm.bar_s_full[g]), ng & 1);
+        ok = ok && mbar_wait_ab(smem_u32(&sm.bar_s_full[g]), ng & 1, &sm.abort);
         tc_fence_after();
         uint8_t* pbrow = sm.pb[g] + j * kQT;
         uint8_t* dsrow = sm.ds[g] + j * kQT;
@@ -577,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the next tile's inputs go to the other buffer (last read by the
         // group's previous tile, before its final barrier)
         if (u + 2 < nq) store_inputs(buf ^ 1);
-        ok = ok && !sm.abort && mbar_wait(smem_u32(&sm.bar_dq_full[g]), ng & 1);
+        ok = ok && mbar_wait_ab(smem_u32(&sm.bar_dq_full[g]), ng & 1, &sm.abort);
         tc_fence_after();
         if (ok) {
           uint32_t v0[32], v1[32];

@@ -448,11 +448,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     };
     // `ok` stays uniform over each warp (the tensor-memory accesses and the
-    // arrives are warp-wide): the abort flag and every wait are decided for
-    // the whole warp.  These phases are completed by the tensor core (pair
+    // arrives are warp-wide): every wait (which gives up once the abort flag
+    // is set) is decided for the whole warp.  These phases are completed by the tensor core (pair
     // commits) or by the other CTA's bulk copy: CTA-scope waits
     auto wait_w = [&](uint64_t* bar, int parity) {
-      ok = __all_sync(0xffffffffu, ok && !sm.abort) && mbar_wait_w(smem_u32(bar), parity);
+      ok = __all_sync(0xffffffffu, ok) && mbar_wait_w_ab(smem_u32(bar), parity, &sm.abort);
     };
     for (int n = 0;; ++n) {
       if (issuer) sm.item_bc[g][n & 1] = ring_get(sm.ring, n, true);
