@@ -1159,10 +1159,10 @@ flamia_status launch_bwd(const flamia_qtensor* q, const flamia_qtensor* k,
   const long long grid = std::min<long long>(static_cast<long long>(L.cap_bwd) * Hkv, num_sms());
   if constexpr (DIM == 128 && !NVF4) {
     // two-CTA items when the caller asks for them; the rule by shape picks
-    // one-CTA items for every call (the pair measured slower on every shape:
-    // 4 x 4096 1.064 against 0.716 ms, the variable-length 65,536 packing
-    // 8.50 against 5.60 ms: each 64-query tile hands its products, dS and
-    // dQ read-out between the two SMs four times, about 540 cycles a hop)
+    // one-CTA items for every call (the pair measured about 1.5x slower on
+    // every shape, 4 x 4096 and the variable-length 65,536 packing: each
+    // 64-query tile hands its products, dS and dQ read-out between the two
+    // SMs four times, about 540 cycles a hop)
     const bool pair = ctas == 2 && bwd_pair_supported(prm);
     const cudaError_t e =
         pair ? launch_bwd128_pair(prm, q, k, v, dout, acc, stream)
