@@ -10,16 +10,10 @@
 // belong to few heads and stay in L2.  Warp roles:
 //   warp 0       TMA producer: K, V per item; Q, dO tiles through a 3-stage ring.
 //   warp 1       tensor-memory owner and single-thread tcgen05 MMA issuer.
-//   warp 2       dQ reducer: one thread issues the bulk reduce-adds.
 //   warps 4-7    compute group 0: query columns 0..63 of every tile
 //   warps 8-11   compute group 1: query columns 64..127
-//                (thread = key row of S^T / dP^T)
-//   warps 12-15  helpers (one per tensor-memory lane quadrant): the block
-//                scales of each tile's products, and the dQ_t read-out and
-//                staging (thread = query row of dQ_t).
-// The compute warps only arrive on the per-tile exchange of dS exponents and
-// go on to the next tile; the helpers wait on it.  Registers are split by
-// warpgroup (setmaxnreg): the compute warps hold a tile's S^T / dP^T rows.
+//   (thread = key row of S^T / dP^T; for the dQ partial thread = query row,
+//   the two groups splitting the head dimension).
 // Per query tile t:
 //   S^T = K Q^T and dP^T = V dO^T (unscaled E4M3, f32 in TMEM);
 //   the compute groups recompute P = exp2(s - lse2) with the forward's
@@ -34,9 +28,9 @@
 // groups signal as soon as they have loaded the last S^T / dP^T columns of
 // tile t into registers, and S^T / dP^T of tile t+1 are issued then, while
 // the groups still turn tile t into P^b and dS; the products of tile t run
-// while the groups compute tile t+1, and the helpers read dQ_t out meanwhile
-// (the P^b / dS payloads and the block scales are double-buffered by tile
-// parity).
+// while the groups compute tile t+1, which reads dQ_t out after its own
+// recompute (the P^b / dS payloads and the block scales are double-buffered
+// by tile parity).
 // Tensor memory (512 columns): S^T [0,128), dP^T [128,256), dV [256,320),
 // dK [320,384), the NVFP4 score scales [384,396), the block scales of the
 // products of even / odd tiles [400,424) / [424,448), dQ_t [448,512).
@@ -48,16 +42,8 @@ namespace flamia {
 namespace {
 
 constexpr int kBStages = 3;
-constexpr int kBwdThreads = 512;
+constexpr int kBwdThreads = 384;
 constexpr int kComputeThreads = 256;
-constexpr int kHelperThreads = 128;
-// Registers per thread of each warpgroup after the split (the launch gives
-// 128 to each of the 512 threads: 65,536; the split takes 128 x 56 + 128 x 88
-// + 256 x 176 = 63,488 of them)
-constexpr int kRegsCtl = 56, kRegsHelper = 88, kRegsCompute = 176;
-static_assert(128 * kRegsCtl + kHelperThreads * kRegsHelper + kComputeThreads * kRegsCompute <=
-                  kBwdThreads * 128,
-              "backward register split");
 constexpr uint32_t kColSP = 0, kColDP = 128, kColDV = 256, kColDQ = 448;
 // block-scale columns of a tile's products, by tile parity
 constexpr uint32_t kColSf = 400;
@@ -81,34 +67,36 @@ struct BwdSmem {
   alignas(1024) float dqs[DIM / 32][kTile * 32];
   alignas(NVF4 ? 1024 : 16) uint8_t k4[kTile4Bytes];
   alignas(NVF4 ? 1024 : 16) uint8_t q4[kBStages][kTile4Bytes];
-  // per-query inputs of each compute warp's 64 query columns, by tile parity
-  // (each warp keeps its own copy, written a tile ahead: no exchange between
-  // warps): 8 - lse2 (-inf outside the document) and D (0 outside)
-  alignas(16) float nlw[8][2][64];
-  alignas(16) float ddw[8][2][64];
-  // per-token operand scales, per warp, query and tile parity: 2^eQ, 2^eD
-  // (dO), 2^(eD - EdO) (dV's fold), 2^(eQ - EQ) (dK's fold); EQ, EdO the
-  // query block's largest exponents
-  alignas(16) float tqw[OPT && !NVF4 ? 4 : 1][8][2][OPT && !NVF4 ? 64 : 4];
+  // per-query-tile inputs, double-buffered by tile parity (the next tile's are
+  // loaded while the current one is processed)
+  alignas(16) float nl[2][kTile];  // 8 - lse2 of each query column (-inf outside the document)
+  alignas(16) float dd[2][kTile];  // D of each query column (0 outside)
+  // FP16 dQ: prescale 2^p of each query (0 outside); four buffers: written a
+  // tile ahead, and a tile's dQ is staged during the next tile, after the
+  // compute threads' arrival on bar_tile of that tile
+  alignas(16) float pf[4][kTile];
+  // per-token operand scales, per query and tile parity: 2^eQ, 2^eD (dO),
+  // 2^(eD - EdO) (dV's fold), 2^(eQ - EQ) (dK's fold); EQ, EdO the query
+  // block's largest exponents
+  alignas(16) float tq[OPT && !NVF4 ? 4 : 1][2][OPT && !NVF4 ? kTile : 4];
+  // E8M0 bytes of the 4 query blocks of Q and dO, three buffers (written a
+  // tile ahead; read for the block scales after the wait on bar_tile)
+  uint32_t qbyte[3][4], dobyte[3][4];
   // by tile parity (a fast warp may start the next tile's recompute while a
-  // helper still reads this tile's to write the block scales)
+  // slow one still reads this tile's to write the block scales)
   uint32_t eds[2][4][4];         // dS block bytes [query block][key block]
   uint8_t erow[2][4][4][32];     // query-row dS bytes [query block][key block][query]
   uint64_t bar_kv;
   uint64_t bar_qd_full[kBStages];
   uint64_t bar_qd_empty[kBStages];
-  uint64_t bar_s_full, bar_sdp_read, bar_dq_full, bar_dq_read, bar_done, bar_sf;
-  // by tile parity: the helpers have written tile t's block scales (and the
-  // compute warps its payloads)
-  uint64_t bar_ds_full[2];
-  uint64_t bar_staged, bar_stage_free;  // dQ staging: helpers <-> reducer warp
+  uint64_t bar_s_full, bar_sdp_read, bar_ds_full, bar_dq_full, bar_dq_read, bar_done, bar_sf;
+  uint64_t bar_staged, bar_stage_free;  // dQ staging: compute groups <-> reducer warp
   uint64_t bar_kv_free, bar_acc_full, bar_acc_empty;
-  // by tile parity: every compute thread has written tile t's dS payloads
-  // and block bytes (the helpers wait for it)
-  uint64_t bar_tile[2];
-  ItemRing<4> ring;  // claimed items: producer -> MMA issuer, compute leader, reducer, helpers
+  // once per query tile: every compute thread has written its dS block bytes
+  // and the next tile's per-query inputs
+  uint64_t bar_tile;
+  ItemRing<4> ring;  // claimed items: producer -> MMA issuer, compute leader
   int item_bc[2];    // the compute leader's copy for the compute groups
-  int item_bh[2];    // the helper leader's copy for the helpers
   unsigned long long dscnt[2];  // dS rounded-to-zero diagnostic of this CTA
   uint32_t tmem_base;
   volatile int abort;
@@ -170,20 +158,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     mbar_init(smem_u32(&sm.bar_s_full), 1);
     mbar_init(smem_u32(&sm.bar_sdp_read), kComputeThreads);
+    mbar_init(smem_u32(&sm.bar_ds_full), kComputeThreads);
     mbar_init(smem_u32(&sm.bar_dq_full), 1);
-    mbar_init(smem_u32(&sm.bar_dq_read), kHelperThreads);
-    mbar_init(smem_u32(&sm.bar_staged), kHelperThreads);
+    mbar_init(smem_u32(&sm.bar_dq_read), kComputeThreads);
+    mbar_init(smem_u32(&sm.bar_staged), kComputeThreads);
     mbar_init(smem_u32(&sm.bar_stage_free), 1);
     mbar_init(smem_u32(&sm.bar_acc_full), 1);
     mbar_init(smem_u32(&sm.bar_acc_empty), kComputeThreads);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&sm.bar_ds_full[b]), kHelperThreads);
-      mbar_init(smem_u32(&sm.bar_tile[b]), kComputeThreads);
-    }
+    mbar_init(smem_u32(&sm.bar_tile), kComputeThreads);
     mbar_init(smem_u32(&sm.bar_done), 1);
     mbar_init(smem_u32(&sm.bar_sf), kTile);
-    // the MMA issuer, the compute leader, the dQ reducer, the helper leader
-    ring_init(sm.ring, 4);
+    ring_init(sm.ring, 3);  // the MMA issuer, the compute leader, the dQ reducer
     sm.abort = 0;
     sm.dscnt[0] = sm.dscnt[1] = 0ull;
     fence_barrier_init();
@@ -203,7 +188,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    setmaxnreg_dec<kRegsCtl>();
     if (lane == 0) {
       prefetch_tensormap(&map_q);
       prefetch_tensormap(&map_k);
@@ -269,7 +253,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // t+1 (once the groups hold tile t's in registers), then dV_t, dK_t and
     // dQ_t (once tile t's dS is written and dQ_{t-1} has been read out).  Each
     // barrier phase is waited for before the next one can complete.
-    setmaxnreg_dec<kRegsCtl>();
     {
       const uint32_t id_s = idesc_f8(kTile, kTile, 0, 0);
       // operand descriptors, built once: a K step, a ring stage or a payload
@@ -343,7 +326,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           // dV / dK restart from zero on an item's first tile: the previous
           // item's epilogue must have read them
-          if (!mbar_wait_w_ab(smem_u32(&sm.bar_ds_full[b]), (uc >> 1) & 1, &sm.abort) ||
+          if (!mbar_wait_w_ab(smem_u32(&sm.bar_ds_full), uc & 1, &sm.abort) ||
               (u == 0 && nk > 1 &&
                !mbar_wait_w_ab(smem_u32(&sm.bar_acc_empty), (nk - 2) & 1, &sm.abort))) {
             ok = false;
@@ -393,7 +376,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // follows the items in claim order, waits for a tile's staging, issues the
     // reduce-adds and frees the staging buffer once they have read it (in the
     // deterministic mode: once they are complete, passing the tile's turn on).
-    setmaxnreg_dec<kRegsCtl>();
     if (lane == 0) {
       bool ok = true;
       int tg = 0;  // query tiles over all items
@@ -442,15 +424,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       bulk_wait_group0();
       if (!ok) sm.abort = 1;
     }
-  } else if (warp == 3) {
-    setmaxnreg_dec<kRegsCtl>();  // idle: its registers go to the compute warps
-  } else if (warp < 12) {
+  } else if (warp >= 4) {
     // ------------------------------------------------------------ compute groups
-    setmaxnreg_inc<kRegsCompute>();
     const int g = (warp - 4) >> 2;   // 0: query columns 0..63, 1: 64..127
     const int quad = warp & 3;
-    const int j = quad * 32 + lane;  // key row (S^T, dP^T, dV, dK)
-    const int wi = warp - 4;         // this warp's slice of the per-query inputs
+    const int j = quad * 32 + lane;  // key row (S^T, dP^T, dV, dK) / query row (dQ_t)
     const bool issuer = (warp == 4 && lane == 0);
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const float LOG2E = 1.4426950408889634f;
@@ -460,6 +438,63 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bool ok = true;
     int uc = 0;  // query tiles processed over all items (phase and buffer parity)
     int nk = 0;  // items processed
+    // dQ_t (tile t = ut of the item, global index tg) from tensor memory to the
+    // staging buffer, for the reducer warp; every compute thread calls it (it
+    // arrives on dq_read, then on staged).  The buffer is free once the
+    // reducer's bulk copies of the previous tile have read it.
+    auto read_dq = [&](const BwdItem& it, int ut, int tg) {
+      ok = ok && mbar_wait_ab(smem_u32(&sm.bar_dq_full), tg & 1, &sm.abort) &&
+           (tg == 0 || mbar_wait_ab(smem_u32(&sm.bar_stage_free), (tg - 1) & 1, &sm.abort));
+      tc_fence_after();
+      if (!ok) return;
+      const bool qv = tile_q0(it, ut) + j < it.e;  // TMEM lane j of dQ_t is query row j
+      constexpr int kCh = DIM / 64;  // 32-column chunks of dQ_t per group
+      uint32_t v[kCh][32];
+#pragma unroll
+      for (int cc = 0; cc < kCh; ++cc)
+        tmem_ld32(tmem + lane_off + kColDQ + 32 * (g * kCh + cc), v[cc]);
+      tmem_ld_wait();
+      // dQ of the next tile may now be written
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm.bar_dq_read));
+      if (OPT && prm.dq_pre != nullptr) {
+        // x 2^p of the query row (0 outside the document), rounded to FP16,
+        // in DIM / 64 boxes [128 query rows][64 halves], 128B-swizzled
+        const float pf = sm.pf[tg & 3][j];
+        __half* box0 = reinterpret_cast<__half*>(sm.dqs[0]);
+#pragma unroll
+        for (int t = 0; t < 4 * kCh; ++t) {  // 8-dim chunk t of this group's dims
+          const int dim0 = g * 32 * kCh + 8 * t;
+          const int b = dim0 / 64, ch = (dim0 % 64) / 8;
+          uint32_t w[4];
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            const __half2 h2 = __floats2half2_rn(
+                __uint_as_float(v[t / 4][8 * (t % 4) + 2 * x]) * pf,
+                __uint_as_float(v[t / 4][8 * (t % 4) + 2 * x + 1]) * pf);
+            w[x] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
+          *reinterpret_cast<uint4*>(box0 + b * (kTile * 64) + j * 64 + 8 * (ch ^ (j & 7))) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      } else {
+#pragma unroll
+        for (int cc = 0; cc < kCh; ++cc) {
+          float* row = sm.dqs[g * kCh + cc] + j * 32;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            // softmax_scale is applied once, in the float32 -> BF16 conversion
+            float4 f = make_float4(__uint_as_float(v[cc][4 * i]), __uint_as_float(v[cc][4 * i + 1]),
+                                   __uint_as_float(v[cc][4 * i + 2]),
+                                   __uint_as_float(v[cc][4 * i + 3]));
+            if (!qv) f = make_float4(0.f, 0.f, 0.f, 0.f);  // rows of other documents add 0
+            *reinterpret_cast<float4*>(row + 4 * (i ^ (j & 7))) = f;
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(&sm.bar_staged));
+    };
     for (int n = 0;; ++n) {
       if (issuer) sm.item_bc[n & 1] = ring_get(sm.ring, n, true);
       named_barrier_sync(1, kComputeThreads);
@@ -479,6 +514,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int evj = key_valid ? static_cast<int>(prm.v_scales[hT + kj]) - 127 : 0;
       const float rowf = pow2_or_zero(ekj) * prm.scale_log2;
       const float rowg = pow2_or_zero(evj);
+      // E8M0 bytes of this key tile's 4 key blocks (B scale of dQ_t = dS K)
+      uint32_t kword = 0;
+#pragma unroll
+      for (int kb = 0; kb < 4; ++kb) {
+        const int kk = k0 + 32 * kb;
+        kword |= (kk < e ? static_cast<uint32_t>(prm.k_scales[hT + kk]) : 127u) << (8 * kb);
+      }
       // NVFP4 score product: block scales in tensor memory, one 32-bit word (4
       // E4M3 scales) per row; column c + i of a lane quadrant holds row 32 i +
       // lane (the same words in every quadrant).  Group 0 writes them.
@@ -498,69 +540,61 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_before();
         mbar_arrive(smem_u32(&sm.bar_sf));
       }
-      // This warp's per-query inputs of tile u: lane i holds the queries 64 g
-      // + i and 64 g + 32 + i (raw loads from clamped, always valid addresses,
-      // issued a tile ahead and only used when stored), and the E8M0 bytes of Q
-      // and dO of the warp's two 32-query blocks (their first query's).
-      float r_lse[2], r_dd[2];
-      uint32_t r_qt[2], r_dot[2], r_qb[2], r_dob[2];
-      bool r_qv[2];
-      uint32_t qb_cur[2], dob_cur[2];  // the bytes of the tile being computed
+      // the per-query inputs of tile u: raw loads from clamped (always valid)
+      // addresses, issued a tile ahead and only used when stored (group 0)
+      float r_lse = 0.f, r_dd = 0.f;
+      uint32_t r_qb = 127u, r_dob = 127u;
+      int r_pre = 0;
+      bool r_qv = false;
       auto fetch_query_inputs = [&](int u) {
-        const int q0 = tile_q0(it, u);
-        const size_t hq = static_cast<size_t>(tile_head(it, u)) * T;
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          const int qb0 = q0 + 64 * g + 32 * h2;  // the block's first query
-          const int qi = qb0 + lane;
-          r_qv[h2] = qi < e;
-          const size_t at = hq + min(qi, T - 1);
-          r_lse[h2] = prm.lse[at];
-          r_dd[h2] = prm.D[at];
-          if (OPT && !NVF4 && prm.token) {
-            r_qt[h2] = prm.q_scales[at];
-            r_dot[h2] = prm.do_scales[at];
-          }
-          const size_t ab = hq + min(qb0, T - 1);
-          r_qb[h2] = qb0 < e ? static_cast<uint32_t>(prm.q_scales[ab]) : 127u;
-          r_dob[h2] = qb0 < e ? static_cast<uint32_t>(prm.do_scales[ab]) : 127u;
+        const int qi = tile_q0(it, u) + j;
+        r_qv = qi < e;
+        const size_t at = static_cast<size_t>(tile_head(it, u)) * T + min(qi, T - 1);
+        r_lse = prm.lse[at];
+        r_dd = prm.D[at];
+        if (OPT && prm.dq_pre != nullptr) r_pre = prm.dq_pre[at];
+        if (lane == 0 || (OPT && !NVF4 && prm.token)) {
+          r_qb = prm.q_scales[at];
+          r_dob = prm.do_scales[at];
         }
       };
-      // into this warp's buffer of tile tg's parity (last read by this warp's
-      // recompute of tile tg - 2)
       auto store_query_inputs = [&](int tg) {
-        const int b = tg & 1;
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          const int q = 32 * h2 + lane;
-          sm.nlw[wi][b][q] = r_qv[h2] ? 8.f - r_lse[h2] * LOG2E : -INFINITY;
-          sm.ddw[wi][b][q] = r_qv[h2] ? r_dd[h2] : 0.f;
-          if constexpr (OPT && !NVF4) {
-            if (prm.token) {
-              // per-token operand scales: this query's factors, against its
-              // block's largest exponents (the B scales of dK and dV)
-              const int eqb = r_qv[h2] ? static_cast<int>(r_qt[h2]) : 0;
-              const int edb = r_qv[h2] ? static_cast<int>(r_dot[h2]) : 0;
-              const int EQ = static_cast<int>(__reduce_max_sync(0xffffffffu, static_cast<unsigned>(eqb)));
-              const int ED = static_cast<int>(__reduce_max_sync(0xffffffffu, static_cast<unsigned>(edb)));
-              sm.tqw[0][wi][b][q] = r_qv[h2] ? pow2_or_zero(eqb - 127) : 0.f;
-              sm.tqw[1][wi][b][q] = r_qv[h2] ? pow2_or_zero(edb - 127) : 0.f;
-              sm.tqw[2][wi][b][q] = r_qv[h2] ? pow2_or_zero(edb - ED) : 0.f;
-              sm.tqw[3][wi][b][q] = r_qv[h2] ? pow2_or_zero(eqb - EQ) : 0.f;
+        const int b = tg & 1, b3 = tg % 3;
+        sm.nl[b][j] = r_qv ? 8.f - r_lse * LOG2E : -INFINITY;
+        sm.dd[b][j] = r_qv ? r_dd : 0.f;
+        if (OPT) sm.pf[tg & 3][j] = r_qv ? exp2i(r_pre) : 0.f;
+        if constexpr (OPT && !NVF4) {
+          if (prm.token) {
+            // per-token operand scales: this query's factors and its block's
+            // largest exponents (the B scales of dK and dV)
+            const int eqb = r_qv ? static_cast<int>(r_qb) : 0;
+            const int edb = r_qv ? static_cast<int>(r_dob) : 0;
+            const int EQ = static_cast<int>(__reduce_max_sync(0xffffffffu, static_cast<unsigned>(eqb)));
+            const int ED = static_cast<int>(__reduce_max_sync(0xffffffffu, static_cast<unsigned>(edb)));
+            sm.tq[0][b][j] = r_qv ? pow2_or_zero(eqb - 127) : 0.f;
+            sm.tq[1][b][j] = r_qv ? pow2_or_zero(edb - 127) : 0.f;
+            sm.tq[2][b][j] = r_qv ? pow2_or_zero(edb - ED) : 0.f;
+            sm.tq[3][b][j] = r_qv ? pow2_or_zero(eqb - EQ) : 0.f;
+            if (lane == 0) {
+              sm.qbyte[b3][quad] = static_cast<uint32_t>(EQ);
+              sm.dobyte[b3][quad] = static_cast<uint32_t>(ED);
             }
+            return;
           }
         }
-        __syncwarp();
-        qb_cur[0] = r_qb[0];
-        qb_cur[1] = r_qb[1];
-        dob_cur[0] = r_dob[0];
-        dob_cur[1] = r_dob[1];
+        if (lane == 0) {
+          sm.qbyte[b3][quad] = r_qv ? r_qb : 127u;
+          sm.dobyte[b3][quad] = r_qv ? r_dob : 127u;
+        }
       };
-      fetch_query_inputs(0);
-      store_query_inputs(uc);
+      if (g == 0) {
+        fetch_query_inputs(0);
+        store_query_inputs(uc);
+      }
+      named_barrier_sync(1, kComputeThreads);
       for (int u = 0; u < nq; ++u, ++uc) {
-        const int ub = uc & 1;
-        if (u + 1 < nq) fetch_query_inputs(u + 1);  // lands during this tile
+        const int ub = uc & 1, ub3 = uc % 3;
+        if (g == 0 && u + 1 < nq) fetch_query_inputs(u + 1);  // lands during this tile
         ok = ok && mbar_wait_ab(smem_u32(&sm.bar_s_full), uc & 1, &sm.abort);
         tc_fence_after();
         uint8_t* pbrow = sm.pb[ub] + j * kTile;
@@ -569,13 +603,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int cc = 0; cc < 2 && ok; ++cc) {
           const int c = 2 * g + cc;  // 32-query block of this chunk
           const float fS =
-              NVF4 ? rowf
-                   : rowf * pow2_or_zero(static_cast<int>(cc == 0 ? qb_cur[0] : qb_cur[1]) - 127);
-          const float fP =
-              rowg * pow2_or_zero(static_cast<int>(cc == 0 ? dob_cur[0] : dob_cur[1]) - 127);
-          // this warp's copies of the chunk's per-query inputs
-          const float* nlc = sm.nlw[wi][ub] + 32 * cc;
-          const float* ddc = sm.ddw[wi][ub] + 32 * cc;
+              NVF4 ? rowf : rowf * pow2_or_zero(static_cast<int>(sm.qbyte[ub3][c]) - 127);
+          const float fP = rowg * pow2_or_zero(static_cast<int>(sm.dobyte[ub3][c]) - 127);
           uint32_t sv[32], dv[32];
           tmem_ld32(tmem + lane_off + kColSP + 32 * c, sv);
           tmem_ld32(tmem + lane_off + kColDP + 32 * c, dv);
@@ -595,27 +624,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           float amax = 0.f;
           const bool tok = OPT && !NVF4 && prm.token;
           // per-token operand scales: dK's operand is dS 2^(eQ - EQ) per query
-          const float* kq = sm.tqw[OPT && !NVF4 ? 3 : 0][wi][ub] + 32 * cc;
+          const float* kq = sm.tq[OPT && !NVF4 ? 3 : 0][ub] + 32 * c;
           if (!key_valid) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) dv[i] = 0u;
           } else if (tok) {
-            const float* q0p = sm.tqw[0][wi][ub] + 32 * cc;
-            const float* d0p = sm.tqw[OPT && !NVF4 ? 1 : 0][wi][ub] + 32 * cc;
-            const float* p0p = sm.tqw[OPT && !NVF4 ? 2 : 0][wi][ub] + 32 * cc;
+            const float* q0p = sm.tq[0][ub] + 32 * c;
+            const float* d0p = sm.tq[OPT && !NVF4 ? 1 : 0][ub] + 32 * c;
+            const float* p0p = sm.tq[OPT && !NVF4 ? 2 : 0][ub] + 32 * c;
             if (prm.causal && (G == 1 ? u : u % nt) == 0)
-              bwd_chunk_tok<true>(sv, dv, nlc, ddc, q0p, d0p, p0p,
+              bwd_chunk_tok<true>(sv, dv, sm.nl[ub] + 32 * c, sm.dd[ub] + 32 * c, q0p, d0p, p0p,
                                   rowf, rowg, 32 * c, j, pw);
             else
-              bwd_chunk_tok<false>(sv, dv, nlc, ddc, q0p, d0p, p0p,
+              bwd_chunk_tok<false>(sv, dv, sm.nl[ub] + 32 * c, sm.dd[ub] + 32 * c, q0p, d0p, p0p,
                                    rowf, rowg, 32 * c, j, pw);
 #pragma unroll
             for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(__uint_as_float(dv[i]) * kq[i]));
           } else if (prm.causal && (G == 1 ? u : u % nt) == 0) {
-            amax = bwd_chunk<true>(sv, dv, nlc, ddc, fS, fP,
+            amax = bwd_chunk<true>(sv, dv, sm.nl[ub] + 32 * c, sm.dd[ub] + 32 * c, fS, fP,
                                    32 * c, j, pw);
           } else {
-            amax = bwd_chunk<false>(sv, dv, nlc, ddc, fS, fP,
+            amax = bwd_chunk<false>(sv, dv, sm.nl[ub] + 32 * c, sm.dd[ub] + 32 * c, fS, fP,
                                     32 * c, j, pw);
           }
           // one exponent per 32x32 block: this warp's 32 key rows x these 32 queries
@@ -680,15 +709,72 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             *reinterpret_cast<uint4*>(ds2row + 16 * ch1) = make_uint4(dr[4], dr[5], dr[6], dr[7]);
           }
         }
-        // the next tile's per-query inputs (this warp's own copy)
-        if (u + 1 < nq) store_query_inputs(uc + 1);
-        // The payloads (read by the tensor core) and the dS block bytes (read
-        // by the helpers) are written: every compute thread arrives once per
-        // tile, whatever happened, and goes on to the next tile.
-        fence_proxy_async_smem();
-        mbar_arrive(smem_u32(&sm.bar_tile[ub]));
+        // the next tile's per-query inputs (their nl / dd buffer was last read
+        // by tile t-1's recompute, the byte buffer by tile t-2's block scales,
+        // the prescale buffer by tile t-3's staging), visible after the wait on
+        // bar_tile, which also completes the dS block exponents.  Split
+        // arrive / wait: the previous tile's dQ is read out in between, so a
+        // fast warp does that instead of waiting for the slowest one.  Every
+        // compute thread arrives once per tile, whatever happened.
+        if (g == 0 && u + 1 < nq) store_query_inputs(uc + 1);
+        mbar_arrive(smem_u32(&sm.bar_tile));
+        // dQ of the previous tile, computed while this tile was recomputed
+        if (u > 0) read_dq(it, u - 1, uc - 1);
+        ok = ok && mbar_wait_ab(smem_u32(&sm.bar_tile), uc & 1, &sm.abort);
+        if (ok) {
+          // block scales of the three products (this tile's parity buffer,
+          // last read by the products of tile t-2, complete before tile t's
+          // S^T); every lane quadrant holds the same words: column (base +
+          // m/32) of an A scale holds the 4 K-block bytes of rows m/32*32 .. +31
+          const uint32_t sfc = col_sf(uc);
+          uint32_t w[8];
+          if (g == 0) {
+            const uint32_t* db = sm.dobyte[ub3];
+            const uint32_t* qb = sm.qbyte[ub3];
+            const uint32_t dow = db[0] | (db[1] << 8) | (db[2] << 16) | (db[3] << 24);
+            const uint32_t qw = qb[0] | (qb[1] << 8) | (qb[2] << 16) | (qb[3] << 24);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              w[i] = 0x7F7F7F7Fu;  // dV: A = P^b, scale 2^0
+              w[4 + i] = dow;      // dV: B = dO, per query block
+            }
+            tmem_st8(tmem + lane_off + sfc + kSfDvA, w);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              // dK: A = dS^T, row block = key block i, K blocks = query blocks
+              w[i] = sm.eds[ub][0][i] | (sm.eds[ub][1][i] << 8) | (sm.eds[ub][2][i] << 16) |
+                     (sm.eds[ub][3][i] << 24);
+              w[4 + i] = qw;  // dK: B = Q, per query block
+            }
+            tmem_st8(tmem + lane_off + sfc + kSfDkA, w);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              // dQ: A = dS, row block = query block i, K blocks = key blocks
+              if (OPT && prm.ds_rows)  // this lane's query 32 i + lane
+                w[i] = static_cast<uint32_t>(sm.erow[ub][i][0][lane]) |
+                       (static_cast<uint32_t>(sm.erow[ub][i][1][lane]) << 8) |
+                       (static_cast<uint32_t>(sm.erow[ub][i][2][lane]) << 16) |
+                       (static_cast<uint32_t>(sm.erow[ub][i][3][lane]) << 24);
+              else
+                w[i] = sm.eds[ub][i][0] | (sm.eds[ub][i][1] << 8) | (sm.eds[ub][i][2] << 16) |
+                       (sm.eds[ub][i][3] << 24);
+              // dQ: B = K, per key block (2^0: per-token K factors are in dS)
+              w[4 + i] = (OPT && !NVF4 && prm.token) ? 0x7F7F7F7Fu : kword;
+            }
+            tmem_st8(tmem + lane_off + sfc + kSfDqA, w);
+          }
+        }
+        if (ok) {
+          tmem_st_wait();
+          fence_proxy_async_smem();
+          tc_fence_before();
+          mbar_arrive(smem_u32(&sm.bar_ds_full));
+        }
         if (!ok) sm.abort = 1;
       }
+      // the item's last dQ
+      if (nq > 0) read_dq(it, nq - 1, uc - 1);
       if (!ok) sm.abort = 1;
       // every product of the item is complete
       ok = ok && !sm.abort && mbar_wait(smem_u32(&sm.bar_acc_full), nk & 1);
@@ -759,179 +845,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_arrive(smem_u32(&sm.bar_acc_empty));
       }
     }
-    if (!ok) sm.abort = 1;
-  } else {
-    // ------------------------------------------------------------ helpers
-    // One thread per tensor-memory lane of dQ_t (query row j).  Per tile t:
-    // read dQ_{t-1} out and stage it for the reducer (it was computed while
-    // the compute warps recomputed tile t), then, once every compute thread
-    // has arrived on tile t's exchange, write the block scales of tile t's
-    // three products and release them to the MMA warp.
-    setmaxnreg_dec<kRegsHelper>();
-    const int quad = warp & 3;
-    const int j = quad * 32 + lane;
-    const bool leader = (warp == 12 && lane == 0);
-    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    bool ok = true;
-    int uc = 0;      // query tiles over all items (phase and buffer parity)
-    BwdItem pit{};   // the item of the tile whose dQ is read out next
-    int pu = -1;     // that tile's index in its item (-1: none)
-    // dQ_t (tile ut of item it, global index tg) from tensor memory to the
-    // staging buffer, for the reducer warp, in 32-column halves.  The buffer is
-    // free once the reducer's bulk copies of the previous tile have read it.
-    auto read_dq = [&](const BwdItem& it, int ut, int tg) {
-      ok = ok && mbar_wait_ab(smem_u32(&sm.bar_dq_full), tg & 1, &sm.abort) &&
-           (tg == 0 || mbar_wait_ab(smem_u32(&sm.bar_stage_free), (tg - 1) & 1, &sm.abort));
-      tc_fence_after();
-      if (!ok) return;
-      const int q0 = tile_q0(it, ut);
-      const bool qv = q0 + j < it.e;  // rows of other documents add 0
-      float pf = 0.f;
-      if (OPT && prm.dq_pre != nullptr) {
-        // FP16 accumulator: x 2^p of the query row (0 outside the document)
-        const size_t at = static_cast<size_t>(tile_head(it, ut)) * T + min(q0 + j, T - 1);
-        pf = qv ? exp2i(prm.dq_pre[at]) : 0.f;
-      }
-#pragma unroll 1
-      for (int c = 0; c < DIM / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_off + kColDQ + 32 * c, v);
-        tmem_ld_wait();
-        if (c == DIM / 32 - 1) {
-          // dQ of the next tile may now be written
-          tc_fence_before();
-          mbar_arrive(smem_u32(&sm.bar_dq_read));
-        }
-        if (OPT && prm.dq_pre != nullptr) {
-          // rounded to FP16, in DIM / 64 boxes [128 query rows][64 halves],
-          // 128B-swizzled
-          __half* box0 = reinterpret_cast<__half*>(sm.dqs[0]);
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {  // 8-dim chunk t of this half
-            const int dim0 = 32 * c + 8 * t;
-            const int b = dim0 / 64, ch = (dim0 % 64) / 8;
-            uint32_t w[4];
-#pragma unroll
-            for (int x = 0; x < 4; ++x) {
-              const __half2 h2 = __floats2half2_rn(__uint_as_float(v[8 * t + 2 * x]) * pf,
-                                                   __uint_as_float(v[8 * t + 2 * x + 1]) * pf);
-              w[x] = *reinterpret_cast<const uint32_t*>(&h2);
-            }
-            *reinterpret_cast<uint4*>(box0 + b * (kTile * 64) + j * 64 + 8 * (ch ^ (j & 7))) =
-                make_uint4(w[0], w[1], w[2], w[3]);
-          }
-        } else {
-          float* row = sm.dqs[c] + j * 32;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            // softmax_scale is applied once, in the float32 -> BF16 conversion
-            float4 f = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                   __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
-            if (!qv) f = make_float4(0.f, 0.f, 0.f, 0.f);
-            *reinterpret_cast<float4*>(row + 4 * (i ^ (j & 7))) = f;
-          }
-        }
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(smem_u32(&sm.bar_staged));
-    };
-    for (int n = 0;; ++n) {
-      if (leader) sm.item_bh[n & 1] = ring_get(sm.ring, n, true);
-      named_barrier_sync(2, kHelperThreads);
-      const int idx = sm.item_bh[n & 1];
-      if (idx < 0) {
-        ok = false;
-        break;
-      }
-      if (idx >= total) break;
-      BwdItem it;
-      if (!decode_bwd_item(prm, n_items, idx, it)) continue;
-      const int e = it.e, k0 = it.k0, nq = it.nq * G;
-      const size_t hT = static_cast<size_t>(it.hk) * T;  // K scale rows
-      const bool tok = OPT && !NVF4 && prm.token;
-      // E8M0 bytes of this key tile's 4 key blocks (B scale of dQ_t = dS K)
-      uint32_t kword = 0;
-#pragma unroll
-      for (int kb = 0; kb < 4; ++kb) {
-        const int kk = k0 + 32 * kb;
-        kword |= (kk < e ? static_cast<uint32_t>(prm.k_scales[hT + kk]) : 127u) << (8 * kb);
-      }
-      for (int u = 0; u < nq; ++u, ++uc) {
-        const int ub = uc & 1;
-        // dQ of the previous tile (of this item or of the one before)
-        if (pu >= 0) read_dq(pit, pu, uc - 1);
-        // the bytes of Q and dO of the tile's 4 query blocks: the block's
-        // first query's, or with per-token operand scales the block's largest
-        const int q0 = tile_q0(it, u);
-        const size_t hq = static_cast<size_t>(tile_head(it, u)) * T;
-        uint32_t qw = 0, dow = 0;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t eq, ed;
-          if (tok) {
-            const int qi = q0 + 32 * c + lane;
-            const size_t at = hq + min(qi, T - 1);
-            eq = __reduce_max_sync(0xffffffffu, qi < e ? static_cast<uint32_t>(prm.q_scales[at]) : 0u);
-            ed = __reduce_max_sync(0xffffffffu, qi < e ? static_cast<uint32_t>(prm.do_scales[at]) : 0u);
-          } else {
-            const int qb0 = q0 + 32 * c;
-            const size_t ab = hq + min(qb0, T - 1);
-            eq = qb0 < e ? static_cast<uint32_t>(prm.q_scales[ab]) : 127u;
-            ed = qb0 < e ? static_cast<uint32_t>(prm.do_scales[ab]) : 127u;
-          }
-          qw |= eq << (8 * c);
-          dow |= ed << (8 * c);
-        }
-        ok = ok && mbar_wait_ab(smem_u32(&sm.bar_tile[ub]), (uc >> 1) & 1, &sm.abort);
-        tc_fence_after();
-        if (ok) {
-          // block scales of the three products (this tile's parity buffer,
-          // last read by the products of tile t-2, complete before tile t's
-          // S^T); every lane quadrant holds the same words: column (base +
-          // m/32) of an A scale holds the 4 K-block bytes of rows m/32*32 .. +31
-          const uint32_t sfc = col_sf(uc);
-          uint32_t w[8];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            w[i] = 0x7F7F7F7Fu;  // dV: A = P^b, scale 2^0
-            w[4 + i] = dow;      // dV: B = dO, per query block
-          }
-          tmem_st8(tmem + lane_off + sfc + kSfDvA, w);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            // dK: A = dS^T, row block = key block i, K blocks = query blocks
-            w[i] = sm.eds[ub][0][i] | (sm.eds[ub][1][i] << 8) | (sm.eds[ub][2][i] << 16) |
-                   (sm.eds[ub][3][i] << 24);
-            w[4 + i] = qw;  // dK: B = Q, per query block
-          }
-          tmem_st8(tmem + lane_off + sfc + kSfDkA, w);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            // dQ: A = dS, row block = query block i, K blocks = key blocks
-            if (OPT && prm.ds_rows)  // this lane's query 32 i + lane
-              w[i] = static_cast<uint32_t>(sm.erow[ub][i][0][lane]) |
-                     (static_cast<uint32_t>(sm.erow[ub][i][1][lane]) << 8) |
-                     (static_cast<uint32_t>(sm.erow[ub][i][2][lane]) << 16) |
-                     (static_cast<uint32_t>(sm.erow[ub][i][3][lane]) << 24);
-            else
-              w[i] = sm.eds[ub][i][0] | (sm.eds[ub][i][1] << 8) | (sm.eds[ub][i][2] << 16) |
-                     (sm.eds[ub][i][3] << 24);
-            // dQ: B = K, per key block (2^0: per-token K factors are in dS)
-            w[4 + i] = tok ? 0x7F7F7F7Fu : kword;
-          }
-          tmem_st8(tmem + lane_off + sfc + kSfDqA, w);
-          tmem_st_wait();
-        }
-        // tile t's products may be issued (every helper arrives once per tile)
-        tc_fence_before();
-        mbar_arrive(smem_u32(&sm.bar_ds_full[ub]));
-        pit = it;
-        pu = u;
-        if (!ok) sm.abort = 1;
-      }
-    }
-    // the last tile's dQ
-    if (pu >= 0) read_dq(pit, pu, uc - 1);
     if (!ok) sm.abort = 1;
   }
 
