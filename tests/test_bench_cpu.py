@@ -46,3 +46,33 @@ def test_cpu_baseline_prefix_sample():
     assert cb["value"] > 0 and "causal prefix" in cb["sample"]
     full = bench.cpu_baseline(W.tiny(), budget_s=5.0)
     assert full["value"] > 0 and "document(s)" in full["sample"]
+
+
+def test_profiled_traffic_only_for_unchanged_sources(tmp_path, monkeypatch):
+    """The roofline line's DRAM traffic comes from a profile summary only while
+    the kernel sources it lists hash to the recorded digest; any change to
+    them turns it into null (a figure measured on other code)."""
+    import hashlib
+    import shutil
+    sys.path.insert(0, ROOT)
+    import bench
+    from precision_causal_attention_block_gb300 import workloads as W
+    csrc = tmp_path / "precision_causal_attention_block_gb300" / "csrc"
+    shutil.copytree(os.path.join(ROOT, "precision_causal_attention_block_gb300", "csrc"), csrc)
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    w = W.tiny()
+    srcs = ["attn_bwd.cu", "ptx.cuh"]
+    h = hashlib.sha256()
+    for s in srcs:
+        h.update((csrc / s).read_bytes())
+    name = f"{bench.bwd_kernel_name(w, False)}_{w.name.replace('_', '', 1)}.md"
+    prof = tmp_path / "profiles" / name
+    prof.write_text("# summary\n\n    traffic_bytes_per_launch: 123456\n"
+                    f"    sources: {' '.join(srcs)}\n    sources_sha256: {h.hexdigest()}\n")
+    assert bench.profiled_traffic(w, False) == 123456
+    # no summary for the mixed path's kernel
+    assert bench.profiled_traffic(w, True) is None
+    # a changed source invalidates the figure
+    (csrc / "ptx.cuh").write_text((csrc / "ptx.cuh").read_text() + "\n// changed\n")
+    assert bench.profiled_traffic(w, False) is None
