@@ -721,7 +721,31 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (j > 0 && m_new > m) l8 *= pow2_or_zero(static_cast<int>(m - m_new));
         m = m_new;
         const float moff = m - 8.f;  // P8 = 2^8 exp2(s - m)
-        // head dim 64: P^_t's columns are free once the previous P^_t V has read them
+        // pass 2: probabilities, row sum, E4M3 operand (the codes stay in
+        // registers until P^_t's columns are free)
+        float2 lsum = make_float2(0.f, 0.f);
+        // per-token operand scales, causal diagonal tile: the row's own key
+        // block takes EV = the maximum over the keys it sees
+        const bool tdiag = TOK && diag && prm.causal;
+        const float gown = tdiag ? pow2_or_zero(own_max - pm) : 1.f;
+        uint32_t pcode[4][8];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if constexpr (TOK) {
+            const float* vfp = sm.vf[j & 1][t] + 32 * c;
+            if (diag)
+              chunk_probs_tok<true>(sv[c], c_row, moff, lim - 32 * c, lsum, pcode[c], vfp,
+                                    (tdiag && c == quad) ? gown : 1.f);
+            else
+              chunk_probs_tok<false>(sv[c], c_row, moff, 0, lsum, pcode[c], vfp, 1.f);
+          } else if (diag) {
+            chunk_probs<true>(sv[c], cf[c], moff, lim - 32 * c, lsum, pcode[c]);
+          } else {
+            chunk_probs<false>(sv[c], cf[c], moff, 0, lsum, pcode[c]);
+          }
+        }
+        // head dim 64: P^_t's columns are free once the previous P^_t V has
+        // read them (waited for only now, so the wait overlaps the exponentials)
         if (kSep && j > 0) {
           if (!mbar_wait_ab(smem_u32(&sm.bar_pv_done[t]), pv_seen & 1, &sm.abort)) {
             ok = false;
@@ -730,31 +754,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           ++pv_seen;
           tc_fence_after();
         }
-        // pass 2: probabilities, row sum, E4M3 operand
-        float2 lsum = make_float2(0.f, 0.f);
-        // per-token operand scales, causal diagonal tile: the row's own key
-        // block takes EV = the maximum over the keys it sees
-        const bool tdiag = TOK && diag && prm.causal;
-        const float gown = tdiag ? pow2_or_zero(own_max - pm) : 1.f;
+        // the 32 codes of each chunk: row r of P^_t, keys 32 c .. 32 c + 31, into
+        // P^_t's columns (head dim 128: the consumed columns of S_t)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t w[8];
-          if constexpr (TOK) {
-            const float* vfp = sm.vf[j & 1][t] + 32 * c;
-            if (diag)
-              chunk_probs_tok<true>(sv[c], c_row, moff, lim - 32 * c, lsum, w, vfp,
-                                    (tdiag && c == quad) ? gown : 1.f);
-            else
-              chunk_probs_tok<false>(sv[c], c_row, moff, 0, lsum, w, vfp, 1.f);
-          } else if (diag) {
-            chunk_probs<true>(sv[c], cf[c], moff, lim - 32 * c, lsum, w);
-          } else {
-            chunk_probs<false>(sv[c], cf[c], moff, 0, lsum, w);
-          }
-          // the 32 codes of this chunk: row r of P^_t, keys 32 c .. 32 c + 31, into
-          // P^_t's columns (head dim 128: the consumed columns of S_t)
-          tmem_st8(tP + kColP + 8 * c, w);
-        }
+        for (int c = 0; c < 4; ++c) tmem_st8(tP + kColP + 8 * c, pcode[c]);
         l8 += lsum.x + lsum.y;
         // P^_t V_j enters O_t with the block scale 2^(m - m_ref) on P^'s row:
         // O_t stays in the scale of m_ref and needs no rescaling when the
